@@ -1,0 +1,303 @@
+"""Pins for the CPU oracle (no GPU): each check fixes the oracle against
+something other than itself - finite differences, closed forms, invariants of
+batch norm, a hand-worked example, a brute-force restatement of the WGSL
+weight-gradient shader, and an independent torch CPU computation.
+
+Formulas pinned: rl-tools page "operations_generic.h" (`forward`, `evaluate`,
+`backward_full`); WGSL page "conv2d_backward_weight.wgsl" (per-image dW).
+"""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand_layer(rng, L, x_scale=1.0):
+    x = rng.standard_normal(L.x_shape) * x_scale
+    w = rng.standard_normal(L.w_shape) / np.sqrt(L.IC * L.KH * L.KW)
+    b = rng.uniform(-0.3, 0.3, L.OC)
+    gamma = rng.uniform(0.5, 1.5, L.OC)
+    beta = rng.normal(0, 0.1, L.OC)
+    dy = rng.standard_normal(L.y_shape)
+    return x, w, b, gamma, beta, dy
+
+
+def _loss(L, x, w, b, gamma, beta, dy):
+    out = oracle.fwd_train(L, x, w, b, gamma, beta)
+    return float(np.sum(out["y"] * dy))
+
+
+def _act_inputs(L, x, w, b, gamma, beta):
+    out = oracle.fwd_train(L, x, w, b, gamma, beta)
+    if L.norm == 0:
+        return out["ypre"]
+    z = (out["ypre"] - out["mean"]) * out["inv_std"]
+    return gamma * z + beta
+
+
+def _fd(f, arr, h=1e-5):
+    g = np.zeros_like(arr)
+    flat, gf = arr.reshape(-1), g.reshape(-1)
+    for i in range(flat.size):
+        old = flat[i]
+        flat[i] = old + h
+        fp = f()
+        flat[i] = old - h
+        fm = f()
+        flat[i] = old
+        gf[i] = (fp - fm) / (2 * h)
+    return g
+
+
+FD_CASES = [
+    # (N,H,W,IC,OC,K,S,P)
+    (2, 5, 5, 3, 4, 3, 1, 1),
+    (2, 6, 5, 4, 4, 3, 2, 0),
+    (1, 9, 9, 3, 4, 3, 4, 1),
+    (2, 4, 4, 4, 4, 1, 1, 0),
+]
+
+
+@pytest.mark.parametrize("norm", ["none", "batch"])
+@pytest.mark.parametrize("act", ["identity", "relu", "tanh", "sigmoid"])
+@pytest.mark.parametrize("case", FD_CASES)
+def test_finite_differences(case, norm, act):
+    """Every gradient of L = sum(dY * out) against central differences in double."""
+    N, H, W, IC, OC, K, S, P = case
+    L = oracle.Layer(N, H, W, IC, OC, K, K, S, P, norm=norm, act=act)
+    # pick a seed whose activation inputs stay away from the ReLU kink
+    for seed in range(50):
+        rng = np.random.default_rng(1000 + seed)
+        x, w, b, gamma, beta, dy = _rand_layer(rng, L)
+        if act != "relu" or np.min(np.abs(_act_inputs(L, x, w, b, gamma, beta))) > 1e-3:
+            break
+    fwd = oracle.fwd_train(L, x, w, b, gamma, beta)
+    g = oracle.bwd(L, x, w, fwd["ypre"], dy, gamma, beta, fwd["mean"], fwd["inv_std"])
+    f = lambda: _loss(L, x, w, b, gamma, beta, dy)  # noqa: E731
+    checks = [("dx", x, g["dx"]), ("dw", w, g["dw"]), ("db", b, g["db"])]
+    if norm == "batch":
+        checks += [("dgamma", gamma, g["dgamma"]), ("dbeta", beta, g["dbeta"])]
+    for name, arr, an in checks:
+        num = _fd(f, arr)
+        scale = max(np.max(np.abs(num)), np.max(np.abs(an)), 1e-3)
+        err = np.max(np.abs(num - an)) / scale
+        assert err < 1e-6, (name, err)
+
+
+def test_one_by_one_kernel_is_a_matmul():
+    rng = np.random.default_rng(7)
+    L = oracle.Layer(3, 5, 7, 6, 5, 1, 1, 1, 0)
+    x, w, b = rng.standard_normal(L.x_shape), rng.standard_normal(L.w_shape), rng.standard_normal(L.OC)
+    y = oracle.conv_fwd(L, x, w, b)
+    ref = x.reshape(-1, L.IC) @ w.reshape(L.OC, L.IC).T + b
+    np.testing.assert_allclose(y.reshape(-1, L.OC), ref, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("S", [1, 2, 3])
+def test_delta_kernel_is_a_shift(S):
+    """W[oc,c,c,ic] = delta(oc,ic), pad c: the conv reproduces X (subsampled by S)."""
+    rng = np.random.default_rng(11)
+    K, c = 3, 1
+    L = oracle.Layer(2, 7, 6, 4, 4, K, K, S, c)
+    x = rng.standard_normal(L.x_shape)
+    w = np.zeros(L.w_shape)
+    for o in range(4):
+        w[o, c, c, o] = 1.0
+    y = oracle.conv_fwd(L, x, w)
+    np.testing.assert_array_equal(y, x[:, ::S, ::S, :][:, :L.OH, :L.OW, :])
+
+
+def test_shifted_delta_moves_the_image():
+    """A delta off the centre shifts the image, with zeros entering at the border."""
+    rng = np.random.default_rng(12)
+    L = oracle.Layer(1, 5, 5, 2, 2, 3, 3, 1, 1)
+    x = rng.standard_normal(L.x_shape)
+    w = np.zeros(L.w_shape)
+    w[0, 0, 2, 0] = 1.0  # output(oh,ow) = x(oh-1, ow+1)
+    w[1, 2, 0, 1] = 1.0  # output(oh,ow) = x(oh+1, ow-1)
+    y = oracle.conv_fwd(L, x, w)
+    e0 = np.zeros((5, 5))
+    e0[1:, :4] = x[0, :4, 1:, 0]
+    e1 = np.zeros((5, 5))
+    e1[:4, 1:] = x[0, 1:, :4, 1]
+    np.testing.assert_array_equal(y[0, :, :, 0], e0)
+    np.testing.assert_array_equal(y[0, :, :, 1], e1)
+
+
+def test_hand_worked_example():
+    with open(os.path.join(GOLDEN, "hand_worked_3x3.json")) as f:
+        g = json.load(f)
+    L = oracle.Layer(1, 3, 3, 1, 1, 2, 2, 1, 0, norm="none", act="identity")
+    x = np.array(g["x_hw"], float).reshape(L.x_shape)
+    w = np.array(g["w_khkw"], float).reshape(L.w_shape)
+    b = np.array([g["bias"]])
+    y = oracle.conv_fwd(L, x, w, b)
+    np.testing.assert_array_equal(y.reshape(2, 2), np.array(g["ypre_hw"], float))
+    mean, var = oracle.bn_batch_stats(L, y)
+    assert mean[0] == g["bn_mean"] and var[0] == g["bn_var_biased"]
+    out = oracle.bwd(L, x, w, y, np.ones(L.y_shape))
+    h = g["dy_all_ones"]
+    np.testing.assert_array_equal(out["dx"].reshape(3, 3), np.array(h["identity_none_dx_hw"], float))
+    np.testing.assert_array_equal(out["dw"].reshape(2, 2), np.array(h["identity_none_dw_khkw"], float))
+    assert out["db"][0] == h["identity_none_dbias"]
+
+
+def test_batchnorm_invariants():
+    rng = np.random.default_rng(5)
+    L = oracle.Layer(3, 6, 6, 4, 5, 3, 3, 1, 1, norm="batch", act="tanh", eps=1e-3)
+    x, w, b, gamma, beta, dy = _rand_layer(rng, L)
+    f = oracle.fwd_train(L, x, w, b, gamma, beta)
+    n = L.N * L.OH * L.OW
+    z = ((f["ypre"] - f["mean"]) * f["inv_std"]).reshape(n, L.OC)
+    mean, var = oracle.bn_batch_stats(L, f["ypre"])
+    np.testing.assert_allclose(z.mean(0), 0, atol=1e-12)
+    np.testing.assert_allclose((z * z).mean(0), var / (var + L.eps), rtol=1e-12)
+    # running statistics after one step from the initial state (0, 1)
+    np.testing.assert_allclose(f["running_mean"], L.momentum * mean, rtol=1e-14)
+    np.testing.assert_allclose(f["running_var"], (1 - L.momentum) + L.momentum * var, rtol=1e-14)
+    # backward: sum of d_conv is 0, its projection on z is the eps leak
+    dc, dg, _ = oracle.dconv(L, f["ypre"], dy, gamma, beta, f["mean"], f["inv_std"])
+    dc = dc.reshape(n, L.OC)
+    scale = np.abs(dc).sum(0)
+    np.testing.assert_allclose(dc.sum(0) / scale, 0, atol=1e-13)
+    leak = f["inv_std"] * gamma * dg * L.eps / (var + L.eps)
+    np.testing.assert_allclose((dc * z).sum(0), leak, rtol=1e-9, atol=1e-13 * scale.max())
+
+
+def test_adjoint_identities():
+    """<conv(X), G> = <X, dgrad(G)> and <wgrad(X, G), V> = <conv_V(X), G>."""
+    rng = np.random.default_rng(9)
+    for (N, H, W, IC, OC, K, S, P) in [(2, 7, 6, 3, 4, 3, 1, 1), (2, 9, 8, 4, 3, 3, 2, 1), (1, 10, 10, 2, 2, 4, 3, 2)]:
+        L = oracle.Layer(N, H, W, IC, OC, K, K, S, P)
+        x, w = rng.standard_normal(L.x_shape), rng.standard_normal(L.w_shape)
+        G, V = rng.standard_normal(L.y_shape), rng.standard_normal(L.w_shape)
+        lhs = np.sum(oracle.conv_fwd(L, x, w) * G)
+        rhs = np.sum(x * oracle.dgrad(L, G, w))
+        assert abs(lhs - rhs) <= 1e-11 * max(1.0, abs(lhs))
+        lhs2 = np.sum(oracle.wgrad(L, x, G) * V)
+        rhs2 = np.sum(oracle.conv_fwd(L, x, V) * G)
+        assert abs(lhs2 - rhs2) <= 1e-11 * max(1.0, abs(lhs2))
+
+
+def _w1_shader_dw(x_nhwc, dy_nhwc, KH, KW, S, P):
+    """The WGSL weight-gradient shader restated: per image, NCHW, one sum per
+    weight dW[oc,ic,ky,kx] = sum_{oy,ox} dY[oc,oy,ox] * X[ic, oy*S+ky-P, ox*S+kx-P];
+    images summed. Returns [OC,KH,KW,IC] to compare with the oracle."""
+    N, H, W, IC = x_nhwc.shape
+    _, OH, OW, OC = dy_nhwc.shape
+    dw = np.zeros((OC, IC, KH, KW))
+    for n in range(N):
+        X = np.transpose(x_nhwc[n], (2, 0, 1))
+        D = np.transpose(dy_nhwc[n], (2, 0, 1))
+        for oc, ic, ky, kx in itertools.product(range(OC), range(IC), range(KH), range(KW)):
+            s = 0.0
+            for oy in range(OH):
+                iy = oy * S + ky
+                if iy < P or iy >= H + P:
+                    continue
+                for ox in range(OW):
+                    ix = ox * S + kx
+                    if ix < P or ix >= W + P:
+                        continue
+                    s += D[oc, oy, ox] * X[ic, iy - P, ix - P]
+            dw[oc, ic, ky, kx] += s
+    return np.transpose(dw, (0, 2, 3, 1))
+
+
+def test_wgrad_matches_wgsl_shader_math():
+    rng = np.random.default_rng(3)
+    for (N, H, W, IC, OC, K, S, P) in [(2, 6, 5, 3, 2, 3, 1, 1), (2, 7, 7, 2, 3, 3, 2, 0)]:
+        L = oracle.Layer(N, H, W, IC, OC, K, K, S, P)
+        x, g = rng.standard_normal(L.x_shape), rng.standard_normal(L.y_shape)
+        np.testing.assert_allclose(oracle.wgrad(L, x, g), _w1_shader_dw(x, g, K, K, S, P), rtol=1e-12, atol=1e-12)
+
+
+def test_gradients_accumulate_and_dx_overwrites():
+    rng = np.random.default_rng(4)
+    L = oracle.Layer(2, 5, 5, 3, 4, 3, 3, 1, 1, norm="batch", act="relu")
+    x, w, b, gamma, beta, dy = _rand_layer(rng, L)
+    f = oracle.fwd_train(L, x, w, b, gamma, beta)
+    g0 = oracle.bwd(L, x, w, f["ypre"], dy, gamma, beta, f["mean"], f["inv_std"])
+    prev = {k: rng.standard_normal(g0[k].shape) for k in ("dw", "db", "dgamma", "dbeta")}
+    g1 = oracle.bwd(L, x, w, f["ypre"], dy, gamma, beta, f["mean"], f["inv_std"], **prev)
+    for k in prev:
+        np.testing.assert_allclose(g1[k], g0[k] + prev[k], rtol=1e-13, atol=1e-13)
+    np.testing.assert_array_equal(g1["dx"], g0["dx"])
+
+
+def test_activation_values():
+    v = np.array([-2.0, -0.5, 0.0, 0.5, 2.0])
+    np.testing.assert_array_equal(oracle.act("relu", v), [0, 0, 0, 0.5, 2.0])
+    np.testing.assert_allclose(oracle.act("tanh", v), np.tanh(v), rtol=1e-15)
+    np.testing.assert_allclose(oracle.act("sigmoid", v), 1 / (1 + np.exp(-v)), rtol=1e-15)
+    assert oracle.act("sigmoid", 0.0) == 0.5
+    np.testing.assert_array_equal(oracle.dact("relu", v), [0, 0, 0, 1, 1])
+    h = 1e-6
+    for a in ("tanh", "sigmoid", "identity"):
+        fd = (oracle.act(a, v + h) - oracle.act(a, v - h)) / (2 * h)
+        np.testing.assert_allclose(oracle.dact(a, v), fd, rtol=1e-8, atol=1e-9)
+
+
+def test_infer_uses_running_statistics():
+    rng = np.random.default_rng(8)
+    L = oracle.Layer(2, 5, 5, 3, 4, 3, 3, 1, 1, norm="batch", act="sigmoid")
+    x, w, b, gamma, beta, _ = _rand_layer(rng, L)
+    rm, rv = rng.normal(0, 0.3, L.OC), rng.uniform(0.5, 2.0, L.OC)
+    y = oracle.fwd_infer(L, x, w, b, gamma, beta, rm, rv)
+    ypre = oracle.conv_fwd(L, x, w, b)
+    ref = 1 / (1 + np.exp(-(gamma * (ypre - rm) / np.sqrt(rv + L.eps) + beta)))
+    np.testing.assert_allclose(y, ref, rtol=1e-14)
+    Ln = oracle.Layer(2, 5, 5, 3, 4, 3, 3, 1, 1, norm="none", act="tanh")
+    np.testing.assert_array_equal(oracle.fwd_infer(Ln, x, w, b), oracle.fwd_train(Ln, x, w, b)["y"])
+
+
+def test_against_torch_cpu_float64():
+    """Independent third-party computation (torch CPU, float64, autograd)."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    rng = np.random.default_rng(21)
+    acts = {"relu": torch.relu, "tanh": torch.tanh, "sigmoid": torch.sigmoid, "identity": lambda t: t}
+    for (N, H, W, IC, OC, K, S, P, norm, act) in [
+        (3, 9, 8, 5, 6, 3, 1, 1, "batch", "relu"),
+        (2, 11, 11, 4, 8, 5, 2, 2, "batch", "tanh"),
+        (2, 10, 9, 3, 4, 4, 3, 0, "none", "sigmoid"),
+        (2, 6, 6, 8, 4, 1, 1, 0, "batch", "identity"),
+    ]:
+        L = oracle.Layer(N, H, W, IC, OC, K, K, S, P, norm=norm, act=act)
+        x, w, b, gamma, beta, dy = _rand_layer(rng, L)
+        rm0, rv0 = rng.normal(0, 0.2, OC), rng.uniform(0.5, 1.5, OC)
+        f = oracle.fwd_train(L, x, w, b, gamma, beta, rm0, rv0)
+        g = oracle.bwd(L, x, w, f["ypre"], dy, gamma, beta, f["mean"], f["inv_std"])
+
+        tx = torch.tensor(x).permute(0, 3, 1, 2).requires_grad_()
+        tw = torch.tensor(w).permute(0, 3, 1, 2).contiguous().requires_grad_()
+        tb = torch.tensor(b).requires_grad_()
+        tg = torch.tensor(gamma).requires_grad_()
+        tbe = torch.tensor(beta).requires_grad_()
+        trm, trv = torch.tensor(rm0), torch.tensor(rv0)
+        ypre = F.conv2d(tx, tw, tb, stride=S, padding=P)
+        v = F.batch_norm(ypre, trm, trv, tg, tbe, training=True, momentum=L.momentum, eps=L.eps) if norm == "batch" else ypre
+        out = acts[act](v)
+        tdy = torch.tensor(dy).permute(0, 3, 1, 2)
+        (out * tdy).sum().backward()
+
+        nhwc = lambda t: t.detach().permute(0, 2, 3, 1).numpy()  # noqa: E731
+        np.testing.assert_allclose(f["ypre"], nhwc(ypre), rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(f["y"], nhwc(out), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(g["dx"], nhwc(tx.grad), rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(g["dw"], tw.grad.permute(0, 2, 3, 1).numpy(), rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(g["db"], tb.grad.numpy(), rtol=1e-8, atol=1e-10)
+        if norm == "batch":
+            n = N * L.OH * L.OW
+            np.testing.assert_allclose(g["dgamma"], tg.grad.numpy(), rtol=1e-9, atol=1e-11)
+            np.testing.assert_allclose(g["dbeta"], tbe.grad.numpy(), rtol=1e-9, atol=1e-11)
+            np.testing.assert_allclose(f["running_mean"], trm.numpy(), rtol=1e-12, atol=1e-14)
+            # torch keeps the unbiased variance in running_var; the pages keep the biased one
+            var_b = (trv.numpy() - (1 - L.momentum) * rv0) / L.momentum * (n - 1) / n
+            np.testing.assert_allclose(f["running_var"], (1 - L.momentum) * rv0 + L.momentum * var_b, rtol=1e-12)
