@@ -1,0 +1,727 @@
+// api.cu - the C ABI (include/conv2d.h): validation, workspace plan, tensor
+// maps, and the launch sequence of each call.
+//
+// Call sequences (kernels of this library only; nothing runs on the host):
+//   conv2d_fwd_train: [pack x/w] -> fprop GEMM (epilogue: + bias; no norm:
+//                     also y = act) -> [BN: stats -> finalize -> apply]
+//   conv2d_fwd_infer: [fold BN into scale/shift] -> fprop GEMM (epilogue:
+//                     y = act(acc*scale + shift))
+//   conv2d_bwd:       [BN: reduce -> finalize] -> d_conv (+ dbias partials)
+//                     -> finalize -> [dgrad weights -> dgrad GEMM]
+//                     -> [wgrad GEMM -> split reduce]
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "conv2d.h"
+#include "kernels.h"
+
+using namespace c2d;
+
+namespace {
+
+// Device-side error word: kernels record the first bounded wait that ran out.
+__device__ int g_error_word;
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kMaxDynSmem = 232448;  // 227 KB opt-in per block
+
+struct DevInfo {
+  bool init = false;
+  int sms = 0;
+  int* err = nullptr;
+};
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+
+int device_info(DevInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CONV2D_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return CONV2D_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return CONV2D_ERR_CUDA;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_error_word) != cudaSuccess) return CONV2D_ERR_CUDA;
+    d.init = true;
+  }
+  *out = &d;
+  return CONV2D_OK;
+}
+
+// SM count used for sizing when no device is visible (workspace queries on a
+// machine without a GPU).
+int sms_for_sizing() {
+  DevInfo* d = nullptr;
+  if (device_info(&d) == CONV2D_OK) return d->sms;
+  cudaGetLastError();
+  return 152;
+}
+
+// ------------------------------------------------------------ profiling ring
+constexpr int kProfCap = 256;
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+  bool used;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+ProfRec g_prof[kProfCap];
+int g_prof_head = 0, g_prof_count = 0;
+bool g_prof_events = false;
+
+int prof_begin(const char* name, cudaStream_t st) {
+  if (!g_prof_on) return -1;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_events) {
+    for (int i = 0; i < kProfCap; ++i) {
+      cudaEventCreate(&g_prof[i].a);
+      cudaEventCreate(&g_prof[i].b);
+      g_prof[i].used = false;
+    }
+    g_prof_events = true;
+  }
+  const int slot = (g_prof_head + g_prof_count) % kProfCap;
+  if (g_prof_count < kProfCap)
+    ++g_prof_count;
+  else
+    g_prof_head = (g_prof_head + 1) % kProfCap;
+  g_prof[slot].name = name;
+  g_prof[slot].used = true;
+  cudaEventRecord(g_prof[slot].a, st);
+  return slot;
+}
+void prof_end(int slot, cudaStream_t st) {
+  if (slot < 0) return;
+  cudaEventRecord(g_prof[slot].b, st);
+}
+
+#define LAUNCH(name, st, call)                \
+  do {                                        \
+    const int _slot = prof_begin(name, st);   \
+    const cudaError_t _e = (call);            \
+    prof_end(_slot, st);                      \
+    if (_e != cudaSuccess) return CONV2D_ERR_CUDA; \
+  } while (0)
+
+// ------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major tensor [rows][cols], 128-byte swizzled boxes of
+// box_cols x box_rows; out-of-range elements read as zero.
+bool encode_2d(CUtensorMap* m, const void* base, bool bf16, uint64_t cols, uint64_t rows, uint32_t box_cols,
+               uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t es = bf16 ? 2 : 4;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * es};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ geometry
+long ceil_div(long a, long b) { return (a + b - 1) / b; }
+long round_up(long a, long b) { return ceil_div(a, b) * b; }
+
+struct Geo {
+  int N, H, W, IC, OC, KH, KW, S, P, norm, act, dt;
+  float eps, mom;
+  int OH, OW;
+  long n_pix;
+  int ES, EC, BKE;
+  int ICp, OCp, taps;
+  long Kf;
+  bool pack_x;
+};
+
+int make_geo(const conv2d_desc* d, Geo* g) {
+  if (!d) return CONV2D_ERR_INVALID_ARG;
+  if (d->N < 1 || d->H < 1 || d->W < 1 || d->IC < 1 || d->OC < 1 || d->KH < 1 || d->KW < 1 || d->stride < 1 ||
+      d->pad < 0)
+    return CONV2D_ERR_INVALID_ARG;
+  if (static_cast<long>(d->H) + 2L * d->pad < d->KH || static_cast<long>(d->W) + 2L * d->pad < d->KW)
+    return CONV2D_ERR_INVALID_ARG;
+  if (d->norm < 0 || d->norm > 2 || d->act < 0 || d->act > 3 || d->dtype < 0 || d->dtype > 1)
+    return CONV2D_ERR_INVALID_ARG;
+  if (d->norm == CONV2D_NORM_BATCH) {
+    if (!(d->eps > 0.f) || !std::isfinite(d->eps)) return CONV2D_ERR_INVALID_ARG;
+    if (!(d->momentum >= 0.f && d->momentum <= 1.f)) return CONV2D_ERR_INVALID_ARG;
+  }
+  if (d->norm == CONV2D_NORM_LAYER) return CONV2D_ERR_UNSUPPORTED;
+  if (d->stride > 8) return CONV2D_ERR_UNSUPPORTED;
+  Geo& G = *g;
+  G.N = d->N; G.H = d->H; G.W = d->W; G.IC = d->IC; G.OC = d->OC; G.KH = d->KH; G.KW = d->KW;
+  G.S = d->stride; G.P = d->pad; G.norm = d->norm; G.act = d->act; G.dt = d->dtype;
+  G.eps = d->eps; G.mom = d->momentum;
+  G.OH = (G.H + 2 * G.P - G.KH) / G.S + 1;
+  G.OW = (G.W + 2 * G.P - G.KW) / G.S + 1;
+  G.n_pix = static_cast<long>(G.N) * G.OH * G.OW;
+  G.ES = G.dt == CONV2D_BF16 ? 2 : 4;
+  G.EC = 16 / G.ES;
+  G.BKE = 128 / G.ES;
+  G.ICp = static_cast<int>(round_up(G.IC, G.EC));
+  G.OCp = G.dt == CONV2D_BF16 ? (G.OC < 64 ? 64 : static_cast<int>(round_up(G.OC, 8)))
+                              : static_cast<int>(round_up(G.OC, 4));
+  G.taps = G.KH * G.KW;
+  G.Kf = static_cast<long>(G.taps) * G.ICp;
+  G.pack_x = G.ICp != G.IC;
+  const long lim = INT_MAX;
+  if (static_cast<long>(G.N) * G.H * G.W > lim / 2 || G.n_pix > lim / 2 || G.Kf > lim / 2 ||
+      static_cast<long>(G.N) * G.H * G.W * G.ICp > (1L << 40) || G.n_pix * G.OCp > (1L << 40) ||
+      static_cast<long>(G.OC) * G.Kf > lim / 2 || G.OC > 65535)
+    return CONV2D_ERR_UNSUPPORTED;
+  return CONV2D_OK;
+}
+
+// ------------------------------------------------------------ GEMM planning
+struct Tile {
+  int BN, n_tiles, stages;
+  size_t smem;
+};
+
+Tile conv_tile(const Geo& g, int ncols) {
+  Tile t;
+  const int bn_max = g.dt == CONV2D_BF16 ? 256 : 128;
+  t.n_tiles = static_cast<int>(ceil_div(ncols, bn_max));
+  t.BN = static_cast<int>(round_up(ceil_div(ncols, t.n_tiles), 16));
+  const size_t ns = g.dt == CONV2D_BF16 ? 1 : 2;
+  const size_t stage = ns * (kBM * 128 + static_cast<size_t>(t.BN) * 128);
+  t.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048) / stage));
+  t.smem = t.stages * stage + 1024 + 256;
+  return t;
+}
+
+struct WgradPlan {
+  int Mk, m_tiles, BN, n_tiles, KP, kb_total, kb_per_split, splits, stages, units;
+  size_t smem;
+};
+
+WgradPlan wgrad_plan(const Geo& g, int sms) {
+  WgradPlan w;
+  const bool bf = g.dt == CONV2D_BF16;
+  w.Mk = static_cast<int>(g.Kf);
+  w.m_tiles = static_cast<int>(ceil_div(w.Mk, kBM));
+  if (bf) {
+    w.n_tiles = static_cast<int>(ceil_div(g.OC, 256));
+    w.BN = static_cast<int>(round_up(ceil_div(g.OC, w.n_tiles), 64));
+  } else {
+    w.n_tiles = static_cast<int>(ceil_div(g.OC, 128));
+    w.BN = static_cast<int>(round_up(ceil_div(g.OC, w.n_tiles), 16));
+  }
+  w.KP = bf ? 64 : 32;
+  w.kb_total = static_cast<int>(ceil_div(g.n_pix, w.KP));
+  const int base = w.m_tiles * w.n_tiles;
+  // time model: per-CTA serial k-blocks (waves x k-blocks per split) plus the
+  // HBM traffic of writing and re-reading the fp32 partials
+  const double flops_kb = 2.0 * kBM * w.BN * w.KP * (bf ? 1.0 : 6.0);
+  const double t_kb = flops_kb / (2.25e15 / 152.0);
+  const double t_split = static_cast<double>(base) * kBM * w.BN * 8.0 / 6.8e12;
+  int best = 1;
+  double best_t = 1e30;
+  const int smax = std::max(1, std::min(w.kb_total, 16 * sms));
+  for (int s = 1; s <= smax; ++s) {
+    const int kbp = static_cast<int>(ceil_div(w.kb_total, s));
+    const int s_eff = static_cast<int>(ceil_div(w.kb_total, kbp));
+    if (s_eff != s) continue;
+    const long units = static_cast<long>(base) * s;
+    const long waves = ceil_div(units, sms);
+    const double t = waves * kbp * t_kb + s * t_split;
+    if (t < best_t) {
+      best_t = t;
+      best = s;
+    }
+  }
+  w.splits = best;
+  w.kb_per_split = static_cast<int>(ceil_div(w.kb_total, w.splits));
+  w.units = base * w.splits;
+  const size_t ns = bf ? 1 : 2;
+  const size_t stage = ns * (kBM * 128 + static_cast<size_t>(w.BN) * 128);
+  w.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048) / stage));
+  w.smem = w.stages * stage + 1024 + 256;
+  return w;
+}
+
+struct DgradPlan {
+  int num_phases;
+  ConvPhase ph[kMaxPhases];
+  DgradWeightTable table;
+  int Kd;
+  int units;
+  Tile tile;
+};
+
+DgradPlan dgrad_plan(const Geo& g) {
+  DgradPlan d;
+  std::memset(&d, 0, sizeof(d));
+  d.tile = conv_tile(g, g.IC);
+  const int S = g.S;
+  int unit = 0, col = 0, n = 0;
+  for (int ph_h = 0; ph_h < S; ++ph_h)
+    for (int ph_w = 0; ph_w < S; ++ph_w) {
+      const int Ha = ph_h < g.H ? static_cast<int>(ceil_div(g.H - ph_h, S)) : 0;
+      const int Wa = ph_w < g.W ? static_cast<int>(ceil_div(g.W - ph_w, S)) : 0;
+      if (Ha == 0 || Wa == 0) continue;
+      const int rh = (ph_h + g.P) % S, rw = (ph_w + g.P) % S;
+      const int Th = rh < g.KH ? static_cast<int>(ceil_div(g.KH - rh, S)) : 0;
+      const int Tw = rw < g.KW ? static_cast<int>(ceil_div(g.KW - rw, S)) : 0;
+      ConvPhase& p = d.ph[d.num_phases++];
+      p.rows = g.N * Ha * Wa;
+      p.Ha = Ha;
+      p.Wa = Wa;
+      p.qh = (ph_h + g.P - rh) / S;
+      p.qw = (ph_w + g.P - rw) / S;
+      p.Tw = std::max(Tw, 1);
+      p.K = Th * Tw * g.OCp;
+      p.num_kb = static_cast<int>(ceil_div(p.K, g.BKE));
+      p.unit_begin = unit;
+      p.b_col = col;
+      p.oh0 = ph_h;
+      p.ow0 = ph_w;
+      p.div_Wa = make_fastdiv(Wa);
+      p.div_HaWa = make_fastdiv(Ha * Wa);
+      p.div_Tw = make_fastdiv(p.Tw);
+      if (Th * Tw > 0) {
+        d.table.col_off[n] = col;
+        d.table.Th[n] = Th;
+        d.table.Tw[n] = Tw;
+        d.table.rh[n] = rh;
+        d.table.rw[n] = rw;
+        ++n;
+        col += p.K;
+      }
+      unit += static_cast<int>(ceil_div(p.rows, kBM)) * d.tile.n_tiles;
+    }
+  d.table.n = n;
+  d.Kd = std::max(col, g.BKE);
+  d.units = unit;
+  return d;
+}
+
+// ------------------------------------------------------------ workspace plan
+enum Reg { R_XP, R_WB, R_WBLO, R_PART, R_FOLD, R_DC, R_C12, R_WD, R_WDLO, R_WPART, R_NREG };
+
+struct Plan {
+  size_t off[R_NREG];
+  size_t total;
+  RowWalk walk;
+  WgradPlan wg;
+};
+
+void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
+  size_t sz[R_NREG] = {0};
+  const size_t es = g.ES;
+  pl->walk = make_walk(g.n_pix, g.OC, g.dt, sms);
+  const size_t G = pl->walk.G;
+  if (op == CONV2D_OP_FWD_TRAIN || op == CONV2D_OP_FWD_INFER) {
+    if (g.pack_x) sz[R_XP] = static_cast<size_t>(g.N) * g.H * g.W * g.ICp * es;
+    if (g.dt == CONV2D_FP32 || g.pack_x) sz[R_WB] = static_cast<size_t>(g.OC) * g.Kf * es;
+    if (g.dt == CONV2D_FP32) sz[R_WBLO] = static_cast<size_t>(g.OC) * g.Kf * 4;
+    if (op == CONV2D_OP_FWD_TRAIN && g.norm == CONV2D_NORM_BATCH) sz[R_PART] = G * g.OC * 3 * 4;
+    if (op == CONV2D_OP_FWD_INFER) sz[R_FOLD] = 2 * static_cast<size_t>(g.OC) * 4;
+  } else {
+    const DgradPlan* unused = nullptr;
+    (void)unused;
+    sz[R_DC] = static_cast<size_t>(g.n_pix) * g.OCp * es;
+    sz[R_PART] = G * g.OC * 2 * 4;
+    sz[R_C12] = 2 * static_cast<size_t>(g.OC) * 4;
+    // dgrad weights: every phase's taps together hold each kernel tap once
+    const size_t kd = std::max<size_t>(static_cast<size_t>(g.taps) * g.OCp, g.BKE);
+    sz[R_WD] = static_cast<size_t>(g.ICp) * kd * es;
+    if (g.dt == CONV2D_FP32) sz[R_WDLO] = static_cast<size_t>(g.ICp) * kd * 4;
+    if (g.pack_x) sz[R_XP] = static_cast<size_t>(g.N) * g.H * g.W * g.ICp * es;
+    pl->wg = wgrad_plan(g, sms);
+    sz[R_WPART] = static_cast<size_t>(pl->wg.splits) * g.OC * pl->wg.Mk * 4;
+  }
+  size_t o = 0;
+  for (int r = 0; r < R_NREG; ++r) {
+    pl->off[r] = o;
+    o += round_up(static_cast<long>(sz[r]), 1024);
+  }
+  pl->total = o;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+#define REQ_PTR(p) \
+  do { if (!(p) || !aligned16(p)) return CONV2D_ERR_INVALID_ARG; } while (0)
+#define OPT_PTR(p) \
+  do { if ((p) && !aligned16(p)) return CONV2D_ERR_INVALID_ARG; } while (0)
+
+char* region(void* ws, const Plan& pl, Reg r) { return static_cast<char*>(ws) + pl.off[r]; }
+
+// fprop GEMM: D[pix][oc] = im2col(x) * B^T, epilogue per ConvGemmParams.
+int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bhi, const void* blo, void* out,
+              void* out2, const float* scale, const float* shift, int out_act, cudaStream_t st) {
+  static ConvGemmParams p;  // guarded by g_launch_mu below (large struct)
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  std::memset(&p, 0, sizeof(p));
+  const Tile t = conv_tile(g, g.OC);
+  const bool bf = g.dt == CONV2D_BF16;
+  if (!encode_2d(&p.tmap_b, bhi, bf, g.Kf, g.OC, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
+  if (!bf && !encode_2d(&p.tmap_b_lo, blo, false, g.Kf, g.OC, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
+  p.src = xsrc;
+  p.Hs = g.H;
+  p.Ws = g.W;
+  p.Cs = g.ICp;
+  p.rs = g.S;
+  p.tap_sign = 1;
+  p.div_Cs = make_fastdiv(g.ICp);
+  p.num_phases = 1;
+  ConvPhase& ph = p.ph[0];
+  ph.rows = static_cast<int>(g.n_pix);
+  ph.Ha = g.OH;
+  ph.Wa = g.OW;
+  ph.qh = -g.P;
+  ph.qw = -g.P;
+  ph.Tw = g.KW;
+  ph.K = static_cast<int>(g.Kf);
+  ph.num_kb = static_cast<int>(ceil_div(g.Kf, g.BKE));
+  ph.unit_begin = 0;
+  ph.b_col = 0;
+  ph.div_Wa = make_fastdiv(g.OW);
+  ph.div_HaWa = make_fastdiv(g.OH * g.OW);
+  ph.div_Tw = make_fastdiv(g.KW);
+  p.n_tiles = t.n_tiles;
+  p.BN = t.BN;
+  p.N = g.OC;
+  p.num_units = static_cast<int>(ceil_div(g.n_pix, kBM)) * t.n_tiles;
+  p.out = out;
+  p.out2 = out2;
+  p.out_ld = g.OC;
+  p.Ho = g.OH;
+  p.Wo = g.OW;
+  p.os = 1;
+  p.ep_scale = scale;
+  p.ep_shift = shift;
+  p.act = g.act;
+  p.out_act = out_act;
+  p.stages = t.stages;
+  p.err = dev->err;
+  const int grid = std::min(p.num_units, dev->sms);
+  LAUNCH("fprop_gemm", st, bf ? launch_conv_gemm_bf16(p, grid, t.smem, st) : launch_conv_gemm_tf32(p, grid, t.smem, st));
+  return CONV2D_OK;
+}
+
+int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv, void* dx, void* ws,
+              const Plan& pl, cudaStream_t st) {
+  static ConvGemmParams p;
+  static DgradPlan d;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  const bool bf = g.dt == CONV2D_BF16;
+  d = dgrad_plan(g);
+  void* whi = region(ws, pl, R_WD);
+  float* wlo = reinterpret_cast<float*>(region(ws, pl, R_WDLO));
+  LAUNCH("dgrad_weights", st,
+         launch_prep_dgrad_weights(g.dt, w, whi, bf ? nullptr : wlo, g.OC, g.KH, g.KW, g.IC, g.ICp, g.OCp, g.S, d.Kd,
+                                   d.table, st));
+  std::memset(&p, 0, sizeof(p));
+  if (!encode_2d(&p.tmap_b, whi, bf, d.Kd, g.ICp, g.BKE, d.tile.BN)) return CONV2D_ERR_CUDA;
+  if (!bf && !encode_2d(&p.tmap_b_lo, wlo, false, d.Kd, g.ICp, g.BKE, d.tile.BN)) return CONV2D_ERR_CUDA;
+  p.src = dconv;
+  p.Hs = g.OH;
+  p.Ws = g.OW;
+  p.Cs = g.OCp;
+  p.rs = 1;
+  p.tap_sign = -1;
+  p.div_Cs = make_fastdiv(g.OCp);
+  p.num_phases = d.num_phases;
+  for (int i = 0; i < d.num_phases; ++i) p.ph[i] = d.ph[i];
+  p.n_tiles = d.tile.n_tiles;
+  p.BN = d.tile.BN;
+  p.N = g.IC;
+  p.num_units = d.units;
+  p.out = dx;
+  p.out2 = nullptr;
+  p.out_ld = g.IC;
+  p.Ho = g.H;
+  p.Wo = g.W;
+  p.os = g.S;
+  p.act = 0;
+  p.out_act = 0;
+  p.stages = d.tile.stages;
+  p.err = dev->err;
+  const int grid = std::min(p.num_units, dev->sms);
+  LAUNCH("dgrad_gemm", st,
+         bf ? launch_conv_gemm_bf16(p, grid, d.tile.smem, st) : launch_conv_gemm_tf32(p, grid, d.tile.smem, st));
+  return CONV2D_OK;
+}
+
+int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dconv, float* dw, void* ws,
+              const Plan& pl, cudaStream_t st) {
+  WgradParams p;
+  std::memset(&p, 0, sizeof(p));
+  const WgradPlan& w = pl.wg;
+  const bool bf = g.dt == CONV2D_BF16;
+  if (bf && !encode_2d(&p.tmap_dc, dconv, true, g.OCp, g.n_pix, 64, 64)) return CONV2D_ERR_CUDA;
+  p.x = xsrc;
+  p.dc32 = bf ? nullptr : static_cast<const float*>(dconv);
+  p.H = g.H;
+  p.W = g.W;
+  p.Cs = g.ICp;
+  p.OH = g.OH;
+  p.OW = g.OW;
+  p.S = g.S;
+  p.P = g.P;
+  p.KW = g.KW;
+  p.div_Cs = make_fastdiv(g.ICp);
+  p.div_KW = make_fastdiv(g.KW);
+  p.div_OW = make_fastdiv(g.OW);
+  p.div_OHOW = make_fastdiv(g.OH * g.OW);
+  p.Mk = w.Mk;
+  p.m_tiles = w.m_tiles;
+  p.n_tiles = w.n_tiles;
+  p.BN = w.BN;
+  p.N = g.OC;
+  p.OCp = g.OCp;
+  p.n_pix = static_cast<int>(g.n_pix);
+  p.kb_total = w.kb_total;
+  p.kb_per_split = w.kb_per_split;
+  p.splits = w.splits;
+  p.num_units = w.units;
+  p.partial = reinterpret_cast<float*>(region(ws, pl, R_WPART));
+  p.stages = w.stages;
+  p.err = dev->err;
+  const int grid = std::min(p.num_units, dev->sms);
+  LAUNCH("wgrad_gemm", st,
+         bf ? launch_wgrad_gemm_bf16(p, grid, w.smem, st) : launch_wgrad_gemm_tf32(p, grid, w.smem, st));
+  LAUNCH("wgrad_reduce", st, launch_wgrad_reduce(p.partial, w.splits, g.OC, g.taps, g.ICp, g.IC, dw, st));
+  return CONV2D_OK;
+}
+
+// Pack x (and w) to ICp channels when IC is not a multiple of the 16-byte
+// vector; for fp32 split w into tf32 hi / lo. Returns the GEMM operands.
+int prep_forward_operands(const Geo& g, const void* x, const void* w, void* ws, const Plan& pl, const void** xsrc,
+                          const void** bhi, const void** blo, cudaStream_t st) {
+  *xsrc = x;
+  *bhi = w;
+  *blo = nullptr;
+  if (g.pack_x) {
+    void* xp = region(ws, pl, R_XP);
+    LAUNCH("pack_x", st, launch_pack_channels(g.dt, x, xp, static_cast<long>(g.N) * g.H * g.W, g.IC, g.ICp, st));
+    *xsrc = xp;
+  }
+  if (g.dt == CONV2D_FP32 || g.pack_x) {
+    void* wb = region(ws, pl, R_WB);
+    float* wl = reinterpret_cast<float*>(region(ws, pl, R_WBLO));
+    LAUNCH("prep_w", st,
+           launch_prep_fprop_weights(g.dt, w, wb, g.dt == CONV2D_FP32 ? wl : nullptr, g.OC, g.taps, g.IC, g.ICp, st));
+    *bhi = wb;
+    if (g.dt == CONV2D_FP32) *blo = wl;
+  }
+  return CONV2D_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int conv2d_out_hw(const conv2d_desc* desc, int32_t* OH, int32_t* OW) {
+  Geo g;
+  const int rc = make_geo(desc, &g);
+  if (rc == CONV2D_ERR_INVALID_ARG) return rc;
+  if (!desc || !OH || !OW) return CONV2D_ERR_INVALID_ARG;
+  *OH = (desc->H + 2 * desc->pad - desc->KH) / desc->stride + 1;
+  *OW = (desc->W + 2 * desc->pad - desc->KW) / desc->stride + 1;
+  return CONV2D_OK;
+}
+
+int conv2d_validate(const conv2d_desc* desc) {
+  Geo g;
+  return make_geo(desc, &g);
+}
+
+size_t conv2d_workspace_size(const conv2d_desc* desc, int op) {
+  Geo g;
+  if (make_geo(desc, &g) != CONV2D_OK) return 0;
+  if (op < 0 || op > 2) return 0;
+  Plan pl;
+  plan_ws(g, op, sms_for_sizing(), &pl);
+  return pl.total;
+}
+
+int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, const float* bias, const float* gamma,
+                     const float* beta, float* running_mean, float* running_var, void* pre_act, float* save_mean,
+                     float* save_inv_std, void* y, void* ws, size_t ws_bytes, void* stream) {
+  Geo g;
+  int rc = make_geo(desc, &g);
+  if (rc) return rc;
+  REQ_PTR(x); REQ_PTR(w); REQ_PTR(pre_act); REQ_PTR(y); OPT_PTR(bias);
+  if (g.norm == CONV2D_NORM_BATCH) {
+    REQ_PTR(gamma); REQ_PTR(beta); REQ_PTR(running_mean); REQ_PTR(running_var); REQ_PTR(save_mean);
+    REQ_PTR(save_inv_std);
+  }
+  DevInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  Plan pl;
+  plan_ws(g, CONV2D_OP_FWD_TRAIN, dev->sms, &pl);
+  if (!ws || ws_bytes < pl.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CONV2D_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const void *xsrc, *bhi, *blo;
+  if ((rc = prep_forward_operands(g, x, w, ws, pl, &xsrc, &bhi, &blo, st))) return rc;
+  const bool bn = g.norm == CONV2D_NORM_BATCH;
+  if ((rc = run_fprop(g, dev, xsrc, bhi, blo, pre_act, bn ? nullptr : y, nullptr, bias, 0, st))) return rc;
+  if (bn) {
+    float* part = reinterpret_cast<float*>(region(ws, pl, R_PART));
+    LAUNCH("bn_stats", st, launch_bn_stats(g.dt, pre_act, pl.walk, part, st));
+    LAUNCH("bn_stats_finalize", st,
+           launch_bn_stats_finalize(part, pl.walk, g.eps, g.mom, save_mean, save_inv_std, running_mean, running_var,
+                                    st));
+    LAUNCH("bn_apply", st, launch_bn_apply(g.dt, pre_act, y, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, st));
+  }
+  return CONV2D_OK;
+}
+
+int conv2d_fwd_infer(const conv2d_desc* desc, const void* x, const void* w, const float* bias, const float* gamma,
+                     const float* beta, const float* running_mean, const float* running_var, void* y, void* ws,
+                     size_t ws_bytes, void* stream) {
+  Geo g;
+  int rc = make_geo(desc, &g);
+  if (rc) return rc;
+  REQ_PTR(x); REQ_PTR(w); REQ_PTR(y); OPT_PTR(bias);
+  if (g.norm == CONV2D_NORM_BATCH) {
+    REQ_PTR(gamma); REQ_PTR(beta); REQ_PTR(running_mean); REQ_PTR(running_var);
+  }
+  DevInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  Plan pl;
+  plan_ws(g, CONV2D_OP_FWD_INFER, dev->sms, &pl);
+  if (!ws || ws_bytes < pl.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CONV2D_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const void *xsrc, *bhi, *blo;
+  if ((rc = prep_forward_operands(g, x, w, ws, pl, &xsrc, &bhi, &blo, st))) return rc;
+  float* scale = reinterpret_cast<float*>(region(ws, pl, R_FOLD));
+  float* shift = scale + g.OC;
+  LAUNCH("infer_fold", st,
+         launch_infer_fold(bias, gamma, beta, running_mean, running_var, g.eps, g.norm, g.OC, scale, shift, st));
+  return run_fprop(g, dev, xsrc, bhi, blo, y, nullptr, scale, shift, 1, st);
+}
+
+int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const float* gamma, const float* beta,
+               const void* pre_act, const float* save_mean, const float* save_inv_std, const void* dy, void* dx,
+               float* dw, float* dbias, float* dgamma, float* dbeta, void* ws, size_t ws_bytes, void* stream) {
+  Geo g;
+  int rc = make_geo(desc, &g);
+  if (rc) return rc;
+  REQ_PTR(pre_act); REQ_PTR(dy); OPT_PTR(dx); OPT_PTR(dw); OPT_PTR(dbias); OPT_PTR(dgamma); OPT_PTR(dbeta);
+  if (!dx && !dw) return CONV2D_ERR_INVALID_ARG;
+  if (dw && !dbias) return CONV2D_ERR_INVALID_ARG;
+  if (dx) REQ_PTR(w);
+  if (dw) REQ_PTR(x);
+  const bool bn = g.norm == CONV2D_NORM_BATCH;
+  if (bn) {
+    REQ_PTR(gamma); REQ_PTR(beta); REQ_PTR(save_mean); REQ_PTR(save_inv_std);
+    if (static_cast<bool>(dgamma) != static_cast<bool>(dbeta)) return CONV2D_ERR_INVALID_ARG;
+  }
+  DevInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  Plan pl;
+  plan_ws(g, CONV2D_OP_BWD, dev->sms, &pl);
+  if (!ws || ws_bytes < pl.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CONV2D_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* dconv = region(ws, pl, R_DC);
+  float* part = reinterpret_cast<float*>(region(ws, pl, R_PART));
+  float* c12 = reinterpret_cast<float*>(region(ws, pl, R_C12));
+  if (bn) {
+    LAUNCH("bn_bwd_reduce", st,
+           launch_bn_bwd_reduce(g.dt, pre_act, dy, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, part, st));
+    LAUNCH("bn_bwd_finalize", st, launch_sum_finalize(part, pl.walk, 2, 0, c12, dbeta, dgamma, st));
+    LAUNCH("bn_bwd_dconv", st,
+           launch_bn_bwd_apply(g.dt, pre_act, dy, pl.walk, g.OCp, save_mean, save_inv_std, gamma, beta, g.act, c12,
+                               dconv, part, st));
+  } else {
+    LAUNCH("act_bwd_dconv", st, launch_act_bwd(g.dt, pre_act, dy, pl.walk, g.OCp, g.act, dconv, part, st));
+  }
+  if (dbias) LAUNCH("dbias_finalize", st, launch_sum_finalize(part, pl.walk, 1, 1, nullptr, dbias, nullptr, st));
+  if (dx && (rc = run_dgrad(g, dev, w, dconv, dx, ws, pl, st))) return rc;
+  if (dw) {
+    const void* xsrc = x;
+    if (g.pack_x) {
+      void* xp = region(ws, pl, R_XP);
+      LAUNCH("pack_x", st, launch_pack_channels(g.dt, x, xp, static_cast<long>(g.N) * g.H * g.W, g.IC, g.ICp, st));
+      xsrc = xp;
+    }
+    if ((rc = run_wgrad(g, dev, xsrc, dconv, dw, ws, pl, st))) return rc;
+  }
+  return CONV2D_OK;
+}
+
+int conv2d_device_status(void* stream, int32_t* site) {
+  DevInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return CONV2D_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, dev->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CONV2D_ERR_CUDA;
+  if (site) *site = v;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(dev->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return CONV2D_ERR_CUDA;
+    return CONV2D_ERR_TIMEOUT;
+  }
+  return CONV2D_OK;
+}
+
+const char* conv2d_status_str(int status) {
+  switch (status) {
+    case CONV2D_OK: return "ok";
+    case CONV2D_ERR_INVALID_ARG: return "invalid argument";
+    case CONV2D_ERR_UNSUPPORTED: return "unsupported configuration";
+    case CONV2D_ERR_WORKSPACE: return "workspace missing or too small";
+    case CONV2D_ERR_CUDA: return "CUDA error";
+    case CONV2D_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int conv2d_prof_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = on != 0;
+  return CONV2D_OK;
+}
+
+int conv2d_prof_read(const char** names, float* ms, int cap) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  int n = 0;
+  for (int i = 0; i < g_prof_count && n < cap; ++i) {
+    ProfRec& r = g_prof[(g_prof_head + i) % kProfCap];
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) t = -1.f;
+    if (names) names[n] = r.name;
+    if (ms) ms[n] = t;
+    ++n;
+  }
+  g_prof_head = 0;
+  g_prof_count = 0;
+  return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,679 @@
+// bn_kernels.cu - the bandwidth-bound steps of the conv2d training step:
+// batch-norm statistics, normalise + affine + activation, activation /
+// batch-norm backward (d_conv, dgamma, dbeta, dbias), weight preparation for
+// the tensor-core GEMMs, and the split-K reduction of dW.
+//
+// Formulas: rl-tools "operations_generic.h" (`forward` BN training branch and
+// Phase 3; `backward_full` training branch) and the per-channel kernels of
+// "operations_cuda.h" (`bn_stats_training`, `bn_forward_affine`,
+// `bn_training_backward`, `bias_backward_partial/finalize`). The layout work
+// is different from those kernels: NHWC rows are read with 16-byte vector
+// loads, a thread keeps a fixed group of channels for its whole walk, and
+// each block writes one partial per channel that a small finalize kernel
+// merges in double in a fixed order (deterministic). The variance is a
+// shifted single pass merged with Chan's formula, not E[x^2] - mean^2.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace c2d {
+
+namespace {
+
+constexpr int kBlock = 256;
+
+template <int EC>
+__device__ __forceinline__ void load_v(const float* p, float (&v)[EC]) {
+  if constexpr (EC == 4) {
+    const float4 t = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < EC; ++e) v[e] = __ldg(p + e);
+  }
+}
+template <int EC>
+__device__ __forceinline__ void load_v(const __nv_bfloat16* p, float (&v)[EC]) {
+  if constexpr (EC == 8) {
+    const uint4 t = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+      const float2 f = __bfloat1622float2(h);
+      v[2 * e] = f.x;
+      v[2 * e + 1] = f.y;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < EC; ++e) v[e] = __bfloat162float(p[e]);
+  }
+}
+template <int EC>
+__device__ __forceinline__ void store_v(float* p, const float (&v)[EC]) {
+  if constexpr (EC == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < EC; ++e) p[e] = v[e];
+  }
+}
+template <int EC>
+__device__ __forceinline__ void store_v(__nv_bfloat16* p, const float (&v)[EC]) {
+  if constexpr (EC == 8) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+      w[e] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < EC; ++e) p[e] = __float2bfloat16_rn(v[e]);
+  }
+}
+
+// Thread geometry of a block walking [rows][C]: `tpr` threads share a row,
+// each owning EC consecutive channels; `rpp` rows are in flight per pass.
+struct Lane {
+  int cg, tpr, rpp, rl, g0;
+  long r0, r1;
+};
+__device__ __forceinline__ Lane lane_of(long rows, int Cw, int EC, long rpb) {
+  Lane l;
+  l.cg = Cw / EC;
+  l.tpr = l.cg < kBlock ? l.cg : kBlock;
+  l.rpp = kBlock / l.tpr;
+  l.rl = threadIdx.x / l.tpr;
+  l.g0 = threadIdx.x % l.tpr;
+  l.r0 = static_cast<long>(blockIdx.x) * rpb;
+  l.r1 = min(rows, l.r0 + rpb);
+  return l;
+}
+
+__device__ __forceinline__ void chan_merge(float& na, float& ma, float& Ma, float nb, float mb, float Mb) {
+  const float n = na + nb;
+  if (nb == 0.f) return;
+  if (na == 0.f) {
+    na = nb; ma = mb; Ma = Mb;
+    return;
+  }
+  const float d = mb - ma;
+  ma = ma + d * (nb / n);
+  Ma = Ma + Mb + d * d * (na * nb / n);
+  na = n;
+}
+
+// ------------------------------------------------------------ BN statistics
+template <typename T, int EC>
+__global__ void __launch_bounds__(kBlock) bn_stats_kernel(const T* __restrict__ pre, long rows, int C, long rpb,
+                                                          float* __restrict__ part) {
+  __shared__ float s_n[kBlock], s_m[kBlock * EC], s_M[kBlock * EC];
+  const Lane l = lane_of(rows, C, EC, rpb);
+  for (int gb = 0; gb < l.cg; gb += l.tpr) {
+    const int g = gb + l.g0;
+    const bool active = g < l.cg && l.rl < l.rpp;
+    float shift[EC], s1[EC], s2[EC];
+    int cnt = 0;
+#pragma unroll
+    for (int e = 0; e < EC; ++e) shift[e] = s1[e] = s2[e] = 0.f;
+    if (active) {
+      for (long r = l.r0 + l.rl; r < l.r1; r += l.rpp) {
+        float v[EC];
+        load_v<EC>(pre + r * C + g * EC, v);
+        if (cnt == 0) {
+#pragma unroll
+          for (int e = 0; e < EC; ++e) shift[e] = v[e];
+        }
+#pragma unroll
+        for (int e = 0; e < EC; ++e) {
+          const float d = v[e] - shift[e];
+          s1[e] += d;
+          s2[e] = fmaf(d, d, s2[e]);
+        }
+        ++cnt;
+      }
+    }
+    s_n[threadIdx.x] = static_cast<float>(cnt);
+#pragma unroll
+    for (int e = 0; e < EC; ++e) {
+      const float fc = cnt > 0 ? static_cast<float>(cnt) : 1.f;
+      s_m[threadIdx.x * EC + e] = shift[e] + s1[e] / fc;
+      s_M[threadIdx.x * EC + e] = fmaxf(s2[e] - s1[e] * (s1[e] / fc), 0.f);
+    }
+    __syncthreads();
+    if (active && l.rl == 0) {
+      for (int e = 0; e < EC; ++e) {
+        float n = 0.f, m = 0.f, M = 0.f;
+        for (int k = 0; k < l.rpp; ++k) {
+          const int src = k * l.tpr + l.g0;
+          chan_merge(n, m, M, s_n[src], s_m[src * EC + e], s_M[src * EC + e]);
+        }
+        const int c = g * EC + e;
+        float* o = part + (static_cast<size_t>(blockIdx.x) * C + c) * 3;
+        o[0] = n;
+        o[1] = m;
+        o[2] = M;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(128) bn_stats_finalize_kernel(const float* __restrict__ part, int G, int C,
+                                                                float eps, float momentum, float* mean,
+                                                                float* inv_std, float* rm, float* rv) {
+  __shared__ double s_n[128], s_m[128], s_M[128];
+  const int c = blockIdx.x;
+  double n = 0, m = 0, M = 0;
+  for (int b = threadIdx.x; b < G; b += 128) {
+    const float* p = part + (static_cast<size_t>(b) * C + c) * 3;
+    const double nb = p[0], mb = p[1], Mb = p[2];
+    if (nb == 0) continue;
+    const double nn = n + nb, d = mb - m;
+    m += d * nb / nn;
+    M += Mb + d * d * n * nb / nn;
+    n = nn;
+  }
+  s_n[threadIdx.x] = n;
+  s_m[threadIdx.x] = m;
+  s_M[threadIdx.x] = M;
+  __syncthreads();
+  for (int off = 64; off > 0; off >>= 1) {
+    if (threadIdx.x < off) {
+      const double na = s_n[threadIdx.x], nb = s_n[threadIdx.x + off];
+      if (nb > 0) {
+        const double nn = na + nb, d = s_m[threadIdx.x + off] - s_m[threadIdx.x];
+        s_m[threadIdx.x] += d * nb / nn;
+        s_M[threadIdx.x] += s_M[threadIdx.x + off] + d * d * na * nb / nn;
+        s_n[threadIdx.x] = nn;
+      }
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double nt = s_n[0];
+    const double mu = s_m[0];
+    const double var = nt > 0 ? s_M[0] / nt : 0.0;  // biased, as on the pages
+    mean[c] = static_cast<float>(mu);
+    inv_std[c] = static_cast<float>(1.0 / sqrt(var + static_cast<double>(eps)));
+    rm[c] = static_cast<float>((1.0 - momentum) * rm[c] + static_cast<double>(momentum) * mu);
+    rv[c] = static_cast<float>((1.0 - momentum) * rv[c] + static_cast<double>(momentum) * var);
+  }
+}
+
+// ------------------------------------------------------------ BN apply + act
+template <typename T, int EC>
+__global__ void __launch_bounds__(kBlock) bn_apply_kernel(const T* __restrict__ pre, T* __restrict__ y, long rows,
+                                                          int C, long rpb, const float* __restrict__ mean,
+                                                          const float* __restrict__ inv_std,
+                                                          const float* __restrict__ gamma,
+                                                          const float* __restrict__ beta, int act) {
+  const Lane l = lane_of(rows, C, EC, rpb);
+  if (l.rl >= l.rpp) return;
+  for (int g = l.g0; g < l.cg; g += l.tpr) {
+    float mu[EC], sc[EC], be[EC];
+#pragma unroll
+    for (int e = 0; e < EC; ++e) {
+      const int c = g * EC + e;
+      mu[e] = mean[c];
+      sc[e] = gamma[c] * inv_std[c];
+      be[e] = beta[c];
+    }
+    for (long r = l.r0 + l.rl; r < l.r1; r += l.rpp) {
+      float v[EC];
+      load_v<EC>(pre + r * C + g * EC, v);
+#pragma unroll
+      for (int e = 0; e < EC; ++e) v[e] = act_f(act, fmaf(v[e] - mu[e], sc[e], be[e]));
+      store_v<EC>(y + r * C + g * EC, v);
+    }
+  }
+}
+
+// ------------------------------------------------------------ BN backward
+// part[b][c] = {sum d_norm, sum d_norm * z}, d_norm = act'(gamma z + beta) dy.
+template <typename T, int EC>
+__global__ void __launch_bounds__(kBlock) bn_bwd_reduce_kernel(const T* __restrict__ pre, const T* __restrict__ dy,
+                                                               long rows, int C, long rpb,
+                                                               const float* __restrict__ mean,
+                                                               const float* __restrict__ inv_std,
+                                                               const float* __restrict__ gamma,
+                                                               const float* __restrict__ beta, int act,
+                                                               float* __restrict__ part) {
+  __shared__ float s_a[kBlock * EC], s_b[kBlock * EC];
+  const Lane l = lane_of(rows, C, EC, rpb);
+  for (int gb = 0; gb < l.cg; gb += l.tpr) {
+    const int g = gb + l.g0;
+    const bool active = g < l.cg && l.rl < l.rpp;
+    float a[EC], b[EC];
+#pragma unroll
+    for (int e = 0; e < EC; ++e) a[e] = b[e] = 0.f;
+    if (active) {
+      float mu[EC], is[EC], ga[EC], be[EC];
+#pragma unroll
+      for (int e = 0; e < EC; ++e) {
+        const int c = g * EC + e;
+        mu[e] = mean[c];
+        is[e] = inv_std[c];
+        ga[e] = gamma[c];
+        be[e] = beta[c];
+      }
+      for (long r = l.r0 + l.rl; r < l.r1; r += l.rpp) {
+        float v[EC], d[EC];
+        load_v<EC>(pre + r * C + g * EC, v);
+        load_v<EC>(dy + r * C + g * EC, d);
+#pragma unroll
+        for (int e = 0; e < EC; ++e) {
+          const float z = (v[e] - mu[e]) * is[e];
+          const float dn = dact_f(act, fmaf(ga[e], z, be[e])) * d[e];
+          a[e] += dn;
+          b[e] = fmaf(dn, z, b[e]);
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EC; ++e) {
+      s_a[threadIdx.x * EC + e] = a[e];
+      s_b[threadIdx.x * EC + e] = b[e];
+    }
+    __syncthreads();
+    if (active && l.rl == 0) {
+      for (int e = 0; e < EC; ++e) {
+        float sa = 0.f, sb = 0.f;
+        for (int k = 0; k < l.rpp; ++k) {
+          sa += s_a[(k * l.tpr + l.g0) * EC + e];
+          sb += s_b[(k * l.tpr + l.g0) * EC + e];
+        }
+        float* o = part + (static_cast<size_t>(blockIdx.x) * C + g * EC + e) * 2;
+        o[0] = sa;
+        o[1] = sb;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// d_conv = gamma*inv_std*(d_norm - c1/n - z*c2/n); part[b][c] = sum d_conv.
+// MODE 0: batch norm; MODE 1: no norm (d_conv = act'(pre) * dy).
+template <typename T, int EC, int MODE>
+__global__ void __launch_bounds__(kBlock) dconv_kernel(const T* __restrict__ pre, const T* __restrict__ dy,
+                                                       long rows, int C, int Cp, long rpb,
+                                                       const float* __restrict__ mean,
+                                                       const float* __restrict__ inv_std,
+                                                       const float* __restrict__ gamma,
+                                                       const float* __restrict__ beta, int act,
+                                                       const float* __restrict__ c12, T* __restrict__ dconv,
+                                                       float* __restrict__ part) {
+  __shared__ float s_a[kBlock * EC];
+  // the walk covers Cp channels so that padded channels of d_conv get zeros
+  const Lane l = lane_of(rows, Cp, EC, rpb);
+  const float inv_n = 1.f / static_cast<float>(rows);
+  for (int gb = 0; gb < l.cg; gb += l.tpr) {
+    const int g = gb + l.g0;
+    const bool active = g < l.cg && l.rl < l.rpp;
+    const bool real = g * EC < C;  // EC divides C whenever EC > 1
+    float a[EC];
+#pragma unroll
+    for (int e = 0; e < EC; ++e) a[e] = 0.f;
+    if (active) {
+      float mu[EC], is[EC], ga[EC], be[EC], k1[EC], k2[EC];
+#pragma unroll
+      for (int e = 0; e < EC; ++e) {
+        const int c = real ? g * EC + e : 0;
+        if (MODE == 0) {
+          mu[e] = mean[c];
+          is[e] = inv_std[c];
+          ga[e] = gamma[c];
+          be[e] = beta[c];
+          k1[e] = c12[2 * c] * inv_n;
+          k2[e] = c12[2 * c + 1] * inv_n;
+        }
+      }
+      for (long r = l.r0 + l.rl; r < l.r1; r += l.rpp) {
+        float o[EC];
+        if (real) {
+          float v[EC], d[EC];
+          load_v<EC>(pre + r * C + g * EC, v);
+          load_v<EC>(dy + r * C + g * EC, d);
+#pragma unroll
+          for (int e = 0; e < EC; ++e) {
+            if (MODE == 0) {
+              const float z = (v[e] - mu[e]) * is[e];
+              const float dn = dact_f(act, fmaf(ga[e], z, be[e])) * d[e];
+              o[e] = ga[e] * is[e] * (dn - k1[e] - z * k2[e]);
+            } else {
+              o[e] = dact_f(act, v[e]) * d[e];
+            }
+            a[e] += o[e];
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < EC; ++e) o[e] = 0.f;
+        }
+        store_v<EC>(dconv + r * Cp + g * EC, o);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EC; ++e) s_a[threadIdx.x * EC + e] = a[e];
+    __syncthreads();
+    if (active && real && l.rl == 0) {
+      for (int e = 0; e < EC; ++e) {
+        float sa = 0.f;
+        for (int k = 0; k < l.rpp; ++k) sa += s_a[(k * l.tpr + l.g0) * EC + e];
+        part[static_cast<size_t>(blockIdx.x) * C + g * EC + e] = sa;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(128) sum_finalize_kernel(const float* __restrict__ part, int G, int C, int nv,
+                                                           int mode, float* c12, float* acc0, float* acc1) {
+  __shared__ double s[2][128];
+  const int c = blockIdx.x;
+  double a = 0, b = 0;
+  for (int k = threadIdx.x; k < G; k += 128) {
+    const float* p = part + (static_cast<size_t>(k) * C + c) * nv;
+    a += p[0];
+    if (nv > 1) b += p[1];
+  }
+  s[0][threadIdx.x] = a;
+  s[1][threadIdx.x] = b;
+  __syncthreads();
+  for (int off = 64; off > 0; off >>= 1) {
+    if (threadIdx.x < off) {
+      s[0][threadIdx.x] += s[0][threadIdx.x + off];
+      s[1][threadIdx.x] += s[1][threadIdx.x + off];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    if (mode == 0) {
+      c12[2 * c] = static_cast<float>(s[0][0]);
+      c12[2 * c + 1] = static_cast<float>(s[1][0]);
+      if (acc0) acc0[c] += static_cast<float>(s[0][0]);  // dbeta
+      if (acc1) acc1[c] += static_cast<float>(s[1][0]);  // dgamma
+    } else {
+      if (acc0) acc0[c] += static_cast<float>(s[0][0]);  // dbias
+    }
+  }
+}
+
+// ------------------------------------------------------------ layout prep
+template <typename T>
+__global__ void pack_channels_kernel(const T* __restrict__ src, T* __restrict__ dst, long rows, int C, int Cp) {
+  const long total = rows * Cp;
+  for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const long r = i / Cp;
+    const int c = static_cast<int>(i - r * Cp);
+    dst[i] = c < C ? src[r * C + c] : T(0.f);
+  }
+}
+
+// B[oc][tap][icp] from W[oc][tap][ic]; fp32: tf32 hi / lo split.
+template <typename T>
+__global__ void prep_fprop_weights_kernel(const T* __restrict__ w, T* __restrict__ bhi, float* __restrict__ blo,
+                                          int OC, int taps, int IC, int ICp) {
+  const long total = static_cast<long>(OC) * taps * ICp;
+  for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const int ic = static_cast<int>(i % ICp);
+    const long ot = i / ICp;
+    const T v = ic < IC ? w[ot * IC + ic] : T(0.f);
+    if constexpr (sizeof(T) == 4) {
+      uint32_t hi, lo;
+      split_tf32(static_cast<float>(v), hi, lo);
+      reinterpret_cast<uint32_t*>(bhi)[i] = hi;
+      reinterpret_cast<uint32_t*>(blo)[i] = lo;
+    } else {
+      bhi[i] = v;
+    }
+  }
+}
+
+// dgrad weight matrix B[icp][col]; for phase ph the columns (t,u,oc) hold
+// W[oc][rh + S*t][rw + S*u][ic].
+template <typename T>
+__global__ void prep_dgrad_weights_kernel(const T* __restrict__ w, T* __restrict__ bhi, float* __restrict__ blo,
+                                          int OC, int KH, int KW, int IC, int ICp, int OCp, int S, int Kd,
+                                          const DgradWeightTable t) {
+  const long total = static_cast<long>(ICp) * Kd;
+  for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const int ic = static_cast<int>(i / Kd);
+    const int col = static_cast<int>(i - static_cast<long>(ic) * Kd);
+    int ph = 0;
+    while (ph + 1 < t.n && t.col_off[ph + 1] <= col) ++ph;
+    const int local = col - t.col_off[ph];
+    const int oc = local % OCp;
+    const int tap = local / OCp;
+    const int tt = tap / t.Tw[ph], uu = tap % t.Tw[ph];
+    const int kh = t.rh[ph] + S * tt, kw = t.rw[ph] + S * uu;
+    T v = T(0.f);
+    if (ic < IC && oc < OC && tt < t.Th[ph] && kh < KH && kw < KW)
+      v = w[((static_cast<long>(oc) * KH + kh) * KW + kw) * IC + ic];
+    if constexpr (sizeof(T) == 4) {
+      uint32_t hi, lo;
+      split_tf32(static_cast<float>(v), hi, lo);
+      reinterpret_cast<uint32_t*>(bhi)[i] = hi;
+      reinterpret_cast<uint32_t*>(blo)[i] = lo;
+    } else {
+      bhi[i] = v;
+    }
+  }
+}
+
+// dW[oc][tap][ic] += sum over splits of partial[s][oc][tap*ICp + ic].
+__global__ void wgrad_reduce_kernel(const float* __restrict__ partial, int splits, int OC, int taps, int ICp, int IC,
+                                    float* __restrict__ dw) {
+  const long total = static_cast<long>(OC) * taps * IC;
+  const long Mk = static_cast<long>(taps) * ICp;
+  for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const int ic = static_cast<int>(i % IC);
+    const long ot = i / IC;
+    const int tap = static_cast<int>(ot % taps);
+    const int oc = static_cast<int>(ot / taps);
+    const long m = static_cast<long>(tap) * ICp + ic;
+    double s = 0;
+    for (int k = 0; k < splits; ++k) s += partial[(static_cast<long>(k) * OC + oc) * Mk + m];
+    dw[i] += static_cast<float>(s);
+  }
+}
+
+// Inference epilogue constants: v = acc*scale + shift folds bias and the
+// running-statistics normalisation (`evaluate`, BN branch).
+__global__ void infer_fold_kernel(const float* bias, const float* gamma, const float* beta, const float* rm,
+                                  const float* rv, float eps, int norm, int OC, float* scale, float* shift) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= OC) return;
+  const float b = bias ? bias[c] : 0.f;
+  if (norm == 1) {
+    const float is = static_cast<float>(1.0 / sqrt(static_cast<double>(rv[c]) + eps));
+    const float sc = gamma[c] * is;
+    scale[c] = sc;
+    shift[c] = fmaf(b - rm[c], sc, beta[c]);
+  } else {
+    scale[c] = 1.f;
+    shift[c] = b;
+  }
+}
+
+int grid_for(long total, int block) {
+  long g = (total + block - 1) / block;
+  if (g < 1) g = 1;
+  if (g > 65535L * 16) g = 65535L * 16;
+  return static_cast<int>(g);
+}
+
+int vec_ec(int dtype, int C) {
+  const int ec = dtype == 1 ? 8 : 4;
+  return (C % ec == 0) ? ec : 1;
+}
+
+}  // namespace
+
+RowWalk make_walk(long rows, int C, int dtype, int sms) {
+  RowWalk w;
+  w.rows = rows;
+  w.C = C;
+  const int ec = vec_ec(dtype, C);
+  const int cg = C / ec;
+  const int tpr = cg < kBlock ? cg : kBlock;
+  const int rpp = kBlock / tpr;
+  long g = (rows + rpp - 1) / rpp;
+  const long gmax = 8L * sms;
+  if (g > gmax) g = gmax;
+  if (g < 1) g = 1;
+  w.G = static_cast<int>(g);
+  w.rows_per_block = (rows + w.G - 1) / w.G;
+  return w;
+}
+
+#define DISPATCH_EC(dtype, C, FP32_CALL, BF16_CALL)                           \
+  do {                                                                        \
+    if ((dtype) == 1) {                                                       \
+      if ((C) % 8 == 0) { constexpr int EC = 8; using T = __nv_bfloat16; BF16_CALL; } \
+      else { constexpr int EC = 1; using T = __nv_bfloat16; BF16_CALL; }      \
+    } else {                                                                  \
+      if ((C) % 4 == 0) { constexpr int EC = 4; using T = float; FP32_CALL; } \
+      else { constexpr int EC = 1; using T = float; FP32_CALL; }              \
+    }                                                                         \
+  } while (0)
+
+cudaError_t launch_pack_channels(int dtype, const void* src, void* dst, long rows, int C, int Cp, cudaStream_t st) {
+  const int g = grid_for(rows * Cp, 256);
+  if (dtype == 1)
+    pack_channels_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src),
+                                                           static_cast<__nv_bfloat16*>(dst), rows, C, Cp);
+  else
+    pack_channels_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(src), static_cast<float*>(dst), rows,
+                                                   C, Cp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep_fprop_weights(int dtype, const void* w, void* bhi, float* blo, int OC, int taps, int IC,
+                                      int ICp, cudaStream_t st) {
+  const int g = grid_for(static_cast<long>(OC) * taps * ICp, 256);
+  if (dtype == 1)
+    prep_fprop_weights_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w),
+                                                                static_cast<__nv_bfloat16*>(bhi), nullptr, OC, taps,
+                                                                IC, ICp);
+  else
+    prep_fprop_weights_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(w), static_cast<float*>(bhi), blo,
+                                                        OC, taps, IC, ICp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep_dgrad_weights(int dtype, const void* w, void* bhi, float* blo, int OC, int KH, int KW,
+                                      int IC, int ICp, int OCp, int S, int Kd, const DgradWeightTable& t,
+                                      cudaStream_t st) {
+  const int g = grid_for(static_cast<long>(ICp) * Kd, 256);
+  if (dtype == 1)
+    prep_dgrad_weights_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w),
+                                                                static_cast<__nv_bfloat16*>(bhi), nullptr, OC, KH, KW,
+                                                                IC, ICp, OCp, S, Kd, t);
+  else
+    prep_dgrad_weights_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(w), static_cast<float*>(bhi), blo,
+                                                        OC, KH, KW, IC, ICp, OCp, S, Kd, t);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bn_stats(int dtype, const void* pre, const RowWalk& wk, float* part, cudaStream_t st) {
+  DISPATCH_EC(dtype, wk.C,
+              (bn_stats_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), wk.rows, wk.C,
+                                                                 wk.rows_per_block, part)),
+              (bn_stats_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), wk.rows, wk.C,
+                                                                 wk.rows_per_block, part)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float eps, float momentum, float* mean,
+                                     float* inv_std, float* rm, float* rv, cudaStream_t st) {
+  bn_stats_finalize_kernel<<<wk.C, 128, 0, st>>>(part, wk.G, wk.C, eps, momentum, mean, inv_std, rm, rv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bn_apply(int dtype, const void* pre, void* y, const RowWalk& wk, const float* mean,
+                            const float* inv_std, const float* gamma, const float* beta, int act, cudaStream_t st) {
+  DISPATCH_EC(dtype, wk.C,
+              (bn_apply_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), static_cast<T*>(y),
+                                                                 wk.rows, wk.C, wk.rows_per_block, mean, inv_std,
+                                                                 gamma, beta, act)),
+              (bn_apply_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), static_cast<T*>(y),
+                                                                 wk.rows, wk.C, wk.rows_per_block, mean, inv_std,
+                                                                 gamma, beta, act)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, const RowWalk& wk, const float* mean,
+                                 const float* inv_std, const float* gamma, const float* beta, int act, float* part,
+                                 cudaStream_t st) {
+  DISPATCH_EC(dtype, wk.C,
+              (bn_bwd_reduce_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
+                                                                      static_cast<const T*>(dy), wk.rows, wk.C,
+                                                                      wk.rows_per_block, mean, inv_std, gamma, beta,
+                                                                      act, part)),
+              (bn_bwd_reduce_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
+                                                                      static_cast<const T*>(dy), wk.rows, wk.C,
+                                                                      wk.rows_per_block, mean, inv_std, gamma, beta,
+                                                                      act, part)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sum_finalize(const float* part, const RowWalk& wk, int nv, int mode, float* c12, float* acc0,
+                                float* acc1, cudaStream_t st) {
+  sum_finalize_kernel<<<wk.C, 128, 0, st>>>(part, wk.G, wk.C, nv, mode, c12, acc0, acc1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bn_bwd_apply(int dtype, const void* pre, const void* dy, const RowWalk& wk, int Cp,
+                                const float* mean, const float* inv_std, const float* gamma, const float* beta,
+                                int act, const float* c12, void* dconv, float* part, cudaStream_t st) {
+  // the vector path needs C == Cp (EC divides C); otherwise one channel per thread
+  DISPATCH_EC(dtype, (wk.C == Cp ? wk.C : 1),
+              (dconv_kernel<T, EC, 0><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
+                                                                 static_cast<const T*>(dy), wk.rows, wk.C, Cp,
+                                                                 wk.rows_per_block, mean, inv_std, gamma, beta, act,
+                                                                 c12, static_cast<T*>(dconv), part)),
+              (dconv_kernel<T, EC, 0><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
+                                                                 static_cast<const T*>(dy), wk.rows, wk.C, Cp,
+                                                                 wk.rows_per_block, mean, inv_std, gamma, beta, act,
+                                                                 c12, static_cast<T*>(dconv), part)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_act_bwd(int dtype, const void* pre, const void* dy, const RowWalk& wk, int Cp, int act,
+                           void* dconv, float* part, cudaStream_t st) {
+  DISPATCH_EC(dtype, (wk.C == Cp ? wk.C : 1),
+              (dconv_kernel<T, EC, 1><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
+                                                                 static_cast<const T*>(dy), wk.rows, wk.C, Cp,
+                                                                 wk.rows_per_block, nullptr, nullptr, nullptr,
+                                                                 nullptr, act, nullptr, static_cast<T*>(dconv),
+                                                                 part)),
+              (dconv_kernel<T, EC, 1><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
+                                                                 static_cast<const T*>(dy), wk.rows, wk.C, Cp,
+                                                                 wk.rows_per_block, nullptr, nullptr, nullptr,
+                                                                 nullptr, act, nullptr, static_cast<T*>(dconv),
+                                                                 part)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int taps, int ICp, int IC, float* dw,
+                                cudaStream_t st) {
+  const int g = grid_for(static_cast<long>(OC) * taps * IC, 256);
+  wgrad_reduce_kernel<<<g, 256, 0, st>>>(partial, splits, OC, taps, ICp, IC, dw);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_infer_fold(const float* bias, const float* gamma, const float* beta, const float* rm,
+                              const float* rv, float eps, int norm, int OC, float* scale, float* shift,
+                              cudaStream_t st) {
+  infer_fold_kernel<<<(OC + 127) / 128, 128, 0, st>>>(bias, gamma, beta, rm, rv, eps, norm, OC, scale, shift);
+  return cudaGetLastError();
+}
+
+}  // namespace c2d

@@ -1,0 +1,746 @@
+// conv_gemm.cuh - implicit-GEMM convolution kernels on the 5th-generation
+// tensor cores (tcgen05, accumulators in TMEM).
+//
+// The three contractions of the conv2d training step (rl-tools
+// "operations_generic.h", `forward` Phase 1 and the two scatter updates of
+// `backward_full`) are run as GEMMs without materialising im2col:
+//   fprop  D[pix][oc]  = sum_k A[pix][k] B[oc][k],  k = (kh,kw,ic),
+//          A gathered from X, B = W [OC][KH*KW*IC]
+//   dgrad  D[ipix][ic] = sum_k A[ipix][k] B[ic][k], k = (tap,oc) of one
+//          stride phase, A gathered from d_conv, B = phase-packed W^T
+//   wgrad  D[k][oc]    = sum_pix A[k][pix] B[oc][pix] over a split of the
+//          pixels; fp32 partials per split, reduced afterwards.
+//
+// One persistent CTA per SM (grid = #SMs), 10 warps:
+//   warp 0      TMA producer of the B operand (one elected lane)
+//   warp 1      TMEM allocator and MMA issuer (one elected lane)
+//   warps 2-5   A-operand producers: gather 128-byte rows of NHWC data into
+//               128B-swizzled shared memory (cp.async for bf16; load, tf32
+//               split and store for fp32)
+//   warps 6-9   epilogue: TMEM -> registers -> bias / scale / activation ->
+//               global memory
+// A ring of `stages` shared-memory stages (full/empty mbarriers) feeds the
+// MMA warp; two TMEM accumulators (tfull/tempty mbarriers) let the epilogue
+// of one tile overlap the main loop of the next.
+//
+// Precision: BF16 operands accumulate in fp32. FP32 operands run 3xTF32:
+// x = hi + lo (both tf32), acc += lo*hi + hi*lo + hi*hi.
+#pragma once
+#include "ptx.cuh"
+
+namespace c2d {
+
+constexpr int kThreads = 320;
+constexpr int kMaxStages = 8;
+constexpr int kMaxPhases = 64;
+constexpr int kBM = 128;          // rows of a tile (TMEM lanes)
+constexpr int kLag = 2;           // cp.async groups kept in flight per producer thread
+
+// wait sites recorded in the error word
+enum : int { kSiteFull = 1, kSiteEmpty = 2, kSiteTFull = 3, kSiteTEmpty = 4 };
+
+template <int DT>
+struct Dt;
+template <>
+struct Dt<1> {  // bf16
+  using T = __nv_bfloat16;
+  static constexpr int ES = 2, EC = 8, BKE = 64, UK = 16, NS = 1;
+  static constexpr uint32_t FMT = 1;
+};
+template <>
+struct Dt<0> {  // fp32 storage, 3xTF32 arithmetic
+  using T = float;
+  static constexpr int ES = 4, EC = 4, BKE = 32, UK = 8, NS = 2;
+  static constexpr uint32_t FMT = 2;
+};
+
+// One stride phase of the row domain. fprop has a single phase; dgrad with
+// stride S has S*S phases (input pixels with the same (ih+P) mod S,
+// (iw+P) mod S see the same subset of kernel taps).
+struct ConvPhase {
+  int rows;            // rows of D in this phase: Nimg*Ha*Wa
+  int Ha, Wa;          // per-image row grid
+  int qh, qw;          // source base: hb = a*rs + qh, wb = b*rs + qw
+  int Tw;              // taps along w in this phase
+  int K;               // reduction length: taps * Cs
+  int num_kb;          // ceil(K / BKE)
+  int unit_begin;      // first work unit of this phase
+  int b_col;           // first column of this phase in the B matrix
+  int oh0, ow0;        // output pixel = (oh0 + a*os, ow0 + b*os)
+  FastDiv div_Wa, div_HaWa, div_Tw;
+};
+
+struct ConvGemmParams {
+  CUtensorMap tmap_b;     // B [Nrows][Kcols] K-major (bf16, or tf32 hi)
+  CUtensorMap tmap_b_lo;  // tf32 lo (fp32 mode only)
+  const void* src;        // A source, NHWC [Nimg][Hs][Ws][Cs]
+  int Hs, Ws, Cs;
+  int rs, tap_sign;       // fprop: rs = stride, taps add; dgrad: rs = 1, taps subtract
+  FastDiv div_Cs;
+  int num_phases;
+  int n_tiles, BN, N;     // N = valid output columns
+  int num_units;
+  void* out;              // dtype, [pixels][out_ld]
+  void* out2;             // optional second output act(v)
+  int out_ld, Ho, Wo, os;
+  const float* ep_scale;  // optional per-column scale
+  const float* ep_shift;  // optional per-column shift
+  int act, out_act;       // out = out_act ? act(v) : v
+  int stages;
+  int* err;
+  ConvPhase ph[kMaxPhases];
+};
+
+struct WgradParams {
+  CUtensorMap tmap_dc;    // bf16 d_conv [n_pix][OCp], box {64 ch, 64 pix}
+  const void* x;          // NHWC [Nimg][H][W][Cs]
+  const float* dc32;      // fp32 d_conv [n_pix][OCp] (fp32 mode)
+  int H, W, Cs, OH, OW, S, P, KW;
+  FastDiv div_Cs, div_KW, div_OW, div_OHOW;
+  int Mk;                 // rows of D: KH*KW*Cs
+  int m_tiles, n_tiles, BN, N, OCp;
+  int n_pix, kb_total, kb_per_split, splits;
+  int num_units;
+  float* partial;         // [splits][N][Mk]
+  int stages;
+  int* err;
+};
+
+__host__ __device__ inline uint32_t tmem_cols_for(int cols) {
+  uint32_t c = 32;
+  while (c < static_cast<uint32_t>(cols)) c <<= 1;
+  return c;
+}
+
+__device__ __forceinline__ const ConvPhase& find_phase(const ConvGemmParams& p, int u) {
+  int i = 0;
+  while (i + 1 < p.num_phases && p.ph[i + 1].unit_begin <= u) ++i;
+  return p.ph[i];
+}
+
+template <typename T>
+__device__ __forceinline__ void store_row16(T* dst, const float* v, int ncols, bool vec);
+
+template <>
+__device__ __forceinline__ void store_row16<__nv_bfloat16>(__nv_bfloat16* dst, const float* v, int ncols, bool vec) {
+  if (vec && ncols >= 16) {
+    uint32_t w[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+      w[e] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if (e < ncols) dst[e] = __float2bfloat16_rn(v[e]);
+  }
+}
+template <>
+__device__ __forceinline__ void store_row16<float>(float* dst, const float* v, int ncols, bool vec) {
+  if (vec && ncols >= 16) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      reinterpret_cast<float4*>(dst)[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if (e < ncols) dst[e] = v[e];
+  }
+}
+
+// --------------------------------------------------------------------------
+// fprop / dgrad
+// --------------------------------------------------------------------------
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_constant__ ConvGemmParams p) {
+  using D = Dt<DT>;
+  using T = typename D::T;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int BN = p.BN;
+  const uint32_t a_bytes = kBM * 128, b_bytes = BN * 128;
+  const uint32_t stage_bytes = D::NS * (a_bytes + b_bytes);
+  const int S = p.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_bytes);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* tfull = empty + kMaxStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t tcols = tmem_cols_for(2 * BN);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 128 + 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    fence_mbar_init();
+    tma_prefetch_desc(&p.tmap_b);
+    if (D::NS == 2) tma_prefetch_desc(&p.tmap_b_lo);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, tcols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ B producer (TMA)
+    if (lane == 0) {
+      int s = 0;
+      uint32_t par = 0;
+      bool alive = true;
+      for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
+        const ConvPhase& ph = find_phase(p, u);
+        const int n_tile = (u - ph.unit_begin) % p.n_tiles;
+        for (int kb = 0; kb < ph.num_kb; ++kb) {
+          if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
+            alive = false;
+            break;
+          }
+          const uint32_t b0 = sbase + s * stage_bytes + D::NS * a_bytes;
+          mbar_arrive_expect_tx(&full[s], D::NS * b_bytes);
+          tma_load_2d(b0, &p.tmap_b, &full[s], ph.b_col + kb * D::BKE, n_tile * BN);
+          if (D::NS == 2) tma_load_2d(b0 + b_bytes, &p.tmap_b_lo, &full[s], ph.b_col + kb * D::BKE, n_tile * BN);
+          if (++s == S) {
+            s = 0;
+            par ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f32acc(kBM, BN, D::FMT, false, false);
+      int s = 0;
+      uint32_t par = 0;
+      int tc = 0;
+      bool alive = true;
+      for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x, ++tc) {
+        const ConvPhase& ph = find_phase(p, u);
+        const int buf = tc & 1;
+        if (!wait(&tempty[buf], ((tc >> 1) & 1) ^ 1, p.err, kSiteTEmpty)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * BN;
+        for (int kb = 0; kb < ph.num_kb; ++kb) {
+          if (!wait(&full[s], par, p.err, kSiteFull)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = sbase + s * stage_bytes;
+          const uint32_t b0 = a0 + D::NS * a_bytes;
+#pragma unroll
+          for (int kk = 0; kk < 128 / 32; ++kk) {
+            const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
+            const uint32_t acc = (kb | kk) ? 1u : 0u;
+            if (DT == 1) {
+              mma_bf16(d, ad, bd, idesc, acc);
+            } else {
+              const uint64_t al = sdesc_sw128(a0 + a_bytes + kk * 32, 16, 1024);
+              const uint64_t bl = sdesc_sw128(b0 + b_bytes + kk * 32, 16, 1024);
+              mma_tf32(d, al, bd, idesc, acc);
+              mma_tf32(d, ad, bl, idesc, 1u);
+              mma_tf32(d, ad, bd, idesc, 1u);
+            }
+          }
+          mma_commit(&empty[s]);
+          if (++s == S) {
+            s = 0;
+            par ^= 1;
+          }
+        }
+        if (alive) mma_commit(&tfull[buf]);
+      }
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------ A producers (gather)
+    const int t = threadIdx.x - 64;
+    const int j = t & 7;       // 16-byte chunk within the 128-byte row
+    const int r0 = t >> 3;     // rows r0 + 16*i
+    const uint32_t swz = static_cast<uint32_t>((j ^ (r0 & 7)) << 4);
+    const char* src = static_cast<const char*>(p.src);
+    int s = 0;
+    uint32_t par = 0;
+    int it = 0;
+    bool alive = true;
+    for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
+      const ConvPhase& ph = find_phase(p, u);
+      const int m_tile = (u - ph.unit_begin) / p.n_tiles;
+      int hb[8], wb[8], pb[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int m = m_tile * kBM + r0 + 16 * i;
+        if (m < ph.rows) {
+          const int n = static_cast<int>(fdiv(static_cast<uint32_t>(m), ph.div_HaWa));
+          const int rem = m - n * ph.Ha * ph.Wa;
+          const int a = static_cast<int>(fdiv(static_cast<uint32_t>(rem), ph.div_Wa));
+          const int b = rem - a * ph.Wa;
+          hb[i] = a * p.rs + ph.qh;
+          wb[i] = b * p.rs + ph.qw;
+          pb[i] = n * p.Hs * p.Ws;
+        } else {
+          hb[i] = -(1 << 28);  // never in bounds
+          wb[i] = 0;
+          pb[i] = 0;
+        }
+      }
+      for (int kb = 0; kb < ph.num_kb; ++kb) {
+        const int k0 = kb * D::BKE + j * D::EC;
+        const bool okc = k0 < ph.K;
+        const int tap = static_cast<int>(fdiv(static_cast<uint32_t>(k0), p.div_Cs));
+        const int c = k0 - tap * p.Cs;
+        const int tt = static_cast<int>(fdiv(static_cast<uint32_t>(tap), ph.div_Tw));
+        const int dh = p.tap_sign * tt;
+        const int dw = p.tap_sign * (tap - tt * ph.Tw);
+        if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
+          alive = false;
+          break;
+        }
+        const uint32_t a0 = sbase + s * stage_bytes;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int ih = hb[i] + dh, iw = wb[i] + dw;
+          const bool ok = okc && static_cast<unsigned>(ih) < static_cast<unsigned>(p.Hs) &&
+                          static_cast<unsigned>(iw) < static_cast<unsigned>(p.Ws);
+          const size_t off = ok ? (static_cast<size_t>(pb[i] + ih * p.Ws + iw) * p.Cs + c) * D::ES : 0;
+          const uint32_t dst = a0 + (r0 + 16 * i) * 128 + swz;
+          if (DT == 1) {
+            cp_async16(dst, src + off, ok ? 16u : 0u);
+          } else {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (ok) v = __ldg(reinterpret_cast<const float4*>(src + off));
+            uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+            split_tf32(v.x, h0, l0);
+            split_tf32(v.y, h1, l1);
+            split_tf32(v.z, h2, l2);
+            split_tf32(v.w, h3, l3);
+            st_shared_v4(dst, h0, h1, h2, h3);
+            st_shared_v4(dst + a_bytes, l0, l1, l2, l3);
+          }
+        }
+        if (DT == 1) {
+          cp_async_commit();
+          if (it >= kLag) {
+            cp_async_wait<kLag>();
+            fence_proxy_async_smem();
+            mbar_arrive(&full[(it - kLag) % S]);
+          }
+        } else {
+          fence_proxy_async_smem();
+          mbar_arrive(&full[s]);
+        }
+        ++it;
+        if (++s == S) {
+          s = 0;
+          par ^= 1;
+        }
+      }
+    }
+    if (DT == 1) {
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      if (alive)
+        for (int q = (it > kLag ? it - kLag : 0); q < it; ++q) mbar_arrive(&full[q % S]);
+    }
+  } else {
+    // ------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    T* out = static_cast<T*>(p.out);
+    T* out2 = static_cast<T*>(p.out2);
+    const bool vec = (p.out_ld % D::EC) == 0;
+    int tc = 0;
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tc) {
+      const ConvPhase& ph = find_phase(p, u);
+      const int local = u - ph.unit_begin;
+      const int m_tile = local / p.n_tiles, n_tile = local % p.n_tiles;
+      const int buf = tc & 1;
+      // lane 0 waits, the warp follows: the tcgen05.ld below is warp-aligned, so
+      // control flow must stay uniform even when the wait gives up
+      int ok = 1;
+      if (lane == 0) ok = wait(&tfull[buf], (tc >> 1) & 1, p.err, kSiteTFull) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      tc_fence_after();
+      const int m = m_tile * kBM + row;
+      const bool valid = m < ph.rows;
+      size_t obase = 0;
+      if (valid) {
+        const int n = static_cast<int>(fdiv(static_cast<uint32_t>(m), ph.div_HaWa));
+        const int rem = m - n * ph.Ha * ph.Wa;
+        const int a = static_cast<int>(fdiv(static_cast<uint32_t>(rem), ph.div_Wa));
+        const int b = rem - a * ph.Wa;
+        const int oh = ph.oh0 + a * p.os, ow = ph.ow0 + b * p.os;
+        obase = (static_cast<size_t>(n * p.Ho + oh) * p.Wo + ow) * p.out_ld;
+      }
+      const bool zero = ph.num_kb == 0;
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c0, r);
+        tmem_ld_wait(r);
+        const int col0 = n_tile * BN + c0;
+        const int ncols = p.N - col0;
+        if (!valid || ncols <= 0) continue;
+        float v[16], w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int col = col0 + e;
+          float x = zero ? 0.f : __uint_as_float(r[e]);
+          if (col < p.N) {
+            if (p.ep_scale) x *= __ldg(p.ep_scale + col);
+            if (p.ep_shift) x += __ldg(p.ep_shift + col);
+          }
+          v[e] = p.out_act ? act_f(p.act, x) : x;
+          w[e] = act_f(p.act, x);
+        }
+        store_row16<T>(out + obase + col0, v, ncols, vec);
+        if (out2) store_row16<T>(out2 + obase + col0, w, ncols, vec);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tcols);
+  }
+}
+
+// --------------------------------------------------------------------------
+// wgrad: D[k][oc] = sum over a split of the pixels of im2col(X)[pix][k] *
+// d_conv[pix][oc]; written as fp32 partials [split][oc][k].
+// --------------------------------------------------------------------------
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_constant__ WgradParams p) {
+  using D = Dt<DT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int BN = p.BN;
+  const uint32_t a_bytes = kBM * 128, b_bytes = BN * 128;
+  const uint32_t stage_bytes = D::NS * (a_bytes + b_bytes);
+  const int S = p.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_bytes);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* tfull = empty + kMaxStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t tcols = tmem_cols_for(2 * BN);
+  constexpr int KP = (DT == 1) ? 64 : 32;  // pixels per k-block
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], DT == 1 ? 128 + 1 : 128);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    fence_mbar_init();
+    if (DT == 1) tma_prefetch_desc(&p.tmap_dc);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, tcols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto decode = [&](int u, int& m_tile, int& n_tile, int& kb0, int& kb1) {
+    m_tile = u % p.m_tiles;
+    const int rest = u / p.m_tiles;
+    n_tile = rest % p.n_tiles;
+    const int split = rest / p.n_tiles;
+    kb0 = split * p.kb_per_split;
+    kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------ B producer (bf16: TMA of d_conv)
+    if (DT == 1 && lane == 0) {
+      int s = 0;
+      uint32_t par = 0;
+      bool alive = true;
+      for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
+        int m_tile, n_tile, kb0, kb1;
+        decode(u, m_tile, n_tile, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
+            alive = false;
+            break;
+          }
+          const uint32_t b0 = sbase + s * stage_bytes + a_bytes;
+          mbar_arrive_expect_tx(&full[s], b_bytes);
+          for (int jn = 0; jn < BN / 64; ++jn)
+            tma_load_2d(b0 + jn * 8192, &p.tmap_dc, &full[s], n_tile * BN + 64 * jn, kb * KP);
+          if (++s == S) {
+            s = 0;
+            par ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f32acc(kBM, BN, D::FMT, DT == 1, DT == 1);
+      int s = 0;
+      uint32_t par = 0;
+      int tc = 0;
+      bool alive = true;
+      for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x, ++tc) {
+        int m_tile, n_tile, kb0, kb1;
+        decode(u, m_tile, n_tile, kb0, kb1);
+        const int buf = tc & 1;
+        if (!wait(&tempty[buf], ((tc >> 1) & 1) ^ 1, p.err, kSiteTEmpty)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * BN;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait(&full[s], par, p.err, kSiteFull)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = sbase + s * stage_bytes;
+          const uint32_t b0 = a0 + D::NS * a_bytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc = (kb > kb0 || kk) ? 1u : 0u;
+            if (DT == 1) {
+              // MN-major: 16 pixel rows per MMA (2048 B), atoms of 64 k / 64 oc 8192 B apart
+              const uint64_t ad = sdesc_sw128(a0 + kk * 2048, 8192, 1024);
+              const uint64_t bd = sdesc_sw128(b0 + kk * 2048, 8192, 1024);
+              mma_bf16(d, ad, bd, idesc, acc);
+            } else {
+              const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
+              const uint64_t al = sdesc_sw128(a0 + a_bytes + kk * 32, 16, 1024);
+              const uint64_t bl = sdesc_sw128(b0 + b_bytes + kk * 32, 16, 1024);
+              mma_tf32(d, al, bd, idesc, acc);
+              mma_tf32(d, ad, bl, idesc, 1u);
+              mma_tf32(d, ad, bd, idesc, 1u);
+            }
+          }
+          mma_commit(&empty[s]);
+          if (++s == S) {
+            s = 0;
+            par ^= 1;
+          }
+        }
+        if (alive) mma_commit(&tfull[buf]);
+      }
+    }
+  } else if (warp < 6) {
+    const int t = threadIdx.x - 64;
+    const char* xs = static_cast<const char*>(p.x);
+    int s = 0;
+    uint32_t par = 0;
+    int it = 0;
+    bool alive = true;
+    if (DT == 1) {
+      // ------------------------------------------------ A producer, bf16, MN-major
+      // smem A: two panels (k 0-63, 64-127) of [64 pixel rows][128 B]
+      const int qc = t & 15, panel = qc >> 3, jj = qc & 7, r0 = t >> 4;
+      const uint32_t swz = static_cast<uint32_t>((jj ^ (r0 & 7)) << 4);
+      for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
+        int m_tile, n_tile, kb0, kb1;
+        decode(u, m_tile, n_tile, kb0, kb1);
+        const int kc = m_tile * kBM + qc * 8;
+        const bool okc = kc < p.Mk;
+        const int tap = static_cast<int>(fdiv(static_cast<uint32_t>(kc), p.div_Cs));
+        const int c = kc - tap * p.Cs;
+        const int kh = static_cast<int>(fdiv(static_cast<uint32_t>(tap), p.div_KW));
+        const int dh = kh - p.P, dw = (tap - kh * p.KW) - p.P;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
+            alive = false;
+            break;
+          }
+          const uint32_t a0 = sbase + s * stage_bytes + panel * 8192;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = r0 + 8 * i;
+            const int pix = kb * KP + r;
+            bool ok = okc && pix < p.n_pix;
+            size_t off = 0;
+            if (ok) {
+              const int n = static_cast<int>(fdiv(static_cast<uint32_t>(pix), p.div_OHOW));
+              const int rem = pix - n * p.OH * p.OW;
+              const int oh = static_cast<int>(fdiv(static_cast<uint32_t>(rem), p.div_OW));
+              const int ow = rem - oh * p.OW;
+              const int ih = oh * p.S + dh, iw = ow * p.S + dw;
+              ok = static_cast<unsigned>(ih) < static_cast<unsigned>(p.H) &&
+                   static_cast<unsigned>(iw) < static_cast<unsigned>(p.W);
+              if (ok) off = ((static_cast<size_t>(n * p.H + ih) * p.W + iw) * p.Cs + c) * 2;
+            }
+            cp_async16(a0 + r * 128 + swz, xs + off, ok ? 16u : 0u);
+          }
+          cp_async_commit();
+          if (it >= kLag) {
+            cp_async_wait<kLag>();
+            fence_proxy_async_smem();
+            mbar_arrive(&full[(it - kLag) % S]);
+          }
+          ++it;
+          if (++s == S) {
+            s = 0;
+            par ^= 1;
+          }
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      if (alive)
+        for (int q2 = (it > kLag ? it - kLag : 0); q2 < it; ++q2) mbar_arrive(&full[q2 % S]);
+    } else {
+      // ------------------------------------------------ A and B producers, fp32 -> tf32 hi/lo, K-major
+      // A smem rows: k (128), 32 pixel columns; B smem rows: oc (BN), 32 pixel columns.
+      const int pc = t & 31, g0 = t >> 5;
+      const uint32_t colsw = static_cast<uint32_t>(pc & 3) * 4;
+      for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
+        int m_tile, n_tile, kb0, kb1;
+        decode(u, m_tile, n_tile, kb0, kb1);
+        int dhs[8], dws[8], cs[8];
+        bool oks[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int kc = m_tile * kBM + 4 * (g0 + 4 * i);
+          oks[i] = kc < p.Mk;
+          const int tap = static_cast<int>(fdiv(static_cast<uint32_t>(kc), p.div_Cs));
+          cs[i] = kc - tap * p.Cs;
+          const int kh = static_cast<int>(fdiv(static_cast<uint32_t>(tap), p.div_KW));
+          dhs[i] = kh - p.P;
+          dws[i] = (tap - kh * p.KW) - p.P;
+        }
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const int pix = kb * KP + pc;
+          const bool okp = pix < p.n_pix;
+          int n = 0, oh = 0, ow = 0;
+          if (okp) {
+            n = static_cast<int>(fdiv(static_cast<uint32_t>(pix), p.div_OHOW));
+            const int rem = pix - n * p.OH * p.OW;
+            oh = static_cast<int>(fdiv(static_cast<uint32_t>(rem), p.div_OW));
+            ow = rem - oh * p.OW;
+          }
+          float4 av[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int ih = oh * p.S + dhs[i], iw = ow * p.S + dws[i];
+            const bool ok = okp && oks[i] && static_cast<unsigned>(ih) < static_cast<unsigned>(p.H) &&
+                            static_cast<unsigned>(iw) < static_cast<unsigned>(p.W);
+            av[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (ok)
+              av[i] = __ldg(reinterpret_cast<const float4*>(
+                  xs + ((static_cast<size_t>(n * p.H + ih) * p.W + iw) * p.Cs + cs[i]) * 4));
+          }
+          if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
+            alive = false;
+            break;
+          }
+          const uint32_t a0 = sbase + s * stage_bytes;
+          const uint32_t b0 = a0 + 2 * a_bytes;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rb = 4 * (g0 + 4 * i);
+            const float vv[4] = {av[i].x, av[i].y, av[i].z, av[i].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int rr = rb + e;
+              const uint32_t addr = a0 + rr * 128 + ((((pc >> 2) ^ (rr & 7)) << 4)) + colsw;
+              uint32_t hi, lo;
+              split_tf32(vv[e], hi, lo);
+              st_shared_b32(addr, hi);
+              st_shared_b32(addr + a_bytes, lo);
+            }
+          }
+          for (int gb = g0; gb < BN / 4; gb += 4) {
+            const int oc = n_tile * BN + 4 * gb;
+            float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (okp && oc < p.OCp)
+              bv = __ldg(reinterpret_cast<const float4*>(p.dc32 + static_cast<size_t>(pix) * p.OCp + oc));
+            const float vv[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int rr = 4 * gb + e;
+              const uint32_t addr = b0 + rr * 128 + ((((pc >> 2) ^ (rr & 7)) << 4)) + colsw;
+              uint32_t hi, lo;
+              split_tf32(vv[e], hi, lo);
+              st_shared_b32(addr, hi);
+              st_shared_b32(addr + b_bytes, lo);
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&full[s]);
+          if (++s == S) {
+            s = 0;
+            par ^= 1;
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue: partial[split][oc][k]
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    int tc = 0;
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tc) {
+      int m_tile, n_tile, kb0, kb1;
+      decode(u, m_tile, n_tile, kb0, kb1);
+      const int split = u / (p.m_tiles * p.n_tiles);
+      const int buf = tc & 1;
+      // lane 0 waits, the warp follows: the tcgen05.ld below is warp-aligned, so
+      // control flow must stay uniform even when the wait gives up
+      int ok = 1;
+      if (lane == 0) ok = wait(&tfull[buf], (tc >> 1) & 1, p.err, kSiteTFull) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      tc_fence_after();
+      const int m = m_tile * kBM + row;
+      const bool zero = kb1 <= kb0;
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c0, r);
+        tmem_ld_wait(r);
+        if (m >= p.Mk) continue;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int col = n_tile * BN + c0 + e;
+          if (col < p.N)
+            p.partial[(static_cast<size_t>(split) * p.N + col) * p.Mk + m] = zero ? 0.f : __uint_as_float(r[e]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tcols);
+  }
+}
+
+}  // namespace c2d

@@ -1,0 +1,62 @@
+// kernels.h - launchers shared between the library's translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+#include "conv_gemm.cuh"
+
+namespace c2d {
+
+// tcgen05 GEMMs (gemm_bf16.cu / gemm_tf32.cu)
+cudaError_t launch_conv_gemm_bf16(const ConvGemmParams& p, int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_conv_gemm_tf32(const ConvGemmParams& p, int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_wgrad_gemm_bf16(const WgradParams& p, int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_wgrad_gemm_tf32(const WgradParams& p, int grid, size_t smem, cudaStream_t st);
+
+// Per-phase description of the dgrad weight matrix (see prep_dgrad_weights).
+struct DgradWeightTable {
+  int n;
+  int col_off[kMaxPhases];
+  int Th[kMaxPhases], Tw[kMaxPhases], rh[kMaxPhases], rw[kMaxPhases];
+};
+
+// Row walk of an NHWC tensor seen as [rows][C]: G blocks, each owning a
+// contiguous slice of rows.
+struct RowWalk {
+  long rows;
+  int C;
+  int G;
+  long rows_per_block;
+};
+RowWalk make_walk(long rows, int C, int dtype, int sms);
+
+// elementwise / reduction kernels (bn_kernels.cu); dtype 0 = fp32, 1 = bf16
+cudaError_t launch_pack_channels(int dtype, const void* src, void* dst, long rows, int C, int Cp, cudaStream_t st);
+cudaError_t launch_prep_fprop_weights(int dtype, const void* w, void* bhi, float* blo, int OC, int taps, int IC,
+                                      int ICp, cudaStream_t st);
+cudaError_t launch_prep_dgrad_weights(int dtype, const void* w, void* bhi, float* blo, int OC, int KH, int KW,
+                                      int IC, int ICp, int OCp, int S, int Kd, const DgradWeightTable& t,
+                                      cudaStream_t st);
+cudaError_t launch_bn_stats(int dtype, const void* pre, const RowWalk& wk, float* part, cudaStream_t st);
+cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float eps, float momentum, float* mean,
+                                     float* inv_std, float* rm, float* rv, cudaStream_t st);
+cudaError_t launch_bn_apply(int dtype, const void* pre, void* y, const RowWalk& wk, const float* mean,
+                            const float* inv_std, const float* gamma, const float* beta, int act, cudaStream_t st);
+cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, const RowWalk& wk, const float* mean,
+                                 const float* inv_std, const float* gamma, const float* beta, int act, float* part,
+                                 cudaStream_t st);
+// sums[c][v] over the G block partials (v < nv); mode 0: c12 <- sums, dbeta += s0, dgamma += s1;
+// mode 1: dbias += s0.
+cudaError_t launch_sum_finalize(const float* part, const RowWalk& wk, int nv, int mode, float* c12, float* acc0,
+                                float* acc1, cudaStream_t st);
+cudaError_t launch_bn_bwd_apply(int dtype, const void* pre, const void* dy, const RowWalk& wk, int Cp,
+                                const float* mean, const float* inv_std, const float* gamma, const float* beta,
+                                int act, const float* c12, void* dconv, float* part, cudaStream_t st);
+cudaError_t launch_act_bwd(int dtype, const void* pre, const void* dy, const RowWalk& wk, int Cp, int act,
+                           void* dconv, float* part, cudaStream_t st);
+cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int taps, int ICp, int IC, float* dw,
+                                cudaStream_t st);
+cudaError_t launch_infer_fold(const float* bias, const float* gamma, const float* beta, const float* rm,
+                              const float* rv, float eps, int norm, int OC, float* scale, float* shift,
+                              cudaStream_t st);
+
+}  // namespace c2d

@@ -1,0 +1,72 @@
+"""Conv2dLayer: torch-owned device memory around the C ABI.
+
+PyTorch supplies device memory and the stream; every step of the layer runs
+in the library's kernels (through conv2d_layer_gb300.abi). The class holds
+the parameters, running statistics, saved forward state and a workspace sized
+by conv2d_workspace_size.
+"""
+import torch
+
+from . import abi
+
+_TORCH_DT = {abi.FP32: torch.float32, abi.BF16: torch.bfloat16}
+
+
+class Conv2dLayer:
+    def __init__(self, spec, w, b=None, gamma=None, beta=None, running_mean=None, running_var=None,
+                 device="cuda"):
+        self.spec = spec
+        self.desc = abi.desc(spec.N, spec.H, spec.W, spec.IC, spec.OC, spec.KH, spec.KW, spec.stride, spec.pad,
+                             spec.norm, spec.act, spec.dtype, spec.eps, spec.momentum)
+        abi.check(abi.conv2d_validate(self.desc), "conv2d_validate")
+        self.dt = _TORCH_DT[spec.dtype]
+        dev = torch.device(device)
+        f32 = dict(device=dev, dtype=torch.float32)
+        self.w = w.to(dev, self.dt).contiguous()
+        self.b = (b if b is not None else torch.zeros(spec.OC)).to(**f32).contiguous()
+        self.gamma = (gamma if gamma is not None else torch.ones(spec.OC)).to(**f32).contiguous()
+        self.beta = (beta if beta is not None else torch.zeros(spec.OC)).to(**f32).contiguous()
+        self.running_mean = (running_mean if running_mean is not None else torch.zeros(spec.OC)).to(**f32).clone()
+        self.running_var = (running_var if running_var is not None else torch.ones(spec.OC)).to(**f32).clone()
+        y_shape = (spec.N, spec.OH, spec.OW, spec.OC)
+        self.pre_act = torch.empty(y_shape, device=dev, dtype=self.dt)
+        self.y = torch.empty(y_shape, device=dev, dtype=self.dt)
+        self.save_mean = torch.zeros(spec.OC, **f32)
+        self.save_inv_std = torch.zeros(spec.OC, **f32)
+        self.dw = torch.zeros(spec.OC, spec.KH, spec.KW, spec.IC, **f32)
+        self.db = torch.zeros(spec.OC, **f32)
+        self.dgamma = torch.zeros(spec.OC, **f32)
+        self.dbeta = torch.zeros(spec.OC, **f32)
+        self.dx = torch.empty(spec.N, spec.H, spec.W, spec.IC, device=dev, dtype=self.dt)
+        ws = max(abi.conv2d_workspace_size(self.desc, op) for op in (0, 1, 2))
+        self.ws = torch.empty(max(ws, 256), device=dev, dtype=torch.uint8)
+
+    def zero_grad(self):
+        for t in (self.dw, self.db, self.dgamma, self.dbeta):
+            t.zero_()
+
+    def fwd_train(self, x, stream=None):
+        bn = self.spec.norm == abi.NORM_BATCH
+        abi.check(abi.conv2d_fwd_train(self.desc, x, self.w, self.b, self.gamma if bn else None,
+                                       self.beta if bn else None, self.running_mean if bn else None,
+                                       self.running_var if bn else None, self.pre_act,
+                                       self.save_mean if bn else None, self.save_inv_std if bn else None, self.y,
+                                       self.ws, stream=stream), "conv2d_fwd_train")
+        return self.y
+
+    def fwd_infer(self, x, y=None, stream=None):
+        y = self.y if y is None else y
+        abi.check(abi.conv2d_fwd_infer(self.desc, x, self.w, self.b, self.gamma, self.beta, self.running_mean,
+                                       self.running_var, y, self.ws, stream=stream), "conv2d_fwd_infer")
+        return y
+
+    def bwd(self, x, dy, need_dx=True, need_params=True, stream=None):
+        bn = self.spec.norm == abi.NORM_BATCH
+        abi.check(abi.conv2d_bwd(self.desc, x, self.w, self.gamma if bn else None, self.beta if bn else None,
+                                 self.pre_act, self.save_mean if bn else None, self.save_inv_std if bn else None, dy,
+                                 self.dx if need_dx else None, self.dw if need_params else None,
+                                 self.db if need_params else None,
+                                 self.dgamma if (bn and need_params) else None,
+                                 self.dbeta if (bn and need_params) else None, self.ws, stream=stream),
+                  "conv2d_bwd")
+        return self.dx if need_dx else None

@@ -1,0 +1,147 @@
+/*
+ * conv2d.h - C ABI of the GB300 (sm_103a) conv2d training-step library
+ * (libconv2d.so).
+ *
+ * One NHWC 2D convolution layer: conv + bias, optional training-mode batch
+ * norm, activation; and its backward pass. The operation is the one defined by
+ * the rl-tools conv2d layer pages ("operations_generic.h": `forward`,
+ * `evaluate`, `backward`, `backward_input`, `backward_full`; the CUDA page
+ * "operations_cuda.h" splits the same work into cuDNN calls and per-channel
+ * kernels). The layer spec (N,H,W,IC,OC,KH,KW,stride,pad, normalization,
+ * activation, eps, momentum, type policy) follows the template parameters
+ * those pages read from their LayerSpec.
+ *
+ * Conventions (all calls):
+ *   - Tensors are dense, contiguous NHWC: x [N][H][W][IC], y / pre_act / dy
+ *     [N][OH][OW][OC], weights w [OC][KH][KW][IC]; OH = (H+2*pad-KH)/stride+1
+ *     (floor), OW likewise; symmetric zero padding; cross-correlation (no
+ *     kernel flip); no dilation, no groups.
+ *   - x, w, pre_act, y, dy, dx have the element type named by desc->dtype
+ *     (CONV2D_FP32: float; CONV2D_BF16: bfloat16). bias, gamma, beta, running
+ *     statistics, saved statistics and every parameter gradient are float32.
+ *   - Every pointer is a DEVICE pointer on the current CUDA device, aligned to
+ *     16 bytes. The caller owns every buffer; the library allocates no device
+ *     memory on any path. Scratch space is the caller's workspace `ws` of at
+ *     least conv2d_workspace_size(desc, op) bytes (alignment 256 bytes); its
+ *     contents need not be initialised and are clobbered.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream). Buffers must not be touched by other work until the
+ *     stream reaches the call. Calls that share a workspace must be ordered.
+ *   - Return value: CONV2D_OK, or an error code from host-side validation or
+ *     launch (no kernel is launched when validation fails). Device-side
+ *     failures (a bounded wait that ran out) are reported later by
+ *     conv2d_device_status().
+ *   - Accumulate / overwrite semantics follow `backward_full`: dw, dbias,
+ *     dgamma, dbeta are ACCUMULATED into (the caller zeroes them, as the
+ *     pages' `zero_gradient` does); dx is OVERWRITTEN.
+ *   - The library is stateless apart from per-device constant data; it is
+ *     safe to call from several host threads.
+ */
+#ifndef CONV2D_GB300_H
+#define CONV2D_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum {
+    CONV2D_OK = 0,
+    CONV2D_ERR_INVALID_ARG = 1, /* bad size, NULL or misaligned pointer, bad enum, eps<=0, momentum outside [0,1] */
+    CONV2D_ERR_UNSUPPORTED = 2, /* valid but not implemented (layer norm, stride > 8, sizes beyond 2^31 elements) */
+    CONV2D_ERR_WORKSPACE = 3,   /* ws NULL or smaller than conv2d_workspace_size() */
+    CONV2D_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed (launch, tensor-map encode) */
+    CONV2D_ERR_TIMEOUT = 5      /* a device-side bounded wait expired (reported by conv2d_device_status) */
+};
+
+/* Normalization (the pages' `Normalization` enum; LAYER_NORM is not implemented). */
+enum { CONV2D_NORM_NONE = 0, CONV2D_NORM_BATCH = 1, CONV2D_NORM_LAYER = 2 };
+
+/* Activation applied after (optional) normalization. */
+enum { CONV2D_ACT_IDENTITY = 0, CONV2D_ACT_RELU = 1, CONV2D_ACT_TANH = 2, CONV2D_ACT_SIGMOID = 3 };
+
+/* Element type of x, w, pre_act, y, dy, dx. FP32 runs the contractions as
+ * 3xTF32 (split operands, fp32 accumulation) for fp32 accuracy; BF16 runs
+ * bf16 x bf16 -> fp32 accumulation. */
+enum { CONV2D_FP32 = 0, CONV2D_BF16 = 1 };
+
+/* Operation selector for conv2d_workspace_size(). */
+enum { CONV2D_OP_FWD_TRAIN = 0, CONV2D_OP_FWD_INFER = 1, CONV2D_OP_BWD = 2 };
+
+/* Layer spec. eps and momentum are read only when norm == CONV2D_NORM_BATCH
+ * (running = (1-momentum)*running + momentum*batch, biased batch variance). */
+typedef struct {
+    int32_t N, H, W, IC, OC, KH, KW, stride, pad;
+    int32_t norm, act, dtype;
+    float eps, momentum;
+} conv2d_desc;
+
+/* Output spatial size. Returns CONV2D_OK or CONV2D_ERR_INVALID_ARG. */
+int conv2d_out_hw(const conv2d_desc* desc, int32_t* OH, int32_t* OW);
+
+/* Host-side validation of a layer spec alone (no pointers). */
+int conv2d_validate(const conv2d_desc* desc);
+
+/* Bytes of workspace needed by `op` for this spec (0 if the spec is invalid). */
+size_t conv2d_workspace_size(const conv2d_desc* desc, int op);
+
+/* Training forward (`forward` on the generic page; cuDNN conv + bias, batch
+ * statistics, affine and activation kernels on the CUDA page).
+ *   pre_act  [N][OH][OW][OC] out: conv + bias (the pages' `pre_activations`)
+ *   y        [N][OH][OW][OC] out: activation(normalised pre_act)
+ *   BATCH norm only (else may be NULL):
+ *     gamma, beta [OC] in; running_mean, running_var [OC] in/out (EMA update);
+ *     save_mean, save_inv_std [OC] out: batch mean and 1/sqrt(var+eps) that
+ *     conv2d_bwd needs.
+ *   bias may be NULL (treated as zero). */
+int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, const float* bias,
+                     const float* gamma, const float* beta, float* running_mean, float* running_var,
+                     void* pre_act, float* save_mean, float* save_inv_std, void* y,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* Inference forward (`evaluate`): y = act(norm(conv + bias)), batch norm with
+ * the running statistics (`bn_stats_eval` / `bn_forward_eval_running` on the
+ * CUDA page); no state is written. gamma, beta, running_mean, running_var are
+ * read only for BATCH norm. */
+int conv2d_fwd_infer(const conv2d_desc* desc, const void* x, const void* w, const float* bias,
+                     const float* gamma, const float* beta, const float* running_mean,
+                     const float* running_var, void* y, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward (`backward_full`; `backward_input` when dw..dbeta are all NULL;
+ * `backward` when dx is NULL). Inputs: x, w, pre_act and (BATCH) gamma, beta,
+ * save_mean, save_inv_std from conv2d_fwd_train, dy = dLoss/dy.
+ *   dx [N][H][W][IC]   out (overwritten), may be NULL
+ *   dw [OC][KH][KW][IC], dbias [OC]        accumulated, may be NULL together
+ *   dgamma, dbeta [OC] (BATCH norm only)    accumulated, may be NULL together
+ * Batch-norm backward uses the saved batch statistics, not recomputed ones.
+ * At least one of dx / dw must be non-NULL. */
+int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const float* gamma,
+               const float* beta, const void* pre_act, const float* save_mean,
+               const float* save_inv_std, const void* dy, void* dx, float* dw, float* dbias,
+               float* dgamma, float* dbeta, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, then reads and clears this device's error word,
+ * which kernels set when a bounded wait expires. Returns CONV2D_OK,
+ * CONV2D_ERR_TIMEOUT (with *site, if non-NULL, set to the wait site code) or
+ * CONV2D_ERR_CUDA. */
+int conv2d_device_status(void* stream, int32_t* site);
+
+/* Human-readable name of a status code (static string). */
+const char* conv2d_status_str(int status);
+
+/* Kernel timing for measurement. While enabled (on != 0), every kernel the
+ * library launches is bracketed by CUDA events on its stream and recorded in
+ * a fixed ring of 256 launches. conv2d_prof_read synchronises the device and
+ * copies up to `cap` records (oldest first): a static kernel name and the
+ * elapsed milliseconds; it returns the number copied and clears the ring.
+ * Off by default; when off no events are recorded. */
+int conv2d_prof_enable(int on);
+int conv2d_prof_read(const char** names, float* ms, int cap);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CONV2D_GB300_H */

@@ -1,0 +1,96 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a, loads,
+exports every entry point include/conv2d.h declares, and rejects bad
+arguments on the host (no kernel is launched when validation fails)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conv2d_layer_gb300 import abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "conv2d.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(conv2d_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared() == sorted(abi.EXPORTS)
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    L = abi.lib()
+    for name in _declared():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def good(**kw):
+    base = dict(N=2, H=8, W=8, IC=3, OC=4, KH=3, KW=3, stride=1, pad=1, norm=abi.NORM_BATCH, act=abi.ACT_RELU,
+                dtype=abi.FP32, eps=1e-5, momentum=0.1)
+    base.update(kw)
+    return abi.desc(**base)
+
+
+def test_out_hw():
+    rc, oh, ow = abi.conv2d_out_hw(good(H=84, W=84, KH=8, KW=8, stride=4, pad=0))
+    assert (rc, oh, ow) == (abi.OK, 20, 20)
+    rc, oh, ow = abi.conv2d_out_hw(good(H=56, W=56, stride=2, pad=1))
+    assert (rc, oh, ow) == (abi.OK, 28, 28)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("N", 0, abi.ERR_INVALID_ARG), ("H", -1, abi.ERR_INVALID_ARG), ("IC", 0, abi.ERR_INVALID_ARG),
+    ("OC", 0, abi.ERR_INVALID_ARG), ("KH", 0, abi.ERR_INVALID_ARG), ("stride", 0, abi.ERR_INVALID_ARG),
+    ("pad", -1, abi.ERR_INVALID_ARG), ("KH", 11, abi.ERR_INVALID_ARG), ("norm", 3, abi.ERR_INVALID_ARG),
+    ("act", 4, abi.ERR_INVALID_ARG), ("dtype", 2, abi.ERR_INVALID_ARG), ("eps", 0.0, abi.ERR_INVALID_ARG),
+    ("eps", float("nan"), abi.ERR_INVALID_ARG), ("momentum", 1.5, abi.ERR_INVALID_ARG),
+    ("momentum", -0.1, abi.ERR_INVALID_ARG), ("norm", abi.NORM_LAYER, abi.ERR_UNSUPPORTED),
+    ("stride", 9, abi.ERR_UNSUPPORTED),
+])
+def test_validation_codes(field, value, code):
+    d = good()
+    setattr(d, field, value)
+    assert abi.conv2d_validate(d) == code
+    assert abi.conv2d_workspace_size(d, abi.OP_FWD_TRAIN) == 0
+
+
+def test_eps_and_momentum_ignored_without_norm():
+    assert abi.conv2d_validate(good(norm=abi.NORM_NONE, eps=0.0, momentum=7.0)) == abi.OK
+
+
+def test_workspace_sizes_positive_and_op_checked():
+    d = good(dtype=abi.BF16, H=56, W=56, IC=256, OC=256)
+    for op in (abi.OP_FWD_TRAIN, abi.OP_FWD_INFER, abi.OP_BWD):
+        assert abi.conv2d_workspace_size(d, op) > 0
+    assert abi.conv2d_workspace_size(d, 7) == 0
+    # backward keeps d_conv (n_pix x OC operand elements) in the workspace
+    assert abi.conv2d_workspace_size(d, abi.OP_BWD) >= 2 * 56 * 56 * 256 * 2
+
+
+def test_null_and_misaligned_pointers_rejected_before_launch():
+    d = good(norm=abi.NORM_NONE)
+    ws = ctypes.create_string_buffer(1 << 16)
+    addr = ctypes.addressof(ws)
+    al = (addr + 255) & ~255
+    rc = abi.conv2d_fwd_train(d, None, al, None, None, None, None, None, al, None, None, al, al, 1 << 15, 0)
+    assert rc == abi.ERR_INVALID_ARG
+    rc = abi.conv2d_fwd_train(d, al + 4, al, None, None, None, None, None, al, None, None, al, al, 1 << 15, 0)
+    assert rc == abi.ERR_INVALID_ARG
+    dbn = good()
+    rc = abi.conv2d_fwd_train(dbn, al, al, None, None, None, None, None, al, None, None, al, al, 1 << 15, 0)
+    assert rc == abi.ERR_INVALID_ARG  # batch norm needs gamma, beta, running and saved statistics
+    rc = abi.conv2d_bwd(d, al, al, None, None, al, None, None, al, None, None, None, None, None, al, 1 << 15, 0)
+    assert rc == abi.ERR_INVALID_ARG  # neither dx nor dw requested
+    rc = abi.conv2d_fwd_infer(good(norm=abi.NORM_LAYER), al, al, None, None, None, None, None, al, al, 1 << 15, 0)
+    assert rc == abi.ERR_UNSUPPORTED
+
+
+def test_status_strings():
+    for s in range(6):
+        assert abi.status_str(s)
+    assert abi.status_str(99) == "unknown status"

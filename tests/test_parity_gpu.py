@@ -1,0 +1,172 @@
+"""GPU parity: the C-ABI CUDA path against the CPU oracle, element by element,
+on the same seeded inputs, at sizes the oracle finishes in seconds that still
+span several tiles and a ragged tail; plus the edge cases of the layer
+(channel counts that are not a multiple of the vector width, more than one
+column tile, 1x1 outputs, strides larger than the kernel, stride-4 dgrad).
+"""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+from conv2d_layer_gb300 import abi
+from conv2d_layer_gb300.layer import Conv2dLayer
+from conv2d_layer_gb300.workloads import (ACT_IDENTITY, ACT_RELU, ACT_SIGMOID, ACT_TANH, BF16, FP32, NORM_BATCH,
+                                          NORM_NONE, WORKLOADS, LayerSpec, make_inputs, random_layer_inputs)
+from parity_util import check_pair, f64, oracle_layer, rel_err, run_pair, TOL
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _wl(name, **over):
+    spec = replace(WORKLOADS[name].layers[0], **over)
+    return spec, make_inputs(name, layers=[spec])
+
+
+CONFIG_CASES = {
+    # the five workloads at reduced batch / spatial size (same channels, kernels, strides, modes)
+    "tiny": lambda: (WORKLOADS["tiny"].layers[0], make_inputs("tiny")),
+    "rl_n3": lambda: _wl("rl", N=3),
+    "bn_n4": lambda: _wl("bn", N=4),
+    "mixed_l1_20x20": lambda: (lambda s: (s, random_layer_inputs(s, 31)))(
+        replace(WORKLOADS["mixed"].layers[0], N=2, H=20, W=20)),
+    "mixed_l2_20x20": lambda: (lambda s: (s, random_layer_inputs(s, 32)))(
+        replace(WORKLOADS["mixed"].layers[1], N=2, H=20, W=20)),
+    "large_20x20": lambda: _wl("large", N=1, H=20, W=20),
+}
+
+EDGE_CASES = {
+    "bf16_ic3_oc20_k5s3p2_sigmoid": LayerSpec(N=2, H=13, W=13, IC=3, OC=20, KH=5, KW=5, stride=3, pad=2,
+                                              norm=NORM_NONE, act=ACT_SIGMOID, dtype=BF16),
+    "fp32_ic5_oc130_k3s2p1_bn_tanh": LayerSpec(N=2, H=9, W=9, IC=5, OC=130, KH=3, KW=3, stride=2, pad=1,
+                                               norm=NORM_BATCH, act=ACT_TANH, dtype=FP32),
+    "bf16_oc320_1x1_identity": LayerSpec(N=3, H=7, W=7, IC=64, OC=320, KH=1, KW=1, stride=1, pad=0,
+                                         norm=NORM_NONE, act=ACT_IDENTITY, dtype=BF16),
+    "fp32_out1x1_bn_relu": LayerSpec(N=5, H=3, W=3, IC=4, OC=8, KH=3, KW=3, stride=1, pad=0, norm=NORM_BATCH,
+                                     act=ACT_RELU, dtype=FP32),
+    "bf16_k8s4p2": LayerSpec(N=2, H=36, W=36, IC=8, OC=64, KH=8, KW=8, stride=4, pad=2, norm=NORM_NONE,
+                             act=ACT_TANH, dtype=BF16),
+    "fp32_k4s2p1_identity": LayerSpec(N=2, H=10, W=10, IC=4, OC=16, KH=4, KW=4, stride=2, pad=1, norm=NORM_NONE,
+                                      act=ACT_IDENTITY, dtype=FP32),
+    "bf16_ic16_bn_sigmoid": LayerSpec(N=2, H=16, W=16, IC=16, OC=64, KH=3, KW=3, stride=1, pad=1,
+                                      norm=NORM_BATCH, act=ACT_SIGMOID, dtype=BF16),
+    "fp32_stride_gt_kernel": LayerSpec(N=2, H=9, W=9, IC=4, OC=4, KH=2, KW=2, stride=3, pad=0, norm=NORM_NONE,
+                                       act=ACT_IDENTITY, dtype=FP32),
+    "fp32_rect_kernel": LayerSpec(N=2, H=11, W=7, IC=8, OC=12, KH=3, KW=1, stride=1, pad=1, norm=NORM_BATCH,
+                                  act=ACT_SIGMOID, dtype=FP32),
+}
+
+
+@pytest.mark.parametrize("name", list(CONFIG_CASES))
+def test_config_parity(name):
+    spec, inp = CONFIG_CASES[name]()
+    gpu, ref = run_pair(spec, inp)
+    check_pair(spec, gpu, ref)
+
+
+@pytest.mark.parametrize("name", list(EDGE_CASES))
+def test_edge_parity(name):
+    spec = EDGE_CASES[name]
+    inp = random_layer_inputs(spec, 7)
+    gpu, ref = run_pair(spec, inp)
+    check_pair(spec, gpu, ref)
+
+
+@pytest.mark.parametrize("dtype", [FP32, BF16])
+def test_accumulate_and_partial_backward(dtype):
+    """dW/dbias/dgamma/dbeta accumulate into existing values; dx is overwritten;
+    backward_input (params NULL) and backward (dx NULL) variants."""
+    spec = LayerSpec(N=2, H=12, W=12, IC=16, OC=32, KH=3, KW=3, stride=1, pad=1, norm=NORM_BATCH, act=ACT_TANH,
+                     dtype=dtype)
+    inp = random_layer_inputs(spec, 11)
+    gpu, ref = run_pair(spec, inp, prev_grads=True)
+    check_pair(spec, gpu, ref)
+    gpu, ref = run_pair(spec, inp, need_params=False)
+    check_pair(spec, gpu, ref, need_params=False)
+    gpu, ref = run_pair(spec, inp, need_dx=False)
+    check_pair(spec, gpu, ref, need_dx=False)
+
+
+@pytest.mark.parametrize("norm,act,dtype", [(NORM_BATCH, ACT_RELU, FP32), (NORM_NONE, ACT_SIGMOID, FP32),
+                                            (NORM_BATCH, ACT_TANH, BF16), (NORM_NONE, ACT_RELU, BF16)])
+def test_infer_parity(norm, act, dtype):
+    spec = LayerSpec(N=3, H=15, W=15, IC=32, OC=48, KH=3, KW=3, stride=2, pad=1, norm=norm, act=act, dtype=dtype)
+    inp = random_layer_inputs(spec, 5)
+    li = inp["layers"][0]
+    g = torch.Generator().manual_seed(5)
+    rm = torch.randn(spec.OC, generator=g) * 0.2
+    rv = torch.rand(spec.OC, generator=g) + 0.5
+    L = Conv2dLayer(spec, li.w, li.b, li.gamma, li.beta, rm, rv)
+    y = L.fwd_infer(inp["x"].cuda())
+    torch.cuda.synchronize()
+    ref = oracle.fwd_infer(oracle_layer(spec), f64(inp["x"]), f64(li.w), f64(li.b), f64(li.gamma), f64(li.beta),
+                           f64(rm), f64(rv))
+    assert rel_err(f64(y), ref) <= TOL[dtype]
+    # no state written by inference
+    assert torch.equal(L.running_mean.cpu(), rm.float()) and torch.equal(L.running_var.cpu(), rv.float())
+
+
+def test_deterministic_bitwise():
+    spec = LayerSpec(N=4, H=16, W=16, IC=32, OC=64, KH=3, KW=3, stride=1, pad=1, norm=NORM_BATCH, act=ACT_RELU,
+                     dtype=BF16)
+    inp = random_layer_inputs(spec, 3)
+    li = inp["layers"][0]
+    outs = []
+    for _ in range(2):
+        L = Conv2dLayer(spec, li.w, li.b, li.gamma, li.beta)
+        x, dy = inp["x"].cuda(), inp["dy"].cuda()
+        L.zero_grad()
+        L.fwd_train(x)
+        L.bwd(x, dy)
+        torch.cuda.synchronize()
+        outs.append([t.clone() for t in (L.y, L.dx, L.dw, L.db, L.dgamma, L.dbeta, L.running_var)])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+def test_outputs_stay_inside_their_buffers():
+    """Canary-filled guard regions before and after every output stay intact."""
+    spec = EDGE_CASES["bf16_ic3_oc20_k5s3p2_sigmoid"]
+    spec = replace(spec, norm=NORM_BATCH)
+    inp = random_layer_inputs(spec, 9)
+    li = inp["layers"][0]
+    d = abi.desc(spec.N, spec.H, spec.W, spec.IC, spec.OC, spec.KH, spec.KW, spec.stride, spec.pad, spec.norm,
+                 spec.act, spec.dtype, spec.eps, spec.momentum)
+    G = 256  # guard elements on each side (keeps 16-byte alignment)
+
+    def guarded(n, dtype, fill):
+        buf = torch.full((n + 2 * G,), fill, dtype=dtype, device="cuda")
+        return buf, buf[G:G + n]
+
+    y_shape = spec.N * spec.OH * spec.OW * spec.OC
+    bufs = {}
+    bufs["pre"], pre = guarded(y_shape, torch.bfloat16, 7.0)
+    bufs["y"], y = guarded(y_shape, torch.bfloat16, 7.0)
+    bufs["dx"], dx = guarded(spec.N * spec.H * spec.W * spec.IC, torch.bfloat16, 7.0)
+    bufs["dw"], dw = guarded(spec.OC * spec.KH * spec.KW * spec.IC, torch.float32, 0.0)
+    small = {}
+    for k in ("db", "dg", "dbt", "mean", "istd", "rm", "rv"):
+        bufs[k], small[k] = guarded(spec.OC, torch.float32, 0.0)
+    small["rv"].fill_(1.0)
+    ws_n = max(abi.conv2d_workspace_size(d, op) for op in range(3))
+    ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda")
+    x, dyv = inp["x"].cuda(), inp["dy"].cuda()
+    w, b = li.w.cuda(), li.b.cuda()
+    gm, bt = li.gamma.cuda(), li.beta.cuda()
+    abi.check(abi.conv2d_fwd_train(d, x, w, b, gm, bt, small["rm"], small["rv"], pre, small["mean"],
+                                   small["istd"], y, ws))
+    abi.check(abi.conv2d_bwd(d, x, w, gm, bt, pre, small["mean"], small["istd"], dyv, dx, dw, small["db"],
+                             small["dg"], small["dbt"], ws))
+    torch.cuda.synchronize()
+    for k, buf in bufs.items():
+        fill = 7.0 if buf.dtype == torch.bfloat16 else 0.0
+        head, tail = buf[:G].float().cpu(), buf[-G:].float().cpu()
+        assert torch.all(head == fill) and torch.all(tail == fill), k
+
+
+def test_device_status_clean():
+    rc, site = abi.conv2d_device_status()
+    assert rc == abi.OK and site == 0
