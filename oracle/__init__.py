@@ -20,11 +20,13 @@ import numpy as np
 from . import build as _build
 
 ACT = {"identity": 0, "relu": 1, "tanh": 2, "sigmoid": 3}
+STORE = {None: 0, "f64": 0, "f32": 1, "bf16": 2}
 NORM = {"none": 0, "batch": 1}
 
 
 class _Desc(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int32) for n in ("N", "H", "W", "IC", "OC", "KH", "KW", "S", "P", "norm", "act")] + [
+    _fields_ = [(n, ctypes.c_int32) for n in ("N", "H", "W", "IC", "OC", "KH", "KW", "S", "P", "norm", "act",
+                                              "store")] + [
         ("eps", ctypes.c_double),
         ("momentum", ctypes.c_double),
     ]
@@ -49,6 +51,8 @@ def _load():
         lib.oracle_dact.restype = ctypes.c_double
         lib.oracle_dact.argtypes = [ctypes.c_int, ctypes.c_double]
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_store_round.restype = ctypes.c_double
+        lib.oracle_store_round.argtypes = [ctypes.c_int, ctypes.c_double]
         _lib = lib
     return _lib
 
@@ -58,21 +62,23 @@ def num_threads() -> int:
 
 
 class Layer:
-    """Layer spec: N,H,W,IC,OC,KH,KW,stride,pad, normalization, activation, eps, momentum."""
+    """Layer spec: N,H,W,IC,OC,KH,KW,stride,pad, normalization, activation, eps, momentum, and the
+    element type the pre-activations are stored in (store: None/"f64" keeps fp64, "f32", "bf16")."""
 
     def __init__(self, N, H, W, IC, OC, KH, KW, stride=1, pad=0, norm="none", act="identity",
-                 eps=1e-5, momentum=0.1):
+                 eps=1e-5, momentum=0.1, store=None):
         self.N, self.H, self.W, self.IC, self.OC = N, H, W, IC, OC
         self.KH, self.KW, self.S, self.P = KH, KW, stride, pad
         self.norm = norm if isinstance(norm, int) else NORM[norm]
         self.act = act if isinstance(act, int) else ACT[act]
         self.eps, self.momentum = float(eps), float(momentum)
+        self.store = store if isinstance(store, int) else STORE[store]
         self.OH = (H + 2 * pad - KH) // stride + 1
         self.OW = (W + 2 * pad - KW) // stride + 1
 
     def _c(self):
         return _Desc(self.N, self.H, self.W, self.IC, self.OC, self.KH, self.KW, self.S, self.P,
-                     self.norm, self.act, self.eps, self.momentum)
+                     self.norm, self.act, self.store, self.eps, self.momentum)
 
     @property
     def x_shape(self):
@@ -223,6 +229,13 @@ def bwd(L: Layer, x, w, ypre, dy, gamma=None, beta=None, mean=None, inv_std=None
     lib.oracle_bwd(ctypes.byref(c), _p(x), _p(w), _p(gamma), _p(beta), _p(ypre), _p(mean), _p(inv_std), _p(dy),
                    _p(dx), _p(dw), _p(db), _p(dg), _p(dbt), _p(dc))
     return dict(dx=dx, dw=dw, db=db, dgamma=dg, dbeta=dbt, dconv=dc)
+
+
+def store_round(store, v):
+    """Round to the pre-activation storage type (vectorised over an array)."""
+    lib = _load()
+    k = store if isinstance(store, int) else STORE[store]
+    return np.vectorize(lambda t: lib.oracle_store_round(k, float(t)))(v)
 
 
 def act(kind, v):

@@ -24,6 +24,12 @@
  *     derivative is taken at the activation input, ReLU'(0) = 0.
  *   - dX is overwritten, dW / dBias / dGamma / dBeta are accumulated into
  *     (`backward_full` loads the existing gradients first).
+ *   - the pre-activations are stored in the layer's element type T (`forward`
+ *     Phase 1 writes `(T)acc` into `pre_activations`; the CUDA page's
+ *     `bn_stats_training` reads `const T* pre_act`), and the batch statistics,
+ *     the normalisation and the backward pass all read that stored value. The
+ *     `store` field names T: fp32 (round to nearest) or bf16 (round to
+ *     nearest even, through fp32); 0 keeps fp64 (the pure definition).
  * Parallelism (OpenMP) is only over independent output elements; every
  * element is the plain sum its definition states.
  */
@@ -40,6 +46,7 @@ typedef struct {
     int32_t N, H, W, IC, OC, KH, KW, S, P;
     int32_t norm; /* 0 none, 1 batch norm */
     int32_t act;  /* 0 identity, 1 relu, 2 tanh, 3 sigmoid */
+    int32_t store; /* element type T of the stored pre-activations: 0 keep fp64, 1 fp32, 2 bf16 */
     double eps, momentum;
 } oracle_desc;
 
@@ -49,6 +56,21 @@ int oracle_num_threads(void) {
 #else
     return 1;
 #endif
+}
+
+/* Round v to the storage type T of the pre-activations. */
+double oracle_store_round(int store, double v) {
+    if (store == 1) return (double)(float)v;
+    if (store == 2) {
+        float f = (float)v;
+        uint32_t u;
+        memcpy(&u, &f, 4);
+        if ((u & 0x7f800000u) != 0x7f800000u) u += 0x7fffu + ((u >> 16) & 1u); /* nearest, ties to even */
+        u &= 0xffff0000u;
+        memcpy(&f, &u, 4);
+        return (double)f;
+    }
+    return v;
 }
 
 static int out_h(const oracle_desc* d) { return (d->H + 2 * d->P - d->KH) / d->S + 1; }
@@ -146,6 +168,8 @@ void oracle_fwd_train(const oracle_desc* d, const double* x, const double* w, co
     const long npix = (long)d->N * out_h(d) * out_w(d);
     const int C = d->OC;
     oracle_conv_fwd(d, x, w, b, ypre);
+    if (d->store)
+        for (long i = 0; i < npix * C; i++) ypre[i] = oracle_store_round(d->store, ypre[i]);
     if (d->norm == 0) {
         for (long i = 0; i < npix * C; i++) y[i] = oracle_act(d->act, ypre[i]);
         return;
@@ -181,6 +205,8 @@ void oracle_fwd_infer(const oracle_desc* d, const double* x, const double* w, co
             size_t i = (size_t)p * C + c;
             double v = y[i];
             if (d->norm == 1) {
+                /* `evaluate` BN branch: the conv output is stored as T first */
+                v = oracle_store_round(d->store, v);
                 double is = 1.0 / sqrt(rv[c] + d->eps);
                 v = gamma[c] * ((v - rm[c]) * is) + beta[c];
             }

@@ -301,3 +301,38 @@ def test_against_torch_cpu_float64():
             # torch keeps the unbiased variance in running_var; the pages keep the biased one
             var_b = (trv.numpy() - (1 - L.momentum) * rv0) / L.momentum * (n - 1) / n
             np.testing.assert_allclose(f["running_var"], (1 - L.momentum) * rv0 + L.momentum * var_b, rtol=1e-12)
+
+
+def test_store_rounding_matches_bf16_and_fp32_conversion():
+    """Pre-activation storage rounding: bf16 round-to-nearest-even (through fp32) and fp32 round-to-nearest,
+    checked against torch's conversions and a few hand-picked ties."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(17)
+    v = np.concatenate([rng.standard_normal(4000) * 10.0 ** rng.integers(-30, 30, 4000),
+                        [0.0, -0.0, 1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 65504.0, 3e38, 1e-40]])
+    f32 = v.astype(np.float32)
+    got = oracle.store_round("bf16", f32.astype(np.float64))
+    ref = torch.from_numpy(f32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(got, ref)
+    # ties go to the even mantissa: 1+2^-8 -> 1, 1+3*2^-8 -> 1+2^-6
+    assert oracle.store_round("bf16", 1 + 2 ** -8) == 1.0
+    assert oracle.store_round("bf16", 1 + 3 * 2 ** -8) == 1 + 2 ** -6
+    np.testing.assert_array_equal(oracle.store_round("f32", v), v.astype(np.float32).astype(np.float64))
+    np.testing.assert_array_equal(oracle.store_round("f64", v), v)
+
+
+@pytest.mark.parametrize("store", ["f32", "bf16"])
+def test_stored_preactivations_feed_the_statistics(store):
+    """With a storage type, Ypre is rounded once and everything downstream reads the rounded value."""
+    rng = np.random.default_rng(23)
+    L = oracle.Layer(2, 6, 6, 4, 5, 3, 3, 1, 1, norm="batch", act="relu", store=store)
+    L0 = oracle.Layer(2, 6, 6, 4, 5, 3, 3, 1, 1, norm="batch", act="relu")
+    x, w, b, gamma, beta, _ = _rand_layer(rng, L)
+    f = oracle.fwd_train(L, x, w, b, gamma, beta)
+    exact = oracle.conv_fwd(L0, x, w, b)
+    np.testing.assert_array_equal(f["ypre"], oracle.store_round(store, exact))
+    yp = f["ypre"].reshape(-1, L.OC)
+    np.testing.assert_allclose(f["mean"], yp.mean(0), rtol=1e-13)
+    np.testing.assert_allclose(f["inv_std"], 1 / np.sqrt(yp.var(0) + L.eps), rtol=1e-12)
+    z = (f["ypre"] - f["mean"]) * f["inv_std"]
+    np.testing.assert_allclose(f["y"], np.maximum(gamma * z + beta, 0), rtol=1e-13, atol=1e-15)
