@@ -3,7 +3,8 @@
 //
 // Call sequences (kernels of this library only; nothing runs on the host):
 //   conv2d_fwd_train: [pack x/w] -> fprop GEMM (epilogue: + bias; no norm:
-//                     also y = act) -> [BN: stats -> finalize -> apply]
+//                     also y = act; BN: per-tile statistics) -> [BN:
+//                     finalize -> apply]
 //   conv2d_fwd_infer: [fold BN into scale/shift] -> fprop GEMM (epilogue:
 //                     y = act(acc*scale + shift))
 //   conv2d_bwd:       [BN: reduce -> finalize] -> d_conv (+ dbias partials)
@@ -212,8 +213,9 @@ Tile conv_tile(const Geo& g, int ncols) {
   t.BN = static_cast<int>(round_up(ceil_div(ncols, t.n_tiles), 16));
   const size_t ns = g.dt == CONV2D_BF16 ? 1 : 2;
   const size_t stage = ns * (kBM * 128 + static_cast<size_t>(t.BN) * 128);
-  t.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048) / stage));
-  t.smem = t.stages * stage + 1024 + 256;
+  const size_t stats = 9 * static_cast<size_t>(t.BN) * 4;  // epilogue batch-statistics scratch
+  t.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048 - stats) / stage));
+  t.smem = t.stages * stage + 1024 + 256 + stats;
   return t;
 }
 
@@ -342,11 +344,10 @@ void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
     if (g.pack_x) sz[R_XP] = static_cast<size_t>(g.N) * g.H * g.W * g.ICp * es;
     if (g.dt == CONV2D_FP32 || g.pack_x) sz[R_WB] = static_cast<size_t>(g.OC) * g.Kf * es;
     if (g.dt == CONV2D_FP32) sz[R_WBLO] = static_cast<size_t>(g.OC) * g.Kf * 4;
-    if (op == CONV2D_OP_FWD_TRAIN && g.norm == CONV2D_NORM_BATCH) sz[R_PART] = G * g.OC * 3 * 4;
+    if (op == CONV2D_OP_FWD_TRAIN && g.norm == CONV2D_NORM_BATCH)
+      sz[R_PART] = static_cast<size_t>(ceil_div(g.n_pix, kBM)) * g.OC * 3 * 4;  // per-tile statistics
     if (op == CONV2D_OP_FWD_INFER) sz[R_FOLD] = 2 * static_cast<size_t>(g.OC) * 4;
   } else {
-    const DgradPlan* unused = nullptr;
-    (void)unused;
     sz[R_DC] = static_cast<size_t>(g.n_pix) * g.OCp * es;
     sz[R_PART] = G * g.OC * 2 * 4;
     sz[R_C12] = 2 * static_cast<size_t>(g.OC) * 4;
@@ -376,7 +377,7 @@ char* region(void* ws, const Plan& pl, Reg r) { return static_cast<char*>(ws) + 
 
 // fprop GEMM: D[pix][oc] = im2col(x) * B^T, epilogue per ConvGemmParams.
 int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bhi, const void* blo, void* out,
-              void* out2, const float* scale, const float* shift, int out_act, cudaStream_t st) {
+              void* out2, const float* scale, const float* shift, int out_act, float* stats, cudaStream_t st) {
   static ConvGemmParams p;  // guarded by g_launch_mu below (large struct)
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
@@ -421,6 +422,7 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   p.ep_shift = shift;
   p.act = g.act;
   p.out_act = out_act;
+  p.stats = stats;
   p.stages = t.stages;
   p.err = dev->err;
   const int grid = std::min(p.num_units, dev->sms);
@@ -586,12 +588,13 @@ int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, cons
   const void *xsrc, *bhi, *blo;
   if ((rc = prep_forward_operands(g, x, w, ws, pl, &xsrc, &bhi, &blo, st))) return rc;
   const bool bn = g.norm == CONV2D_NORM_BATCH;
-  if ((rc = run_fprop(g, dev, xsrc, bhi, blo, pre_act, bn ? nullptr : y, nullptr, bias, 0, st))) return rc;
+  float* part = bn ? reinterpret_cast<float*>(region(ws, pl, R_PART)) : nullptr;
+  if ((rc = run_fprop(g, dev, xsrc, bhi, blo, pre_act, bn ? nullptr : y, nullptr, bias, 0, part, st))) return rc;
   if (bn) {
-    float* part = reinterpret_cast<float*>(region(ws, pl, R_PART));
-    LAUNCH("bn_stats", st, launch_bn_stats(g.dt, pre_act, pl.walk, part, st));
+    RowWalk tiles = pl.walk;  // partials: one per 128-row tile of the fprop GEMM
+    tiles.G = static_cast<int>(ceil_div(g.n_pix, kBM));
     LAUNCH("bn_stats_finalize", st,
-           launch_bn_stats_finalize(part, pl.walk, g.eps, g.mom, save_mean, save_inv_std, running_mean, running_var,
+           launch_bn_stats_finalize(part, tiles, g.eps, g.mom, save_mean, save_inv_std, running_mean, running_var,
                                     st));
     LAUNCH("bn_apply", st, launch_bn_apply(g.dt, pre_act, y, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, st));
   }
@@ -620,7 +623,7 @@ int conv2d_fwd_infer(const conv2d_desc* desc, const void* x, const void* w, cons
   float* shift = scale + g.OC;
   LAUNCH("infer_fold", st,
          launch_infer_fold(bias, gamma, beta, running_mean, running_var, g.eps, g.norm, g.OC, scale, shift, st));
-  return run_fprop(g, dev, xsrc, bhi, blo, y, nullptr, scale, shift, 1, st);
+  return run_fprop(g, dev, xsrc, bhi, blo, y, nullptr, scale, shift, 1, nullptr, st);
 }
 
 int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const float* gamma, const float* beta,

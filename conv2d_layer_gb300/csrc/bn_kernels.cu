@@ -10,8 +10,9 @@
 // is different from those kernels: NHWC rows are read with 16-byte vector
 // loads, a thread keeps a fixed group of channels for its whole walk, and
 // each block writes one partial per channel that a small finalize kernel
-// merges in double in a fixed order (deterministic). The variance is a
-// shifted single pass merged with Chan's formula, not E[x^2] - mean^2.
+// merges in double in a fixed order (deterministic). The batch variance is
+// merged from per-tile two-pass (mean, M2) with Chan's formula, never
+// E[x^2] - mean^2.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include "kernels.h"
@@ -93,75 +94,9 @@ __device__ __forceinline__ Lane lane_of(long rows, int Cw, int EC, long rpb) {
   return l;
 }
 
-__device__ __forceinline__ void chan_merge(float& na, float& ma, float& Ma, float nb, float mb, float Mb) {
-  const float n = na + nb;
-  if (nb == 0.f) return;
-  if (na == 0.f) {
-    na = nb; ma = mb; Ma = Mb;
-    return;
-  }
-  const float d = mb - ma;
-  ma = ma + d * (nb / n);
-  Ma = Ma + Mb + d * d * (na * nb / n);
-  na = n;
-}
-
 // ------------------------------------------------------------ BN statistics
-template <typename T, int EC>
-__global__ void __launch_bounds__(kBlock) bn_stats_kernel(const T* __restrict__ pre, long rows, int C, long rpb,
-                                                          float* __restrict__ part) {
-  __shared__ float s_n[kBlock], s_m[kBlock * EC], s_M[kBlock * EC];
-  const Lane l = lane_of(rows, C, EC, rpb);
-  for (int gb = 0; gb < l.cg; gb += l.tpr) {
-    const int g = gb + l.g0;
-    const bool active = g < l.cg && l.rl < l.rpp;
-    float shift[EC], s1[EC], s2[EC];
-    int cnt = 0;
-#pragma unroll
-    for (int e = 0; e < EC; ++e) shift[e] = s1[e] = s2[e] = 0.f;
-    if (active) {
-      for (long r = l.r0 + l.rl; r < l.r1; r += l.rpp) {
-        float v[EC];
-        load_v<EC>(pre + r * C + g * EC, v);
-        if (cnt == 0) {
-#pragma unroll
-          for (int e = 0; e < EC; ++e) shift[e] = v[e];
-        }
-#pragma unroll
-        for (int e = 0; e < EC; ++e) {
-          const float d = v[e] - shift[e];
-          s1[e] += d;
-          s2[e] = fmaf(d, d, s2[e]);
-        }
-        ++cnt;
-      }
-    }
-    s_n[threadIdx.x] = static_cast<float>(cnt);
-#pragma unroll
-    for (int e = 0; e < EC; ++e) {
-      const float fc = cnt > 0 ? static_cast<float>(cnt) : 1.f;
-      s_m[threadIdx.x * EC + e] = shift[e] + s1[e] / fc;
-      s_M[threadIdx.x * EC + e] = fmaxf(s2[e] - s1[e] * (s1[e] / fc), 0.f);
-    }
-    __syncthreads();
-    if (active && l.rl == 0) {
-      for (int e = 0; e < EC; ++e) {
-        float n = 0.f, m = 0.f, M = 0.f;
-        for (int k = 0; k < l.rpp; ++k) {
-          const int src = k * l.tpr + l.g0;
-          chan_merge(n, m, M, s_n[src], s_m[src * EC + e], s_M[src * EC + e]);
-        }
-        const int c = g * EC + e;
-        float* o = part + (static_cast<size_t>(blockIdx.x) * C + c) * 3;
-        o[0] = n;
-        o[1] = m;
-        o[2] = M;
-      }
-    }
-    __syncthreads();
-  }
-}
-
+// Chan merge, in double and in a fixed order, of per-tile (count, mean, M2)
+// partials [G][C][3] written by the fprop GEMM epilogue.
 __global__ void __launch_bounds__(128) bn_stats_finalize_kernel(const float* __restrict__ part, int G, int C,
                                                                 float eps, float momentum, float* mean,
                                                                 float* inv_std, float* rm, float* rv) {
@@ -579,15 +514,6 @@ cudaError_t launch_prep_dgrad_weights(int dtype, const void* w, void* bhi, float
   else
     prep_dgrad_weights_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(w), static_cast<float*>(bhi), blo,
                                                         OC, KH, KW, IC, ICp, OCp, S, Kd, t);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_bn_stats(int dtype, const void* pre, const RowWalk& wk, float* part, cudaStream_t st) {
-  DISPATCH_EC(dtype, wk.C,
-              (bn_stats_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), wk.rows, wk.C,
-                                                                 wk.rows_per_block, part)),
-              (bn_stats_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), wk.rows, wk.C,
-                                                                 wk.rows_per_block, part)));
   return cudaGetLastError();
 }
 

@@ -85,7 +85,8 @@ struct ConvGemmParams {
   int out_ld, Ho, Wo, os;
   const float* ep_scale;  // optional per-column scale
   const float* ep_shift;  // optional per-column shift
-  int act, out_act;       // out = out_act ? act(v) : v
+  int act, out_act;       // out = out_act ? act(v) : T(v); out2 = act(T(v))
+  float* stats;           // optional per-tile batch statistics [m_tile][N][3] = (count, mean, M2) of T(v)
   int stages;
   int* err;
   ConvPhase ph[kMaxPhases];
@@ -116,6 +117,42 @@ __device__ __forceinline__ const ConvPhase& find_phase(const ConvGemmParams& p, 
   int i = 0;
   while (i + 1 < p.num_phases && p.ph[i + 1].unit_begin <= u) ++i;
   return p.ph[i];
+}
+
+// Value as stored in T (bf16: round to nearest even; fp32: unchanged).
+template <typename T>
+__device__ __forceinline__ float to_stored(float v);
+template <>
+__device__ __forceinline__ float to_stored<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ float to_stored<__nv_bfloat16>(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// Column sums of a 32-row x 16-column block held one row per lane: a
+// butterfly that halves the columns each lane keeps at every step. Afterwards
+// x[0] of lane L is the sum over all 32 lanes of column colsum16_col(L).
+template <int W, int O>
+__device__ __forceinline__ void colsum_step(float (&x)[16], int lane) {
+  const bool up = (lane & O) != 0;
+#pragma unroll
+  for (int e = 0; e < W / 2; ++e) {
+    const float send = up ? x[e] : x[e + W / 2];
+    const float keep = up ? x[e + W / 2] : x[e];
+    x[e] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+  }
+}
+__device__ __forceinline__ void colsum16(float (&x)[16], int lane) {
+  colsum_step<16, 16>(x, lane);
+  colsum_step<8, 8>(x, lane);
+  colsum_step<4, 4>(x, lane);
+  colsum_step<2, 2>(x, lane);
+  x[0] += __shfl_xor_sync(0xffffffffu, x[0], 1);
+}
+__device__ __forceinline__ int colsum16_col(int lane) {
+  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
 }
 
 template <typename T>
@@ -360,20 +397,27 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     // ------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
+    const int et = threadIdx.x - 192;  // 0..127 within the epilogue warps
     T* out = static_cast<T*>(p.out);
     T* out2 = static_cast<T*>(p.out2);
     const bool vec = (p.out_ld % D::EC) == 0;
+    // batch-statistics scratch: per-warp column sums (two passes) and tile means
+    float* red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16);
+    float* red2 = red + 4 * BN;
+    float* tmean = red2 + 4 * BN;
     int tc = 0;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tc) {
       const ConvPhase& ph = find_phase(p, u);
       const int local = u - ph.unit_begin;
       const int m_tile = local / p.n_tiles, n_tile = local % p.n_tiles;
       const int buf = tc & 1;
-      // lane 0 waits, the warp follows: the tcgen05.ld below is warp-aligned, so
-      // control flow must stay uniform even when the wait gives up
+      // lane 0 of each warp waits; the four warps agree before anyone goes on,
+      // so the warp-aligned tcgen05.ld and the named barriers below stay
+      // uniform even when a wait gives up
       int ok = 1;
       if (lane == 0) ok = wait(&tfull[buf], (tc >> 1) & 1, p.err, kSiteTFull) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!named_bar_and(1, 128, ok)) break;
       tc_fence_after();
       const int m = m_tile * kBM + row;
       const bool valid = m < ph.rows;
@@ -387,14 +431,12 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         obase = (static_cast<size_t>(n * p.Ho + oh) * p.Wo + ow) * p.out_ld;
       }
       const bool zero = ph.num_kb == 0;
-      for (int c0 = 0; c0 < BN; c0 += 16) {
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+      auto load16 = [&](int c0, float (&v)[16]) {
         uint32_t r[16];
-        tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c0, r);
+        tmem_ld16(taddr + c0, r);
         tmem_ld_wait(r);
         const int col0 = n_tile * BN + c0;
-        const int ncols = p.N - col0;
-        if (!valid || ncols <= 0) continue;
-        float v[16], w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int col = col0 + e;
@@ -403,11 +445,59 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
             if (p.ep_scale) x *= __ldg(p.ep_scale + col);
             if (p.ep_shift) x += __ldg(p.ep_shift + col);
           }
-          v[e] = p.out_act ? act_f(p.act, x) : x;
-          w[e] = act_f(p.act, x);
+          v[e] = x;
         }
-        store_row16<T>(out + obase + col0, v, ncols, vec);
-        if (out2) store_row16<T>(out2 + obase + col0, w, ncols, vec);
+      };
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16];
+        load16(c0, v);
+        const int col0 = n_tile * BN + c0;
+        const int ncols = p.N - col0;
+        if (ncols <= 0) continue;  // uniform across the warp
+        float o[16], w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float vs = to_stored<T>(v[e]);
+          o[e] = p.out_act ? act_f(p.act, v[e]) : vs;
+          w[e] = out2 ? act_f(p.act, vs) : 0.f;
+          v[e] = (valid && e < ncols) ? vs : 0.f;
+        }
+        if (valid) {
+          store_row16<T>(out + obase + col0, o, ncols, vec);
+          if (out2) store_row16<T>(out2 + obase + col0, w, ncols, vec);
+        }
+        if (p.stats) {
+          colsum16(v, lane);
+          if ((lane & 1) == 0) red[q * BN + c0 + colsum16_col(lane)] = v[0];
+        }
+      }
+      if (p.stats) {
+        // two passes over the tile: mean from the column sums, then the sum of
+        // squared deviations from that mean (TMEM is read a second time)
+        const int cnt = min(kBM, ph.rows - m_tile * kBM);
+        const int cols = min(BN, p.N - n_tile * BN);
+        named_bar_sync(1, 128);
+        for (int c = et; c < cols; c += 128)
+          tmean[c] = (red[c] + red[BN + c] + red[2 * BN + c] + red[3 * BN + c]) / static_cast<float>(cnt);
+        named_bar_sync(1, 128);
+        for (int c0 = 0; c0 < cols; c0 += 16) {
+          float v[16];
+          load16(c0, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float d = (valid && c0 + e < cols) ? to_stored<T>(v[e]) - tmean[c0 + e] : 0.f;
+            v[e] = d * d;
+          }
+          colsum16(v, lane);
+          if ((lane & 1) == 0) red2[q * BN + c0 + colsum16_col(lane)] = v[0];
+        }
+        named_bar_sync(1, 128);
+        for (int c = et; c < cols; c += 128) {
+          float* o = p.stats + (static_cast<size_t>(m_tile) * p.N + n_tile * BN + c) * 3;
+          o[0] = static_cast<float>(cnt);
+          o[1] = tmean[c];
+          o[2] = red2[c] + red2[BN + c] + red2[2 * BN + c] + red2[3 * BN + c];
+        }
       }
       tc_fence_before();
       __syncwarp();

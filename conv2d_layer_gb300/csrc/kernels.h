@@ -36,7 +36,6 @@ cudaError_t launch_prep_fprop_weights(int dtype, const void* w, void* bhi, float
 cudaError_t launch_prep_dgrad_weights(int dtype, const void* w, void* bhi, float* blo, int OC, int KH, int KW,
                                       int IC, int ICp, int OCp, int S, int Kd, const DgradWeightTable& t,
                                       cudaStream_t st);
-cudaError_t launch_bn_stats(int dtype, const void* pre, const RowWalk& wk, float* part, cudaStream_t st);
 cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float eps, float momentum, float* mean,
                                      float* inv_std, float* rm, float* rv, cudaStream_t st);
 cudaError_t launch_bn_apply(int dtype, const void* pre, void* y, const RowWalk& wk, const float* mean,

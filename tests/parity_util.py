@@ -31,8 +31,10 @@ def rel_err(a, ref):
 
 
 def oracle_layer(spec):
+    """Oracle layer with the pre-activations stored in the layer's element type, as the pages do."""
     return oracle.Layer(spec.N, spec.H, spec.W, spec.IC, spec.OC, spec.KH, spec.KW, spec.stride, spec.pad,
-                        norm=spec.norm, act=spec.act, eps=spec.eps, momentum=spec.momentum)
+                        norm=spec.norm, act=spec.act, eps=spec.eps, momentum=spec.momentum,
+                        store="bf16" if spec.dtype == BF16 else "f32")
 
 
 def run_pair(spec, inp, prev_grads=False, need_dx=True, need_params=True, seed=0):
