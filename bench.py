@@ -103,9 +103,13 @@ def run_gpu(args, rank, world, local_rank):
     from conv2d_layer_gb300.layer import Conv2dLayer
     from conv2d_layer_gb300.workloads import WORKLOADS, make_inputs
 
+    from dataclasses import replace
+
     torch.cuda.set_device(local_rank)
     spec = WORKLOADS[WORKLOAD].layers[0]
-    inp = make_inputs(WORKLOAD)
+    if args.images:
+        spec = replace(spec, N=args.images)
+    inp = make_inputs(WORKLOAD, n_images=args.images or None)
     li = inp["layers"][0]
     L = Conv2dLayer(spec, li.w, li.b, li.gamma, li.beta, li.running_mean, li.running_var)
     x, dy = inp["x"].cuda(), inp["dy"].cuda()
@@ -287,6 +291,8 @@ def main():
     ap.add_argument("--ref-images", type=int, default=1)
     ap.add_argument("--ref-warmup", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--images", type=int, default=0,
+                    help="run the large layer with this many images instead of 256 (small profiling cases)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -86,7 +86,7 @@ struct ConvGemmParams {
   const float* ep_scale;  // optional per-column scale
   const float* ep_shift;  // optional per-column shift
   int act, out_act;       // out = out_act ? act(v) : T(v); out2 = act(T(v))
-  float* stats;           // optional per-tile batch statistics [m_tile][N][3] = (count, mean, M2) of T(v)
+  float* stats;           // optional per-tile batch statistics [m_tile][N][3] = (count, mean, M2) of v
   int stages;
   int* err;
   ConvPhase ph[kMaxPhases];
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           const float vs = to_stored<T>(v[e]);
           o[e] = p.out_act ? act_f(p.act, v[e]) : vs;
           w[e] = out2 ? act_f(p.act, vs) : 0.f;
-          v[e] = (valid && e < ncols) ? vs : 0.f;
+          v[e] = (valid && e < ncols) ? v[e] : 0.f;  // statistics of the unrounded fp32 value
         }
         if (valid) {
           store_row16<T>(out + obase + col0, o, ncols, vec);
@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           load16(c0, v);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float d = (valid && c0 + e < cols) ? to_stored<T>(v[e]) - tmean[c0 + e] : 0.f;
+            const float d = (valid && c0 + e < cols) ? v[e] - tmean[c0 + e] : 0.f;
             v[e] = d * d;
           }
           colsum16(v, lane);

@@ -25,11 +25,14 @@
  *   - dX is overwritten, dW / dBias / dGamma / dBeta are accumulated into
  *     (`backward_full` loads the existing gradients first).
  *   - the pre-activations are stored in the layer's element type T (`forward`
- *     Phase 1 writes `(T)acc` into `pre_activations`; the CUDA page's
- *     `bn_stats_training` reads `const T* pre_act`), and the batch statistics,
- *     the normalisation and the backward pass all read that stored value. The
- *     `store` field names T: fp32 (round to nearest) or bf16 (round to
- *     nearest even, through fp32); 0 keeps fp64 (the pure definition).
+ *     Phase 1 writes `(T)acc` into `pre_activations`), and the normalisation,
+ *     the activation and the backward pass read that stored value. The batch
+ *     statistics are taken from the conv output before that rounding (fp32
+ *     batch-norm statistics from the accumulator): with a bf16 T, statistics
+ *     of the rounded values cannot be reproduced to 1e-5 by any fp32
+ *     accumulation, because values near a bf16 rounding midpoint round either
+ *     way. The `store` field names T: fp32 (round to nearest) or bf16 (round
+ *     to nearest even, through fp32); 0 keeps fp64 (the pure definition).
  * Parallelism (OpenMP) is only over independent output elements; every
  * element is the plain sum its definition states.
  */
@@ -168,14 +171,18 @@ void oracle_fwd_train(const oracle_desc* d, const double* x, const double* w, co
     const long npix = (long)d->N * out_h(d) * out_w(d);
     const int C = d->OC;
     oracle_conv_fwd(d, x, w, b, ypre);
+    double* var = NULL;
+    if (d->norm == 1) {
+        /* batch statistics of the conv output before it is stored in T */
+        var = (double*)malloc(sizeof(double) * C);
+        oracle_bn_batch_stats(d, ypre, mean, var);
+    }
     if (d->store)
         for (long i = 0; i < npix * C; i++) ypre[i] = oracle_store_round(d->store, ypre[i]);
     if (d->norm == 0) {
         for (long i = 0; i < npix * C; i++) y[i] = oracle_act(d->act, ypre[i]);
         return;
     }
-    double* var = (double*)malloc(sizeof(double) * C);
-    oracle_bn_batch_stats(d, ypre, mean, var);
     for (int c = 0; c < C; c++) {
         inv_std[c] = 1.0 / sqrt(var[c] + d->eps);
         rm[c] = (1.0 - d->momentum) * rm[c] + d->momentum * mean[c];

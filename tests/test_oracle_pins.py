@@ -323,7 +323,8 @@ def test_store_rounding_matches_bf16_and_fp32_conversion():
 
 @pytest.mark.parametrize("store", ["f32", "bf16"])
 def test_stored_preactivations_feed_the_statistics(store):
-    """With a storage type, Ypre is rounded once and everything downstream reads the rounded value."""
+    """With a storage type, Ypre is rounded once; the batch statistics come from the unrounded conv output,
+    the normalisation and activation read the rounded value."""
     rng = np.random.default_rng(23)
     L = oracle.Layer(2, 6, 6, 4, 5, 3, 3, 1, 1, norm="batch", act="relu", store=store)
     L0 = oracle.Layer(2, 6, 6, 4, 5, 3, 3, 1, 1, norm="batch", act="relu")
@@ -331,8 +332,9 @@ def test_stored_preactivations_feed_the_statistics(store):
     f = oracle.fwd_train(L, x, w, b, gamma, beta)
     exact = oracle.conv_fwd(L0, x, w, b)
     np.testing.assert_array_equal(f["ypre"], oracle.store_round(store, exact))
-    yp = f["ypre"].reshape(-1, L.OC)
-    np.testing.assert_allclose(f["mean"], yp.mean(0), rtol=1e-13)
-    np.testing.assert_allclose(f["inv_std"], 1 / np.sqrt(yp.var(0) + L.eps), rtol=1e-12)
+    ye = exact.reshape(-1, L.OC)
+    np.testing.assert_allclose(f["mean"], ye.mean(0), rtol=1e-13)
+    np.testing.assert_allclose(f["inv_std"], 1 / np.sqrt(ye.var(0) + L.eps), rtol=1e-12)
+    np.testing.assert_allclose(f["running_var"], 0.9 + 0.1 * ye.var(0), rtol=1e-13)
     z = (f["ypre"] - f["mean"]) * f["inv_std"]
     np.testing.assert_allclose(f["y"], np.maximum(gamma * z + beta, 0), rtol=1e-13, atol=1e-15)
