@@ -213,7 +213,7 @@ Tile conv_tile(const Geo& g, int ncols) {
   t.BN = static_cast<int>(round_up(ceil_div(ncols, t.n_tiles), 16));
   const size_t ns = g.dt == CONV2D_BF16 ? 1 : 2;
   const size_t stage = ns * (kBM * 128 + static_cast<size_t>(t.BN) * 128);
-  const size_t stats = 9 * static_cast<size_t>(t.BN) * 4;  // epilogue batch-statistics scratch
+  const size_t stats = 11 * static_cast<size_t>(t.BN) * 4;  // epilogue statistics scratch + column constants
   t.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048 - stats) / stage));
   t.smem = t.stages * stage + 1024 + 256 + stats;
   return t;
@@ -425,6 +425,7 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   p.stats = stats;
   p.stages = t.stages;
   p.err = dev->err;
+  if (bf && t.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
   const int grid = std::min(p.num_units, dev->sms);
   LAUNCH("fprop_gemm", st, bf ? launch_conv_gemm_bf16(p, grid, t.smem, st) : launch_conv_gemm_tf32(p, grid, t.smem, st));
   return CONV2D_OK;
@@ -469,6 +470,7 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
   p.out_act = 0;
   p.stages = d.tile.stages;
   p.err = dev->err;
+  if (bf && d.tile.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
   const int grid = std::min(p.num_units, dev->sms);
   LAUNCH("dgrad_gemm", st,
          bf ? launch_conv_gemm_bf16(p, grid, d.tile.smem, st) : launch_conv_gemm_tf32(p, grid, d.tile.smem, st));
@@ -510,6 +512,7 @@ int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dc
   p.partial = reinterpret_cast<float*>(region(ws, pl, R_WPART));
   p.stages = w.stages;
   p.err = dev->err;
+  if (bf && w.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
   const int grid = std::min(p.num_units, dev->sms);
   LAUNCH("wgrad_gemm", st,
          bf ? launch_wgrad_gemm_bf16(p, grid, w.smem, st) : launch_wgrad_gemm_tf32(p, grid, w.smem, st));

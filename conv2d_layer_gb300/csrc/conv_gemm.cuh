@@ -34,7 +34,7 @@ constexpr int kThreads = 320;
 constexpr int kMaxStages = 8;
 constexpr int kMaxPhases = 64;
 constexpr int kBM = 128;          // rows of a tile (TMEM lanes)
-constexpr int kLag = 2;           // cp.async groups kept in flight per producer thread
+constexpr int kLag = 3;           // cp.async groups kept in flight per producer thread (needs >= 4 stages)
 
 // wait sites recorded in the error word
 enum : int { kSiteFull = 1, kSiteEmpty = 2, kSiteTFull = 3, kSiteTEmpty = 4 };
@@ -405,6 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     float* red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16);
     float* red2 = red + 4 * BN;
     float* tmean = red2 + 4 * BN;
+    // per-column epilogue constants of the current column tile
+    float* sc_s = tmean + BN;
+    float* sh_s = sc_s + BN;
+    int cur_n_tile = -1;
     int tc = 0;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tc) {
       const ConvPhase& ph = find_phase(p, u);
@@ -414,6 +418,16 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       // lane 0 of each warp waits; the four warps agree before anyone goes on,
       // so the warp-aligned tcgen05.ld and the named barriers below stay
       // uniform even when a wait gives up
+      if (n_tile != cur_n_tile) {
+        // safe to overwrite: every epilogue thread has passed the previous
+        // unit's barrier below, after its last read of these arrays
+        for (int c = et; c < BN; c += 128) {
+          const int col = n_tile * BN + c;
+          sc_s[c] = (p.ep_scale && col < p.N) ? p.ep_scale[col] : 1.f;
+          sh_s[c] = (p.ep_shift && col < p.N) ? p.ep_shift[col] : 0.f;
+        }
+        cur_n_tile = n_tile;
+      }
       int ok = 1;
       if (lane == 0) ok = wait(&tfull[buf], (tc >> 1) & 1, p.err, kSiteTFull) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -436,16 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         uint32_t r[16];
         tmem_ld16(taddr + c0, r);
         tmem_ld_wait(r);
-        const int col0 = n_tile * BN + c0;
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int col = col0 + e;
-          float x = zero ? 0.f : __uint_as_float(r[e]);
-          if (col < p.N) {
-            if (p.ep_scale) x *= __ldg(p.ep_scale + col);
-            if (p.ep_shift) x += __ldg(p.ep_shift + col);
-          }
-          v[e] = x;
+          const float x = zero ? 0.f : __uint_as_float(r[e]);
+          v[e] = fmaf(x, sc_s[c0 + e], sh_s[c0 + e]);
         }
       };
       for (int c0 = 0; c0 < BN; c0 += 16) {

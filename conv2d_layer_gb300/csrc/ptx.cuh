@@ -49,18 +49,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete. On expiry (or
-// when another thread of the grid already reported an error) it records `site`
-// in *err (first error wins) and returns false.
+// Bounded wait for the phase with the given parity to complete. The fast path
+// is a plain poll of try_wait (which itself suspends the warp in hardware);
+// the clock is read only every 1024 polls. On expiry it records `site` in
+// *err (first error wins) and returns false.
 __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, int* err, int site) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*reinterpret_cast<volatile int*>(err) != 0) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
       atomicCAS(err, 0, site);
       return false;
     }
