@@ -210,7 +210,7 @@ Tile conv_tile(const Geo& g, int ncols) {
   Tile t;
   const int bn_max = g.dt == CONV2D_BF16 ? 256 : 128;
   t.n_tiles = static_cast<int>(ceil_div(ncols, bn_max));
-  t.BN = static_cast<int>(round_up(ceil_div(ncols, t.n_tiles), 16));
+  t.BN = static_cast<int>(round_up(ceil_div(ncols, t.n_tiles), 32));  // the epilogue reads 32 columns at a time
   const size_t ns = g.dt == CONV2D_BF16 ? 1 : 2;
   const size_t stage = ns * (kBM * 128 + static_cast<size_t>(t.BN) * 128);
   const size_t stats = 11 * static_cast<size_t>(t.BN) * 4;  // epilogue statistics scratch + column constants
@@ -234,7 +234,7 @@ WgradPlan wgrad_plan(const Geo& g, int sms) {
     w.BN = static_cast<int>(round_up(ceil_div(g.OC, w.n_tiles), 64));
   } else {
     w.n_tiles = static_cast<int>(ceil_div(g.OC, 128));
-    w.BN = static_cast<int>(round_up(ceil_div(g.OC, w.n_tiles), 16));
+    w.BN = static_cast<int>(round_up(ceil_div(g.OC, w.n_tiles), 32));
   }
   w.KP = bf ? 64 : 32;
   w.kb_total = static_cast<int>(ceil_div(g.n_pix, w.KP));

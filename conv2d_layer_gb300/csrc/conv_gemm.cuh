@@ -188,6 +188,31 @@ __device__ __forceinline__ void store_row16<float>(float* dst, const float* v, i
   }
 }
 
+template <typename T>
+__device__ __forceinline__ void store_row32(T* dst, const float (&v)[32], int ncols, bool vec) {
+  if (vec && ncols >= 32) {
+    if constexpr (sizeof(T) == 2) {
+      uint32_t w[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+        w[e] = *reinterpret_cast<uint32_t*>(&h);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        reinterpret_cast<uint4*>(dst)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        reinterpret_cast<float4*>(dst)[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (e < ncols) dst[e] = static_cast<T>(v[e]);
+  }
+}
+
 // --------------------------------------------------------------------------
 // fprop / dgrad
 // --------------------------------------------------------------------------
@@ -446,38 +471,47 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       }
       const bool zero = ph.num_kb == 0;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
-      auto load16 = [&](int c0, float (&v)[16]) {
-        uint32_t r[16];
-        tmem_ld16(taddr + c0, r);
-        tmem_ld_wait(r);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float x = zero ? 0.f : __uint_as_float(r[e]);
-          v[e] = fmaf(x, sc_s[c0 + e], sh_s[c0 + e]);
-        }
+      // columns are read from TMEM 64 at a time (two 32-column loads, one wait)
+      auto fetch = [&](int c0, uint32_t (&ra)[32], uint32_t (&rb)[32]) {
+        const int c1 = c0 + 32 < BN ? c0 + 32 : c0;
+        tmem_ld32(taddr + c0, ra);
+        tmem_ld32(taddr + c1, rb);
+        tmem_ld_wait2(ra, rb);
       };
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        float v[16];
-        load16(c0, v);
-        const int col0 = n_tile * BN + c0;
+      auto pass1 = [&](int cc, const uint32_t (&r)[32]) {
+        const int col0 = n_tile * BN + cc;
         const int ncols = p.N - col0;
-        if (ncols <= 0) continue;  // uniform across the warp
-        float o[16], w[16];
+        if (ncols <= 0) return;  // uniform across the warp
+        float v[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float vs = to_stored<T>(v[e]);
-          o[e] = p.out_act ? act_f(p.act, v[e]) : vs;
-          w[e] = out2 ? act_f(p.act, vs) : 0.f;
-          v[e] = (valid && e < ncols) ? v[e] : 0.f;  // statistics of the unrounded fp32 value
+        for (int e = 0; e < 32; ++e) v[e] = fmaf(zero ? 0.f : __uint_as_float(r[e]), sc_s[cc + e], sh_s[cc + e]);
+        if (p.stats) {  // statistics of the unrounded value
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float sv[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sv[e] = (valid && h * 16 + e < ncols) ? v[h * 16 + e] : 0.f;
+            colsum16(sv, lane);
+            if ((lane & 1) == 0) red[q * BN + cc + h * 16 + colsum16_col(lane)] = sv[0];
+          }
         }
         if (valid) {
-          store_row16<T>(out + obase + col0, o, ncols, vec);
-          if (out2) store_row16<T>(out2 + obase + col0, w, ncols, vec);
+          float o[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = p.out_act ? act_f(p.act, v[e]) : to_stored<T>(v[e]);
+          store_row32<T>(out + obase + col0, o, ncols, vec);
+          if (out2) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = act_f(p.act, to_stored<T>(v[e]));
+            store_row32<T>(out2 + obase + col0, o, ncols, vec);
+          }
         }
-        if (p.stats) {
-          colsum16(v, lane);
-          if ((lane & 1) == 0) red[q * BN + c0 + colsum16_col(lane)] = v[0];
-        }
+      };
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        uint32_t ra[32], rb[32];
+        fetch(c0, ra, rb);
+        pass1(c0, ra);
+        if (c0 + 32 < BN) pass1(c0 + 32, rb);
       }
       if (p.stats) {
         // two passes over the tile: mean from the column sums, then the sum of
@@ -488,16 +522,27 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         for (int c = et; c < cols; c += 128)
           tmean[c] = (red[c] + red[BN + c] + red[2 * BN + c] + red[3 * BN + c]) / static_cast<float>(cnt);
         named_bar_sync(1, 128);
-        for (int c0 = 0; c0 < cols; c0 += 16) {
-          float v[16];
-          load16(c0, v);
+        auto pass2 = [&](int cc, const uint32_t (&r)[32]) {
+          if (cc >= cols) return;  // uniform
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float d = (valid && c0 + e < cols) ? v[e] - tmean[c0 + e] : 0.f;
-            v[e] = d * d;
+          for (int h = 0; h < 2; ++h) {
+            float sv[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int c = cc + h * 16 + e;
+              const float x = fmaf(zero ? 0.f : __uint_as_float(r[h * 16 + e]), sc_s[c], sh_s[c]);
+              const float d = (valid && c < cols) ? x - tmean[c] : 0.f;
+              sv[e] = d * d;
+            }
+            colsum16(sv, lane);
+            if ((lane & 1) == 0) red2[q * BN + cc + h * 16 + colsum16_col(lane)] = sv[0];
           }
-          colsum16(v, lane);
-          if ((lane & 1) == 0) red2[q * BN + c0 + colsum16_col(lane)] = v[0];
+        };
+        for (int c0 = 0; c0 < cols; c0 += 64) {
+          uint32_t ra[32], rb[32];
+          fetch(c0, ra, rb);
+          pass2(c0, ra);
+          if (c0 + 32 < BN) pass2(c0 + 32, rb);
         }
         named_bar_sync(1, 128);
         for (int c = et; c < cols; c += 128) {
@@ -658,41 +703,50 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
     bool alive = true;
     if (DT == 1) {
       // ------------------------------------------------ A producer, bf16, MN-major
-      // smem A: two panels (k 0-63, 64-127) of [64 pixel rows][128 B]
-      const int qc = t & 15, panel = qc >> 3, jj = qc & 7, r0 = t >> 4;
-      const uint32_t swz = static_cast<uint32_t>((jj ^ (r0 & 7)) << 4);
+      // smem A: two panels (k 0-63, 64-127) of [64 pixel rows][128 B]. Thread
+      // pair (2r, 2r+1) owns pixel row r and copies its 16-byte chunks
+      // q = 2j + (t & 1), j = 0..7: adjacent lanes read adjacent chunks.
+      const int r = t >> 1, half = t & 1;
       for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
         int m_tile, n_tile, kb0, kb1;
         decode(u, m_tile, n_tile, kb0, kb1);
-        const int kc = m_tile * kBM + qc * 8;
-        const bool okc = kc < p.Mk;
-        const int tap = static_cast<int>(fdiv(static_cast<uint32_t>(kc), p.div_Cs));
-        const int c = kc - tap * p.Cs;
-        const int kh = static_cast<int>(fdiv(static_cast<uint32_t>(tap), p.div_KW));
-        const int dh = kh - p.P, dw = (tap - kh * p.KW) - p.P;
+        int dh[8], dw[8], cofs[8];
+        uint32_t dsto[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int q = 2 * j + half;
+          const int kc = m_tile * kBM + q * 8;
+          const int tap = static_cast<int>(fdiv(static_cast<uint32_t>(kc), p.div_Cs));
+          const int kh = static_cast<int>(fdiv(static_cast<uint32_t>(tap), p.div_KW));
+          cofs[j] = kc - tap * p.Cs;
+          dh[j] = kc < p.Mk ? kh - p.P : -(1 << 28);  // k padding rows read as zero
+          dw[j] = (tap - kh * p.KW) - p.P;
+          dsto[j] = static_cast<uint32_t>((q >> 3) * 8192 + r * 128 + (((q & 7) ^ (r & 7)) << 4));
+        }
         for (int kb = kb0; kb < kb1; ++kb) {
+          const int pix = kb * KP + r;
+          const bool okp = pix < p.n_pix;
+          int n = 0, oh = 0, ow = 0;
+          if (okp) {
+            n = static_cast<int>(fdiv(static_cast<uint32_t>(pix), p.div_OHOW));
+            const int rem = pix - n * p.OH * p.OW;
+            oh = static_cast<int>(fdiv(static_cast<uint32_t>(rem), p.div_OW));
+            ow = rem - oh * p.OW;
+          }
+          const int ih0 = oh * p.S, iw0 = ow * p.S;
+          const size_t img = static_cast<size_t>(n) * p.H;
           if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
             alive = false;
             break;
           }
-          const uint32_t a0 = sbase + s * stage_bytes + panel * 8192;
+          const uint32_t a0 = sbase + s * stage_bytes;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = r0 + 8 * i;
-            const int pix = kb * KP + r;
-            bool ok = okc && pix < p.n_pix;
-            size_t off = 0;
-            if (ok) {
-              const int n = static_cast<int>(fdiv(static_cast<uint32_t>(pix), p.div_OHOW));
-              const int rem = pix - n * p.OH * p.OW;
-              const int oh = static_cast<int>(fdiv(static_cast<uint32_t>(rem), p.div_OW));
-              const int ow = rem - oh * p.OW;
-              const int ih = oh * p.S + dh, iw = ow * p.S + dw;
-              ok = static_cast<unsigned>(ih) < static_cast<unsigned>(p.H) &&
-                   static_cast<unsigned>(iw) < static_cast<unsigned>(p.W);
-              if (ok) off = ((static_cast<size_t>(n * p.H + ih) * p.W + iw) * p.Cs + c) * 2;
-            }
-            cp_async16(a0 + r * 128 + swz, xs + off, ok ? 16u : 0u);
+          for (int j = 0; j < 8; ++j) {
+            const int ih = ih0 + dh[j], iw = iw0 + dw[j];
+            const bool ok = okp && static_cast<unsigned>(ih) < static_cast<unsigned>(p.H) &&
+                            static_cast<unsigned>(iw) < static_cast<unsigned>(p.W);
+            const size_t off = ok ? (((img + ih) * p.W + iw) * p.Cs + cofs[j]) * 2 : 0;
+            cp_async16(a0 + dsto[j], xs + off, ok ? 16u : 0u);
           }
           cp_async_commit();
           if (it >= kLag) {
@@ -815,17 +869,22 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
       tc_fence_after();
       const int m = m_tile * kBM + row;
       const bool zero = kb1 <= kb0;
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c0, r);
-        tmem_ld_wait(r);
-        if (m >= p.Mk) continue;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+      auto put = [&](int cc, const uint32_t (&r)[32]) {
+        if (m >= p.Mk) return;
+        float* dst = p.partial + (static_cast<size_t>(split) * p.N + n_tile * BN + cc) * p.Mk + m;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int col = n_tile * BN + c0 + e;
-          if (col < p.N)
-            p.partial[(static_cast<size_t>(split) * p.N + col) * p.Mk + m] = zero ? 0.f : __uint_as_float(r[e]);
-        }
+        for (int e = 0; e < 32; ++e)
+          if (n_tile * BN + cc + e < p.N) dst[static_cast<size_t>(e) * p.Mk] = zero ? 0.f : __uint_as_float(r[e]);
+      };
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        uint32_t ra[32], rb[32];
+        const int c1 = c0 + 32 < BN ? c0 + 32 : c0;
+        tmem_ld32(taddr + c0, ra);
+        tmem_ld32(taddr + c1, rb);
+        tmem_ld_wait2(ra, rb);
+        put(c0, ra);
+        if (c0 + 32 < BN) put(c0 + 32, rb);
       }
       tc_fence_before();
       __syncwarp();
