@@ -102,14 +102,16 @@ __global__ void __launch_bounds__(128) bn_stats_finalize_kernel(const float* __r
                                                                 float* inv_std, float* rm, float* rv) {
   __shared__ double s_n[128], s_m[128], s_M[128];
   const int c = blockIdx.x;
-  double n = 0, m = 0, M = 0;
+  // each thread merges its share in fp32 (GB300's fp64 rate is low); the
+  // 128-way tree below runs in fp64
+  float n = 0.f, m = 0.f, M = 0.f;
   for (int b = threadIdx.x; b < G; b += 128) {
     const float* p = part + (static_cast<size_t>(b) * C + c) * 3;
-    const double nb = p[0], mb = p[1], Mb = p[2];
-    if (nb == 0) continue;
-    const double nn = n + nb, d = mb - m;
-    m += d * nb / nn;
-    M += Mb + d * d * n * nb / nn;
+    const float nb = p[0], mb = p[1], Mb = p[2];
+    if (nb == 0.f) continue;
+    const float nn = n + nb, d = mb - m, f = nb / nn;
+    m = fmaf(d, f, m);
+    M += Mb + d * d * n * f;
     n = nn;
   }
   s_n[threadIdx.x] = n;
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(128) sum_finalize_kernel(const float* __restri
                                                            int mode, float* c12, float* acc0, float* acc1) {
   __shared__ double s[2][128];
   const int c = blockIdx.x;
-  double a = 0, b = 0;
+  float a = 0.f, b = 0.f;
   for (int k = threadIdx.x; k < G; k += 128) {
     const float* p = part + (static_cast<size_t>(k) * C + c) * nv;
     a += p[0];
