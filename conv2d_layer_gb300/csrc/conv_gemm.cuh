@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 128 + 1);
+      mbar_init(&full[s], 4 + 1);  // one arrival per producer warp + the TMA thread
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         const int tt = static_cast<int>(fdiv(static_cast<uint32_t>(tap), ph.div_Tw));
         const int dh = p.tap_sign * tt;
         const int dw = p.tap_sign * (tap - tt * ph.Tw);
-        if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
+        if (!__all_sync(0xffffffffu, wait(&empty[s], par ^ 1, p.err, kSiteEmpty))) {  // warp-uniform
           alive = false;
           break;
         }
@@ -399,11 +399,13 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           if (it >= kLag) {
             cp_async_wait<kLag>();
             fence_proxy_async_smem();
-            mbar_arrive(&full[(it - kLag) % S]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[(it - kLag) % S]);
           }
         } else {
           fence_proxy_async_smem();
-          mbar_arrive(&full[s]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[s]);
         }
         ++it;
         if (++s == S) {
@@ -415,7 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     if (DT == 1) {
       cp_async_wait<0>();
       fence_proxy_async_smem();
-      if (alive)
+      __syncwarp();
+      if (alive && lane == 0)
         for (int q = (it > kLag ? it - kLag : 0); q < it; ++q) mbar_arrive(&full[q % S]);
     }
   } else {
@@ -591,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], DT == 1 ? 128 + 1 : 128);
+      mbar_init(&full[s], DT == 1 ? 4 + 1 : 4);  // one arrival per producer warp (+ the TMA thread)
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -735,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
           }
           const int ih0 = oh * p.S, iw0 = ow * p.S;
           const size_t img = static_cast<size_t>(n) * p.H;
-          if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
+          if (!__all_sync(0xffffffffu, wait(&empty[s], par ^ 1, p.err, kSiteEmpty))) {  // warp-uniform
             alive = false;
             break;
           }
@@ -752,7 +755,8 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
           if (it >= kLag) {
             cp_async_wait<kLag>();
             fence_proxy_async_smem();
-            mbar_arrive(&full[(it - kLag) % S]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[(it - kLag) % S]);
           }
           ++it;
           if (++s == S) {
@@ -763,7 +767,8 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
       }
       cp_async_wait<0>();
       fence_proxy_async_smem();
-      if (alive)
+      __syncwarp();
+      if (alive && lane == 0)
         for (int q2 = (it > kLag ? it - kLag : 0); q2 < it; ++q2) mbar_arrive(&full[q2 % S]);
     } else {
       // ------------------------------------------------ A and B producers, fp32 -> tf32 hi/lo, K-major
@@ -806,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
               av[i] = __ldg(reinterpret_cast<const float4*>(
                   xs + ((static_cast<size_t>(n * p.H + ih) * p.W + iw) * p.Cs + cs[i]) * 4));
           }
-          if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
+          if (!__all_sync(0xffffffffu, wait(&empty[s], par ^ 1, p.err, kSiteEmpty))) {  // warp-uniform
             alive = false;
             break;
           }
@@ -843,7 +848,8 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
             }
           }
           fence_proxy_async_smem();
-          mbar_arrive(&full[s]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[s]);
           if (++s == S) {
             s = 0;
             par ^= 1;
