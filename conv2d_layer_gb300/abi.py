@@ -21,6 +21,7 @@ OP_FWD_TRAIN, OP_FWD_INFER, OP_BWD = 0, 1, 2
 EXPORTS = (
     "conv2d_out_hw", "conv2d_validate", "conv2d_workspace_size", "conv2d_fwd_train", "conv2d_fwd_infer",
     "conv2d_bwd", "conv2d_device_status", "conv2d_status_str", "conv2d_prof_enable", "conv2d_prof_read",
+    "conv2d_fwd_train_noalloc",
 )
 
 
@@ -58,6 +59,7 @@ def lib():
     L.conv2d_workspace_size.argtypes = [pd, i32]
     L.conv2d_workspace_size.restype = sz
     L.conv2d_fwd_train.argtypes = [pd] + [vp] * 11 + [vp, sz, vp]
+    L.conv2d_fwd_train_noalloc.argtypes = [pd] + [vp] * 11 + [vp]
     L.conv2d_fwd_infer.argtypes = [pd] + [vp] * 8 + [vp, sz, vp]
     L.conv2d_bwd.argtypes = [pd] + [vp] * 13 + [vp, sz, vp]
     L.conv2d_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
@@ -121,6 +123,14 @@ def conv2d_fwd_train(d, x, w, bias, gamma, beta, running_mean, running_var, pre_
     return lib().conv2d_fwd_train(ctypes.byref(d), _ptr(x), _ptr(w), _ptr(bias), _ptr(gamma), _ptr(beta),
                                   _ptr(running_mean), _ptr(running_var), _ptr(pre_act), _ptr(save_mean),
                                   _ptr(save_inv_std), _ptr(y), _ptr(ws), ws_bytes, _stream(stream))
+
+
+def conv2d_fwd_train_noalloc(d, x, w, bias, gamma, beta, running_mean, running_var, pre_act, save_mean,
+                             save_inv_std, y, stream=None):
+    """conv2d_fwd_train with the library's static scratch instead of a caller workspace (no allocation)."""
+    return lib().conv2d_fwd_train_noalloc(ctypes.byref(d), _ptr(x), _ptr(w), _ptr(bias), _ptr(gamma), _ptr(beta),
+                                          _ptr(running_mean), _ptr(running_var), _ptr(pre_act), _ptr(save_mean),
+                                          _ptr(save_inv_std), _ptr(y), _stream(stream))
 
 
 def conv2d_fwd_infer(d, x, w, bias, gamma, beta, running_mean, running_var, y, ws, ws_bytes=None, stream=None):

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libconv2d.so")
-SOURCES = ["api.cu", "bn_kernels.cu", "gemm_bf16.cu", "gemm_tf32.cu"]
+SOURCES = ["api.cu", "bn_kernels.cu", "gemm_bf16.cu", "gemm_tf32.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

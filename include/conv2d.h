@@ -102,6 +102,26 @@ int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, cons
                      void* pre_act, float* save_mean, float* save_inv_std, void* y,
                      void* ws, size_t ws_bytes, void* stream);
 
+/* Training forward without a caller workspace. The pages have no counterpart
+ * of this call; it exists for callers that cannot allocate device memory: a
+ * process whose device memory is fixed at start-up and that may not allocate
+ * afterwards (cudaMalloc / cudaFree can synchronise the device and can fail
+ * mid-run), or code that is handed only the tensors it passes here and has
+ * no way to obtain a scratch buffer.
+ * Same arguments and results as conv2d_fwd_train minus ws / ws_bytes. Its
+ * scratch is one static 32 MiB device array inside the library (every GPU
+ * that loads the library holds it until the process exits). A spec whose
+ * conv2d_workspace_size(desc, CONV2D_OP_FWD_TRAIN) exceeds 32 MiB is refused
+ * with CONV2D_ERR_WORKSPACE before anything is launched. The first call on a
+ * device looks up the array's device address (with that device current);
+ * make that first call before any stream capture. All calls share the array
+ * and a call rewrites every scratch byte it reads, so nothing is cleared
+ * between calls, but calls that overlap on the GPU (several streams, several
+ * host threads) race on it: order them. */
+int conv2d_fwd_train_noalloc(const conv2d_desc* desc, const void* x, const void* w, const float* bias,
+                             const float* gamma, const float* beta, float* running_mean, float* running_var,
+                             void* pre_act, float* save_mean, float* save_inv_std, void* y, void* stream);
+
 /* Inference forward (`evaluate`): y = act(norm(conv + bias)), batch norm with
  * the running statistics (`bn_stats_eval` / `bn_forward_eval_running` on the
  * CUDA page); no state is written. gamma, beta, running_mean, running_var are
