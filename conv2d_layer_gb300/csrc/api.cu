@@ -146,6 +146,48 @@ bool encode_2d(CUtensorMap* m, const void* base, bool bf16, uint64_t cols, uint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+typedef CUresult (*EncodeIm2colFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const int*, const int*, cuuint32_t, cuuint32_t,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeIm2colFn encode_im2col_fn() {
+  static EncodeIm2colFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeIm2colFn>(p);
+  });
+  return fn;
+}
+
+// bf16 NHWC tensor [N][H][W][C] read by im2col TMA: boxes of `pixels` window
+// corners x 64 channels, 128-byte swizzle. The corner of output (y, x) is
+// (y*stride + lo_h, x*stride + lo_w); `up_h`, `up_w` place the last corner at
+// (H-1+up_h, W-1+up_w). Returns false when a corner offset is outside the
+// [-128, 127] range the 4-D form supports, or encoding fails.
+bool encode_im2col(CUtensorMap* m, const void* base, int N, int H, int W, int C, int lo_h, int lo_w, int up_h,
+                   int up_w, int stride, int pixels) {
+  EncodeIm2colFn fn = encode_im2col_fn();
+  if (!fn) return false;
+  for (int v : {lo_h, lo_w, up_h, up_w})
+    if (v < -128 || v > 127) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(N)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(C) * 2, static_cast<cuuint64_t>(W) * C * 2,
+                           static_cast<cuuint64_t>(H) * W * C * 2};
+  int lower[2] = {lo_w, lo_h};
+  int upper[2] = {up_w, up_h};
+  cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(stride), static_cast<cuuint32_t>(stride), 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, lower, upper, 64,
+            static_cast<cuuint32_t>(pixels), estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------ geometry
 long ceil_div(long a, long b) { return (a + b - 1) / b; }
 long round_up(long a, long b) { return ceil_div(a, b) * b; }
@@ -278,10 +320,14 @@ struct DgradPlan {
   Tile tile;
 };
 
+// dgrad through TMA im2col: stride 1, bf16, whole 64-channel chunks of d_conv.
+bool dgrad_tma(const Geo& g) { return g.dt == CONV2D_BF16 && g.S == 1 && g.OCp % 64 == 0; }
+
 DgradPlan dgrad_plan(const Geo& g) {
   DgradPlan d;
   std::memset(&d, 0, sizeof(d));
   d.tile = conv_tile(g, g.IC);
+  d.table.flip = dgrad_tma(g) ? 1 : 0;
   const int S = g.S;
   int unit = 0, col = 0, n = 0;
   for (int ph_h = 0; ph_h < S; ++ph_h)
@@ -423,6 +469,14 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   p.act = g.act;
   p.out_act = out_act;
   p.stats = stats;
+  if (bf && g.ICp % 64 == 0 &&
+      encode_im2col(&p.tmap_a, xsrc, g.N, g.H, g.W, g.ICp, -g.P, -g.P, (g.OH - 1) * g.S - g.P - (g.H - 1),
+                    (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, kBM)) {
+    p.a_tma = 1;
+    p.a_chunks = g.ICp / 64;
+    p.a_qh = -g.P;
+    p.a_qw = -g.P;
+  }
   p.stages = t.stages;
   p.err = dev->err;
   if (bf && t.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
@@ -468,6 +522,18 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
   p.os = g.S;
   p.act = 0;
   p.out_act = 0;
+  if (d.table.flip) {
+    // window corner of input pixel (ih, iw) in d_conv: (ih - (KH-1-P), iw - (KW-1-P)); tap offsets are the
+    // flipped kernel indices, matching the flipped weight columns
+    const int lo_h = g.P - g.KH + 1, lo_w = g.P - g.KW + 1;
+    if (!encode_im2col(&p.tmap_a, dconv, g.N, g.OH, g.OW, g.OCp, lo_h, lo_w, (g.H - 1) + lo_h - (g.OH - 1),
+                       (g.W - 1) + lo_w - (g.OW - 1), 1, kBM))
+      return CONV2D_ERR_CUDA;
+    p.a_tma = 1;
+    p.a_chunks = g.OCp / 64;
+    p.a_qh = lo_h;
+    p.a_qw = lo_w;
+  }
   p.stages = d.tile.stages;
   p.err = dev->err;
   if (bf && d.tile.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
@@ -510,6 +576,10 @@ int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dc
   p.splits = w.splits;
   p.num_units = w.units;
   p.partial = reinterpret_cast<float*>(region(ws, pl, R_WPART));
+  if (bf && g.ICp % 64 == 0 &&
+      encode_im2col(&p.tmap_x, xsrc, g.N, g.H, g.W, g.ICp, -g.P, -g.P, (g.OH - 1) * g.S - g.P - (g.H - 1),
+                    (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, w.KP))
+    p.a_tma = 1;
   p.stages = w.stages;
   p.err = dev->err;
   if (bf && w.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;

@@ -387,7 +387,11 @@ __global__ void prep_dgrad_weights_kernel(const T* __restrict__ w, T* __restrict
     const int local = col - t.col_off[ph];
     const int oc = local % OCp;
     const int tap = local / OCp;
-    const int tt = tap / t.Tw[ph], uu = tap % t.Tw[ph];
+    int tt = tap / t.Tw[ph], uu = tap % t.Tw[ph];
+    if (t.flip) {
+      tt = t.Th[ph] - 1 - tt;
+      uu = t.Tw[ph] - 1 - uu;
+    }
     const int kh = t.rh[ph] + S * tt, kw = t.rw[ph] + S * uu;
     T v = T(0.f);
     if (ic < IC && oc < OC && tt < t.Th[ph] && kh < KH && kw < KW)

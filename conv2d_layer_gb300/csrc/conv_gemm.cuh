@@ -87,6 +87,14 @@ struct ConvGemmParams {
   const float* ep_shift;  // optional per-column shift
   int act, out_act;       // out = out_act ? act(v) : T(v); out2 = act(T(v))
   float* stats;           // optional per-tile batch statistics [m_tile][N][3] = (count, mean, M2) of v
+  // A operand by TMA im2col (bf16, Cs a multiple of 64, one phase): the map
+  // walks the row domain; a k-block is (tap, 64-channel chunk) and the tap is
+  // the im2col offset, so taps must be non-negative offsets from the window
+  // corner (dgrad uses tap-flipped weights for this)
+  CUtensorMap tmap_a;
+  int a_tma;
+  int a_chunks;           // Cs / 64
+  int a_qh, a_qw;         // window corner of row (a, b): (a*rs + a_qh, b*rs + a_qw)
   int stages;
   int* err;
   ConvPhase ph[kMaxPhases];
@@ -94,6 +102,8 @@ struct ConvGemmParams {
 
 struct WgradParams {
   CUtensorMap tmap_dc;    // bf16 d_conv [n_pix][OCp], box {64 ch, 64 pix}
+  CUtensorMap tmap_x;     // bf16 im2col map of X, 64 pixels x 64 channels (when a_tma)
+  int a_tma;              // A panels by TMA im2col (bf16, Cs a multiple of 64)
   const void* x;          // NHWC [Nimg][H][W][Cs]
   const float* dc32;      // fp32 d_conv [n_pix][OCp] (fp32 mode)
   int H, W, Cs, OH, OW, S, P, KW;
@@ -237,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 4 + 1);  // one arrival per producer warp + the TMA thread
+      mbar_init(&full[s], p.a_tma ? 1 : 4 + 1);  // the TMA thread (+ one arrival per producer warp)
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -247,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     fence_mbar_init();
     tma_prefetch_desc(&p.tmap_b);
     if (D::NS == 2) tma_prefetch_desc(&p.tmap_b_lo);
+    if (p.a_tma) tma_prefetch_desc(&p.tmap_a);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, tcols);
@@ -265,14 +276,31 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       bool alive = true;
       for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
         const ConvPhase& ph = find_phase(p, u);
-        const int n_tile = (u - ph.unit_begin) % p.n_tiles;
+        const int local = u - ph.unit_begin;
+        const int n_tile = local % p.n_tiles;
+        int an = 0, ah = 0, aw = 0;  // window corner of the tile's first row (TMA im2col)
+        if (p.a_tma) {
+          const int m0 = (local / p.n_tiles) * kBM;
+          an = static_cast<int>(fdiv(static_cast<uint32_t>(m0), ph.div_HaWa));
+          const int rem = m0 - an * ph.Ha * ph.Wa;
+          const int a = static_cast<int>(fdiv(static_cast<uint32_t>(rem), ph.div_Wa));
+          ah = a * p.rs + p.a_qh;
+          aw = (rem - a * ph.Wa) * p.rs + p.a_qw;
+        }
         for (int kb = 0; kb < ph.num_kb; ++kb) {
           if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
             alive = false;
             break;
           }
-          const uint32_t b0 = sbase + s * stage_bytes + D::NS * a_bytes;
-          mbar_arrive_expect_tx(&full[s], D::NS * b_bytes);
+          const uint32_t a0 = sbase + s * stage_bytes;
+          const uint32_t b0 = a0 + D::NS * a_bytes;
+          mbar_arrive_expect_tx(&full[s], D::NS * b_bytes + (p.a_tma ? a_bytes : 0u));
+          if (p.a_tma) {
+            const int tap = kb / p.a_chunks;
+            const int tt = static_cast<int>(fdiv(static_cast<uint32_t>(tap), ph.div_Tw));
+            tma_load_im2col_4d(a0, &p.tmap_a, &full[s], (kb - tap * p.a_chunks) * 64, aw, ah, an,
+                               static_cast<uint16_t>(tap - tt * ph.Tw), static_cast<uint16_t>(tt));
+          }
           tma_load_2d(b0, &p.tmap_b, &full[s], ph.b_col + kb * D::BKE, n_tile * BN);
           if (D::NS == 2) tma_load_2d(b0 + b_bytes, &p.tmap_b_lo, &full[s], ph.b_col + kb * D::BKE, n_tile * BN);
           if (++s == S) {
@@ -330,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     }
   } else if (warp < 6) {
     // ------------------------------------------------ A producers (gather)
+    // (idle when the A operand comes by TMA im2col)
     const int t = threadIdx.x - 64;
     const int j = t & 7;       // 16-byte chunk within the 128-byte row
     const int r0 = t >> 3;     // rows r0 + 16*i
@@ -338,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     int s = 0;
     uint32_t par = 0;
     int it = 0;
-    bool alive = true;
+    bool alive = !p.a_tma;
     for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
       const ConvPhase& ph = find_phase(p, u);
       const int m_tile = (u - ph.unit_begin) / p.n_tiles;
@@ -594,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], DT == 1 ? 4 + 1 : 4);  // one arrival per producer warp (+ the TMA thread)
+      mbar_init(&full[s], DT == 1 ? (p.a_tma ? 1 : 4 + 1) : 4);  // the TMA thread and/or one per producer warp
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -603,6 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
     }
     fence_mbar_init();
     if (DT == 1) tma_prefetch_desc(&p.tmap_dc);
+    if (p.a_tma) tma_prefetch_desc(&p.tmap_x);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, tcols);
@@ -631,13 +661,40 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
       for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
         int m_tile, n_tile, kb0, kb1;
         decode(u, m_tile, n_tile, kb0, kb1);
+        // A panels (64 k-rows each): tap offsets and channel of each panel
+        int pc[2], pkw[2], pkh[2];
+        uint32_t a_tx = 0;
+        if (p.a_tma) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int kc = m_tile * kBM + 64 * j;
+            const int tap = static_cast<int>(fdiv(static_cast<uint32_t>(kc), p.div_Cs));
+            pkh[j] = static_cast<int>(fdiv(static_cast<uint32_t>(tap), p.div_KW));
+            pkw[j] = tap - pkh[j] * p.KW;
+            pc[j] = kc < p.Mk ? kc - tap * p.Cs : -1;  // -1: k padding, panel not loaded (its rows are discarded)
+            if (pc[j] >= 0) a_tx += 8192;
+          }
+        }
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
             alive = false;
             break;
           }
-          const uint32_t b0 = sbase + s * stage_bytes + a_bytes;
-          mbar_arrive_expect_tx(&full[s], b_bytes);
+          const uint32_t a0 = sbase + s * stage_bytes;
+          const uint32_t b0 = a0 + a_bytes;
+          mbar_arrive_expect_tx(&full[s], b_bytes + a_tx);
+          if (p.a_tma) {
+            const int pix = kb * KP;  // first pixel of the k-block; the map walks the next 64
+            const int n = static_cast<int>(fdiv(static_cast<uint32_t>(pix), p.div_OHOW));
+            const int rem = pix - n * p.OH * p.OW;
+            const int oh = static_cast<int>(fdiv(static_cast<uint32_t>(rem), p.div_OW));
+            const int ow = rem - oh * p.OW;
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              if (pc[j] >= 0)
+                tma_load_im2col_4d(a0 + j * 8192, &p.tmap_x, &full[s], pc[j], ow * p.S - p.P, oh * p.S - p.P, n,
+                                   static_cast<uint16_t>(pkw[j]), static_cast<uint16_t>(pkh[j]));
+          }
           for (int jn = 0; jn < BN / 64; ++jn)
             tma_load_2d(b0 + jn * 8192, &p.tmap_dc, &full[s], n_tile * BN + 64 * jn, kb * KP);
           if (++s == S) {
@@ -710,6 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
       // pair (2r, 2r+1) owns pixel row r and copies its 16-byte chunks
       // q = 2j + (t & 1), j = 0..7: adjacent lanes read adjacent chunks.
       const int r = t >> 1, half = t & 1;
+      if (p.a_tma) alive = false;  // A comes by TMA im2col: nothing to gather
       for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
         int m_tile, n_tile, kb0, kb1;
         decode(u, m_tile, n_tile, kb0, kb1);

@@ -15,6 +15,7 @@ cudaError_t launch_wgrad_gemm_tf32(const WgradParams& p, int grid, size_t smem, 
 // Per-phase description of the dgrad weight matrix (see prep_dgrad_weights).
 struct DgradWeightTable {
   int n;
+  int flip;  // columns in reversed tap order within each phase (for TMA im2col, whose offsets are >= 0)
   int col_off[kMaxPhases];
   int Th[kMaxPhases], Tw[kMaxPhases], rh[kMaxPhases], rw[kMaxPhases];
 };

@@ -57,6 +57,12 @@ EDGE_CASES = {
                                        act=ACT_IDENTITY, dtype=FP32),
     "fp32_rect_kernel": LayerSpec(N=2, H=11, W=7, IC=8, OC=12, KH=3, KW=1, stride=1, pad=1, norm=NORM_BATCH,
                                   act=ACT_SIGMOID, dtype=FP32),
+    # bf16 with 64-channel multiples takes the TMA im2col paths; a rectangular kernel on a non-square
+    # image makes the H and W bounding-box corners differ
+    "bf16_rect_k3x1_tma": LayerSpec(N=3, H=11, W=7, IC=64, OC=64, KH=3, KW=1, stride=1, pad=1, norm=NORM_BATCH,
+                                    act=ACT_TANH, dtype=BF16),
+    "bf16_k1x5_s2_tma": LayerSpec(N=2, H=9, W=16, IC=128, OC=96, KH=1, KW=5, stride=2, pad=2, norm=NORM_NONE,
+                                  act=ACT_RELU, dtype=BF16),
 }
 
 
