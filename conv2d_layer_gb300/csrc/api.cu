@@ -656,6 +656,7 @@ int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, cons
   if ((rc = device_info(&dev))) return rc;
   Plan pl;
   plan_ws(g, CONV2D_OP_FWD_TRAIN, dev->sms, &pl);
+  pl.walk.err = dev->err;
   if (!ws || ws_bytes < pl.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CONV2D_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const void *xsrc, *bhi, *blo;
@@ -688,6 +689,7 @@ int conv2d_fwd_infer(const conv2d_desc* desc, const void* x, const void* w, cons
   if ((rc = device_info(&dev))) return rc;
   Plan pl;
   plan_ws(g, CONV2D_OP_FWD_INFER, dev->sms, &pl);
+  pl.walk.err = dev->err;
   if (!ws || ws_bytes < pl.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CONV2D_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const void *xsrc, *bhi, *blo;
@@ -719,6 +721,7 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
   if ((rc = device_info(&dev))) return rc;
   Plan pl;
   plan_ws(g, CONV2D_OP_BWD, dev->sms, &pl);
+  pl.walk.err = dev->err;
   if (!ws || ws_bytes < pl.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CONV2D_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* dconv = region(ws, pl, R_DC);

@@ -455,13 +455,278 @@ int vec_ec(int dtype, int C) {
   return (C % ec == 0) ? ec : 1;
 }
 
+// ------------------------------------------------------------ streamed row walks
+// The bandwidth-bound kernels below move NHWC rows through shared memory with
+// bulk TMA copies (cp.async.bulk): a ring of kStreamStages chunks of R rows
+// per input tensor, refilled by one thread, so that many bytes are in flight
+// per SM without holding them in registers. One persistent block per SM walks
+// a contiguous range of rows; every thread keeps a fixed group of EC channels.
+constexpr int kStreamStages = 4;
+constexpr int kChunkBytes = 16384;
+
+template <int EC>
+__device__ __forceinline__ void lds_v(const float* p, float (&v)[EC]) {
+  const float4 t = *reinterpret_cast<const float4*>(p);
+  v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+}
+template <int EC>
+__device__ __forceinline__ void lds_v(const __nv_bfloat16* p, float (&v)[EC]) {
+  const uint4 t = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+    v[2 * e] = f.x;
+    v[2 * e + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Walk rows [r0, r1) of NIN tensors [rows][C] (EC channels per thread, the
+// group g fixed per thread); proc(row, v) gets the NIN vectors of one row.
+// Returns false if a wait gave up (recorded in *err).
+template <typename T, int EC, int NIN, typename Proc>
+__device__ __forceinline__ bool stream_walk(const T* const (&in)[NIN], long r0, long r1, int C, int R, int g,
+                                            int rl, int rpp, uint8_t* sm, uint64_t* full, int* err, Proc&& proc) {
+  const size_t row_bytes = static_cast<size_t>(C) * sizeof(T);
+  const uint32_t chunk = static_cast<uint32_t>(R * row_bytes);
+  const long nchunks = r1 > r0 ? (r1 - r0 + R - 1) / R : 0;
+  auto issue = [&](long k) {
+    const int s = static_cast<int>(k % kStreamStages);
+    const long rb = r0 + k * R;
+    const long re = min(r1, rb + R);
+    const uint32_t bytes = static_cast<uint32_t>((re - rb) * row_bytes);
+    mbar_arrive_expect_tx(&full[s], NIN * bytes);
+#pragma unroll
+    for (int i = 0; i < NIN; ++i) bulk_load(smem_u32(sm + (s * NIN + i) * chunk), in[i] + rb * C, bytes, &full[s]);
+  };
+  if (threadIdx.x == 0)
+    for (long k = 0; k < nchunks && k < kStreamStages; ++k) issue(k);
+  bool ok = true;
+  for (long k = 0; k < nchunks; ++k) {
+    const int s = static_cast<int>(k % kStreamStages);
+    const int w = wait(&full[s], static_cast<uint32_t>((k / kStreamStages) & 1), err, 7) ? 1 : 0;
+    if (!__syncthreads_and(w)) {
+      ok = false;
+      break;
+    }
+    const long rb = r0 + k * R;
+    const int nrows = static_cast<int>(min(static_cast<long>(R), r1 - rb));
+    if (rl < rpp) {
+      for (int rr = rl; rr < nrows; rr += rpp) {
+        float v[NIN][EC];
+#pragma unroll
+        for (int i = 0; i < NIN; ++i)
+          lds_v<EC>(reinterpret_cast<const T*>(sm + (s * NIN + i) * chunk) + static_cast<size_t>(rr) * C + g * EC, v[i]);
+        proc(rb + rr, v);
+      }
+    }
+    __syncthreads();  // stage s consumed by every thread
+    if (threadIdx.x == 0 && k + kStreamStages < nchunks) issue(k + kStreamStages);
+  }
+  if (!ok && threadIdx.x == 0) {
+    // let the copies already issued land before the block exits (each wait bounded)
+    for (long k = 0; k < nchunks && k < kStreamStages; ++k) {
+      const int s = static_cast<int>(k % kStreamStages);
+      (void)mbar_try_wait(&full[s], 0);
+    }
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 1000000ull) {
+    }
+  }
+  return ok;
+}
+
+template <typename T, int EC, int NIN>
+struct StreamSetup {
+  int cg, tpr, rpp, rl, g;
+  long r0, r1;
+  __device__ StreamSetup(long rows, int C, long rpb) {
+    cg = C / EC;
+    tpr = cg;  // the streamed path is used when C / EC <= kBlock
+    rpp = kBlock / tpr;
+    rl = threadIdx.x / tpr;
+    g = threadIdx.x % tpr;
+    r0 = static_cast<long>(blockIdx.x) * rpb;
+    r1 = min(rows, r0 + rpb);
+  }
+};
+
+__device__ __forceinline__ void stream_init(uint64_t* full) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStreamStages; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+}
+
+template <typename T, int EC>
+__global__ void __launch_bounds__(kBlock, 1) bn_apply_stream(const T* __restrict__ pre, T* __restrict__ y, long rows,
+                                                             int C, long rpb, int R, const float* __restrict__ mean,
+                                                             const float* __restrict__ inv_std,
+                                                             const float* __restrict__ gamma,
+                                                             const float* __restrict__ beta, int act, int* err) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  __shared__ uint64_t full[kStreamStages];
+  stream_init(full);
+  const StreamSetup<T, EC, 1> st(rows, C, rpb);
+  float mu[EC], sc[EC], be[EC];
+#pragma unroll
+  for (int e = 0; e < EC; ++e) {
+    const int c = st.g * EC + e;
+    mu[e] = mean[c];
+    sc[e] = gamma[c] * inv_std[c];
+    be[e] = beta[c];
+  }
+  const T* const in[1] = {pre};
+  stream_walk<T, EC, 1>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err,
+                        [&](long row, const float (&v)[1][EC]) {
+                          float o[EC];
+#pragma unroll
+                          for (int e = 0; e < EC; ++e) o[e] = act_f(act, fmaf(v[0][e] - mu[e], sc[e], be[e]));
+                          store_v<EC>(y + row * C + st.g * EC, o);
+                        });
+}
+
+// part[b][c] = {sum d_norm, sum d_norm * z}
+template <typename T, int EC>
+__global__ void __launch_bounds__(kBlock, 1) bn_bwd_reduce_stream(const T* __restrict__ pre, const T* __restrict__ dy,
+                                                                  long rows, int C, long rpb, int R,
+                                                                  const float* __restrict__ mean,
+                                                                  const float* __restrict__ inv_std,
+                                                                  const float* __restrict__ gamma,
+                                                                  const float* __restrict__ beta, int act,
+                                                                  float* __restrict__ part, int* err) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  __shared__ uint64_t full[kStreamStages];
+  __shared__ float s_a[kBlock * EC], s_b[kBlock * EC];
+  stream_init(full);
+  const StreamSetup<T, EC, 2> st(rows, C, rpb);
+  float mu[EC], is[EC], ga[EC], be[EC], a[EC], b[EC];
+#pragma unroll
+  for (int e = 0; e < EC; ++e) {
+    const int c = st.g * EC + e;
+    mu[e] = mean[c];
+    is[e] = inv_std[c];
+    ga[e] = gamma[c];
+    be[e] = beta[c];
+    a[e] = b[e] = 0.f;
+  }
+  const T* const in[2] = {pre, dy};
+  stream_walk<T, EC, 2>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err,
+                        [&](long, const float (&v)[2][EC]) {
+#pragma unroll
+                          for (int e = 0; e < EC; ++e) {
+                            const float z = (v[0][e] - mu[e]) * is[e];
+                            const float dn = dact_f(act, fmaf(ga[e], z, be[e])) * v[1][e];
+                            a[e] += dn;
+                            b[e] = fmaf(dn, z, b[e]);
+                          }
+                        });
+#pragma unroll
+  for (int e = 0; e < EC; ++e) {
+    s_a[threadIdx.x * EC + e] = a[e];
+    s_b[threadIdx.x * EC + e] = b[e];
+  }
+  __syncthreads();
+  if (st.rl == 0) {
+    for (int e = 0; e < EC; ++e) {
+      float sa = 0.f, sb = 0.f;
+      for (int k = 0; k < st.rpp; ++k) {
+        sa += s_a[(k * st.tpr + st.g) * EC + e];
+        sb += s_b[(k * st.tpr + st.g) * EC + e];
+      }
+      float* o = part + (static_cast<size_t>(blockIdx.x) * C + st.g * EC + e) * 2;
+      o[0] = sa;
+      o[1] = sb;
+    }
+  }
+}
+
+// d_conv (MODE 0: batch norm, 1: no norm) and part[b][c] = sum d_conv.
+template <typename T, int EC, int MODE>
+__global__ void __launch_bounds__(kBlock, 1) dconv_stream(const T* __restrict__ pre, const T* __restrict__ dy,
+                                                          long rows, int C, long rpb, int R,
+                                                          const float* __restrict__ mean,
+                                                          const float* __restrict__ inv_std,
+                                                          const float* __restrict__ gamma,
+                                                          const float* __restrict__ beta, int act,
+                                                          const float* __restrict__ c12, T* __restrict__ dconv,
+                                                          float* __restrict__ part, int* err) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  __shared__ uint64_t full[kStreamStages];
+  __shared__ float s_a[kBlock * EC];
+  stream_init(full);
+  const StreamSetup<T, EC, 2> st(rows, C, rpb);
+  const float inv_n = 1.f / static_cast<float>(rows);
+  float mu[EC], is[EC], ga[EC], be[EC], k1[EC], k2[EC], a[EC];
+#pragma unroll
+  for (int e = 0; e < EC; ++e) {
+    const int c = st.g * EC + e;
+    a[e] = 0.f;
+    if (MODE == 0) {
+      mu[e] = mean[c];
+      is[e] = inv_std[c];
+      ga[e] = gamma[c];
+      be[e] = beta[c];
+      k1[e] = c12[2 * c] * inv_n;
+      k2[e] = c12[2 * c + 1] * inv_n;
+    }
+  }
+  const T* const in[2] = {pre, dy};
+  stream_walk<T, EC, 2>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err,
+                        [&](long row, const float (&v)[2][EC]) {
+                          float o[EC];
+#pragma unroll
+                          for (int e = 0; e < EC; ++e) {
+                            if (MODE == 0) {
+                              const float z = (v[0][e] - mu[e]) * is[e];
+                              const float dn = dact_f(act, fmaf(ga[e], z, be[e])) * v[1][e];
+                              o[e] = ga[e] * is[e] * (dn - k1[e] - z * k2[e]);
+                            } else {
+                              o[e] = dact_f(act, v[0][e]) * v[1][e];
+                            }
+                            a[e] += o[e];
+                          }
+                          store_v<EC>(dconv + row * C + st.g * EC, o);
+                        });
+#pragma unroll
+  for (int e = 0; e < EC; ++e) s_a[threadIdx.x * EC + e] = a[e];
+  __syncthreads();
+  if (st.rl == 0) {
+    for (int e = 0; e < EC; ++e) {
+      float sa = 0.f;
+      for (int k = 0; k < st.rpp; ++k) sa += s_a[(k * st.tpr + st.g) * EC + e];
+      part[static_cast<size_t>(blockIdx.x) * C + st.g * EC + e] = sa;
+    }
+  }
+}
+
 }  // namespace
 
 RowWalk make_walk(long rows, int C, int dtype, int sms) {
   RowWalk w;
   w.rows = rows;
   w.C = C;
+  w.err = nullptr;
   const int ec = vec_ec(dtype, C);
+  const long row_bytes = static_cast<long>(C) * (dtype == 1 ? 2 : 4);
+  w.stream = (ec > 1 && C / ec <= kBlock && row_bytes <= kChunkBytes) ? 1 : 0;
+  if (w.stream) {
+    w.R = static_cast<int>(kChunkBytes / row_bytes);
+    long g = (rows + w.R - 1) / w.R;
+    if (g > sms) g = sms;
+    if (g < 1) g = 1;
+    w.G = static_cast<int>(g);
+    w.rows_per_block = (rows + w.G - 1) / w.G;
+    return w;
+  }
+  w.R = 0;
   const int cg = C / ec;
   const int tpr = cg < kBlock ? cg : kBlock;
   const int rpp = kBlock / tpr;
@@ -529,8 +794,31 @@ cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float
   return cudaGetLastError();
 }
 
+// Launch a streamed kernel: EC is 8 (bf16) or 4 (fp32); dynamic shared memory holds the chunk ring.
+#define STREAM_LAUNCH(dtype, NIN, KERNEL, ...)                                                           \
+  do {                                                                                                  \
+    const size_t es = (dtype) == 1 ? 2 : 4;                                                             \
+    const size_t smem = static_cast<size_t>(kStreamStages) * (NIN) * wk.R * wk.C * es;                  \
+    if ((dtype) == 1) {                                                                                 \
+      constexpr int EC = 8;                                                                             \
+      using T = __nv_bfloat16;                                                                          \
+      cudaFuncSetAttribute(KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
+      KERNEL<<<wk.G, kBlock, smem, st>>>(__VA_ARGS__);                                                  \
+    } else {                                                                                            \
+      constexpr int EC = 4;                                                                             \
+      using T = float;                                                                                  \
+      cudaFuncSetAttribute(KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
+      KERNEL<<<wk.G, kBlock, smem, st>>>(__VA_ARGS__);                                                  \
+    }                                                                                                   \
+  } while (0)
+
 cudaError_t launch_bn_apply(int dtype, const void* pre, void* y, const RowWalk& wk, const float* mean,
                             const float* inv_std, const float* gamma, const float* beta, int act, cudaStream_t st) {
+  if (wk.stream) {
+    STREAM_LAUNCH(dtype, 1, (bn_apply_stream<T, EC>), static_cast<const T*>(pre), static_cast<T*>(y), wk.rows, wk.C,
+                  wk.rows_per_block, wk.R, mean, inv_std, gamma, beta, act, wk.err);
+    return cudaGetLastError();
+  }
   DISPATCH_EC(dtype, wk.C,
               (bn_apply_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), static_cast<T*>(y),
                                                                  wk.rows, wk.C, wk.rows_per_block, mean, inv_std,
@@ -544,6 +832,11 @@ cudaError_t launch_bn_apply(int dtype, const void* pre, void* y, const RowWalk& 
 cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, const RowWalk& wk, const float* mean,
                                  const float* inv_std, const float* gamma, const float* beta, int act, float* part,
                                  cudaStream_t st) {
+  if (wk.stream) {
+    STREAM_LAUNCH(dtype, 2, (bn_bwd_reduce_stream<T, EC>), static_cast<const T*>(pre), static_cast<const T*>(dy),
+                  wk.rows, wk.C, wk.rows_per_block, wk.R, mean, inv_std, gamma, beta, act, part, wk.err);
+    return cudaGetLastError();
+  }
   DISPATCH_EC(dtype, wk.C,
               (bn_bwd_reduce_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
                                                                       static_cast<const T*>(dy), wk.rows, wk.C,
@@ -565,6 +858,12 @@ cudaError_t launch_sum_finalize(const float* part, const RowWalk& wk, int nv, in
 cudaError_t launch_bn_bwd_apply(int dtype, const void* pre, const void* dy, const RowWalk& wk, int Cp,
                                 const float* mean, const float* inv_std, const float* gamma, const float* beta,
                                 int act, const float* c12, void* dconv, float* part, cudaStream_t st) {
+  if (wk.stream && wk.C == Cp) {
+    STREAM_LAUNCH(dtype, 2, (dconv_stream<T, EC, 0>), static_cast<const T*>(pre), static_cast<const T*>(dy), wk.rows,
+                  wk.C, wk.rows_per_block, wk.R, mean, inv_std, gamma, beta, act, c12, static_cast<T*>(dconv), part,
+                  wk.err);
+    return cudaGetLastError();
+  }
   // the vector path needs C == Cp (EC divides C); otherwise one channel per thread
   DISPATCH_EC(dtype, (wk.C == Cp ? wk.C : 1),
               (dconv_kernel<T, EC, 0><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
@@ -580,6 +879,12 @@ cudaError_t launch_bn_bwd_apply(int dtype, const void* pre, const void* dy, cons
 
 cudaError_t launch_act_bwd(int dtype, const void* pre, const void* dy, const RowWalk& wk, int Cp, int act,
                            void* dconv, float* part, cudaStream_t st) {
+  if (wk.stream && wk.C == Cp) {
+    STREAM_LAUNCH(dtype, 2, (dconv_stream<T, EC, 1>), static_cast<const T*>(pre), static_cast<const T*>(dy), wk.rows,
+                  wk.C, wk.rows_per_block, wk.R, nullptr, nullptr, nullptr, nullptr, act, nullptr,
+                  static_cast<T*>(dconv), part, wk.err);
+    return cudaGetLastError();
+  }
   DISPATCH_EC(dtype, (wk.C == Cp ? wk.C : 1),
               (dconv_kernel<T, EC, 1><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
                                                                  static_cast<const T*>(dy), wk.rows, wk.C, Cp,

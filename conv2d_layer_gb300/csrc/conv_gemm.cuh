@@ -466,6 +466,9 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     float* sc_s = tmean + BN;
     float* sh_s = sc_s + BN;
     int cur_n_tile = -1;
+    // After the first tile, tmean holds the previous tile's column means and
+    // serves as the shift of a single-pass (shifted sums) statistic.
+    bool have_shift = false;
     int tc = 0;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tc) {
       const ConvPhase& ph = find_phase(p, u);
@@ -502,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         obase = (static_cast<size_t>(n * p.Ho + oh) * p.Wo + ow) * p.out_ld;
       }
       const bool zero = ph.num_kb == 0;
+      const bool one_pass = p.stats && have_shift;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
       // columns are read from TMEM 64 at a time (two 32-column loads, one wait)
       auto fetch = [&](int c0, uint32_t (&ra)[32], uint32_t (&rb)[32]) {
@@ -520,11 +524,20 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         if (p.stats) {  // statistics of the unrounded value
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            float sv[16];
+            float sv[16], sq[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) sv[e] = (valid && h * 16 + e < ncols) ? v[h * 16 + e] : 0.f;
+            for (int e = 0; e < 16; ++e) {
+              const bool in = valid && h * 16 + e < ncols;
+              const float d = one_pass ? v[h * 16 + e] - tmean[cc + h * 16 + e] : v[h * 16 + e];
+              sv[e] = in ? d : 0.f;
+              sq[e] = sv[e] * sv[e];
+            }
             colsum16(sv, lane);
             if ((lane & 1) == 0) red[q * BN + cc + h * 16 + colsum16_col(lane)] = sv[0];
+            if (one_pass) {
+              colsum16(sq, lane);
+              if ((lane & 1) == 0) red2[q * BN + cc + h * 16 + colsum16_col(lane)] = sq[0];
+            }
           }
         }
         if (valid) {
@@ -545,8 +558,25 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         pass1(c0, ra);
         if (c0 + 32 < BN) pass1(c0 + 32, rb);
       }
-      if (p.stats) {
-        // two passes over the tile: mean from the column sums, then the sum of
+      if (one_pass) {
+        // shifted sums d = v - s with s the previous tile's mean:
+        // mean = s + sum(d)/n, M2 = sum(d^2) - sum(d)^2/n
+        const int cnt = min(kBM, ph.rows - m_tile * kBM);
+        const int cols = min(BN, p.N - n_tile * BN);
+        const float fc = static_cast<float>(cnt);
+        named_bar_sync(1, 128);
+        for (int c = et; c < cols; c += 128) {
+          const float s1 = red[c] + red[BN + c] + red[2 * BN + c] + red[3 * BN + c];
+          const float s2 = red2[c] + red2[BN + c] + red2[2 * BN + c] + red2[3 * BN + c];
+          const float mean = tmean[c] + s1 / fc;
+          float* o = p.stats + (static_cast<size_t>(m_tile) * p.N + n_tile * BN + c) * 3;
+          o[0] = fc;
+          o[1] = mean;
+          o[2] = fmaxf(s2 - s1 * (s1 / fc), 0.f);
+          tmean[c] = mean;  // next tile's shift (read after the next unit's barrier)
+        }
+      } else if (p.stats) {
+        // first tile: two passes, mean from the column sums, then the sum of
         // squared deviations from that mean (TMEM is read a second time)
         const int cnt = min(kBM, ph.rows - m_tile * kBM);
         const int cols = min(BN, p.N - n_tile * BN);
@@ -583,6 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           o[1] = tmean[c];
           o[2] = red2[c] + red2[BN + c] + red2[2 * BN + c] + red2[3 * BN + c];
         }
+        have_shift = p.n_tiles == 1;  // tmean now holds this tile's means
       }
       tc_fence_before();
       __syncwarp();

@@ -27,6 +27,9 @@ struct RowWalk {
   int C;
   int G;
   long rows_per_block;
+  int stream;  // rows move through shared memory by bulk TMA copies (vector path)
+  int R;       // rows per streamed chunk
+  int* err;    // device error word for bounded waits
 };
 RowWalk make_walk(long rows, int C, int dtype, int sms);
 
