@@ -29,6 +29,11 @@ METRIC = "conv2d fwd+bwd TFLOP/s (and % of dense TC peak) per layer on 1 GB300"
 WORKLOAD = "large"
 NOMINAL_BF16_TFLOPS = 2250.0
 
+# DRAM bytes (read + write) per launch of the GEMM kernels on the 256-image layer, from the ncu capture
+# summarised in profiles/large_step_kernels.md (96-image case, scaled by 256/96). Reset to None whenever
+# a GEMM kernel changes and re-capture.
+NCU_TRAFFIC_BYTES = {"fprop_gemm": 704e6, "dgrad_gemm": 688e6, "wgrad_gemm": 831e6}
+
 
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -345,7 +350,8 @@ def main():
                               "of_nominal_2250": round(value / world / NOMINAL_BF16_TFLOPS, 4),
                               "peaks": peaks["src"]},
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": d["achieved"], "peak": peaks["bf16_sust"],
-                     "unit": "TFLOP/s", "frac": d["frac"], "traffic": None,
+                     "unit": "TFLOP/s", "frac": d["frac"],
+                     "traffic": NCU_TRAFFIC_BYTES.get(dom) if spec.N == 256 else None,
                      "peak_kind": "bf16 sustained (%s)" % peaks["src"]},
         "kernels": kern,
         "gpu_launches": r["per_step"] * args.steps,
