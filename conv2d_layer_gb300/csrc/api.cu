@@ -302,7 +302,12 @@ WgradPlan wgrad_plan(const Geo& g, int sms) {
     }
   }
   w.splits = best;
+  // 3xTF32: the tensor core's fp32 accumulation is not round-to-nearest, and its error grows with the
+  // number of accumulations into one TMEM accumulator; cap a split at 32 k-blocks (1024 pixels), the
+  // splits are then summed in fp64
+  if (!bf) w.splits = std::max(w.splits, static_cast<int>(ceil_div(w.kb_total, 32)));
   w.kb_per_split = static_cast<int>(ceil_div(w.kb_total, w.splits));
+  w.splits = static_cast<int>(ceil_div(w.kb_total, w.kb_per_split));
   w.units = base * w.splits;
   const size_t ns = bf ? 1 : 2;
   const size_t stage = ns * (kBM * 128 + static_cast<size_t>(w.BN) * 128);

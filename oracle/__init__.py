@@ -44,6 +44,8 @@ def _load():
         pd = ctypes.POINTER(_Desc)
         lib.oracle_conv_point.restype = ctypes.c_double
         lib.oracle_conv_point.argtypes = [pd, dp, dp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.oracle_dgrad_point.restype = ctypes.c_double
+        lib.oracle_dgrad_point.argtypes = [pd, dp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.oracle_wgrad_point.restype = ctypes.c_double
         lib.oracle_wgrad_point.argtypes = [pd, dp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.oracle_act.restype = ctypes.c_double
@@ -199,6 +201,12 @@ def wgrad(L: Layer, x, dconv_):
     c = L._c()
     lib.oracle_wgrad(ctypes.byref(c), _p(x), _p(dc), _p(dw))
     return dw
+
+
+def dgrad_point(L: Layer, dconv_, w, n, ih, iw, ic):
+    lib = _load()
+    c = L._c()
+    return lib.oracle_dgrad_point(ctypes.byref(c), _p(dconv_), _p(w), n, ih, iw, ic)
 
 
 def wgrad_point(L: Layer, x, dconv_, oc, kh, kw, ic):

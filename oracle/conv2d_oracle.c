@@ -304,6 +304,28 @@ void oracle_dgrad(const oracle_desc* d, const double* dconv, const double* w, do
     }
 }
 
+/* One input-gradient element (the sum of `oracle_dgrad` for one (n,ih,iw,ic)). */
+double oracle_dgrad_point(const oracle_desc* d, const double* dconv, const double* w, int n, int ih, int iw,
+                          int ic) {
+    const int OH = out_h(d), OW = out_w(d);
+    double acc = 0.0;
+    for (int kh = 0; kh < d->KH; kh++) {
+        int th = ih + d->P - kh;
+        if (th < 0 || th % d->S) continue;
+        int oh = th / d->S;
+        if (oh >= OH) continue;
+        for (int kw = 0; kw < d->KW; kw++) {
+            int tw = iw + d->P - kw;
+            if (tw < 0 || tw % d->S) continue;
+            int ow = tw / d->S;
+            if (ow >= OW) continue;
+            const double* g = dconv + (((size_t)n * OH + oh) * OW + ow) * d->OC;
+            for (int oc = 0; oc < d->OC; oc++) acc += W_AT(w, oc, kh, kw, ic) * g[oc];
+        }
+    }
+    return acc;
+}
+
 /* One weight-gradient element, sum over batch and output pixels of
  * d_conv[n,oh,ow,oc] * X[n, oh*S+kh-P, ow*S+kw-P, ic] (backward_full,
  * `d_weights_acc`); not accumulated into anything. */

@@ -338,3 +338,19 @@ def test_stored_preactivations_feed_the_statistics(store):
     np.testing.assert_allclose(f["running_var"], 0.9 + 0.1 * ye.var(0), rtol=1e-13)
     z = (f["ypre"] - f["mean"]) * f["inv_std"]
     np.testing.assert_allclose(f["y"], np.maximum(gamma * z + beta, 0), rtol=1e-13, atol=1e-15)
+
+
+def test_point_functions_match_full_passes():
+    """The single-element forms used by the full-size GPU checks agree with the full passes (which the
+    adjoint, finite-difference and torch pins fix)."""
+    rng = np.random.default_rng(31)
+    L = oracle.Layer(2, 9, 8, 3, 5, 3, 3, 2, 1)
+    x, w, b = rng.standard_normal(L.x_shape), rng.standard_normal(L.w_shape), rng.standard_normal(L.OC)
+    g = rng.standard_normal(L.y_shape)
+    y, dx, dw = oracle.conv_fwd(L, x, w, b), oracle.dgrad(L, g, w), oracle.wgrad(L, x, g)
+    for n, a, bb, c in [(0, 0, 0, 0), (1, 3, 2, 4), (1, 3, 3, 2)]:
+        assert oracle.conv_point(L, x, w, b, n, a, bb, c) == y[n, a, bb, c]
+    for n, ih, iw, ic in [(0, 0, 0, 0), (1, 8, 7, 2), (0, 4, 5, 1)]:
+        assert abs(oracle.dgrad_point(L, g, w, n, ih, iw, ic) - dx[n, ih, iw, ic]) <= 1e-12
+    for oc, kh, kw, ic in [(0, 0, 0, 0), (4, 2, 1, 2)]:
+        assert abs(oracle.wgrad_point(L, x, g, oc, kh, kw, ic) - dw[oc, kh, kw, ic]) <= 1e-12

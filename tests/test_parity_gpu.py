@@ -176,3 +176,45 @@ def test_outputs_stay_inside_their_buffers():
 def test_device_status_clean():
     rc, site = abi.conv2d_device_status()
     assert rc == abi.OK and site == 0
+
+
+def test_mixed_two_layer_chain():
+    """The mixed workload as a stack: layer 1's output (stored in bf16) feeds layer 2; layer 2's dX
+    (stored in bf16) is layer 1's dY. Every output of both layers against the oracle run the same way."""
+    specs = [replace(WORKLOADS["mixed"].layers[0], N=2, H=20, W=20),
+             replace(WORKLOADS["mixed"].layers[1], N=2, H=20, W=20)]
+    inp = make_inputs("mixed", layers=specs)
+    l1, l2 = inp["layers"]
+    L1 = Conv2dLayer(specs[0], l1.w, l1.b, l1.gamma, l1.beta)
+    L2 = Conv2dLayer(specs[1], l2.w, l2.b, l2.gamma, l2.beta)
+    x, dy = inp["x"].cuda(), inp["dy"].cuda()
+    L1.zero_grad()
+    L2.zero_grad()
+    y1 = L1.fwd_train(x)
+    L2.fwd_train(y1)
+    dx2 = L2.bwd(y1, dy)
+    L1.bwd(x, dx2)
+    torch.cuda.synchronize()
+    assert abi.conv2d_device_status()[0] == abi.OK
+
+    O1, O2 = oracle_layer(specs[0]), oracle_layer(specs[1])
+    f1 = oracle.fwd_train(O1, f64(inp["x"]), f64(l1.w), f64(l1.b), f64(l1.gamma), f64(l1.beta))
+    y1r = oracle.store_round("bf16", f1["y"])
+    f2 = oracle.fwd_train(O2, y1r, f64(l2.w), f64(l2.b), f64(l2.gamma), f64(l2.beta))
+    g2 = oracle.bwd(O2, y1r, f64(l2.w), f2["ypre"], f64(inp["dy"]), f64(l2.gamma), f64(l2.beta), f2["mean"],
+                    f2["inv_std"])
+    dx2r = oracle.store_round("bf16", g2["dx"])
+    g1 = oracle.bwd(O1, f64(inp["x"]), f64(l1.w), f1["ypre"], dx2r, f64(l1.gamma), f64(l1.beta), f1["mean"],
+                    f1["inv_std"])
+    tol = TOL[BF16]
+    checks = {"y1": (y1, f1["y"]), "y2": (L2.y, f2["y"]), "dx2": (dx2, g2["dx"]), "dw2": (L2.dw, g2["dw"]),
+              "dgamma2": (L2.dgamma, g2["dgamma"]), "dbeta2": (L2.dbeta, g2["dbeta"]), "dx1": (L1.dx, g1["dx"]),
+              "dw1": (L1.dw, g1["dw"]), "dgamma1": (L1.dgamma, g1["dgamma"]), "dbeta1": (L1.dbeta, g1["dbeta"])}
+    errs = {k: rel_err(f64(a), b) for k, (a, b) in checks.items()}
+    assert all(v <= tol for v in errs.values()), errs
+    # layer 1 sees the shared seeded input: running statistics to 1e-5. Layer 2's input is layer 1's
+    # bf16 output, whose values next to a bf16 rounding midpoint may round either way on either side,
+    # so its statistics get the BF16 tensor bar.
+    for L, f, t in ((L1, f1, 1e-5), (L2, f2, tol)):
+        assert rel_err(f64(L.running_mean), f["running_mean"]) <= t
+        assert rel_err(f64(L.running_var), f["running_var"]) <= t
