@@ -427,8 +427,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 char* region(void* ws, const Plan& pl, Reg r) { return static_cast<char*>(ws) + pl.off[r]; }
 
 // fprop GEMM: D[pix][oc] = im2col(x) * B^T, epilogue per ConvGemmParams.
+// stats_groups (if stats): receives the number of statistics partials written (per CTA or per tile).
 int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bhi, const void* blo, void* out,
-              void* out2, const float* scale, const float* shift, int out_act, float* stats, cudaStream_t st) {
+              void* out2, const float* scale, const float* shift, int out_act, float* stats, int* stats_groups,
+              cudaStream_t st) {
   static ConvGemmParams p;  // guarded by g_launch_mu below (large struct)
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
@@ -486,6 +488,8 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   p.err = dev->err;
   if (bf && t.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
   const int grid = std::min(p.num_units, dev->sms);
+  p.stats_per_cta = t.n_tiles == 1 ? 1 : 0;
+  if (stats_groups) *stats_groups = p.stats_per_cta ? grid : static_cast<int>(ceil_div(g.n_pix, kBM));
   LAUNCH("fprop_gemm", st, bf ? launch_conv_gemm_bf16(p, grid, t.smem, st) : launch_conv_gemm_tf32(p, grid, t.smem, st));
   return CONV2D_OK;
 }
@@ -668,10 +672,12 @@ int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, cons
   if ((rc = prep_forward_operands(g, x, w, ws, pl, &xsrc, &bhi, &blo, st))) return rc;
   const bool bn = g.norm == CONV2D_NORM_BATCH;
   float* part = bn ? reinterpret_cast<float*>(region(ws, pl, R_PART)) : nullptr;
-  if ((rc = run_fprop(g, dev, xsrc, bhi, blo, pre_act, bn ? nullptr : y, nullptr, bias, 0, part, st))) return rc;
+  int groups = 0;
+  if ((rc = run_fprop(g, dev, xsrc, bhi, blo, pre_act, bn ? nullptr : y, nullptr, bias, 0, part, &groups, st)))
+    return rc;
   if (bn) {
-    RowWalk tiles = pl.walk;  // partials: one per 128-row tile of the fprop GEMM
-    tiles.G = static_cast<int>(ceil_div(g.n_pix, kBM));
+    RowWalk tiles = pl.walk;  // statistics partials written by the fprop GEMM
+    tiles.G = groups;
     LAUNCH("bn_stats_finalize", st,
            launch_bn_stats_finalize(part, tiles, g.eps, g.mom, save_mean, save_inv_std, running_mean, running_var,
                                     st));
@@ -703,7 +709,7 @@ int conv2d_fwd_infer(const conv2d_desc* desc, const void* x, const void* w, cons
   float* shift = scale + g.OC;
   LAUNCH("infer_fold", st,
          launch_infer_fold(bias, gamma, beta, running_mean, running_var, g.eps, g.norm, g.OC, scale, shift, st));
-  return run_fprop(g, dev, xsrc, bhi, blo, y, nullptr, scale, shift, 1, nullptr, st);
+  return run_fprop(g, dev, xsrc, bhi, blo, y, nullptr, scale, shift, 1, nullptr, nullptr, st);
 }
 
 int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const float* gamma, const float* beta,

@@ -407,7 +407,7 @@ __global__ void prep_dgrad_weights_kernel(const T* __restrict__ w, T* __restrict
   }
 }
 
-// dW[oc][tap][ic] += sum over splits of partial[s][oc][tap*ICp + ic].
+// dW[oc][tap][ic] += sum over splits of partial[s][oc][tap*ICp + ic] (fixed order: deterministic).
 __global__ void wgrad_reduce_kernel(const float* __restrict__ partial, int splits, int OC, int taps, int ICp, int IC,
                                     float* __restrict__ dw) {
   const long total = static_cast<long>(OC) * taps * IC;
@@ -419,9 +419,15 @@ __global__ void wgrad_reduce_kernel(const float* __restrict__ partial, int split
     const int tap = static_cast<int>(ot % taps);
     const int oc = static_cast<int>(ot / taps);
     const long m = static_cast<long>(tap) * ICp + ic;
-    double s = 0;
-    for (int k = 0; k < splits; ++k) s += partial[(static_cast<long>(k) * OC + oc) * Mk + m];
-    dw[i] += static_cast<float>(s);
+    // compensated (Kahan) fp32 summation in split order: fp64 is slow on this part
+    float s = 0.f, comp = 0.f;
+    for (int k = 0; k < splits; ++k) {
+      const float yk = partial[(static_cast<long>(k) * OC + oc) * Mk + m] - comp;
+      const float t = s + yk;
+      comp = (t - s) - yk;
+      s = t;
+    }
+    dw[i] += s;
   }
 }
 

@@ -86,7 +86,8 @@ struct ConvGemmParams {
   const float* ep_scale;  // optional per-column scale
   const float* ep_shift;  // optional per-column shift
   int act, out_act;       // out = out_act ? act(v) : T(v); out2 = act(T(v))
-  float* stats;           // optional per-tile batch statistics [m_tile][N][3] = (count, mean, M2) of v
+  float* stats;           // optional batch statistics (count, mean, M2) of v: [m_tile][N][3], or
+  int stats_per_cta;      // [blockIdx][N][3] merged over the CTA's tiles (single column tile only)
   // A operand by TMA im2col (bf16, Cs a multiple of 64, one phase): the map
   // walks the row domain; a k-block is (tap, 64-channel chunk) and the tap is
   // the im2col offset, so taps must be non-negative offsets from the window
@@ -469,6 +470,27 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     // After the first tile, tmean holds the previous tile's column means and
     // serves as the shift of a single-pass (shifted sums) statistic.
     bool have_shift = false;
+    // running merge of this CTA's tile statistics, columns et and et + 128
+    float cta_n = 0.f, cta_mean0 = 0.f, cta_m20 = 0.f, cta_mean1 = 0.f, cta_m21 = 0.f;
+    auto emit = [&](int m_tile, int n_tile, int c, float cnt, float mean, float m2) {
+      if (p.stats_per_cta) {
+        const float nn = cta_n + cnt, f = cnt / nn;
+        if (c < 128) {
+          const float d = mean - cta_mean0;
+          cta_mean0 = fmaf(d, f, cta_mean0);
+          cta_m20 += m2 + d * d * cta_n * f;
+        } else {
+          const float d = mean - cta_mean1;
+          cta_mean1 = fmaf(d, f, cta_mean1);
+          cta_m21 += m2 + d * d * cta_n * f;
+        }
+      } else {
+        float* o = p.stats + (static_cast<size_t>(m_tile) * p.N + n_tile * BN + c) * 3;
+        o[0] = cnt;
+        o[1] = mean;
+        o[2] = m2;
+      }
+    };
     int tc = 0;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tc) {
       const ConvPhase& ph = find_phase(p, u);
@@ -569,12 +591,10 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           const float s1 = red[c] + red[BN + c] + red[2 * BN + c] + red[3 * BN + c];
           const float s2 = red2[c] + red2[BN + c] + red2[2 * BN + c] + red2[3 * BN + c];
           const float mean = tmean[c] + s1 / fc;
-          float* o = p.stats + (static_cast<size_t>(m_tile) * p.N + n_tile * BN + c) * 3;
-          o[0] = fc;
-          o[1] = mean;
-          o[2] = fmaxf(s2 - s1 * (s1 / fc), 0.f);
+          emit(m_tile, n_tile, c, fc, mean, fmaxf(s2 - s1 * (s1 / fc), 0.f));
           tmean[c] = mean;  // next tile's shift (read after the next unit's barrier)
         }
+        cta_n += fc;
       } else if (p.stats) {
         // first tile: two passes, mean from the column sums, then the sum of
         // squared deviations from that mean (TMEM is read a second time)
@@ -607,17 +627,23 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           if (c0 + 32 < BN) pass2(c0 + 32, rb);
         }
         named_bar_sync(1, 128);
-        for (int c = et; c < cols; c += 128) {
-          float* o = p.stats + (static_cast<size_t>(m_tile) * p.N + n_tile * BN + c) * 3;
-          o[0] = static_cast<float>(cnt);
-          o[1] = tmean[c];
-          o[2] = red2[c] + red2[BN + c] + red2[2 * BN + c] + red2[3 * BN + c];
-        }
+        for (int c = et; c < cols; c += 128)
+          emit(m_tile, n_tile, c, static_cast<float>(cnt), tmean[c],
+               red2[c] + red2[BN + c] + red2[2 * BN + c] + red2[3 * BN + c]);
+        cta_n += static_cast<float>(cnt);
         have_shift = p.n_tiles == 1;  // tmean now holds this tile's means
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+    if (p.stats && p.stats_per_cta) {
+      for (int c = et; c < min(BN, p.N); c += 128) {
+        float* o = p.stats + (static_cast<size_t>(blockIdx.x) * p.N + c) * 3;
+        o[0] = cta_n;
+        o[1] = c < 128 ? cta_mean0 : cta_mean1;
+        o[2] = c < 128 ? cta_m20 : cta_m21;
+      }
     }
   }
 
