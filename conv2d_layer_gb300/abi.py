@@ -21,7 +21,7 @@ OP_FWD_TRAIN, OP_FWD_INFER, OP_BWD = 0, 1, 2
 EXPORTS = (
     "conv2d_out_hw", "conv2d_validate", "conv2d_workspace_size", "conv2d_fwd_train", "conv2d_fwd_infer",
     "conv2d_bwd", "conv2d_device_status", "conv2d_status_str", "conv2d_prof_enable", "conv2d_prof_read",
-    "conv2d_fwd_train_noalloc",
+    "conv2d_fwd_train_noalloc", "conv2d_selftest_wait_limit",
 )
 
 
@@ -65,6 +65,7 @@ def lib():
     L.conv2d_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     L.conv2d_status_str.argtypes = [i32]
     L.conv2d_status_str.restype = ctypes.c_char_p
+    L.conv2d_selftest_wait_limit.argtypes = [vp]
     L.conv2d_prof_enable.argtypes = [i32]
     L.conv2d_prof_read.argtypes = [ctypes.POINTER(ctypes.c_char_p), fp, i32]
     _lib = L
@@ -152,6 +153,10 @@ def conv2d_device_status(stream=None):
     site = ctypes.c_int32(0)
     rc = lib().conv2d_device_status(_stream(stream), ctypes.byref(site))
     return rc, site.value
+
+
+def conv2d_selftest_wait_limit(stream=None):
+    return lib().conv2d_selftest_wait_limit(_stream(stream))
 
 
 def conv2d_prof_enable(on):

@@ -622,9 +622,31 @@ int prep_forward_operands(const Geo& g, const void* x, const void* w, void* ws, 
   return CONV2D_OK;
 }
 
+// One thread waits on a barrier that nothing completes: the library's bounded
+// wait must give up, record `site` in the error word and let the kernel end.
+__global__ void wait_limit_selftest_kernel(int* err, int site) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)wait(&bar, 0, err, site);
+}
+
 }  // namespace
 
 extern "C" {
+
+int conv2d_selftest_wait_limit(void* stream) {
+  DevInfo* dev = nullptr;
+  const int rc = device_info(&dev);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LAUNCH("wait_limit_selftest", st, (wait_limit_selftest_kernel<<<1, 32, 0, st>>>(dev->err, 6), cudaGetLastError()));
+  return CONV2D_OK;
+}
+
 
 int conv2d_out_hw(const conv2d_desc* desc, int32_t* OH, int32_t* OW) {
   Geo g;

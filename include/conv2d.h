@@ -149,6 +149,14 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
  * CONV2D_ERR_CUDA. */
 int conv2d_device_status(void* stream, int32_t* site);
 
+/* Diagnostic for the device-side failure path (no counterpart on the pages).
+ * Launches one block whose thread waits, with the library's bounded wait, on a
+ * barrier that nothing completes. After the wait limit (about 2 s) the wait
+ * gives up, records site 6 in the device error word and the kernel ends; no
+ * fault, trap or hang is involved and the context stays usable.
+ * conv2d_device_status then returns CONV2D_ERR_TIMEOUT with site 6. */
+int conv2d_selftest_wait_limit(void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* conv2d_status_str(int status);
 

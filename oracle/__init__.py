@@ -26,7 +26,7 @@ NORM = {"none": 0, "batch": 1}
 
 class _Desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("N", "H", "W", "IC", "OC", "KH", "KW", "S", "P", "norm", "act",
-                                              "store")] + [
+                                              "store", "bn_eval")] + [
         ("eps", ctypes.c_double),
         ("momentum", ctypes.c_double),
     ]
@@ -68,19 +68,20 @@ class Layer:
     element type the pre-activations are stored in (store: None/"f64" keeps fp64, "f32", "bf16")."""
 
     def __init__(self, N, H, W, IC, OC, KH, KW, stride=1, pad=0, norm="none", act="identity",
-                 eps=1e-5, momentum=0.1, store=None):
+                 eps=1e-5, momentum=0.1, store=None, bn_eval=False):
         self.N, self.H, self.W, self.IC, self.OC = N, H, W, IC, OC
         self.KH, self.KW, self.S, self.P = KH, KW, stride, pad
         self.norm = norm if isinstance(norm, int) else NORM[norm]
         self.act = act if isinstance(act, int) else ACT[act]
         self.eps, self.momentum = float(eps), float(momentum)
         self.store = store if isinstance(store, int) else STORE[store]
+        self.bn_eval = 1 if bn_eval else 0
         self.OH = (H + 2 * pad - KH) // stride + 1
         self.OW = (W + 2 * pad - KW) // stride + 1
 
     def _c(self):
         return _Desc(self.N, self.H, self.W, self.IC, self.OC, self.KH, self.KW, self.S, self.P,
-                     self.norm, self.act, self.store, self.eps, self.momentum)
+                     self.norm, self.act, self.store, self.bn_eval, self.eps, self.momentum)
 
     @property
     def x_shape(self):

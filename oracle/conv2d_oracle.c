@@ -24,6 +24,8 @@
  *     derivative is taken at the activation input, ReLU'(0) = 0.
  *   - dX is overwritten, dW / dBias / dGamma / dBeta are accumulated into
  *     (`backward_full` loads the existing gradients first).
+ *   - `bn_eval` selects the pages' evaluation mode of batch norm inside
+ *     training (`forward` / `backward_full` with mode::Evaluation).
  *   - the pre-activations are stored in the layer's element type T (`forward`
  *     Phase 1 writes `(T)acc` into `pre_activations`), and the normalisation,
  *     the activation and the backward pass read that stored value. The batch
@@ -50,6 +52,7 @@ typedef struct {
     int32_t norm; /* 0 none, 1 batch norm */
     int32_t act;  /* 0 identity, 1 relu, 2 tanh, 3 sigmoid */
     int32_t store; /* element type T of the stored pre-activations: 0 keep fp64, 1 fp32, 2 bf16 */
+    int32_t bn_eval; /* batch norm in evaluation mode: running statistics, nothing updated */
     double eps, momentum;
 } oracle_desc;
 
@@ -172,7 +175,13 @@ void oracle_fwd_train(const oracle_desc* d, const double* x, const double* w, co
     const int C = d->OC;
     oracle_conv_fwd(d, x, w, b, ypre);
     double* var = NULL;
-    if (d->norm == 1) {
+    if (d->norm == 1 && d->bn_eval) {
+        /* `forward` with mode::Evaluation: the cached statistics are the running ones, no update */
+        for (int c = 0; c < C; c++) {
+            mean[c] = rm[c];
+            inv_std[c] = 1.0 / sqrt(rv[c] + d->eps);
+        }
+    } else if (d->norm == 1) {
         /* batch statistics of the conv output before it is stored in T */
         var = (double*)malloc(sizeof(double) * C);
         oracle_bn_batch_stats(d, ypre, mean, var);
@@ -183,12 +192,14 @@ void oracle_fwd_train(const oracle_desc* d, const double* x, const double* w, co
         for (long i = 0; i < npix * C; i++) y[i] = oracle_act(d->act, ypre[i]);
         return;
     }
-    for (int c = 0; c < C; c++) {
-        inv_std[c] = 1.0 / sqrt(var[c] + d->eps);
-        rm[c] = (1.0 - d->momentum) * rm[c] + d->momentum * mean[c];
-        rv[c] = (1.0 - d->momentum) * rv[c] + d->momentum * var[c];
+    if (!d->bn_eval) {
+        for (int c = 0; c < C; c++) {
+            inv_std[c] = 1.0 / sqrt(var[c] + d->eps);
+            rm[c] = (1.0 - d->momentum) * rm[c] + d->momentum * mean[c];
+            rv[c] = (1.0 - d->momentum) * rv[c] + d->momentum * var[c];
+        }
+        free(var);
     }
-    free(var);
 #pragma omp parallel for schedule(static)
     for (long p = 0; p < npix; p++)
         for (int c = 0; c < C; c++) {
@@ -235,6 +246,24 @@ void oracle_dconv(const oracle_desc* d, const double* gamma, const double* beta,
     if (d->norm == 0) {
 #pragma omp parallel for schedule(static)
         for (long i = 0; i < npix * C; i++) dconv[i] = oracle_dact(d->act, ypre[i]) * dy[i];
+        return;
+    }
+    if (d->bn_eval) {
+        /* `backward_full` evaluation branch: frozen statistics, d_conv = d_norm * gamma * inv_std */
+#pragma omp parallel for schedule(static)
+        for (int c = 0; c < C; c++) {
+            double s_g = 0.0, s_b = 0.0;
+            for (long p = 0; p < npix; p++) {
+                size_t i = (size_t)p * C + c;
+                double z = (ypre[i] - mean[c]) * inv_std[c];
+                double dn = oracle_dact(d->act, gamma[c] * z + beta[c]) * dy[i];
+                s_g += dn * z;
+                s_b += dn;
+                dconv[i] = dn * gamma[c] * inv_std[c];
+            }
+            if (dgamma) dgamma[c] += s_g;
+            if (dbeta) dbeta[c] += s_b;
+        }
         return;
     }
 #pragma omp parallel for schedule(static)

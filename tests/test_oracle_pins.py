@@ -354,3 +354,52 @@ def test_point_functions_match_full_passes():
         assert abs(oracle.dgrad_point(L, g, w, n, ih, iw, ic) - dx[n, ih, iw, ic]) <= 1e-12
     for oc, kh, kw, ic in [(0, 0, 0, 0), (4, 2, 1, 2)]:
         assert abs(oracle.wgrad_point(L, x, g, oc, kh, kw, ic) - dw[oc, kh, kw, ic]) <= 1e-12
+
+
+@pytest.mark.parametrize("act", ["relu", "tanh", "sigmoid"])
+def test_eval_mode_batchnorm_finite_differences(act):
+    """Batch norm in evaluation mode inside training: running statistics, nothing updated; every gradient
+    against central differences."""
+    L = oracle.Layer(2, 6, 5, 3, 4, 3, 3, 1, 1, norm="batch", act=act, bn_eval=True)
+    for seed in range(50):
+        rng = np.random.default_rng(2000 + seed)
+        x, w, b, gamma, beta, dy = _rand_layer(rng, L)
+        rm, rv = rng.normal(0, 0.3, L.OC), rng.uniform(0.5, 2.0, L.OC)
+        f = oracle.fwd_train(L, x, w, b, gamma, beta, rm, rv)
+        u = gamma * (f["ypre"] - f["mean"]) * f["inv_std"] + beta
+        if act != "relu" or np.min(np.abs(u)) > 1e-3:
+            break
+    np.testing.assert_array_equal(f["running_mean"], rm)
+    np.testing.assert_array_equal(f["running_var"], rv)
+    np.testing.assert_array_equal(f["mean"], rm)
+    np.testing.assert_allclose(f["inv_std"], 1 / np.sqrt(rv + L.eps), rtol=1e-15)
+    g = oracle.bwd(L, x, w, f["ypre"], dy, gamma, beta, f["mean"], f["inv_std"])
+    loss = lambda: float(np.sum(oracle.fwd_train(L, x, w, b, gamma, beta, rm, rv)["y"] * dy))  # noqa: E731
+    for name, arr in (("dx", x), ("dw", w), ("db", b), ("dgamma", gamma), ("dbeta", beta)):
+        num = _fd(loss, arr)
+        scale = max(np.max(np.abs(num)), 1e-3)
+        assert np.max(np.abs(num - g[name])) / scale < 1e-6, name
+
+
+def test_eval_mode_against_torch_cpu():
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    rng = np.random.default_rng(22)
+    L = oracle.Layer(2, 9, 8, 4, 6, 3, 3, 2, 1, norm="batch", act="tanh", bn_eval=True)
+    x, w, b, gamma, beta, dy = _rand_layer(rng, L)
+    rm, rv = rng.normal(0, 0.3, L.OC), rng.uniform(0.5, 2.0, L.OC)
+    f = oracle.fwd_train(L, x, w, b, gamma, beta, rm, rv)
+    g = oracle.bwd(L, x, w, f["ypre"], dy, gamma, beta, f["mean"], f["inv_std"])
+    tx = torch.tensor(x).permute(0, 3, 1, 2).requires_grad_()
+    tw = torch.tensor(w).permute(0, 3, 1, 2).contiguous().requires_grad_()
+    tb, tg, tbe = (torch.tensor(v).requires_grad_() for v in (b, gamma, beta))
+    out = torch.tanh(F.batch_norm(F.conv2d(tx, tw, tb, stride=2, padding=1), torch.tensor(rm), torch.tensor(rv),
+                                  tg, tbe, training=False, eps=L.eps))
+    (out * torch.tensor(dy).permute(0, 3, 1, 2)).sum().backward()
+    nhwc = lambda t: t.detach().permute(0, 2, 3, 1).numpy()  # noqa: E731
+    np.testing.assert_allclose(f["y"], nhwc(out), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g["dx"], nhwc(tx.grad), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(g["dw"], tw.grad.permute(0, 2, 3, 1).numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(g["db"], tb.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(g["dgamma"], tg.grad.numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(g["dbeta"], tbe.grad.numpy(), rtol=1e-9, atol=1e-11)
