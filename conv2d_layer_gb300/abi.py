@@ -27,7 +27,8 @@ EXPORTS = (
 
 class Conv2dDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("N", "H", "W", "IC", "OC", "KH", "KW", "stride", "pad", "norm", "act",
-                                              "dtype")] + [("eps", ctypes.c_float), ("momentum", ctypes.c_float)]
+                                              "dtype")] + [("eps", ctypes.c_float), ("momentum", ctypes.c_float),
+                                                           ("bn_eval", ctypes.c_int32)]
 
 
 class Conv2dError(RuntimeError):
@@ -90,8 +91,8 @@ def _stream(s):
 
 
 def desc(N, H, W, IC, OC, KH, KW, stride=1, pad=0, norm=NORM_NONE, act=ACT_RELU, dtype=FP32, eps=1e-5,
-         momentum=0.1):
-    return Conv2dDesc(N, H, W, IC, OC, KH, KW, stride, pad, norm, act, dtype, eps, momentum)
+         momentum=0.1, bn_eval=0):
+    return Conv2dDesc(N, H, W, IC, OC, KH, KW, stride, pad, norm, act, dtype, eps, momentum, bn_eval)
 
 
 def status_str(status):

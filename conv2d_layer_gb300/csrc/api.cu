@@ -193,7 +193,7 @@ long ceil_div(long a, long b) { return (a + b - 1) / b; }
 long round_up(long a, long b) { return ceil_div(a, b) * b; }
 
 struct Geo {
-  int N, H, W, IC, OC, KH, KW, S, P, norm, act, dt;
+  int N, H, W, IC, OC, KH, KW, S, P, norm, act, dt, bn_eval;
   float eps, mom;
   int OH, OW;
   long n_pix;
@@ -222,6 +222,7 @@ int make_geo(const conv2d_desc* d, Geo* g) {
   G.N = d->N; G.H = d->H; G.W = d->W; G.IC = d->IC; G.OC = d->OC; G.KH = d->KH; G.KW = d->KW;
   G.S = d->stride; G.P = d->pad; G.norm = d->norm; G.act = d->act; G.dt = d->dtype;
   G.eps = d->eps; G.mom = d->momentum;
+  G.bn_eval = (d->norm == CONV2D_NORM_BATCH && d->bn_eval != 0) ? 1 : 0;
   G.OH = (G.H + 2 * G.P - G.KH) / G.S + 1;
   G.OW = (G.W + 2 * G.P - G.KW) / G.S + 1;
   G.n_pix = static_cast<long>(G.N) * G.OH * G.OW;
@@ -693,11 +694,15 @@ int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, cons
   const void *xsrc, *bhi, *blo;
   if ((rc = prep_forward_operands(g, x, w, ws, pl, &xsrc, &bhi, &blo, st))) return rc;
   const bool bn = g.norm == CONV2D_NORM_BATCH;
-  float* part = bn ? reinterpret_cast<float*>(region(ws, pl, R_PART)) : nullptr;
+  float* part = (bn && !g.bn_eval) ? reinterpret_cast<float*>(region(ws, pl, R_PART)) : nullptr;
   int groups = 0;
   if ((rc = run_fprop(g, dev, xsrc, bhi, blo, pre_act, bn ? nullptr : y, nullptr, bias, 0, part, &groups, st)))
     return rc;
-  if (bn) {
+  if (bn && g.bn_eval) {
+    // evaluation mode: normalise with the running statistics, update nothing
+    LAUNCH("bn_eval_stats", st, launch_bn_eval_stats(running_mean, running_var, g.eps, g.OC, save_mean, save_inv_std, st));
+    LAUNCH("bn_apply", st, launch_bn_apply(g.dt, pre_act, y, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, st));
+  } else if (bn) {
     RowWalk tiles = pl.walk;  // statistics partials written by the fprop GEMM
     tiles.G = groups;
     LAUNCH("bn_stats_finalize", st,
@@ -764,9 +769,10 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
     LAUNCH("bn_bwd_reduce", st,
            launch_bn_bwd_reduce(g.dt, pre_act, dy, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, part, st));
     LAUNCH("bn_bwd_finalize", st, launch_sum_finalize(part, pl.walk, 2, 0, c12, dbeta, dgamma, st));
+    // evaluation mode (frozen statistics): d_conv = d_norm * gamma * inv_std, no projection terms
     LAUNCH("bn_bwd_dconv", st,
-           launch_bn_bwd_apply(g.dt, pre_act, dy, pl.walk, g.OCp, save_mean, save_inv_std, gamma, beta, g.act, c12,
-                               dconv, part, st));
+           launch_bn_bwd_apply(g.dt, pre_act, dy, pl.walk, g.OCp, save_mean, save_inv_std, gamma, beta, g.act,
+                               g.bn_eval ? nullptr : c12, dconv, part, st));
   } else {
     LAUNCH("act_bwd_dconv", st, launch_act_bwd(g.dt, pre_act, dy, pl.walk, g.OCp, g.act, dconv, part, st));
   }

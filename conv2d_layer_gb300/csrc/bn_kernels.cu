@@ -264,8 +264,8 @@ __global__ void __launch_bounds__(kBlock) dconv_kernel(const T* __restrict__ pre
           is[e] = inv_std[c];
           ga[e] = gamma[c];
           be[e] = beta[c];
-          k1[e] = c12[2 * c] * inv_n;
-          k2[e] = c12[2 * c + 1] * inv_n;
+          k1[e] = c12 ? c12[2 * c] * inv_n : 0.f;  // no c12: evaluation mode, no projection terms
+          k2[e] = c12 ? c12[2 * c + 1] * inv_n : 0.f;
         }
       }
       for (long r = l.r0 + l.rl; r < l.r1; r += l.rpp) {
@@ -429,6 +429,16 @@ __global__ void wgrad_reduce_kernel(const float* __restrict__ partial, int split
     }
     dw[i] += s;
   }
+}
+
+// Batch norm in evaluation mode inside training: the saved statistics are the
+// running ones (`forward` with mode::Evaluation), nothing is updated.
+__global__ void bn_eval_stats_kernel(const float* rm, const float* rv, float eps, int C, float* mean,
+                                     float* inv_std) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= C) return;
+  mean[c] = rm[c];
+  inv_std[c] = static_cast<float>(1.0 / sqrt(static_cast<double>(rv[c]) + eps));
 }
 
 // Inference epilogue constants: v = acc*scale + shift folds bias and the
@@ -680,8 +690,8 @@ __global__ void __launch_bounds__(kBlock, 1) dconv_stream(const T* __restrict__ 
       is[e] = inv_std[c];
       ga[e] = gamma[c];
       be[e] = beta[c];
-      k1[e] = c12[2 * c] * inv_n;
-      k2[e] = c12[2 * c + 1] * inv_n;
+      k1[e] = c12 ? c12[2 * c] * inv_n : 0.f;  // no c12: evaluation mode, no projection terms
+      k2[e] = c12 ? c12[2 * c + 1] * inv_n : 0.f;
     }
   }
   const T* const in[2] = {pre, dy};
@@ -909,6 +919,12 @@ cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int ta
                                 cudaStream_t st) {
   const int g = grid_for(static_cast<long>(OC) * taps * IC, 256);
   wgrad_reduce_kernel<<<g, 256, 0, st>>>(partial, splits, OC, taps, ICp, IC, dw);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bn_eval_stats(const float* rm, const float* rv, float eps, int C, float* mean, float* inv_std,
+                                 cudaStream_t st) {
+  bn_eval_stats_kernel<<<(C + 127) / 128, 128, 0, st>>>(rm, rv, eps, C, mean, inv_std);
   return cudaGetLastError();
 }
 

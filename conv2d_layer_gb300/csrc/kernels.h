@@ -58,6 +58,8 @@ cudaError_t launch_act_bwd(int dtype, const void* pre, const void* dy, const Row
                            void* dconv, float* part, cudaStream_t st);
 cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int taps, int ICp, int IC, float* dw,
                                 cudaStream_t st);
+cudaError_t launch_bn_eval_stats(const float* rm, const float* rv, float eps, int C, float* mean, float* inv_std,
+                                 cudaStream_t st);
 cudaError_t launch_infer_fold(const float* bias, const float* gamma, const float* beta, const float* rm,
                               const float* rv, float eps, int norm, int OC, float* scale, float* shift,
                               cudaStream_t st);

@@ -17,7 +17,7 @@ class Conv2dLayer:
                  device="cuda"):
         self.spec = spec
         self.desc = abi.desc(spec.N, spec.H, spec.W, spec.IC, spec.OC, spec.KH, spec.KW, spec.stride, spec.pad,
-                             spec.norm, spec.act, spec.dtype, spec.eps, spec.momentum)
+                             spec.norm, spec.act, spec.dtype, spec.eps, spec.momentum, spec.bn_eval)
         abi.check(abi.conv2d_validate(self.desc), "conv2d_validate")
         self.dt = _TORCH_DT[spec.dtype]
         dev = torch.device(device)

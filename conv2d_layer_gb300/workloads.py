@@ -45,6 +45,7 @@ class LayerSpec:
     dtype: int = FP32
     eps: float = 1e-5
     momentum: float = 0.1
+    bn_eval: int = 0      # batch norm in evaluation mode inside training
 
     @property
     def OH(self):

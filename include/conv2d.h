@@ -72,11 +72,17 @@ enum { CONV2D_FP32 = 0, CONV2D_BF16 = 1 };
 enum { CONV2D_OP_FWD_TRAIN = 0, CONV2D_OP_FWD_INFER = 1, CONV2D_OP_BWD = 2 };
 
 /* Layer spec. eps and momentum are read only when norm == CONV2D_NORM_BATCH
- * (running = (1-momentum)*running + momentum*batch, biased batch variance). */
+ * (running = (1-momentum)*running + momentum*batch, biased batch variance).
+ * bn_eval != 0 selects batch norm in evaluation mode inside training (the
+ * pages' mode::Evaluation): conv2d_fwd_train normalises with the running
+ * statistics, writes them as save_mean / save_inv_std (= 1/sqrt(var+eps)) and
+ * updates nothing; conv2d_bwd then uses the frozen-statistics backward
+ * (d_conv = act'(bn) * dy * gamma * inv_std). Zero keeps training mode. */
 typedef struct {
     int32_t N, H, W, IC, OC, KH, KW, stride, pad;
     int32_t norm, act, dtype;
     float eps, momentum;
+    int32_t bn_eval;
 } conv2d_desc;
 
 /* Output spatial size. Returns CONV2D_OK or CONV2D_ERR_INVALID_ARG. */

@@ -34,7 +34,7 @@ def oracle_layer(spec):
     """Oracle layer with the pre-activations stored in the layer's element type, as the pages do."""
     return oracle.Layer(spec.N, spec.H, spec.W, spec.IC, spec.OC, spec.KH, spec.KW, spec.stride, spec.pad,
                         norm=spec.norm, act=spec.act, eps=spec.eps, momentum=spec.momentum,
-                        store="bf16" if spec.dtype == BF16 else "f32")
+                        store="bf16" if spec.dtype == BF16 else "f32", bn_eval=spec.bn_eval)
 
 
 def run_pair(spec, inp, prev_grads=False, need_dx=True, need_params=True, seed=0):
@@ -86,11 +86,12 @@ def check_pair(spec, gpu, ref, need_dx=True, need_params=True):
         names += ["mean", "inv_std"]
     if need_dx:
         names += ["dx"]
+    bn_train = spec.norm == NORM_BATCH and not spec.bn_eval
     if need_params:
         names += ["dw"]
         if spec.norm == NORM_BATCH:
             names += ["dgamma", "dbeta"]
-        else:
+        if not bn_train:
             names += ["db"]
     for k in names:
         errs[k] = rel_err(gpu[k], ref[k])
@@ -100,7 +101,7 @@ def check_pair(spec, gpu, ref, need_dx=True, need_params=True):
             errs[k] = rel_err(gpu[k], ref[k])
             if not errs[k] <= STAT_TOL:
                 bad[k] = errs[k]
-        if need_params:
+        if need_params and bn_train:
             dc = ref["dconv"].reshape(-1, spec.OC)
             bound = DBIAS_TOL[spec.dtype] * np.abs(dc).sum(0)
             prev = ref["prev"]["db"] if "prev" in ref else 0.0

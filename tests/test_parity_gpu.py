@@ -218,3 +218,29 @@ def test_mixed_two_layer_chain():
     for L, f, t in ((L1, f1, 1e-5), (L2, f2, tol)):
         assert rel_err(f64(L.running_mean), f["running_mean"]) <= t
         assert rel_err(f64(L.running_var), f["running_var"]) <= t
+
+
+EVAL_CASES = {
+    "fp32_relu_s1": LayerSpec(N=3, H=12, W=12, IC=16, OC=32, KH=3, KW=3, stride=1, pad=1, norm=NORM_BATCH,
+                              act=ACT_RELU, dtype=FP32, bn_eval=1),
+    "bf16_tanh_s2": LayerSpec(N=2, H=17, W=15, IC=64, OC=96, KH=3, KW=3, stride=2, pad=1, norm=NORM_BATCH,
+                              act=ACT_TANH, dtype=BF16, bn_eval=1),
+    "bf16_sigmoid_1x1": LayerSpec(N=4, H=9, W=9, IC=128, OC=64, KH=1, KW=1, stride=1, pad=0, norm=NORM_BATCH,
+                                  act=ACT_SIGMOID, dtype=BF16, bn_eval=1),
+}
+
+
+@pytest.mark.parametrize("name", list(EVAL_CASES))
+def test_eval_mode_batchnorm_parity(name):
+    """Batch norm in evaluation mode inside training: running statistics used and left unchanged, the
+    frozen-statistics backward."""
+    spec = EVAL_CASES[name]
+    inp = random_layer_inputs(spec, 19)
+    li = inp["layers"][0]
+    g = torch.Generator().manual_seed(19)
+    li.running_mean = torch.randn(spec.OC, generator=g) * 0.3
+    li.running_var = torch.rand(spec.OC, generator=g) + 0.5
+    gpu, ref = run_pair(spec, inp)
+    check_pair(spec, gpu, ref)
+    np.testing.assert_array_equal(gpu["running_mean"], f64(li.running_mean))
+    np.testing.assert_array_equal(gpu["running_var"], f64(li.running_var))
