@@ -200,6 +200,47 @@ def run_gpu(args, rank, world, local_rank):
                 d2h=d2h, n_e2e=n_e2e)
 
 
+def per_config_timing(steps=10, warmup=3):
+    """TFLOP/s of fwd_train + bwd for every workload (the mixed stack as its two chained layers)."""
+    import torch
+
+    from conv2d_layer_gb300.layer import Conv2dLayer
+    from conv2d_layer_gb300.workloads import WORKLOADS, make_inputs
+
+    out = {}
+    for name in ("tiny", "rl", "bn", "mixed", "large"):
+        wl = WORKLOADS[name]
+        inp = make_inputs(name)
+        layers = [Conv2dLayer(s, li.w, li.b, li.gamma, li.beta, li.running_mean, li.running_var)
+                  for s, li in zip(wl.layers, inp["layers"])]
+        x, dy = inp["x"].cuda(), inp["dy"].cuda()
+
+        def step():
+            acts = [x]
+            for L in layers:
+                acts.append(L.fwd_train(acts[-1]))
+            g = dy
+            for L, a in zip(reversed(layers), reversed(acts[:-1])):
+                g = L.bwd(a, g)
+
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        fl = sum(s.flops_step() for s in wl.layers)
+        out[name] = {"ms_per_step": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
+                     "dtype": "bf16" if wl.layers[0].dtype == 1 else "fp32 (3xTF32)", "layers": len(wl.layers)}
+        del layers, x, dy, inp
+        torch.cuda.empty_cache()
+    return out
+
+
 def gemm_roofline(spec, kern, steps, peaks):
     """Per-kernel figures; the dominant kernel (largest total time) becomes the roofline entry."""
     gemm_flops = 2.0 * spec.n_pix * spec.OC * spec.KH * spec.KW * spec.IC
@@ -296,6 +337,7 @@ def main():
     ap.add_argument("--ref-images", type=int, default=1)
     ap.add_argument("--ref-warmup", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--images", type=int, default=0,
                     help="run the large layer with this many images instead of 256 (small profiling cases)")
     args = ap.parse_args()
@@ -322,6 +364,9 @@ def main():
 
     r = run_gpu(args, rank, world, local_rank)
     ms, e2e_ms = r["ms"], r["e2e_ms"]
+    per_cfg = None
+    if rank == 0 and world == 1 and not args.no_per_config and not args.images:
+        per_cfg = per_config_timing()
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([ms, e2e_ms], device="cuda")
@@ -359,6 +404,7 @@ def main():
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(e2e_ms, 4),
                 "what": "pinned host X, dY copied in; dW, dbias, dgamma, dbeta copied out; same ABI calls"},
         "clocks": r["clocks"],
+        "per_config": per_cfg,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
