@@ -21,7 +21,7 @@ from . import build as _build
 
 ACT = {"identity": 0, "relu": 1, "tanh": 2, "sigmoid": 3}
 STORE = {None: 0, "f64": 0, "f32": 1, "bf16": 2}
-NORM = {"none": 0, "batch": 1}
+NORM = {"none": 0, "batch": 1, "layer": 2}
 
 
 class _Desc(ctypes.Structure):
@@ -149,11 +149,12 @@ def fwd_train(L: Layer, x, w, b, gamma=None, beta=None, running_mean=None, runni
     rm = _zeros_if_none(running_mean, L.OC)
     rv = np.ones(L.OC) if running_var is None else _d(running_var).reshape(L.OC).copy()
     ypre, y = np.empty(L.y_shape), np.empty(L.y_shape)
-    mean, inv_std = np.zeros(L.OC), np.zeros(L.OC)
+    ns = L.N if L.norm == 2 else L.OC  # layer norm keeps per-sample statistics
+    mean, inv_std = np.zeros(max(ns, L.OC)), np.zeros(max(ns, L.OC))
     c = L._c()
     lib.oracle_fwd_train(ctypes.byref(c), _p(x), _p(w), _p(b), _p(gamma), _p(beta), _p(rm), _p(rv),
                          _p(ypre), _p(mean), _p(inv_std), _p(y))
-    return dict(ypre=ypre, mean=mean, inv_std=inv_std, y=y, running_mean=rm, running_var=rv)
+    return dict(ypre=ypre, mean=mean[:ns], inv_std=inv_std[:ns], y=y, running_mean=rm, running_var=rv)
 
 
 def fwd_infer(L: Layer, x, w, b, gamma=None, beta=None, running_mean=None, running_var=None):
@@ -176,8 +177,9 @@ def dconv(L: Layer, ypre, dy, gamma=None, beta=None, mean=None, inv_std=None):
     ypre, dy = _d(ypre, L.y_shape), _d(dy, L.y_shape)
     gamma = _d(gamma).reshape(L.OC) if gamma is not None else np.ones(L.OC)
     beta = _zeros_if_none(beta, L.OC)
-    mean = _zeros_if_none(mean, L.OC)
-    inv_std = _d(inv_std).reshape(L.OC) if inv_std is not None else np.ones(L.OC)
+    ns = L.N if L.norm == 2 else L.OC  # per-sample statistics under layer norm
+    mean = _zeros_if_none(mean, ns)
+    inv_std = _d(inv_std).reshape(ns) if inv_std is not None else np.ones(ns)
     out = np.empty(L.y_shape)
     dg, dbt = np.zeros(L.OC), np.zeros(L.OC)
     c = L._c()
@@ -226,8 +228,9 @@ def bwd(L: Layer, x, w, ypre, dy, gamma=None, beta=None, mean=None, inv_std=None
     ypre, dy = _d(ypre, L.y_shape), _d(dy, L.y_shape)
     gamma = _d(gamma).reshape(L.OC) if gamma is not None else np.ones(L.OC)
     beta = _zeros_if_none(beta, L.OC)
-    mean = _zeros_if_none(mean, L.OC)
-    inv_std = _d(inv_std).reshape(L.OC) if inv_std is not None else np.ones(L.OC)
+    ns = L.N if L.norm == 2 else L.OC  # per-sample statistics under layer norm
+    mean = _zeros_if_none(mean, ns)
+    inv_std = _d(inv_std).reshape(ns) if inv_std is not None else np.ones(ns)
     dx = np.empty(L.x_shape) if need_dx else None
     dw = (np.zeros(L.w_shape) if dw is None else _d(dw, L.w_shape).copy()) if need_params else None
     db = _zeros_if_none(db, L.OC) if need_params else None

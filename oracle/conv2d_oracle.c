@@ -26,6 +26,9 @@
  *     (`backward_full` loads the existing gradients first).
  *   - `bn_eval` selects the pages' evaluation mode of batch norm inside
  *     training (`forward` / `backward_full` with mode::Evaluation).
+ *   - norm 2 is layer norm: per-sample statistics over OH*OW*OC of the
+ *     stored pre-activations (it keeps no running statistics), per-channel
+ *     gamma / beta; mean / inv_std then have N entries.
  *   - the pre-activations are stored in the layer's element type T (`forward`
  *     Phase 1 writes `(T)acc` into `pre_activations`), and the normalisation,
  *     the activation and the backward pass read that stored value. The batch
@@ -49,7 +52,7 @@
 
 typedef struct {
     int32_t N, H, W, IC, OC, KH, KW, S, P;
-    int32_t norm; /* 0 none, 1 batch norm */
+    int32_t norm; /* 0 none, 1 batch norm, 2 layer norm */
     int32_t act;  /* 0 identity, 1 relu, 2 tanh, 3 sigmoid */
     int32_t store; /* element type T of the stored pre-activations: 0 keep fp64, 1 fp32, 2 bf16 */
     int32_t bn_eval; /* batch norm in evaluation mode: running statistics, nothing updated */
@@ -166,6 +169,24 @@ void oracle_bn_batch_stats(const oracle_desc* d, const double* ypre, double* mea
     }
 }
 
+/* Per-sample layer-norm statistics over all OH*OW*OC elements of image n, two passes, biased variance
+ * (`forward` / `evaluate`, LAYER_NORM branch). */
+void oracle_ln_stats(const oracle_desc* d, const double* ypre, double* mean, double* inv_std) {
+    const long per = (long)out_h(d) * out_w(d) * d->OC;
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < d->N; n++) {
+        const double* v = ypre + (size_t)n * per;
+        double m = 0.0;
+        for (long i = 0; i < per; i++) m += v[i];
+        m /= (double)per;
+        double var = 0.0;
+        for (long i = 0; i < per; i++) var += (v[i] - m) * (v[i] - m);
+        var /= (double)per;
+        mean[n] = m;
+        inv_std[n] = 1.0 / sqrt(var + d->eps);
+    }
+}
+
 /* Training forward: Ypre, batch stats, running-stat EMA, normalise + affine +
  * activation (forward, all phases). rm / rv are updated in place. */
 void oracle_fwd_train(const oracle_desc* d, const double* x, const double* w, const double* b,
@@ -190,6 +211,22 @@ void oracle_fwd_train(const oracle_desc* d, const double* x, const double* w, co
         for (long i = 0; i < npix * C; i++) ypre[i] = oracle_store_round(d->store, ypre[i]);
     if (d->norm == 0) {
         for (long i = 0; i < npix * C; i++) y[i] = oracle_act(d->act, ypre[i]);
+        return;
+    }
+    if (d->norm == 2) {
+        /* layer norm (`forward`, LAYER_NORM branch): per-sample two-pass statistics over OH*OW*OC of
+         * the stored pre-activations; mean / inv_std have N entries; per-channel gamma, beta */
+        oracle_ln_stats(d, ypre, mean, inv_std);
+        const long per = npix / d->N;
+#pragma omp parallel for schedule(static)
+        for (long p = 0; p < npix; p++) {
+            const int n = (int)(p / per);
+            for (int c = 0; c < C; c++) {
+                size_t i = (size_t)p * C + c;
+                double z = (ypre[i] - mean[n]) * inv_std[n];
+                y[i] = oracle_act(d->act, gamma[c] * z + beta[c]);
+            }
+        }
         return;
     }
     if (!d->bn_eval) {
@@ -222,6 +259,7 @@ void oracle_fwd_infer(const oracle_desc* d, const double* x, const double* w, co
         for (int c = 0; c < C; c++) {
             size_t i = (size_t)p * C + c;
             double v = y[i];
+            if (d->norm == 2) continue; /* layer norm: below, per sample */
             if (d->norm == 1) {
                 /* `evaluate` BN branch: the conv output is stored as T first */
                 v = oracle_store_round(d->store, v);
@@ -230,6 +268,23 @@ void oracle_fwd_infer(const oracle_desc* d, const double* x, const double* w, co
             }
             y[i] = oracle_act(d->act, v);
         }
+    if (d->norm == 2) {
+        /* `evaluate`, LAYER_NORM branch: the conv output is stored as T, per-sample statistics on the fly */
+        for (long i = 0; i < npix * C; i++) y[i] = oracle_store_round(d->store, y[i]);
+        double* m = (double*)malloc(sizeof(double) * d->N);
+        double* is = (double*)malloc(sizeof(double) * d->N);
+        oracle_ln_stats(d, y, m, is);
+        const long per = npix / d->N;
+        for (long p = 0; p < npix; p++) {
+            const int n = (int)(p / per);
+            for (int c = 0; c < C; c++) {
+                size_t i = (size_t)p * C + c;
+                y[i] = oracle_act(d->act, gamma[c] * ((y[i] - m[n]) * is[n]) + beta[c]);
+            }
+        }
+        free(m);
+        free(is);
+    }
 }
 
 /* Gradient at the conv output (backward_full, before the scatter loops):
@@ -246,6 +301,39 @@ void oracle_dconv(const oracle_desc* d, const double* gamma, const double* beta,
     if (d->norm == 0) {
 #pragma omp parallel for schedule(static)
         for (long i = 0; i < npix * C; i++) dconv[i] = oracle_dact(d->act, ypre[i]) * dy[i];
+        return;
+    }
+    if (d->norm == 2) {
+        /* `backward_full` training branch with NORM_DIM = batch: the sums of dz and dz*z run over the
+         * OH*OW*OC elements of each image (M of them); dgamma / dbeta stay per channel */
+        const long per_pix = npix / d->N;
+        const double M = (double)(per_pix * C);
+        double* sdz = (double*)calloc(d->N, sizeof(double));
+        double* sdzz = (double*)calloc(d->N, sizeof(double));
+        for (int n = 0; n < d->N; n++)
+            for (long p = n * per_pix; p < (n + 1) * per_pix; p++)
+                for (int c = 0; c < C; c++) {
+                    size_t i = (size_t)p * C + c;
+                    double z = (ypre[i] - mean[n]) * inv_std[n];
+                    double dn = oracle_dact(d->act, gamma[c] * z + beta[c]) * dy[i];
+                    double dz = dn * gamma[c];
+                    if (dgamma) dgamma[c] += dn * z;
+                    if (dbeta) dbeta[c] += dn;
+                    sdz[n] += dz;
+                    sdzz[n] += dz * z;
+                }
+#pragma omp parallel for schedule(static)
+        for (long p = 0; p < npix; p++) {
+            const int n = (int)(p / per_pix);
+            for (int c = 0; c < C; c++) {
+                size_t i = (size_t)p * C + c;
+                double z = (ypre[i] - mean[n]) * inv_std[n];
+                double dz = oracle_dact(d->act, gamma[c] * z + beta[c]) * dy[i] * gamma[c];
+                dconv[i] = inv_std[n] * (1.0 / M) * (M * dz - sdz[n] - z * sdzz[n]);
+            }
+        }
+        free(sdz);
+        free(sdzz);
         return;
     }
     if (d->bn_eval) {

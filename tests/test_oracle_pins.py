@@ -37,7 +37,10 @@ def _act_inputs(L, x, w, b, gamma, beta):
     out = oracle.fwd_train(L, x, w, b, gamma, beta)
     if L.norm == 0:
         return out["ypre"]
-    z = (out["ypre"] - out["mean"]) * out["inv_std"]
+    if L.norm == 2:  # per-sample statistics
+        z = (out["ypre"] - out["mean"][:, None, None, None]) * out["inv_std"][:, None, None, None]
+    else:
+        z = (out["ypre"] - out["mean"]) * out["inv_std"]
     return gamma * z + beta
 
 
@@ -64,7 +67,7 @@ FD_CASES = [
 ]
 
 
-@pytest.mark.parametrize("norm", ["none", "batch"])
+@pytest.mark.parametrize("norm", ["none", "batch", "layer"])
 @pytest.mark.parametrize("act", ["identity", "relu", "tanh", "sigmoid"])
 @pytest.mark.parametrize("case", FD_CASES)
 def test_finite_differences(case, norm, act):
@@ -81,7 +84,7 @@ def test_finite_differences(case, norm, act):
     g = oracle.bwd(L, x, w, fwd["ypre"], dy, gamma, beta, fwd["mean"], fwd["inv_std"])
     f = lambda: _loss(L, x, w, b, gamma, beta, dy)  # noqa: E731
     checks = [("dx", x, g["dx"]), ("dw", w, g["dw"]), ("db", b, g["db"])]
-    if norm == "batch":
+    if norm != "none":
         checks += [("dgamma", gamma, g["dgamma"]), ("dbeta", beta, g["dbeta"])]
     for name, arr, an in checks:
         num = _fd(f, arr)
@@ -403,3 +406,96 @@ def test_eval_mode_against_torch_cpu():
     np.testing.assert_allclose(g["db"], tb.grad.numpy(), rtol=1e-9, atol=1e-11)
     np.testing.assert_allclose(g["dgamma"], tg.grad.numpy(), rtol=1e-9, atol=1e-11)
     np.testing.assert_allclose(g["dbeta"], tbe.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+# ---------------------------------------------------------------- layer norm
+def _per_image(a, N):
+    return a.reshape(N, -1)
+
+
+def test_layernorm_invariants():
+    """Layer norm (per-sample statistics over OH*OW*OC): z has mean 0 and mean square var/(var+eps) per
+    image; the backward's d_conv sums to 0 per image and its projection on z is the eps leak; a common shift
+    of every bias leaves the output unchanged, so the bias gradient sums to 0 over channels."""
+    rng = np.random.default_rng(41)
+    L = oracle.Layer(3, 6, 5, 4, 5, 3, 3, 1, 1, norm="layer", act="tanh", eps=1e-3)
+    x, w, b, gamma, beta, dy = _rand_layer(rng, L)
+    f = oracle.fwd_train(L, x, w, b, gamma, beta)
+    assert f["mean"].shape == (L.N,) and f["inv_std"].shape == (L.N,)
+    yp = _per_image(f["ypre"], L.N)
+    var = yp.var(1)
+    np.testing.assert_allclose(f["mean"], yp.mean(1), rtol=1e-13)
+    np.testing.assert_allclose(f["inv_std"], 1 / np.sqrt(var + L.eps), rtol=1e-13)
+    z = (yp - f["mean"][:, None]) * f["inv_std"][:, None]
+    np.testing.assert_allclose(z.mean(1), 0, atol=1e-13)
+    np.testing.assert_allclose((z * z).mean(1), var / (var + L.eps), rtol=1e-12)
+    # no running statistics under layer norm
+    np.testing.assert_array_equal(f["running_mean"], np.zeros(L.OC))
+    np.testing.assert_array_equal(f["running_var"], np.ones(L.OC))
+    dc, dg, _ = oracle.dconv(L, f["ypre"], dy, gamma, beta, f["mean"], f["inv_std"])
+    dc = _per_image(dc, L.N)
+    scale = np.abs(dc).sum(1)
+    np.testing.assert_allclose(dc.sum(1) / scale, 0, atol=1e-13)
+    u = gamma * z.reshape(L.y_shape) + beta
+    dzz = _per_image(oracle.dact("tanh", u) * dy * gamma * z.reshape(L.y_shape), L.N).sum(1)
+    leak = f["inv_std"] * dzz * L.eps / (var + L.eps)
+    np.testing.assert_allclose((dc * z).sum(1), leak, rtol=1e-9, atol=1e-13 * scale.max())
+    # bias shift invariance
+    f2 = oracle.fwd_train(L, x, w, b + 0.37, gamma, beta)
+    np.testing.assert_allclose(f2["y"], f["y"], rtol=1e-12, atol=1e-13)
+    g = oracle.bwd(L, x, w, f["ypre"], dy, gamma, beta, f["mean"], f["inv_std"])
+    assert abs(g["db"].sum()) <= 1e-12 * np.abs(g["db"]).sum() + 1e-14
+
+
+def test_layernorm_against_torch_cpu_float64():
+    """Independent computation: torch CPU float64 conv2d + layer_norm over (C, H, W) with the per-channel
+    gamma / beta broadcast over the image, autograd for every gradient."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    rng = np.random.default_rng(43)
+    acts = {"relu": torch.relu, "tanh": torch.tanh, "sigmoid": torch.sigmoid, "identity": lambda t: t}
+    for (N, H, W, IC, OC, K, S, P, act) in [
+        (3, 9, 8, 5, 6, 3, 1, 1, "relu"),
+        (2, 11, 11, 4, 8, 5, 2, 2, "sigmoid"),
+        (2, 6, 6, 8, 4, 1, 1, 0, "identity"),
+    ]:
+        L = oracle.Layer(N, H, W, IC, OC, K, K, S, P, norm="layer", act=act)
+        x, w, b, gamma, beta, dy = _rand_layer(rng, L)
+        f = oracle.fwd_train(L, x, w, b, gamma, beta)
+        g = oracle.bwd(L, x, w, f["ypre"], dy, gamma, beta, f["mean"], f["inv_std"])
+        tx = torch.tensor(x).permute(0, 3, 1, 2).requires_grad_()
+        tw = torch.tensor(w).permute(0, 3, 1, 2).contiguous().requires_grad_()
+        tb, tg, tbe = (torch.tensor(v).requires_grad_() for v in (b, gamma, beta))
+        ypre = F.conv2d(tx, tw, tb, stride=S, padding=P)
+        shp = (OC, L.OH, L.OW)
+        v = F.layer_norm(ypre, shp, tg[:, None, None].expand(shp), tbe[:, None, None].expand(shp), eps=L.eps)
+        out = acts[act](v)
+        (out * torch.tensor(dy).permute(0, 3, 1, 2)).sum().backward()
+        nhwc = lambda t: t.detach().permute(0, 2, 3, 1).numpy()  # noqa: E731
+        np.testing.assert_allclose(f["y"], nhwc(out), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(g["dx"], nhwc(tx.grad), rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(g["dw"], tw.grad.permute(0, 2, 3, 1).numpy(), rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(g["db"], tb.grad.numpy(), rtol=1e-8, atol=1e-10)
+        np.testing.assert_allclose(g["dgamma"], tg.grad.numpy(), rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(g["dbeta"], tbe.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+@pytest.mark.parametrize("store", ["f32", "bf16"])
+def test_layernorm_statistics_come_from_the_stored_values(store):
+    """Under layer norm the per-sample statistics are those of the stored pre-activations (the pages'
+    LAYER_NORM branch reads `pre_activations`), and inference recomputes the same statistics, so it
+    matches the training forward."""
+    rng = np.random.default_rng(45)
+    L = oracle.Layer(2, 6, 6, 4, 5, 3, 3, 1, 1, norm="layer", act="relu", store=store)
+    L0 = oracle.Layer(2, 6, 6, 4, 5, 3, 3, 1, 1, norm="layer", act="relu")
+    x, w, b, gamma, beta, _ = _rand_layer(rng, L)
+    f = oracle.fwd_train(L, x, w, b, gamma, beta)
+    stored = oracle.store_round(store, oracle.conv_fwd(L0, x, w, b))
+    np.testing.assert_array_equal(f["ypre"], stored)
+    ys = _per_image(stored, L.N)
+    np.testing.assert_allclose(f["mean"], ys.mean(1), rtol=1e-13)
+    np.testing.assert_allclose(f["inv_std"], 1 / np.sqrt(ys.var(1) + L.eps), rtol=1e-12)
+    z = (ys - f["mean"][:, None]) * f["inv_std"][:, None]
+    np.testing.assert_allclose(f["y"], np.maximum(gamma * z.reshape(L.y_shape) + beta, 0), rtol=1e-13,
+                               atol=1e-15)
+    np.testing.assert_allclose(oracle.fwd_infer(L, x, w, b, gamma, beta), f["y"], rtol=1e-14, atol=1e-15)
