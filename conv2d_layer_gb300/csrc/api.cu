@@ -212,11 +212,8 @@ int make_geo(const conv2d_desc* d, Geo* g) {
     return CONV2D_ERR_INVALID_ARG;
   if (d->norm < 0 || d->norm > 2 || d->act < 0 || d->act > 3 || d->dtype < 0 || d->dtype > 1)
     return CONV2D_ERR_INVALID_ARG;
-  if (d->norm == CONV2D_NORM_BATCH) {
-    if (!(d->eps > 0.f) || !std::isfinite(d->eps)) return CONV2D_ERR_INVALID_ARG;
-    if (!(d->momentum >= 0.f && d->momentum <= 1.f)) return CONV2D_ERR_INVALID_ARG;
-  }
-  if (d->norm == CONV2D_NORM_LAYER) return CONV2D_ERR_UNSUPPORTED;
+  if (d->norm != CONV2D_NORM_NONE && (!(d->eps > 0.f) || !std::isfinite(d->eps))) return CONV2D_ERR_INVALID_ARG;
+  if (d->norm == CONV2D_NORM_BATCH && !(d->momentum >= 0.f && d->momentum <= 1.f)) return CONV2D_ERR_INVALID_ARG;
   if (d->stride > 8) return CONV2D_ERR_UNSUPPORTED;
   Geo& G = *g;
   G.N = d->N; G.H = d->H; G.W = d->W; G.IC = d->IC; G.OC = d->OC; G.KH = d->KH; G.KW = d->KW;
@@ -390,7 +387,9 @@ struct Plan {
 void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
   size_t sz[R_NREG] = {0};
   const size_t es = g.ES;
-  pl->walk = make_walk(g.n_pix, g.OC, g.dt, sms);
+  const bool ln = g.norm == CONV2D_NORM_LAYER;
+  // layer norm walks each image as a segment of its own
+  pl->walk = make_walk(g.n_pix, g.OC, g.dt, sms, ln ? g.N : 1);
   const size_t G = pl->walk.G;
   if (op == CONV2D_OP_FWD_TRAIN || op == CONV2D_OP_FWD_INFER) {
     if (g.pack_x) sz[R_XP] = static_cast<size_t>(g.N) * g.H * g.W * g.ICp * es;
@@ -398,11 +397,16 @@ void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
     if (g.dt == CONV2D_FP32) sz[R_WBLO] = static_cast<size_t>(g.OC) * g.Kf * 4;
     if (op == CONV2D_OP_FWD_TRAIN && g.norm == CONV2D_NORM_BATCH)
       sz[R_PART] = static_cast<size_t>(ceil_div(g.n_pix, kBM)) * g.OC * 3 * 4;  // per-tile statistics
-    if (op == CONV2D_OP_FWD_INFER) sz[R_FOLD] = 2 * static_cast<size_t>(g.OC) * 4;
+    if (ln)  // per-pixel, per-column-tile (mean, M2) of the stored conv output
+      sz[R_PART] = static_cast<size_t>(g.n_pix) * conv_tile(g, g.OC).n_tiles * 2 * 4;
+    if (op == CONV2D_OP_FWD_INFER) {
+      sz[R_FOLD] = (2 * static_cast<size_t>(g.OC) + 2 * static_cast<size_t>(g.N)) * 4;  // scale, shift, LN stats
+      if (ln) sz[R_DC] = static_cast<size_t>(g.n_pix) * g.OC * es;  // stored conv output, normalised into y
+    }
   } else {
     sz[R_DC] = static_cast<size_t>(g.n_pix) * g.OCp * es;
     sz[R_PART] = G * g.OC * 2 * 4;
-    sz[R_C12] = 2 * static_cast<size_t>(g.OC) * 4;
+    sz[R_C12] = 2 * (static_cast<size_t>(g.OC) + (ln ? g.N : 0)) * 4;  // channel sums, then per-image sums
     // dgrad weights: every phase's taps together hold each kernel tap once
     const size_t kd = std::max<size_t>(static_cast<size_t>(g.taps) * g.OCp, g.BKE);
     sz[R_WD] = static_cast<size_t>(g.ICp) * kd * es;
@@ -431,7 +435,8 @@ char* region(void* ws, const Plan& pl, Reg r) { return static_cast<char*>(ws) + 
 // stats_groups (if stats): receives the number of statistics partials written (per CTA or per tile).
 int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bhi, const void* blo, void* out,
               void* out2, const float* scale, const float* shift, int out_act, float* stats, int* stats_groups,
-              cudaStream_t st) {
+              float* rstats, cudaStream_t st) {
+  if (rstats && (out_act || out2)) return CONV2D_ERR_INVALID_ARG;  // row partials are of the stored value
   static ConvGemmParams p;  // guarded by g_launch_mu below (large struct)
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
@@ -477,6 +482,7 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   p.act = g.act;
   p.out_act = out_act;
   p.stats = stats;
+  p.rstats = rstats;
   if (bf && g.ICp % 64 == 0 &&
       encode_im2col(&p.tmap_a, xsrc, g.N, g.H, g.W, g.ICp, -g.P, -g.P, (g.OH - 1) * g.S - g.P - (g.H - 1),
                     (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, kBM)) {
@@ -684,6 +690,9 @@ int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, cons
     REQ_PTR(gamma); REQ_PTR(beta); REQ_PTR(running_mean); REQ_PTR(running_var); REQ_PTR(save_mean);
     REQ_PTR(save_inv_std);
   }
+  if (g.norm == CONV2D_NORM_LAYER) {
+    REQ_PTR(gamma); REQ_PTR(beta); REQ_PTR(save_mean); REQ_PTR(save_inv_std);
+  }
   DevInfo* dev = nullptr;
   if ((rc = device_info(&dev))) return rc;
   Plan pl;
@@ -694,9 +703,22 @@ int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, cons
   const void *xsrc, *bhi, *blo;
   if ((rc = prep_forward_operands(g, x, w, ws, pl, &xsrc, &bhi, &blo, st))) return rc;
   const bool bn = g.norm == CONV2D_NORM_BATCH;
+  if (g.norm == CONV2D_NORM_LAYER) {
+    // layer norm: per-image statistics of the stored conv output from the epilogue's row partials
+    float* rs = reinterpret_cast<float*>(region(ws, pl, R_PART));
+    if ((rc = run_fprop(g, dev, xsrc, bhi, blo, pre_act, nullptr, nullptr, bias, 0, nullptr, nullptr, rs, st)))
+      return rc;
+    const Tile t = conv_tile(g, g.OC);
+    LAUNCH("ln_stats_finalize", st,
+           launch_ln_stats_finalize(rs, g.N, static_cast<long>(g.OH) * g.OW, t.n_tiles, t.BN, g.OC, g.eps,
+                                    save_mean, save_inv_std, st));
+    LAUNCH("ln_apply", st, launch_bn_apply(g.dt, pre_act, y, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, st));
+    return CONV2D_OK;
+  }
   float* part = (bn && !g.bn_eval) ? reinterpret_cast<float*>(region(ws, pl, R_PART)) : nullptr;
   int groups = 0;
-  if ((rc = run_fprop(g, dev, xsrc, bhi, blo, pre_act, bn ? nullptr : y, nullptr, bias, 0, part, &groups, st)))
+  if ((rc = run_fprop(g, dev, xsrc, bhi, blo, pre_act, bn ? nullptr : y, nullptr, bias, 0, part, &groups, nullptr,
+                      st)))
     return rc;
   if (bn && g.bn_eval) {
     // evaluation mode: normalise with the running statistics, update nothing
@@ -723,6 +745,9 @@ int conv2d_fwd_infer(const conv2d_desc* desc, const void* x, const void* w, cons
   if (g.norm == CONV2D_NORM_BATCH) {
     REQ_PTR(gamma); REQ_PTR(beta); REQ_PTR(running_mean); REQ_PTR(running_var);
   }
+  if (g.norm == CONV2D_NORM_LAYER) {
+    REQ_PTR(gamma); REQ_PTR(beta);
+  }
   DevInfo* dev = nullptr;
   if ((rc = device_info(&dev))) return rc;
   Plan pl;
@@ -736,7 +761,23 @@ int conv2d_fwd_infer(const conv2d_desc* desc, const void* x, const void* w, cons
   float* shift = scale + g.OC;
   LAUNCH("infer_fold", st,
          launch_infer_fold(bias, gamma, beta, running_mean, running_var, g.eps, g.norm, g.OC, scale, shift, st));
-  return run_fprop(g, dev, xsrc, bhi, blo, y, nullptr, scale, shift, 1, nullptr, nullptr, st);
+  if (g.norm == CONV2D_NORM_LAYER) {
+    // `evaluate`, LAYER_NORM branch: the conv output is stored, then normalised with per-image
+    // statistics computed on the fly (layer norm keeps no running statistics)
+    void* ybuf = region(ws, pl, R_DC);
+    float* rs = reinterpret_cast<float*>(region(ws, pl, R_PART));
+    float* mean = shift + g.OC;
+    float* istd = mean + g.N;
+    if ((rc = run_fprop(g, dev, xsrc, bhi, blo, ybuf, nullptr, scale, shift, 0, nullptr, nullptr, rs, st)))
+      return rc;
+    const Tile t = conv_tile(g, g.OC);
+    LAUNCH("ln_stats_finalize", st,
+           launch_ln_stats_finalize(rs, g.N, static_cast<long>(g.OH) * g.OW, t.n_tiles, t.BN, g.OC, g.eps, mean,
+                                    istd, st));
+    LAUNCH("ln_apply", st, launch_bn_apply(g.dt, ybuf, y, pl.walk, mean, istd, gamma, beta, g.act, st));
+    return CONV2D_OK;
+  }
+  return run_fprop(g, dev, xsrc, bhi, blo, y, nullptr, scale, shift, 1, nullptr, nullptr, nullptr, st);
 }
 
 int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const float* gamma, const float* beta,
@@ -751,7 +792,8 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
   if (dx) REQ_PTR(w);
   if (dw) REQ_PTR(x);
   const bool bn = g.norm == CONV2D_NORM_BATCH;
-  if (bn) {
+  const bool ln = g.norm == CONV2D_NORM_LAYER;
+  if (bn || ln) {
     REQ_PTR(gamma); REQ_PTR(beta); REQ_PTR(save_mean); REQ_PTR(save_inv_std);
     if (static_cast<bool>(dgamma) != static_cast<bool>(dbeta)) return CONV2D_ERR_INVALID_ARG;
   }
@@ -765,7 +807,17 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
   void* dconv = region(ws, pl, R_DC);
   float* part = reinterpret_cast<float*>(region(ws, pl, R_PART));
   float* c12 = reinterpret_cast<float*>(region(ws, pl, R_C12));
-  if (bn) {
+  if (ln) {
+    // per-channel sums of d_norm and d_norm * z (dbeta, dgamma) and, from the same image-aligned block
+    // partials, the per-image sums of gamma * d_norm and gamma * d_norm * z
+    LAUNCH("ln_bwd_reduce", st,
+           launch_bn_bwd_reduce(g.dt, pre_act, dy, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, part, st));
+    LAUNCH("ln_bwd_finalize", st, launch_sum_finalize(part, pl.walk, 2, 0, c12, dbeta, dgamma, st));
+    LAUNCH("ln_seg_finalize", st, launch_ln_seg_finalize(part, pl.walk, gamma, c12 + 2 * g.OC, st));
+    LAUNCH("ln_bwd_dconv", st,
+           launch_bn_bwd_apply(g.dt, pre_act, dy, pl.walk, g.OCp, save_mean, save_inv_std, gamma, beta, g.act, c12,
+                               dconv, part, st));
+  } else if (bn) {
     LAUNCH("bn_bwd_reduce", st,
            launch_bn_bwd_reduce(g.dt, pre_act, dy, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, part, st));
     LAUNCH("bn_bwd_finalize", st, launch_sum_finalize(part, pl.walk, 2, 0, c12, dbeta, dgamma, st));

@@ -13,6 +13,8 @@
 // merges in double in a fixed order (deterministic). The batch variance is
 // merged from per-tile two-pass (mean, M2) with Chan's formula, never
 // E[x^2] - mean^2.
+#include <algorithm>
+#include <cmath>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include "kernels.h"
@@ -76,21 +78,39 @@ __device__ __forceinline__ void store_v(__nv_bfloat16* p, const float (&v)[EC]) 
   }
 }
 
+// Rows of a walk are grouped in segments of seg_rows rows (one segment for
+// batch norm: every row; one per image for layer norm), each split over bps
+// blocks of at most rpb rows, so that a block never straddles two segments.
+struct SegRange {
+  int seg;
+  long r0, r1;
+};
+__device__ __forceinline__ SegRange seg_range(long seg_rows, int bps, long rpb) {
+  SegRange r;
+  r.seg = static_cast<int>(blockIdx.x / bps);
+  const long sb = static_cast<long>(r.seg) * seg_rows;
+  r.r0 = sb + static_cast<long>(blockIdx.x % bps) * rpb;
+  r.r1 = min(sb + seg_rows, r.r0 + rpb);
+  return r;
+}
+
 // Thread geometry of a block walking [rows][C]: `tpr` threads share a row,
 // each owning EC consecutive channels; `rpp` rows are in flight per pass.
 struct Lane {
-  int cg, tpr, rpp, rl, g0;
+  int cg, tpr, rpp, rl, g0, seg;
   long r0, r1;
 };
-__device__ __forceinline__ Lane lane_of(long rows, int Cw, int EC, long rpb) {
+__device__ __forceinline__ Lane lane_of(long seg_rows, int bps, int Cw, int EC, long rpb) {
   Lane l;
   l.cg = Cw / EC;
   l.tpr = l.cg < kBlock ? l.cg : kBlock;
   l.rpp = kBlock / l.tpr;
   l.rl = threadIdx.x / l.tpr;
   l.g0 = threadIdx.x % l.tpr;
-  l.r0 = static_cast<long>(blockIdx.x) * rpb;
-  l.r1 = min(rows, l.r0 + rpb);
+  const SegRange r = seg_range(seg_rows, bps, rpb);
+  l.seg = r.seg;
+  l.r0 = r.r0;
+  l.r1 = r.r1;
   return l;
 }
 
@@ -142,21 +162,24 @@ __global__ void __launch_bounds__(128) bn_stats_finalize_kernel(const float* __r
 }
 
 // ------------------------------------------------------------ BN apply + act
+// Statistics are per channel (batch norm) or per segment = image (layer norm, ln != 0).
 template <typename T, int EC>
-__global__ void __launch_bounds__(kBlock) bn_apply_kernel(const T* __restrict__ pre, T* __restrict__ y, long rows,
-                                                          int C, long rpb, const float* __restrict__ mean,
+__global__ void __launch_bounds__(kBlock) bn_apply_kernel(const T* __restrict__ pre, T* __restrict__ y,
+                                                          long seg_rows, int bps, int C, long rpb, int ln,
+                                                          const float* __restrict__ mean,
                                                           const float* __restrict__ inv_std,
                                                           const float* __restrict__ gamma,
                                                           const float* __restrict__ beta, int act) {
-  const Lane l = lane_of(rows, C, EC, rpb);
+  const Lane l = lane_of(seg_rows, bps, C, EC, rpb);
   if (l.rl >= l.rpp) return;
   for (int g = l.g0; g < l.cg; g += l.tpr) {
     float mu[EC], sc[EC], be[EC];
 #pragma unroll
     for (int e = 0; e < EC; ++e) {
       const int c = g * EC + e;
-      mu[e] = mean[c];
-      sc[e] = gamma[c] * inv_std[c];
+      const int si = ln ? l.seg : c;
+      mu[e] = mean[si];
+      sc[e] = gamma[c] * inv_std[si];
       be[e] = beta[c];
     }
     for (long r = l.r0 + l.rl; r < l.r1; r += l.rpp) {
@@ -173,14 +196,14 @@ __global__ void __launch_bounds__(kBlock) bn_apply_kernel(const T* __restrict__ 
 // part[b][c] = {sum d_norm, sum d_norm * z}, d_norm = act'(gamma z + beta) dy.
 template <typename T, int EC>
 __global__ void __launch_bounds__(kBlock) bn_bwd_reduce_kernel(const T* __restrict__ pre, const T* __restrict__ dy,
-                                                               long rows, int C, long rpb,
+                                                               long seg_rows, int bps, int C, long rpb, int ln,
                                                                const float* __restrict__ mean,
                                                                const float* __restrict__ inv_std,
                                                                const float* __restrict__ gamma,
                                                                const float* __restrict__ beta, int act,
                                                                float* __restrict__ part) {
   __shared__ float s_a[kBlock * EC], s_b[kBlock * EC];
-  const Lane l = lane_of(rows, C, EC, rpb);
+  const Lane l = lane_of(seg_rows, bps, C, EC, rpb);
   for (int gb = 0; gb < l.cg; gb += l.tpr) {
     const int g = gb + l.g0;
     const bool active = g < l.cg && l.rl < l.rpp;
@@ -192,8 +215,9 @@ __global__ void __launch_bounds__(kBlock) bn_bwd_reduce_kernel(const T* __restri
 #pragma unroll
       for (int e = 0; e < EC; ++e) {
         const int c = g * EC + e;
-        mu[e] = mean[c];
-        is[e] = inv_std[c];
+        const int si = ln ? l.seg : c;
+        mu[e] = mean[si];
+        is[e] = inv_std[si];
         ga[e] = gamma[c];
         be[e] = beta[c];
       }
@@ -232,11 +256,30 @@ __global__ void __launch_bounds__(kBlock) bn_bwd_reduce_kernel(const T* __restri
   }
 }
 
-// d_conv = gamma*inv_std*(d_norm - c1/n - z*c2/n); part[b][c] = sum d_conv.
-// MODE 0: batch norm; MODE 1: no norm (d_conv = act'(pre) * dy).
+// Normalisation coefficients of d_conv = inv_std * (gamma * d_norm - K1 - z * K2):
+//   batch norm  K1 = gamma * c1[c] / n,   K2 = gamma * c2[c] / n    (n = rows; c12 = [C][2] sums)
+//   layer norm  K1 = s1[seg] / M,         K2 = s2[seg] / M          (M = seg_rows * C; per-image sums
+//               of gamma * d_norm and gamma * d_norm * z stored after the channel sums: c12 + 2C)
+//   no c12      evaluation-mode batch norm, no projection terms.
+__device__ __forceinline__ void norm_bwd_coef(const float* c12, int ln, int seg, int c, int C, float ga,
+                                              long seg_rows, float& k1, float& k2) {
+  if (!c12) {
+    k1 = k2 = 0.f;
+  } else if (ln) {
+    const float inv_m = 1.f / static_cast<float>(seg_rows * C);
+    k1 = c12[2 * C + 2 * seg] * inv_m;
+    k2 = c12[2 * C + 2 * seg + 1] * inv_m;
+  } else {
+    const float inv_n = 1.f / static_cast<float>(seg_rows);
+    k1 = ga * c12[2 * c] * inv_n;
+    k2 = ga * c12[2 * c + 1] * inv_n;
+  }
+}
+
+// part[b][c] = sum d_conv. MODE 0: batch / layer norm; MODE 1: no norm (d_conv = act'(pre) * dy).
 template <typename T, int EC, int MODE>
 __global__ void __launch_bounds__(kBlock) dconv_kernel(const T* __restrict__ pre, const T* __restrict__ dy,
-                                                       long rows, int C, int Cp, long rpb,
+                                                       long seg_rows, int bps, int C, int Cp, long rpb, int ln,
                                                        const float* __restrict__ mean,
                                                        const float* __restrict__ inv_std,
                                                        const float* __restrict__ gamma,
@@ -245,8 +288,7 @@ __global__ void __launch_bounds__(kBlock) dconv_kernel(const T* __restrict__ pre
                                                        float* __restrict__ part) {
   __shared__ float s_a[kBlock * EC];
   // the walk covers Cp channels so that padded channels of d_conv get zeros
-  const Lane l = lane_of(rows, Cp, EC, rpb);
-  const float inv_n = 1.f / static_cast<float>(rows);
+  const Lane l = lane_of(seg_rows, bps, Cp, EC, rpb);
   for (int gb = 0; gb < l.cg; gb += l.tpr) {
     const int g = gb + l.g0;
     const bool active = g < l.cg && l.rl < l.rpp;
@@ -260,12 +302,12 @@ __global__ void __launch_bounds__(kBlock) dconv_kernel(const T* __restrict__ pre
       for (int e = 0; e < EC; ++e) {
         const int c = real ? g * EC + e : 0;
         if (MODE == 0) {
-          mu[e] = mean[c];
-          is[e] = inv_std[c];
+          const int si = ln ? l.seg : c;
+          mu[e] = mean[si];
+          is[e] = inv_std[si];
           ga[e] = gamma[c];
           be[e] = beta[c];
-          k1[e] = c12 ? c12[2 * c] * inv_n : 0.f;  // no c12: evaluation mode, no projection terms
-          k2[e] = c12 ? c12[2 * c + 1] * inv_n : 0.f;
+          norm_bwd_coef(c12, ln, l.seg, c, C, ga[e], seg_rows, k1[e], k2[e]);
         }
       }
       for (long r = l.r0 + l.rl; r < l.r1; r += l.rpp) {
@@ -279,7 +321,7 @@ __global__ void __launch_bounds__(kBlock) dconv_kernel(const T* __restrict__ pre
             if (MODE == 0) {
               const float z = (v[e] - mu[e]) * is[e];
               const float dn = dact_f(act, fmaf(ga[e], z, be[e])) * d[e];
-              o[e] = ga[e] * is[e] * (dn - k1[e] - z * k2[e]);
+              o[e] = is[e] * (ga[e] * dn - k1[e] - z * k2[e]);
             } else {
               o[e] = dact_f(act, v[e]) * d[e];
             }
@@ -459,6 +501,81 @@ __global__ void infer_fold_kernel(const float* bias, const float* gamma, const f
   }
 }
 
+// ------------------------------------------------------------ layer norm
+// Per-image statistics (`forward` LAYER_NORM branch, over OH*OW*OC of the
+// stored pre-activations) from the per-pixel, per-column-tile (mean, M2)
+// partials of the fprop epilogue: block n merges the partials of image n,
+// in fp32 per thread (Chan) and then in fp64 in a fixed tree.
+__global__ void __launch_bounds__(128) ln_stats_finalize_kernel(const float* __restrict__ rs, int n_tiles, int BN,
+                                                                int OC, long hw, float eps, float* mean,
+                                                                float* inv_std) {
+  __shared__ double s_n[128], s_m[128], s_M[128];
+  const long n_ent = hw * n_tiles;
+  const float* base = rs + static_cast<size_t>(blockIdx.x) * n_ent * 2;
+  float n = 0.f, m = 0.f, M = 0.f;
+  for (long e = threadIdx.x; e < n_ent; e += 128) {
+    const int t = static_cast<int>(e % n_tiles);
+    const float nb = static_cast<float>(min(BN, OC - t * BN));
+    const float mb = base[2 * e], Mb = base[2 * e + 1];
+    const float nn = n + nb, d = mb - m, f = nb / nn;
+    m = fmaf(d, f, m);
+    M += Mb + d * d * n * f;
+    n = nn;
+  }
+  s_n[threadIdx.x] = n;
+  s_m[threadIdx.x] = m;
+  s_M[threadIdx.x] = M;
+  __syncthreads();
+  for (int off = 64; off > 0; off >>= 1) {
+    if (threadIdx.x < off) {
+      const double na = s_n[threadIdx.x], nb = s_n[threadIdx.x + off];
+      if (nb > 0) {
+        const double nn = na + nb, d = s_m[threadIdx.x + off] - s_m[threadIdx.x];
+        s_m[threadIdx.x] += d * nb / nn;
+        s_M[threadIdx.x] += s_M[threadIdx.x + off] + d * d * na * nb / nn;
+        s_n[threadIdx.x] = nn;
+      }
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double var = s_n[0] > 0 ? s_M[0] / s_n[0] : 0.0;  // biased
+    mean[blockIdx.x] = static_cast<float>(s_m[0]);
+    inv_std[blockIdx.x] = static_cast<float>(1.0 / sqrt(var + static_cast<double>(eps)));
+  }
+}
+
+// Per-image sums of gamma * d_norm and gamma * d_norm * z (`backward_full`
+// training branch, NORM_DIM = batch) from the per-block, per-channel partials
+// part[b][c][2] of an image-aligned walk (bps blocks per image):
+// out[2n], out[2n+1].
+__global__ void __launch_bounds__(128) ln_seg_finalize_kernel(const float* __restrict__ part, int bps, int C,
+                                                              const float* __restrict__ gamma, float* out) {
+  __shared__ double s[2][128];
+  const long n_ent = static_cast<long>(bps) * C;
+  const float* base = part + static_cast<size_t>(blockIdx.x) * n_ent * 2;
+  float a = 0.f, b = 0.f;
+  for (long k = threadIdx.x; k < n_ent; k += 128) {
+    const float g = gamma[k % C];
+    a = fmaf(g, base[2 * k], a);
+    b = fmaf(g, base[2 * k + 1], b);
+  }
+  s[0][threadIdx.x] = a;
+  s[1][threadIdx.x] = b;
+  __syncthreads();
+  for (int off = 64; off > 0; off >>= 1) {
+    if (threadIdx.x < off) {
+      s[0][threadIdx.x] += s[0][threadIdx.x + off];
+      s[1][threadIdx.x] += s[1][threadIdx.x + off];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    out[2 * blockIdx.x] = static_cast<float>(s[0][0]);
+    out[2 * blockIdx.x + 1] = static_cast<float>(s[1][0]);
+  }
+}
+
 int grid_for(long total, int block) {
   long g = (total + block - 1) / block;
   if (g < 1) g = 1;
@@ -560,16 +677,18 @@ __device__ __forceinline__ bool stream_walk(const T* const (&in)[NIN], long r0, 
 
 template <typename T, int EC, int NIN>
 struct StreamSetup {
-  int cg, tpr, rpp, rl, g;
+  int cg, tpr, rpp, rl, g, seg;
   long r0, r1;
-  __device__ StreamSetup(long rows, int C, long rpb) {
+  __device__ StreamSetup(long seg_rows, int bps, int C, long rpb) {
     cg = C / EC;
     tpr = cg;  // the streamed path is used when C / EC <= kBlock
     rpp = kBlock / tpr;
     rl = threadIdx.x / tpr;
     g = threadIdx.x % tpr;
-    r0 = static_cast<long>(blockIdx.x) * rpb;
-    r1 = min(rows, r0 + rpb);
+    const SegRange r = seg_range(seg_rows, bps, rpb);
+    seg = r.seg;
+    r0 = r.r0;
+    r1 = r.r1;
   }
 };
 
@@ -582,21 +701,23 @@ __device__ __forceinline__ void stream_init(uint64_t* full) {
 }
 
 template <typename T, int EC>
-__global__ void __launch_bounds__(kBlock, 1) bn_apply_stream(const T* __restrict__ pre, T* __restrict__ y, long rows,
-                                                             int C, long rpb, int R, const float* __restrict__ mean,
+__global__ void __launch_bounds__(kBlock, 1) bn_apply_stream(const T* __restrict__ pre, T* __restrict__ y,
+                                                             long seg_rows, int bps, int C, long rpb, int R, int ln,
+                                                             const float* __restrict__ mean,
                                                              const float* __restrict__ inv_std,
                                                              const float* __restrict__ gamma,
                                                              const float* __restrict__ beta, int act, int* err) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t full[kStreamStages];
   stream_init(full);
-  const StreamSetup<T, EC, 1> st(rows, C, rpb);
+  const StreamSetup<T, EC, 1> st(seg_rows, bps, C, rpb);
   float mu[EC], sc[EC], be[EC];
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
     const int c = st.g * EC + e;
-    mu[e] = mean[c];
-    sc[e] = gamma[c] * inv_std[c];
+    const int si = ln ? st.seg : c;
+    mu[e] = mean[si];
+    sc[e] = gamma[c] * inv_std[si];
     be[e] = beta[c];
   }
   const T* const in[1] = {pre};
@@ -612,8 +733,8 @@ __global__ void __launch_bounds__(kBlock, 1) bn_apply_stream(const T* __restrict
 // part[b][c] = {sum d_norm, sum d_norm * z}
 template <typename T, int EC>
 __global__ void __launch_bounds__(kBlock, 1) bn_bwd_reduce_stream(const T* __restrict__ pre, const T* __restrict__ dy,
-                                                                  long rows, int C, long rpb, int R,
-                                                                  const float* __restrict__ mean,
+                                                                  long seg_rows, int bps, int C, long rpb, int R,
+                                                                  int ln, const float* __restrict__ mean,
                                                                   const float* __restrict__ inv_std,
                                                                   const float* __restrict__ gamma,
                                                                   const float* __restrict__ beta, int act,
@@ -622,13 +743,14 @@ __global__ void __launch_bounds__(kBlock, 1) bn_bwd_reduce_stream(const T* __res
   __shared__ uint64_t full[kStreamStages];
   __shared__ float s_a[kBlock * EC], s_b[kBlock * EC];
   stream_init(full);
-  const StreamSetup<T, EC, 2> st(rows, C, rpb);
+  const StreamSetup<T, EC, 2> st(seg_rows, bps, C, rpb);
   float mu[EC], is[EC], ga[EC], be[EC], a[EC], b[EC];
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
     const int c = st.g * EC + e;
-    mu[e] = mean[c];
-    is[e] = inv_std[c];
+    const int si = ln ? st.seg : c;
+    mu[e] = mean[si];
+    is[e] = inv_std[si];
     ga[e] = gamma[c];
     be[e] = beta[c];
     a[e] = b[e] = 0.f;
@@ -664,10 +786,10 @@ __global__ void __launch_bounds__(kBlock, 1) bn_bwd_reduce_stream(const T* __res
   }
 }
 
-// d_conv (MODE 0: batch norm, 1: no norm) and part[b][c] = sum d_conv.
+// d_conv (MODE 0: batch / layer norm, 1: no norm) and part[b][c] = sum d_conv.
 template <typename T, int EC, int MODE>
 __global__ void __launch_bounds__(kBlock, 1) dconv_stream(const T* __restrict__ pre, const T* __restrict__ dy,
-                                                          long rows, int C, long rpb, int R,
+                                                          long seg_rows, int bps, int C, long rpb, int R, int ln,
                                                           const float* __restrict__ mean,
                                                           const float* __restrict__ inv_std,
                                                           const float* __restrict__ gamma,
@@ -678,20 +800,19 @@ __global__ void __launch_bounds__(kBlock, 1) dconv_stream(const T* __restrict__ 
   __shared__ uint64_t full[kStreamStages];
   __shared__ float s_a[kBlock * EC];
   stream_init(full);
-  const StreamSetup<T, EC, 2> st(rows, C, rpb);
-  const float inv_n = 1.f / static_cast<float>(rows);
+  const StreamSetup<T, EC, 2> st(seg_rows, bps, C, rpb);
   float mu[EC], is[EC], ga[EC], be[EC], k1[EC], k2[EC], a[EC];
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
     const int c = st.g * EC + e;
     a[e] = 0.f;
     if (MODE == 0) {
-      mu[e] = mean[c];
-      is[e] = inv_std[c];
+      const int si = ln ? st.seg : c;
+      mu[e] = mean[si];
+      is[e] = inv_std[si];
       ga[e] = gamma[c];
       be[e] = beta[c];
-      k1[e] = c12 ? c12[2 * c] * inv_n : 0.f;  // no c12: evaluation mode, no projection terms
-      k2[e] = c12 ? c12[2 * c + 1] * inv_n : 0.f;
+      norm_bwd_coef(c12, ln, st.seg, c, C, ga[e], seg_rows, k1[e], k2[e]);
     }
   }
   const T* const in[2] = {pre, dy};
@@ -703,7 +824,7 @@ __global__ void __launch_bounds__(kBlock, 1) dconv_stream(const T* __restrict__ 
                             if (MODE == 0) {
                               const float z = (v[0][e] - mu[e]) * is[e];
                               const float dn = dact_f(act, fmaf(ga[e], z, be[e])) * v[1][e];
-                              o[e] = ga[e] * is[e] * (dn - k1[e] - z * k2[e]);
+                              o[e] = is[e] * (ga[e] * dn - k1[e] - z * k2[e]);
                             } else {
                               o[e] = dact_f(act, v[0][e]) * v[1][e];
                             }
@@ -725,33 +846,69 @@ __global__ void __launch_bounds__(kBlock, 1) dconv_stream(const T* __restrict__ 
 
 }  // namespace
 
-RowWalk make_walk(long rows, int C, int dtype, int sms) {
+// Blocks per segment for a walk of `segs` segments with `resident` blocks
+// resident on the GPU at once. Time model: waves * (rows per block + ovh),
+// ovh standing for a block's start-up (barrier set-up, first copies) in rows;
+// the smallest modelled time wins (ties go to fewer blocks).
+static int pick_bps(int segs, long seg_rows, long resident, long ovh) {
+  int best = 1;
+  double best_t = 1e300;
+  for (int b = 1; b <= 64; ++b) {
+    const long rpb = (seg_rows + b - 1) / b;
+    if (b > 1 && rpb < ovh / 2) break;
+    const double waves = std::ceil(static_cast<double>(segs) * b / static_cast<double>(resident));
+    const double t = waves * static_cast<double>(rpb + ovh);
+    if (t < best_t * (1 - 1e-9)) {
+      best_t = t;
+      best = b;
+    }
+  }
+  return best;
+}
+
+RowWalk make_walk(long rows, int C, int dtype, int sms, int segs) {
   RowWalk w;
   w.rows = rows;
   w.C = C;
   w.err = nullptr;
+  w.segs = segs < 1 ? 1 : segs;
+  w.seg_rows = rows / w.segs;
   const int ec = vec_ec(dtype, C);
   const long row_bytes = static_cast<long>(C) * (dtype == 1 ? 2 : 4);
   w.stream = (ec > 1 && C / ec <= kBlock && row_bytes <= kChunkBytes) ? 1 : 0;
-  if (w.stream) {
-    w.R = static_cast<int>(kChunkBytes / row_bytes);
-    long g = (rows + w.R - 1) / w.R;
-    if (g > sms) g = sms;
-    if (g < 1) g = 1;
-    w.G = static_cast<int>(g);
-    w.rows_per_block = (rows + w.G - 1) / w.G;
-    return w;
-  }
-  w.R = 0;
   const int cg = C / ec;
   const int tpr = cg < kBlock ? cg : kBlock;
   const int rpp = kBlock / tpr;
-  long g = (rows + rpp - 1) / rpp;
-  const long gmax = 8L * sms;
-  if (g > gmax) g = gmax;
-  if (g < 1) g = 1;
-  w.G = static_cast<int>(g);
-  w.rows_per_block = (rows + w.G - 1) / w.G;
+  if (w.segs == 1) {
+    // one persistent block per SM (streamed) or up to 8 per SM, each owning a contiguous slice
+    long g;
+    if (w.stream) {
+      w.R = static_cast<int>(kChunkBytes / row_bytes);
+      g = std::min<long>((rows + w.R - 1) / w.R, sms);
+    } else {
+      w.R = 0;
+      g = std::min<long>((rows + rpp - 1) / rpp, 8L * sms);
+    }
+    if (g < 1) g = 1;
+    w.G = static_cast<int>(g);
+    w.bps = w.G;
+    w.rows_per_block = (rows + w.G - 1) / w.G;
+    return w;
+  }
+  // several segments (one per image): blocks never straddle a segment; half-size chunks so that
+  // three streamed blocks fit on an SM and the last wave stays full
+  long resident;
+  if (w.stream) {
+    w.R = static_cast<int>(std::max<long>(1, (kChunkBytes / 2) / row_bytes));
+    const long smem = static_cast<long>(kStreamStages) * 2 * w.R * row_bytes;
+    resident = static_cast<long>(sms) * std::max<long>(1, std::min<long>(8, (220L * 1024) / smem));
+  } else {
+    w.R = 0;
+    resident = 8L * sms;
+  }
+  w.bps = pick_bps(w.segs, w.seg_rows, resident, 2L * std::max<long>(w.R, rpp));
+  w.G = w.segs * w.bps;
+  w.rows_per_block = (w.seg_rows + w.bps - 1) / w.bps;
   return w;
 }
 
@@ -828,20 +985,24 @@ cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float
     }                                                                                                   \
   } while (0)
 
+// Walk arguments shared by every row-walk kernel: segment geometry and the layer-norm flag.
+#define WALK_ARGS wk.seg_rows, wk.bps, wk.C, wk.rows_per_block
+#define LN_FLAG (wk.segs > 1 ? 1 : 0)
+
 cudaError_t launch_bn_apply(int dtype, const void* pre, void* y, const RowWalk& wk, const float* mean,
                             const float* inv_std, const float* gamma, const float* beta, int act, cudaStream_t st) {
   if (wk.stream) {
-    STREAM_LAUNCH(dtype, 1, (bn_apply_stream<T, EC>), static_cast<const T*>(pre), static_cast<T*>(y), wk.rows, wk.C,
-                  wk.rows_per_block, wk.R, mean, inv_std, gamma, beta, act, wk.err);
+    STREAM_LAUNCH(dtype, 1, (bn_apply_stream<T, EC>), static_cast<const T*>(pre), static_cast<T*>(y), WALK_ARGS,
+                  wk.R, LN_FLAG, mean, inv_std, gamma, beta, act, wk.err);
     return cudaGetLastError();
   }
   DISPATCH_EC(dtype, wk.C,
               (bn_apply_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), static_cast<T*>(y),
-                                                                 wk.rows, wk.C, wk.rows_per_block, mean, inv_std,
-                                                                 gamma, beta, act)),
+                                                                 WALK_ARGS, LN_FLAG, mean, inv_std, gamma, beta,
+                                                                 act)),
               (bn_apply_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), static_cast<T*>(y),
-                                                                 wk.rows, wk.C, wk.rows_per_block, mean, inv_std,
-                                                                 gamma, beta, act)));
+                                                                 WALK_ARGS, LN_FLAG, mean, inv_std, gamma, beta,
+                                                                 act)));
   return cudaGetLastError();
 }
 
@@ -850,18 +1011,16 @@ cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, con
                                  cudaStream_t st) {
   if (wk.stream) {
     STREAM_LAUNCH(dtype, 2, (bn_bwd_reduce_stream<T, EC>), static_cast<const T*>(pre), static_cast<const T*>(dy),
-                  wk.rows, wk.C, wk.rows_per_block, wk.R, mean, inv_std, gamma, beta, act, part, wk.err);
+                  WALK_ARGS, wk.R, LN_FLAG, mean, inv_std, gamma, beta, act, part, wk.err);
     return cudaGetLastError();
   }
   DISPATCH_EC(dtype, wk.C,
               (bn_bwd_reduce_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
-                                                                      static_cast<const T*>(dy), wk.rows, wk.C,
-                                                                      wk.rows_per_block, mean, inv_std, gamma, beta,
-                                                                      act, part)),
+                                                                      static_cast<const T*>(dy), WALK_ARGS, LN_FLAG,
+                                                                      mean, inv_std, gamma, beta, act, part)),
               (bn_bwd_reduce_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
-                                                                      static_cast<const T*>(dy), wk.rows, wk.C,
-                                                                      wk.rows_per_block, mean, inv_std, gamma, beta,
-                                                                      act, part)));
+                                                                      static_cast<const T*>(dy), WALK_ARGS, LN_FLAG,
+                                                                      mean, inv_std, gamma, beta, act, part)));
   return cudaGetLastError();
 }
 
@@ -875,45 +1034,60 @@ cudaError_t launch_bn_bwd_apply(int dtype, const void* pre, const void* dy, cons
                                 const float* mean, const float* inv_std, const float* gamma, const float* beta,
                                 int act, const float* c12, void* dconv, float* part, cudaStream_t st) {
   if (wk.stream && wk.C == Cp) {
-    STREAM_LAUNCH(dtype, 2, (dconv_stream<T, EC, 0>), static_cast<const T*>(pre), static_cast<const T*>(dy), wk.rows,
-                  wk.C, wk.rows_per_block, wk.R, mean, inv_std, gamma, beta, act, c12, static_cast<T*>(dconv), part,
+    STREAM_LAUNCH(dtype, 2, (dconv_stream<T, EC, 0>), static_cast<const T*>(pre), static_cast<const T*>(dy),
+                  WALK_ARGS, wk.R, LN_FLAG, mean, inv_std, gamma, beta, act, c12, static_cast<T*>(dconv), part,
                   wk.err);
     return cudaGetLastError();
   }
   // the vector path needs C == Cp (EC divides C); otherwise one channel per thread
   DISPATCH_EC(dtype, (wk.C == Cp ? wk.C : 1),
               (dconv_kernel<T, EC, 0><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
-                                                                 static_cast<const T*>(dy), wk.rows, wk.C, Cp,
-                                                                 wk.rows_per_block, mean, inv_std, gamma, beta, act,
-                                                                 c12, static_cast<T*>(dconv), part)),
+                                                                 static_cast<const T*>(dy), wk.seg_rows, wk.bps, wk.C,
+                                                                 Cp, wk.rows_per_block, LN_FLAG, mean, inv_std, gamma,
+                                                                 beta, act, c12, static_cast<T*>(dconv), part)),
               (dconv_kernel<T, EC, 0><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
-                                                                 static_cast<const T*>(dy), wk.rows, wk.C, Cp,
-                                                                 wk.rows_per_block, mean, inv_std, gamma, beta, act,
-                                                                 c12, static_cast<T*>(dconv), part)));
+                                                                 static_cast<const T*>(dy), wk.seg_rows, wk.bps, wk.C,
+                                                                 Cp, wk.rows_per_block, LN_FLAG, mean, inv_std, gamma,
+                                                                 beta, act, c12, static_cast<T*>(dconv), part)));
   return cudaGetLastError();
 }
 
 cudaError_t launch_act_bwd(int dtype, const void* pre, const void* dy, const RowWalk& wk, int Cp, int act,
                            void* dconv, float* part, cudaStream_t st) {
   if (wk.stream && wk.C == Cp) {
-    STREAM_LAUNCH(dtype, 2, (dconv_stream<T, EC, 1>), static_cast<const T*>(pre), static_cast<const T*>(dy), wk.rows,
-                  wk.C, wk.rows_per_block, wk.R, nullptr, nullptr, nullptr, nullptr, act, nullptr,
-                  static_cast<T*>(dconv), part, wk.err);
+    STREAM_LAUNCH(dtype, 2, (dconv_stream<T, EC, 1>), static_cast<const T*>(pre), static_cast<const T*>(dy),
+                  WALK_ARGS, wk.R, 0, nullptr, nullptr, nullptr, nullptr, act, nullptr, static_cast<T*>(dconv), part,
+                  wk.err);
     return cudaGetLastError();
   }
   DISPATCH_EC(dtype, (wk.C == Cp ? wk.C : 1),
               (dconv_kernel<T, EC, 1><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
-                                                                 static_cast<const T*>(dy), wk.rows, wk.C, Cp,
-                                                                 wk.rows_per_block, nullptr, nullptr, nullptr,
+                                                                 static_cast<const T*>(dy), wk.seg_rows, wk.bps, wk.C,
+                                                                 Cp, wk.rows_per_block, 0, nullptr, nullptr, nullptr,
                                                                  nullptr, act, nullptr, static_cast<T*>(dconv),
                                                                  part)),
               (dconv_kernel<T, EC, 1><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
-                                                                 static_cast<const T*>(dy), wk.rows, wk.C, Cp,
-                                                                 wk.rows_per_block, nullptr, nullptr, nullptr,
+                                                                 static_cast<const T*>(dy), wk.seg_rows, wk.bps, wk.C,
+                                                                 Cp, wk.rows_per_block, 0, nullptr, nullptr, nullptr,
                                                                  nullptr, act, nullptr, static_cast<T*>(dconv),
                                                                  part)));
   return cudaGetLastError();
 }
+
+cudaError_t launch_ln_stats_finalize(const float* rstats, int n_images, long hw, int n_tiles, int BN, int OC,
+                                     float eps, float* mean, float* inv_std, cudaStream_t st) {
+  ln_stats_finalize_kernel<<<n_images, 128, 0, st>>>(rstats, n_tiles, BN, OC, hw, eps, mean, inv_std);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ln_seg_finalize(const float* part, const RowWalk& wk, const float* gamma, float* out,
+                                   cudaStream_t st) {
+  ln_seg_finalize_kernel<<<wk.segs, 128, 0, st>>>(part, wk.bps, wk.C, gamma, out);
+  return cudaGetLastError();
+}
+
+#undef WALK_ARGS
+#undef LN_FLAG
 
 cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int taps, int ICp, int IC, float* dw,
                                 cudaStream_t st) {

@@ -88,6 +88,8 @@ struct ConvGemmParams {
   int act, out_act;       // out = out_act ? act(v) : T(v); out2 = act(T(v))
   float* stats;           // optional batch statistics (count, mean, M2) of v: [m_tile][N][3], or
   int stats_per_cta;      // [blockIdx][N][3] merged over the CTA's tiles (single column tile only)
+  float* rstats;          // optional layer-norm partials of the stored value, one per output pixel and
+                          // column tile: [pixel][n_tiles][2] = (mean, M2) over the tile's columns
   // A operand by TMA im2col (bf16, Cs a multiple of 64, one phase): the map
   // walks the row domain; a k-block is (tap, 64-channel chunk) and the tap is
   // the im2col offset, so taps must be non-negative offsets from the window
@@ -526,6 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         const int oh = ph.oh0 + a * p.os, ow = ph.ow0 + b * p.os;
         obase = (static_cast<size_t>(n * p.Ho + oh) * p.Wo + ow) * p.out_ld;
       }
+      // layer-norm partials of this row over the tile's columns: exact two-pass per 32 columns, merged
+      // across the chunks with Chan's formula (the chunks before column cc hold cc values)
+      float rmean = 0.f, rm2 = 0.f;
       const bool zero = ph.num_kb == 0;
       const bool one_pass = p.stats && have_shift;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
@@ -566,6 +571,22 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           float o[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = p.out_act ? act_f(p.act, v[e]) : to_stored<T>(v[e]);
+          if (p.rstats) {  // o holds the stored value (the host never combines rstats with out_act)
+            const int nc = ncols < 32 ? ncols : 32;
+            float sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sum += e < nc ? o[e] : 0.f;
+            const float fnc = static_cast<float>(nc), cm = sum / fnc;
+            float m2 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float d = e < nc ? o[e] - cm : 0.f;
+              m2 = fmaf(d, d, m2);
+            }
+            const float rn = static_cast<float>(cc), nn = rn + fnc, dl = cm - rmean, f = fnc / nn;
+            rmean = fmaf(dl, f, rmean);
+            rm2 += m2 + dl * dl * rn * f;
+          }
           store_row32<T>(out + obase + col0, o, ncols, vec);
           if (out2) {
 #pragma unroll
@@ -579,6 +600,11 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         fetch(c0, ra, rb);
         pass1(c0, ra);
         if (c0 + 32 < BN) pass1(c0 + 32, rb);
+      }
+      if (p.rstats && valid) {
+        float* o = p.rstats + (obase / p.out_ld * p.n_tiles + n_tile) * 2;
+        o[0] = rmean;
+        o[1] = rm2;
       }
       if (one_pass) {
         // shifted sums d = v - s with s the previous tile's mean:

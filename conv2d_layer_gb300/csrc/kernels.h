@@ -21,17 +21,22 @@ struct DgradWeightTable {
 };
 
 // Row walk of an NHWC tensor seen as [rows][C]: G blocks, each owning a
-// contiguous slice of rows.
+// contiguous slice of rows. The rows form `segs` segments of seg_rows rows
+// (1 segment for batch norm and no norm; one per image for layer norm), each
+// split over bps blocks, so that no block straddles a segment and the
+// per-block partials of one segment are contiguous (block = seg * bps + j).
 struct RowWalk {
   long rows;
   int C;
   int G;
   long rows_per_block;
+  int segs, bps;
+  long seg_rows;
   int stream;  // rows move through shared memory by bulk TMA copies (vector path)
   int R;       // rows per streamed chunk
   int* err;    // device error word for bounded waits
 };
-RowWalk make_walk(long rows, int C, int dtype, int sms);
+RowWalk make_walk(long rows, int C, int dtype, int sms, int segs);
 
 // elementwise / reduction kernels (bn_kernels.cu); dtype 0 = fp32, 1 = bf16
 cudaError_t launch_pack_channels(int dtype, const void* src, void* dst, long rows, int C, int Cp, cudaStream_t st);
@@ -51,11 +56,20 @@ cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, con
 // mode 1: dbias += s0.
 cudaError_t launch_sum_finalize(const float* part, const RowWalk& wk, int nv, int mode, float* c12, float* acc0,
                                 float* acc1, cudaStream_t st);
+// d_conv under batch norm (c12 = per-channel sums from launch_sum_finalize; null: evaluation mode) or,
+// on a segmented walk, layer norm (c12 + 2C = the per-image sums of launch_ln_seg_finalize).
 cudaError_t launch_bn_bwd_apply(int dtype, const void* pre, const void* dy, const RowWalk& wk, int Cp,
                                 const float* mean, const float* inv_std, const float* gamma, const float* beta,
                                 int act, const float* c12, void* dconv, float* part, cudaStream_t st);
 cudaError_t launch_act_bwd(int dtype, const void* pre, const void* dy, const RowWalk& wk, int Cp, int act,
                            void* dconv, float* part, cudaStream_t st);
+// Layer norm: per-image mean / inv_std from the fprop epilogue's per-pixel, per-column-tile (mean, M2)
+// partials [n_images * hw][n_tiles][2]; per-image sums of gamma * d_norm and gamma * d_norm * z from the
+// bwd-reduce partials of an image-aligned walk, written to out[2n], out[2n + 1].
+cudaError_t launch_ln_stats_finalize(const float* rstats, int n_images, long hw, int n_tiles, int BN, int OC,
+                                     float eps, float* mean, float* inv_std, cudaStream_t st);
+cudaError_t launch_ln_seg_finalize(const float* part, const RowWalk& wk, const float* gamma, float* out,
+                                   cudaStream_t st);
 cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int taps, int ICp, int IC, float* dw,
                                 cudaStream_t st);
 cudaError_t launch_bn_eval_stats(const float* rm, const float* rv, float eps, int C, float* mean, float* inv_std,

@@ -31,8 +31,10 @@ class Conv2dLayer:
         y_shape = (spec.N, spec.OH, spec.OW, spec.OC)
         self.pre_act = torch.empty(y_shape, device=dev, dtype=self.dt)
         self.y = torch.empty(y_shape, device=dev, dtype=self.dt)
-        self.save_mean = torch.zeros(spec.OC, **f32)
-        self.save_inv_std = torch.zeros(spec.OC, **f32)
+        # saved statistics: per channel (batch norm) or per image (layer norm)
+        n_stat = spec.N if spec.norm == abi.NORM_LAYER else spec.OC
+        self.save_mean = torch.zeros(n_stat, **f32)
+        self.save_inv_std = torch.zeros(n_stat, **f32)
         self.dw = torch.zeros(spec.OC, spec.KH, spec.KW, spec.IC, **f32)
         self.db = torch.zeros(spec.OC, **f32)
         self.dgamma = torch.zeros(spec.OC, **f32)
@@ -47,10 +49,11 @@ class Conv2dLayer:
 
     def fwd_train(self, x, stream=None):
         bn = self.spec.norm == abi.NORM_BATCH
-        abi.check(abi.conv2d_fwd_train(self.desc, x, self.w, self.b, self.gamma if bn else None,
-                                       self.beta if bn else None, self.running_mean if bn else None,
+        nrm = self.spec.norm != abi.NORM_NONE
+        abi.check(abi.conv2d_fwd_train(self.desc, x, self.w, self.b, self.gamma if nrm else None,
+                                       self.beta if nrm else None, self.running_mean if bn else None,
                                        self.running_var if bn else None, self.pre_act,
-                                       self.save_mean if bn else None, self.save_inv_std if bn else None, self.y,
+                                       self.save_mean if nrm else None, self.save_inv_std if nrm else None, self.y,
                                        self.ws, stream=stream), "conv2d_fwd_train")
         return self.y
 
@@ -61,7 +64,7 @@ class Conv2dLayer:
         return y
 
     def bwd(self, x, dy, need_dx=True, need_params=True, stream=None):
-        bn = self.spec.norm == abi.NORM_BATCH
+        bn = self.spec.norm != abi.NORM_NONE  # batch or layer norm
         abi.check(abi.conv2d_bwd(self.desc, x, self.w, self.gamma if bn else None, self.beta if bn else None,
                                  self.pre_act, self.save_mean if bn else None, self.save_inv_std if bn else None, dy,
                                  self.dx if need_dx else None, self.dw if need_params else None,

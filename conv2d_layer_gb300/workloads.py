@@ -25,7 +25,7 @@ import math
 import torch
 
 FP32, BF16 = 0, 1
-NORM_NONE, NORM_BATCH = 0, 1
+NORM_NONE, NORM_BATCH, NORM_LAYER = 0, 1, 2
 ACT_IDENTITY, ACT_RELU, ACT_TANH, ACT_SIGMOID = 0, 1, 2, 3
 
 

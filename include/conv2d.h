@@ -3,7 +3,7 @@
  * (libconv2d.so).
  *
  * One NHWC 2D convolution layer: conv + bias, optional training-mode batch
- * norm, activation; and its backward pass. The operation is the one defined by
+ * norm or layer norm, activation; and its backward pass. The operation is the one defined by
  * the rl-tools conv2d layer pages ("operations_generic.h": `forward`,
  * `evaluate`, `backward`, `backward_input`, `backward_full`; the CUDA page
  * "operations_cuda.h" splits the same work into cuDNN calls and per-channel
@@ -51,13 +51,16 @@ extern "C" {
 enum {
     CONV2D_OK = 0,
     CONV2D_ERR_INVALID_ARG = 1, /* bad size, NULL or misaligned pointer, bad enum, eps<=0, momentum outside [0,1] */
-    CONV2D_ERR_UNSUPPORTED = 2, /* valid but not implemented (layer norm, stride > 8, sizes beyond 2^31 elements) */
+    CONV2D_ERR_UNSUPPORTED = 2, /* valid but not implemented (stride > 8, sizes beyond 2^31 elements) */
     CONV2D_ERR_WORKSPACE = 3,   /* ws NULL or smaller than conv2d_workspace_size() */
     CONV2D_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed (launch, tensor-map encode) */
     CONV2D_ERR_TIMEOUT = 5      /* a device-side bounded wait expired (reported by conv2d_device_status) */
 };
 
-/* Normalization (the pages' `Normalization` enum; LAYER_NORM is not implemented). */
+/* Normalization (the pages' `Normalization` enum). BATCH: per-channel
+ * statistics over N*OH*OW with running statistics. LAYER: per-image
+ * statistics over OH*OW*OC of the stored pre-activations (the pages'
+ * LAYER_NORM branches), per-channel gamma / beta, no running statistics. */
 enum { CONV2D_NORM_NONE = 0, CONV2D_NORM_BATCH = 1, CONV2D_NORM_LAYER = 2 };
 
 /* Activation applied after (optional) normalization. */
@@ -71,13 +74,15 @@ enum { CONV2D_FP32 = 0, CONV2D_BF16 = 1 };
 /* Operation selector for conv2d_workspace_size(). */
 enum { CONV2D_OP_FWD_TRAIN = 0, CONV2D_OP_FWD_INFER = 1, CONV2D_OP_BWD = 2 };
 
-/* Layer spec. eps and momentum are read only when norm == CONV2D_NORM_BATCH
+/* Layer spec. eps is read for BATCH and LAYER norm (1/sqrt(var+eps), biased
+ * variance); momentum only for BATCH
  * (running = (1-momentum)*running + momentum*batch, biased batch variance).
  * bn_eval != 0 selects batch norm in evaluation mode inside training (the
  * pages' mode::Evaluation): conv2d_fwd_train normalises with the running
  * statistics, writes them as save_mean / save_inv_std (= 1/sqrt(var+eps)) and
  * updates nothing; conv2d_bwd then uses the frozen-statistics backward
- * (d_conv = act'(bn) * dy * gamma * inv_std). Zero keeps training mode. */
+ * (d_conv = act'(bn) * dy * gamma * inv_std). Zero keeps training mode.
+ * Layer norm has no evaluation mode on the pages: bn_eval is ignored there. */
 typedef struct {
     int32_t N, H, W, IC, OC, KH, KW, stride, pad;
     int32_t norm, act, dtype;
@@ -98,10 +103,13 @@ size_t conv2d_workspace_size(const conv2d_desc* desc, int op);
  * statistics, affine and activation kernels on the CUDA page).
  *   pre_act  [N][OH][OW][OC] out: conv + bias (the pages' `pre_activations`)
  *   y        [N][OH][OW][OC] out: activation(normalised pre_act)
- *   BATCH norm only (else may be NULL):
+ *   BATCH norm (else may be NULL):
  *     gamma, beta [OC] in; running_mean, running_var [OC] in/out (EMA update);
  *     save_mean, save_inv_std [OC] out: batch mean and 1/sqrt(var+eps) that
  *     conv2d_bwd needs.
+ *   LAYER norm: gamma, beta [OC] in; save_mean, save_inv_std [N] out: the
+ *     per-image mean and 1/sqrt(var+eps) of the stored pre_act;
+ *     running_mean / running_var are not read and may be NULL.
  *   bias may be NULL (treated as zero). */
 int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, const float* bias,
                      const float* gamma, const float* beta, float* running_mean, float* running_var,
@@ -130,19 +138,21 @@ int conv2d_fwd_train_noalloc(const conv2d_desc* desc, const void* x, const void*
 
 /* Inference forward (`evaluate`): y = act(norm(conv + bias)), batch norm with
  * the running statistics (`bn_stats_eval` / `bn_forward_eval_running` on the
- * CUDA page); no state is written. gamma, beta, running_mean, running_var are
- * read only for BATCH norm. */
+ * CUDA page), layer norm with per-image statistics of the stored conv output
+ * computed on the fly; no state is written. gamma, beta are read for BATCH
+ * and LAYER norm, running_mean, running_var only for BATCH. */
 int conv2d_fwd_infer(const conv2d_desc* desc, const void* x, const void* w, const float* bias,
                      const float* gamma, const float* beta, const float* running_mean,
                      const float* running_var, void* y, void* ws, size_t ws_bytes, void* stream);
 
 /* Backward (`backward_full`; `backward_input` when dw..dbeta are all NULL;
- * `backward` when dx is NULL). Inputs: x, w, pre_act and (BATCH) gamma, beta,
- * save_mean, save_inv_std from conv2d_fwd_train, dy = dLoss/dy.
+ * `backward` when dx is NULL). Inputs: x, w, pre_act and (BATCH / LAYER)
+ * gamma, beta, save_mean, save_inv_std from conv2d_fwd_train, dy = dLoss/dy.
  *   dx [N][H][W][IC]   out (overwritten), may be NULL
  *   dw [OC][KH][KW][IC], dbias [OC]        accumulated, may be NULL together
- *   dgamma, dbeta [OC] (BATCH norm only)    accumulated, may be NULL together
- * Batch-norm backward uses the saved batch statistics, not recomputed ones.
+ *   dgamma, dbeta [OC] (BATCH / LAYER)      accumulated, may be NULL together
+ * The norm backward uses the saved statistics, not recomputed ones; under
+ * layer norm its projection sums run over each image (OH*OW*OC elements).
  * At least one of dx / dw must be non-NULL. */
 int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const float* gamma,
                const float* beta, const void* pre_act, const float* save_mean,

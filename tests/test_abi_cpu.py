@@ -49,8 +49,7 @@ def test_out_hw():
     ("pad", -1, abi.ERR_INVALID_ARG), ("KH", 11, abi.ERR_INVALID_ARG), ("norm", 3, abi.ERR_INVALID_ARG),
     ("act", 4, abi.ERR_INVALID_ARG), ("dtype", 2, abi.ERR_INVALID_ARG), ("eps", 0.0, abi.ERR_INVALID_ARG),
     ("eps", float("nan"), abi.ERR_INVALID_ARG), ("momentum", 1.5, abi.ERR_INVALID_ARG),
-    ("momentum", -0.1, abi.ERR_INVALID_ARG), ("norm", abi.NORM_LAYER, abi.ERR_UNSUPPORTED),
-    ("stride", 9, abi.ERR_UNSUPPORTED),
+    ("momentum", -0.1, abi.ERR_INVALID_ARG), ("stride", 9, abi.ERR_UNSUPPORTED),
 ])
 def test_validation_codes(field, value, code):
     d = good()
@@ -61,6 +60,15 @@ def test_validation_codes(field, value, code):
 
 def test_eps_and_momentum_ignored_without_norm():
     assert abi.conv2d_validate(good(norm=abi.NORM_NONE, eps=0.0, momentum=7.0)) == abi.OK
+
+
+def test_layer_norm_reads_eps_not_momentum():
+    assert abi.conv2d_validate(good(norm=abi.NORM_LAYER)) == abi.OK
+    assert abi.conv2d_validate(good(norm=abi.NORM_LAYER, momentum=7.0)) == abi.OK
+    assert abi.conv2d_validate(good(norm=abi.NORM_LAYER, eps=0.0)) == abi.ERR_INVALID_ARG
+    d = good(norm=abi.NORM_LAYER, dtype=abi.BF16, H=56, W=56, IC=256, OC=256)
+    for op in (abi.OP_FWD_TRAIN, abi.OP_FWD_INFER, abi.OP_BWD):
+        assert abi.conv2d_workspace_size(d, op) > 0
 
 
 def test_workspace_sizes_positive_and_op_checked():
@@ -86,8 +94,13 @@ def test_null_and_misaligned_pointers_rejected_before_launch():
     assert rc == abi.ERR_INVALID_ARG  # batch norm needs gamma, beta, running and saved statistics
     rc = abi.conv2d_bwd(d, al, al, None, None, al, None, None, al, None, None, None, None, None, al, 1 << 15, 0)
     assert rc == abi.ERR_INVALID_ARG  # neither dx nor dw requested
-    rc = abi.conv2d_fwd_infer(good(norm=abi.NORM_LAYER), al, al, None, None, None, None, None, al, al, 1 << 15, 0)
-    assert rc == abi.ERR_UNSUPPORTED
+    dln = good(norm=abi.NORM_LAYER)
+    rc = abi.conv2d_fwd_infer(dln, al, al, None, None, None, None, None, al, al, 1 << 15, 0)
+    assert rc == abi.ERR_INVALID_ARG  # layer norm needs gamma, beta
+    rc = abi.conv2d_fwd_train(dln, al, al, None, al, al, None, None, al, None, None, al, al, 1 << 15, 0)
+    assert rc == abi.ERR_INVALID_ARG  # ... and the saved per-image statistics
+    rc = abi.conv2d_bwd(dln, al, al, al, al, al, None, None, al, al, None, None, None, None, al, 1 << 15, 0)
+    assert rc == abi.ERR_INVALID_ARG
 
 
 def test_status_strings():
