@@ -32,7 +32,7 @@ NOMINAL_BF16_TFLOPS = 2250.0
 # DRAM bytes (read + write) per launch of the GEMM kernels on the 256-image layer, from the ncu capture
 # summarised in profiles/large_step_kernels.md (96-image case, scaled by 256/96). Reset to None whenever
 # a GEMM kernel changes and re-capture.
-NCU_TRAFFIC_BYTES = {"fprop_gemm": 704e6, "dgrad_gemm": 688e6, "wgrad_gemm": 831e6}
+NCU_TRAFFIC_BYTES = {"fprop_gemm": 686e6, "dgrad_gemm": 680e6, "wgrad_gemm": 823e6}
 
 
 def _peaks():
@@ -200,19 +200,43 @@ def run_gpu(args, rank, world, local_rank):
                 d2h=d2h, n_e2e=n_e2e)
 
 
-def per_config_timing(steps=10, warmup=3):
-    """TFLOP/s of fwd_train + bwd for every workload (the mixed stack as its two chained layers)."""
+# Per-launch algorithmic bytes of the bandwidth-bound kernels, in units of one [n_pix][OC] tensor of the
+# layer's element type: apply reads pre_act and writes y; the backward reduce reads pre_act and dY; d_conv
+# reads both and writes d_conv.
+HBM_TENSORS = {"bn_apply": 2, "ln_apply": 2, "bn_bwd_reduce": 2, "ln_bwd_reduce": 2, "bn_bwd_dconv": 3,
+               "ln_bwd_dconv": 3, "act_bwd_dconv": 3}
+
+PER_CONFIG = (
+    # (label, workload, overrides of every layer spec)
+    ("tiny", "tiny", {}),
+    ("rl", "rl", {}),
+    ("bn", "bn", {}),
+    ("mixed", "mixed", {}),
+    ("large", "large", {}),
+    ("bn+layernorm", "bn", {"norm": 2}),
+    ("large+layernorm", "large", {"norm": 2}),
+)
+
+
+def per_config_timing(peaks, steps=10, warmup=3):
+    """fwd_train + bwd of every workload (the mixed stack as its two chained layers) and of the BN-layer and
+    large shapes with layer norm: step time, TFLOP/s, and per-kernel times from one extra profiled step,
+    with the HBM fraction of the bandwidth-bound kernels."""
     import torch
 
+    from dataclasses import replace
+
+    from conv2d_layer_gb300 import abi
     from conv2d_layer_gb300.layer import Conv2dLayer
     from conv2d_layer_gb300.workloads import WORKLOADS, make_inputs
 
     out = {}
-    for name in ("tiny", "rl", "bn", "mixed", "large"):
+    for label, name, over in PER_CONFIG:
         wl = WORKLOADS[name]
-        inp = make_inputs(name)
+        specs = [replace(s, **over) for s in wl.layers]
+        inp = make_inputs(name, layers=specs)
         layers = [Conv2dLayer(s, li.w, li.b, li.gamma, li.beta, li.running_mean, li.running_var)
-                  for s, li in zip(wl.layers, inp["layers"])]
+                  for s, li in zip(specs, inp["layers"])]
         x, dy = inp["x"].cuda(), inp["dy"].cuda()
 
         def step():
@@ -233,11 +257,25 @@ def per_config_timing(steps=10, warmup=3):
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
-        fl = sum(s.flops_step() for s in wl.layers)
-        out[name] = {"ms_per_step": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
-                     "dtype": "bf16" if wl.layers[0].dtype == 1 else "fp32 (3xTF32)", "layers": len(wl.layers)}
+        abi.conv2d_prof_enable(True)
+        abi.conv2d_prof_read()
+        step()
+        torch.cuda.synchronize()
+        abi.conv2d_prof_enable(False)
+        kern = {}
+        for kname, t in abi.conv2d_prof_read(4096):
+            kern[kname] = kern.get(kname, 0.0) + t
+        fl = sum(s.flops_step() for s in specs)
+        s0 = specs[-1]
+        tensor_bytes = s0.n_pix * s0.OC * (2 if s0.dtype == 1 else 4)
+        hbm = {k: round(HBM_TENSORS[k] * tensor_bytes / (t * 1e-3) / 1e9 / peaks["hbm"], 3)
+               for k, t in kern.items() if k in HBM_TENSORS and len(specs) == 1}
+        out[label] = {"ms_per_step": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
+                      "dtype": "bf16" if specs[0].dtype == 1 else "fp32 (3xTF32)", "layers": len(specs),
+                      "kernels_ms": {k: round(t, 4) for k, t in kern.items()}, "hbm_frac_of_measured": hbm}
         del layers, x, dy, inp
         torch.cuda.empty_cache()
+    abi.check(abi.conv2d_device_status()[0], "device status")
     return out
 
 
@@ -366,7 +404,7 @@ def main():
     ms, e2e_ms = r["ms"], r["e2e_ms"]
     per_cfg = None
     if rank == 0 and world == 1 and not args.no_per_config and not args.images:
-        per_cfg = per_config_timing()
+        per_cfg = per_config_timing(_peaks())
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([ms, e2e_ms], device="cuda")
