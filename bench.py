@@ -142,22 +142,34 @@ def run_gpu(args, rank, world, local_rank):
     abi.conv2d_prof_read()
     step()
     per_step = len(abi.conv2d_prof_read())
+    abi.conv2d_prof_enable(False)
+
+    def timed(n, instrumented):
+        # n steps between two events on the launching stream; with `instrumented` the library also
+        # brackets every launch with its own CUDA events (per-kernel durations), which costs a little
+        if instrumented:
+            abi.conv2d_prof_enable(True)
+            abi.conv2d_prof_read()
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        recs = []
+        if instrumented:
+            abi.conv2d_prof_enable(False)
+            recs = abi.conv2d_prof_read(8192)
+        return e0.elapsed_time(e1) / n, recs
 
     clocks = Clocks(local_rank)
-    barrier()
-    torch.cuda.synchronize()
     clocks.start()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
+    ms, _ = timed(args.steps, False)                   # the headline: no per-launch instrumentation
+    ms_instr, recs = timed(args.steps, True)           # per-kernel durations over a second timed region
     ck = clocks.stop()
-    abi.conv2d_prof_enable(False)
-    recs = abi.conv2d_prof_read(4096)
-    ms = e0.elapsed_time(e1) / args.steps
     rc, site = abi.conv2d_device_status()
     if rc != abi.OK:
         raise RuntimeError("device status %d site %d" % (rc, site))
@@ -196,8 +208,8 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = f0.elapsed_time(f1) / n_e2e
 
-    return dict(ms=ms, e2e_ms=e2e_ms, flops=flops, spec=spec, kern=kern, per_step=per_step, clocks=ck, h2d=h2d,
-                d2h=d2h, n_e2e=n_e2e)
+    return dict(ms=ms, ms_instr=ms_instr, e2e_ms=e2e_ms, flops=flops, spec=spec, kern=kern, per_step=per_step,
+                clocks=ck, h2d=h2d, d2h=d2h, n_e2e=n_e2e)
 
 
 # Per-launch algorithmic bytes of the bandwidth-bound kernels, in units of one [n_pix][OC] tensor of the
@@ -437,6 +449,8 @@ def main():
                      "traffic": NCU_TRAFFIC_BYTES.get(dom) if spec.N == 256 else None,
                      "peak_kind": "bf16 sustained (%s)" % peaks["src"]},
         "kernels": kern,
+        "kernels_timing": {"ms_per_step_instrumented": round(r["ms_instr"], 4),
+                           "what": "per-launch CUDA events over a second timed region of the same steps"},
         "gpu_launches": r["per_step"] * args.steps,
         "e2e": {"value": round(world * r["flops"] / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(e2e_ms, 4),

@@ -397,8 +397,8 @@ void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
     if (g.dt == CONV2D_FP32) sz[R_WBLO] = static_cast<size_t>(g.OC) * g.Kf * 4;
     if (op == CONV2D_OP_FWD_TRAIN && g.norm == CONV2D_NORM_BATCH)
       sz[R_PART] = static_cast<size_t>(ceil_div(g.n_pix, kBM)) * g.OC * 3 * 4;  // per-tile statistics
-    if (ln)  // per-pixel, per-column-tile (mean, M2) of the stored conv output
-      sz[R_PART] = static_cast<size_t>(g.n_pix) * conv_tile(g, g.OC).n_tiles * 2 * 4;
+    if (ln)  // per-pixel, per-column-tile, per-half (mean, M2) of the stored conv output
+      sz[R_PART] = static_cast<size_t>(g.n_pix) * conv_tile(g, g.OC).n_tiles * 2 * 2 * 4;
     if (op == CONV2D_OP_FWD_INFER) {
       sz[R_FOLD] = (2 * static_cast<size_t>(g.OC) + 2 * static_cast<size_t>(g.N)) * 4;  // scale, shift, LN stats
       if (ln) sz[R_DC] = static_cast<size_t>(g.n_pix) * g.OC * es;  // stored conv output, normalised into y
@@ -433,9 +433,15 @@ char* region(void* ws, const Plan& pl, Reg r) { return static_cast<char*>(ws) + 
 
 // fprop GEMM: D[pix][oc] = im2col(x) * B^T, epilogue per ConvGemmParams.
 // stats_groups (if stats): receives the number of statistics partials written (per CTA or per tile).
+// Layout of the layer-norm row partials the fprop epilogue writes: per pixel, n_tiles column tiles of BN
+// columns, each in `halves` halves (two when the epilogue runs on eight warps), half 0 = hcols columns.
+struct RowStatLayout {
+  int n_tiles, halves, BN, hcols;
+};
+
 int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bhi, const void* blo, void* out,
               void* out2, const float* scale, const float* shift, int out_act, float* stats, int* stats_groups,
-              float* rstats, cudaStream_t st) {
+              float* rstats, RowStatLayout* rs_layout, cudaStream_t st) {
   if (rstats && (out_act || out2)) return CONV2D_ERR_INVALID_ARG;  // row partials are of the stored value
   static ConvGemmParams p;  // guarded by g_launch_mu below (large struct)
   static std::mutex mu;
@@ -494,6 +500,12 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   p.stages = t.stages;
   p.err = dev->err;
   if (bf && t.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
+  if (rs_layout) {
+    rs_layout->n_tiles = t.n_tiles;
+    rs_layout->halves = p.a_tma ? 2 : 1;
+    rs_layout->BN = t.BN;
+    rs_layout->hcols = p.a_tma ? 32 * ((t.BN / 32 + 1) / 2) : t.BN;  // the kernel's column split
+  }
   const int grid = std::min(p.num_units, dev->sms);
   p.stats_per_cta = t.n_tiles == 1 ? 1 : 0;
   if (stats_groups) *stats_groups = p.stats_per_cta ? grid : static_cast<int>(ceil_div(g.n_pix, kBM));
@@ -706,19 +718,20 @@ int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, cons
   if (g.norm == CONV2D_NORM_LAYER) {
     // layer norm: per-image statistics of the stored conv output from the epilogue's row partials
     float* rs = reinterpret_cast<float*>(region(ws, pl, R_PART));
-    if ((rc = run_fprop(g, dev, xsrc, bhi, blo, pre_act, nullptr, nullptr, bias, 0, nullptr, nullptr, rs, st)))
+    RowStatLayout lay;
+    if ((rc = run_fprop(g, dev, xsrc, bhi, blo, pre_act, nullptr, nullptr, bias, 0, nullptr, nullptr, rs, &lay,
+                        st)))
       return rc;
-    const Tile t = conv_tile(g, g.OC);
     LAUNCH("ln_stats_finalize", st,
-           launch_ln_stats_finalize(rs, g.N, static_cast<long>(g.OH) * g.OW, t.n_tiles, t.BN, g.OC, g.eps,
-                                    save_mean, save_inv_std, st));
+           launch_ln_stats_finalize(rs, g.N, static_cast<long>(g.OH) * g.OW, lay.n_tiles, lay.halves, lay.BN,
+                                    lay.hcols, g.OC, g.eps, save_mean, save_inv_std, st));
     LAUNCH("ln_apply", st, launch_bn_apply(g.dt, pre_act, y, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, st));
     return CONV2D_OK;
   }
   float* part = (bn && !g.bn_eval) ? reinterpret_cast<float*>(region(ws, pl, R_PART)) : nullptr;
   int groups = 0;
   if ((rc = run_fprop(g, dev, xsrc, bhi, blo, pre_act, bn ? nullptr : y, nullptr, bias, 0, part, &groups, nullptr,
-                      st)))
+                      nullptr, st)))
     return rc;
   if (bn && g.bn_eval) {
     // evaluation mode: normalise with the running statistics, update nothing
@@ -768,16 +781,16 @@ int conv2d_fwd_infer(const conv2d_desc* desc, const void* x, const void* w, cons
     float* rs = reinterpret_cast<float*>(region(ws, pl, R_PART));
     float* mean = shift + g.OC;
     float* istd = mean + g.N;
-    if ((rc = run_fprop(g, dev, xsrc, bhi, blo, ybuf, nullptr, scale, shift, 0, nullptr, nullptr, rs, st)))
+    RowStatLayout lay;
+    if ((rc = run_fprop(g, dev, xsrc, bhi, blo, ybuf, nullptr, scale, shift, 0, nullptr, nullptr, rs, &lay, st)))
       return rc;
-    const Tile t = conv_tile(g, g.OC);
     LAUNCH("ln_stats_finalize", st,
-           launch_ln_stats_finalize(rs, g.N, static_cast<long>(g.OH) * g.OW, t.n_tiles, t.BN, g.OC, g.eps, mean,
-                                    istd, st));
+           launch_ln_stats_finalize(rs, g.N, static_cast<long>(g.OH) * g.OW, lay.n_tiles, lay.halves, lay.BN,
+                                    lay.hcols, g.OC, g.eps, mean, istd, st));
     LAUNCH("ln_apply", st, launch_bn_apply(g.dt, ybuf, y, pl.walk, mean, istd, gamma, beta, g.act, st));
     return CONV2D_OK;
   }
-  return run_fprop(g, dev, xsrc, bhi, blo, y, nullptr, scale, shift, 1, nullptr, nullptr, nullptr, st);
+  return run_fprop(g, dev, xsrc, bhi, blo, y, nullptr, scale, shift, 1, nullptr, nullptr, nullptr, nullptr, st);
 }
 
 int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const float* gamma, const float* beta,

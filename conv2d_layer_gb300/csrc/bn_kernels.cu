@@ -503,30 +503,40 @@ __global__ void infer_fold_kernel(const float* bias, const float* gamma, const f
 
 // ------------------------------------------------------------ layer norm
 // Per-image statistics (`forward` LAYER_NORM branch, over OH*OW*OC of the
-// stored pre-activations) from the per-pixel, per-column-tile (mean, M2)
-// partials of the fprop epilogue: block n merges the partials of image n,
-// in fp32 per thread (Chan) and then in fp64 in a fixed tree.
-__global__ void __launch_bounds__(128) ln_stats_finalize_kernel(const float* __restrict__ rs, int n_tiles, int BN,
-                                                                int OC, long hw, float eps, float* mean,
-                                                                float* inv_std) {
-  __shared__ double s_n[128], s_m[128], s_M[128];
-  const long n_ent = hw * n_tiles;
+// stored pre-activations) from the per-pixel (mean, M2) partials of the
+// fprop epilogue, one per column tile and column half (halves = 1 or 2; half
+// 0 holds the first hcols columns of the tile): block n merges the partials
+// of image n, in fp32 per thread (Chan) and then in fp64 in a fixed tree.
+__global__ void __launch_bounds__(256) ln_stats_finalize_kernel(const float* __restrict__ rs, int n_tiles,
+                                                                int halves, int BN, int hcols, int OC, long hw,
+                                                                float eps, float* mean, float* inv_std) {
+  __shared__ double s_n[256], s_m[256], s_M[256];
+  const int per_pix = n_tiles * halves;
+  const long n_ent = hw * per_pix;
   const float* base = rs + static_cast<size_t>(blockIdx.x) * n_ent * 2;
-  float n = 0.f, m = 0.f, M = 0.f;
-  for (long e = threadIdx.x; e < n_ent; e += 128) {
-    const int t = static_cast<int>(e % n_tiles);
-    const float nb = static_cast<float>(min(BN, OC - t * BN));
+  // per thread: sums shifted by the thread's first partial mean K (no division per partial),
+  // S1 = sum n_j (m_j - K), S2 = sum M2_j + n_j (m_j - K)^2
+  float n = 0.f, K = 0.f, S1 = 0.f, S2 = 0.f;
+  for (long e = threadIdx.x; e < n_ent; e += 256) {
+    const int j = static_cast<int>(e % per_pix);
+    const int t = j / halves, h = j % halves;
+    const int c0 = t * BN + h * hcols;
+    const int c1 = min(OC, t * BN + ((h + 1 == halves) ? BN : hcols));
+    if (c1 <= c0) continue;  // a half with no channel of the layer
+    const float nb = static_cast<float>(c1 - c0);
     const float mb = base[2 * e], Mb = base[2 * e + 1];
-    const float nn = n + nb, d = mb - m, f = nb / nn;
-    m = fmaf(d, f, m);
-    M += Mb + d * d * n * f;
-    n = nn;
+    if (n == 0.f) K = mb;
+    const float d = mb - K;
+    S1 = fmaf(nb, d, S1);
+    S2 += fmaf(nb * d, d, Mb);
+    n += nb;
   }
+  const float m = n > 0.f ? K + S1 / n : 0.f;
   s_n[threadIdx.x] = n;
   s_m[threadIdx.x] = m;
-  s_M[threadIdx.x] = M;
+  s_M[threadIdx.x] = n > 0.f ? fmaxf(S2 - S1 * (S1 / n), 0.f) : 0.f;
   __syncthreads();
-  for (int off = 64; off > 0; off >>= 1) {
+  for (int off = 128; off > 0; off >>= 1) {
     if (threadIdx.x < off) {
       const double na = s_n[threadIdx.x], nb = s_n[threadIdx.x + off];
       if (nb > 0) {
@@ -879,34 +889,32 @@ RowWalk make_walk(long rows, int C, int dtype, int sms, int segs) {
   const int cg = C / ec;
   const int tpr = cg < kBlock ? cg : kBlock;
   const int rpp = kBlock / tpr;
+  // Streamed walks use half-size chunks so that two blocks of the two-input kernels fit on an SM
+  // (their registers and shared memory allow two): more warps to hide the latency of each chunk's
+  // arithmetic than one block per SM with bigger chunks.
+  long resident;
+  if (w.stream) {
+    w.R = static_cast<int>(std::max<long>(1, (kChunkBytes / 2) / row_bytes));
+    resident = 2L * sms;
+  } else {
+    w.R = 0;
+    resident = 8L * sms;
+  }
+  const long unit = std::max<long>(w.R, rpp);  // rows of one chunk (streamed) or one pass
   if (w.segs == 1) {
-    // one persistent block per SM (streamed) or up to 8 per SM, each owning a contiguous slice
-    long g;
-    if (w.stream) {
-      w.R = static_cast<int>(kChunkBytes / row_bytes);
-      g = std::min<long>((rows + w.R - 1) / w.R, sms);
-    } else {
-      w.R = 0;
-      g = std::min<long>((rows + rpp - 1) / rpp, 8L * sms);
-    }
+    // Several waves of blocks of about 16 units each, so that blocks finishing early on fast SMs
+    // take more work (one wave of equal blocks waits for the slowest SM); at least one full wave.
+    long g = (rows + 16 * unit - 1) / (16 * unit);
+    g = std::max(g, std::min<long>((rows + unit - 1) / unit, resident));
+    g = std::min(g, 8 * resident);
     if (g < 1) g = 1;
     w.G = static_cast<int>(g);
     w.bps = w.G;
     w.rows_per_block = (rows + w.G - 1) / w.G;
     return w;
   }
-  // several segments (one per image): blocks never straddle a segment; half-size chunks so that
-  // three streamed blocks fit on an SM and the last wave stays full
-  long resident;
-  if (w.stream) {
-    w.R = static_cast<int>(std::max<long>(1, (kChunkBytes / 2) / row_bytes));
-    const long smem = static_cast<long>(kStreamStages) * 2 * w.R * row_bytes;
-    resident = static_cast<long>(sms) * std::max<long>(1, std::min<long>(8, (220L * 1024) / smem));
-  } else {
-    w.R = 0;
-    resident = 8L * sms;
-  }
-  w.bps = pick_bps(w.segs, w.seg_rows, resident, 2L * std::max<long>(w.R, rpp));
+  // several segments (one per image): blocks never straddle a segment and the last wave stays full
+  w.bps = pick_bps(w.segs, w.seg_rows, resident, 2L * unit);
   w.G = w.segs * w.bps;
   w.rows_per_block = (w.seg_rows + w.bps - 1) / w.bps;
   return w;
@@ -1074,9 +1082,10 @@ cudaError_t launch_act_bwd(int dtype, const void* pre, const void* dy, const Row
   return cudaGetLastError();
 }
 
-cudaError_t launch_ln_stats_finalize(const float* rstats, int n_images, long hw, int n_tiles, int BN, int OC,
-                                     float eps, float* mean, float* inv_std, cudaStream_t st) {
-  ln_stats_finalize_kernel<<<n_images, 128, 0, st>>>(rstats, n_tiles, BN, OC, hw, eps, mean, inv_std);
+cudaError_t launch_ln_stats_finalize(const float* rstats, int n_images, long hw, int n_tiles, int halves, int BN,
+                                     int hcols, int OC, float eps, float* mean, float* inv_std, cudaStream_t st) {
+  ln_stats_finalize_kernel<<<n_images, 256, 0, st>>>(rstats, n_tiles, halves, BN, hcols, OC, hw, eps, mean,
+                                                     inv_std);
   return cudaGetLastError();
 }
 

@@ -88,8 +88,9 @@ struct ConvGemmParams {
   int act, out_act;       // out = out_act ? act(v) : T(v); out2 = act(T(v))
   float* stats;           // optional batch statistics (count, mean, M2) of v: [m_tile][N][3], or
   int stats_per_cta;      // [blockIdx][N][3] merged over the CTA's tiles (single column tile only)
-  float* rstats;          // optional layer-norm partials of the stored value, one per output pixel and
-                          // column tile: [pixel][n_tiles][2] = (mean, M2) over the tile's columns
+  float* rstats;          // optional layer-norm partials of the stored value, one per output pixel,
+                          // column tile and epilogue column half (two halves when a_tma, else one):
+                          // [pixel][n_tiles][halves][2] = (mean, M2) over the half's columns
   // A operand by TMA im2col (bf16, Cs a multiple of 64, one phase): the map
   // walks the row domain; a k-block is (tap, 64-channel chunk) and the tap is
   // the im2col offset, so taps must be non-negative offsets from the window
@@ -146,6 +147,35 @@ __device__ __forceinline__ float to_stored<__nv_bfloat16>(float v) {
 
 // Column sums of a 32-row x 16-column block held one row per lane: a
 // butterfly that halves the columns each lane keeps at every step. Afterwards
+// 16 consecutive floats from shared memory (16-byte aligned) as four vector loads.
+__device__ __forceinline__ void lds16(const float* p, float (&x)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 t = *reinterpret_cast<const float4*>(p + 4 * i);
+    x[4 * i] = t.x;
+    x[4 * i + 1] = t.y;
+    x[4 * i + 2] = t.z;
+    x[4 * i + 3] = t.w;
+  }
+}
+
+// v = acc * scale + shift for 32 accumulator columns; scale and shift are per column in shared
+// memory (16-byte aligned); without a scale only the shift is read.
+__device__ __forceinline__ void ep_columns(const uint32_t (&r)[32], bool zero, bool has_scale, const float* sc,
+                                           const float* sh, float (&v)[32]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float b[16], a[16];
+    lds16(sh + 16 * h, b);
+    if (has_scale) lds16(sc + 16 * h, a);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float x = zero ? 0.f : __uint_as_float(r[16 * h + e]);
+      v[16 * h + e] = has_scale ? fmaf(x, a[e], b[e]) : x + b[e];
+    }
+  }
+}
+
 // x[0] of lane L is the sum over all 32 lanes of column colsum16_col(L).
 template <int W, int O>
 __device__ __forceinline__ void colsum_step(float (&x)[16], int lane) {
@@ -255,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], p.a_tma ? 8 : 4);  // one arrival per epilogue warp
     }
     fence_mbar_init();
     tma_prefetch_desc(&p.tmap_b);
@@ -359,9 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         if (alive) mma_commit(&tfull[buf]);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < 6 && !p.a_tma) {
     // ------------------------------------------------ A producers (gather)
-    // (idle when the A operand comes by TMA im2col)
+    // (when the A operand comes by TMA im2col these warps join the epilogue)
     const int t = threadIdx.x - 64;
     const int j = t & 7;       // 16-byte chunk within the 128-byte row
     const int r0 = t >> 3;     // rows r0 + 16*i
@@ -457,7 +487,14 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     // ------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
-    const int et = threadIdx.x - 192;  // 0..127 within the epilogue warps
+    // Epilogue warps: 6-9, or 2-9 when the A operand comes by TMA (the gather warps are free then).
+    // Warp w reads TMEM lane quarter w & 3; with eight warps the two warps of a quarter split the
+    // tile's 32-column chunks in two halves [cb, ce).
+    const int nthr = p.a_tma ? 256 : 128;
+    const int et = threadIdx.x - (kThreads - nthr);  // 0 .. nthr-1 within the epilogue warps
+    const int half = p.a_tma ? (warp - 2) / 4 : 0;
+    const int hcols = p.a_tma ? 32 * ((BN / 32 + 1) / 2) : BN;
+    const int cb = half * hcols, ce = half ? BN : hcols;
     T* out = static_cast<T*>(p.out);
     T* out2 = static_cast<T*>(p.out2);
     const bool vec = (p.out_ld % D::EC) == 0;
@@ -505,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       if (n_tile != cur_n_tile) {
         // safe to overwrite: every epilogue thread has passed the previous
         // unit's barrier below, after its last read of these arrays
-        for (int c = et; c < BN; c += 128) {
+        for (int c = et; c < BN; c += nthr) {
           const int col = n_tile * BN + c;
           sc_s[c] = (p.ep_scale && col < p.N) ? p.ep_scale[col] : 1.f;
           sh_s[c] = (p.ep_shift && col < p.N) ? p.ep_shift[col] : 0.f;
@@ -515,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       int ok = 1;
       if (lane == 0) ok = wait(&tfull[buf], (tc >> 1) & 1, p.err, kSiteTFull) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!named_bar_and(1, 128, ok)) break;
+      if (!named_bar_and(1, nthr, ok)) break;
       tc_fence_after();
       const int m = m_tile * kBM + row;
       const bool valid = m < ph.rows;
@@ -528,15 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         const int oh = ph.oh0 + a * p.os, ow = ph.ow0 + b * p.os;
         obase = (static_cast<size_t>(n * p.Ho + oh) * p.Wo + ow) * p.out_ld;
       }
-      // layer-norm partials of this row over the tile's columns: exact two-pass per 32 columns, merged
-      // across the chunks with Chan's formula (the chunks before column cc hold cc values)
+      // layer-norm partials of this row over the half's columns: exact two-pass per 32 columns, merged
+      // across the chunks with Chan's formula (the chunks before column cc hold cc - cb values)
       float rmean = 0.f, rm2 = 0.f;
       const bool zero = ph.num_kb == 0;
       const bool one_pass = p.stats && have_shift;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
       // columns are read from TMEM 64 at a time (two 32-column loads, one wait)
       auto fetch = [&](int c0, uint32_t (&ra)[32], uint32_t (&rb)[32]) {
-        const int c1 = c0 + 32 < BN ? c0 + 32 : c0;
+        const int c1 = c0 + 32 < ce ? c0 + 32 : c0;
         tmem_ld32(taddr + c0, ra);
         tmem_ld32(taddr + c1, rb);
         tmem_ld_wait2(ra, rb);
@@ -545,17 +582,19 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         const int col0 = n_tile * BN + cc;
         const int ncols = p.N - col0;
         if (ncols <= 0) return;  // uniform across the warp
+        // column constants and shifts are read as 16-byte vectors (the tensor core's operand reads
+        // already use most of the shared-memory bandwidth)
         float v[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = fmaf(zero ? 0.f : __uint_as_float(r[e]), sc_s[cc + e], sh_s[cc + e]);
+        ep_columns(r, zero, p.ep_scale != nullptr, sc_s + cc, sh_s + cc, v);
         if (p.stats) {  // statistics of the unrounded value
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            float sv[16], sq[16];
+            float sv[16], sq[16], sh[16];
+            if (one_pass) lds16(tmean + cc + h * 16, sh);
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const bool in = valid && h * 16 + e < ncols;
-              const float d = one_pass ? v[h * 16 + e] - tmean[cc + h * 16 + e] : v[h * 16 + e];
+              const float d = one_pass ? v[h * 16 + e] - sh[e] : v[h * 16 + e];
               sv[e] = in ? d : 0.f;
               sq[e] = sv[e] * sv[e];
             }
@@ -583,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
               const float d = e < nc ? o[e] - cm : 0.f;
               m2 = fmaf(d, d, m2);
             }
-            const float rn = static_cast<float>(cc), nn = rn + fnc, dl = cm - rmean, f = fnc / nn;
+            const float rn = static_cast<float>(cc - cb), nn = rn + fnc, dl = cm - rmean, f = fnc / nn;
             rmean = fmaf(dl, f, rmean);
             rm2 += m2 + dl * dl * rn * f;
           }
@@ -595,14 +634,15 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           }
         }
       };
-      for (int c0 = 0; c0 < BN; c0 += 64) {
+      for (int c0 = cb; c0 < ce; c0 += 64) {
         uint32_t ra[32], rb[32];
         fetch(c0, ra, rb);
         pass1(c0, ra);
-        if (c0 + 32 < BN) pass1(c0 + 32, rb);
+        if (c0 + 32 < ce) pass1(c0 + 32, rb);
       }
       if (p.rstats && valid) {
-        float* o = p.rstats + (obase / p.out_ld * p.n_tiles + n_tile) * 2;
+        const int nh = p.a_tma ? 2 : 1;
+        float* o = p.rstats + ((obase / p.out_ld * p.n_tiles + n_tile) * nh + half) * 2;
         o[0] = rmean;
         o[1] = rm2;
       }
@@ -612,8 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         const int cnt = min(kBM, ph.rows - m_tile * kBM);
         const int cols = min(BN, p.N - n_tile * BN);
         const float fc = static_cast<float>(cnt);
-        named_bar_sync(1, 128);
-        for (int c = et; c < cols; c += 128) {
+        named_bar_sync(1, nthr);
+        for (int c = et; c < cols; c += nthr) {
           const float s1 = red[c] + red[BN + c] + red[2 * BN + c] + red[3 * BN + c];
           const float s2 = red2[c] + red2[BN + c] + red2[2 * BN + c] + red2[3 * BN + c];
           const float mean = tmean[c] + s1 / fc;
@@ -626,34 +666,37 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         // squared deviations from that mean (TMEM is read a second time)
         const int cnt = min(kBM, ph.rows - m_tile * kBM);
         const int cols = min(BN, p.N - n_tile * BN);
-        named_bar_sync(1, 128);
-        for (int c = et; c < cols; c += 128)
+        named_bar_sync(1, nthr);
+        for (int c = et; c < cols; c += nthr)
           tmean[c] = (red[c] + red[BN + c] + red[2 * BN + c] + red[3 * BN + c]) / static_cast<float>(cnt);
-        named_bar_sync(1, 128);
+        named_bar_sync(1, nthr);
         auto pass2 = [&](int cc, const uint32_t (&r)[32]) {
           if (cc >= cols) return;  // uniform
 #pragma unroll
+          float x[32];
+          ep_columns(r, zero, p.ep_scale != nullptr, sc_s + cc, sh_s + cc, x);
+#pragma unroll
           for (int h = 0; h < 2; ++h) {
-            float sv[16];
+            float sv[16], mu[16];
+            lds16(tmean + cc + h * 16, mu);
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const int c = cc + h * 16 + e;
-              const float x = fmaf(zero ? 0.f : __uint_as_float(r[h * 16 + e]), sc_s[c], sh_s[c]);
-              const float d = (valid && c < cols) ? x - tmean[c] : 0.f;
+              const float d = (valid && c < cols) ? x[h * 16 + e] - mu[e] : 0.f;
               sv[e] = d * d;
             }
             colsum16(sv, lane);
             if ((lane & 1) == 0) red2[q * BN + cc + h * 16 + colsum16_col(lane)] = sv[0];
           }
         };
-        for (int c0 = 0; c0 < cols; c0 += 64) {
+        for (int c0 = cb; c0 < ce && c0 < cols; c0 += 64) {
           uint32_t ra[32], rb[32];
           fetch(c0, ra, rb);
           pass2(c0, ra);
-          if (c0 + 32 < BN) pass2(c0 + 32, rb);
+          if (c0 + 32 < ce) pass2(c0 + 32, rb);
         }
-        named_bar_sync(1, 128);
-        for (int c = et; c < cols; c += 128)
+        named_bar_sync(1, nthr);
+        for (int c = et; c < cols; c += nthr)
           emit(m_tile, n_tile, c, static_cast<float>(cnt), tmean[c],
                red2[c] + red2[BN + c] + red2[2 * BN + c] + red2[3 * BN + c]);
         cta_n += static_cast<float>(cnt);
@@ -664,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       if (lane == 0) mbar_arrive(&tempty[buf]);
     }
     if (p.stats && p.stats_per_cta) {
-      for (int c = et; c < min(BN, p.N); c += 128) {
+      for (int c = et; c < min(BN, p.N); c += nthr) {
         float* o = p.stats + (static_cast<size_t>(blockIdx.x) * p.N + c) * 3;
         o[0] = cta_n;
         o[1] = c < 128 ? cta_mean0 : cta_mean1;

@@ -63,11 +63,12 @@ cudaError_t launch_bn_bwd_apply(int dtype, const void* pre, const void* dy, cons
                                 int act, const float* c12, void* dconv, float* part, cudaStream_t st);
 cudaError_t launch_act_bwd(int dtype, const void* pre, const void* dy, const RowWalk& wk, int Cp, int act,
                            void* dconv, float* part, cudaStream_t st);
-// Layer norm: per-image mean / inv_std from the fprop epilogue's per-pixel, per-column-tile (mean, M2)
-// partials [n_images * hw][n_tiles][2]; per-image sums of gamma * d_norm and gamma * d_norm * z from the
-// bwd-reduce partials of an image-aligned walk, written to out[2n], out[2n + 1].
-cudaError_t launch_ln_stats_finalize(const float* rstats, int n_images, long hw, int n_tiles, int BN, int OC,
-                                     float eps, float* mean, float* inv_std, cudaStream_t st);
+// Layer norm: per-image mean / inv_std from the fprop epilogue's per-pixel (mean, M2) partials
+// [n_images * hw][n_tiles][halves][2] (half 0 = the first hcols columns of a tile); per-image sums of
+// gamma * d_norm and gamma * d_norm * z from the bwd-reduce partials of an image-aligned walk, written to
+// out[2n], out[2n + 1].
+cudaError_t launch_ln_stats_finalize(const float* rstats, int n_images, long hw, int n_tiles, int halves, int BN,
+                                     int hcols, int OC, float eps, float* mean, float* inv_std, cudaStream_t st);
 cudaError_t launch_ln_seg_finalize(const float* part, const RowWalk& wk, const float* gamma, float* out,
                                    cudaStream_t st);
 cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int taps, int ICp, int IC, float* dw,
