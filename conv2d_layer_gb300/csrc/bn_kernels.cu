@@ -731,13 +731,16 @@ __global__ void __launch_bounds__(kBlock, 1) bn_apply_stream(const T* __restrict
     be[e] = beta[c];
   }
   const T* const in[1] = {pre};
-  stream_walk<T, EC, 1>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err,
-                        [&](long row, const float (&v)[1][EC]) {
-                          float o[EC];
+  with_act(act, [&](auto ac) {
+    constexpr int A = decltype(ac)::value;
+    stream_walk<T, EC, 1>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err,
+                          [&](long row, const float (&v)[1][EC]) {
+                            float o[EC];
 #pragma unroll
-                          for (int e = 0; e < EC; ++e) o[e] = act_f(act, fmaf(v[0][e] - mu[e], sc[e], be[e]));
-                          store_v<EC>(y + row * C + st.g * EC, o);
-                        });
+                            for (int e = 0; e < EC; ++e) o[e] = act_t<A>(fmaf(v[0][e] - mu[e], sc[e], be[e]));
+                            store_v<EC>(y + row * C + st.g * EC, o);
+                          });
+  });
 }
 
 // part[b][c] = {sum d_norm, sum d_norm * z}
@@ -766,16 +769,19 @@ __global__ void __launch_bounds__(kBlock, 1) bn_bwd_reduce_stream(const T* __res
     a[e] = b[e] = 0.f;
   }
   const T* const in[2] = {pre, dy};
-  stream_walk<T, EC, 2>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err,
-                        [&](long, const float (&v)[2][EC]) {
+  with_act(act, [&](auto ac) {
+    constexpr int A = decltype(ac)::value;
+    stream_walk<T, EC, 2>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err,
+                          [&](long, const float (&v)[2][EC]) {
 #pragma unroll
-                          for (int e = 0; e < EC; ++e) {
-                            const float z = (v[0][e] - mu[e]) * is[e];
-                            const float dn = dact_f(act, fmaf(ga[e], z, be[e])) * v[1][e];
-                            a[e] += dn;
-                            b[e] = fmaf(dn, z, b[e]);
-                          }
-                        });
+                            for (int e = 0; e < EC; ++e) {
+                              const float z = (v[0][e] - mu[e]) * is[e];
+                              const float dn = dact_t<A>(fmaf(ga[e], z, be[e])) * v[1][e];
+                              a[e] += dn;
+                              b[e] = fmaf(dn, z, b[e]);
+                            }
+                          });
+  });
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
     s_a[threadIdx.x * EC + e] = a[e];
@@ -826,22 +832,25 @@ __global__ void __launch_bounds__(kBlock, 1) dconv_stream(const T* __restrict__ 
     }
   }
   const T* const in[2] = {pre, dy};
-  stream_walk<T, EC, 2>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err,
-                        [&](long row, const float (&v)[2][EC]) {
-                          float o[EC];
+  with_act(act, [&](auto ac) {
+    constexpr int A = decltype(ac)::value;
+    stream_walk<T, EC, 2>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err,
+                          [&](long row, const float (&v)[2][EC]) {
+                            float o[EC];
 #pragma unroll
-                          for (int e = 0; e < EC; ++e) {
-                            if (MODE == 0) {
-                              const float z = (v[0][e] - mu[e]) * is[e];
-                              const float dn = dact_f(act, fmaf(ga[e], z, be[e])) * v[1][e];
-                              o[e] = is[e] * (ga[e] * dn - k1[e] - z * k2[e]);
-                            } else {
-                              o[e] = dact_f(act, v[0][e]) * v[1][e];
+                            for (int e = 0; e < EC; ++e) {
+                              if (MODE == 0) {
+                                const float z = (v[0][e] - mu[e]) * is[e];
+                                const float dn = dact_t<A>(fmaf(ga[e], z, be[e])) * v[1][e];
+                                o[e] = is[e] * (ga[e] * dn - k1[e] - z * k2[e]);
+                              } else {
+                                o[e] = dact_t<A>(v[0][e]) * v[1][e];
+                              }
+                              a[e] += o[e];
                             }
-                            a[e] += o[e];
-                          }
-                          store_v<EC>(dconv + row * C + st.g * EC, o);
-                        });
+                            store_v<EC>(dconv + row * C + st.g * EC, o);
+                          });
+  });
 #pragma unroll
   for (int e = 0; e < EC; ++e) s_a[threadIdx.x * EC + e] = a[e];
   __syncthreads();

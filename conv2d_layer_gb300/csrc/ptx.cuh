@@ -279,4 +279,35 @@ __device__ __forceinline__ float dact_f(int act, float v) {
   }
 }
 
+// The same with the activation fixed at compile time (the per-element switch above costs a
+// compare and branch per element inside the bandwidth-bound loops).
+template <int A>
+__device__ __forceinline__ float act_t(float v) {
+  if constexpr (A == 1) return v > 0.f ? v : 0.f;
+  else if constexpr (A == 2) return tanhf(v);
+  else if constexpr (A == 3) return 1.f / (1.f + expf(-v));
+  else return v;
+}
+template <int A>
+__device__ __forceinline__ float dact_t(float v) {
+  if constexpr (A == 1) return v > 0.f ? 1.f : 0.f;
+  else if constexpr (A == 2) { const float t = tanhf(v); return 1.f - t * t; }
+  else if constexpr (A == 3) { const float s = 1.f / (1.f + expf(-v)); return s * (1.f - s); }
+  else return 1.f;
+}
+template <int A>
+struct ActC {
+  static constexpr int value = A;
+};
+// Calls f(ActC<act>{}) so that f can use the activation as a compile-time constant.
+template <typename F>
+__device__ __forceinline__ void with_act(int act, F&& f) {
+  switch (act) {
+    case 1: f(ActC<1>{}); break;
+    case 2: f(ActC<2>{}); break;
+    case 3: f(ActC<3>{}); break;
+    default: f(ActC<0>{}); break;
+  }
+}
+
 }  // namespace c2d
