@@ -725,7 +725,9 @@ int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, cons
     LAUNCH("ln_stats_finalize", st,
            launch_ln_stats_finalize(rs, g.N, static_cast<long>(g.OH) * g.OW, lay.n_tiles, lay.halves, lay.BN,
                                     lay.hcols, g.OC, g.eps, save_mean, save_inv_std, st));
-    LAUNCH("ln_apply", st, launch_bn_apply(g.dt, pre_act, y, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, st));
+    // reversed: starts on the last rows of pre_act, which the fprop epilogue wrote last
+    LAUNCH("ln_apply", st,
+           launch_bn_apply(g.dt, pre_act, y, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, 1, st));
     return CONV2D_OK;
   }
   float* part = (bn && !g.bn_eval) ? reinterpret_cast<float*>(region(ws, pl, R_PART)) : nullptr;
@@ -736,14 +738,16 @@ int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, cons
   if (bn && g.bn_eval) {
     // evaluation mode: normalise with the running statistics, update nothing
     LAUNCH("bn_eval_stats", st, launch_bn_eval_stats(running_mean, running_var, g.eps, g.OC, save_mean, save_inv_std, st));
-    LAUNCH("bn_apply", st, launch_bn_apply(g.dt, pre_act, y, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, st));
+    LAUNCH("bn_apply", st,
+           launch_bn_apply(g.dt, pre_act, y, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, 1, st));
   } else if (bn) {
     RowWalk tiles = pl.walk;  // statistics partials written by the fprop GEMM
     tiles.G = groups;
     LAUNCH("bn_stats_finalize", st,
            launch_bn_stats_finalize(part, tiles, g.eps, g.mom, save_mean, save_inv_std, running_mean, running_var,
                                     st));
-    LAUNCH("bn_apply", st, launch_bn_apply(g.dt, pre_act, y, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, st));
+    LAUNCH("bn_apply", st,
+           launch_bn_apply(g.dt, pre_act, y, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, 1, st));
   }
   return CONV2D_OK;
 }
@@ -787,7 +791,7 @@ int conv2d_fwd_infer(const conv2d_desc* desc, const void* x, const void* w, cons
     LAUNCH("ln_stats_finalize", st,
            launch_ln_stats_finalize(rs, g.N, static_cast<long>(g.OH) * g.OW, lay.n_tiles, lay.halves, lay.BN,
                                     lay.hcols, g.OC, g.eps, mean, istd, st));
-    LAUNCH("ln_apply", st, launch_bn_apply(g.dt, ybuf, y, pl.walk, mean, istd, gamma, beta, g.act, st));
+    LAUNCH("ln_apply", st, launch_bn_apply(g.dt, ybuf, y, pl.walk, mean, istd, gamma, beta, g.act, 1, st));
     return CONV2D_OK;
   }
   return run_fprop(g, dev, xsrc, bhi, blo, y, nullptr, scale, shift, 1, nullptr, nullptr, nullptr, nullptr, st);

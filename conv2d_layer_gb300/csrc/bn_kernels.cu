@@ -81,15 +81,20 @@ __device__ __forceinline__ void store_v(__nv_bfloat16* p, const float (&v)[EC]) 
 // Rows of a walk are grouped in segments of seg_rows rows (one segment for
 // batch norm: every row; one per image for layer norm), each split over bps
 // blocks of at most rpb rows, so that a block never straddles two segments.
+// A reversed walk (rev != 0) maps launch block b to logical block G-1-b and
+// visits its rows last to first: consecutive bandwidth-bound kernels walk in
+// opposite directions, so each starts on the rows the previous one touched
+// last, which are still in L2. Partials are indexed by the logical block.
 struct SegRange {
-  int seg;
+  int seg, lb;
   long r0, r1;
 };
-__device__ __forceinline__ SegRange seg_range(long seg_rows, int bps, long rpb) {
+__device__ __forceinline__ SegRange seg_range(long seg_rows, int bps, long rpb, int rev = 0) {
   SegRange r;
-  r.seg = static_cast<int>(blockIdx.x / bps);
+  r.lb = rev ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  r.seg = r.lb / bps;
   const long sb = static_cast<long>(r.seg) * seg_rows;
-  r.r0 = sb + static_cast<long>(blockIdx.x % bps) * rpb;
+  r.r0 = sb + static_cast<long>(r.lb % bps) * rpb;
   r.r1 = min(sb + seg_rows, r.r0 + rpb);
   return r;
 }
@@ -635,14 +640,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // Returns false if a wait gave up (recorded in *err).
 template <typename T, int EC, int NIN, typename Proc>
 __device__ __forceinline__ bool stream_walk(const T* const (&in)[NIN], long r0, long r1, int C, int R, int g,
-                                            int rl, int rpp, uint8_t* sm, uint64_t* full, int* err, Proc&& proc) {
+                                            int rl, int rpp, uint8_t* sm, uint64_t* full, int* err, int rev,
+                                            Proc&& proc) {
   const size_t row_bytes = static_cast<size_t>(C) * sizeof(T);
   const uint32_t chunk = static_cast<uint32_t>(R * row_bytes);
   const long nchunks = r1 > r0 ? (r1 - r0 + R - 1) / R : 0;
+  // first row of chunk k: forward from r0, or backward from r1 (the last chunk is the short one)
+  auto chunk_begin = [&](long k) { return rev ? max(r0, r1 - (k + 1) * R) : r0 + k * R; };
+  auto chunk_end = [&](long k) { return rev ? r1 - k * R : min(r1, r0 + (k + 1) * R); };
   auto issue = [&](long k) {
     const int s = static_cast<int>(k % kStreamStages);
-    const long rb = r0 + k * R;
-    const long re = min(r1, rb + R);
+    const long rb = chunk_begin(k);
+    const long re = chunk_end(k);
     const uint32_t bytes = static_cast<uint32_t>((re - rb) * row_bytes);
     mbar_arrive_expect_tx(&full[s], NIN * bytes);
 #pragma unroll
@@ -658,8 +667,8 @@ __device__ __forceinline__ bool stream_walk(const T* const (&in)[NIN], long r0, 
       ok = false;
       break;
     }
-    const long rb = r0 + k * R;
-    const int nrows = static_cast<int>(min(static_cast<long>(R), r1 - rb));
+    const long rb = chunk_begin(k);
+    const int nrows = static_cast<int>(chunk_end(k) - rb);
     if (rl < rpp) {
       for (int rr = rl; rr < nrows; rr += rpp) {
         float v[NIN][EC];
@@ -687,16 +696,17 @@ __device__ __forceinline__ bool stream_walk(const T* const (&in)[NIN], long r0, 
 
 template <typename T, int EC, int NIN>
 struct StreamSetup {
-  int cg, tpr, rpp, rl, g, seg;
+  int cg, tpr, rpp, rl, g, seg, lb;
   long r0, r1;
-  __device__ StreamSetup(long seg_rows, int bps, int C, long rpb) {
+  __device__ StreamSetup(long seg_rows, int bps, int C, long rpb, int rev) {
     cg = C / EC;
     tpr = cg;  // the streamed path is used when C / EC <= kBlock
     rpp = kBlock / tpr;
     rl = threadIdx.x / tpr;
     g = threadIdx.x % tpr;
-    const SegRange r = seg_range(seg_rows, bps, rpb);
+    const SegRange r = seg_range(seg_rows, bps, rpb, rev);
     seg = r.seg;
+    lb = r.lb;
     r0 = r.r0;
     r1 = r.r1;
   }
@@ -713,14 +723,14 @@ __device__ __forceinline__ void stream_init(uint64_t* full) {
 template <typename T, int EC>
 __global__ void __launch_bounds__(kBlock, 1) bn_apply_stream(const T* __restrict__ pre, T* __restrict__ y,
                                                              long seg_rows, int bps, int C, long rpb, int R, int ln,
-                                                             const float* __restrict__ mean,
+                                                             int rev, const float* __restrict__ mean,
                                                              const float* __restrict__ inv_std,
                                                              const float* __restrict__ gamma,
                                                              const float* __restrict__ beta, int act, int* err) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t full[kStreamStages];
   stream_init(full);
-  const StreamSetup<T, EC, 1> st(seg_rows, bps, C, rpb);
+  const StreamSetup<T, EC, 1> st(seg_rows, bps, C, rpb, rev);
   float mu[EC], sc[EC], be[EC];
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
@@ -733,7 +743,7 @@ __global__ void __launch_bounds__(kBlock, 1) bn_apply_stream(const T* __restrict
   const T* const in[1] = {pre};
   with_act(act, [&](auto ac) {
     constexpr int A = decltype(ac)::value;
-    stream_walk<T, EC, 1>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err,
+    stream_walk<T, EC, 1>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err, rev,
                           [&](long row, const float (&v)[1][EC]) {
                             float o[EC];
 #pragma unroll
@@ -747,7 +757,7 @@ __global__ void __launch_bounds__(kBlock, 1) bn_apply_stream(const T* __restrict
 template <typename T, int EC>
 __global__ void __launch_bounds__(kBlock, 1) bn_bwd_reduce_stream(const T* __restrict__ pre, const T* __restrict__ dy,
                                                                   long seg_rows, int bps, int C, long rpb, int R,
-                                                                  int ln, const float* __restrict__ mean,
+                                                                  int ln, int rev, const float* __restrict__ mean,
                                                                   const float* __restrict__ inv_std,
                                                                   const float* __restrict__ gamma,
                                                                   const float* __restrict__ beta, int act,
@@ -756,7 +766,7 @@ __global__ void __launch_bounds__(kBlock, 1) bn_bwd_reduce_stream(const T* __res
   __shared__ uint64_t full[kStreamStages];
   __shared__ float s_a[kBlock * EC], s_b[kBlock * EC];
   stream_init(full);
-  const StreamSetup<T, EC, 2> st(seg_rows, bps, C, rpb);
+  const StreamSetup<T, EC, 2> st(seg_rows, bps, C, rpb, rev);
   float mu[EC], is[EC], ga[EC], be[EC], a[EC], b[EC];
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
@@ -771,7 +781,7 @@ __global__ void __launch_bounds__(kBlock, 1) bn_bwd_reduce_stream(const T* __res
   const T* const in[2] = {pre, dy};
   with_act(act, [&](auto ac) {
     constexpr int A = decltype(ac)::value;
-    stream_walk<T, EC, 2>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err,
+    stream_walk<T, EC, 2>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err, rev,
                           [&](long, const float (&v)[2][EC]) {
 #pragma unroll
                             for (int e = 0; e < EC; ++e) {
@@ -795,7 +805,7 @@ __global__ void __launch_bounds__(kBlock, 1) bn_bwd_reduce_stream(const T* __res
         sa += s_a[(k * st.tpr + st.g) * EC + e];
         sb += s_b[(k * st.tpr + st.g) * EC + e];
       }
-      float* o = part + (static_cast<size_t>(blockIdx.x) * C + st.g * EC + e) * 2;
+      float* o = part + (static_cast<size_t>(st.lb) * C + st.g * EC + e) * 2;
       o[0] = sa;
       o[1] = sb;
     }
@@ -806,7 +816,7 @@ __global__ void __launch_bounds__(kBlock, 1) bn_bwd_reduce_stream(const T* __res
 template <typename T, int EC, int MODE>
 __global__ void __launch_bounds__(kBlock, 1) dconv_stream(const T* __restrict__ pre, const T* __restrict__ dy,
                                                           long seg_rows, int bps, int C, long rpb, int R, int ln,
-                                                          const float* __restrict__ mean,
+                                                          int rev, const float* __restrict__ mean,
                                                           const float* __restrict__ inv_std,
                                                           const float* __restrict__ gamma,
                                                           const float* __restrict__ beta, int act,
@@ -816,7 +826,7 @@ __global__ void __launch_bounds__(kBlock, 1) dconv_stream(const T* __restrict__ 
   __shared__ uint64_t full[kStreamStages];
   __shared__ float s_a[kBlock * EC];
   stream_init(full);
-  const StreamSetup<T, EC, 2> st(seg_rows, bps, C, rpb);
+  const StreamSetup<T, EC, 2> st(seg_rows, bps, C, rpb, rev);
   float mu[EC], is[EC], ga[EC], be[EC], k1[EC], k2[EC], a[EC];
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
@@ -834,7 +844,7 @@ __global__ void __launch_bounds__(kBlock, 1) dconv_stream(const T* __restrict__ 
   const T* const in[2] = {pre, dy};
   with_act(act, [&](auto ac) {
     constexpr int A = decltype(ac)::value;
-    stream_walk<T, EC, 2>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err,
+    stream_walk<T, EC, 2>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err, rev,
                           [&](long row, const float (&v)[2][EC]) {
                             float o[EC];
 #pragma unroll
@@ -858,7 +868,7 @@ __global__ void __launch_bounds__(kBlock, 1) dconv_stream(const T* __restrict__ 
     for (int e = 0; e < EC; ++e) {
       float sa = 0.f;
       for (int k = 0; k < st.rpp; ++k) sa += s_a[(k * st.tpr + st.g) * EC + e];
-      part[static_cast<size_t>(blockIdx.x) * C + st.g * EC + e] = sa;
+      part[static_cast<size_t>(st.lb) * C + st.g * EC + e] = sa;
     }
   }
 }
@@ -911,9 +921,9 @@ RowWalk make_walk(long rows, int C, int dtype, int sms, int segs) {
   }
   const long unit = std::max<long>(w.R, rpp);  // rows of one chunk (streamed) or one pass
   if (w.segs == 1) {
-    // Several waves of blocks of about 16 units each, so that blocks finishing early on fast SMs
+    // Several waves of blocks of about 28 units each, so that blocks finishing early on fast SMs
     // take more work (one wave of equal blocks waits for the slowest SM); at least one full wave.
-    long g = (rows + 16 * unit - 1) / (16 * unit);
+    long g = (rows + 28 * unit - 1) / (28 * unit);
     g = std::max(g, std::min<long>((rows + unit - 1) / unit, resident));
     g = std::min(g, 8 * resident);
     if (g < 1) g = 1;
@@ -1007,10 +1017,11 @@ cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float
 #define LN_FLAG (wk.segs > 1 ? 1 : 0)
 
 cudaError_t launch_bn_apply(int dtype, const void* pre, void* y, const RowWalk& wk, const float* mean,
-                            const float* inv_std, const float* gamma, const float* beta, int act, cudaStream_t st) {
+                            const float* inv_std, const float* gamma, const float* beta, int act, int rev,
+                            cudaStream_t st) {
   if (wk.stream) {
     STREAM_LAUNCH(dtype, 1, (bn_apply_stream<T, EC>), static_cast<const T*>(pre), static_cast<T*>(y), WALK_ARGS,
-                  wk.R, LN_FLAG, mean, inv_std, gamma, beta, act, wk.err);
+                  wk.R, LN_FLAG, rev, mean, inv_std, gamma, beta, act, wk.err);
     return cudaGetLastError();
   }
   DISPATCH_EC(dtype, wk.C,
@@ -1028,7 +1039,7 @@ cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, con
                                  cudaStream_t st) {
   if (wk.stream) {
     STREAM_LAUNCH(dtype, 2, (bn_bwd_reduce_stream<T, EC>), static_cast<const T*>(pre), static_cast<const T*>(dy),
-                  WALK_ARGS, wk.R, LN_FLAG, mean, inv_std, gamma, beta, act, part, wk.err);
+                  WALK_ARGS, wk.R, LN_FLAG, 0, mean, inv_std, gamma, beta, act, part, wk.err);
     return cudaGetLastError();
   }
   DISPATCH_EC(dtype, wk.C,
@@ -1050,9 +1061,9 @@ cudaError_t launch_sum_finalize(const float* part, const RowWalk& wk, int nv, in
 cudaError_t launch_bn_bwd_apply(int dtype, const void* pre, const void* dy, const RowWalk& wk, int Cp,
                                 const float* mean, const float* inv_std, const float* gamma, const float* beta,
                                 int act, const float* c12, void* dconv, float* part, cudaStream_t st) {
-  if (wk.stream && wk.C == Cp) {
+  if (wk.stream && wk.C == Cp) {  // reversed: starts on the rows the backward reduce read last
     STREAM_LAUNCH(dtype, 2, (dconv_stream<T, EC, 0>), static_cast<const T*>(pre), static_cast<const T*>(dy),
-                  WALK_ARGS, wk.R, LN_FLAG, mean, inv_std, gamma, beta, act, c12, static_cast<T*>(dconv), part,
+                  WALK_ARGS, wk.R, LN_FLAG, 1, mean, inv_std, gamma, beta, act, c12, static_cast<T*>(dconv), part,
                   wk.err);
     return cudaGetLastError();
   }
@@ -1073,7 +1084,7 @@ cudaError_t launch_act_bwd(int dtype, const void* pre, const void* dy, const Row
                            void* dconv, float* part, cudaStream_t st) {
   if (wk.stream && wk.C == Cp) {
     STREAM_LAUNCH(dtype, 2, (dconv_stream<T, EC, 1>), static_cast<const T*>(pre), static_cast<const T*>(dy),
-                  WALK_ARGS, wk.R, 0, nullptr, nullptr, nullptr, nullptr, act, nullptr, static_cast<T*>(dconv), part,
+                  WALK_ARGS, wk.R, 0, 1, nullptr, nullptr, nullptr, nullptr, act, nullptr, static_cast<T*>(dconv), part,
                   wk.err);
     return cudaGetLastError();
   }

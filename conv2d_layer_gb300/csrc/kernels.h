@@ -47,8 +47,11 @@ cudaError_t launch_prep_dgrad_weights(int dtype, const void* w, void* bhi, float
                                       cudaStream_t st);
 cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float eps, float momentum, float* mean,
                                      float* inv_std, float* rm, float* rv, cudaStream_t st);
+// rev != 0 walks the rows last to first (streamed path): the kernel starts on the rows the previous
+// kernel touched last, which are still in L2.
 cudaError_t launch_bn_apply(int dtype, const void* pre, void* y, const RowWalk& wk, const float* mean,
-                            const float* inv_std, const float* gamma, const float* beta, int act, cudaStream_t st);
+                            const float* inv_std, const float* gamma, const float* beta, int act, int rev,
+                            cudaStream_t st);
 cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, const RowWalk& wk, const float* mean,
                                  const float* inv_std, const float* gamma, const float* beta, int act, float* part,
                                  cudaStream_t st);
