@@ -32,7 +32,7 @@ NOMINAL_BF16_TFLOPS = 2250.0
 # DRAM bytes (read + write) per launch of the GEMM kernels on the 256-image layer, from the ncu capture
 # summarised in profiles/large_step_kernels.md (96-image case, scaled by 256/96). Reset to None whenever
 # a GEMM kernel changes and re-capture.
-NCU_TRAFFIC_BYTES = {"fprop_gemm": 686e6, "dgrad_gemm": 680e6, "wgrad_gemm": 823e6}
+NCU_TRAFFIC_BYTES = {"fprop_gemm": 688e6, "dgrad_gemm": 680e6, "wgrad_gemm": 822e6}
 
 
 def _peaks():
@@ -54,26 +54,33 @@ def _workload_desc(spec):
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.p = None
+        self.windows = []
 
     def start(self):
+        """Start sampling every 20 ms; called well before the timed regions (nvidia-smi takes a moment)."""
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                                       "--format=csv,noheader,nounits", "-lms", "200"], stdout=subprocess.PIPE,
+                                       "--format=csv,noheader,nounits", "-lms", "20"], stdout=subprocess.PIPE,
                                       stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.p = None
 
+    def mark(self, t0, t1):
+        """Wall-clock bounds of a timed region; only samples inside one are kept."""
+        self.windows.append((t0, t1))
+
     def stop(self):
+        import datetime
         if self.p is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.1)
         self.p.terminate()
         try:
             out, _ = self.p.communicate(timeout=5)
@@ -84,14 +91,18 @@ class Clocks:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, cmax = float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            if self.windows and not any(a - 0.02 <= ts <= b + 0.02 for a, b in self.windows):
+                continue
+            sm.append(clk)
+            mx = cmax
+            for n, v in zip(names, f[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
@@ -167,8 +178,14 @@ def run_gpu(args, rank, world, local_rank):
 
     clocks = Clocks(local_rank)
     clocks.start()
+    time.sleep(0.3)  # let the sampler start
+    w0 = time.time()
     ms, _ = timed(args.steps, False)                   # the headline: no per-launch instrumentation
+    w1 = time.time()
     ms_instr, recs = timed(args.steps, True)           # per-kernel durations over a second timed region
+    w2 = time.time()
+    clocks.mark(w0, w1)
+    clocks.mark(w1, w2)
     ck = clocks.stop()
     rc, site = abi.conv2d_device_status()
     if rc != abi.OK:
