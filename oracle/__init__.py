@@ -21,12 +21,12 @@ from . import build as _build
 
 ACT = {"identity": 0, "relu": 1, "tanh": 2, "sigmoid": 3}
 STORE = {None: 0, "f64": 0, "f32": 1, "bf16": 2}
-NORM = {"none": 0, "batch": 1, "layer": 2}
+NORM = {"none": 0, "batch": 1, "layer": 2, "group": 3}
 
 
 class _Desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("N", "H", "W", "IC", "OC", "KH", "KW", "S", "P", "norm", "act",
-                                              "store", "bn_eval")] + [
+                                              "store", "bn_eval", "groups")] + [
         ("eps", ctypes.c_double),
         ("momentum", ctypes.c_double),
     ]
@@ -68,7 +68,7 @@ class Layer:
     element type the pre-activations are stored in (store: None/"f64" keeps fp64, "f32", "bf16")."""
 
     def __init__(self, N, H, W, IC, OC, KH, KW, stride=1, pad=0, norm="none", act="identity",
-                 eps=1e-5, momentum=0.1, store=None, bn_eval=False):
+                 eps=1e-5, momentum=0.1, store=None, bn_eval=False, groups=1):
         self.N, self.H, self.W, self.IC, self.OC = N, H, W, IC, OC
         self.KH, self.KW, self.S, self.P = KH, KW, stride, pad
         self.norm = norm if isinstance(norm, int) else NORM[norm]
@@ -76,12 +76,18 @@ class Layer:
         self.eps, self.momentum = float(eps), float(momentum)
         self.store = store if isinstance(store, int) else STORE[store]
         self.bn_eval = 1 if bn_eval else 0
+        self.groups = int(groups)  # group norm: channel groups (dividing OC)
         self.OH = (H + 2 * pad - KH) // stride + 1
         self.OW = (W + 2 * pad - KW) // stride + 1
 
+    @property
+    def n_stats(self):
+        """Entries of the saved mean / inv_std."""
+        return {2: self.N, 3: self.N * self.groups}.get(self.norm, self.OC)
+
     def _c(self):
         return _Desc(self.N, self.H, self.W, self.IC, self.OC, self.KH, self.KW, self.S, self.P,
-                     self.norm, self.act, self.store, self.bn_eval, self.eps, self.momentum)
+                     self.norm, self.act, self.store, self.bn_eval, self.groups, self.eps, self.momentum)
 
     @property
     def x_shape(self):
@@ -149,7 +155,7 @@ def fwd_train(L: Layer, x, w, b, gamma=None, beta=None, running_mean=None, runni
     rm = _zeros_if_none(running_mean, L.OC)
     rv = np.ones(L.OC) if running_var is None else _d(running_var).reshape(L.OC).copy()
     ypre, y = np.empty(L.y_shape), np.empty(L.y_shape)
-    ns = L.N if L.norm == 2 else L.OC  # layer norm keeps per-sample statistics
+    ns = L.n_stats  # per channel (batch norm), per image (layer norm), per (image, group) (group norm)
     mean, inv_std = np.zeros(max(ns, L.OC)), np.zeros(max(ns, L.OC))
     c = L._c()
     lib.oracle_fwd_train(ctypes.byref(c), _p(x), _p(w), _p(b), _p(gamma), _p(beta), _p(rm), _p(rv),
@@ -177,7 +183,7 @@ def dconv(L: Layer, ypre, dy, gamma=None, beta=None, mean=None, inv_std=None):
     ypre, dy = _d(ypre, L.y_shape), _d(dy, L.y_shape)
     gamma = _d(gamma).reshape(L.OC) if gamma is not None else np.ones(L.OC)
     beta = _zeros_if_none(beta, L.OC)
-    ns = L.N if L.norm == 2 else L.OC  # per-sample statistics under layer norm
+    ns = L.n_stats
     mean = _zeros_if_none(mean, ns)
     inv_std = _d(inv_std).reshape(ns) if inv_std is not None else np.ones(ns)
     out = np.empty(L.y_shape)
@@ -228,7 +234,7 @@ def bwd(L: Layer, x, w, ypre, dy, gamma=None, beta=None, mean=None, inv_std=None
     ypre, dy = _d(ypre, L.y_shape), _d(dy, L.y_shape)
     gamma = _d(gamma).reshape(L.OC) if gamma is not None else np.ones(L.OC)
     beta = _zeros_if_none(beta, L.OC)
-    ns = L.N if L.norm == 2 else L.OC  # per-sample statistics under layer norm
+    ns = L.n_stats
     mean = _zeros_if_none(mean, ns)
     inv_std = _d(inv_std).reshape(ns) if inv_std is not None else np.ones(ns)
     dx = np.empty(L.x_shape) if need_dx else None

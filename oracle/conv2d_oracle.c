@@ -29,6 +29,11 @@
  *   - norm 2 is layer norm: per-sample statistics over OH*OW*OC of the
  *     stored pre-activations (it keeps no running statistics), per-channel
  *     gamma / beta; mean / inv_std then have N entries.
+ *   - norm 3 is group norm (WebGPU page "groupnorm_backward.wgsl"): the OC
+ *     channels form `groups` groups of OC/groups consecutive channels;
+ *     statistics per (image, group) over OH*OW*OC/groups stored
+ *     pre-activations, per-channel gamma / beta, no running statistics;
+ *     mean / inv_std have N*groups entries, index n*groups + g.
  *   - the pre-activations are stored in the layer's element type T (`forward`
  *     Phase 1 writes `(T)acc` into `pre_activations`), and the normalisation,
  *     the activation and the backward pass read that stored value. The batch
@@ -52,10 +57,11 @@
 
 typedef struct {
     int32_t N, H, W, IC, OC, KH, KW, S, P;
-    int32_t norm; /* 0 none, 1 batch norm, 2 layer norm */
+    int32_t norm; /* 0 none, 1 batch norm, 2 layer norm, 3 group norm */
     int32_t act;  /* 0 identity, 1 relu, 2 tanh, 3 sigmoid */
     int32_t store; /* element type T of the stored pre-activations: 0 keep fp64, 1 fp32, 2 bf16 */
     int32_t bn_eval; /* batch norm in evaluation mode: running statistics, nothing updated */
+    int32_t groups;  /* group norm (norm 3): number of channel groups, dividing OC */
     double eps, momentum;
 } oracle_desc;
 
@@ -187,6 +193,29 @@ void oracle_ln_stats(const oracle_desc* d, const double* ypre, double* mean, dou
     }
 }
 
+/* Group-norm statistics per (image n, group g) over the OH*OW*(OC/groups) stored values of the
+ * group's channels, two passes, biased variance ("groupnorm_backward.wgsl" Phase 1 recomputes the same
+ * mean and variance from its input; its E[x^2] - mean^2 form is not reproduced). */
+void oracle_gn_stats(const oracle_desc* d, const double* ypre, double* mean, double* inv_std) {
+    const long hw = (long)out_h(d) * out_w(d);
+    const int C = d->OC, G = d->groups, cpg = C / G;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int n = 0; n < d->N; n++)
+        for (int g = 0; g < G; g++) {
+            const double* v = ypre + (size_t)n * hw * C;
+            double m = 0.0;
+            for (long p = 0; p < hw; p++)
+                for (int c = g * cpg; c < (g + 1) * cpg; c++) m += v[p * C + c];
+            m /= (double)(hw * cpg);
+            double var = 0.0;
+            for (long p = 0; p < hw; p++)
+                for (int c = g * cpg; c < (g + 1) * cpg; c++) var += (v[p * C + c] - m) * (v[p * C + c] - m);
+            var /= (double)(hw * cpg);
+            mean[n * G + g] = m;
+            inv_std[n * G + g] = 1.0 / sqrt(var + d->eps);
+        }
+}
+
 /* Training forward: Ypre, batch stats, running-stat EMA, normalise + affine +
  * activation (forward, all phases). rm / rv are updated in place. */
 void oracle_fwd_train(const oracle_desc* d, const double* x, const double* w, const double* b,
@@ -211,6 +240,24 @@ void oracle_fwd_train(const oracle_desc* d, const double* x, const double* w, co
         for (long i = 0; i < npix * C; i++) ypre[i] = oracle_store_round(d->store, ypre[i]);
     if (d->norm == 0) {
         for (long i = 0; i < npix * C; i++) y[i] = oracle_act(d->act, ypre[i]);
+        return;
+    }
+    if (d->norm == 3) {
+        /* group norm: statistics of the stored pre-activations per (image, group), then normalise,
+         * per-channel affine and activation */
+        oracle_gn_stats(d, ypre, mean, inv_std);
+        const long per = npix / d->N;
+        const int cpg = C / d->groups;
+#pragma omp parallel for schedule(static)
+        for (long p = 0; p < npix; p++) {
+            const int n = (int)(p / per);
+            for (int c = 0; c < C; c++) {
+                size_t i = (size_t)p * C + c;
+                const int s = n * d->groups + c / cpg;
+                double z = (ypre[i] - mean[s]) * inv_std[s];
+                y[i] = oracle_act(d->act, gamma[c] * z + beta[c]);
+            }
+        }
         return;
     }
     if (d->norm == 2) {
@@ -259,7 +306,7 @@ void oracle_fwd_infer(const oracle_desc* d, const double* x, const double* w, co
         for (int c = 0; c < C; c++) {
             size_t i = (size_t)p * C + c;
             double v = y[i];
-            if (d->norm == 2) continue; /* layer norm: below, per sample */
+            if (d->norm >= 2) continue; /* layer / group norm: below, per sample */
             if (d->norm == 1) {
                 /* `evaluate` BN branch: the conv output is stored as T first */
                 v = oracle_store_round(d->store, v);
@@ -285,6 +332,25 @@ void oracle_fwd_infer(const oracle_desc* d, const double* x, const double* w, co
         free(m);
         free(is);
     }
+    if (d->norm == 3) {
+        /* group norm at inference: the same per-(image, group) statistics of the stored conv output */
+        for (long i = 0; i < npix * C; i++) y[i] = oracle_store_round(d->store, y[i]);
+        const int G = d->groups, cpg = C / G;
+        double* m = (double*)malloc(sizeof(double) * d->N * G);
+        double* is = (double*)malloc(sizeof(double) * d->N * G);
+        oracle_gn_stats(d, y, m, is);
+        const long per = npix / d->N;
+        for (long p = 0; p < npix; p++) {
+            const int n = (int)(p / per);
+            for (int c = 0; c < C; c++) {
+                size_t i = (size_t)p * C + c;
+                const int s = n * G + c / cpg;
+                y[i] = oracle_act(d->act, gamma[c] * ((y[i] - m[s]) * is[s]) + beta[c]);
+            }
+        }
+        free(m);
+        free(is);
+    }
 }
 
 /* Gradient at the conv output (backward_full, before the scatter loops):
@@ -301,6 +367,47 @@ void oracle_dconv(const oracle_desc* d, const double* gamma, const double* beta,
     if (d->norm == 0) {
 #pragma omp parallel for schedule(static)
         for (long i = 0; i < npix * C; i++) dconv[i] = oracle_dact(d->act, ypre[i]) * dy[i];
+        return;
+    }
+    if (d->norm == 3) {
+        /* group norm backward ("groupnorm_backward.wgsl", Phases 2 and 3, with the activation derivative
+         * in front and the per-channel dgamma / dbeta sums the shader leaves out): with w = gamma[c] and
+         * g_out = d_norm the gradient at the norm output, per (image, group) of n_g elements
+         *   term1 = sum g_out*w,   term2 = sum g_out*w*(x - mean) * inv_std^2,
+         *   d_conv = inv_std * (g_out*w - (term1 + (x - mean)*term2) / n_g). */
+        const int G = d->groups, cpg = C / G;
+        const long per = npix / d->N;
+        const double ng = (double)(per * cpg);
+        double* t1 = (double*)calloc((size_t)d->N * G, sizeof(double));
+        double* t2 = (double*)calloc((size_t)d->N * G, sizeof(double));
+        for (long p = 0; p < npix; p++) {
+            const int n = (int)(p / per);
+            for (int c = 0; c < C; c++) {
+                size_t i = (size_t)p * C + c;
+                const int s = n * G + c / cpg;
+                const double xm = ypre[i] - mean[s];
+                const double z = xm * inv_std[s];
+                const double gout = oracle_dact(d->act, gamma[c] * z + beta[c]) * dy[i];
+                if (dgamma) dgamma[c] += gout * z;
+                if (dbeta) dbeta[c] += gout;
+                t1[s] += gout * gamma[c];
+                t2[s] += gout * gamma[c] * xm;
+            }
+        }
+        for (int s2 = 0; s2 < d->N * G; s2++) t2[s2] *= inv_std[s2] * inv_std[s2];
+#pragma omp parallel for schedule(static)
+        for (long p = 0; p < npix; p++) {
+            const int n = (int)(p / per);
+            for (int c = 0; c < C; c++) {
+                size_t i = (size_t)p * C + c;
+                const int s = n * G + c / cpg;
+                const double xm = ypre[i] - mean[s];
+                const double gout = oracle_dact(d->act, gamma[c] * (xm * inv_std[s]) + beta[c]) * dy[i];
+                dconv[i] = inv_std[s] * (gout * gamma[c] - (t1[s] + xm * t2[s]) / ng);
+            }
+        }
+        free(t1);
+        free(t2);
         return;
     }
     if (d->norm == 2) {

@@ -39,9 +39,16 @@ def _act_inputs(L, x, w, b, gamma, beta):
         return out["ypre"]
     if L.norm == 2:  # per-sample statistics
         z = (out["ypre"] - out["mean"][:, None, None, None]) * out["inv_std"][:, None, None, None]
+    elif L.norm == 3:  # per (image, group) statistics
+        z = (out["ypre"] - _group_bcast(L, out["mean"])) * _group_bcast(L, out["inv_std"])
     else:
         z = (out["ypre"] - out["mean"]) * out["inv_std"]
     return gamma * z + beta
+
+
+def _group_bcast(L, v):
+    """[N*G] per-(image, group) values broadcast to [N, 1, 1, OC]."""
+    return np.repeat(np.asarray(v).reshape(L.N, L.groups), L.OC // L.groups, axis=1)[:, None, None, :]
 
 
 def _fd(f, arr, h=1e-5):
@@ -67,13 +74,13 @@ FD_CASES = [
 ]
 
 
-@pytest.mark.parametrize("norm", ["none", "batch", "layer"])
+@pytest.mark.parametrize("norm", ["none", "batch", "layer", "group"])
 @pytest.mark.parametrize("act", ["identity", "relu", "tanh", "sigmoid"])
 @pytest.mark.parametrize("case", FD_CASES)
 def test_finite_differences(case, norm, act):
     """Every gradient of L = sum(dY * out) against central differences in double."""
     N, H, W, IC, OC, K, S, P = case
-    L = oracle.Layer(N, H, W, IC, OC, K, K, S, P, norm=norm, act=act)
+    L = oracle.Layer(N, H, W, IC, OC, K, K, S, P, norm=norm, act=act, groups=2)
     # pick a seed whose activation inputs stay away from the ReLU kink
     for seed in range(50):
         rng = np.random.default_rng(1000 + seed)
@@ -498,4 +505,78 @@ def test_layernorm_statistics_come_from_the_stored_values(store):
     z = (ys - f["mean"][:, None]) * f["inv_std"][:, None]
     np.testing.assert_allclose(f["y"], np.maximum(gamma * z.reshape(L.y_shape) + beta, 0), rtol=1e-13,
                                atol=1e-15)
+    np.testing.assert_allclose(oracle.fwd_infer(L, x, w, b, gamma, beta), f["y"], rtol=1e-14, atol=1e-15)
+
+
+# ---------------------------------------------------------------- group norm
+def test_groupnorm_with_one_group_is_layer_norm():
+    """Group norm with a single group normalises over the whole image: the layer-norm code path."""
+    rng = np.random.default_rng(51)
+    for store in (None, "bf16"):
+        Lg = oracle.Layer(2, 7, 6, 3, 6, 3, 3, 1, 1, norm="group", act="sigmoid", groups=1, store=store)
+        Ll = oracle.Layer(2, 7, 6, 3, 6, 3, 3, 1, 1, norm="layer", act="sigmoid", store=store)
+        x, w, b, gamma, beta, dy = _rand_layer(rng, Lg)
+        fg, fl = oracle.fwd_train(Lg, x, w, b, gamma, beta), oracle.fwd_train(Ll, x, w, b, gamma, beta)
+        for k in ("ypre", "y", "mean", "inv_std"):
+            np.testing.assert_allclose(fg[k], fl[k], rtol=1e-13, atol=1e-15)
+        gg = oracle.bwd(Lg, x, w, fg["ypre"], dy, gamma, beta, fg["mean"], fg["inv_std"])
+        gl = oracle.bwd(Ll, x, w, fl["ypre"], dy, gamma, beta, fl["mean"], fl["inv_std"])
+        for k in ("dx", "dw", "db", "dgamma", "dbeta"):
+            np.testing.assert_allclose(gg[k], gl[k], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(oracle.fwd_infer(Lg, x, w, b, gamma, beta),
+                                   oracle.fwd_infer(Ll, x, w, b, gamma, beta), rtol=1e-13, atol=1e-15)
+
+
+def test_groupnorm_against_torch_cpu_float64():
+    """Independent computation: torch CPU float64 conv2d + group_norm (and, with one channel per group,
+    instance norm), autograd for every gradient."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    rng = np.random.default_rng(53)
+    acts = {"relu": torch.relu, "tanh": torch.tanh, "sigmoid": torch.sigmoid, "identity": lambda t: t}
+    for (N, H, W, IC, OC, K, S, P, G, act) in [
+        (3, 9, 8, 5, 8, 3, 1, 1, 2, "relu"),
+        (2, 11, 11, 4, 12, 5, 2, 2, 3, "tanh"),
+        (2, 6, 6, 8, 6, 1, 1, 0, 6, "identity"),
+    ]:
+        L = oracle.Layer(N, H, W, IC, OC, K, K, S, P, norm="group", act=act, groups=G)
+        x, w, b, gamma, beta, dy = _rand_layer(rng, L)
+        f = oracle.fwd_train(L, x, w, b, gamma, beta)
+        g = oracle.bwd(L, x, w, f["ypre"], dy, gamma, beta, f["mean"], f["inv_std"])
+        tx = torch.tensor(x).permute(0, 3, 1, 2).requires_grad_()
+        tw = torch.tensor(w).permute(0, 3, 1, 2).contiguous().requires_grad_()
+        tb, tg, tbe = (torch.tensor(v).requires_grad_() for v in (b, gamma, beta))
+        v = F.group_norm(F.conv2d(tx, tw, tb, stride=S, padding=P), G, tg, tbe, eps=L.eps)
+        if G == OC:
+            vi = F.instance_norm(F.conv2d(tx, tw, tb, stride=S, padding=P), weight=tg, bias=tbe, eps=L.eps)
+            np.testing.assert_allclose(v.detach().numpy(), vi.detach().numpy(), rtol=1e-12, atol=1e-13)
+        out = acts[act](v)
+        (out * torch.tensor(dy).permute(0, 3, 1, 2)).sum().backward()
+        nhwc = lambda t: t.detach().permute(0, 2, 3, 1).numpy()  # noqa: E731
+        np.testing.assert_allclose(f["y"], nhwc(out), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(g["dx"], nhwc(tx.grad), rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(g["dw"], tw.grad.permute(0, 2, 3, 1).numpy(), rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(g["db"], tb.grad.numpy(), rtol=1e-8, atol=1e-10)
+        np.testing.assert_allclose(g["dgamma"], tg.grad.numpy(), rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(g["dbeta"], tbe.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def test_groupnorm_invariants_and_stored_statistics():
+    """Per (image, group): statistics of the stored values, z of mean 0, d_conv summing to 0; inference
+    recomputes the same statistics."""
+    rng = np.random.default_rng(55)
+    L = oracle.Layer(2, 6, 6, 4, 8, 3, 3, 1, 1, norm="group", act="tanh", groups=4, store="bf16")
+    L0 = oracle.Layer(2, 6, 6, 4, 8, 3, 3, 1, 1, norm="group", act="tanh", groups=4)
+    x, w, b, gamma, beta, dy = _rand_layer(rng, L)
+    f = oracle.fwd_train(L, x, w, b, gamma, beta)
+    assert f["mean"].shape == (L.N * L.groups,)
+    stored = oracle.store_round("bf16", oracle.conv_fwd(L0, x, w, b))
+    np.testing.assert_array_equal(f["ypre"], stored)
+    cpg = L.OC // L.groups
+    grp = stored.reshape(L.N, -1, L.groups, cpg).transpose(0, 2, 1, 3).reshape(L.N * L.groups, -1)
+    np.testing.assert_allclose(f["mean"], grp.mean(1), rtol=1e-13)
+    np.testing.assert_allclose(f["inv_std"], 1 / np.sqrt(grp.var(1) + L.eps), rtol=1e-12)
+    dc, _, _ = oracle.dconv(L, f["ypre"], dy, gamma, beta, f["mean"], f["inv_std"])
+    dg = dc.reshape(L.N, -1, L.groups, cpg).transpose(0, 2, 1, 3).reshape(L.N * L.groups, -1)
+    np.testing.assert_allclose(dg.sum(1) / np.abs(dg).sum(1), 0, atol=1e-13)
     np.testing.assert_allclose(oracle.fwd_infer(L, x, w, b, gamma, beta), f["y"], rtol=1e-14, atol=1e-15)
