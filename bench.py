@@ -232,8 +232,8 @@ def run_gpu(args, rank, world, local_rank):
 # Per-launch algorithmic bytes of the bandwidth-bound kernels, in units of one [n_pix][OC] tensor of the
 # layer's element type: apply reads pre_act and writes y; the backward reduce reads pre_act and dY; d_conv
 # reads both and writes d_conv.
-HBM_TENSORS = {"bn_apply": 2, "ln_apply": 2, "bn_bwd_reduce": 2, "ln_bwd_reduce": 2, "bn_bwd_dconv": 3,
-               "ln_bwd_dconv": 3, "act_bwd_dconv": 3}
+HBM_TENSORS = {"bn_apply": 2, "ln_apply": 2, "gn_apply": 2, "gn_stats": 1, "bn_bwd_reduce": 2, "ln_bwd_reduce": 2,
+               "bn_bwd_dconv": 3, "ln_bwd_dconv": 3, "act_bwd_dconv": 3}
 
 PER_CONFIG = (
     # (label, workload, overrides of every layer spec)
@@ -244,6 +244,7 @@ PER_CONFIG = (
     ("large", "large", {}),
     ("bn+layernorm", "bn", {"norm": 2}),
     ("large+layernorm", "large", {"norm": 2}),
+    ("large+groupnorm32", "large", {"norm": 3, "groups": 32}),
 )
 
 

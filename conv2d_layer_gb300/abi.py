@@ -13,7 +13,7 @@ import os
 from . import build as _build
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
-NORM_NONE, NORM_BATCH, NORM_LAYER = 0, 1, 2
+NORM_NONE, NORM_BATCH, NORM_LAYER, NORM_GROUP = 0, 1, 2, 3
 ACT_IDENTITY, ACT_RELU, ACT_TANH, ACT_SIGMOID = 0, 1, 2, 3
 FP32, BF16 = 0, 1
 OP_FWD_TRAIN, OP_FWD_INFER, OP_BWD = 0, 1, 2
@@ -28,7 +28,7 @@ EXPORTS = (
 class Conv2dDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("N", "H", "W", "IC", "OC", "KH", "KW", "stride", "pad", "norm", "act",
                                               "dtype")] + [("eps", ctypes.c_float), ("momentum", ctypes.c_float),
-                                                           ("bn_eval", ctypes.c_int32)]
+                                                           ("bn_eval", ctypes.c_int32), ("groups", ctypes.c_int32)]
 
 
 class Conv2dError(RuntimeError):
@@ -91,8 +91,8 @@ def _stream(s):
 
 
 def desc(N, H, W, IC, OC, KH, KW, stride=1, pad=0, norm=NORM_NONE, act=ACT_RELU, dtype=FP32, eps=1e-5,
-         momentum=0.1, bn_eval=0):
-    return Conv2dDesc(N, H, W, IC, OC, KH, KW, stride, pad, norm, act, dtype, eps, momentum, bn_eval)
+         momentum=0.1, bn_eval=0, groups=1):
+    return Conv2dDesc(N, H, W, IC, OC, KH, KW, stride, pad, norm, act, dtype, eps, momentum, bn_eval, groups)
 
 
 def status_str(status):

@@ -193,7 +193,7 @@ long ceil_div(long a, long b) { return (a + b - 1) / b; }
 long round_up(long a, long b) { return ceil_div(a, b) * b; }
 
 struct Geo {
-  int N, H, W, IC, OC, KH, KW, S, P, norm, act, dt, bn_eval;
+  int N, H, W, IC, OC, KH, KW, S, P, norm, act, dt, bn_eval, groups;
   float eps, mom;
   int OH, OW;
   long n_pix;
@@ -210,16 +210,19 @@ int make_geo(const conv2d_desc* d, Geo* g) {
     return CONV2D_ERR_INVALID_ARG;
   if (static_cast<long>(d->H) + 2L * d->pad < d->KH || static_cast<long>(d->W) + 2L * d->pad < d->KW)
     return CONV2D_ERR_INVALID_ARG;
-  if (d->norm < 0 || d->norm > 2 || d->act < 0 || d->act > 3 || d->dtype < 0 || d->dtype > 1)
+  if (d->norm < 0 || d->norm > 3 || d->act < 0 || d->act > 3 || d->dtype < 0 || d->dtype > 1)
     return CONV2D_ERR_INVALID_ARG;
   if (d->norm != CONV2D_NORM_NONE && (!(d->eps > 0.f) || !std::isfinite(d->eps))) return CONV2D_ERR_INVALID_ARG;
   if (d->norm == CONV2D_NORM_BATCH && !(d->momentum >= 0.f && d->momentum <= 1.f)) return CONV2D_ERR_INVALID_ARG;
+  if (d->norm == CONV2D_NORM_GROUP && (d->groups < 1 || d->OC % d->groups != 0)) return CONV2D_ERR_INVALID_ARG;
   if (d->stride > 8) return CONV2D_ERR_UNSUPPORTED;
   Geo& G = *g;
   G.N = d->N; G.H = d->H; G.W = d->W; G.IC = d->IC; G.OC = d->OC; G.KH = d->KH; G.KW = d->KW;
   G.S = d->stride; G.P = d->pad; G.norm = d->norm; G.act = d->act; G.dt = d->dtype;
   G.eps = d->eps; G.mom = d->momentum;
   G.bn_eval = (d->norm == CONV2D_NORM_BATCH && d->bn_eval != 0) ? 1 : 0;
+  // layer norm is group norm with one group; the saved statistics have N * groups entries
+  G.groups = d->norm == CONV2D_NORM_GROUP ? d->groups : 1;
   G.OH = (G.H + 2 * G.P - G.KH) / G.S + 1;
   G.OW = (G.W + 2 * G.P - G.KW) / G.S + 1;
   G.n_pix = static_cast<long>(G.N) * G.OH * G.OW;
@@ -388,8 +391,9 @@ void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
   size_t sz[R_NREG] = {0};
   const size_t es = g.ES;
   const bool ln = g.norm == CONV2D_NORM_LAYER;
-  // layer norm walks each image as a segment of its own
-  pl->walk = make_walk(g.n_pix, g.OC, g.dt, sms, ln ? g.N : 1);
+  const bool gn = g.norm == CONV2D_NORM_GROUP;
+  // layer and group norm walk each image as a segment of its own, statistics per group of channels
+  pl->walk = make_walk(g.n_pix, g.OC, g.dt, sms, (ln || gn) ? g.N : 1, (ln || gn) ? g.OC / g.groups : 0);
   const size_t G = pl->walk.G;
   if (op == CONV2D_OP_FWD_TRAIN || op == CONV2D_OP_FWD_INFER) {
     if (g.pack_x) sz[R_XP] = static_cast<size_t>(g.N) * g.H * g.W * g.ICp * es;
@@ -399,14 +403,18 @@ void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
       sz[R_PART] = static_cast<size_t>(ceil_div(g.n_pix, kBM)) * g.OC * 3 * 4;  // per-tile statistics
     if (ln)  // per-pixel, per-column-tile, per-half (mean, M2) of the stored conv output
       sz[R_PART] = static_cast<size_t>(g.n_pix) * conv_tile(g, g.OC).n_tiles * 2 * 2 * 4;
+    if (gn)  // per-block, per-channel (rows, mean, M2) of the stored conv output
+      sz[R_PART] = G * g.OC * 3 * 4;
     if (op == CONV2D_OP_FWD_INFER) {
-      sz[R_FOLD] = (2 * static_cast<size_t>(g.OC) + 2 * static_cast<size_t>(g.N)) * 4;  // scale, shift, LN stats
-      if (ln) sz[R_DC] = static_cast<size_t>(g.n_pix) * g.OC * es;  // stored conv output, normalised into y
+      // scale, shift, then the per-(image, group) statistics of layer / group norm
+      sz[R_FOLD] = (2 * static_cast<size_t>(g.OC) + 2 * static_cast<size_t>(g.N) * g.groups) * 4;
+      if (ln || gn) sz[R_DC] = static_cast<size_t>(g.n_pix) * g.OC * es;  // stored conv output, normalised into y
     }
   } else {
     sz[R_DC] = static_cast<size_t>(g.n_pix) * g.OCp * es;
     sz[R_PART] = G * g.OC * 2 * 4;
-    sz[R_C12] = 2 * (static_cast<size_t>(g.OC) + (ln ? g.N : 0)) * 4;  // channel sums, then per-image sums
+    // channel sums, then per-(image, group) sums
+    sz[R_C12] = 2 * (static_cast<size_t>(g.OC) + ((ln || gn) ? static_cast<size_t>(g.N) * g.groups : 0)) * 4;
     // dgrad weights: every phase's taps together hold each kernel tap once
     const size_t kd = std::max<size_t>(static_cast<size_t>(g.taps) * g.OCp, g.BKE);
     sz[R_WD] = static_cast<size_t>(g.ICp) * kd * es;
@@ -702,7 +710,7 @@ int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, cons
     REQ_PTR(gamma); REQ_PTR(beta); REQ_PTR(running_mean); REQ_PTR(running_var); REQ_PTR(save_mean);
     REQ_PTR(save_inv_std);
   }
-  if (g.norm == CONV2D_NORM_LAYER) {
+  if (g.norm == CONV2D_NORM_LAYER || g.norm == CONV2D_NORM_GROUP) {
     REQ_PTR(gamma); REQ_PTR(beta); REQ_PTR(save_mean); REQ_PTR(save_inv_std);
   }
   DevInfo* dev = nullptr;
@@ -728,6 +736,19 @@ int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, cons
     // reversed: starts on the last rows of pre_act, which the fprop epilogue wrote last
     LAUNCH("ln_apply", st,
            launch_bn_apply(g.dt, pre_act, y, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, 1, st));
+    return CONV2D_OK;
+  }
+  if (g.norm == CONV2D_NORM_GROUP) {
+    // group norm: per-channel partials of the stored conv output on an image-aligned walk (reversed: it
+    // starts on the rows the fprop epilogue wrote last), merged per (image, group); then the apply
+    float* gp = reinterpret_cast<float*>(region(ws, pl, R_PART));
+    if ((rc = run_fprop(g, dev, xsrc, bhi, blo, pre_act, nullptr, nullptr, bias, 0, nullptr, nullptr, nullptr,
+                        nullptr, st)))
+      return rc;
+    LAUNCH("gn_stats", st, launch_norm_stats(g.dt, pre_act, pl.walk, 1, gp, st));
+    LAUNCH("gn_stats_finalize", st, launch_gn_stats_finalize(gp, pl.walk, g.eps, save_mean, save_inv_std, st));
+    LAUNCH("gn_apply", st,
+           launch_bn_apply(g.dt, pre_act, y, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, 0, st));
     return CONV2D_OK;
   }
   float* part = (bn && !g.bn_eval) ? reinterpret_cast<float*>(region(ws, pl, R_PART)) : nullptr;
@@ -762,7 +783,7 @@ int conv2d_fwd_infer(const conv2d_desc* desc, const void* x, const void* w, cons
   if (g.norm == CONV2D_NORM_BATCH) {
     REQ_PTR(gamma); REQ_PTR(beta); REQ_PTR(running_mean); REQ_PTR(running_var);
   }
-  if (g.norm == CONV2D_NORM_LAYER) {
+  if (g.norm == CONV2D_NORM_LAYER || g.norm == CONV2D_NORM_GROUP) {
     REQ_PTR(gamma); REQ_PTR(beta);
   }
   DevInfo* dev = nullptr;
@@ -794,6 +815,20 @@ int conv2d_fwd_infer(const conv2d_desc* desc, const void* x, const void* w, cons
     LAUNCH("ln_apply", st, launch_bn_apply(g.dt, ybuf, y, pl.walk, mean, istd, gamma, beta, g.act, 1, st));
     return CONV2D_OK;
   }
+  if (g.norm == CONV2D_NORM_GROUP) {
+    // group norm at inference: the same per-(image, group) statistics of the stored conv output
+    void* ybuf = region(ws, pl, R_DC);
+    float* gp = reinterpret_cast<float*>(region(ws, pl, R_PART));
+    float* mean = shift + g.OC;
+    float* istd = mean + static_cast<size_t>(g.N) * g.groups;
+    if ((rc = run_fprop(g, dev, xsrc, bhi, blo, ybuf, nullptr, scale, shift, 0, nullptr, nullptr, nullptr, nullptr,
+                        st)))
+      return rc;
+    LAUNCH("gn_stats", st, launch_norm_stats(g.dt, ybuf, pl.walk, 1, gp, st));
+    LAUNCH("gn_stats_finalize", st, launch_gn_stats_finalize(gp, pl.walk, g.eps, mean, istd, st));
+    LAUNCH("gn_apply", st, launch_bn_apply(g.dt, ybuf, y, pl.walk, mean, istd, gamma, beta, g.act, 0, st));
+    return CONV2D_OK;
+  }
   return run_fprop(g, dev, xsrc, bhi, blo, y, nullptr, scale, shift, 1, nullptr, nullptr, nullptr, nullptr, st);
 }
 
@@ -809,7 +844,7 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
   if (dx) REQ_PTR(w);
   if (dw) REQ_PTR(x);
   const bool bn = g.norm == CONV2D_NORM_BATCH;
-  const bool ln = g.norm == CONV2D_NORM_LAYER;
+  const bool ln = g.norm == CONV2D_NORM_LAYER || g.norm == CONV2D_NORM_GROUP;  // per-(image, group) statistics
   if (bn || ln) {
     REQ_PTR(gamma); REQ_PTR(beta); REQ_PTR(save_mean); REQ_PTR(save_inv_std);
     if (static_cast<bool>(dgamma) != static_cast<bool>(dbeta)) return CONV2D_ERR_INVALID_ARG;
@@ -830,7 +865,7 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
     LAUNCH("ln_bwd_reduce", st,
            launch_bn_bwd_reduce(g.dt, pre_act, dy, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, part, st));
     LAUNCH("ln_bwd_finalize", st, launch_sum_finalize(part, pl.walk, 2, 0, c12, dbeta, dgamma, st));
-    LAUNCH("ln_seg_finalize", st, launch_ln_seg_finalize(part, pl.walk, gamma, c12 + 2 * g.OC, st));
+    LAUNCH("ln_seg_finalize", st, launch_norm_seg_finalize(part, pl.walk, gamma, c12 + 2 * g.OC, st));
     LAUNCH("ln_bwd_dconv", st,
            launch_bn_bwd_apply(g.dt, pre_act, dy, pl.walk, g.OCp, save_mean, save_inv_std, gamma, beta, g.act, c12,
                                dconv, part, st));

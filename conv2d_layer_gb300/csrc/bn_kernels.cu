@@ -99,6 +99,12 @@ __device__ __forceinline__ SegRange seg_range(long seg_rows, int bps, long rpb, 
   return r;
 }
 
+// Index of the statistics of channel c in segment seg: per channel (cpg == 0, batch norm) or per
+// group of cpg consecutive channels of one segment = image (layer norm: cpg = C; group norm: C/groups).
+__device__ __forceinline__ int stat_index(int cpg, int seg, int c, int C) {
+  return cpg ? seg * (C / cpg) + c / cpg : c;
+}
+
 // Thread geometry of a block walking [rows][C]: `tpr` threads share a row,
 // each owning EC consecutive channels; `rpp` rows are in flight per pass.
 struct Lane {
@@ -167,10 +173,10 @@ __global__ void __launch_bounds__(128) bn_stats_finalize_kernel(const float* __r
 }
 
 // ------------------------------------------------------------ BN apply + act
-// Statistics are per channel (batch norm) or per segment = image (layer norm, ln != 0).
+// Statistics are per channel (batch norm, cpg == 0) or per image and channel group (layer / group norm).
 template <typename T, int EC>
 __global__ void __launch_bounds__(kBlock) bn_apply_kernel(const T* __restrict__ pre, T* __restrict__ y,
-                                                          long seg_rows, int bps, int C, long rpb, int ln,
+                                                          long seg_rows, int bps, int C, long rpb, int cpg,
                                                           const float* __restrict__ mean,
                                                           const float* __restrict__ inv_std,
                                                           const float* __restrict__ gamma,
@@ -182,7 +188,7 @@ __global__ void __launch_bounds__(kBlock) bn_apply_kernel(const T* __restrict__ 
 #pragma unroll
     for (int e = 0; e < EC; ++e) {
       const int c = g * EC + e;
-      const int si = ln ? l.seg : c;
+      const int si = stat_index(cpg, l.seg, c, C);
       mu[e] = mean[si];
       sc[e] = gamma[c] * inv_std[si];
       be[e] = beta[c];
@@ -197,11 +203,71 @@ __global__ void __launch_bounds__(kBlock) bn_apply_kernel(const T* __restrict__ 
   }
 }
 
+// ------------------------------------------------------------ per-channel statistics of a walk
+// part[b][c][3] = (rows, mean, M2) of channel c over block b's rows (group-norm statistics of the
+// stored pre-activations); per thread sums shifted by its first value of each channel.
+template <typename T, int EC>
+__global__ void __launch_bounds__(kBlock) norm_stats_kernel(const T* __restrict__ pre, long seg_rows, int bps,
+                                                            int C, long rpb, float* __restrict__ part) {
+  __shared__ float s_n[kBlock], s_m[kBlock * EC], s_M[kBlock * EC];
+  const Lane l = lane_of(seg_rows, bps, C, EC, rpb);
+  for (int gb = 0; gb < l.cg; gb += l.tpr) {
+    const int g = gb + l.g0;
+    const bool active = g < l.cg && l.rl < l.rpp;
+    float K[EC], s1[EC], s2[EC], nt = 0.f;
+#pragma unroll
+    for (int e = 0; e < EC; ++e) K[e] = s1[e] = s2[e] = 0.f;
+    if (active) {
+      for (long r = l.r0 + l.rl; r < l.r1; r += l.rpp) {
+        float v[EC];
+        load_v<EC>(pre + r * C + g * EC, v);
+        if (nt == 0.f) {
+#pragma unroll
+          for (int e = 0; e < EC; ++e) K[e] = v[e];
+        }
+#pragma unroll
+        for (int e = 0; e < EC; ++e) {
+          const float d = v[e] - K[e];
+          s1[e] += d;
+          s2[e] = fmaf(d, d, s2[e]);
+        }
+        nt += 1.f;
+      }
+    }
+    s_n[threadIdx.x] = nt;
+#pragma unroll
+    for (int e = 0; e < EC; ++e) {
+      s_m[threadIdx.x * EC + e] = nt > 0.f ? K[e] + s1[e] / nt : 0.f;
+      s_M[threadIdx.x * EC + e] = nt > 0.f ? fmaxf(s2[e] - s1[e] * (s1[e] / nt), 0.f) : 0.f;
+    }
+    __syncthreads();
+    if (active && l.rl == 0) {
+      for (int e = 0; e < EC; ++e) {
+        float n = 0.f, m = 0.f, M = 0.f;
+        for (int k = 0; k < l.rpp; ++k) {
+          const int t = k * l.tpr + l.g0;
+          const float nb = s_n[t];
+          if (nb == 0.f) continue;
+          const float nn = n + nb, d = s_m[t * EC + e] - m, f = nb / nn;
+          m = fmaf(d, f, m);
+          M += s_M[t * EC + e] + d * d * n * f;
+          n = nn;
+        }
+        float* o = part + (static_cast<size_t>(blockIdx.x) * C + g * EC + e) * 3;
+        o[0] = n;
+        o[1] = m;
+        o[2] = M;
+      }
+    }
+    __syncthreads();
+  }
+}
+
 // ------------------------------------------------------------ BN backward
 // part[b][c] = {sum d_norm, sum d_norm * z}, d_norm = act'(gamma z + beta) dy.
 template <typename T, int EC>
 __global__ void __launch_bounds__(kBlock) bn_bwd_reduce_kernel(const T* __restrict__ pre, const T* __restrict__ dy,
-                                                               long seg_rows, int bps, int C, long rpb, int ln,
+                                                               long seg_rows, int bps, int C, long rpb, int cpg,
                                                                const float* __restrict__ mean,
                                                                const float* __restrict__ inv_std,
                                                                const float* __restrict__ gamma,
@@ -220,7 +286,7 @@ __global__ void __launch_bounds__(kBlock) bn_bwd_reduce_kernel(const T* __restri
 #pragma unroll
       for (int e = 0; e < EC; ++e) {
         const int c = g * EC + e;
-        const int si = ln ? l.seg : c;
+        const int si = stat_index(cpg, l.seg, c, C);
         mu[e] = mean[si];
         is[e] = inv_std[si];
         ga[e] = gamma[c];
@@ -263,17 +329,18 @@ __global__ void __launch_bounds__(kBlock) bn_bwd_reduce_kernel(const T* __restri
 
 // Normalisation coefficients of d_conv = inv_std * (gamma * d_norm - K1 - z * K2):
 //   batch norm  K1 = gamma * c1[c] / n,   K2 = gamma * c2[c] / n    (n = rows; c12 = [C][2] sums)
-//   layer norm  K1 = s1[seg] / M,         K2 = s2[seg] / M          (M = seg_rows * C; per-image sums
-//               of gamma * d_norm and gamma * d_norm * z stored after the channel sums: c12 + 2C)
+//   layer / group norm  K1 = s1[si] / M,  K2 = s2[si] / M  (si = stat_index, M = seg_rows * cpg; sums
+//               of gamma * d_norm and gamma * d_norm * z per image and group, after the channel sums: c12 + 2C)
 //   no c12      evaluation-mode batch norm, no projection terms.
-__device__ __forceinline__ void norm_bwd_coef(const float* c12, int ln, int seg, int c, int C, float ga,
+__device__ __forceinline__ void norm_bwd_coef(const float* c12, int cpg, int seg, int c, int C, float ga,
                                               long seg_rows, float& k1, float& k2) {
   if (!c12) {
     k1 = k2 = 0.f;
-  } else if (ln) {
-    const float inv_m = 1.f / static_cast<float>(seg_rows * C);
-    k1 = c12[2 * C + 2 * seg] * inv_m;
-    k2 = c12[2 * C + 2 * seg + 1] * inv_m;
+  } else if (cpg) {
+    const int si = stat_index(cpg, seg, c, C);
+    const float inv_m = 1.f / static_cast<float>(seg_rows * cpg);
+    k1 = c12[2 * C + 2 * si] * inv_m;
+    k2 = c12[2 * C + 2 * si + 1] * inv_m;
   } else {
     const float inv_n = 1.f / static_cast<float>(seg_rows);
     k1 = ga * c12[2 * c] * inv_n;
@@ -284,7 +351,7 @@ __device__ __forceinline__ void norm_bwd_coef(const float* c12, int ln, int seg,
 // part[b][c] = sum d_conv. MODE 0: batch / layer norm; MODE 1: no norm (d_conv = act'(pre) * dy).
 template <typename T, int EC, int MODE>
 __global__ void __launch_bounds__(kBlock) dconv_kernel(const T* __restrict__ pre, const T* __restrict__ dy,
-                                                       long seg_rows, int bps, int C, int Cp, long rpb, int ln,
+                                                       long seg_rows, int bps, int C, int Cp, long rpb, int cpg,
                                                        const float* __restrict__ mean,
                                                        const float* __restrict__ inv_std,
                                                        const float* __restrict__ gamma,
@@ -307,12 +374,12 @@ __global__ void __launch_bounds__(kBlock) dconv_kernel(const T* __restrict__ pre
       for (int e = 0; e < EC; ++e) {
         const int c = real ? g * EC + e : 0;
         if (MODE == 0) {
-          const int si = ln ? l.seg : c;
+          const int si = stat_index(cpg, l.seg, c, C);
           mu[e] = mean[si];
           is[e] = inv_std[si];
           ga[e] = gamma[c];
           be[e] = beta[c];
-          norm_bwd_coef(c12, ln, l.seg, c, C, ga[e], seg_rows, k1[e], k2[e]);
+          norm_bwd_coef(c12, cpg, l.seg, c, C, ga[e], seg_rows, k1[e], k2[e]);
         }
       }
       for (long r = l.r0 + l.rl; r < l.r1; r += l.rpp) {
@@ -515,13 +582,14 @@ __global__ void infer_fold_kernel(const float* bias, const float* gamma, const f
 __global__ void __launch_bounds__(256) ln_stats_finalize_kernel(const float* __restrict__ rs, int n_tiles,
                                                                 int halves, int BN, int hcols, int OC, long hw,
                                                                 float eps, float* mean, float* inv_std) {
-  __shared__ double s_n[256], s_m[256], s_M[256];
+  __shared__ float s_n[8], s_m[8], s_M[8];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int per_pix = n_tiles * halves;
   const long n_ent = hw * per_pix;
   const float* base = rs + static_cast<size_t>(blockIdx.x) * n_ent * 2;
   // per thread: sums shifted by the thread's first partial mean K (no division per partial),
   // S1 = sum n_j (m_j - K), S2 = sum M2_j + n_j (m_j - K)^2
-  float n = 0.f, K = 0.f, S1 = 0.f, S2 = 0.f;
+  float cnt = 0.f, K = 0.f, S1 = 0.f, S2 = 0.f;
   for (long e = threadIdx.x; e < n_ent; e += 256) {
     const int j = static_cast<int>(e % per_pix);
     const int t = j / halves, h = j % halves;
@@ -530,64 +598,157 @@ __global__ void __launch_bounds__(256) ln_stats_finalize_kernel(const float* __r
     if (c1 <= c0) continue;  // a half with no channel of the layer
     const float nb = static_cast<float>(c1 - c0);
     const float mb = base[2 * e], Mb = base[2 * e + 1];
-    if (n == 0.f) K = mb;
+    if (cnt == 0.f) K = mb;
     const float d = mb - K;
     S1 = fmaf(nb, d, S1);
     S2 += fmaf(nb * d, d, Mb);
-    n += nb;
+    cnt += nb;
   }
-  const float m = n > 0.f ? K + S1 / n : 0.f;
-  s_n[threadIdx.x] = n;
-  s_m[threadIdx.x] = m;
-  s_M[threadIdx.x] = n > 0.f ? fmaxf(S2 - S1 * (S1 / n), 0.f) : 0.f;
-  __syncthreads();
-  for (int off = 128; off > 0; off >>= 1) {
-    if (threadIdx.x < off) {
-      const double na = s_n[threadIdx.x], nb = s_n[threadIdx.x + off];
-      if (nb > 0) {
-        const double nn = na + nb, d = s_m[threadIdx.x + off] - s_m[threadIdx.x];
-        s_m[threadIdx.x] += d * nb / nn;
-        s_M[threadIdx.x] += s_M[threadIdx.x + off] + d * d * na * nb / nn;
-        s_n[threadIdx.x] = nn;
-      }
+  float m = cnt > 0.f ? K + S1 / cnt : 0.f;
+  float M = cnt > 0.f ? fmaxf(S2 - S1 * (S1 / cnt), 0.f) : 0.f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float nb = __shfl_xor_sync(0xffffffffu, cnt, off);
+    const float mb = __shfl_xor_sync(0xffffffffu, m, off);
+    const float Mb = __shfl_xor_sync(0xffffffffu, M, off);
+    const float nn = cnt + nb;
+    if (nn > 0.f) {  // symmetric in the two operands: both lanes of a pair agree
+      const float d = mb - m;
+      const float mm = (cnt * m + nb * mb) / nn;
+      M = M + Mb + d * d * (cnt * nb / nn);
+      m = mm;
+      cnt = nn;
     }
-    __syncthreads();
   }
+  if (lane == 0) {
+    s_n[w] = cnt;
+    s_m[w] = m;
+    s_M[w] = M;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
-    const double var = s_n[0] > 0 ? s_M[0] / s_n[0] : 0.0;  // biased
-    mean[blockIdx.x] = static_cast<float>(s_m[0]);
+    double n = 0.0, mu = 0.0, M2 = 0.0;
+    for (int k = 0; k < 8; ++k) {
+      const double nb = s_n[k];
+      if (nb == 0.0) continue;
+      const double nn = n + nb, d = s_m[k] - mu;
+      mu += d * nb / nn;
+      M2 += s_M[k] + d * d * n * nb / nn;
+      n = nn;
+    }
+    const double var = n > 0 ? M2 / n : 0.0;  // biased
+    mean[blockIdx.x] = static_cast<float>(mu);
     inv_std[blockIdx.x] = static_cast<float>(1.0 / sqrt(var + static_cast<double>(eps)));
   }
 }
 
-// Per-image sums of gamma * d_norm and gamma * d_norm * z (`backward_full`
-// training branch, NORM_DIM = batch) from the per-block, per-channel partials
-// part[b][c][2] of an image-aligned walk (bps blocks per image):
-// out[2n], out[2n+1].
-__global__ void __launch_bounds__(128) ln_seg_finalize_kernel(const float* __restrict__ part, int bps, int C,
-                                                              const float* __restrict__ gamma, float* out) {
-  __shared__ double s[2][128];
-  const long n_ent = static_cast<long>(bps) * C;
-  const float* base = part + static_cast<size_t>(blockIdx.x) * n_ent * 2;
+// Warps per output of the per-(image, group) finalize kernels: more warps when an output merges many
+// partials (layer norm: every channel of an image), one when it merges few (group norm).
+static int finalize_wpo(long n_ent) { return n_ent >= 1024 ? 4 : (n_ent >= 256 ? 2 : 1); }
+
+// Per-(image, group) sums of gamma * d_norm and gamma * d_norm * z (`backward_full` training branch
+// with NORM_DIM = batch for layer norm; Phase 2 of the GroupNorm backward shader for group norm) from
+// the per-block, per-channel partials part[b][c][2] of an image-aligned walk (bps blocks per image).
+// wpo warps per output s = n * groups + g: fp32 sums per lane, a fixed shuffle tree per warp, the wpo
+// warp sums added in a fixed order; written to out[2s], out[2s+1].
+__global__ void __launch_bounds__(128) norm_seg_finalize_kernel(const float* __restrict__ part, int bps, int C,
+                                                                int cpg, int n_out, int wpo,
+                                                                const float* __restrict__ gamma, float* out) {
+  __shared__ float s_a[4], s_b[4];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.x * (4 / wpo) + w / wpo, sub = w % wpo;
+  const int groups = C / cpg;
+  const int n = s / groups, g = s % groups;
+  const long n_ent = static_cast<long>(bps) * cpg;
   float a = 0.f, b = 0.f;
-  for (long k = threadIdx.x; k < n_ent; k += 128) {
-    const float g = gamma[k % C];
-    a = fmaf(g, base[2 * k], a);
-    b = fmaf(g, base[2 * k + 1], b);
-  }
-  s[0][threadIdx.x] = a;
-  s[1][threadIdx.x] = b;
-  __syncthreads();
-  for (int off = 64; off > 0; off >>= 1) {
-    if (threadIdx.x < off) {
-      s[0][threadIdx.x] += s[0][threadIdx.x + off];
-      s[1][threadIdx.x] += s[1][threadIdx.x + off];
+  if (s < n_out) {
+    for (long k = sub * 32 + lane; k < n_ent; k += 32 * wpo) {
+      const int j = static_cast<int>(k / cpg), c = g * cpg + static_cast<int>(k % cpg);
+      const float* q = part + (static_cast<size_t>(n * bps + j) * C + c) * 2;
+      a = fmaf(gamma[c], q[0], a);
+      b = fmaf(gamma[c], q[1], b);
     }
-    __syncthreads();
   }
-  if (threadIdx.x == 0) {
-    out[2 * blockIdx.x] = static_cast<float>(s[0][0]);
-    out[2 * blockIdx.x + 1] = static_cast<float>(s[1][0]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, off);
+    b += __shfl_xor_sync(0xffffffffu, b, off);
+  }
+  if (lane == 0) {
+    s_a[w] = a;
+    s_b[w] = b;
+  }
+  __syncthreads();
+  if (s < n_out && sub == 0 && lane == 0) {
+    float ta = 0.f, tb = 0.f;
+    for (int k = 0; k < wpo; ++k) {
+      ta += s_a[w + k];
+      tb += s_b[w + k];
+    }
+    out[2 * s] = ta;
+    out[2 * s + 1] = tb;
+  }
+}
+
+// Group-norm statistics per (image, group) from the per-block, per-channel (count, mean, M2) partials
+// part[b][c][3] of an image-aligned walk over the stored pre-activations. wpo warps per output
+// s = n * groups + g: per lane sums shifted by its first partial mean (no division per partial), a
+// fixed Chan tree over the lanes, then over the wpo warps.
+__device__ __forceinline__ void chan_merge(float& n, float& m, float& M, float nb, float mb, float Mb) {
+  const float nn = n + nb;
+  if (nn > 0.f) {  // symmetric in the two operands (both lanes of a shuffle pair agree)
+    const float d = mb - m;
+    const float mm = (n * m + nb * mb) / nn;
+    M = M + Mb + d * d * (n * nb / nn);
+    m = mm;
+    n = nn;
+  }
+}
+
+__global__ void __launch_bounds__(128) gn_stats_finalize_kernel(const float* __restrict__ part, int bps, int C,
+                                                                int cpg, int n_out, int wpo, float eps, float* mean,
+                                                                float* inv_std) {
+  __shared__ float s_n[4], s_m[4], s_M[4];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.x * (4 / wpo) + w / wpo, sub = w % wpo;
+  const int groups = C / cpg;
+  const int n = s / groups, g = s % groups;
+  const long n_ent = static_cast<long>(bps) * cpg;
+  float cnt = 0.f, K = 0.f, S1 = 0.f, S2 = 0.f;
+  if (s < n_out) {
+    for (long k = sub * 32 + lane; k < n_ent; k += 32 * wpo) {
+      const int j = static_cast<int>(k / cpg), c = g * cpg + static_cast<int>(k % cpg);
+      const float* q = part + (static_cast<size_t>(n * bps + j) * C + c) * 3;
+      const float nb = q[0];
+      if (nb == 0.f) continue;
+      if (cnt == 0.f) K = q[1];
+      const float d = q[1] - K;
+      S1 = fmaf(nb, d, S1);
+      S2 += fmaf(nb * d, d, q[2]);
+      cnt += nb;
+    }
+  }
+  float m = cnt > 0.f ? K + S1 / cnt : 0.f;
+  float M = cnt > 0.f ? fmaxf(S2 - S1 * (S1 / cnt), 0.f) : 0.f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float nb = __shfl_xor_sync(0xffffffffu, cnt, off);
+    const float mb = __shfl_xor_sync(0xffffffffu, m, off);
+    const float Mb = __shfl_xor_sync(0xffffffffu, M, off);
+    chan_merge(cnt, m, M, nb, mb, Mb);
+  }
+  if (lane == 0) {
+    s_n[w] = cnt;
+    s_m[w] = m;
+    s_M[w] = M;
+  }
+  __syncthreads();
+  if (s < n_out && sub == 0 && lane == 0) {
+    float tn = 0.f, tm = 0.f, tM = 0.f;
+    for (int k = 0; k < wpo; ++k) chan_merge(tn, tm, tM, s_n[w + k], s_m[w + k], s_M[w + k]);
+    const float var = tn > 0.f ? tM / tn : 0.f;  // biased
+    mean[s] = tm;
+    inv_std[s] = static_cast<float>(1.0 / sqrt(static_cast<double>(var) + static_cast<double>(eps)));
   }
 }
 
@@ -722,7 +883,7 @@ __device__ __forceinline__ void stream_init(uint64_t* full) {
 
 template <typename T, int EC>
 __global__ void __launch_bounds__(kBlock, 1) bn_apply_stream(const T* __restrict__ pre, T* __restrict__ y,
-                                                             long seg_rows, int bps, int C, long rpb, int R, int ln,
+                                                             long seg_rows, int bps, int C, long rpb, int R, int cpg,
                                                              int rev, const float* __restrict__ mean,
                                                              const float* __restrict__ inv_std,
                                                              const float* __restrict__ gamma,
@@ -735,7 +896,7 @@ __global__ void __launch_bounds__(kBlock, 1) bn_apply_stream(const T* __restrict
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
     const int c = st.g * EC + e;
-    const int si = ln ? st.seg : c;
+    const int si = stat_index(cpg, st.seg, c, C);
     mu[e] = mean[si];
     sc[e] = gamma[c] * inv_std[si];
     be[e] = beta[c];
@@ -753,11 +914,66 @@ __global__ void __launch_bounds__(kBlock, 1) bn_apply_stream(const T* __restrict
   });
 }
 
+// part[b][c][3] = (rows, mean, M2) of channel c over the block's rows (streamed form of norm_stats_kernel)
+template <typename T, int EC>
+__global__ void __launch_bounds__(kBlock, 1) norm_stats_stream(const T* __restrict__ pre, long seg_rows, int bps,
+                                                               int C, long rpb, int R, int rev,
+                                                               float* __restrict__ part, int* err) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  __shared__ uint64_t full[kStreamStages];
+  __shared__ float s_n[kBlock], s_m[kBlock * EC], s_M[kBlock * EC];
+  stream_init(full);
+  const StreamSetup<T, EC, 1> st(seg_rows, bps, C, rpb, rev);
+  float K[EC], s1[EC], s2[EC], nt = 0.f;
+#pragma unroll
+  for (int e = 0; e < EC; ++e) K[e] = s1[e] = s2[e] = 0.f;
+  const T* const in[1] = {pre};
+  stream_walk<T, EC, 1>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err, rev,
+                        [&](long, const float (&v)[1][EC]) {
+                          if (nt == 0.f) {
+#pragma unroll
+                            for (int e = 0; e < EC; ++e) K[e] = v[0][e];
+                          }
+#pragma unroll
+                          for (int e = 0; e < EC; ++e) {
+                            const float d = v[0][e] - K[e];
+                            s1[e] += d;
+                            s2[e] = fmaf(d, d, s2[e]);
+                          }
+                          nt += 1.f;
+                        });
+  s_n[threadIdx.x] = nt;
+#pragma unroll
+  for (int e = 0; e < EC; ++e) {
+    s_m[threadIdx.x * EC + e] = nt > 0.f ? K[e] + s1[e] / nt : 0.f;
+    s_M[threadIdx.x * EC + e] = nt > 0.f ? fmaxf(s2[e] - s1[e] * (s1[e] / nt), 0.f) : 0.f;
+  }
+  __syncthreads();
+  if (st.rl == 0) {
+    for (int e = 0; e < EC; ++e) {
+      float n = 0.f, m = 0.f, M = 0.f;
+      for (int k = 0; k < st.rpp; ++k) {
+        const int t = k * st.tpr + st.g;
+        const float nb = s_n[t];
+        if (nb == 0.f) continue;
+        const float nn = n + nb, d = s_m[t * EC + e] - m, f = nb / nn;
+        m = fmaf(d, f, m);
+        M += s_M[t * EC + e] + d * d * n * f;
+        n = nn;
+      }
+      float* o = part + (static_cast<size_t>(st.lb) * C + st.g * EC + e) * 3;
+      o[0] = n;
+      o[1] = m;
+      o[2] = M;
+    }
+  }
+}
+
 // part[b][c] = {sum d_norm, sum d_norm * z}
 template <typename T, int EC>
 __global__ void __launch_bounds__(kBlock, 1) bn_bwd_reduce_stream(const T* __restrict__ pre, const T* __restrict__ dy,
                                                                   long seg_rows, int bps, int C, long rpb, int R,
-                                                                  int ln, int rev, const float* __restrict__ mean,
+                                                                  int cpg, int rev, const float* __restrict__ mean,
                                                                   const float* __restrict__ inv_std,
                                                                   const float* __restrict__ gamma,
                                                                   const float* __restrict__ beta, int act,
@@ -771,7 +987,7 @@ __global__ void __launch_bounds__(kBlock, 1) bn_bwd_reduce_stream(const T* __res
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
     const int c = st.g * EC + e;
-    const int si = ln ? st.seg : c;
+    const int si = stat_index(cpg, st.seg, c, C);
     mu[e] = mean[si];
     is[e] = inv_std[si];
     ga[e] = gamma[c];
@@ -815,7 +1031,7 @@ __global__ void __launch_bounds__(kBlock, 1) bn_bwd_reduce_stream(const T* __res
 // d_conv (MODE 0: batch / layer norm, 1: no norm) and part[b][c] = sum d_conv.
 template <typename T, int EC, int MODE>
 __global__ void __launch_bounds__(kBlock, 1) dconv_stream(const T* __restrict__ pre, const T* __restrict__ dy,
-                                                          long seg_rows, int bps, int C, long rpb, int R, int ln,
+                                                          long seg_rows, int bps, int C, long rpb, int R, int cpg,
                                                           int rev, const float* __restrict__ mean,
                                                           const float* __restrict__ inv_std,
                                                           const float* __restrict__ gamma,
@@ -833,12 +1049,12 @@ __global__ void __launch_bounds__(kBlock, 1) dconv_stream(const T* __restrict__ 
     const int c = st.g * EC + e;
     a[e] = 0.f;
     if (MODE == 0) {
-      const int si = ln ? st.seg : c;
+      const int si = stat_index(cpg, st.seg, c, C);
       mu[e] = mean[si];
       is[e] = inv_std[si];
       ga[e] = gamma[c];
       be[e] = beta[c];
-      norm_bwd_coef(c12, ln, st.seg, c, C, ga[e], seg_rows, k1[e], k2[e]);
+      norm_bwd_coef(c12, cpg, st.seg, c, C, ga[e], seg_rows, k1[e], k2[e]);
     }
   }
   const T* const in[2] = {pre, dy};
@@ -895,10 +1111,11 @@ static int pick_bps(int segs, long seg_rows, long resident, long ovh) {
   return best;
 }
 
-RowWalk make_walk(long rows, int C, int dtype, int sms, int segs) {
+RowWalk make_walk(long rows, int C, int dtype, int sms, int segs, int cpg) {
   RowWalk w;
   w.rows = rows;
   w.C = C;
+  w.cpg = cpg;
   w.err = nullptr;
   w.segs = segs < 1 ? 1 : segs;
   w.seg_rows = rows / w.segs;
@@ -1014,7 +1231,7 @@ cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float
 
 // Walk arguments shared by every row-walk kernel: segment geometry and the layer-norm flag.
 #define WALK_ARGS wk.seg_rows, wk.bps, wk.C, wk.rows_per_block
-#define LN_FLAG (wk.segs > 1 ? 1 : 0)
+#define LN_FLAG wk.cpg
 
 cudaError_t launch_bn_apply(int dtype, const void* pre, void* y, const RowWalk& wk, const float* mean,
                             const float* inv_std, const float* gamma, const float* beta, int act, int rev,
@@ -1109,9 +1326,34 @@ cudaError_t launch_ln_stats_finalize(const float* rstats, int n_images, long hw,
   return cudaGetLastError();
 }
 
-cudaError_t launch_ln_seg_finalize(const float* part, const RowWalk& wk, const float* gamma, float* out,
-                                   cudaStream_t st) {
-  ln_seg_finalize_kernel<<<wk.segs, 128, 0, st>>>(part, wk.bps, wk.C, gamma, out);
+cudaError_t launch_norm_seg_finalize(const float* part, const RowWalk& wk, const float* gamma, float* out,
+                                     cudaStream_t st) {
+  const int n_out = wk.segs * (wk.C / wk.cpg);
+  const int wpo = finalize_wpo(static_cast<long>(wk.bps) * wk.cpg), opb = 4 / wpo;
+  norm_seg_finalize_kernel<<<(n_out + opb - 1) / opb, 128, 0, st>>>(part, wk.bps, wk.C, wk.cpg, n_out, wpo, gamma,
+                                                                     out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_stats(int dtype, const void* pre, const RowWalk& wk, int rev, float* part,
+                              cudaStream_t st) {
+  if (wk.stream) {
+    STREAM_LAUNCH(dtype, 1, (norm_stats_stream<T, EC>), static_cast<const T*>(pre), WALK_ARGS, wk.R, rev, part,
+                  wk.err);
+    return cudaGetLastError();
+  }
+  DISPATCH_EC(dtype, wk.C,
+              (norm_stats_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), WALK_ARGS, part)),
+              (norm_stats_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), WALK_ARGS, part)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gn_stats_finalize(const float* part, const RowWalk& wk, float eps, float* mean, float* inv_std,
+                                     cudaStream_t st) {
+  const int n_out = wk.segs * (wk.C / wk.cpg);
+  const int wpo = finalize_wpo(static_cast<long>(wk.bps) * wk.cpg), opb = 4 / wpo;
+  gn_stats_finalize_kernel<<<(n_out + opb - 1) / opb, 128, 0, st>>>(part, wk.bps, wk.C, wk.cpg, n_out, wpo, eps,
+                                                                     mean, inv_std);
   return cudaGetLastError();
 }
 

@@ -32,11 +32,12 @@ struct RowWalk {
   long rows_per_block;
   int segs, bps;
   long seg_rows;
+  int cpg;     // statistics per channel (0, batch norm) or per image and group of cpg channels
   int stream;  // rows move through shared memory by bulk TMA copies (vector path)
   int R;       // rows per streamed chunk
   int* err;    // device error word for bounded waits
 };
-RowWalk make_walk(long rows, int C, int dtype, int sms, int segs);
+RowWalk make_walk(long rows, int C, int dtype, int sms, int segs, int cpg);
 
 // elementwise / reduction kernels (bn_kernels.cu); dtype 0 = fp32, 1 = bf16
 cudaError_t launch_pack_channels(int dtype, const void* src, void* dst, long rows, int C, int Cp, cudaStream_t st);
@@ -67,13 +68,19 @@ cudaError_t launch_bn_bwd_apply(int dtype, const void* pre, const void* dy, cons
 cudaError_t launch_act_bwd(int dtype, const void* pre, const void* dy, const RowWalk& wk, int Cp, int act,
                            void* dconv, float* part, cudaStream_t st);
 // Layer norm: per-image mean / inv_std from the fprop epilogue's per-pixel (mean, M2) partials
-// [n_images * hw][n_tiles][halves][2] (half 0 = the first hcols columns of a tile); per-image sums of
-// gamma * d_norm and gamma * d_norm * z from the bwd-reduce partials of an image-aligned walk, written to
-// out[2n], out[2n + 1].
+// [n_images * hw][n_tiles][halves][2] (half 0 = the first hcols columns of a tile).
 cudaError_t launch_ln_stats_finalize(const float* rstats, int n_images, long hw, int n_tiles, int halves, int BN,
                                      int hcols, int OC, float eps, float* mean, float* inv_std, cudaStream_t st);
-cudaError_t launch_ln_seg_finalize(const float* part, const RowWalk& wk, const float* gamma, float* out,
-                                   cudaStream_t st);
+// Layer / group norm backward: per-(image, group) sums of gamma * d_norm and gamma * d_norm * z from the
+// bwd-reduce partials of an image-aligned walk, written to out[2s], out[2s + 1] (s = image * groups + g).
+cudaError_t launch_norm_seg_finalize(const float* part, const RowWalk& wk, const float* gamma, float* out,
+                                     cudaStream_t st);
+// Group norm forward statistics: per-block, per-channel (rows, mean, M2) of the stored pre-activations on
+// an image-aligned walk, then their per-(image, group) merge.
+cudaError_t launch_norm_stats(int dtype, const void* pre, const RowWalk& wk, int rev, float* part,
+                              cudaStream_t st);
+cudaError_t launch_gn_stats_finalize(const float* part, const RowWalk& wk, float eps, float* mean, float* inv_std,
+                                     cudaStream_t st);
 cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int taps, int ICp, int IC, float* dw,
                                 cudaStream_t st);
 cudaError_t launch_bn_eval_stats(const float* rm, const float* rv, float eps, int C, float* mean, float* inv_std,

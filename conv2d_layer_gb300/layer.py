@@ -17,7 +17,7 @@ class Conv2dLayer:
                  device="cuda"):
         self.spec = spec
         self.desc = abi.desc(spec.N, spec.H, spec.W, spec.IC, spec.OC, spec.KH, spec.KW, spec.stride, spec.pad,
-                             spec.norm, spec.act, spec.dtype, spec.eps, spec.momentum, spec.bn_eval)
+                             spec.norm, spec.act, spec.dtype, spec.eps, spec.momentum, spec.bn_eval, spec.groups)
         abi.check(abi.conv2d_validate(self.desc), "conv2d_validate")
         self.dt = _TORCH_DT[spec.dtype]
         dev = torch.device(device)
@@ -31,8 +31,8 @@ class Conv2dLayer:
         y_shape = (spec.N, spec.OH, spec.OW, spec.OC)
         self.pre_act = torch.empty(y_shape, device=dev, dtype=self.dt)
         self.y = torch.empty(y_shape, device=dev, dtype=self.dt)
-        # saved statistics: per channel (batch norm) or per image (layer norm)
-        n_stat = spec.N if spec.norm == abi.NORM_LAYER else spec.OC
+        # saved statistics: per channel (batch norm), per image (layer norm) or per image and group
+        n_stat = {abi.NORM_LAYER: spec.N, abi.NORM_GROUP: spec.N * spec.groups}.get(spec.norm, spec.OC)
         self.save_mean = torch.zeros(n_stat, **f32)
         self.save_inv_std = torch.zeros(n_stat, **f32)
         self.dw = torch.zeros(spec.OC, spec.KH, spec.KW, spec.IC, **f32)

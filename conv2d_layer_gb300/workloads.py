@@ -25,7 +25,7 @@ import math
 import torch
 
 FP32, BF16 = 0, 1
-NORM_NONE, NORM_BATCH, NORM_LAYER = 0, 1, 2
+NORM_NONE, NORM_BATCH, NORM_LAYER, NORM_GROUP = 0, 1, 2, 3
 ACT_IDENTITY, ACT_RELU, ACT_TANH, ACT_SIGMOID = 0, 1, 2, 3
 
 
@@ -46,6 +46,7 @@ class LayerSpec:
     eps: float = 1e-5
     momentum: float = 0.1
     bn_eval: int = 0      # batch norm in evaluation mode inside training
+    groups: int = 1       # group norm: channel groups
 
     @property
     def OH(self):

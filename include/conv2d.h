@@ -3,7 +3,7 @@
  * (libconv2d.so).
  *
  * One NHWC 2D convolution layer: conv + bias, optional training-mode batch
- * norm or layer norm, activation; and its backward pass. The operation is the one defined by
+ * norm, layer norm or group norm, activation; and its backward pass. The operation is the one defined by
  * the rl-tools conv2d layer pages ("operations_generic.h": `forward`,
  * `evaluate`, `backward`, `backward_input`, `backward_full`; the CUDA page
  * "operations_cuda.h" splits the same work into cuDNN calls and per-channel
@@ -57,11 +57,15 @@ enum {
     CONV2D_ERR_TIMEOUT = 5      /* a device-side bounded wait expired (reported by conv2d_device_status) */
 };
 
-/* Normalization (the pages' `Normalization` enum). BATCH: per-channel
- * statistics over N*OH*OW with running statistics. LAYER: per-image
- * statistics over OH*OW*OC of the stored pre-activations (the pages'
- * LAYER_NORM branches), per-channel gamma / beta, no running statistics. */
-enum { CONV2D_NORM_NONE = 0, CONV2D_NORM_BATCH = 1, CONV2D_NORM_LAYER = 2 };
+/* Normalization (the pages' `Normalization` enum, plus the group norm of the
+ * WebGPU page's GroupNorm backward). BATCH: per-channel statistics over
+ * N*OH*OW with running statistics. LAYER: per-image statistics over OH*OW*OC
+ * of the stored pre-activations (the pages' LAYER_NORM branches), per-channel
+ * gamma / beta, no running statistics. GROUP: desc.groups groups of OC/groups
+ * consecutive channels, statistics per (image, group) over OH*OW*OC/groups
+ * stored pre-activations, per-channel gamma / beta, no running statistics
+ * (GROUP with groups = 1 computes LAYER). */
+enum { CONV2D_NORM_NONE = 0, CONV2D_NORM_BATCH = 1, CONV2D_NORM_LAYER = 2, CONV2D_NORM_GROUP = 3 };
 
 /* Activation applied after (optional) normalization. */
 enum { CONV2D_ACT_IDENTITY = 0, CONV2D_ACT_RELU = 1, CONV2D_ACT_TANH = 2, CONV2D_ACT_SIGMOID = 3 };
@@ -82,12 +86,15 @@ enum { CONV2D_OP_FWD_TRAIN = 0, CONV2D_OP_FWD_INFER = 1, CONV2D_OP_BWD = 2 };
  * statistics, writes them as save_mean / save_inv_std (= 1/sqrt(var+eps)) and
  * updates nothing; conv2d_bwd then uses the frozen-statistics backward
  * (d_conv = act'(bn) * dy * gamma * inv_std). Zero keeps training mode.
- * Layer norm has no evaluation mode on the pages: bn_eval is ignored there. */
+ * Layer and group norm have no evaluation mode on the pages: bn_eval is
+ * ignored there. groups is read only for GROUP norm (1 <= groups, OC % groups
+ * == 0). */
 typedef struct {
     int32_t N, H, W, IC, OC, KH, KW, stride, pad;
     int32_t norm, act, dtype;
     float eps, momentum;
     int32_t bn_eval;
+    int32_t groups;
 } conv2d_desc;
 
 /* Output spatial size. Returns CONV2D_OK or CONV2D_ERR_INVALID_ARG. */
@@ -110,6 +117,8 @@ size_t conv2d_workspace_size(const conv2d_desc* desc, int op);
  *   LAYER norm: gamma, beta [OC] in; save_mean, save_inv_std [N] out: the
  *     per-image mean and 1/sqrt(var+eps) of the stored pre_act;
  *     running_mean / running_var are not read and may be NULL.
+ *   GROUP norm: as LAYER with save_mean, save_inv_std [N*groups] (index
+ *     n*groups + g).
  *   bias may be NULL (treated as zero). */
 int conv2d_fwd_train(const conv2d_desc* desc, const void* x, const void* w, const float* bias,
                      const float* gamma, const float* beta, float* running_mean, float* running_var,
@@ -138,21 +147,25 @@ int conv2d_fwd_train_noalloc(const conv2d_desc* desc, const void* x, const void*
 
 /* Inference forward (`evaluate`): y = act(norm(conv + bias)), batch norm with
  * the running statistics (`bn_stats_eval` / `bn_forward_eval_running` on the
- * CUDA page), layer norm with per-image statistics of the stored conv output
- * computed on the fly; no state is written. gamma, beta are read for BATCH
- * and LAYER norm, running_mean, running_var only for BATCH. */
+ * CUDA page), layer / group norm with per-image (per-group) statistics of the
+ * stored conv output computed on the fly; no state is written. gamma, beta
+ * are read for BATCH, LAYER and GROUP norm, running_mean, running_var only
+ * for BATCH. */
 int conv2d_fwd_infer(const conv2d_desc* desc, const void* x, const void* w, const float* bias,
                      const float* gamma, const float* beta, const float* running_mean,
                      const float* running_var, void* y, void* ws, size_t ws_bytes, void* stream);
 
 /* Backward (`backward_full`; `backward_input` when dw..dbeta are all NULL;
- * `backward` when dx is NULL). Inputs: x, w, pre_act and (BATCH / LAYER)
- * gamma, beta, save_mean, save_inv_std from conv2d_fwd_train, dy = dLoss/dy.
+ * `backward` when dx is NULL). Inputs: x, w, pre_act and (BATCH / LAYER /
+ * GROUP) gamma, beta, save_mean, save_inv_std from conv2d_fwd_train,
+ * dy = dLoss/dy.
  *   dx [N][H][W][IC]   out (overwritten), may be NULL
  *   dw [OC][KH][KW][IC], dbias [OC]        accumulated, may be NULL together
- *   dgamma, dbeta [OC] (BATCH / LAYER)      accumulated, may be NULL together
+ *   dgamma, dbeta [OC] (with a norm)        accumulated, may be NULL together
  * The norm backward uses the saved statistics, not recomputed ones; under
- * layer norm its projection sums run over each image (OH*OW*OC elements).
+ * layer / group norm its projection sums run over each image (group): the
+ * GroupNorm backward of the WebGPU page ("groupnorm_backward.wgsl") with the
+ * activation derivative in front and the dgamma / dbeta it leaves out.
  * At least one of dx / dw must be non-NULL. */
 int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const float* gamma,
                const float* beta, const void* pre_act, const float* save_mean,

@@ -3,9 +3,10 @@ same seeded inputs through the CPU oracle, and compare per output tensor.
 
 Tolerance (per output tensor): max|gpu - ref| / max|ref| <= 1e-5 for the FP32
 (3xTF32) mode and <= 2e-2 for the BF16 mode; running statistics <= 1e-5.
-dBias under training batch norm is analytically zero, so it is checked
-against the scale of the summed terms instead: |dbias[c]| <= t * sum|d_conv[:,c]|
-with t = 1e-4 (FP32) / 2e-2 (BF16). Under layer norm the saved statistics are
+dBias under training batch norm (and under group norm with one channel per
+group) is analytically zero, so it is checked against the scale of the summed
+terms instead: |dbias[c]| <= t * sum|d_conv[:,c]| with t = 1e-4 (FP32) / 2e-2
+(BF16). Under layer norm the saved statistics are
 per image ([N]) and are compared like the other outputs.
 """
 import numpy as np
@@ -14,7 +15,7 @@ import torch
 import oracle
 from conv2d_layer_gb300 import abi
 from conv2d_layer_gb300.layer import Conv2dLayer
-from conv2d_layer_gb300.workloads import BF16, NORM_BATCH, NORM_NONE
+from conv2d_layer_gb300.workloads import BF16, NORM_BATCH, NORM_GROUP, NORM_NONE
 
 TOL = {0: 1e-5, 1: 2e-2}
 STAT_TOL = 1e-5
@@ -35,7 +36,8 @@ def oracle_layer(spec):
     """Oracle layer with the pre-activations stored in the layer's element type, as the pages do."""
     return oracle.Layer(spec.N, spec.H, spec.W, spec.IC, spec.OC, spec.KH, spec.KW, spec.stride, spec.pad,
                         norm=spec.norm, act=spec.act, eps=spec.eps, momentum=spec.momentum,
-                        store="bf16" if spec.dtype == BF16 else "f32", bn_eval=spec.bn_eval)
+                        store="bf16" if spec.dtype == BF16 else "f32", bn_eval=spec.bn_eval,
+                        groups=spec.groups)
 
 
 def run_pair(spec, inp, prev_grads=False, need_dx=True, need_params=True, seed=0):
@@ -87,7 +89,9 @@ def check_pair(spec, gpu, ref, need_dx=True, need_params=True):
         names += ["mean", "inv_std"]
     if need_dx:
         names += ["dx"]
-    bn_train = spec.norm == NORM_BATCH and not spec.bn_eval
+    # dbias is analytically zero under training batch norm and under group norm with one channel per
+    # group (instance norm): a shift of a channel's bias leaves the output unchanged
+    bn_train = (spec.norm == NORM_BATCH and not spec.bn_eval) or (spec.norm == NORM_GROUP and spec.groups == spec.OC)
     if need_params:
         names += ["dw"]
         if spec.norm != NORM_NONE:
@@ -102,6 +106,7 @@ def check_pair(spec, gpu, ref, need_dx=True, need_params=True):
             errs[k] = rel_err(gpu[k], ref[k])
             if not errs[k] <= STAT_TOL:
                 bad[k] = errs[k]
+    if spec.norm != NORM_NONE:
         if need_params and bn_train:
             dc = ref["dconv"].reshape(-1, spec.OC)
             bound = DBIAS_TOL[spec.dtype] * np.abs(dc).sum(0)

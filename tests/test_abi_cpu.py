@@ -46,7 +46,7 @@ def test_out_hw():
 @pytest.mark.parametrize("field,value,code", [
     ("N", 0, abi.ERR_INVALID_ARG), ("H", -1, abi.ERR_INVALID_ARG), ("IC", 0, abi.ERR_INVALID_ARG),
     ("OC", 0, abi.ERR_INVALID_ARG), ("KH", 0, abi.ERR_INVALID_ARG), ("stride", 0, abi.ERR_INVALID_ARG),
-    ("pad", -1, abi.ERR_INVALID_ARG), ("KH", 11, abi.ERR_INVALID_ARG), ("norm", 3, abi.ERR_INVALID_ARG),
+    ("pad", -1, abi.ERR_INVALID_ARG), ("KH", 11, abi.ERR_INVALID_ARG), ("norm", 4, abi.ERR_INVALID_ARG),
     ("act", 4, abi.ERR_INVALID_ARG), ("dtype", 2, abi.ERR_INVALID_ARG), ("eps", 0.0, abi.ERR_INVALID_ARG),
     ("eps", float("nan"), abi.ERR_INVALID_ARG), ("momentum", 1.5, abi.ERR_INVALID_ARG),
     ("momentum", -0.1, abi.ERR_INVALID_ARG), ("stride", 9, abi.ERR_UNSUPPORTED),
@@ -60,6 +60,16 @@ def test_validation_codes(field, value, code):
 
 def test_eps_and_momentum_ignored_without_norm():
     assert abi.conv2d_validate(good(norm=abi.NORM_NONE, eps=0.0, momentum=7.0)) == abi.OK
+
+
+def test_group_norm_groups_validated():
+    assert abi.conv2d_validate(good(norm=abi.NORM_GROUP, groups=2)) == abi.OK       # OC = 4
+    assert abi.conv2d_validate(good(norm=abi.NORM_GROUP, groups=3)) == abi.ERR_INVALID_ARG
+    assert abi.conv2d_validate(good(norm=abi.NORM_GROUP, groups=0)) == abi.ERR_INVALID_ARG
+    assert abi.conv2d_validate(good(norm=abi.NORM_LAYER, groups=0)) == abi.OK       # read for group norm only
+    d = good(norm=abi.NORM_GROUP, groups=32, dtype=abi.BF16, H=56, W=56, IC=256, OC=256)
+    for op in (abi.OP_FWD_TRAIN, abi.OP_FWD_INFER, abi.OP_BWD):
+        assert abi.conv2d_workspace_size(d, op) > 0
 
 
 def test_layer_norm_reads_eps_not_momentum():
