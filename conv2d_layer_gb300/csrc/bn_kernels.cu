@@ -1,7 +1,7 @@
 // bn_kernels.cu - the bandwidth-bound steps of the conv2d training step:
-// batch-norm statistics, normalise + affine + activation, activation /
-// batch-norm backward (d_conv, dgamma, dbeta, dbias), weight preparation for
-// the tensor-core GEMMs, and the split-K reduction of dW.
+// batch-, layer- and group-norm statistics, normalise + affine + activation,
+// activation / norm backward (d_conv, dgamma, dbeta, dbias), weight
+// preparation for the tensor-core GEMMs, and the split-K reduction of dW.
 //
 // Formulas: rl-tools "operations_generic.h" (`forward` BN training branch and
 // Phase 3; `backward_full` training branch) and the per-channel kernels of
