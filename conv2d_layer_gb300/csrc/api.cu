@@ -258,7 +258,7 @@ Tile conv_tile(const Geo& g, int ncols) {
   const size_t stage = ns * (kBM * 128 + static_cast<size_t>(t.BN) * 128);
   const size_t stats = 11 * static_cast<size_t>(t.BN) * 4;  // epilogue statistics scratch + column constants
   t.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048 - stats) / stage));
-  t.smem = t.stages * stage + 1024 + 256 + stats;
+  t.smem = t.stages * stage + 1024 + 512 + stats;  // alignment slack, barriers + TMEM slot, epilogue scratch
   return t;
 }
 
@@ -377,8 +377,16 @@ DgradPlan dgrad_plan(const Geo& g) {
   return d;
 }
 
+// dgrad in column form (a 1x1 GEMM d_conv x W^T into dcol[pix][(tap, icp)], then a per-element gather)
+// for strided layers with few input channels: there the stride-phase GEMMs have a column tile of IC
+// padded to 32 and only KH*KW/S^2 taps each, so most of their tensor-core and operand traffic is waste.
+bool dgrad_col2im(const Geo& g) {
+  const size_t dcol = static_cast<size_t>(g.n_pix) * g.taps * g.ICp * g.ES;
+  return g.S > 1 && g.IC <= 16 && g.OCp >= g.BKE && dcol <= (size_t(1) << 31);
+}
+
 // ------------------------------------------------------------ workspace plan
-enum Reg { R_XP, R_WB, R_WBLO, R_PART, R_FOLD, R_DC, R_C12, R_WD, R_WDLO, R_WPART, R_NREG };
+enum Reg { R_XP, R_WB, R_WBLO, R_PART, R_FOLD, R_DC, R_C12, R_WD, R_WDLO, R_WPART, R_COL, R_NREG };
 
 struct Plan {
   size_t off[R_NREG];
@@ -420,6 +428,7 @@ void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
     sz[R_WD] = static_cast<size_t>(g.ICp) * kd * es;
     if (g.dt == CONV2D_FP32) sz[R_WDLO] = static_cast<size_t>(g.ICp) * kd * 4;
     if (g.pack_x) sz[R_XP] = static_cast<size_t>(g.N) * g.H * g.W * g.ICp * es;
+    if (dgrad_col2im(g)) sz[R_COL] = static_cast<size_t>(g.n_pix) * g.taps * g.ICp * es;
     pl->wg = wgrad_plan(g, sms);
     sz[R_WPART] = static_cast<size_t>(pl->wg.splits) * g.OC * pl->wg.Mk * 4;
   }
@@ -521,8 +530,35 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   return CONV2D_OK;
 }
 
+// Column-form dgrad (see dgrad_col2im): dcol = d_conv [n_pix][OCp] x B[(tap, icp)][oc] as the fprop of a
+// 1x1 convolution over the d_conv image, then dX gathered per element.
+int run_dgrad_col2im(const Geo& g, const DevInfo* dev, const void* w, const void* dconv, void* dx, void* ws,
+                     const Plan& pl, cudaStream_t st) {
+  void* bhi = region(ws, pl, R_WD);
+  float* blo = reinterpret_cast<float*>(region(ws, pl, R_WDLO));
+  const bool bf = g.dt == CONV2D_BF16;
+  LAUNCH("dgrad_weights", st,
+         launch_prep_col2im_weights(g.dt, w, bhi, bf ? nullptr : blo, g.OC, g.taps, g.IC, g.ICp, g.OCp, st));
+  conv2d_desc d2;
+  std::memset(&d2, 0, sizeof(d2));
+  d2.N = g.N; d2.H = g.OH; d2.W = g.OW; d2.IC = g.OCp; d2.OC = g.taps * g.ICp;
+  d2.KH = 1; d2.KW = 1; d2.stride = 1; d2.pad = 0;
+  d2.norm = CONV2D_NORM_NONE; d2.act = CONV2D_ACT_IDENTITY; d2.dtype = g.dt;
+  Geo g2;
+  int rc = make_geo(&d2, &g2);
+  if (rc) return rc;
+  void* dcol = region(ws, pl, R_COL);
+  if ((rc = run_fprop(g2, dev, dconv, bhi, bf ? nullptr : blo, dcol, nullptr, nullptr, nullptr, 0, nullptr, nullptr,
+                      nullptr, nullptr, st)))
+    return rc;
+  LAUNCH("dgrad_col2im", st,
+         launch_col2im(g.dt, dcol, dx, g.N, g.H, g.W, g.IC, g.ICp, g.OH, g.OW, g.KH, g.KW, g.S, g.P, st));
+  return CONV2D_OK;
+}
+
 int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv, void* dx, void* ws,
               const Plan& pl, cudaStream_t st) {
+  if (dgrad_col2im(g)) return run_dgrad_col2im(g, dev, w, dconv, dx, ws, pl, st);
   static ConvGemmParams p;
   static DgradPlan d;
   static std::mutex mu;

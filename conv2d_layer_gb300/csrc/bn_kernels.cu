@@ -485,6 +485,68 @@ __global__ void prep_fprop_weights_kernel(const T* __restrict__ w, T* __restrict
   }
 }
 
+// Column-form dgrad weights: B[(tap, icp)][oc], K = OCp, the transpose of W[oc][tap][ic] (zero in the
+// padded ic and oc positions); 3xTF32 splits into hi / lo.
+template <typename T>
+__global__ void prep_col2im_weights_kernel(const T* __restrict__ w, T* __restrict__ bhi, float* __restrict__ blo,
+                                           int OC, int taps, int IC, int ICp, int OCp) {
+  const long total = static_cast<long>(taps) * ICp * OCp;
+  for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const int oc = static_cast<int>(i % OCp);
+    const long r = i / OCp;
+    const int ic = static_cast<int>(r % ICp), tap = static_cast<int>(r / ICp);
+    const T v = (oc < OC && ic < IC) ? w[(static_cast<long>(oc) * taps + tap) * IC + ic] : T(0.f);
+    if constexpr (sizeof(T) == 4) {
+      uint32_t hi, lo;
+      split_tf32(static_cast<float>(v), hi, lo);
+      reinterpret_cast<uint32_t*>(bhi)[i] = hi;
+      reinterpret_cast<uint32_t*>(blo)[i] = lo;
+    } else {
+      bhi[i] = v;
+    }
+  }
+}
+
+// dX from the column form dcol[(n, oh, ow)][(kh, kw, icp)] = sum_oc d_conv * W: each input pixel sums
+// the kernel taps whose window covers it (`backward_full`'s scatter of d_conv * W, gathered per dX
+// element), in a fixed (kh, kw) order.
+template <typename T, int EC>
+__global__ void col2im_kernel(const T* __restrict__ dcol, T* __restrict__ dx, int N, int H, int W, int IC, int ICp,
+                              int OH, int OW, int KH, int KW, int S, int P) {
+  const int groups = IC / EC;
+  const long total = static_cast<long>(N) * H * W * groups;
+  const int taps_icp = KH * KW * ICp;
+  for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const int g = static_cast<int>(i % groups);
+    const long pix = i / groups;
+    const int iw = static_cast<int>(pix % W);
+    const long t = pix / W;
+    const int ih = static_cast<int>(t % H);
+    const int n = static_cast<int>(t / H);
+    float acc[EC];
+#pragma unroll
+    for (int e = 0; e < EC; ++e) acc[e] = 0.f;
+    for (int kh = (ih + P) % S; kh < KH; kh += S) {
+      const int oh = (ih + P - kh) / S;
+      if (oh < 0) break;
+      if (oh >= OH) continue;
+      for (int kw = (iw + P) % S; kw < KW; kw += S) {
+        const int ow = (iw + P - kw) / S;
+        if (ow < 0) break;
+        if (ow >= OW) continue;
+        float v[EC];
+        load_v<EC>(dcol + (static_cast<size_t>(n * OH + oh) * OW + ow) * taps_icp + (kh * KW + kw) * ICp + g * EC,
+                   v);
+#pragma unroll
+        for (int e = 0; e < EC; ++e) acc[e] += v[e];
+      }
+    }
+    store_v<EC>(dx + pix * IC + g * EC, acc);
+  }
+}
+
 // dgrad weight matrix B[icp][col]; for phase ph the columns (t,u,oc) hold
 // W[oc][rh + S*t][rw + S*u][ic].
 template <typename T>
@@ -1359,6 +1421,29 @@ cudaError_t launch_gn_stats_finalize(const float* part, const RowWalk& wk, float
 
 #undef WALK_ARGS
 #undef LN_FLAG
+
+cudaError_t launch_prep_col2im_weights(int dtype, const void* w, void* bhi, float* blo, int OC, int taps, int IC,
+                                       int ICp, int OCp, cudaStream_t st) {
+  const int g = grid_for(static_cast<long>(taps) * ICp * OCp, 256);
+  if (dtype == 1)
+    prep_col2im_weights_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w),
+                                                                 static_cast<__nv_bfloat16*>(bhi), nullptr, OC, taps,
+                                                                 IC, ICp, OCp);
+  else
+    prep_col2im_weights_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(w), static_cast<float*>(bhi), blo,
+                                                         OC, taps, IC, ICp, OCp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_col2im(int dtype, const void* dcol, void* dx, int N, int H, int W, int IC, int ICp, int OH, int OW,
+                          int KH, int KW, int S, int P, cudaStream_t st) {
+  DISPATCH_EC(dtype, IC,
+              (col2im_kernel<T, EC><<<grid_for(static_cast<long>(N) * H * W * (IC / EC), 256), 256, 0, st>>>(
+                  static_cast<const T*>(dcol), static_cast<T*>(dx), N, H, W, IC, ICp, OH, OW, KH, KW, S, P)),
+              (col2im_kernel<T, EC><<<grid_for(static_cast<long>(N) * H * W * (IC / EC), 256), 256, 0, st>>>(
+                  static_cast<const T*>(dcol), static_cast<T*>(dx), N, H, W, IC, ICp, OH, OW, KH, KW, S, P)));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int taps, int ICp, int IC, float* dw,
                                 cudaStream_t st) {

@@ -20,7 +20,7 @@
 //   warps 6-9   epilogue: TMEM -> registers -> bias / scale / activation ->
 //               global memory
 // A ring of `stages` shared-memory stages (full/empty mbarriers) feeds the
-// MMA warp; two TMEM accumulators (tfull/tempty mbarriers) let the epilogue
+// MMA warp; two or more TMEM accumulators (tfull/tempty mbarriers) let the epilogue
 // of one tile overlap the main loop of the next.
 //
 // Precision: BF16 operands accumulate in fp32. FP32 operands run 3xTF32:
@@ -34,6 +34,7 @@ constexpr int kThreads = 320;
 constexpr int kMaxStages = 8;
 constexpr int kMaxPhases = 64;
 constexpr int kBM = 128;          // rows of a tile (TMEM lanes)
+constexpr int kMaxTmemBufs = 8;   // TMEM accumulators of the fprop / dgrad kernel (512 columns / BN, capped)
 constexpr int kLag = 3;           // cp.async groups kept in flight per producer thread (needs >= 4 stages)
 
 // wait sites recorded in the error word
@@ -272,18 +273,21 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_bytes);
   uint64_t* empty = full + kMaxStages;
   uint64_t* tfull = empty + kMaxStages;
-  uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tempty = tfull + kMaxTmemBufs;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + kMaxTmemBufs);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t tcols = tmem_cols_for(2 * BN);
+  // TMEM accumulators in flight: as many BN-column buffers as fit (at least two), so that short tiles
+  // (few k-blocks) keep the MMA busy while the epilogue of earlier tiles completes
+  const int nbuf = 512 / BN < kMaxTmemBufs ? 512 / BN : kMaxTmemBufs;
+  const uint32_t tcols = tmem_cols_for(nbuf * BN);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], p.a_tma ? 1 : 4 + 1);  // the TMA thread (+ one arrival per producer warp)
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < nbuf; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], p.a_tma ? 8 : 4);  // one arrival per epilogue warp
     }
@@ -353,8 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       bool alive = true;
       for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x, ++tc) {
         const ConvPhase& ph = find_phase(p, u);
-        const int buf = tc & 1;
-        if (!wait(&tempty[buf], ((tc >> 1) & 1) ^ 1, p.err, kSiteTEmpty)) break;
+        const int buf = tc % nbuf;
+        if (!wait(&tempty[buf], ((tc / nbuf) & 1) ^ 1, p.err, kSiteTEmpty)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + buf * BN;
         for (int kb = 0; kb < ph.num_kb; ++kb) {
@@ -401,6 +405,35 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     uint32_t par = 0;
     int it = 0;
     bool alive = !p.a_tma;
+    // k-blocks whose copies stay in flight before the stage is released (fewer when the ring is short).
+    // fp32 keeps one: its stages are twice as large (hi and lo tiles), so the ring holds only 3-5 of
+    // them, and every k-block of lag is a stage the MMA cannot use as slack.
+    const int lag = DT == 0 ? 1 : (S - 1 < kLag ? S - 1 : kLag);
+    // fp32: the copied rows land in the hi tile; once they are in, each thread splits its own chunks in
+    // place (hi stays, lo goes to the lo tile)
+    auto split_stage = [&](int q) {
+      const uint32_t b0 = sbase + (q % S) * stage_bytes;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t dst = b0 + (r0 + 16 * i) * 128 + swz;
+        uint32_t x0, x1, x2, x3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3) : "r"(dst));
+        uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+        split_tf32(__uint_as_float(x0), h0, l0);
+        split_tf32(__uint_as_float(x1), h1, l1);
+        split_tf32(__uint_as_float(x2), h2, l2);
+        split_tf32(__uint_as_float(x3), h3, l3);
+        st_shared_v4(dst, h0, h1, h2, h3);
+        st_shared_v4(dst + a_bytes, l0, l1, l2, l3);
+      }
+    };
+    // wait for all but the newest `lag` copy groups (an immediate operand, hence the switch)
+    auto wait_lag = [&]() {
+      if (lag >= 3) cp_async_wait<3>();
+      else if (lag == 2) cp_async_wait<2>();
+      else if (lag == 1) cp_async_wait<1>();
+      else cp_async_wait<0>();
+    };
     for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
       const ConvPhase& ph = find_phase(p, u);
       const int m_tile = (u - ph.unit_begin) / p.n_tiles;
@@ -442,32 +475,15 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
                           static_cast<unsigned>(iw) < static_cast<unsigned>(p.Ws);
           const size_t off = ok ? (static_cast<size_t>(pb[i] + ih * p.Ws + iw) * p.Cs + c) * D::ES : 0;
           const uint32_t dst = a0 + (r0 + 16 * i) * 128 + swz;
-          if (DT == 1) {
-            cp_async16(dst, src + off, ok ? 16u : 0u);
-          } else {
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (ok) v = __ldg(reinterpret_cast<const float4*>(src + off));
-            uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
-            split_tf32(v.x, h0, l0);
-            split_tf32(v.y, h1, l1);
-            split_tf32(v.z, h2, l2);
-            split_tf32(v.w, h3, l3);
-            st_shared_v4(dst, h0, h1, h2, h3);
-            st_shared_v4(dst + a_bytes, l0, l1, l2, l3);
-          }
+          cp_async16(dst, src + off, ok ? 16u : 0u);  // out of bounds: 16 zero bytes
         }
-        if (DT == 1) {
-          cp_async_commit();
-          if (it >= kLag) {
-            cp_async_wait<kLag>();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[(it - kLag) % S]);
-          }
-        } else {
+        cp_async_commit();
+        if (it >= lag) {
+          wait_lag();
+          if (DT == 0) split_stage(it - lag);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&full[s]);
+          if (lane == 0) mbar_arrive(&full[(it - lag) % S]);
         }
         ++it;
         if (++s == S) {
@@ -476,12 +492,15 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         }
       }
     }
-    if (DT == 1) {
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (alive && lane == 0)
-        for (int q = (it > kLag ? it - kLag : 0); q < it; ++q) mbar_arrive(&full[q % S]);
+    // the last `lag` stages: wait for every copy, split, release
+    cp_async_wait<0>();
+    if (alive) {
+      for (int q = (it > lag ? it - lag : 0); q < it; ++q) {
+        if (DT == 0) split_stage(q);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[q % S]);
+      }
     }
   } else {
     // ------------------------------------------------ epilogue
@@ -535,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       const ConvPhase& ph = find_phase(p, u);
       const int local = u - ph.unit_begin;
       const int m_tile = local / p.n_tiles, n_tile = local % p.n_tiles;
-      const int buf = tc & 1;
+      const int buf = tc % nbuf;
       // lane 0 of each warp waits; the four warps agree before anyone goes on,
       // so the warp-aligned tcgen05.ld and the named barriers below stay
       // uniform even when a wait gives up
@@ -550,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         cur_n_tile = n_tile;
       }
       int ok = 1;
-      if (lane == 0) ok = wait(&tfull[buf], (tc >> 1) & 1, p.err, kSiteTFull) ? 1 : 0;
+      if (lane == 0) ok = wait(&tfull[buf], (tc / nbuf) & 1, p.err, kSiteTFull) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!named_bar_and(1, nthr, ok)) break;
       tc_fence_after();

@@ -81,6 +81,12 @@ cudaError_t launch_norm_stats(int dtype, const void* pre, const RowWalk& wk, int
                               cudaStream_t st);
 cudaError_t launch_gn_stats_finalize(const float* part, const RowWalk& wk, float eps, float* mean, float* inv_std,
                                      cudaStream_t st);
+// Column-form dgrad for small input-channel counts with stride: dcol = d_conv x B (a 1x1 fprop over
+// d_conv with B[(tap, icp)][oc] from prep_col2im_weights), then dX gathered from dcol per element.
+cudaError_t launch_prep_col2im_weights(int dtype, const void* w, void* bhi, float* blo, int OC, int taps, int IC,
+                                       int ICp, int OCp, cudaStream_t st);
+cudaError_t launch_col2im(int dtype, const void* dcol, void* dx, int N, int H, int W, int IC, int ICp, int OH, int OW,
+                          int KH, int KW, int S, int P, cudaStream_t st);
 cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int taps, int ICp, int IC, float* dw,
                                 cudaStream_t st);
 cudaError_t launch_bn_eval_stats(const float* rm, const float* rv, float eps, int C, float* mean, float* inv_std,
