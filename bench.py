@@ -197,33 +197,47 @@ def run_gpu(args, rank, world, local_rank):
         k[0] += 1
         k[1] += t
 
-    # end to end through the public API with host buffers: pinned X, dY in;
-    # the parameter gradients (dW, dbias, dgamma, dbeta) out
+    # end to end through the public API with host buffers: every step copies its X and dY in from pinned
+    # host memory and its parameter gradients (dW, dbias, dgamma, dbeta) out. The copies of step k+1 run
+    # on a second stream while step k computes (two device input buffers), as a training loop would;
+    # every step's copies are inside the timed region.
     xh = inp["x"].pin_memory()
     dyh = inp["dy"].pin_memory()
     outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (L.dw, L.db, L.dgamma, L.dbeta)]
     h2d = xh.numel() * xh.element_size() + dyh.numel() * dyh.element_size()
     d2h = sum(t.numel() * t.element_size() for t in outs)
+    xs = [x, torch.empty_like(x)]
+    dys = [dy, torch.empty_like(dy)]
+    copy_stream = torch.cuda.Stream()
 
-    def e2e_step():
-        x.copy_(xh, non_blocking=True)
-        dy.copy_(dyh, non_blocking=True)
-        L.fwd_train(x)
-        L.bwd(x, dy)
-        for o, t in zip(outs, (L.dw, L.db, L.dgamma, L.dbeta)):
-            o.copy_(t, non_blocking=True)
+    def e2e_run(n):
+        copied = [torch.cuda.Event() for _ in range(n)]
+        done = [torch.cuda.Event() for _ in range(n)]
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        copy_stream.wait_stream(stream)
+        for k in range(n):
+            b = k % 2
+            with torch.cuda.stream(copy_stream):
+                if k >= 2:
+                    copy_stream.wait_event(done[k - 2])  # buffer b is free once step k-2 is done
+                xs[b].copy_(xh, non_blocking=True)
+                dys[b].copy_(dyh, non_blocking=True)
+                copied[k].record(copy_stream)
+            stream.wait_event(copied[k])
+            L.fwd_train(xs[b])
+            L.bwd(xs[b], dys[b])
+            for o, t in zip(outs, (L.dw, L.db, L.dgamma, L.dbeta)):
+                o.copy_(t, non_blocking=True)
+            done[k].record(stream)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        return f0.elapsed_time(f1) / n
 
-    e2e_step()
-    torch.cuda.synchronize()
+    e2e_run(2)
     n_e2e = max(3, min(args.steps, 10))
     barrier()
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(n_e2e):
-        e2e_step()
-    f1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = f0.elapsed_time(f1) / n_e2e
+    e2e_ms = e2e_run(n_e2e)
 
     return dict(ms=ms, ms_instr=ms_instr, e2e_ms=e2e_ms, flops=flops, spec=spec, kern=kern, per_step=per_step,
                 clocks=ck, h2d=h2d, d2h=d2h, n_e2e=n_e2e)
@@ -472,7 +486,8 @@ def main():
         "gpu_launches": r["per_step"] * args.steps,
         "e2e": {"value": round(world * r["flops"] / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(e2e_ms, 4),
-                "what": "pinned host X, dY copied in; dW, dbias, dgamma, dbeta copied out; same ABI calls"},
+                "what": "every step: pinned host X, dY copied in, dW, dbias, dgamma, dbeta copied out, same ABI "
+                        "calls; the copies of step k+1 overlap step k (second stream, two input buffers)"},
         "clocks": r["clocks"],
         "per_config": per_cfg,
         "cpu_baseline": cpu,
