@@ -262,6 +262,45 @@ Tile conv_tile(const Geo& g, int ncols) {
   return t;
 }
 
+// CTA pairs (cta_group::2, clusters of two) for the bf16 fprop / dgrad GEMMs whose A operand comes by
+// TMA in a single phase: each CTA holds half of B's columns, so a stage is smaller (more stages), and
+// the shared-memory and TMA traffic per tile drops by a third.
+constexpr bool kUsePair = true;
+
+bool try_pair(ConvGemmParams& p, Tile& t, const Geo& g, const DevInfo* dev, long m_tiles, const void* bmat,
+              uint64_t bcols, uint64_t brows, int* grid) {
+  // an even tile count: every tile of a pair holds rows of the layer
+  if (!kUsePair || g.dt != CONV2D_BF16 || !p.a_tma || p.num_phases != 1 || t.BN % 32 != 0 || (m_tiles & 1))
+    return false;
+  const size_t stage = kBM * 128 + static_cast<size_t>(t.BN / 2) * 128;
+  const size_t stats = 11 * static_cast<size_t>(t.BN) * 4;
+  const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048 - stats) / stage));
+  const size_t smem = stages * stage + 1024 + 512 + stats;
+  static std::mutex mu;
+  static size_t cached_smem = 0;
+  static int cached_clusters = 0;
+  int clusters;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (cached_smem != smem) {
+      cached_clusters = conv_gemm_pair_clusters(smem);
+      cached_smem = smem;
+    }
+    clusters = cached_clusters;
+  }
+  if (clusters < 1) return false;
+  CUtensorMap half;
+  if (!encode_2d(&half, bmat, true, bcols, brows, g.BKE, t.BN / 2)) return false;
+  p.tmap_b = half;
+  p.pair = 1;
+  p.num_units = static_cast<int>(m_tiles / 2) * t.n_tiles;
+  p.stages = stages;
+  t.stages = stages;
+  t.smem = smem;
+  *grid = 2 * std::min(p.num_units, std::min(clusters, dev->sms / 2));
+  return true;
+}
+
 struct WgradPlan {
   int Mk, m_tiles, BN, n_tiles, KP, kb_total, kb_per_split, splits, stages, units;
   size_t smem;
@@ -464,7 +503,7 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
   std::memset(&p, 0, sizeof(p));
-  const Tile t = conv_tile(g, g.OC);
+  Tile t = conv_tile(g, g.OC);
   const bool bf = g.dt == CONV2D_BF16;
   if (!encode_2d(&p.tmap_b, bhi, bf, g.Kf, g.OC, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
   if (!bf && !encode_2d(&p.tmap_b_lo, blo, false, g.Kf, g.OC, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
@@ -523,7 +562,8 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
     rs_layout->BN = t.BN;
     rs_layout->hcols = p.a_tma ? 32 * ((t.BN / 32 + 1) / 2) : t.BN;  // the kernel's column split
   }
-  const int grid = std::min(p.num_units, dev->sms);
+  int grid = std::min(p.num_units, dev->sms);
+  if (bf) try_pair(p, t, g, dev, ceil_div(g.n_pix, kBM), bhi, g.Kf, g.OC, &grid);
   p.stats_per_cta = t.n_tiles == 1 ? 1 : 0;
   if (stats_groups) *stats_groups = p.stats_per_cta ? grid : static_cast<int>(ceil_div(g.n_pix, kBM));
   LAUNCH("fprop_gemm", st, bf ? launch_conv_gemm_bf16(p, grid, t.smem, st) : launch_conv_gemm_tf32(p, grid, t.smem, st));
@@ -609,7 +649,8 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
   p.stages = d.tile.stages;
   p.err = dev->err;
   if (bf && d.tile.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
-  const int grid = std::min(p.num_units, dev->sms);
+  int grid = std::min(p.num_units, dev->sms);
+  if (bf) try_pair(p, d.tile, g, dev, ceil_div(p.ph[0].rows, kBM), whi, d.Kd, g.ICp, &grid);
   LAUNCH("dgrad_gemm", st,
          bf ? launch_conv_gemm_bf16(p, grid, d.tile.smem, st) : launch_conv_gemm_tf32(p, grid, d.tile.smem, st));
   return CONV2D_OK;

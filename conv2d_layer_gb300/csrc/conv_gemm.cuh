@@ -89,6 +89,8 @@ struct ConvGemmParams {
   int act, out_act;       // out = out_act ? act(v) : T(v); out2 = act(T(v))
   float* stats;           // optional batch statistics (count, mean, M2) of v: [m_tile][N][3], or
   int stats_per_cta;      // [blockIdx][N][3] merged over the CTA's tiles (single column tile only)
+  int pair;               // CTA pairs (clusters of two, cta_group::2): units are pairs of m-tiles (an even
+                          // count); bf16 with A by TMA and one phase only; B tiles are BN/2 rows per CTA
   float* rstats;          // optional layer-norm partials of the stored value, one per output pixel,
                           // column tile and epilogue column half (two halves when a_tma, else one):
                           // [pixel][n_tiles][halves][2] = (mean, M2) over the half's columns
@@ -260,15 +262,21 @@ __device__ __forceinline__ void store_row32(T* dst, const float (&v)[32], int nc
 // --------------------------------------------------------------------------
 // fprop / dgrad
 // --------------------------------------------------------------------------
-template <int DT>
+// PAIR: CTA pairs (cta_group::2); bf16 with A by TMA and one phase only. A kernel may not mix
+// single-CTA and pair tcgen05 forms, hence the separate instantiation.
+template <int DT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_constant__ ConvGemmParams p) {
   using D = Dt<DT>;
   using T = typename D::T;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int BN = p.BN;
+  constexpr bool pair = PAIR;
+  static_assert(!PAIR || DT == 1, "CTA pairs run bf16 only");
   const uint32_t a_bytes = kBM * 128, b_bytes = BN * 128;
-  const uint32_t stage_bytes = D::NS * (a_bytes + b_bytes);
+  // a pair member holds its 128 rows of A and half of B's columns
+  const uint32_t b_own = pair ? b_bytes / 2 : b_bytes;
+  const uint32_t stage_bytes = D::NS * (a_bytes + b_own);
   const int S = p.stages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_bytes);
   uint64_t* empty = full + kMaxStages;
@@ -277,6 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + kMaxTmemBufs);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = pair ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;  // issues the MMAs of the pair
+  // units this CTA (pair) walks: pairs of m-tiles when paired
+  const int cid = pair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ncl = pair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   // TMEM accumulators in flight: as many BN-column buffers as fit (at least two), so that short tiles
   // (few k-blocks) keep the MMA busy while the epilogue of earlier tiles completes
   const int nbuf = 512 / BN < kMaxTmemBufs ? 512 / BN : kMaxTmemBufs;
@@ -289,7 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     }
     for (int b = 0; b < nbuf; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], p.a_tma ? 8 : 4);  // one arrival per epilogue warp
+      // one arrival per epilogue warp (of both CTAs when paired: the even CTA's MMA writes both TMEMs)
+      mbar_init(&tempty[b], (p.a_tma ? 8 : 4) * (pair ? 2 : 1));
     }
     fence_mbar_init();
     tma_prefetch_desc(&p.tmap_b);
@@ -297,11 +311,17 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     if (p.a_tma) tma_prefetch_desc(&p.tmap_a);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, tcols);
-    tmem_relinquish();
+    if (pair) {
+      tmem_alloc_pair(tmem_slot, tcols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, tcols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (pair) cluster_sync();  // the peer's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -311,13 +331,14 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       int s = 0;
       uint32_t par = 0;
       bool alive = true;
-      for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
+      for (int u = cid; u < p.num_units && alive; u += ncl) {
         const ConvPhase& ph = find_phase(p, u);
         const int local = u - ph.unit_begin;
         const int n_tile = local % p.n_tiles;
         int an = 0, ah = 0, aw = 0;  // window corner of the tile's first row (TMA im2col)
         if (p.a_tma) {
-          const int m0 = (local / p.n_tiles) * kBM;
+          const int m_tile = pair ? 2 * (local / p.n_tiles) + static_cast<int>(rank) : local / p.n_tiles;
+          const int m0 = m_tile * kBM;
           an = static_cast<int>(fdiv(static_cast<uint32_t>(m0), ph.div_HaWa));
           const int rem = m0 - an * ph.Ha * ph.Wa;
           const int a = static_cast<int>(fdiv(static_cast<uint32_t>(rem), ph.div_Wa));
@@ -331,15 +352,38 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           }
           const uint32_t a0 = sbase + s * stage_bytes;
           const uint32_t b0 = a0 + D::NS * a_bytes;
-          mbar_arrive_expect_tx(&full[s], D::NS * b_bytes + (p.a_tma ? a_bytes : 0u));
-          if (p.a_tma) {
+          if (pair) {
+            // both members' loads complete on the even CTA's full barrier, which expects them all
+            const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+            if (leader) mbar_arrive_expect_tx(&full[s], 2 * (a_bytes + b_own));
             const int tap = kb / p.a_chunks;
             const int tt = static_cast<int>(fdiv(static_cast<uint32_t>(tap), ph.div_Tw));
-            tma_load_im2col_4d(a0, &p.tmap_a, &full[s], (kb - tap * p.a_chunks) * 64, aw, ah, an,
-                               static_cast<uint16_t>(tap - tt * ph.Tw), static_cast<uint16_t>(tt));
+            tma_load_im2col_4d_pair(a0, &p.tmap_a, bar, (kb - tap * p.a_chunks) * 64, aw, ah, an,
+                                    static_cast<uint16_t>(tap - tt * ph.Tw), static_cast<uint16_t>(tt));
+            tma_load_2d_pair(b0, &p.tmap_b, bar, ph.b_col + kb * D::BKE,
+                             n_tile * BN + static_cast<int>(rank) * (BN / 2));
+          } else {
+            mbar_arrive_expect_tx(&full[s], D::NS * b_bytes + (p.a_tma ? a_bytes : 0u));
+            if (p.a_tma) {
+              const int tap = kb / p.a_chunks;
+              const int tt = static_cast<int>(fdiv(static_cast<uint32_t>(tap), ph.div_Tw));
+              tma_load_im2col_4d(a0, &p.tmap_a, &full[s], (kb - tap * p.a_chunks) * 64, aw, ah, an,
+                                 static_cast<uint16_t>(tap - tt * ph.Tw), static_cast<uint16_t>(tt));
+            }
+            tma_load_2d(b0, &p.tmap_b, &full[s], ph.b_col + kb * D::BKE, n_tile * BN);
+            if (D::NS == 2) tma_load_2d(b0 + b_bytes, &p.tmap_b_lo, &full[s], ph.b_col + kb * D::BKE, n_tile * BN);
           }
-          tma_load_2d(b0, &p.tmap_b, &full[s], ph.b_col + kb * D::BKE, n_tile * BN);
-          if (D::NS == 2) tma_load_2d(b0 + b_bytes, &p.tmap_b_lo, &full[s], ph.b_col + kb * D::BKE, n_tile * BN);
+          if (++s == S) {
+            s = 0;
+            par ^= 1;
+          }
+        }
+      }
+      if (pair) {
+        // the even CTA's commits land in this CTA's empty barriers: let every stage's last use finish
+        // before the CTA can exit
+        for (int i = 0; i < S && alive; ++i) {
+          if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) break;
           if (++s == S) {
             s = 0;
             par ^= 1;
@@ -349,13 +393,13 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f32acc(kBM, BN, D::FMT, false, false);
+    if (lane == 0 && leader) {
+      const uint32_t idesc = idesc_f32acc(pair ? 2 * kBM : kBM, BN, D::FMT, false, false);
       int s = 0;
       uint32_t par = 0;
       int tc = 0;
       bool alive = true;
-      for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x, ++tc) {
+      for (int u = cid; u < p.num_units && alive; u += ncl, ++tc) {
         const ConvPhase& ph = find_phase(p, u);
         const int buf = tc % nbuf;
         if (!wait(&tempty[buf], ((tc / nbuf) & 1) ^ 1, p.err, kSiteTEmpty)) break;
@@ -375,7 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
             const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
             const uint32_t acc = (kb | kk) ? 1u : 0u;
             if (DT == 1) {
-              mma_bf16(d, ad, bd, idesc, acc);
+              if (pair) mma_bf16_pair(d, ad, bd, idesc, acc);
+              else mma_bf16(d, ad, bd, idesc, acc);
             } else {
               const uint64_t al = sdesc_sw128(a0 + a_bytes + kk * 32, 16, 1024);
               const uint64_t bl = sdesc_sw128(b0 + b_bytes + kk * 32, 16, 1024);
@@ -384,13 +429,17 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
               mma_tf32(d, ad, bd, idesc, 1u);
             }
           }
-          mma_commit(&empty[s]);
+          if (pair) mma_commit_pair(&empty[s]);
+          else mma_commit(&empty[s]);
           if (++s == S) {
             s = 0;
             par ^= 1;
           }
         }
-        if (alive) mma_commit(&tfull[buf]);
+        if (alive) {
+          if (pair) mma_commit_pair(&tfull[buf]);
+          else mma_commit(&tfull[buf]);
+        }
       }
     }
   } else if (warp < 6 && !p.a_tma) {
@@ -550,10 +599,11 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       }
     };
     int tc = 0;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tc) {
+    for (int u = cid; u < p.num_units; u += ncl, ++tc) {
       const ConvPhase& ph = find_phase(p, u);
       const int local = u - ph.unit_begin;
-      const int m_tile = local / p.n_tiles, n_tile = local % p.n_tiles;
+      const int m_tile = pair ? 2 * (local / p.n_tiles) + static_cast<int>(rank) : local / p.n_tiles;
+      const int n_tile = local % p.n_tiles;
       const int buf = tc % nbuf;
       // lane 0 of each warp waits; the four warps agree before anyone goes on,
       // so the warp-aligned tcgen05.ld and the named barriers below stay
@@ -723,7 +773,10 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (lane == 0) {
+        if (pair && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
+        else mbar_arrive(&tempty[buf]);
+      }
     }
     if (p.stats && p.stats_per_cta) {
       for (int c = et; c < min(BN, p.N); c += nthr) {
@@ -737,9 +790,11 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
 
   tc_fence_before();
   __syncthreads();
+  if (pair) cluster_sync();  // no remote arrival or MMA write into this CTA is still in flight
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, tcols);
+    if (pair) tmem_dealloc_pair(tmem_base, tcols);
+    else tmem_dealloc(tmem_base, tcols);
   }
 }
 

@@ -5,10 +5,10 @@
 namespace c2d {
 
 cudaError_t launch_conv_gemm_tf32(const ConvGemmParams& p, int grid, size_t smem, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(conv_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(conv_gemm_kernel<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  conv_gemm_kernel<0><<<grid, kThreads, smem, st>>>(p);
+  conv_gemm_kernel<0, false><<<grid, kThreads, smem, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -8,6 +8,8 @@ namespace c2d {
 
 // tcgen05 GEMMs (gemm_bf16.cu / gemm_tf32.cu)
 cudaError_t launch_conv_gemm_bf16(const ConvGemmParams& p, int grid, size_t smem, cudaStream_t st);
+// Clusters of two CTAs of the pair form that can be resident at once (0 if the query fails).
+int conv_gemm_pair_clusters(size_t smem);
 cudaError_t launch_conv_gemm_tf32(const ConvGemmParams& p, int grid, size_t smem, cudaStream_t st);
 cudaError_t launch_wgrad_gemm_bf16(const WgradParams& p, int grid, size_t smem, cudaStream_t st);
 cudaError_t launch_wgrad_gemm_tf32(const WgradParams& p, int grid, size_t smem, cudaStream_t st);
