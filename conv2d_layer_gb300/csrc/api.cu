@@ -696,9 +696,36 @@ int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dc
   p.stages = w.stages;
   p.err = dev->err;
   if (bf && w.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
-  const int grid = std::min(p.num_units, dev->sms);
+  int grid = std::min(p.num_units, dev->sms);
+  size_t smem = w.smem;
+  // CTA pairs: two m-tiles per pair, each CTA with half of the d_conv columns
+  if (kUsePair && bf && p.a_tma && (w.m_tiles % 2) == 0 && w.BN % 128 == 0) {
+    const size_t stage = kBM * 128 + static_cast<size_t>(w.BN / 2) * 128;
+    const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048) / stage));
+    const size_t psmem = stages * stage + 1024 + 256;
+    static std::mutex mu;
+    static size_t cached_smem = 0;
+    static int cached_clusters = 0;
+    int clusters;
+    {
+      std::lock_guard<std::mutex> lk(mu);
+      if (cached_smem != psmem) {
+        cached_clusters = wgrad_gemm_pair_clusters(psmem);
+        cached_smem = psmem;
+      }
+      clusters = cached_clusters;
+    }
+    if (clusters > 0) {
+      p.pair = 1;
+      p.m_tiles = w.m_tiles / 2;
+      p.num_units = w.units / 2;
+      p.stages = stages;
+      smem = psmem;
+      grid = 2 * std::min(p.num_units, std::min(clusters, dev->sms / 2));
+    }
+  }
   LAUNCH("wgrad_gemm", st,
-         bf ? launch_wgrad_gemm_bf16(p, grid, w.smem, st) : launch_wgrad_gemm_tf32(p, grid, w.smem, st));
+         bf ? launch_wgrad_gemm_bf16(p, grid, smem, st) : launch_wgrad_gemm_tf32(p, grid, smem, st));
   LAUNCH("wgrad_reduce", st, launch_wgrad_reduce(p.partial, w.splits, g.OC, g.taps, g.ICp, g.IC, dw, st));
   return CONV2D_OK;
 }

@@ -121,6 +121,7 @@ struct WgradParams {
   int num_units;
   float* partial;         // [splits][N][Mk]
   int stages;
+  int pair;               // CTA pairs (cta_group::2, bf16 with A by TMA): m_tiles counts pairs of m-tiles
   int* err;
 };
 
@@ -802,14 +803,19 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
 // wgrad: D[k][oc] = sum over a split of the pixels of im2col(X)[pix][k] *
 // d_conv[pix][oc]; written as fp32 partials [split][oc][k].
 // --------------------------------------------------------------------------
-template <int DT>
+// PAIR: CTA pairs (cta_group::2): the pair computes 256 rows of dW (two m-tiles); each CTA holds its
+// 128 rows of A and half of the d_conv columns (BN a multiple of 128).
+template <int DT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_constant__ WgradParams p) {
   using D = Dt<DT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int BN = p.BN;
+  constexpr bool pair = PAIR;
+  static_assert(!PAIR || DT == 1, "CTA pairs run bf16 only");
   const uint32_t a_bytes = kBM * 128, b_bytes = BN * 128;
-  const uint32_t stage_bytes = D::NS * (a_bytes + b_bytes);
+  const uint32_t b_own = pair ? b_bytes / 2 : b_bytes;  // a pair member holds half of the oc columns
+  const uint32_t stage_bytes = D::NS * (a_bytes + b_own);
   const int S = p.stages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_bytes);
   uint64_t* empty = full + kMaxStages;
@@ -820,6 +826,10 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t tcols = tmem_cols_for(2 * BN);
   constexpr int KP = (DT == 1) ? 64 : 32;  // pixels per k-block
+  const uint32_t rank = pair ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int cid = pair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ncl = pair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -828,23 +838,29 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], pair ? 8 : 4);  // epilogue warps (of both CTAs when paired)
     }
     fence_mbar_init();
     if (DT == 1) tma_prefetch_desc(&p.tmap_dc);
     if (p.a_tma) tma_prefetch_desc(&p.tmap_x);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, tcols);
-    tmem_relinquish();
+    if (pair) {
+      tmem_alloc_pair(tmem_slot, tcols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, tcols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (pair) cluster_sync();  // the peer's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   auto decode = [&](int u, int& m_tile, int& n_tile, int& kb0, int& kb1) {
-    m_tile = u % p.m_tiles;
+    m_tile = pair ? 2 * (u % p.m_tiles) + static_cast<int>(rank) : u % p.m_tiles;
     const int rest = u / p.m_tiles;
     n_tile = rest % p.n_tiles;
     const int split = rest / p.n_tiles;
@@ -858,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
       int s = 0;
       uint32_t par = 0;
       bool alive = true;
-      for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
+      for (int u = cid; u < p.num_units && alive; u += ncl) {
         int m_tile, n_tile, kb0, kb1;
         decode(u, m_tile, n_tile, kb0, kb1);
         // A panels (64 k-rows each): tap offsets and channel of each panel
@@ -875,6 +891,13 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
             if (pc[j] >= 0) a_tx += 8192;
           }
         }
+        if (pair) {
+          // the even CTA's barrier expects both members' panels: add the peer's loaded panels
+          const int peer = m_tile ^ 1;
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            if (peer * kBM + 64 * j < p.Mk) a_tx += 8192;
+        }
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
             alive = false;
@@ -882,9 +905,10 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
           }
           const uint32_t a0 = sbase + s * stage_bytes;
           const uint32_t b0 = a0 + a_bytes;
-          mbar_arrive_expect_tx(&full[s], b_bytes + a_tx);
-          if (p.a_tma) {
-            const int pix = kb * KP;  // first pixel of the k-block; the map walks the next 64
+          if (pair) {
+            const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+            if (leader) mbar_arrive_expect_tx(&full[s], b_bytes + a_tx);
+            const int pix = kb * KP;
             const int n = static_cast<int>(fdiv(static_cast<uint32_t>(pix), p.div_OHOW));
             const int rem = pix - n * p.OH * p.OW;
             const int oh = static_cast<int>(fdiv(static_cast<uint32_t>(rem), p.div_OW));
@@ -892,11 +916,39 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
 #pragma unroll
             for (int j = 0; j < 2; ++j)
               if (pc[j] >= 0)
-                tma_load_im2col_4d(a0 + j * 8192, &p.tmap_x, &full[s], pc[j], ow * p.S - p.P, oh * p.S - p.P, n,
-                                   static_cast<uint16_t>(pkw[j]), static_cast<uint16_t>(pkh[j]));
+                tma_load_im2col_4d_pair(a0 + j * 8192, &p.tmap_x, bar, pc[j], ow * p.S - p.P, oh * p.S - p.P, n,
+                                        static_cast<uint16_t>(pkw[j]), static_cast<uint16_t>(pkh[j]));
+            const int nb = BN / 128;  // this member's 64-column boxes
+            for (int jn = 0; jn < nb; ++jn)
+              tma_load_2d_pair(b0 + jn * 8192, &p.tmap_dc, bar,
+                               n_tile * BN + 64 * (static_cast<int>(rank) * nb + jn), kb * KP);
+          } else {
+            mbar_arrive_expect_tx(&full[s], b_bytes + a_tx);
+            if (p.a_tma) {
+              const int pix = kb * KP;  // first pixel of the k-block; the map walks the next 64
+              const int n = static_cast<int>(fdiv(static_cast<uint32_t>(pix), p.div_OHOW));
+              const int rem = pix - n * p.OH * p.OW;
+              const int oh = static_cast<int>(fdiv(static_cast<uint32_t>(rem), p.div_OW));
+              const int ow = rem - oh * p.OW;
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+                if (pc[j] >= 0)
+                  tma_load_im2col_4d(a0 + j * 8192, &p.tmap_x, &full[s], pc[j], ow * p.S - p.P, oh * p.S - p.P, n,
+                                     static_cast<uint16_t>(pkw[j]), static_cast<uint16_t>(pkh[j]));
+            }
+            for (int jn = 0; jn < BN / 64; ++jn)
+              tma_load_2d(b0 + jn * 8192, &p.tmap_dc, &full[s], n_tile * BN + 64 * jn, kb * KP);
           }
-          for (int jn = 0; jn < BN / 64; ++jn)
-            tma_load_2d(b0 + jn * 8192, &p.tmap_dc, &full[s], n_tile * BN + 64 * jn, kb * KP);
+          if (++s == S) {
+            s = 0;
+            par ^= 1;
+          }
+        }
+      }
+      if (pair) {
+        // the even CTA's commits land in this CTA's empty barriers: let every stage's last use finish
+        for (int i = 0; i < S && alive; ++i) {
+          if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) break;
           if (++s == S) {
             s = 0;
             par ^= 1;
@@ -906,13 +958,13 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f32acc(kBM, BN, D::FMT, DT == 1, DT == 1);
+    if (lane == 0 && leader) {
+      const uint32_t idesc = idesc_f32acc(pair ? 2 * kBM : kBM, BN, D::FMT, DT == 1, DT == 1);
       int s = 0;
       uint32_t par = 0;
       int tc = 0;
       bool alive = true;
-      for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x, ++tc) {
+      for (int u = cid; u < p.num_units && alive; u += ncl, ++tc) {
         int m_tile, n_tile, kb0, kb1;
         decode(u, m_tile, n_tile, kb0, kb1);
         const int buf = tc & 1;
@@ -934,7 +986,8 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
               // MN-major: 16 pixel rows per MMA (2048 B), atoms of 64 k / 64 oc 8192 B apart
               const uint64_t ad = sdesc_sw128(a0 + kk * 2048, 8192, 1024);
               const uint64_t bd = sdesc_sw128(b0 + kk * 2048, 8192, 1024);
-              mma_bf16(d, ad, bd, idesc, acc);
+              if (pair) mma_bf16_pair(d, ad, bd, idesc, acc);
+              else mma_bf16(d, ad, bd, idesc, acc);
             } else {
               const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
               const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
@@ -945,13 +998,17 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
               mma_tf32(d, ad, bd, idesc, 1u);
             }
           }
-          mma_commit(&empty[s]);
+          if (pair) mma_commit_pair(&empty[s]);
+          else mma_commit(&empty[s]);
           if (++s == S) {
             s = 0;
             par ^= 1;
           }
         }
-        if (alive) mma_commit(&tfull[buf]);
+        if (alive) {
+          if (pair) mma_commit_pair(&tfull[buf]);
+          else mma_commit(&tfull[buf]);
+        }
       }
     }
   } else if (warp < 6) {
@@ -1120,7 +1177,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
     const int q = warp & 3;
     const int row = q * 32 + lane;
     int tc = 0;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tc) {
+    for (int u = cid; u < p.num_units; u += ncl, ++tc) {
       int m_tile, n_tile, kb0, kb1;
       decode(u, m_tile, n_tile, kb0, kb1);
       const int split = u / (p.m_tiles * p.n_tiles);
@@ -1152,15 +1209,20 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (lane == 0) {
+        if (pair && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[buf]), 0));
+        else mbar_arrive(&tempty[buf]);
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (pair) cluster_sync();  // no remote arrival or MMA write into this CTA is still in flight
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, tcols);
+    if (pair) tmem_dealloc_pair(tmem_base, tcols);
+    else tmem_dealloc(tmem_base, tcols);
   }
 }
 

@@ -51,12 +51,47 @@ int conv_gemm_pair_clusters(size_t smem) {
   return n;
 }
 
+// Launch configuration of a kernel run in clusters of two CTAs.
+static cudaLaunchConfig_t pair_config(int grid, size_t smem, cudaStream_t st, cudaLaunchAttribute* at) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 cudaError_t launch_wgrad_gemm_bf16(const WgradParams& p, int grid, size_t smem, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(wgrad_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (!p.pair) {
+    cudaError_t e = cudaFuncSetAttribute(wgrad_gemm_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    wgrad_gemm_kernel<1, false><<<grid, kThreads, smem, st>>>(p);
+    return cudaGetLastError();
+  }
+  cudaError_t e = cudaFuncSetAttribute(wgrad_gemm_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  wgrad_gemm_kernel<1><<<grid, kThreads, smem, st>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute at[1];
+  const cudaLaunchConfig_t cfg = pair_config(grid, smem, st, at);
+  return cudaLaunchKernelEx(&cfg, wgrad_gemm_kernel<1, true>, p);
+}
+
+int wgrad_gemm_pair_clusters(size_t smem) {
+  if (cudaFuncSetAttribute(wgrad_gemm_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  cudaLaunchAttribute at[1];
+  const cudaLaunchConfig_t cfg = pair_config(2, smem, nullptr, at);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, wgrad_gemm_kernel<1, true>, &cfg) != cudaSuccess) return 0;
+  return n;
 }
 
 }  // namespace c2d

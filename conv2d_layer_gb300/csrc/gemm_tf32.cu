@@ -13,10 +13,10 @@ cudaError_t launch_conv_gemm_tf32(const ConvGemmParams& p, int grid, size_t smem
 }
 
 cudaError_t launch_wgrad_gemm_tf32(const WgradParams& p, int grid, size_t smem, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(wgrad_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(wgrad_gemm_kernel<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  wgrad_gemm_kernel<0><<<grid, kThreads, smem, st>>>(p);
+  wgrad_gemm_kernel<0, false><<<grid, kThreads, smem, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -12,6 +12,7 @@ cudaError_t launch_conv_gemm_bf16(const ConvGemmParams& p, int grid, size_t smem
 int conv_gemm_pair_clusters(size_t smem);
 cudaError_t launch_conv_gemm_tf32(const ConvGemmParams& p, int grid, size_t smem, cudaStream_t st);
 cudaError_t launch_wgrad_gemm_bf16(const WgradParams& p, int grid, size_t smem, cudaStream_t st);
+int wgrad_gemm_pair_clusters(size_t smem);
 cudaError_t launch_wgrad_gemm_tf32(const WgradParams& p, int grid, size_t smem, cudaStream_t st);
 
 // Per-phase description of the dgrad weight matrix (see prep_dgrad_weights).
