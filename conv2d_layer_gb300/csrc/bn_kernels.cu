@@ -1033,7 +1033,7 @@ __global__ void __launch_bounds__(kBlock, 1) norm_stats_stream(const T* __restri
 
 // part[b][c] = {sum d_norm, sum d_norm * z}
 template <typename T, int EC>
-__global__ void __launch_bounds__(kBlock, 1) bn_bwd_reduce_stream(const T* __restrict__ pre, const T* __restrict__ dy,
+__global__ void __launch_bounds__(kBlock, 3) bn_bwd_reduce_stream(const T* __restrict__ pre, const T* __restrict__ dy,
                                                                   long seg_rows, int bps, int C, long rpb, int R,
                                                                   int cpg, int rev, const float* __restrict__ mean,
                                                                   const float* __restrict__ inv_std,
@@ -1290,6 +1290,23 @@ cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float
       KERNEL<<<wk.G, kBlock, smem, st>>>(__VA_ARGS__);                                                  \
     }                                                                                                   \
   } while (0)
+// The same with an explicit walk (a different chunk size).
+#define STREAM_LAUNCH_W(WK, dtype, NIN, KERNEL, ...)                                                           \
+  do {                                                                                                  \
+    const size_t es = (dtype) == 1 ? 2 : 4;                                                             \
+    const size_t smem = static_cast<size_t>(kStreamStages) * (NIN) * WK.R * WK.C * es;                  \
+    if ((dtype) == 1) {                                                                                 \
+      constexpr int EC = 8;                                                                             \
+      using T = __nv_bfloat16;                                                                          \
+      cudaFuncSetAttribute(KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
+      KERNEL<<<WK.G, kBlock, smem, st>>>(__VA_ARGS__);                                                  \
+    } else {                                                                                            \
+      constexpr int EC = 4;                                                                             \
+      using T = float;                                                                                  \
+      cudaFuncSetAttribute(KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
+      KERNEL<<<WK.G, kBlock, smem, st>>>(__VA_ARGS__);                                                  \
+    }                                                                                                   \
+  } while (0)
 
 // Walk arguments shared by every row-walk kernel: segment geometry and the layer-norm flag.
 #define WALK_ARGS wk.seg_rows, wk.bps, wk.C, wk.rows_per_block
@@ -1317,8 +1334,13 @@ cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, con
                                  const float* inv_std, const float* gamma, const float* beta, int act, float* part,
                                  cudaStream_t st) {
   if (wk.stream) {
-    STREAM_LAUNCH(dtype, 2, (bn_bwd_reduce_stream<T, EC>), static_cast<const T*>(pre), static_cast<const T*>(dy),
-                  WALK_ARGS, wk.R, LN_FLAG, 0, mean, inv_std, gamma, beta, act, part, wk.err);
+    // three blocks per SM (registers capped for it): chunks of three quarters of the walk's size so that
+    // three rings fit in shared memory; the rows each block walks are unchanged
+    RowWalk w3 = wk;
+    w3.R = std::max(1, wk.R * 3 / 4);
+    STREAM_LAUNCH_W(w3, dtype, 2, (bn_bwd_reduce_stream<T, EC>), static_cast<const T*>(pre),
+                    static_cast<const T*>(dy), WALK_ARGS, w3.R, LN_FLAG, 0, mean, inv_std, gamma, beta, act, part,
+                    wk.err);
     return cudaGetLastError();
   }
   DISPATCH_EC(dtype, wk.C,
