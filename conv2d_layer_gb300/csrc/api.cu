@@ -249,17 +249,37 @@ struct Tile {
   size_t smem;
 };
 
-Tile conv_tile(const Geo& g, int ncols) {
+// fp32 (3xTF32): the tensor core's fp32 accumulation loses a little on every MMA step (12 per k-block),
+// and the loss grows with the steps that feed one accumulator, so a deep K loop accumulates in chunks of
+// at most kFp32ChunkKb k-blocks (768 elements), each in its own TMEM columns, summed by the epilogue.
+constexpr int kFp32ChunkKb = 24;
+
+int fp32_chunks(long kdepth) { return static_cast<int>(std::max<long>(1, ceil_div(ceil_div(kdepth, 32), kFp32ChunkKb))); }
+
+// kdepth: the longest K loop of a tile (elements); it bounds the column tile of fp32 GEMMs so that
+// its accumulator chunks fit the 512 TMEM columns.
+Tile conv_tile(const Geo& g, int ncols, long kdepth) {
   Tile t;
-  const int bn_max = g.dt == CONV2D_BF16 ? 256 : 128;
+  int bn_max = g.dt == CONV2D_BF16 ? 256 : 128;
+  if (g.dt != CONV2D_BF16) bn_max = std::max(32, std::min(bn_max, 512 / fp32_chunks(kdepth) / 32 * 32));
   t.n_tiles = static_cast<int>(ceil_div(ncols, bn_max));
   t.BN = static_cast<int>(round_up(ceil_div(ncols, t.n_tiles), 32));  // the epilogue reads 32 columns at a time
   const size_t ns = g.dt == CONV2D_BF16 ? 1 : 2;
   const size_t stage = ns * (kBM * 128 + static_cast<size_t>(t.BN) * 128);
-  const size_t stats = 11 * static_cast<size_t>(t.BN) * 4;  // epilogue statistics scratch + column constants
+  const size_t stats = 12 * static_cast<size_t>(t.BN) * 4;  // epilogue statistics scratch + column constants
   t.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048 - stats) / stage));
   t.smem = t.stages * stage + 1024 + 512 + stats;  // alignment slack, barriers + TMEM slot, epilogue scratch
   return t;
+}
+
+// Accumulator chunks of an fp32 GEMM whose longest tile K loop has max_kb k-blocks (see kFp32ChunkKb).
+void set_chunks(ConvGemmParams& p, const Geo& g, int BN, int max_kb) {
+  p.nch = 1;
+  p.kpc = std::max(max_kb, 1);
+  if (g.dt == CONV2D_BF16) return;
+  p.nch = std::min(fp32_chunks(static_cast<long>(max_kb) * 32), 512 / BN);
+  p.kpc = static_cast<int>(ceil_div(std::max(max_kb, 1), p.nch));
+  p.nch = static_cast<int>(ceil_div(std::max(max_kb, 1), p.kpc));
 }
 
 // CTA pairs (cta_group::2, clusters of two) for the bf16 fprop / dgrad GEMMs whose A operand comes by
@@ -273,7 +293,7 @@ bool try_pair(ConvGemmParams& p, Tile& t, const Geo& g, const DevInfo* dev, long
   if (!kUsePair || g.dt != CONV2D_BF16 || !p.a_tma || p.num_phases != 1 || t.BN % 32 != 0 || (m_tiles & 1))
     return false;
   const size_t stage = kBM * 128 + static_cast<size_t>(t.BN / 2) * 128;
-  const size_t stats = 11 * static_cast<size_t>(t.BN) * 4;
+  const size_t stats = 12 * static_cast<size_t>(t.BN) * 4;
   const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048 - stats) / stage));
   const size_t smem = stages * stage + 1024 + 512 + stats;
   static std::mutex mu;
@@ -371,7 +391,7 @@ bool dgrad_tma(const Geo& g) { return g.dt == CONV2D_BF16 && g.S == 1 && g.OCp %
 DgradPlan dgrad_plan(const Geo& g) {
   DgradPlan d;
   std::memset(&d, 0, sizeof(d));
-  d.tile = conv_tile(g, g.IC);
+  d.tile = conv_tile(g, g.IC, static_cast<long>(g.taps) * g.OCp);
   d.table.flip = dgrad_tma(g) ? 1 : 0;
   const int S = g.S;
   int unit = 0, col = 0, n = 0;
@@ -449,7 +469,7 @@ void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
     if (op == CONV2D_OP_FWD_TRAIN && g.norm == CONV2D_NORM_BATCH)
       sz[R_PART] = static_cast<size_t>(ceil_div(g.n_pix, kBM)) * g.OC * 3 * 4;  // per-tile statistics
     if (ln)  // per-pixel, per-column-tile, per-half (mean, M2) of the stored conv output
-      sz[R_PART] = static_cast<size_t>(g.n_pix) * conv_tile(g, g.OC).n_tiles * 2 * 2 * 4;
+      sz[R_PART] = static_cast<size_t>(g.n_pix) * conv_tile(g, g.OC, g.Kf).n_tiles * 2 * 2 * 4;
     if (gn)  // per-block, per-channel (rows, mean, M2) of the stored conv output
       sz[R_PART] = G * g.OC * 3 * 4;
     if (op == CONV2D_OP_FWD_INFER) {
@@ -503,7 +523,7 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
   std::memset(&p, 0, sizeof(p));
-  Tile t = conv_tile(g, g.OC);
+  Tile t = conv_tile(g, g.OC, g.Kf);
   const bool bf = g.dt == CONV2D_BF16;
   if (!encode_2d(&p.tmap_b, bhi, bf, g.Kf, g.OC, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
   if (!bf && !encode_2d(&p.tmap_b_lo, blo, false, g.Kf, g.OC, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
@@ -555,6 +575,7 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   }
   p.stages = t.stages;
   p.err = dev->err;
+  set_chunks(p, g, t.BN, ph.num_kb);
   if (bf && t.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
   if (rs_layout) {
     rs_layout->n_tiles = t.n_tiles;
@@ -648,6 +669,11 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
   }
   p.stages = d.tile.stages;
   p.err = dev->err;
+  {
+    int max_kb = 0;
+    for (int i = 0; i < d.num_phases; ++i) max_kb = std::max(max_kb, d.ph[i].num_kb);
+    set_chunks(p, g, d.tile.BN, max_kb);
+  }
   if (bf && d.tile.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
   int grid = std::min(p.num_units, dev->sms);
   if (bf) try_pair(p, d.tile, g, dev, ceil_div(p.ph[0].rows, kBM), whi, d.Kd, g.ICp, &grid);

@@ -103,6 +103,9 @@ struct ConvGemmParams {
   int a_chunks;           // Cs / 64
   int a_qh, a_qw;         // window corner of row (a, b): (a*rs + a_qh, b*rs + a_qw)
   int stages;
+  // fp32 (3xTF32) only: the K loop of a tile accumulates in nch chunks of kpc k-blocks, each in its own
+  // BN TMEM columns, summed by the epilogue (nch * BN <= 512); bf16 uses one chunk
+  int kpc, nch;
   int* err;
   ConvPhase ph[kMaxPhases];
 };
@@ -180,7 +183,9 @@ __device__ __forceinline__ void ep_columns(const uint32_t (&r)[32], bool zero, b
   }
 }
 
-// x[0] of lane L is the sum over all 32 lanes of column colsum16_col(L).
+// One level of a transposed butterfly over lane bit O: the pairs (x[e], x[e + W/2]) are
+// exchanged with lane L ^ O, lanes with bit O set keep (and add up) the upper half,
+// the others the lower half; afterwards x[0 .. W/2) holds the kept sums.
 template <int W, int O>
 __device__ __forceinline__ void colsum_step(float (&x)[16], int lane) {
   const bool up = (lane & O) != 0;
@@ -191,15 +196,87 @@ __device__ __forceinline__ void colsum_step(float (&x)[16], int lane) {
     x[e] = keep + __shfl_xor_sync(0xffffffffu, send, O);
   }
 }
-__device__ __forceinline__ void colsum16(float (&x)[16], int lane) {
-  colsum_step<16, 16>(x, lane);
-  colsum_step<8, 8>(x, lane);
-  colsum_step<4, 4>(x, lane);
-  colsum_step<2, 2>(x, lane);
-  x[0] += __shfl_xor_sync(0xffffffffu, x[0], 1);
+
+__device__ __forceinline__ float2 f2(uint32_t a, uint32_t b) { return make_float2(__uint_as_float(a), __uint_as_float(b)); }
+
+// Column sums of d and of d*d over the 32 rows of this warp's TMEM lane quarter, for the 32
+// accumulator columns at taddr, with d = acc * a + k per column (a = null: d = acc + k; k is
+// the epilogue shift minus the statistics shift; both 8-byte aligned, indexed from the
+// chunk's first column). Two 16-lane loads give thread t rows t/4 + {0, 8, 16, 24} of the
+// column pairs 8j + 2(t%4) + {0, 1}: the four rows are added in the thread with packed
+// f32x2 arithmetic (one load at a time), then a transposed butterfly over lane bits 4, 3, 2 leaves each lane one
+// column pair of one statistic. rowmask bit i clears row t/4 + 8i (rows past the tile's
+// end); zero: the accumulator was never written (read as 0). Writes sum(d) to s1[0..31]
+// and sum(d*d) to s2[0..31]. Warp-collective. Kept out of line: inlined into both
+// statistics passes it pushed the epilogue past the register budget of the 320-thread CTA.
+static __device__ __noinline__ void colstats32(uint32_t taddr, bool zero, const float* a, const float* k, unsigned rowmask,
+                                           int lane, float* s1, float* s2) {
+  const int cp = 2 * (lane & 3);
+  float x[16];  // x[2j + kk]: sum over the four rows of column 8j + cp + kk; x[8 + 2j + kk]: sum of squares
+#pragma unroll
+  for (int e = 0; e < 16; ++e) x[e] = 0.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {  // lanes 0-15, then 16-31 of the quarter
+    uint32_t r[16];
+    if (zero) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) r[e] = 0u;
+    } else {
+      tmem_ld16x256(taddr + (static_cast<uint32_t>(16 * h) << 16), r);
+      tmem_ld_wait(r);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 kv = *reinterpret_cast<const float2*>(k + 8 * j + cp);
+      float2 d0 = f2(r[4 * j], r[4 * j + 1]), d1 = f2(r[4 * j + 2], r[4 * j + 3]);
+      if (a) {
+        const float2 av = *reinterpret_cast<const float2*>(a + 8 * j + cp);
+        d0 = __ffma2_rn(d0, av, kv);
+        d1 = __ffma2_rn(d1, av, kv);
+      } else {
+        d0 = __fadd2_rn(d0, kv);
+        d1 = __fadd2_rn(d1, kv);
+      }
+      if (rowmask != 0u) {
+        if ((rowmask >> (2 * h)) & 1u) d0 = make_float2(0.f, 0.f);
+        if ((rowmask >> (2 * h + 1)) & 1u) d1 = make_float2(0.f, 0.f);
+      }
+      float2 sv = make_float2(x[2 * j], x[2 * j + 1]), sq = make_float2(x[8 + 2 * j], x[8 + 2 * j + 1]);
+      sv = __fadd2_rn(sv, __fadd2_rn(d0, d1));
+      sq = __ffma2_rn(d0, d0, sq);
+      sq = __ffma2_rn(d1, d1, sq);
+      x[2 * j] = sv.x;
+      x[2 * j + 1] = sv.y;
+      x[8 + 2 * j] = sq.x;
+      x[8 + 2 * j + 1] = sq.y;
+    }
+  }
+  colsum_step<16, 16>(x, lane);  // lanes with bit 4 set keep the squares
+  colsum_step<8, 8>(x, lane);    // bit 3: column groups j = 2, 3 (else 0, 1)
+  colsum_step<4, 4>(x, lane);    // bit 2: the odd group of the two
+  const int j = 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+  float* dst = (lane & 16) ? s2 : s1;
+  *reinterpret_cast<float2*>(dst + 8 * j + cp) = make_float2(x[0], x[1]);
 }
-__device__ __forceinline__ int colsum16_col(int lane) {
-  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+
+// Sum the accumulator chunks 1 .. n-1 of a tile into chunk 0, in fp32 round-to-nearest: columns
+// [c0, c1) (multiples of 16) of this warp's lane quarter, chunk i starting i * stride columns after
+// taddr. The tensor core's fp32 accumulation loses a little on every MMA step; a deep K loop split
+// over chunks keeps that loss to the steps of one chunk. Warp-collective.
+static __device__ __noinline__ void fold_chunks(uint32_t taddr, int stride, int n, int c0, int c1) {
+  for (int c = c0; c < c1; c += 16) {
+    uint32_t a[16], b[16];
+    tmem_ld16(taddr + c, a);
+    tmem_ld_wait(a);
+    for (int i = 1; i < n; ++i) {
+      tmem_ld16(taddr + static_cast<uint32_t>(i * stride + c), b);
+      tmem_ld_wait(b);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) a[e] = __float_as_uint(__uint_as_float(a[e]) + __uint_as_float(b[e]));
+    }
+    tmem_st16(taddr + c, a);
+  }
+  tmem_st_wait();
 }
 
 template <typename T>
@@ -293,8 +370,12 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
   const int ncl = pair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   // TMEM accumulators in flight: as many BN-column buffers as fit (at least two), so that short tiles
   // (few k-blocks) keep the MMA busy while the epilogue of earlier tiles completes
-  const int nbuf = 512 / BN < kMaxTmemBufs ? 512 / BN : kMaxTmemBufs;
-  const uint32_t tcols = tmem_cols_for(nbuf * BN);
+  // fp32: nch accumulator chunks of BN columns per tile (see ConvGemmParams::kpc)
+  const int nch = DT == 0 && p.nch > 1 ? p.nch : 1;
+  const int kpc = DT == 0 && p.nch > 1 ? p.kpc : (1 << 30);
+  const int tcs = nch * BN;  // TMEM columns of one tile
+  const int nbuf = 512 / tcs < kMaxTmemBufs ? 512 / tcs : kMaxTmemBufs;
+  const uint32_t tcols = tmem_cols_for(nbuf * tcs);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -405,8 +486,10 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         const int buf = tc % nbuf;
         if (!wait(&tempty[buf], ((tc / nbuf) & 1) ^ 1, p.err, kSiteTEmpty)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + buf * BN;
+        const uint32_t dt = tmem_base + buf * tcs;
         for (int kb = 0; kb < ph.num_kb; ++kb) {
+          const uint32_t d = DT == 0 ? dt + static_cast<uint32_t>((kb / kpc) * BN) : dt;
+          const int kc = DT == 0 ? kb % kpc : kb;  // k-block within the accumulator chunk
           if (!wait(&full[s], par, p.err, kSiteFull)) {
             alive = false;
             break;
@@ -418,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           for (int kk = 0; kk < 128 / 32; ++kk) {
             const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
-            const uint32_t acc = (kb | kk) ? 1u : 0u;
+            const uint32_t acc = (kc | kk) ? 1u : 0u;
             if (DT == 1) {
               if (pair) mma_bf16_pair(d, ad, bd, idesc, acc);
               else mma_bf16(d, ad, bd, idesc, acc);
@@ -567,13 +650,15 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     T* out = static_cast<T*>(p.out);
     T* out2 = static_cast<T*>(p.out2);
     const bool vec = (p.out_ld % D::EC) == 0;
-    // batch-statistics scratch: per-warp column sums (two passes) and tile means
+    // batch-statistics scratch: per-warp column sums and squares, tile means
     float* red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16);
     float* red2 = red + 4 * BN;
     float* tmean = red2 + 4 * BN;
     // per-column epilogue constants of the current column tile
     float* sc_s = tmean + BN;
     float* sh_s = sc_s + BN;
+    // per-column shift of the statistics pass: epilogue shift minus the statistics shift
+    float* kst = sh_s + BN;
     int cur_n_tile = -1;
     // After the first tile, tmean holds the previous tile's column means and
     // serves as the shift of a single-pass (shifted sums) statistic.
@@ -639,8 +724,9 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       // across the chunks with Chan's formula (the chunks before column cc hold cc - cb values)
       float rmean = 0.f, rm2 = 0.f;
       const bool zero = ph.num_kb == 0;
-      const bool one_pass = p.stats && have_shift;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * tcs;
+      if (DT == 0 && ph.num_kb > kpc)  // several accumulator chunks: summed into the first
+        fold_chunks(taddr, BN, (ph.num_kb + kpc - 1) / kpc, cb, ce);
       // columns are read from TMEM 64 at a time (two 32-column loads, one wait)
       auto fetch = [&](int c0, uint32_t (&ra)[32], uint32_t (&rb)[32]) {
         const int c1 = c0 + 32 < ce ? c0 + 32 : c0;
@@ -656,26 +742,6 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         // already use most of the shared-memory bandwidth)
         float v[32];
         ep_columns(r, zero, p.ep_scale != nullptr, sc_s + cc, sh_s + cc, v);
-        if (p.stats) {  // statistics of the unrounded value
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float sv[16], sq[16], sh[16];
-            if (one_pass) lds16(tmean + cc + h * 16, sh);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const bool in = valid && h * 16 + e < ncols;
-              const float d = one_pass ? v[h * 16 + e] - sh[e] : v[h * 16 + e];
-              sv[e] = in ? d : 0.f;
-              sq[e] = sv[e] * sv[e];
-            }
-            colsum16(sv, lane);
-            if ((lane & 1) == 0) red[q * BN + cc + h * 16 + colsum16_col(lane)] = sv[0];
-            if (one_pass) {
-              colsum16(sq, lane);
-              if ((lane & 1) == 0) red2[q * BN + cc + h * 16 + colsum16_col(lane)] = sq[0];
-            }
-          }
-        }
         if (valid) {
           float o[32];
 #pragma unroll
@@ -716,61 +782,49 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         o[0] = rmean;
         o[1] = rm2;
       }
-      if (one_pass) {
-        // shifted sums d = v - s with s the previous tile's mean:
-        // mean = s + sum(d)/n, M2 = sum(d^2) - sum(d)^2/n
+      if (p.stats) {
+        // Statistics of the unrounded value v, from a second read of the accumulator
+        // (colstats32): shifted sums d = v - s give mean = s + sum(d)/n and
+        // M2 = sum(d^2) - sum(d)^2/n. After the first tile s is the previous tile's
+        // column mean; the first tile takes its own mean from a plain pass first.
         const int cnt = min(kBM, ph.rows - m_tile * kBM);
         const int cols = min(BN, p.N - n_tile * BN);
         const float fc = static_cast<float>(cnt);
-        named_bar_sync(1, nthr);
+        const int qrows = cnt - q * 32;  // valid rows of this warp's lane quarter
+        unsigned rowmask = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rowmask |= ((lane >> 2) + 8 * i >= qrows ? 1u : 0u) << i;
+        const float* av = p.ep_scale ? sc_s : nullptr;
+        const uint32_t tq = taddr;
+        // pass 0 (first tile only): plain sums for the tile's own mean; pass 1: shifted sums
+#pragma unroll 1
+        for (int pass = have_shift ? 1 : 0; pass < 2; ++pass) {
+          const float* kc = pass ? kst : sh_s;
+          for (int cc = cb; cc < ce && cc < cols; cc += 32)
+            colstats32(tq + cc, zero, av ? av + cc : nullptr, kc + cc, rowmask, lane, red + q * BN + cc,
+                       red2 + q * BN + cc);
+          named_bar_sync(1, nthr);
+          if (pass == 0) {
+            for (int c = et; c < BN; c += nthr) {
+              const float m = c < cols ? (red[c] + red[BN + c] + red[2 * BN + c] + red[3 * BN + c]) / fc : 0.f;
+              tmean[c] = m;
+              kst[c] = sh_s[c] - m;
+            }
+            named_bar_sync(1, nthr);
+          }
+        }
         for (int c = et; c < cols; c += nthr) {
           const float s1 = red[c] + red[BN + c] + red[2 * BN + c] + red[3 * BN + c];
           const float s2 = red2[c] + red2[BN + c] + red2[2 * BN + c] + red2[3 * BN + c];
           const float mean = tmean[c] + s1 / fc;
           emit(m_tile, n_tile, c, fc, mean, fmaxf(s2 - s1 * (s1 / fc), 0.f));
-          tmean[c] = mean;  // next tile's shift (read after the next unit's barrier)
+          // the next tile's shift (read after the next unit's barrier; used when the
+          // column tile stays the same)
+          tmean[c] = mean;
+          kst[c] = sh_s[c] - mean;
         }
         cta_n += fc;
-      } else if (p.stats) {
-        // first tile: two passes, mean from the column sums, then the sum of
-        // squared deviations from that mean (TMEM is read a second time)
-        const int cnt = min(kBM, ph.rows - m_tile * kBM);
-        const int cols = min(BN, p.N - n_tile * BN);
-        named_bar_sync(1, nthr);
-        for (int c = et; c < cols; c += nthr)
-          tmean[c] = (red[c] + red[BN + c] + red[2 * BN + c] + red[3 * BN + c]) / static_cast<float>(cnt);
-        named_bar_sync(1, nthr);
-        auto pass2 = [&](int cc, const uint32_t (&r)[32]) {
-          if (cc >= cols) return;  // uniform
-#pragma unroll
-          float x[32];
-          ep_columns(r, zero, p.ep_scale != nullptr, sc_s + cc, sh_s + cc, x);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float sv[16], mu[16];
-            lds16(tmean + cc + h * 16, mu);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int c = cc + h * 16 + e;
-              const float d = (valid && c < cols) ? x[h * 16 + e] - mu[e] : 0.f;
-              sv[e] = d * d;
-            }
-            colsum16(sv, lane);
-            if ((lane & 1) == 0) red2[q * BN + cc + h * 16 + colsum16_col(lane)] = sv[0];
-          }
-        };
-        for (int c0 = cb; c0 < ce && c0 < cols; c0 += 64) {
-          uint32_t ra[32], rb[32];
-          fetch(c0, ra, rb);
-          pass2(c0, ra);
-          if (c0 + 32 < ce) pass2(c0 + 32, rb);
-        }
-        named_bar_sync(1, nthr);
-        for (int c = et; c < cols; c += nthr)
-          emit(m_tile, n_tile, c, static_cast<float>(cnt), tmean[c],
-               red2[c] + red2[BN + c] + red2[2 * BN + c] + red2[3 * BN + c]);
-        cta_n += static_cast<float>(cnt);
-        have_shift = p.n_tiles == 1;  // tmean now holds this tile's means
+        have_shift = p.n_tiles == 1;
       }
       tc_fence_before();
       __syncwarp();

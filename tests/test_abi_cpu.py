@@ -117,3 +117,45 @@ def test_status_strings():
     for s in range(6):
         assert abi.status_str(s)
     assert abi.status_str(99) == "unknown status"
+
+
+def test_layer_binding_rejects_mismatched_tensors_before_launch():
+    """The C ABI trusts buffer sizes; Conv2dLayer checks every caller tensor first.
+
+    A d_y drawn for a different layer (e.g. the last layer of a stack handed to
+    the first) must raise, not reach a kernel that would read past its end."""
+    import torch
+    from conv2d_layer_gb300.layer import Conv2dLayer
+    from conv2d_layer_gb300.workloads import LayerSpec
+    spec = LayerSpec(N=2, H=8, W=8, IC=16, OC=32, KH=1, KW=1, stride=1, pad=0, norm=abi.NORM_BATCH,
+                     act=abi.ACT_RELU, dtype=abi.BF16)
+    L = Conv2dLayer(spec, torch.randn(32, 1, 1, 16), device="cpu")
+    bf = torch.bfloat16
+    good_x = torch.zeros(2, 8, 8, 16, dtype=bf)
+    cases = [
+        (lambda: L.fwd_train(torch.zeros(2, 8, 8, 8, dtype=bf)), "x: shape"),
+        (lambda: L.fwd_train(good_x.float()), "x: dtype"),
+        (lambda: L.fwd_train(torch.zeros(2, 16, 8, 8, dtype=bf).permute(0, 2, 3, 1)), "x: must be contiguous"),
+        (lambda: L.fwd_train(good_x), "x: must be in CUDA device memory"),
+        (lambda: L.fwd_train(None), "torch.Tensor"),
+        (lambda: L.fwd_infer(good_x, y=torch.zeros(2, 8, 8, 16, dtype=bf)), "x: must be in CUDA"),
+        (lambda: L.bwd(torch.zeros(1, 8, 8, 16, dtype=bf), torch.zeros(2, 8, 8, 32, dtype=bf)), "x: shape"),
+    ]
+    for call, msg in cases:
+        with pytest.raises(ValueError, match=msg):
+            call()
+
+
+def test_layer_binding_tensor_check_rules():
+    import torch
+    from conv2d_layer_gb300.layer import _expect
+    bf = torch.bfloat16
+    # d_y of the last layer of the mixed stack (28x28) offered to its first layer (56x56)
+    with pytest.raises(ValueError, match="dy: shape"):
+        _expect(torch.zeros(2, 28, 28, 256, dtype=bf), "dy", (2, 56, 56, 256), bf)
+    with pytest.raises(ValueError, match="y: shape"):
+        _expect(torch.zeros(2, 8, 8, 15, dtype=bf), "y", (2, 8, 8, 16), bf)
+    with pytest.raises(ValueError, match="CUDA"):
+        _expect(torch.zeros(2, 3), "x", (2, 3), torch.float32)
+    with pytest.raises(ValueError, match="torch.Tensor"):
+        _expect(3, "x", (2, 3), torch.float32)

@@ -63,6 +63,17 @@ EDGE_CASES = {
                                     act=ACT_TANH, dtype=BF16),
     "bf16_k1x5_s2_tma": LayerSpec(N=2, H=9, W=16, IC=128, OC=96, KH=1, KW=5, stride=2, pad=2, norm=NORM_NONE,
                                   act=ACT_RELU, dtype=BF16),
+    # batch statistics over two column tiles (every tile takes its own mean first) with a last
+    # row tile of 19 pixels (three of four TMEM lane quarters empty, one partly filled)
+    "bf16_oc320_1x1_bn_ragged": LayerSpec(N=3, H=7, W=7, IC=64, OC=320, KH=1, KW=1, stride=1, pad=0,
+                                          norm=NORM_BATCH, act=ACT_RELU, dtype=BF16),
+    "fp32_oc288_k3_bn_ragged": LayerSpec(N=2, H=10, W=9, IC=8, OC=288, KH=3, KW=3, stride=1, pad=1,
+                                         norm=NORM_BATCH, act=ACT_IDENTITY, dtype=FP32),
+    # deep fp32 K loops: the accumulation is split over TMEM chunks (dgrad K = 5184, fprop K = 2304)
+    "fp32_deep_dgrad_oc576": LayerSpec(N=2, H=10, W=9, IC=8, OC=576, KH=3, KW=3, stride=1, pad=1,
+                                       norm=NORM_BATCH, act=ACT_IDENTITY, dtype=FP32),
+    "fp32_deep_fprop_ic256": LayerSpec(N=2, H=9, W=9, IC=256, OC=40, KH=3, KW=3, stride=1, pad=1,
+                                       norm=NORM_NONE, act=ACT_RELU, dtype=FP32),
 }
 
 
