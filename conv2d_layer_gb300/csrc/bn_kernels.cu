@@ -852,6 +852,16 @@ __device__ __forceinline__ void lds_v(const __nv_bfloat16* p, float (&v)[EC]) {
   }
 }
 
+// Elements e, e+1 of a per-thread channel group as one packed pair (f32x2 arithmetic below: the
+// same operations as per element, two per instruction).
+__device__ __forceinline__ float2 pr(const float* v, int e) { return make_float2(v[e], v[e + 1]); }
+// act'(t) * dy (ReLU: a select, no multiply)
+template <int A>
+__device__ __forceinline__ float dact_mul(float t, float dy) {
+  if constexpr (A == 1) return t > 0.f ? dy : 0.f;
+  else return dact_t<A>(t) * dy;
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
@@ -943,37 +953,41 @@ __device__ __forceinline__ void stream_init(uint64_t* full) {
   __syncthreads();
 }
 
-template <typename T, int EC>
+template <typename T, int EC, int A>
 __global__ void __launch_bounds__(kBlock, 1) bn_apply_stream(const T* __restrict__ pre, T* __restrict__ y,
                                                              long seg_rows, int bps, int C, long rpb, int R, int cpg,
                                                              int rev, const float* __restrict__ mean,
                                                              const float* __restrict__ inv_std,
                                                              const float* __restrict__ gamma,
-                                                             const float* __restrict__ beta, int act, int* err) {
+                                                             const float* __restrict__ beta, int* err) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t full[kStreamStages];
   stream_init(full);
   const StreamSetup<T, EC, 1> st(seg_rows, bps, C, rpb, rev);
-  float mu[EC], sc[EC], be[EC];
+  float nmu[EC], sc[EC], be[EC];
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
     const int c = st.g * EC + e;
     const int si = stat_index(cpg, st.seg, c, C);
-    mu[e] = mean[si];
+    nmu[e] = -mean[si];
     sc[e] = gamma[c] * inv_std[si];
     be[e] = beta[c];
   }
   const T* const in[1] = {pre};
-  with_act(act, [&](auto ac) {
-    constexpr int A = decltype(ac)::value;
+  {
     stream_walk<T, EC, 1>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err, rev,
                           [&](long row, const float (&v)[1][EC]) {
                             float o[EC];
 #pragma unroll
-                            for (int e = 0; e < EC; ++e) o[e] = act_t<A>(fmaf(v[0][e] - mu[e], sc[e], be[e]));
+                            for (int e = 0; e < EC; e += 2) {
+                              // (x - mean) * gamma * inv_std + beta
+                              const float2 t = __ffma2_rn(__fadd2_rn(pr(v[0], e), pr(nmu, e)), pr(sc, e), pr(be, e));
+                              o[e] = act_t<A>(t.x);
+                              o[e + 1] = act_t<A>(t.y);
+                            }
                             store_v<EC>(y + row * C + st.g * EC, o);
                           });
-  });
+  }
 }
 
 // part[b][c][3] = (rows, mean, M2) of channel c over the block's rows (streamed form of norm_stats_kernel)
@@ -1032,44 +1046,52 @@ __global__ void __launch_bounds__(kBlock, 1) norm_stats_stream(const T* __restri
 }
 
 // part[b][c] = {sum d_norm, sum d_norm * z}
-template <typename T, int EC>
+template <typename T, int EC, int A>
 __global__ void __launch_bounds__(kBlock, 3) bn_bwd_reduce_stream(const T* __restrict__ pre, const T* __restrict__ dy,
                                                                   long seg_rows, int bps, int C, long rpb, int R,
                                                                   int cpg, int rev, const float* __restrict__ mean,
                                                                   const float* __restrict__ inv_std,
                                                                   const float* __restrict__ gamma,
-                                                                  const float* __restrict__ beta, int act,
+                                                                  const float* __restrict__ beta,
                                                                   float* __restrict__ part, int* err) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t full[kStreamStages];
-  __shared__ float s_a[kBlock * EC], s_b[kBlock * EC];
   stream_init(full);
   const StreamSetup<T, EC, 2> st(seg_rows, bps, C, rpb, rev);
-  float mu[EC], is[EC], ga[EC], be[EC], a[EC], b[EC];
+  float nmu[EC], is[EC], ga[EC], be[EC], a[EC], b[EC];
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
     const int c = st.g * EC + e;
     const int si = stat_index(cpg, st.seg, c, C);
-    mu[e] = mean[si];
+    nmu[e] = -mean[si];
     is[e] = inv_std[si];
     ga[e] = gamma[c];
     be[e] = beta[c];
     a[e] = b[e] = 0.f;
   }
   const T* const in[2] = {pre, dy};
-  with_act(act, [&](auto ac) {
-    constexpr int A = decltype(ac)::value;
+  {
     stream_walk<T, EC, 2>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err, rev,
                           [&](long, const float (&v)[2][EC]) {
 #pragma unroll
-                            for (int e = 0; e < EC; ++e) {
-                              const float z = (v[0][e] - mu[e]) * is[e];
-                              const float dn = dact_t<A>(fmaf(ga[e], z, be[e])) * v[1][e];
-                              a[e] += dn;
-                              b[e] = fmaf(dn, z, b[e]);
+                            for (int e = 0; e < EC; e += 2) {
+                              const float2 z = __fmul2_rn(__fadd2_rn(pr(v[0], e), pr(nmu, e)), pr(is, e));
+                              const float2 t = __ffma2_rn(pr(ga, e), z, pr(be, e));
+                              const float2 dn = make_float2(dact_mul<A>(t.x, v[1][e]), dact_mul<A>(t.y, v[1][e + 1]));
+                              const float2 sa = __fadd2_rn(pr(a, e), dn);
+                              const float2 sb = __ffma2_rn(dn, z, pr(b, e));
+                              a[e] = sa.x;
+                              a[e + 1] = sa.y;
+                              b[e] = sb.x;
+                              b[e + 1] = sb.y;
                             }
                           });
-  });
+  }
+  // the ring is free once the walk has returned (every chunk consumed, or the copies of a walk that
+  // gave up landed): it holds the block's per-thread sums (2 * kBlock * EC floats <= the ring)
+  __syncthreads();
+  float* s_a = reinterpret_cast<float*>(sm);
+  float* s_b = s_a + kBlock * EC;
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
     s_a[threadIdx.x * EC + e] = a[e];
@@ -1091,54 +1113,68 @@ __global__ void __launch_bounds__(kBlock, 3) bn_bwd_reduce_stream(const T* __res
 }
 
 // d_conv (MODE 0: batch / layer norm, 1: no norm) and part[b][c] = sum d_conv.
-template <typename T, int EC, int MODE>
-__global__ void __launch_bounds__(kBlock, 1) dconv_stream(const T* __restrict__ pre, const T* __restrict__ dy,
+// Without an activation three blocks fit an SM (registers capped for it); an activation needs more
+// registers (ReLU: gamma and beta stay live for its test; capped for three blocks it spills): two.
+template <typename T, int EC, int MODE, int A>
+__global__ void __launch_bounds__(kBlock, A == 0 ? 3 : 2) dconv_stream(const T* __restrict__ pre, const T* __restrict__ dy,
                                                           long seg_rows, int bps, int C, long rpb, int R, int cpg,
                                                           int rev, const float* __restrict__ mean,
                                                           const float* __restrict__ inv_std,
                                                           const float* __restrict__ gamma,
-                                                          const float* __restrict__ beta, int act,
+                                                          const float* __restrict__ beta,
                                                           const float* __restrict__ c12, T* __restrict__ dconv,
                                                           float* __restrict__ part, int* err) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t full[kStreamStages];
-  __shared__ float s_a[kBlock * EC];
   stream_init(full);
   const StreamSetup<T, EC, 2> st(seg_rows, bps, C, rpb, rev);
-  float mu[EC], is[EC], ga[EC], be[EC], k1[EC], k2[EC], a[EC];
+  float nmu[EC], is[EC], ga[EC], be[EC], nk1[EC], k2[EC], a[EC];
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
     const int c = st.g * EC + e;
     a[e] = 0.f;
     if (MODE == 0) {
       const int si = stat_index(cpg, st.seg, c, C);
-      mu[e] = mean[si];
+      nmu[e] = -mean[si];
       is[e] = inv_std[si];
       ga[e] = gamma[c];
       be[e] = beta[c];
-      norm_bwd_coef(c12, cpg, st.seg, c, C, ga[e], seg_rows, k1[e], k2[e]);
+      float k1;
+      norm_bwd_coef(c12, cpg, st.seg, c, C, ga[e], seg_rows, k1, k2[e]);
+      nk1[e] = -k1;
     }
   }
   const T* const in[2] = {pre, dy};
-  with_act(act, [&](auto ac) {
-    constexpr int A = decltype(ac)::value;
+  {
     stream_walk<T, EC, 2>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err, rev,
                           [&](long row, const float (&v)[2][EC]) {
                             float o[EC];
 #pragma unroll
-                            for (int e = 0; e < EC; ++e) {
+                            for (int e = 0; e < EC; e += 2) {
+                              float2 r;
                               if (MODE == 0) {
-                                const float z = (v[0][e] - mu[e]) * is[e];
-                                const float dn = dact_t<A>(fmaf(ga[e], z, be[e])) * v[1][e];
-                                o[e] = is[e] * (ga[e] * dn - k1[e] - z * k2[e]);
+                                // inv_std * (gamma * d_norm - k1 - z * k2)
+                                const float2 z = __fmul2_rn(__fadd2_rn(pr(v[0], e), pr(nmu, e)), pr(is, e));
+                                const float2 t = __ffma2_rn(pr(ga, e), z, pr(be, e));
+                                const float2 dn =
+                                    make_float2(dact_mul<A>(t.x, v[1][e]), dact_mul<A>(t.y, v[1][e + 1]));
+                                const float2 u = __ffma2_rn(pr(ga, e), dn, pr(nk1, e));
+                                r = __fmul2_rn(pr(is, e), __ffma2_rn(make_float2(-z.x, -z.y), pr(k2, e), u));
                               } else {
-                                o[e] = dact_t<A>(v[0][e]) * v[1][e];
+                                r = make_float2(dact_mul<A>(v[0][e], v[1][e]), dact_mul<A>(v[0][e + 1], v[1][e + 1]));
                               }
-                              a[e] += o[e];
+                              o[e] = r.x;
+                              o[e + 1] = r.y;
+                              const float2 sa = __fadd2_rn(pr(a, e), r);
+                              a[e] = sa.x;
+                              a[e + 1] = sa.y;
                             }
                             store_v<EC>(dconv + row * C + st.g * EC, o);
                           });
-  });
+  }
+  // the ring is free once the walk has returned: it holds the block's per-thread sums
+  __syncthreads();
+  float* s_a = reinterpret_cast<float*>(sm);
 #pragma unroll
   for (int e = 0; e < EC; ++e) s_a[threadIdx.x * EC + e] = a[e];
   __syncthreads();
@@ -1193,6 +1229,7 @@ RowWalk make_walk(long rows, int C, int dtype, int sms, int segs, int cpg) {
   long resident;
   if (w.stream) {
     w.R = static_cast<int>(std::max<long>(1, (kChunkBytes / 2) / row_bytes));
+    if (w.R > rpp) w.R = w.R / rpp * rpp;  // whole passes of the block's rows per chunk
     resident = 2L * sms;
   } else {
     w.R = 0;
@@ -1274,6 +1311,17 @@ cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float
 }
 
 // Launch a streamed kernel: EC is 8 (bf16) or 4 (fp32); dynamic shared memory holds the chunk ring.
+// STREAM_LAUNCH_ACT also makes the activation a compile-time constant A of the kernel, so that each
+// activation gets its own register allocation (tanh and sigmoid need far more registers than ReLU).
+#define STREAM_LAUNCH_ACT(act, dtype, NIN, KERNEL, ...)                         \
+  do {                                                                          \
+    switch (act) {                                                              \
+      case 1: { constexpr int A = 1; STREAM_LAUNCH(dtype, NIN, KERNEL, __VA_ARGS__); } break; \
+      case 2: { constexpr int A = 2; STREAM_LAUNCH(dtype, NIN, KERNEL, __VA_ARGS__); } break; \
+      case 3: { constexpr int A = 3; STREAM_LAUNCH(dtype, NIN, KERNEL, __VA_ARGS__); } break; \
+      default: { constexpr int A = 0; STREAM_LAUNCH(dtype, NIN, KERNEL, __VA_ARGS__); } break; \
+    }                                                                           \
+  } while (0)
 #define STREAM_LAUNCH(dtype, NIN, KERNEL, ...)                                                           \
   do {                                                                                                  \
     const size_t es = (dtype) == 1 ? 2 : 4;                                                             \
@@ -1290,23 +1338,6 @@ cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float
       KERNEL<<<wk.G, kBlock, smem, st>>>(__VA_ARGS__);                                                  \
     }                                                                                                   \
   } while (0)
-// The same with an explicit walk (a different chunk size).
-#define STREAM_LAUNCH_W(WK, dtype, NIN, KERNEL, ...)                                                           \
-  do {                                                                                                  \
-    const size_t es = (dtype) == 1 ? 2 : 4;                                                             \
-    const size_t smem = static_cast<size_t>(kStreamStages) * (NIN) * WK.R * WK.C * es;                  \
-    if ((dtype) == 1) {                                                                                 \
-      constexpr int EC = 8;                                                                             \
-      using T = __nv_bfloat16;                                                                          \
-      cudaFuncSetAttribute(KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
-      KERNEL<<<WK.G, kBlock, smem, st>>>(__VA_ARGS__);                                                  \
-    } else {                                                                                            \
-      constexpr int EC = 4;                                                                             \
-      using T = float;                                                                                  \
-      cudaFuncSetAttribute(KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
-      KERNEL<<<WK.G, kBlock, smem, st>>>(__VA_ARGS__);                                                  \
-    }                                                                                                   \
-  } while (0)
 
 // Walk arguments shared by every row-walk kernel: segment geometry and the layer-norm flag.
 #define WALK_ARGS wk.seg_rows, wk.bps, wk.C, wk.rows_per_block
@@ -1316,8 +1347,8 @@ cudaError_t launch_bn_apply(int dtype, const void* pre, void* y, const RowWalk& 
                             const float* inv_std, const float* gamma, const float* beta, int act, int rev,
                             cudaStream_t st) {
   if (wk.stream) {
-    STREAM_LAUNCH(dtype, 1, (bn_apply_stream<T, EC>), static_cast<const T*>(pre), static_cast<T*>(y), WALK_ARGS,
-                  wk.R, LN_FLAG, rev, mean, inv_std, gamma, beta, act, wk.err);
+    STREAM_LAUNCH_ACT(act, dtype, 1, (bn_apply_stream<T, EC, A>), static_cast<const T*>(pre), static_cast<T*>(y),
+                      WALK_ARGS, wk.R, LN_FLAG, rev, mean, inv_std, gamma, beta, wk.err);
     return cudaGetLastError();
   }
   DISPATCH_EC(dtype, wk.C,
@@ -1334,13 +1365,11 @@ cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, con
                                  const float* inv_std, const float* gamma, const float* beta, int act, float* part,
                                  cudaStream_t st) {
   if (wk.stream) {
-    // three blocks per SM (registers capped for it): chunks of three quarters of the walk's size so that
-    // three rings fit in shared memory; the rows each block walks are unchanged
-    RowWalk w3 = wk;
-    w3.R = std::max(1, wk.R * 3 / 4);
-    STREAM_LAUNCH_W(w3, dtype, 2, (bn_bwd_reduce_stream<T, EC>), static_cast<const T*>(pre),
-                    static_cast<const T*>(dy), WALK_ARGS, w3.R, LN_FLAG, 0, mean, inv_std, gamma, beta, act, part,
-                    wk.err);
+    // three blocks per SM (registers capped for it); the column-sum scratch reuses the ring, so three
+    // rings of full chunks fit in shared memory
+    STREAM_LAUNCH_ACT(act, dtype, 2, (bn_bwd_reduce_stream<T, EC, A>), static_cast<const T*>(pre),
+                      static_cast<const T*>(dy), WALK_ARGS, wk.R, LN_FLAG, 0, mean, inv_std, gamma, beta, part,
+                      wk.err);
     return cudaGetLastError();
   }
   DISPATCH_EC(dtype, wk.C,
@@ -1363,9 +1392,9 @@ cudaError_t launch_bn_bwd_apply(int dtype, const void* pre, const void* dy, cons
                                 const float* mean, const float* inv_std, const float* gamma, const float* beta,
                                 int act, const float* c12, void* dconv, float* part, cudaStream_t st) {
   if (wk.stream && wk.C == Cp) {  // reversed: starts on the rows the backward reduce read last
-    STREAM_LAUNCH(dtype, 2, (dconv_stream<T, EC, 0>), static_cast<const T*>(pre), static_cast<const T*>(dy),
-                  WALK_ARGS, wk.R, LN_FLAG, 1, mean, inv_std, gamma, beta, act, c12, static_cast<T*>(dconv), part,
-                  wk.err);
+    STREAM_LAUNCH_ACT(act, dtype, 2, (dconv_stream<T, EC, 0, A>), static_cast<const T*>(pre),
+                      static_cast<const T*>(dy), WALK_ARGS, wk.R, LN_FLAG, 1, mean, inv_std, gamma, beta, c12,
+                      static_cast<T*>(dconv), part, wk.err);
     return cudaGetLastError();
   }
   // the vector path needs C == Cp (EC divides C); otherwise one channel per thread
@@ -1384,9 +1413,9 @@ cudaError_t launch_bn_bwd_apply(int dtype, const void* pre, const void* dy, cons
 cudaError_t launch_act_bwd(int dtype, const void* pre, const void* dy, const RowWalk& wk, int Cp, int act,
                            void* dconv, float* part, cudaStream_t st) {
   if (wk.stream && wk.C == Cp) {
-    STREAM_LAUNCH(dtype, 2, (dconv_stream<T, EC, 1>), static_cast<const T*>(pre), static_cast<const T*>(dy),
-                  WALK_ARGS, wk.R, 0, 1, nullptr, nullptr, nullptr, nullptr, act, nullptr, static_cast<T*>(dconv), part,
-                  wk.err);
+    STREAM_LAUNCH_ACT(act, dtype, 2, (dconv_stream<T, EC, 1, A>), static_cast<const T*>(pre),
+                      static_cast<const T*>(dy), WALK_ARGS, wk.R, 0, 1, nullptr, nullptr, nullptr, nullptr, nullptr,
+                      static_cast<T*>(dconv), part, wk.err);
     return cudaGetLastError();
   }
   DISPATCH_EC(dtype, (wk.C == Cp ? wk.C : 1),
