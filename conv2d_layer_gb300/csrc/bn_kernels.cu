@@ -126,49 +126,56 @@ __device__ __forceinline__ Lane lane_of(long seg_rows, int bps, int Cw, int EC, 
 }
 
 // ------------------------------------------------------------ BN statistics
-// Chan merge, in double and in a fixed order, of per-tile (count, mean, M2)
-// partials [G][C][3] written by the fprop GEMM epilogue.
+// Pairwise Chan merge of (count, mean, M2): symmetric in its two operands, so both lanes of a
+// shuffle pair reach the same result.
+__device__ __forceinline__ void chan_merge(float& n, float& m, float& M, float nb, float mb, float Mb) {
+  const float nn = n + nb;
+  if (nn > 0.f) {
+    const float d = mb - m;
+    const float mm = (n * m + nb * mb) / nn;
+    M = M + Mb + d * d * (n * nb / nn);
+    m = mm;
+    n = nn;
+  }
+}
+
+// Merge of per-tile (count, mean, M2) partials [G][C][3] written by the fprop GEMM epilogue: one warp
+// per channel; each lane combines every 32nd partial as sums shifted by its first partial's mean
+// (exact for M2 up to rounding: sum(M2_b + n_b (mean_b - K)^2) - (sum n_b (mean_b - K))^2 / n), then
+// a fixed-order shuffle tree of Chan merges. fp32 throughout (GB300's fp64 rate is low); the same
+// order on every run.
 __global__ void __launch_bounds__(128) bn_stats_finalize_kernel(const float* __restrict__ part, int G, int C,
                                                                 float eps, float momentum, float* mean,
                                                                 float* inv_std, float* rm, float* rv) {
-  __shared__ double s_n[128], s_m[128], s_M[128];
-  const int c = blockIdx.x;
-  // each thread merges its share in fp32 (GB300's fp64 rate is low); the
-  // 128-way tree below runs in fp64
-  float n = 0.f, m = 0.f, M = 0.f;
-  for (int b = threadIdx.x; b < G; b += 128) {
-    const float* p = part + (static_cast<size_t>(b) * C + c) * 3;
-    const float nb = p[0], mb = p[1], Mb = p[2];
+  const int c = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (c >= C) return;  // the whole warp
+  float cnt = 0.f, K = 0.f, S1 = 0.f, S2 = 0.f;
+#pragma unroll 4
+  for (int b = lane; b < G; b += 32) {
+    const float* q = part + (static_cast<size_t>(b) * C + c) * 3;
+    const float nb = q[0], mb = q[1], Mb = q[2];
     if (nb == 0.f) continue;
-    const float nn = n + nb, d = mb - m, f = nb / nn;
-    m = fmaf(d, f, m);
-    M += Mb + d * d * n * f;
-    n = nn;
+    if (cnt == 0.f) K = mb;
+    const float d = mb - K;
+    S1 = fmaf(nb, d, S1);
+    S2 += fmaf(nb * d, d, Mb);
+    cnt += nb;
   }
-  s_n[threadIdx.x] = n;
-  s_m[threadIdx.x] = m;
-  s_M[threadIdx.x] = M;
-  __syncthreads();
-  for (int off = 64; off > 0; off >>= 1) {
-    if (threadIdx.x < off) {
-      const double na = s_n[threadIdx.x], nb = s_n[threadIdx.x + off];
-      if (nb > 0) {
-        const double nn = na + nb, d = s_m[threadIdx.x + off] - s_m[threadIdx.x];
-        s_m[threadIdx.x] += d * nb / nn;
-        s_M[threadIdx.x] += s_M[threadIdx.x + off] + d * d * na * nb / nn;
-        s_n[threadIdx.x] = nn;
-      }
-    }
-    __syncthreads();
+  float m = cnt > 0.f ? K + S1 / cnt : 0.f;
+  float M = cnt > 0.f ? fmaxf(S2 - S1 * (S1 / cnt), 0.f) : 0.f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float nb = __shfl_xor_sync(0xffffffffu, cnt, off);
+    const float mb = __shfl_xor_sync(0xffffffffu, m, off);
+    const float Mb = __shfl_xor_sync(0xffffffffu, M, off);
+    chan_merge(cnt, m, M, nb, mb, Mb);
   }
-  if (threadIdx.x == 0) {
-    const double nt = s_n[0];
-    const double mu = s_m[0];
-    const double var = nt > 0 ? s_M[0] / nt : 0.0;  // biased, as on the pages
-    mean[c] = static_cast<float>(mu);
-    inv_std[c] = static_cast<float>(1.0 / sqrt(var + static_cast<double>(eps)));
-    rm[c] = static_cast<float>((1.0 - momentum) * rm[c] + static_cast<double>(momentum) * mu);
-    rv[c] = static_cast<float>((1.0 - momentum) * rv[c] + static_cast<double>(momentum) * var);
+  if (lane == 0) {
+    const float var = cnt > 0.f ? M / cnt : 0.f;  // biased, as on the pages
+    mean[c] = m;
+    inv_std[c] = static_cast<float>(1.0 / sqrt(static_cast<double>(var) + static_cast<double>(eps)));
+    rm[c] = (1.f - momentum) * rm[c] + momentum * m;
+    rv[c] = (1.f - momentum) * rv[c] + momentum * var;
   }
 }
 
@@ -420,34 +427,50 @@ __global__ void __launch_bounds__(kBlock) dconv_kernel(const T* __restrict__ pre
   }
 }
 
+__device__ __forceinline__ void kahan_add(float& s, float& comp, float x) {
+  const float y = x - comp;
+  const float t = s + y;
+  comp = (t - s) - y;
+  s = t;
+}
+
+// Per-channel sums of per-block partials [G][C][nv]: one 128-thread block per channel; compensated
+// fp32 sums per thread over every 128th partial, fp64 shuffle trees within the warps and the four warp
+// totals added in a fixed order (the same result on every run). mode 0: c12 = (sum d_norm,
+// sum d_norm z), dbeta += first, dgamma += second; mode 1: dbias += the sum.
 __global__ void __launch_bounds__(128) sum_finalize_kernel(const float* __restrict__ part, int G, int C, int nv,
                                                            int mode, float* c12, float* acc0, float* acc1) {
-  __shared__ double s[2][128];
-  const int c = blockIdx.x;
-  float a = 0.f, b = 0.f;
+  __shared__ double s_w[2][4];
+  const int c = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float a = 0.f, ca = 0.f, b = 0.f, cb = 0.f;
+#pragma unroll 4
   for (int k = threadIdx.x; k < G; k += 128) {
     const float* p = part + (static_cast<size_t>(k) * C + c) * nv;
-    a += p[0];
-    if (nv > 1) b += p[1];
+    kahan_add(a, ca, p[0]);
+    if (nv > 1) kahan_add(b, cb, p[1]);
   }
-  s[0][threadIdx.x] = a;
-  s[1][threadIdx.x] = b;
+  double da = static_cast<double>(a) - static_cast<double>(ca);
+  double db = static_cast<double>(b) - static_cast<double>(cb);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    da += __shfl_xor_sync(0xffffffffu, da, off);
+    db += __shfl_xor_sync(0xffffffffu, db, off);
+  }
+  if (lane == 0) {
+    s_w[0][w] = da;
+    s_w[1][w] = db;
+  }
   __syncthreads();
-  for (int off = 64; off > 0; off >>= 1) {
-    if (threadIdx.x < off) {
-      s[0][threadIdx.x] += s[0][threadIdx.x + off];
-      s[1][threadIdx.x] += s[1][threadIdx.x + off];
-    }
-    __syncthreads();
-  }
   if (threadIdx.x == 0) {
+    const double ta = (s_w[0][0] + s_w[0][1]) + (s_w[0][2] + s_w[0][3]);
+    const double tb = (s_w[1][0] + s_w[1][1]) + (s_w[1][2] + s_w[1][3]);
     if (mode == 0) {
-      c12[2 * c] = static_cast<float>(s[0][0]);
-      c12[2 * c + 1] = static_cast<float>(s[1][0]);
-      if (acc0) acc0[c] += static_cast<float>(s[0][0]);  // dbeta
-      if (acc1) acc1[c] += static_cast<float>(s[1][0]);  // dgamma
+      c12[2 * c] = static_cast<float>(ta);
+      c12[2 * c + 1] = static_cast<float>(tb);
+      if (acc0) acc0[c] += static_cast<float>(ta);  // dbeta
+      if (acc1) acc1[c] += static_cast<float>(tb);  // dgamma
     } else {
-      if (acc0) acc0[c] += static_cast<float>(s[0][0]);  // dbias
+      if (acc0) acc0[c] += static_cast<float>(ta);  // dbias
     }
   }
 }
@@ -595,10 +618,26 @@ __global__ void wgrad_reduce_kernel(const float* __restrict__ partial, int split
     const int tap = static_cast<int>(ot % taps);
     const int oc = static_cast<int>(ot / taps);
     const long m = static_cast<long>(tap) * ICp + ic;
-    // compensated (Kahan) fp32 summation in split order: fp64 is slow on this part
+    // compensated (Kahan) fp32 summation in split order: fp64 is slow on this part; the loads of eight
+    // splits are issued before their sums
     float s = 0.f, comp = 0.f;
-    for (int k = 0; k < splits; ++k) {
-      const float yk = partial[(static_cast<long>(k) * OC + oc) * Mk + m] - comp;
+    const float* q = partial + static_cast<long>(oc) * Mk + m;
+    const long stride = static_cast<long>(OC) * Mk;
+    int k = 0;
+    for (; k + 8 <= splits; k += 8) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = q[(k + j) * stride];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float yk = v[j] - comp;
+        const float t = s + yk;
+        comp = (t - s) - yk;
+        s = t;
+      }
+    }
+    for (; k < splits; ++k) {
+      const float yk = q[k * stride] - comp;
       const float t = s + yk;
       comp = (t - s) - yk;
       s = t;
@@ -756,16 +795,6 @@ __global__ void __launch_bounds__(128) norm_seg_finalize_kernel(const float* __r
 // part[b][c][3] of an image-aligned walk over the stored pre-activations. wpo warps per output
 // s = n * groups + g: per lane sums shifted by its first partial mean (no division per partial), a
 // fixed Chan tree over the lanes, then over the wpo warps.
-__device__ __forceinline__ void chan_merge(float& n, float& m, float& M, float nb, float mb, float Mb) {
-  const float nn = n + nb;
-  if (nn > 0.f) {  // symmetric in the two operands (both lanes of a shuffle pair agree)
-    const float d = mb - m;
-    const float mm = (n * m + nb * mb) / nn;
-    M = M + Mb + d * d * (n * nb / nn);
-    m = mm;
-    n = nn;
-  }
-}
 
 __global__ void __launch_bounds__(128) gn_stats_finalize_kernel(const float* __restrict__ part, int bps, int C,
                                                                 int cpg, int n_out, int wpo, float eps, float* mean,
@@ -1306,7 +1335,7 @@ cudaError_t launch_prep_dgrad_weights(int dtype, const void* w, void* bhi, float
 
 cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float eps, float momentum, float* mean,
                                      float* inv_std, float* rm, float* rv, cudaStream_t st) {
-  bn_stats_finalize_kernel<<<wk.C, 128, 0, st>>>(part, wk.G, wk.C, eps, momentum, mean, inv_std, rm, rv);
+  bn_stats_finalize_kernel<<<(wk.C + 3) / 4, 128, 0, st>>>(part, wk.G, wk.C, eps, momentum, mean, inv_std, rm, rv);
   return cudaGetLastError();
 }
 
