@@ -310,10 +310,11 @@ def per_config_timing(peaks, steps=10, warmup=3):
         for kname, t in abi.conv2d_prof_read(4096):
             kern[kname] = kern.get(kname, 0.0) + t
         fl = sum(s.flops_step() for s in specs)
-        s0 = specs[-1]
-        tensor_bytes = s0.n_pix * s0.OC * (2 if s0.dtype == 1 else 4)
+        # a layer's output tensor; over a stack (every layer with the same norm and activation) the
+        # algorithmic bytes and the kernel times are both summed over the layers
+        tensor_bytes = sum(s.n_pix * s.OC * (2 if s.dtype == 1 else 4) for s in specs)
         hbm = {k: round(HBM_TENSORS[k] * tensor_bytes / (t * 1e-3) / 1e9 / peaks["hbm"], 3)
-               for k, t in kern.items() if k in HBM_TENSORS and len(specs) == 1}
+               for k, t in kern.items() if k in HBM_TENSORS}
         out[label] = {"ms_per_step": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
                       "dtype": "bf16" if specs[0].dtype == 1 else "fp32 (3xTF32)", "layers": len(specs),
                       "kernels_ms": {k: round(t, 4) for k, t in kern.items()}, "hbm_frac_of_measured": hbm}

@@ -15,6 +15,7 @@
 // E[x^2] - mean^2.
 #include <algorithm>
 #include <cmath>
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include "kernels.h"
@@ -25,6 +26,9 @@ namespace c2d {
 namespace {
 
 constexpr int kBlock = 256;
+// Layers stored in bf16 take the fast activations (see act_f).
+template <typename T>
+constexpr bool kFastAct = std::is_same<T, __nv_bfloat16>::value;
 
 template <int EC>
 __device__ __forceinline__ void load_v(const float* p, float (&v)[EC]) {
@@ -204,7 +208,7 @@ __global__ void __launch_bounds__(kBlock) bn_apply_kernel(const T* __restrict__ 
       float v[EC];
       load_v<EC>(pre + r * C + g * EC, v);
 #pragma unroll
-      for (int e = 0; e < EC; ++e) v[e] = act_f(act, fmaf(v[e] - mu[e], sc[e], be[e]));
+      for (int e = 0; e < EC; ++e) v[e] = act_f(act, fmaf(v[e] - mu[e], sc[e], be[e]), kFastAct<T>);
       store_v<EC>(y + r * C + g * EC, v);
     }
   }
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(kBlock) bn_bwd_reduce_kernel(const T* __restri
 #pragma unroll
         for (int e = 0; e < EC; ++e) {
           const float z = (v[e] - mu[e]) * is[e];
-          const float dn = dact_f(act, fmaf(ga[e], z, be[e])) * d[e];
+          const float dn = dact_f(act, fmaf(ga[e], z, be[e]), kFastAct<T>) * d[e];
           a[e] += dn;
           b[e] = fmaf(dn, z, b[e]);
         }
@@ -399,10 +403,10 @@ __global__ void __launch_bounds__(kBlock) dconv_kernel(const T* __restrict__ pre
           for (int e = 0; e < EC; ++e) {
             if (MODE == 0) {
               const float z = (v[e] - mu[e]) * is[e];
-              const float dn = dact_f(act, fmaf(ga[e], z, be[e])) * d[e];
+              const float dn = dact_f(act, fmaf(ga[e], z, be[e]), kFastAct<T>) * d[e];
               o[e] = is[e] * (ga[e] * dn - k1[e] - z * k2[e]);
             } else {
-              o[e] = dact_f(act, v[e]) * d[e];
+              o[e] = dact_f(act, v[e], kFastAct<T>) * d[e];
             }
             a[e] += o[e];
           }
@@ -884,12 +888,13 @@ __device__ __forceinline__ void lds_v(const __nv_bfloat16* p, float (&v)[EC]) {
 // Elements e, e+1 of a per-thread channel group as one packed pair (f32x2 arithmetic below: the
 // same operations as per element, two per instruction).
 __device__ __forceinline__ float2 pr(const float* v, int e) { return make_float2(v[e], v[e + 1]); }
-// act'(t) * dy (ReLU: a select, no multiply)
-template <int A>
+// act'(t) * dy (ReLU: a select, no multiply); FAST for layers stored in bf16 (see act_f)
+template <int A, bool FAST>
 __device__ __forceinline__ float dact_mul(float t, float dy) {
   if constexpr (A == 1) return t > 0.f ? dy : 0.f;
-  else return dact_t<A>(t) * dy;
+  else return dact_t<A, FAST>(t) * dy;
 }
+
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -1011,8 +1016,8 @@ __global__ void __launch_bounds__(kBlock, 1) bn_apply_stream(const T* __restrict
                             for (int e = 0; e < EC; e += 2) {
                               // (x - mean) * gamma * inv_std + beta
                               const float2 t = __ffma2_rn(__fadd2_rn(pr(v[0], e), pr(nmu, e)), pr(sc, e), pr(be, e));
-                              o[e] = act_t<A>(t.x);
-                              o[e + 1] = act_t<A>(t.y);
+                              o[e] = act_t<A, kFastAct<T>>(t.x);
+                              o[e + 1] = act_t<A, kFastAct<T>>(t.y);
                             }
                             store_v<EC>(y + row * C + st.g * EC, o);
                           });
@@ -1106,7 +1111,8 @@ __global__ void __launch_bounds__(kBlock, 3) bn_bwd_reduce_stream(const T* __res
                             for (int e = 0; e < EC; e += 2) {
                               const float2 z = __fmul2_rn(__fadd2_rn(pr(v[0], e), pr(nmu, e)), pr(is, e));
                               const float2 t = __ffma2_rn(pr(ga, e), z, pr(be, e));
-                              const float2 dn = make_float2(dact_mul<A>(t.x, v[1][e]), dact_mul<A>(t.y, v[1][e + 1]));
+                              const float2 dn = make_float2(dact_mul<A, kFastAct<T>>(t.x, v[1][e]),
+                                                            dact_mul<A, kFastAct<T>>(t.y, v[1][e + 1]));
                               const float2 sa = __fadd2_rn(pr(a, e), dn);
                               const float2 sb = __ffma2_rn(dn, z, pr(b, e));
                               a[e] = sa.x;
@@ -1186,11 +1192,13 @@ __global__ void __launch_bounds__(kBlock, A == 0 ? 3 : 2) dconv_stream(const T* 
                                 const float2 z = __fmul2_rn(__fadd2_rn(pr(v[0], e), pr(nmu, e)), pr(is, e));
                                 const float2 t = __ffma2_rn(pr(ga, e), z, pr(be, e));
                                 const float2 dn =
-                                    make_float2(dact_mul<A>(t.x, v[1][e]), dact_mul<A>(t.y, v[1][e + 1]));
+                                    make_float2(dact_mul<A, kFastAct<T>>(t.x, v[1][e]),
+                                                dact_mul<A, kFastAct<T>>(t.y, v[1][e + 1]));
                                 const float2 u = __ffma2_rn(pr(ga, e), dn, pr(nk1, e));
                                 r = __fmul2_rn(pr(is, e), __ffma2_rn(make_float2(-z.x, -z.y), pr(k2, e), u));
                               } else {
-                                r = make_float2(dact_mul<A>(v[0][e], v[1][e]), dact_mul<A>(v[0][e + 1], v[1][e + 1]));
+                                r = make_float2(dact_mul<A, kFastAct<T>>(v[0][e], v[1][e]),
+                                                dact_mul<A, kFastAct<T>>(v[0][e + 1], v[1][e + 1]));
                               }
                               o[e] = r.x;
                               o[e + 1] = r.y;

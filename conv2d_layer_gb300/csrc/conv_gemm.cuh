@@ -745,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         if (valid) {
           float o[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = p.out_act ? act_f(p.act, v[e]) : to_stored<T>(v[e]);
+          for (int e = 0; e < 32; ++e) o[e] = p.out_act ? act_f(p.act, v[e], DT == 1) : to_stored<T>(v[e]);
           if (p.rstats) {  // o holds the stored value (the host never combines rstats with out_act)
             const int nc = ncols < 32 ? ncols : 32;
             float sum = 0.f;
@@ -765,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           store_row32<T>(out + obase + col0, o, ncols, vec);
           if (out2) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = act_f(p.act, to_stored<T>(v[e]));
+            for (int e = 0; e < 32; ++e) o[e] = act_f(p.act, to_stored<T>(v[e]), DT == 1);
             store_row32<T>(out2 + obase + col0, o, ncols, vec);
           }
         }

@@ -364,37 +364,47 @@ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
 
 // ---------------------------------------------------------------- activations
 // 0 identity, 1 relu, 2 tanh, 3 sigmoid; derivative at the activation input.
-__device__ __forceinline__ float act_f(int act, float v) {
+// fast (layers stored in bf16): tanh by the hardware's approximate instruction (tanh.approx.f32,
+// relative error about 2^-11, below bf16's rounding step of 2^-9) and sigmoid with the fast
+// exponential and division intrinsics; fp32 layers call tanhf / expf.
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+
+__device__ __forceinline__ float act_f(int act, float v, bool fast = false) {
   switch (act) {
     case 1: return v > 0.f ? v : 0.f;
-    case 2: return tanhf(v);
-    case 3: return 1.f / (1.f + expf(-v));
+    case 2: return fast ? tanh_fast(v) : tanhf(v);
+    case 3: return fast ? sigmoid_fast(v) : 1.f / (1.f + expf(-v));
     default: return v;
   }
 }
-__device__ __forceinline__ float dact_f(int act, float v) {
+__device__ __forceinline__ float dact_f(int act, float v, bool fast = false) {
   switch (act) {
     case 1: return v > 0.f ? 1.f : 0.f;
-    case 2: { float t = tanhf(v); return 1.f - t * t; }
-    case 3: { float s = 1.f / (1.f + expf(-v)); return s * (1.f - s); }
+    case 2: { const float t = fast ? tanh_fast(v) : tanhf(v); return 1.f - t * t; }
+    case 3: { const float s = fast ? sigmoid_fast(v) : 1.f / (1.f + expf(-v)); return s * (1.f - s); }
     default: return 1.f;
   }
 }
 
 // The same with the activation fixed at compile time (the per-element switch above costs a
 // compare and branch per element inside the bandwidth-bound loops).
-template <int A>
+template <int A, bool FAST = false>
 __device__ __forceinline__ float act_t(float v) {
   if constexpr (A == 1) return v > 0.f ? v : 0.f;
-  else if constexpr (A == 2) return tanhf(v);
-  else if constexpr (A == 3) return 1.f / (1.f + expf(-v));
+  else if constexpr (A == 2) return FAST ? tanh_fast(v) : tanhf(v);
+  else if constexpr (A == 3) return FAST ? sigmoid_fast(v) : 1.f / (1.f + expf(-v));
   else return v;
 }
-template <int A>
+template <int A, bool FAST = false>
 __device__ __forceinline__ float dact_t(float v) {
   if constexpr (A == 1) return v > 0.f ? 1.f : 0.f;
-  else if constexpr (A == 2) { const float t = tanhf(v); return 1.f - t * t; }
-  else if constexpr (A == 3) { const float s = 1.f / (1.f + expf(-v)); return s * (1.f - s); }
+  else if constexpr (A == 2) { const float t = FAST ? tanh_fast(v) : tanhf(v); return 1.f - t * t; }
+  else if constexpr (A == 3) { const float s = FAST ? sigmoid_fast(v) : 1.f / (1.f + expf(-v)); return s * (1.f - s); }
   else return 1.f;
 }
 template <int A>
