@@ -782,6 +782,7 @@ int prep_forward_operands(const Geo& g, const void* x, const void* w, void* ws, 
 // One thread waits on a barrier that nothing completes: the library's bounded
 // wait must give up, record `site` in the error word and let the kernel end.
 __global__ void wait_limit_selftest_kernel(int* err, int site) {
+  pdl_entry();
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
@@ -800,7 +801,7 @@ int conv2d_selftest_wait_limit(void* stream) {
   const int rc = device_info(&dev);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  LAUNCH("wait_limit_selftest", st, (wait_limit_selftest_kernel<<<1, 32, 0, st>>>(dev->err, 6), cudaGetLastError()));
+  LAUNCH("wait_limit_selftest", st, (launch_k(wait_limit_selftest_kernel, 1, 32, 0, st, 1, dev->err, 6), cudaGetLastError()));
   return CONV2D_OK;
 }
 

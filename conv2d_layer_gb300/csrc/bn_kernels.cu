@@ -151,6 +151,7 @@ __device__ __forceinline__ void chan_merge(float& n, float& m, float& M, float n
 __global__ void __launch_bounds__(128) bn_stats_finalize_kernel(const float* __restrict__ part, int G, int C,
                                                                 float eps, float momentum, float* mean,
                                                                 float* inv_std, float* rm, float* rv) {
+  pdl_entry();
   const int c = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (c >= C) return;  // the whole warp
   float cnt = 0.f, K = 0.f, S1 = 0.f, S2 = 0.f;
@@ -192,6 +193,7 @@ __global__ void __launch_bounds__(kBlock) bn_apply_kernel(const T* __restrict__ 
                                                           const float* __restrict__ inv_std,
                                                           const float* __restrict__ gamma,
                                                           const float* __restrict__ beta, int act) {
+  pdl_entry();
   const Lane l = lane_of(seg_rows, bps, C, EC, rpb);
   if (l.rl >= l.rpp) return;
   for (int g = l.g0; g < l.cg; g += l.tpr) {
@@ -220,6 +222,7 @@ __global__ void __launch_bounds__(kBlock) bn_apply_kernel(const T* __restrict__ 
 template <typename T, int EC>
 __global__ void __launch_bounds__(kBlock) norm_stats_kernel(const T* __restrict__ pre, long seg_rows, int bps,
                                                             int C, long rpb, float* __restrict__ part) {
+  pdl_entry();
   __shared__ float s_n[kBlock], s_m[kBlock * EC], s_M[kBlock * EC];
   const Lane l = lane_of(seg_rows, bps, C, EC, rpb);
   for (int gb = 0; gb < l.cg; gb += l.tpr) {
@@ -284,6 +287,7 @@ __global__ void __launch_bounds__(kBlock) bn_bwd_reduce_kernel(const T* __restri
                                                                const float* __restrict__ gamma,
                                                                const float* __restrict__ beta, int act,
                                                                float* __restrict__ part) {
+  pdl_entry();
   __shared__ float s_a[kBlock * EC], s_b[kBlock * EC];
   const Lane l = lane_of(seg_rows, bps, C, EC, rpb);
   for (int gb = 0; gb < l.cg; gb += l.tpr) {
@@ -369,6 +373,7 @@ __global__ void __launch_bounds__(kBlock) dconv_kernel(const T* __restrict__ pre
                                                        const float* __restrict__ beta, int act,
                                                        const float* __restrict__ c12, T* __restrict__ dconv,
                                                        float* __restrict__ part) {
+  pdl_entry();
   __shared__ float s_a[kBlock * EC];
   // the walk covers Cp channels so that padded channels of d_conv get zeros
   const Lane l = lane_of(seg_rows, bps, Cp, EC, rpb);
@@ -444,6 +449,7 @@ __device__ __forceinline__ void kahan_add(float& s, float& comp, float x) {
 // sum d_norm z), dbeta += first, dgamma += second; mode 1: dbias += the sum.
 __global__ void __launch_bounds__(128) sum_finalize_kernel(const float* __restrict__ part, int G, int C, int nv,
                                                            int mode, float* c12, float* acc0, float* acc1) {
+  pdl_entry();
   __shared__ double s_w[2][4];
   const int c = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float a = 0.f, ca = 0.f, b = 0.f, cb = 0.f;
@@ -482,6 +488,7 @@ __global__ void __launch_bounds__(128) sum_finalize_kernel(const float* __restri
 // ------------------------------------------------------------ layout prep
 template <typename T>
 __global__ void pack_channels_kernel(const T* __restrict__ src, T* __restrict__ dst, long rows, int C, int Cp) {
+  pdl_entry();
   const long total = rows * Cp;
   for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long>(gridDim.x) * blockDim.x) {
@@ -495,6 +502,7 @@ __global__ void pack_channels_kernel(const T* __restrict__ src, T* __restrict__ 
 template <typename T>
 __global__ void prep_fprop_weights_kernel(const T* __restrict__ w, T* __restrict__ bhi, float* __restrict__ blo,
                                           int OC, int taps, int IC, int ICp) {
+  pdl_entry();
   const long total = static_cast<long>(OC) * taps * ICp;
   for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long>(gridDim.x) * blockDim.x) {
@@ -517,6 +525,7 @@ __global__ void prep_fprop_weights_kernel(const T* __restrict__ w, T* __restrict
 template <typename T>
 __global__ void prep_col2im_weights_kernel(const T* __restrict__ w, T* __restrict__ bhi, float* __restrict__ blo,
                                            int OC, int taps, int IC, int ICp, int OCp) {
+  pdl_entry();
   const long total = static_cast<long>(taps) * ICp * OCp;
   for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long>(gridDim.x) * blockDim.x) {
@@ -541,6 +550,7 @@ __global__ void prep_col2im_weights_kernel(const T* __restrict__ w, T* __restric
 template <typename T, int EC>
 __global__ void col2im_kernel(const T* __restrict__ dcol, T* __restrict__ dx, int N, int H, int W, int IC, int ICp,
                               int OH, int OW, int KH, int KW, int S, int P) {
+  pdl_entry();
   const int groups = IC / EC;
   const long total = static_cast<long>(N) * H * W * groups;
   const int taps_icp = KH * KW * ICp;
@@ -580,6 +590,7 @@ template <typename T>
 __global__ void prep_dgrad_weights_kernel(const T* __restrict__ w, T* __restrict__ bhi, float* __restrict__ blo,
                                           int OC, int KH, int KW, int IC, int ICp, int OCp, int S, int Kd,
                                           const DgradWeightTable t) {
+  pdl_entry();
   const long total = static_cast<long>(ICp) * Kd;
   for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long>(gridDim.x) * blockDim.x) {
@@ -613,6 +624,7 @@ __global__ void prep_dgrad_weights_kernel(const T* __restrict__ w, T* __restrict
 // dW[oc][tap][ic] += sum over splits of partial[s][oc][tap*ICp + ic] (fixed order: deterministic).
 __global__ void wgrad_reduce_kernel(const float* __restrict__ partial, int splits, int OC, int taps, int ICp, int IC,
                                     float* __restrict__ dw) {
+  pdl_entry();
   const long total = static_cast<long>(OC) * taps * IC;
   const long Mk = static_cast<long>(taps) * ICp;
   for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < total;
@@ -654,6 +666,7 @@ __global__ void wgrad_reduce_kernel(const float* __restrict__ partial, int split
 // running ones (`forward` with mode::Evaluation), nothing is updated.
 __global__ void bn_eval_stats_kernel(const float* rm, const float* rv, float eps, int C, float* mean,
                                      float* inv_std) {
+  pdl_entry();
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= C) return;
   mean[c] = rm[c];
@@ -664,6 +677,7 @@ __global__ void bn_eval_stats_kernel(const float* rm, const float* rv, float eps
 // running-statistics normalisation (`evaluate`, BN branch).
 __global__ void infer_fold_kernel(const float* bias, const float* gamma, const float* beta, const float* rm,
                                   const float* rv, float eps, int norm, int OC, float* scale, float* shift) {
+  pdl_entry();
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= OC) return;
   const float b = bias ? bias[c] : 0.f;
@@ -687,6 +701,7 @@ __global__ void infer_fold_kernel(const float* bias, const float* gamma, const f
 __global__ void __launch_bounds__(256) ln_stats_finalize_kernel(const float* __restrict__ rs, int n_tiles,
                                                                 int halves, int BN, int hcols, int OC, long hw,
                                                                 float eps, float* mean, float* inv_std) {
+  pdl_entry();
   __shared__ float s_n[8], s_m[8], s_M[8];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int per_pix = n_tiles * halves;
@@ -759,6 +774,7 @@ static int finalize_wpo(long n_ent) { return n_ent >= 1024 ? 4 : (n_ent >= 256 ?
 __global__ void __launch_bounds__(128) norm_seg_finalize_kernel(const float* __restrict__ part, int bps, int C,
                                                                 int cpg, int n_out, int wpo,
                                                                 const float* __restrict__ gamma, float* out) {
+  pdl_entry();
   __shared__ float s_a[4], s_b[4];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = blockIdx.x * (4 / wpo) + w / wpo, sub = w % wpo;
@@ -803,6 +819,7 @@ __global__ void __launch_bounds__(128) norm_seg_finalize_kernel(const float* __r
 __global__ void __launch_bounds__(128) gn_stats_finalize_kernel(const float* __restrict__ part, int bps, int C,
                                                                 int cpg, int n_out, int wpo, float eps, float* mean,
                                                                 float* inv_std) {
+  pdl_entry();
   __shared__ float s_n[4], s_m[4], s_M[4];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = blockIdx.x * (4 / wpo) + w / wpo, sub = w % wpo;
@@ -994,6 +1011,7 @@ __global__ void __launch_bounds__(kBlock, 1) bn_apply_stream(const T* __restrict
                                                              const float* __restrict__ inv_std,
                                                              const float* __restrict__ gamma,
                                                              const float* __restrict__ beta, int* err) {
+  pdl_entry();
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t full[kStreamStages];
   stream_init(full);
@@ -1029,6 +1047,7 @@ template <typename T, int EC>
 __global__ void __launch_bounds__(kBlock, 1) norm_stats_stream(const T* __restrict__ pre, long seg_rows, int bps,
                                                                int C, long rpb, int R, int rev,
                                                                float* __restrict__ part, int* err) {
+  pdl_entry();
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t full[kStreamStages];
   __shared__ float s_n[kBlock], s_m[kBlock * EC], s_M[kBlock * EC];
@@ -1088,6 +1107,7 @@ __global__ void __launch_bounds__(kBlock, 3) bn_bwd_reduce_stream(const T* __res
                                                                   const float* __restrict__ gamma,
                                                                   const float* __restrict__ beta,
                                                                   float* __restrict__ part, int* err) {
+  pdl_entry();
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t full[kStreamStages];
   stream_init(full);
@@ -1159,6 +1179,7 @@ __global__ void __launch_bounds__(kBlock, A == 0 ? 3 : 2) dconv_stream(const T* 
                                                           const float* __restrict__ beta,
                                                           const float* __restrict__ c12, T* __restrict__ dconv,
                                                           float* __restrict__ part, int* err) {
+  pdl_entry();
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ uint64_t full[kStreamStages];
   stream_init(full);
@@ -1306,10 +1327,10 @@ RowWalk make_walk(long rows, int C, int dtype, int sms, int segs, int cpg) {
 cudaError_t launch_pack_channels(int dtype, const void* src, void* dst, long rows, int C, int Cp, cudaStream_t st) {
   const int g = grid_for(rows * Cp, 256);
   if (dtype == 1)
-    pack_channels_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src),
+    launch_k(pack_channels_kernel<__nv_bfloat16>, g, 256, 0, st, 1, static_cast<const __nv_bfloat16*>(src),
                                                            static_cast<__nv_bfloat16*>(dst), rows, C, Cp);
   else
-    pack_channels_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(src), static_cast<float*>(dst), rows,
+    launch_k(pack_channels_kernel<float>, g, 256, 0, st, 1, static_cast<const float*>(src), static_cast<float*>(dst), rows,
                                                    C, Cp);
   return cudaGetLastError();
 }
@@ -1318,11 +1339,11 @@ cudaError_t launch_prep_fprop_weights(int dtype, const void* w, void* bhi, float
                                       int ICp, cudaStream_t st) {
   const int g = grid_for(static_cast<long>(OC) * taps * ICp, 256);
   if (dtype == 1)
-    prep_fprop_weights_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w),
+    launch_k(prep_fprop_weights_kernel<__nv_bfloat16>, g, 256, 0, st, 1, static_cast<const __nv_bfloat16*>(w),
                                                                 static_cast<__nv_bfloat16*>(bhi), nullptr, OC, taps,
                                                                 IC, ICp);
   else
-    prep_fprop_weights_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(w), static_cast<float*>(bhi), blo,
+    launch_k(prep_fprop_weights_kernel<float>, g, 256, 0, st, 1, static_cast<const float*>(w), static_cast<float*>(bhi), blo,
                                                         OC, taps, IC, ICp);
   return cudaGetLastError();
 }
@@ -1332,18 +1353,18 @@ cudaError_t launch_prep_dgrad_weights(int dtype, const void* w, void* bhi, float
                                       cudaStream_t st) {
   const int g = grid_for(static_cast<long>(ICp) * Kd, 256);
   if (dtype == 1)
-    prep_dgrad_weights_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w),
+    launch_k(prep_dgrad_weights_kernel<__nv_bfloat16>, g, 256, 0, st, 1, static_cast<const __nv_bfloat16*>(w),
                                                                 static_cast<__nv_bfloat16*>(bhi), nullptr, OC, KH, KW,
                                                                 IC, ICp, OCp, S, Kd, t);
   else
-    prep_dgrad_weights_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(w), static_cast<float*>(bhi), blo,
+    launch_k(prep_dgrad_weights_kernel<float>, g, 256, 0, st, 1, static_cast<const float*>(w), static_cast<float*>(bhi), blo,
                                                         OC, KH, KW, IC, ICp, OCp, S, Kd, t);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float eps, float momentum, float* mean,
                                      float* inv_std, float* rm, float* rv, cudaStream_t st) {
-  bn_stats_finalize_kernel<<<(wk.C + 3) / 4, 128, 0, st>>>(part, wk.G, wk.C, eps, momentum, mean, inv_std, rm, rv);
+  launch_k(bn_stats_finalize_kernel, (wk.C + 3) / 4, 128, 0, st, 1, part, wk.G, wk.C, eps, momentum, mean, inv_std, rm, rv);
   return cudaGetLastError();
 }
 
@@ -1367,12 +1388,12 @@ cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float
       constexpr int EC = 8;                                                                             \
       using T = __nv_bfloat16;                                                                          \
       cudaFuncSetAttribute(KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
-      KERNEL<<<wk.G, kBlock, smem, st>>>(__VA_ARGS__);                                                  \
+      launch_k(KERNEL, wk.G, kBlock, smem, st, 1, __VA_ARGS__);                                                  \
     } else {                                                                                            \
       constexpr int EC = 4;                                                                             \
       using T = float;                                                                                  \
       cudaFuncSetAttribute(KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
-      KERNEL<<<wk.G, kBlock, smem, st>>>(__VA_ARGS__);                                                  \
+      launch_k(KERNEL, wk.G, kBlock, smem, st, 1, __VA_ARGS__);                                                  \
     }                                                                                                   \
   } while (0)
 
@@ -1389,10 +1410,10 @@ cudaError_t launch_bn_apply(int dtype, const void* pre, void* y, const RowWalk& 
     return cudaGetLastError();
   }
   DISPATCH_EC(dtype, wk.C,
-              (bn_apply_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), static_cast<T*>(y),
+              (launch_k(bn_apply_kernel<T, EC>, wk.G, kBlock, 0, st, 1, static_cast<const T*>(pre), static_cast<T*>(y),
                                                                  WALK_ARGS, LN_FLAG, mean, inv_std, gamma, beta,
                                                                  act)),
-              (bn_apply_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), static_cast<T*>(y),
+              (launch_k(bn_apply_kernel<T, EC>, wk.G, kBlock, 0, st, 1, static_cast<const T*>(pre), static_cast<T*>(y),
                                                                  WALK_ARGS, LN_FLAG, mean, inv_std, gamma, beta,
                                                                  act)));
   return cudaGetLastError();
@@ -1410,10 +1431,10 @@ cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, con
     return cudaGetLastError();
   }
   DISPATCH_EC(dtype, wk.C,
-              (bn_bwd_reduce_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
+              (launch_k(bn_bwd_reduce_kernel<T, EC>, wk.G, kBlock, 0, st, 1, static_cast<const T*>(pre),
                                                                       static_cast<const T*>(dy), WALK_ARGS, LN_FLAG,
                                                                       mean, inv_std, gamma, beta, act, part)),
-              (bn_bwd_reduce_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
+              (launch_k(bn_bwd_reduce_kernel<T, EC>, wk.G, kBlock, 0, st, 1, static_cast<const T*>(pre),
                                                                       static_cast<const T*>(dy), WALK_ARGS, LN_FLAG,
                                                                       mean, inv_std, gamma, beta, act, part)));
   return cudaGetLastError();
@@ -1421,7 +1442,7 @@ cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, con
 
 cudaError_t launch_sum_finalize(const float* part, const RowWalk& wk, int nv, int mode, float* c12, float* acc0,
                                 float* acc1, cudaStream_t st) {
-  sum_finalize_kernel<<<wk.C, 128, 0, st>>>(part, wk.G, wk.C, nv, mode, c12, acc0, acc1);
+  launch_k(sum_finalize_kernel, wk.C, 128, 0, st, 1, part, wk.G, wk.C, nv, mode, c12, acc0, acc1);
   return cudaGetLastError();
 }
 
@@ -1436,11 +1457,11 @@ cudaError_t launch_bn_bwd_apply(int dtype, const void* pre, const void* dy, cons
   }
   // the vector path needs C == Cp (EC divides C); otherwise one channel per thread
   DISPATCH_EC(dtype, (wk.C == Cp ? wk.C : 1),
-              (dconv_kernel<T, EC, 0><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
+              (launch_k(dconv_kernel<T, EC, 0>, wk.G, kBlock, 0, st, 1, static_cast<const T*>(pre),
                                                                  static_cast<const T*>(dy), wk.seg_rows, wk.bps, wk.C,
                                                                  Cp, wk.rows_per_block, LN_FLAG, mean, inv_std, gamma,
                                                                  beta, act, c12, static_cast<T*>(dconv), part)),
-              (dconv_kernel<T, EC, 0><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
+              (launch_k(dconv_kernel<T, EC, 0>, wk.G, kBlock, 0, st, 1, static_cast<const T*>(pre),
                                                                  static_cast<const T*>(dy), wk.seg_rows, wk.bps, wk.C,
                                                                  Cp, wk.rows_per_block, LN_FLAG, mean, inv_std, gamma,
                                                                  beta, act, c12, static_cast<T*>(dconv), part)));
@@ -1456,12 +1477,12 @@ cudaError_t launch_act_bwd(int dtype, const void* pre, const void* dy, const Row
     return cudaGetLastError();
   }
   DISPATCH_EC(dtype, (wk.C == Cp ? wk.C : 1),
-              (dconv_kernel<T, EC, 1><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
+              (launch_k(dconv_kernel<T, EC, 1>, wk.G, kBlock, 0, st, 1, static_cast<const T*>(pre),
                                                                  static_cast<const T*>(dy), wk.seg_rows, wk.bps, wk.C,
                                                                  Cp, wk.rows_per_block, 0, nullptr, nullptr, nullptr,
                                                                  nullptr, act, nullptr, static_cast<T*>(dconv),
                                                                  part)),
-              (dconv_kernel<T, EC, 1><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre),
+              (launch_k(dconv_kernel<T, EC, 1>, wk.G, kBlock, 0, st, 1, static_cast<const T*>(pre),
                                                                  static_cast<const T*>(dy), wk.seg_rows, wk.bps, wk.C,
                                                                  Cp, wk.rows_per_block, 0, nullptr, nullptr, nullptr,
                                                                  nullptr, act, nullptr, static_cast<T*>(dconv),
@@ -1471,7 +1492,7 @@ cudaError_t launch_act_bwd(int dtype, const void* pre, const void* dy, const Row
 
 cudaError_t launch_ln_stats_finalize(const float* rstats, int n_images, long hw, int n_tiles, int halves, int BN,
                                      int hcols, int OC, float eps, float* mean, float* inv_std, cudaStream_t st) {
-  ln_stats_finalize_kernel<<<n_images, 256, 0, st>>>(rstats, n_tiles, halves, BN, hcols, OC, hw, eps, mean,
+  launch_k(ln_stats_finalize_kernel, n_images, 256, 0, st, 1, rstats, n_tiles, halves, BN, hcols, OC, hw, eps, mean,
                                                      inv_std);
   return cudaGetLastError();
 }
@@ -1480,7 +1501,7 @@ cudaError_t launch_norm_seg_finalize(const float* part, const RowWalk& wk, const
                                      cudaStream_t st) {
   const int n_out = wk.segs * (wk.C / wk.cpg);
   const int wpo = finalize_wpo(static_cast<long>(wk.bps) * wk.cpg), opb = 4 / wpo;
-  norm_seg_finalize_kernel<<<(n_out + opb - 1) / opb, 128, 0, st>>>(part, wk.bps, wk.C, wk.cpg, n_out, wpo, gamma,
+  launch_k(norm_seg_finalize_kernel, (n_out + opb - 1) / opb, 128, 0, st, 1, part, wk.bps, wk.C, wk.cpg, n_out, wpo, gamma,
                                                                      out);
   return cudaGetLastError();
 }
@@ -1493,8 +1514,8 @@ cudaError_t launch_norm_stats(int dtype, const void* pre, const RowWalk& wk, int
     return cudaGetLastError();
   }
   DISPATCH_EC(dtype, wk.C,
-              (norm_stats_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), WALK_ARGS, part)),
-              (norm_stats_kernel<T, EC><<<wk.G, kBlock, 0, st>>>(static_cast<const T*>(pre), WALK_ARGS, part)));
+              (launch_k(norm_stats_kernel<T, EC>, wk.G, kBlock, 0, st, 1, static_cast<const T*>(pre), WALK_ARGS, part)),
+              (launch_k(norm_stats_kernel<T, EC>, wk.G, kBlock, 0, st, 1, static_cast<const T*>(pre), WALK_ARGS, part)));
   return cudaGetLastError();
 }
 
@@ -1502,7 +1523,7 @@ cudaError_t launch_gn_stats_finalize(const float* part, const RowWalk& wk, float
                                      cudaStream_t st) {
   const int n_out = wk.segs * (wk.C / wk.cpg);
   const int wpo = finalize_wpo(static_cast<long>(wk.bps) * wk.cpg), opb = 4 / wpo;
-  gn_stats_finalize_kernel<<<(n_out + opb - 1) / opb, 128, 0, st>>>(part, wk.bps, wk.C, wk.cpg, n_out, wpo, eps,
+  launch_k(gn_stats_finalize_kernel, (n_out + opb - 1) / opb, 128, 0, st, 1, part, wk.bps, wk.C, wk.cpg, n_out, wpo, eps,
                                                                      mean, inv_std);
   return cudaGetLastError();
 }
@@ -1514,11 +1535,11 @@ cudaError_t launch_prep_col2im_weights(int dtype, const void* w, void* bhi, floa
                                        int ICp, int OCp, cudaStream_t st) {
   const int g = grid_for(static_cast<long>(taps) * ICp * OCp, 256);
   if (dtype == 1)
-    prep_col2im_weights_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w),
+    launch_k(prep_col2im_weights_kernel<__nv_bfloat16>, g, 256, 0, st, 1, static_cast<const __nv_bfloat16*>(w),
                                                                  static_cast<__nv_bfloat16*>(bhi), nullptr, OC, taps,
                                                                  IC, ICp, OCp);
   else
-    prep_col2im_weights_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(w), static_cast<float*>(bhi), blo,
+    launch_k(prep_col2im_weights_kernel<float>, g, 256, 0, st, 1, static_cast<const float*>(w), static_cast<float*>(bhi), blo,
                                                          OC, taps, IC, ICp, OCp);
   return cudaGetLastError();
 }
@@ -1526,9 +1547,9 @@ cudaError_t launch_prep_col2im_weights(int dtype, const void* w, void* bhi, floa
 cudaError_t launch_col2im(int dtype, const void* dcol, void* dx, int N, int H, int W, int IC, int ICp, int OH, int OW,
                           int KH, int KW, int S, int P, cudaStream_t st) {
   DISPATCH_EC(dtype, IC,
-              (col2im_kernel<T, EC><<<grid_for(static_cast<long>(N) * H * W * (IC / EC), 256), 256, 0, st>>>(
+              (launch_k(col2im_kernel<T, EC>, grid_for(static_cast<long>(N) * H * W * (IC / EC), 256), 256, 0, st, 1,
                   static_cast<const T*>(dcol), static_cast<T*>(dx), N, H, W, IC, ICp, OH, OW, KH, KW, S, P)),
-              (col2im_kernel<T, EC><<<grid_for(static_cast<long>(N) * H * W * (IC / EC), 256), 256, 0, st>>>(
+              (launch_k(col2im_kernel<T, EC>, grid_for(static_cast<long>(N) * H * W * (IC / EC), 256), 256, 0, st, 1,
                   static_cast<const T*>(dcol), static_cast<T*>(dx), N, H, W, IC, ICp, OH, OW, KH, KW, S, P)));
   return cudaGetLastError();
 }
@@ -1536,20 +1557,20 @@ cudaError_t launch_col2im(int dtype, const void* dcol, void* dx, int N, int H, i
 cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int taps, int ICp, int IC, float* dw,
                                 cudaStream_t st) {
   const int g = grid_for(static_cast<long>(OC) * taps * IC, 256);
-  wgrad_reduce_kernel<<<g, 256, 0, st>>>(partial, splits, OC, taps, ICp, IC, dw);
+  launch_k(wgrad_reduce_kernel, g, 256, 0, st, 1, partial, splits, OC, taps, ICp, IC, dw);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bn_eval_stats(const float* rm, const float* rv, float eps, int C, float* mean, float* inv_std,
                                  cudaStream_t st) {
-  bn_eval_stats_kernel<<<(C + 127) / 128, 128, 0, st>>>(rm, rv, eps, C, mean, inv_std);
+  launch_k(bn_eval_stats_kernel, (C + 127) / 128, 128, 0, st, 1, rm, rv, eps, C, mean, inv_std);
   return cudaGetLastError();
 }
 
 cudaError_t launch_infer_fold(const float* bias, const float* gamma, const float* beta, const float* rm,
                               const float* rv, float eps, int norm, int OC, float* scale, float* shift,
                               cudaStream_t st) {
-  infer_fold_kernel<<<(OC + 127) / 128, 128, 0, st>>>(bias, gamma, beta, rm, rv, eps, norm, OC, scale, shift);
+  launch_k(infer_fold_kernel, (OC + 127) / 128, 128, 0, st, 1, bias, gamma, beta, rm, rv, eps, norm, OC, scale, shift);
   return cudaGetLastError();
 }
 

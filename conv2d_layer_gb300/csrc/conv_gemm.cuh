@@ -344,6 +344,7 @@ __device__ __forceinline__ void store_row32(T* dst, const float (&v)[32], int nc
 // single-CTA and pair tcgen05 forms, hence the separate instantiation.
 template <int DT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_constant__ ConvGemmParams p) {
+  pdl_entry();
   using D = Dt<DT>;
   using T = typename D::T;
   extern __shared__ uint8_t smem_raw[];
@@ -861,6 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
 // 128 rows of A and half of the d_conv columns (BN a multiple of 128).
 template <int DT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_constant__ WgradParams p) {
+  pdl_entry();
   using D = Dt<DT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

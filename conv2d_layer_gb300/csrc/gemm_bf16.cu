@@ -9,26 +9,14 @@ cudaError_t launch_conv_gemm_bf16(const ConvGemmParams& p, int grid, size_t smem
     cudaError_t e = cudaFuncSetAttribute(conv_gemm_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    conv_gemm_kernel<1, false><<<grid, kThreads, smem, st>>>(p);
+    launch_k(conv_gemm_kernel<1, false>, grid, kThreads, smem, st, 1, p);
     return cudaGetLastError();
   }
   // CTA pairs: clusters of two (grid even)
   cudaError_t e = cudaFuncSetAttribute(conv_gemm_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, conv_gemm_kernel<1, true>, p);
+  return launch_k(conv_gemm_kernel<1, true>, grid, kThreads, smem, st, 2, p);
 }
 
 int conv_gemm_pair_clusters(size_t smem) {
@@ -72,15 +60,13 @@ cudaError_t launch_wgrad_gemm_bf16(const WgradParams& p, int grid, size_t smem, 
     cudaError_t e = cudaFuncSetAttribute(wgrad_gemm_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    wgrad_gemm_kernel<1, false><<<grid, kThreads, smem, st>>>(p);
+    launch_k(wgrad_gemm_kernel<1, false>, grid, kThreads, smem, st, 1, p);
     return cudaGetLastError();
   }
   cudaError_t e = cudaFuncSetAttribute(wgrad_gemm_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute at[1];
-  const cudaLaunchConfig_t cfg = pair_config(grid, smem, st, at);
-  return cudaLaunchKernelEx(&cfg, wgrad_gemm_kernel<1, true>, p);
+  return launch_k(wgrad_gemm_kernel<1, true>, grid, kThreads, smem, st, 2, p);
 }
 
 int wgrad_gemm_pair_clusters(size_t smem) {

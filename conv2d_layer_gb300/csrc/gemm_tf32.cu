@@ -8,7 +8,7 @@ cudaError_t launch_conv_gemm_tf32(const ConvGemmParams& p, int grid, size_t smem
   cudaError_t e = cudaFuncSetAttribute(conv_gemm_kernel<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  conv_gemm_kernel<0, false><<<grid, kThreads, smem, st>>>(p);
+  launch_k(conv_gemm_kernel<0, false>, grid, kThreads, smem, st, 1, p);
   return cudaGetLastError();
 }
 
@@ -16,7 +16,7 @@ cudaError_t launch_wgrad_gemm_tf32(const WgradParams& p, int grid, size_t smem, 
   cudaError_t e = cudaFuncSetAttribute(wgrad_gemm_kernel<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  wgrad_gemm_kernel<0, false><<<grid, kThreads, smem, st>>>(p);
+  launch_k(wgrad_gemm_kernel<0, false>, grid, kThreads, smem, st, 1, p);
   return cudaGetLastError();
 }
 

@@ -362,6 +362,14 @@ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
   return (__umulhi(n, f.mul) + n) >> f.shr;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel is launched with programmatic stream serialization (launch_k): its blocks may be
+// scheduled as the blocks of the kernel before it in the stream exit, and it waits here for that
+// kernel's completion and memory before any global-memory access (without the launch attribute the
+// wait does nothing). No kernel releases its successor earlier (griddepcontrol.launch_dependents):
+// successor blocks waiting on the SMs from a kernel's start slowed the kernels they shared SMs with.
+__device__ __forceinline__ void pdl_entry() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- activations
 // 0 identity, 1 relu, 2 tanh, 3 sigmoid; derivative at the activation input.
 // fast (layers stored in bf16): tanh by the hardware's approximate instruction (tanh.approx.f32,
