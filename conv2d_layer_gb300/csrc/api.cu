@@ -335,7 +335,8 @@ WgradPlan wgrad_plan(const Geo& g, int sms) {
     w.n_tiles = static_cast<int>(ceil_div(g.OC, 256));
     w.BN = static_cast<int>(round_up(ceil_div(g.OC, w.n_tiles), 64));
   } else {
-    w.n_tiles = static_cast<int>(ceil_div(g.OC, 128));
+    // at most 64 columns: the fp32 producers keep two k-blocks of X and one of d_conv in registers
+    w.n_tiles = static_cast<int>(ceil_div(g.OC, 64));
     w.BN = static_cast<int>(round_up(ceil_div(g.OC, w.n_tiles), 32));
   }
   w.KP = bf ? 64 : 32;

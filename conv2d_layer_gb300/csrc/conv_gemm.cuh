@@ -1161,26 +1161,50 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
           dhs[i] = kh - p.P;
           dws[i] = (tap - kh * p.KW) - p.P;
         }
-        for (int kb = kb0; kb < kb1; ++kb) {
+        // the X loads of k-block kb + 1 are issued before k-block kb is split and stored, and the d_conv
+        // loads of k-block kb before its X values are, so that their latency overlaps that work
+        constexpr int kBv = 4;  // B float4 per thread: BN / 16 <= 4 (BN <= 64 in fp32 mode)
+        auto pix_of = [&](int kb, int& n, int& oh, int& ow) {
           const int pix = kb * KP + pc;
-          const bool okp = pix < p.n_pix;
-          int n = 0, oh = 0, ow = 0;
+          const bool okp = kb < kb1 && pix < p.n_pix;
+          n = oh = ow = 0;
           if (okp) {
             n = static_cast<int>(fdiv(static_cast<uint32_t>(pix), p.div_OHOW));
             const int rem = pix - n * p.OH * p.OW;
             oh = static_cast<int>(fdiv(static_cast<uint32_t>(rem), p.div_OW));
             ow = rem - oh * p.OW;
           }
-          float4 av[8];
+          return okp;
+        };
+        auto load_a = [&](int kb, float4 (&a)[8]) {
+          int n, oh, ow;
+          const bool okp = pix_of(kb, n, oh, ow);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int ih = oh * p.S + dhs[i], iw = ow * p.S + dws[i];
             const bool ok = okp && oks[i] && static_cast<unsigned>(ih) < static_cast<unsigned>(p.H) &&
                             static_cast<unsigned>(iw) < static_cast<unsigned>(p.W);
-            av[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (ok)
-              av[i] = __ldg(reinterpret_cast<const float4*>(
+              a[i] = __ldg(reinterpret_cast<const float4*>(
                   xs + ((static_cast<size_t>(n * p.H + ih) * p.W + iw) * p.Cs + cs[i]) * 4));
+          }
+        };
+        float4 av[8];
+        load_a(kb0, av);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          float4 an[8], bv[kBv];
+          load_a(kb + 1, an);  // past kb1: zeros, no memory access
+          {
+            const int pix = kb * KP + pc;
+            const bool okp = pix < p.n_pix;
+#pragma unroll
+            for (int j = 0; j < kBv; ++j) {
+              const int oc = n_tile * BN + 4 * (g0 + 4 * j);
+              bv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (okp && 4 * (g0 + 4 * j) < BN && oc < p.OCp)
+                bv[j] = __ldg(reinterpret_cast<const float4*>(p.dc32 + static_cast<size_t>(pix) * p.OCp + oc));
+            }
           }
           if (!__all_sync(0xffffffffu, wait(&empty[s], par ^ 1, p.err, kSiteEmpty))) {  // warp-uniform
             alive = false;
@@ -1202,12 +1226,11 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
               st_shared_b32(addr + a_bytes, lo);
             }
           }
-          for (int gb = g0; gb < BN / 4; gb += 4) {
-            const int oc = n_tile * BN + 4 * gb;
-            float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (okp && oc < p.OCp)
-              bv = __ldg(reinterpret_cast<const float4*>(p.dc32 + static_cast<size_t>(pix) * p.OCp + oc));
-            const float vv[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+          for (int j = 0; j < kBv; ++j) {
+            const int gb = g0 + 4 * j;
+            if (4 * gb >= BN) break;  // uniform across the warp
+            const float vv[4] = {bv[j].x, bv[j].y, bv[j].z, bv[j].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int rr = 4 * gb + e;
@@ -1225,6 +1248,8 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
             s = 0;
             par ^= 1;
           }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) av[i] = an[i];
         }
       }
     }
