@@ -170,22 +170,27 @@ EncodeIm2colFn encode_im2col_fn() {
 // (y*stride + lo_h, x*stride + lo_w); `up_h`, `up_w` place the last corner at
 // (H-1+up_h, W-1+up_w). Returns false when a corner offset is outside the
 // [-128, 127] range the 4-D form supports, or encoding fails.
+// im2col map of an NHWC tensor of dtype dt: one 128-byte channel chunk (64 bf16 / 32 fp32) x `pixels`
+// rows per copy, 128-byte swizzle.
 bool encode_im2col(CUtensorMap* m, const void* base, int N, int H, int W, int C, int lo_h, int lo_w, int up_h,
-                   int up_w, int stride, int pixels) {
+                   int up_w, int stride, int pixels, int dt = CONV2D_BF16) {
   EncodeIm2colFn fn = encode_im2col_fn();
   if (!fn) return false;
   for (int v : {lo_h, lo_w, up_h, up_w})
     if (v < -128 || v > 127) return false;
+  const bool bf = dt == CONV2D_BF16;
+  const cuuint64_t es = bf ? 2 : 4;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(N)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(C) * 2, static_cast<cuuint64_t>(W) * C * 2,
-                           static_cast<cuuint64_t>(H) * W * C * 2};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(C) * es, static_cast<cuuint64_t>(W) * C * es,
+                           static_cast<cuuint64_t>(H) * W * C * es};
   int lower[2] = {lo_w, lo_h};
   int upper[2] = {up_w, up_h};
   cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(stride), static_cast<cuuint32_t>(stride), 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, lower, upper, 64,
-            static_cast<cuuint32_t>(pixels), estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base),
+            dims, strides, lower, upper, bf ? 64 : 32, static_cast<cuuint32_t>(pixels), estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ------------------------------------------------------------ geometry
@@ -386,8 +391,8 @@ struct DgradPlan {
   Tile tile;
 };
 
-// dgrad through TMA im2col: stride 1, bf16, whole 64-channel chunks of d_conv.
-bool dgrad_tma(const Geo& g) { return g.dt == CONV2D_BF16 && g.S == 1 && g.OCp % 64 == 0; }
+// dgrad through TMA im2col: stride 1, whole 128-byte channel chunks of d_conv (64 bf16 / 32 fp32).
+bool dgrad_tma(const Geo& g) { return g.S == 1 && g.OCp % g.BKE == 0; }
 
 DgradPlan dgrad_plan(const Geo& g) {
   DgradPlan d;
@@ -566,11 +571,12 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   p.out_act = out_act;
   p.stats = stats;
   p.rstats = rstats;
-  if (bf && g.ICp % 64 == 0 &&
+  // A by TMA im2col when the channels come in whole 128-byte chunks (64 bf16 / 32 fp32)
+  if (g.ICp % g.BKE == 0 &&
       encode_im2col(&p.tmap_a, xsrc, g.N, g.H, g.W, g.ICp, -g.P, -g.P, (g.OH - 1) * g.S - g.P - (g.H - 1),
-                    (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, kBM)) {
+                    (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, kBM, g.dt)) {
     p.a_tma = 1;
-    p.a_chunks = g.ICp / 64;
+    p.a_chunks = g.ICp / g.BKE;
     p.a_qh = -g.P;
     p.a_qw = -g.P;
   }
@@ -579,10 +585,11 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   set_chunks(p, g, t.BN, ph.num_kb);
   if (bf && t.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
   if (rs_layout) {
+    const bool ep8 = bf && p.a_tma;  // the kernel's eight-warp epilogue splits the columns in two halves
     rs_layout->n_tiles = t.n_tiles;
-    rs_layout->halves = p.a_tma ? 2 : 1;
+    rs_layout->halves = ep8 ? 2 : 1;
     rs_layout->BN = t.BN;
-    rs_layout->hcols = p.a_tma ? 32 * ((t.BN / 32 + 1) / 2) : t.BN;  // the kernel's column split
+    rs_layout->hcols = ep8 ? 32 * ((t.BN / 32 + 1) / 2) : t.BN;
   }
   int grid = std::min(p.num_units, dev->sms);
   if (bf) try_pair(p, t, g, dev, ceil_div(g.n_pix, kBM), bhi, g.Kf, g.OC, &grid);
@@ -661,10 +668,10 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
     // flipped kernel indices, matching the flipped weight columns
     const int lo_h = g.P - g.KH + 1, lo_w = g.P - g.KW + 1;
     if (!encode_im2col(&p.tmap_a, dconv, g.N, g.OH, g.OW, g.OCp, lo_h, lo_w, (g.H - 1) + lo_h - (g.OH - 1),
-                       (g.W - 1) + lo_w - (g.OW - 1), 1, kBM))
+                       (g.W - 1) + lo_w - (g.OW - 1), 1, kBM, g.dt))
       return CONV2D_ERR_CUDA;
     p.a_tma = 1;
-    p.a_chunks = g.OCp / 64;
+    p.a_chunks = g.OCp / g.BKE;
     p.a_qh = lo_h;
     p.a_qw = lo_w;
   }

@@ -94,13 +94,14 @@ struct ConvGemmParams {
   float* rstats;          // optional layer-norm partials of the stored value, one per output pixel,
                           // column tile and epilogue column half (two halves when a_tma, else one):
                           // [pixel][n_tiles][halves][2] = (mean, M2) over the half's columns
-  // A operand by TMA im2col (bf16, Cs a multiple of 64, one phase): the map
-  // walks the row domain; a k-block is (tap, 64-channel chunk) and the tap is
-  // the im2col offset, so taps must be non-negative offsets from the window
-  // corner (dgrad uses tap-flipped weights for this)
+  // A operand by TMA im2col (Cs a multiple of one 128-byte channel chunk: 64 bf16 or 32 fp32, one
+  // phase): the map walks the row domain; a k-block is (tap, channel chunk) and the tap is the im2col
+  // offset, so taps must be non-negative offsets from the window corner (dgrad uses tap-flipped
+  // weights for this). fp32: the raw values land in the hi tile and the four producer warps split
+  // each stage into tf32 hi / lo before the MMA may read it
   CUtensorMap tmap_a;
   int a_tma;
-  int a_chunks;           // Cs / 64
+  int a_chunks;           // Cs / channels per chunk
   int a_qh, a_qw;         // window corner of row (a, b): (a*rs + a_qh, b*rs + a_qw)
   int stages;
   // fp32 (3xTF32) only: the K loop of a tile accumulates in nch chunks of kpc k-blocks, each in its own
@@ -361,8 +362,13 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
   uint64_t* empty = full + kMaxStages;
   uint64_t* tfull = empty + kMaxStages;
   uint64_t* tempty = tfull + kMaxTmemBufs;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + kMaxTmemBufs);
+  uint64_t* sfull = tempty + kMaxTmemBufs;  // fp32 with A by TMA: the stage is split into hi / lo
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfull + kMaxStages);
   const uint32_t sbase = smem_u32(smem);
+  // fp32 with A by TMA: warps 2-5 split the stages (and the epilogue keeps four warps)
+  const bool split_a = DT == 0 && p.a_tma;
+  // epilogue of eight warps (warps 2-9) when the gather warps are free: bf16 with A by TMA
+  const bool ep8 = DT == 1 && p.a_tma;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = pair ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;  // issues the MMAs of the pair
@@ -386,8 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     for (int b = 0; b < nbuf; ++b) {
       mbar_init(&tfull[b], 1);
       // one arrival per epilogue warp (of both CTAs when paired: the even CTA's MMA writes both TMEMs)
-      mbar_init(&tempty[b], (p.a_tma ? 8 : 4) * (pair ? 2 : 1));
+      mbar_init(&tempty[b], (ep8 ? 8 : 4) * (pair ? 2 : 1));
     }
+    if (split_a)
+      for (int s = 0; s < S; ++s) mbar_init(&sfull[s], 4);  // one arrival per splitting warp
     fence_mbar_init();
     tma_prefetch_desc(&p.tmap_b);
     if (D::NS == 2) tma_prefetch_desc(&p.tmap_b_lo);
@@ -441,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
             if (leader) mbar_arrive_expect_tx(&full[s], 2 * (a_bytes + b_own));
             const int tap = kb / p.a_chunks;
             const int tt = static_cast<int>(fdiv(static_cast<uint32_t>(tap), ph.div_Tw));
-            tma_load_im2col_4d_pair(a0, &p.tmap_a, bar, (kb - tap * p.a_chunks) * 64, aw, ah, an,
+            tma_load_im2col_4d_pair(a0, &p.tmap_a, bar, (kb - tap * p.a_chunks) * D::BKE, aw, ah, an,
                                     static_cast<uint16_t>(tap - tt * ph.Tw), static_cast<uint16_t>(tt));
             tma_load_2d_pair(b0, &p.tmap_b, bar, ph.b_col + kb * D::BKE,
                              n_tile * BN + static_cast<int>(rank) * (BN / 2));
@@ -450,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
             if (p.a_tma) {
               const int tap = kb / p.a_chunks;
               const int tt = static_cast<int>(fdiv(static_cast<uint32_t>(tap), ph.div_Tw));
-              tma_load_im2col_4d(a0, &p.tmap_a, &full[s], (kb - tap * p.a_chunks) * 64, aw, ah, an,
+              tma_load_im2col_4d(a0, &p.tmap_a, &full[s], (kb - tap * p.a_chunks) * D::BKE, aw, ah, an,
                                  static_cast<uint16_t>(tap - tt * ph.Tw), static_cast<uint16_t>(tt));
             }
             tma_load_2d(b0, &p.tmap_b, &full[s], ph.b_col + kb * D::BKE, n_tile * BN);
@@ -491,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         for (int kb = 0; kb < ph.num_kb; ++kb) {
           const uint32_t d = DT == 0 ? dt + static_cast<uint32_t>((kb / kpc) * BN) : dt;
           const int kc = DT == 0 ? kb % kpc : kb;  // k-block within the accumulator chunk
-          if (!wait(&full[s], par, p.err, kSiteFull)) {
+          if (!wait(split_a ? &sfull[s] : &full[s], par, p.err, kSiteFull)) {
             alive = false;
             break;
           }
@@ -636,17 +644,58 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         if (lane == 0) mbar_arrive(&full[q % S]);
       }
     }
+  } else if (warp < 6 && split_a) {
+    // ------------------------------------------------ fp32 stage split (A by TMA)
+    // each thread splits its eight 16-byte chunks of the stage's A tile in place: hi stays, lo goes
+    // to the lo tile (the chunk layout of the TMA's 128-byte swizzle does not matter to an
+    // element-wise split)
+    const int t = threadIdx.x - 64;
+    const int j = t & 7, r0 = t >> 3;
+    const uint32_t swz = static_cast<uint32_t>((j ^ (r0 & 7)) << 4);
+    int s = 0;
+    uint32_t par = 0;
+    bool alive = true;
+    for (int u = cid; u < p.num_units && alive; u += ncl) {
+      const ConvPhase& ph = find_phase(p, u);
+      for (int kb = 0; kb < ph.num_kb; ++kb) {
+        if (!__all_sync(0xffffffffu, wait(&full[s], par, p.err, kSiteFull))) {  // warp-uniform
+          alive = false;
+          break;
+        }
+        const uint32_t a0 = sbase + s * stage_bytes;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t dst = a0 + (r0 + 16 * i) * 128 + swz;
+          uint32_t x0, x1, x2, x3;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3) : "r"(dst));
+          uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+          split_tf32(__uint_as_float(x0), h0, l0);
+          split_tf32(__uint_as_float(x1), h1, l1);
+          split_tf32(__uint_as_float(x2), h2, l2);
+          split_tf32(__uint_as_float(x3), h3, l3);
+          st_shared_v4(dst, h0, h1, h2, h3);
+          st_shared_v4(dst + a_bytes, l0, l1, l2, l3);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[s]);
+        if (++s == S) {
+          s = 0;
+          par ^= 1;
+        }
+      }
+    }
   } else {
     // ------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
-    // Epilogue warps: 6-9, or 2-9 when the A operand comes by TMA (the gather warps are free then).
+    // Epilogue warps: 6-9, or 2-9 for bf16 with the A operand by TMA (the gather warps are free then).
     // Warp w reads TMEM lane quarter w & 3; with eight warps the two warps of a quarter split the
     // tile's 32-column chunks in two halves [cb, ce).
-    const int nthr = p.a_tma ? 256 : 128;
+    const int nthr = ep8 ? 256 : 128;
     const int et = threadIdx.x - (kThreads - nthr);  // 0 .. nthr-1 within the epilogue warps
-    const int half = p.a_tma ? (warp - 2) / 4 : 0;
-    const int hcols = p.a_tma ? 32 * ((BN / 32 + 1) / 2) : BN;
+    const int half = ep8 ? (warp - 2) / 4 : 0;
+    const int hcols = ep8 ? 32 * ((BN / 32 + 1) / 2) : BN;
     const int cb = half * hcols, ce = half ? BN : hcols;
     T* out = static_cast<T*>(p.out);
     T* out2 = static_cast<T*>(p.out2);
@@ -778,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         if (c0 + 32 < ce) pass1(c0 + 32, rb);
       }
       if (p.rstats && valid) {
-        const int nh = p.a_tma ? 2 : 1;
+        const int nh = ep8 ? 2 : 1;
         float* o = p.rstats + ((obase / p.out_ld * p.n_tiles + n_tile) * nh + half) * 2;
         o[0] = rmean;
         o[1] = rm2;
