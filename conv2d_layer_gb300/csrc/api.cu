@@ -328,8 +328,13 @@ bool try_pair(ConvGemmParams& p, Tile& t, const Geo& g, const DevInfo* dev, long
 
 struct WgradPlan {
   int Mk, m_tiles, BN, n_tiles, KP, kb_total, kb_per_split, splits, stages, units;
+  int rstages;  // fp32 with X by TMA: raw-tile ring
   size_t smem;
 };
+
+// fp32 weight gradient with X and d_conv by TMA (raw tiles transposed by the producer warps): the
+// channels come in whole 32-float chunks.
+bool wgrad_raw_tma(const Geo& g) { return g.dt != CONV2D_BF16 && g.ICp % 32 == 0; }
 
 WgradPlan wgrad_plan(const Geo& g, int sms) {
   WgradPlan w;
@@ -377,8 +382,17 @@ WgradPlan wgrad_plan(const Geo& g, int sms) {
   w.units = base * w.splits;
   const size_t ns = bf ? 1 : 2;
   const size_t stage = ns * (kBM * 128 + static_cast<size_t>(w.BN) * 128);
+  w.rstages = 0;
+  if (wgrad_raw_tma(g)) {
+    // two hi / lo stages for the MMA, the rest of shared memory for raw tiles in flight
+    const size_t raw = kBM * 128 + static_cast<size_t>(w.BN) * 128;
+    w.stages = 2;
+    w.rstages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048 - 2 * stage) / raw));
+    w.smem = 2 * stage + w.rstages * raw + 1024 + 512;
+    return w;
+  }
   w.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048) / stage));
-  w.smem = w.stages * stage + 1024 + 256;
+  w.smem = w.stages * stage + 1024 + 512;  // alignment slack; barriers and the TMEM slot
   return w;
 }
 
@@ -727,6 +741,14 @@ int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dc
       encode_im2col(&p.tmap_x, xsrc, g.N, g.H, g.W, g.ICp, -g.P, -g.P, (g.OH - 1) * g.S - g.P - (g.H - 1),
                     (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, w.KP))
     p.a_tma = 1;
+  if (wgrad_raw_tma(g)) {
+    if (!encode_im2col(&p.tmap_x, xsrc, g.N, g.H, g.W, g.ICp, -g.P, -g.P, (g.OH - 1) * g.S - g.P - (g.H - 1),
+                       (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, w.KP, g.dt) ||
+        !encode_2d(&p.tmap_dc, dconv, false, g.OCp, g.n_pix, 32, 32))
+      return CONV2D_ERR_CUDA;
+    p.a_tma = 1;
+    p.rstages = w.rstages;
+  }
   p.stages = w.stages;
   p.err = dev->err;
   if (bf && w.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
@@ -736,7 +758,7 @@ int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dc
   if (kUsePair && bf && p.a_tma && (w.m_tiles % 2) == 0 && w.BN % 128 == 0) {
     const size_t stage = kBM * 128 + static_cast<size_t>(w.BN / 2) * 128;
     const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048) / stage));
-    const size_t psmem = stages * stage + 1024 + 256;
+    const size_t psmem = stages * stage + 1024 + 512;
     static std::mutex mu;
     static size_t cached_smem = 0;
     static int cached_clusters = 0;

@@ -113,8 +113,11 @@ struct ConvGemmParams {
 
 struct WgradParams {
   CUtensorMap tmap_dc;    // bf16 d_conv [n_pix][OCp], box {64 ch, 64 pix}
-  CUtensorMap tmap_x;     // bf16 im2col map of X, 64 pixels x 64 channels (when a_tma)
-  int a_tma;              // A panels by TMA im2col (bf16, Cs a multiple of 64)
+  CUtensorMap tmap_x;     // im2col map of X (when a_tma): bf16 64 pixels x 64 channels, fp32 32 x 32
+  int a_tma;              // A by TMA im2col (Cs a multiple of 64 bf16 / 32 fp32). fp32: X and d_conv
+                          // land as raw pixel-major tiles in a ring of rstages and the producer
+                          // warps transpose them into tf32 hi / lo K-major stages
+  int rstages;
   const void* x;          // NHWC [Nimg][H][W][Cs]
   const float* dc32;      // fp32 d_conv [n_pix][OCp] (fp32 mode)
   int H, W, Cs, OH, OW, S, P, KW;
@@ -922,12 +925,20 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
   const uint32_t b_own = pair ? b_bytes / 2 : b_bytes;  // a pair member holds half of the oc columns
   const uint32_t stage_bytes = D::NS * (a_bytes + b_own);
   const int S = p.stages;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_bytes);
+  // fp32 with X by TMA: a ring of raw tiles (X chunks then d_conv chunks, 32 pixel rows x 128 B each)
+  const bool raw_a = DT == 0 && p.a_tma;
+  const int NR = raw_a ? p.rstages : 0;
+  const uint32_t raw_bytes = a_bytes + b_bytes;
+  uint8_t* rawp = smem + S * stage_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(rawp + NR * raw_bytes);
   uint64_t* empty = full + kMaxStages;
   uint64_t* tfull = empty + kMaxStages;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* rfull = tempty + 2;
+  uint64_t* rempty = rfull + kMaxStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rempty + kMaxStages);
   const uint32_t sbase = smem_u32(smem);
+  const uint32_t rbase = smem_u32(rawp);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t tcols = tmem_cols_for(2 * BN);
   constexpr int KP = (DT == 1) ? 64 : 32;  // pixels per k-block
@@ -945,8 +956,12 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], pair ? 8 : 4);  // epilogue warps (of both CTAs when paired)
     }
+    for (int r = 0; r < NR; ++r) {
+      mbar_init(&rfull[r], 1);   // the TMA thread
+      mbar_init(&rempty[r], 4);  // one arrival per transposing warp
+    }
     fence_mbar_init();
-    if (DT == 1) tma_prefetch_desc(&p.tmap_dc);
+    if (DT == 1 || raw_a) tma_prefetch_desc(&p.tmap_dc);
     if (p.a_tma) tma_prefetch_desc(&p.tmap_x);
   }
   if (warp == 1) {
@@ -1057,6 +1072,52 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
           if (++s == S) {
             s = 0;
             par ^= 1;
+          }
+        }
+      }
+    }
+    if (raw_a && lane == 0) {
+      // ------------------------------------------------ fp32: raw X and d_conv tiles by TMA
+      int r = 0;
+      uint32_t rpar = 0;
+      bool alive = true;
+      for (int u = cid; u < p.num_units && alive; u += ncl) {
+        int m_tile, n_tile, kb0, kb1;
+        decode(u, m_tile, n_tile, kb0, kb1);
+        // X chunks: 32 k-rows (one tap, 32 channels) each; past Mk not loaded (those rows are discarded)
+        int pc[4], pkw[4], pkh[4];
+        uint32_t tx = static_cast<uint32_t>(BN / 32) * 4096u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int kc = m_tile * kBM + 32 * c;
+          const int tap = static_cast<int>(fdiv(static_cast<uint32_t>(kc), p.div_Cs));
+          pkh[c] = static_cast<int>(fdiv(static_cast<uint32_t>(tap), p.div_KW));
+          pkw[c] = tap - pkh[c] * p.KW;
+          pc[c] = kc < p.Mk ? kc - tap * p.Cs : -1;
+          if (pc[c] >= 0) tx += 4096u;
+        }
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait(&rempty[r], rpar ^ 1, p.err, kSiteEmpty)) {
+            alive = false;
+            break;
+          }
+          const uint32_t r0 = rbase + r * raw_bytes;
+          mbar_arrive_expect_tx(&rfull[r], tx);
+          const int pix = kb * KP;  // first pixel of the k-block; the maps walk the next 32
+          const int n = static_cast<int>(fdiv(static_cast<uint32_t>(pix), p.div_OHOW));
+          const int rem = pix - n * p.OH * p.OW;
+          const int oh = static_cast<int>(fdiv(static_cast<uint32_t>(rem), p.div_OW));
+          const int ow = rem - oh * p.OW;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (pc[c] >= 0)
+              tma_load_im2col_4d(r0 + c * 4096, &p.tmap_x, &rfull[r], pc[c], ow * p.S - p.P, oh * p.S - p.P, n,
+                                 static_cast<uint16_t>(pkw[c]), static_cast<uint16_t>(pkh[c]));
+          for (int jn = 0; jn < BN / 32; ++jn)
+            tma_load_2d(r0 + a_bytes + jn * 4096, &p.tmap_dc, &rfull[r], n_tile * BN + 32 * jn, pix);
+          if (++r == NR) {
+            r = 0;
+            rpar ^= 1;
           }
         }
       }
@@ -1190,6 +1251,79 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
       __syncwarp();
       if (alive && lane == 0)
         for (int q2 = (it > kLag ? it - kLag : 0); q2 < it; ++q2) mbar_arrive(&full[q2 % S]);
+    } else if (raw_a) {
+      // ------------------------------------------------ fp32: transpose the raw tiles into tf32 hi / lo
+      // A raw chunk is 32 pixel rows x 32 channels (128-byte swizzle as the TMA wrote it); the stage wants
+      // K-major rows of 32 pixels per channel. A warp iteration takes half a chunk: lane (pq, cq) reads the
+      // 4 x 4 block of pixels 4pq.. and channels 4cq.. (four 16-byte reads), splits it and writes four
+      // channel rows of four pixels to the hi and lo tiles (both sides spread over all banks).
+      const int wi = warp - 2;
+      const int pq = lane & 7, cql = lane >> 3;
+      int r = 0;
+      uint32_t rpar = 0;
+      const int nchunk = 4 + BN / 32;
+      for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
+        int m_tile, n_tile, kb0, kb1;
+        decode(u, m_tile, n_tile, kb0, kb1);
+        (void)n_tile;
+        const int nvalid = min(4, (p.Mk - m_tile * kBM + 31) / 32);  // X chunks inside Mk
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!__all_sync(0xffffffffu, wait(&rfull[r], rpar, p.err, kSiteFull) &&
+                                           wait(&empty[s], par ^ 1, p.err, kSiteEmpty))) {  // warp-uniform
+            alive = false;
+            break;
+          }
+          const uint32_t r0 = rbase + r * raw_bytes;
+          const uint32_t a0 = sbase + s * stage_bytes;
+          const uint32_t b0 = a0 + 2 * a_bytes;
+          for (int it = wi; it < 2 * nchunk; it += 4) {
+            const int c = it >> 1;
+            if (c < 4 && c >= nvalid) continue;  // uniform across the warp
+            const int cq = cql + 4 * (it & 1);
+            const bool isa = c < 4;
+            const uint32_t src = isa ? r0 + c * 4096 : r0 + a_bytes + (c - 4) * 4096;
+            const uint32_t hi = isa ? a0 + c * 4096 : b0 + (c - 4) * 4096;
+            const uint32_t lo_off = isa ? a_bytes : b_bytes;
+            float v[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int px = 4 * pq + i;
+              uint32_t x0, x1, x2, x3;
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                           : "r"(src + px * 128 + ((cq ^ (px & 7)) << 4)));
+              v[i][0] = __uint_as_float(x0);
+              v[i][1] = __uint_as_float(x1);
+              v[i][2] = __uint_as_float(x2);
+              v[i][3] = __uint_as_float(x3);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int row = 4 * cq + e;  // channel row within the chunk (the chunk starts on an 8-row atom)
+              const uint32_t addr = hi + row * 128 + ((pq ^ (row & 7)) << 4);
+              uint32_t h[4], l[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) split_tf32(v[i][e], h[i], l[i]);
+              st_shared_v4(addr, h[0], h[1], h[2], h[3]);
+              st_shared_v4(addr + lo_off, l[0], l[1], l[2], l[3]);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&full[s]);
+            mbar_arrive(&rempty[r]);
+          }
+          if (++r == NR) {
+            r = 0;
+            rpar ^= 1;
+          }
+          if (++s == S) {
+            s = 0;
+            par ^= 1;
+          }
+        }
+      }
     } else {
       // ------------------------------------------------ A and B producers, fp32 -> tf32 hi/lo, K-major
       // A smem rows: k (128), 32 pixel columns; B smem rows: oc (BN), 32 pixel columns.
