@@ -176,13 +176,29 @@ __device__ __forceinline__ void ep_columns(const uint32_t (&r)[32], bool zero, b
                                            const float* sh, float (&v)[32]) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    float b[16], a[16];
+    float b[16];
     lds16(sh + 16 * h, b);
-    if (has_scale) lds16(sc + 16 * h, a);
+    if (zero) {  // no k-block reached the accumulator: v = shift (uniform branches below)
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const float x = zero ? 0.f : __uint_as_float(r[16 * h + e]);
-      v[16 * h + e] = has_scale ? fmaf(x, a[e], b[e]) : x + b[e];
+      for (int e = 0; e < 16; ++e) v[16 * h + e] = b[e];
+    } else if (has_scale) {
+      float a[16];
+      lds16(sc + 16 * h, a);
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[16 * h + e]), __uint_as_float(r[16 * h + e + 1])),
+                                    make_float2(a[e], a[e + 1]), make_float2(b[e], b[e + 1]));
+        v[16 * h + e] = x.x;
+        v[16 * h + e + 1] = x.y;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        const float2 x = __fadd2_rn(make_float2(__uint_as_float(r[16 * h + e]), __uint_as_float(r[16 * h + e + 1])),
+                                    make_float2(b[e], b[e + 1]));
+        v[16 * h + e] = x.x;
+        v[16 * h + e + 1] = x.y;
+      }
     }
   }
 }
@@ -795,7 +811,9 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         // already use most of the shared-memory bandwidth)
         float v[32];
         ep_columns(r, zero, p.ep_scale != nullptr, sc_s + cc, sh_s + cc, v);
-        if (valid) {
+        if (valid && !p.out_act && !p.rstats && !out2) {
+          store_row32<T>(out + obase + col0, v, ncols, vec);  // one rounding to T
+        } else if (valid) {
           float o[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = p.out_act ? act_f(p.act, v[e], DT == 1) : to_stored<T>(v[e]);
