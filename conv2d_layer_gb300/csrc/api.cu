@@ -405,8 +405,9 @@ struct DgradPlan {
   Tile tile;
 };
 
-// dgrad through TMA im2col: stride 1, whole 128-byte channel chunks of d_conv (64 bf16 / 32 fp32).
-bool dgrad_tma(const Geo& g) { return g.S == 1 && g.OCp % g.BKE == 0; }
+// dgrad through TMA im2col: stride 1 or 2 (one map per stride phase), whole 128-byte channel chunks of
+// d_conv (64 bf16 / 32 fp32).
+bool dgrad_tma(const Geo& g) { return g.S * g.S <= kMaxTmaPhases && g.OCp % g.BKE == 0; }
 
 DgradPlan dgrad_plan(const Geo& g) {
   DgradPlan d;
@@ -587,12 +588,13 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   p.rstats = rstats;
   // A by TMA im2col when the channels come in whole 128-byte chunks (64 bf16 / 32 fp32)
   if (g.ICp % g.BKE == 0 &&
-      encode_im2col(&p.tmap_a, xsrc, g.N, g.H, g.W, g.ICp, -g.P, -g.P, (g.OH - 1) * g.S - g.P - (g.H - 1),
+      encode_im2col(&p.tmap_a[0], xsrc, g.N, g.H, g.W, g.ICp, -g.P, -g.P, (g.OH - 1) * g.S - g.P - (g.H - 1),
                     (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, kBM, g.dt)) {
     p.a_tma = 1;
     p.a_chunks = g.ICp / g.BKE;
-    p.a_qh = -g.P;
-    p.a_qw = -g.P;
+    ph.a_lo_h = -g.P;
+    ph.a_lo_w = -g.P;
+    ph.a_map = 0;
   }
   p.stages = t.stages;
   p.err = dev->err;
@@ -678,16 +680,23 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
   p.act = 0;
   p.out_act = 0;
   if (d.table.flip) {
-    // window corner of input pixel (ih, iw) in d_conv: (ih - (KH-1-P), iw - (KW-1-P)); tap offsets are the
-    // flipped kernel indices, matching the flipped weight columns
-    const int lo_h = g.P - g.KH + 1, lo_w = g.P - g.KW + 1;
-    if (!encode_im2col(&p.tmap_a, dconv, g.N, g.OH, g.OW, g.OCp, lo_h, lo_w, (g.H - 1) + lo_h - (g.OH - 1),
-                       (g.W - 1) + lo_w - (g.OW - 1), 1, kBM, g.dt))
-      return CONV2D_ERR_CUDA;
+    // One im2col map per stride phase. Phase row (a, b) reads d_conv at (a + qh - tt, b + qw - uu) for
+    // its taps (tt, uu) < (Th, Tw): with the window corner (a + qh - (Th - 1), b + qw - (Tw - 1)) the
+    // tap offsets are the flipped indices (Th - 1 - tt, Tw - 1 - uu), matching the flipped weight
+    // columns, and the map walks the phase's own Ha x Wa grid.
+    for (int i = 0; i < d.num_phases; ++i) {
+      ConvPhase& ph = p.ph[i];
+      const int Th = ph.K / (ph.Tw * g.OCp);
+      ph.a_map = i;
+      ph.a_lo_h = ph.qh - (Th - 1);
+      ph.a_lo_w = ph.qw - (ph.Tw - 1);
+      if (ph.num_kb == 0) continue;  // no taps: nothing is loaded
+      if (!encode_im2col(&p.tmap_a[i], dconv, g.N, g.OH, g.OW, g.OCp, ph.a_lo_h, ph.a_lo_w,
+                         (ph.Ha - 1) + ph.a_lo_h - (g.OH - 1), (ph.Wa - 1) + ph.a_lo_w - (g.OW - 1), 1, kBM, g.dt))
+        return CONV2D_ERR_CUDA;
+    }
     p.a_tma = 1;
     p.a_chunks = g.OCp / g.BKE;
-    p.a_qh = lo_h;
-    p.a_qw = lo_w;
   }
   p.stages = d.tile.stages;
   p.err = dev->err;

@@ -33,6 +33,7 @@ namespace c2d {
 constexpr int kThreads = 320;
 constexpr int kMaxStages = 8;
 constexpr int kMaxPhases = 64;
+constexpr int kMaxTmaPhases = 4;  // stride phases whose A operand may come by TMA im2col
 constexpr int kBM = 128;          // rows of a tile (TMEM lanes)
 constexpr int kMaxTmemBufs = 8;   // TMEM accumulators of the fprop / dgrad kernel (512 columns / BN, capped)
 constexpr int kLag = 3;           // cp.async groups kept in flight per producer thread (needs >= 4 stages)
@@ -68,6 +69,8 @@ struct ConvPhase {
   int unit_begin;      // first work unit of this phase
   int b_col;           // first column of this phase in the B matrix
   int oh0, ow0;        // output pixel = (oh0 + a*os, ow0 + b*os)
+  int a_lo_h, a_lo_w;  // A by TMA im2col: window corner of row (a, b) = (a*rs + a_lo_h, b*rs + a_lo_w)
+  int a_map;           // ... and the index of this phase's im2col map
   FastDiv div_Wa, div_HaWa, div_Tw;
 };
 
@@ -99,10 +102,9 @@ struct ConvGemmParams {
   // offset, so taps must be non-negative offsets from the window corner (dgrad uses tap-flipped
   // weights for this). fp32: the raw values land in the hi tile and the four producer warps split
   // each stage into tf32 hi / lo before the MMA may read it
-  CUtensorMap tmap_a;
+  CUtensorMap tmap_a[kMaxTmaPhases];  // one im2col map per stride phase (dgrad with stride 2: four)
   int a_tma;
   int a_chunks;           // Cs / channels per chunk
-  int a_qh, a_qw;         // window corner of row (a, b): (a*rs + a_qh, b*rs + a_qw)
   int stages;
   // fp32 (3xTF32) only: the K loop of a tile accumulates in nch chunks of kpc k-blocks, each in its own
   // BN TMEM columns, summed by the epilogue (nch * BN <= 512); bf16 uses one chunk
@@ -418,7 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     fence_mbar_init();
     tma_prefetch_desc(&p.tmap_b);
     if (D::NS == 2) tma_prefetch_desc(&p.tmap_b_lo);
-    if (p.a_tma) tma_prefetch_desc(&p.tmap_a);
+    if (p.a_tma)
+      for (int i = 0; i < p.num_phases && i < kMaxTmaPhases; ++i) tma_prefetch_desc(&p.tmap_a[i]);
   }
   if (warp == 1) {
     if (pair) {
@@ -452,8 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           an = static_cast<int>(fdiv(static_cast<uint32_t>(m0), ph.div_HaWa));
           const int rem = m0 - an * ph.Ha * ph.Wa;
           const int a = static_cast<int>(fdiv(static_cast<uint32_t>(rem), ph.div_Wa));
-          ah = a * p.rs + p.a_qh;
-          aw = (rem - a * ph.Wa) * p.rs + p.a_qw;
+          ah = a * p.rs + ph.a_lo_h;
+          aw = (rem - a * ph.Wa) * p.rs + ph.a_lo_w;
         }
         for (int kb = 0; kb < ph.num_kb; ++kb) {
           if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
@@ -468,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
             if (leader) mbar_arrive_expect_tx(&full[s], 2 * (a_bytes + b_own));
             const int tap = kb / p.a_chunks;
             const int tt = static_cast<int>(fdiv(static_cast<uint32_t>(tap), ph.div_Tw));
-            tma_load_im2col_4d_pair(a0, &p.tmap_a, bar, (kb - tap * p.a_chunks) * D::BKE, aw, ah, an,
+            tma_load_im2col_4d_pair(a0, &p.tmap_a[0], bar, (kb - tap * p.a_chunks) * D::BKE, aw, ah, an,
                                     static_cast<uint16_t>(tap - tt * ph.Tw), static_cast<uint16_t>(tt));
             tma_load_2d_pair(b0, &p.tmap_b, bar, ph.b_col + kb * D::BKE,
                              n_tile * BN + static_cast<int>(rank) * (BN / 2));
@@ -477,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
             if (p.a_tma) {
               const int tap = kb / p.a_chunks;
               const int tt = static_cast<int>(fdiv(static_cast<uint32_t>(tap), ph.div_Tw));
-              tma_load_im2col_4d(a0, &p.tmap_a, &full[s], (kb - tap * p.a_chunks) * D::BKE, aw, ah, an,
+              tma_load_im2col_4d(a0, &p.tmap_a[ph.a_map], &full[s], (kb - tap * p.a_chunks) * D::BKE, aw, ah, an,
                                  static_cast<uint16_t>(tap - tt * ph.Tw), static_cast<uint16_t>(tt));
             }
             tma_load_2d(b0, &p.tmap_b, &full[s], ph.b_col + kb * D::BKE, n_tile * BN);

@@ -69,6 +69,12 @@ EDGE_CASES = {
                                           norm=NORM_BATCH, act=ACT_RELU, dtype=BF16),
     "fp32_oc288_k3_bn_ragged": LayerSpec(N=2, H=10, W=9, IC=8, OC=288, KH=3, KW=3, stride=1, pad=1,
                                          norm=NORM_BATCH, act=ACT_IDENTITY, dtype=FP32),
+    # stride-2 dgrad with d_conv by TMA, one im2col map per stride phase (ragged phase grids; 2 x 2 taps
+    # in every phase of the 4 x 4 kernel)
+    "bf16_s2_tma_phases": LayerSpec(N=2, H=13, W=11, IC=64, OC=128, KH=3, KW=3, stride=2, pad=1,
+                                    norm=NORM_BATCH, act=ACT_RELU, dtype=BF16),
+    "bf16_k4s2_tma_phases": LayerSpec(N=2, H=10, W=10, IC=64, OC=64, KH=4, KW=4, stride=2, pad=1,
+                                      norm=NORM_NONE, act=ACT_TANH, dtype=BF16),
     # deep fp32 K loops: the accumulation is split over TMEM chunks (dgrad K = 5184, fprop K = 2304)
     "fp32_deep_dgrad_oc576": LayerSpec(N=2, H=10, W=9, IC=8, OC=576, KH=3, KW=3, stride=1, pad=1,
                                        norm=NORM_BATCH, act=ACT_IDENTITY, dtype=FP32),
