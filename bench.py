@@ -164,6 +164,11 @@ def run_gpu(args, rank, world, local_rank):
         barrier()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if instrumented:
+            # the GPU idles in a ~2 ms sleep kernel before the first event while the host runs ahead, so
+            # that the per-launch events bracket back-to-back kernels
+            with torch.cuda.stream(stream):
+                torch.cuda._sleep(4_000_000)
         e0.record(stream)
         for _ in range(n):
             step()
@@ -303,6 +308,9 @@ def per_config_timing(peaks, steps=10, warmup=3):
         ms = e0.elapsed_time(e1) / steps
         abi.conv2d_prof_enable(True)
         abi.conv2d_prof_read()
+        # the GPU idles in a ~2 ms sleep kernel while the host queues the whole step, so that the per-launch
+        # events bracket back-to-back kernels (not the host's launch work between short kernels)
+        torch.cuda._sleep(4_000_000)
         step()
         torch.cuda.synchronize()
         abi.conv2d_prof_enable(False)
