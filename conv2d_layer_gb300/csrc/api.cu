@@ -171,19 +171,21 @@ EncodeIm2colFn encode_im2col_fn() {
 // (H-1+up_h, W-1+up_w). Returns false when a corner offset is outside the
 // [-128, 127] range the 4-D form supports, or encoding fails.
 // im2col map of an NHWC tensor of dtype dt: one 128-byte channel chunk (64 bf16 / 32 fp32) x `pixels`
-// rows per copy, 128-byte swizzle.
+// rows per copy, 128-byte swizzle. pix (elements from one pixel to the next, default C) smaller than C
+// gives the folded view: "channel" c' of pixel w is element c' of the run starting at pixel w, i.e.
+// channel c' % pix of pixel w + c' / pix.
 bool encode_im2col(CUtensorMap* m, const void* base, int N, int H, int W, int C, int lo_h, int lo_w, int up_h,
-                   int up_w, int stride, int pixels, int dt = CONV2D_BF16) {
+                   int up_w, int stride, int pixels, int dt = CONV2D_BF16, int pix = 0) {
   EncodeIm2colFn fn = encode_im2col_fn();
   if (!fn) return false;
   for (int v : {lo_h, lo_w, up_h, up_w})
     if (v < -128 || v > 127) return false;
   const bool bf = dt == CONV2D_BF16;
   const cuuint64_t es = bf ? 2 : 4;
+  const cuuint64_t P = pix > 0 ? static_cast<cuuint64_t>(pix) : static_cast<cuuint64_t>(C);
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(N)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(C) * es, static_cast<cuuint64_t>(W) * C * es,
-                           static_cast<cuuint64_t>(H) * W * C * es};
+  cuuint64_t strides[3] = {P * es, static_cast<cuuint64_t>(W) * P * es, static_cast<cuuint64_t>(H) * W * P * es};
   int lower[2] = {lo_w, lo_h};
   int upper[2] = {up_w, up_h};
   cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(stride), static_cast<cuuint32_t>(stride), 1};
@@ -334,7 +336,16 @@ struct WgradPlan {
 
 // fp32 weight gradient with X and d_conv by TMA (raw tiles transposed by the producer warps): the
 // channels come in whole 32-float chunks.
-bool wgrad_raw_tma(const Geo& g) { return g.dt != CONV2D_BF16 && g.ICp % 32 == 0; }
+bool wgrad_raw_tma(const Geo& g);
+
+// fp32 layers whose kernel row covers one 128-byte run of X: KW * ICp = 32 floats of KW consecutive
+// pixels (a stride-4, 4-channel, 8-wide kernel). Without horizontal padding the TMA paths read each
+// kernel row as one 32-channel tap of the folded view (see encode_im2col).
+bool fold_kw(const Geo& g) {
+  return g.dt != CONV2D_BF16 && g.P == 0 && g.KW * g.ICp == 32 && g.ICp % 32 != 0;
+}
+
+bool wgrad_raw_tma(const Geo& g) { return g.dt != CONV2D_BF16 && (g.ICp % 32 == 0 || fold_kw(g)); }
 
 WgradPlan wgrad_plan(const Geo& g, int sms) {
   WgradPlan w;
@@ -586,12 +597,24 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   p.out_act = out_act;
   p.stats = stats;
   p.rstats = rstats;
-  // A by TMA im2col when the channels come in whole 128-byte chunks (64 bf16 / 32 fp32)
+  // A by TMA im2col when the channels come in whole 128-byte chunks (64 bf16 / 32 fp32), or through the
+  // folded view (one 32-float run per kernel row: the taps are the KH rows, Tw = 1)
   if (g.ICp % g.BKE == 0 &&
       encode_im2col(&p.tmap_a[0], xsrc, g.N, g.H, g.W, g.ICp, -g.P, -g.P, (g.OH - 1) * g.S - g.P - (g.H - 1),
                     (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, kBM, g.dt)) {
     p.a_tma = 1;
     p.a_chunks = g.ICp / g.BKE;
+    ph.a_lo_h = -g.P;
+    ph.a_lo_w = -g.P;
+    ph.a_map = 0;
+  } else if (fold_kw(g) &&
+             encode_im2col(&p.tmap_a[0], xsrc, g.N, g.H, g.W, g.KW * g.ICp, -g.P, -g.P,
+                           (g.OH - 1) * g.S - g.P - (g.H - 1), (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, kBM, g.dt,
+                           g.ICp)) {
+    p.a_tma = 1;
+    p.a_chunks = 1;
+    ph.Tw = 1;
+    ph.div_Tw = make_fastdiv(1);
     ph.a_lo_h = -g.P;
     ph.a_lo_w = -g.P;
     ph.a_map = 0;
@@ -751,12 +774,22 @@ int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dc
                     (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, w.KP))
     p.a_tma = 1;
   if (wgrad_raw_tma(g)) {
-    if (!encode_im2col(&p.tmap_x, xsrc, g.N, g.H, g.W, g.ICp, -g.P, -g.P, (g.OH - 1) * g.S - g.P - (g.H - 1),
-                       (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, w.KP, g.dt) ||
+    // folded view: the rows of the weight gradient are (kh, kw, ic) with one 32-float run per kh, i.e.
+    // 32-channel chunks of KW = 1 taps
+    const bool fold = fold_kw(g);
+    const int cs = fold ? g.KW * g.ICp : g.ICp;
+    if (!encode_im2col(&p.tmap_x, xsrc, g.N, g.H, g.W, cs, -g.P, -g.P, (g.OH - 1) * g.S - g.P - (g.H - 1),
+                       (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, w.KP, g.dt, g.ICp) ||
         !encode_2d(&p.tmap_dc, dconv, false, g.OCp, g.n_pix, 32, 32))
       return CONV2D_ERR_CUDA;
     p.a_tma = 1;
     p.rstages = w.rstages;
+    if (fold) {
+      p.Cs = cs;
+      p.div_Cs = make_fastdiv(cs);
+      p.KW = 1;
+      p.div_KW = make_fastdiv(1);
+    }
   }
   p.stages = w.stages;
   p.err = dev->err;
