@@ -75,6 +75,12 @@ EDGE_CASES = {
                                     norm=NORM_BATCH, act=ACT_RELU, dtype=BF16),
     "bf16_k4s2_tma_phases": LayerSpec(N=2, H=10, W=10, IC=64, OC=64, KH=4, KW=4, stride=2, pad=1,
                                       norm=NORM_NONE, act=ACT_TANH, dtype=BF16),
+    # fp32 with KW * IC = 32 and no padding: X through the folded im2col view (each kernel row one
+    # 32-float run) in the fprop and the weight gradient, at strides 2 and 1
+    "fp32_fold_k8_s2": LayerSpec(N=2, H=20, W=21, IC=4, OC=16, KH=8, KW=8, stride=2, pad=0,
+                                 norm=NORM_NONE, act=ACT_RELU, dtype=FP32),
+    "fp32_fold_k4x8_s1_bn": LayerSpec(N=2, H=9, W=13, IC=4, OC=40, KH=4, KW=8, stride=1, pad=0,
+                                      norm=NORM_BATCH, act=ACT_SIGMOID, dtype=FP32),
     # deep fp32 K loops: the accumulation is split over TMEM chunks (dgrad K = 5184, fprop K = 2304)
     "fp32_deep_dgrad_oc576": LayerSpec(N=2, H=10, W=9, IC=8, OC=576, KH=3, KW=3, stride=1, pad=1,
                                        norm=NORM_BATCH, act=ACT_IDENTITY, dtype=FP32),
