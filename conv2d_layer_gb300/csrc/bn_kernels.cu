@@ -625,40 +625,79 @@ __global__ void prep_dgrad_weights_kernel(const T* __restrict__ w, T* __restrict
 __global__ void wgrad_reduce_kernel(const float* __restrict__ partial, int splits, int OC, int taps, int ICp, int IC,
                                     float* __restrict__ dw) {
   pdl_entry();
-  const long total = static_cast<long>(OC) * taps * IC;
+  // V consecutive input channels per thread (4 when IC == ICp is a multiple of 4: 16-byte loads and
+  // stores), each summed over the splits with compensated (Kahan) fp32 summation in split order
+  // (fp64 is slow on this part); the loads of eight splits are issued before their sums
+  const int V = (IC == ICp && IC % 4 == 0) ? 4 : 1;
+  const long total = static_cast<long>(OC) * taps * IC / V;
   const long Mk = static_cast<long>(taps) * ICp;
+  const long stride = static_cast<long>(OC) * Mk;
   for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long>(gridDim.x) * blockDim.x) {
-    const int ic = static_cast<int>(i % IC);
-    const long ot = i / IC;
+    const long e = i * V;  // first dw element of this thread
+    const int ic = static_cast<int>(e % IC);
+    const long ot = e / IC;
     const int tap = static_cast<int>(ot % taps);
     const int oc = static_cast<int>(ot / taps);
-    const long m = static_cast<long>(tap) * ICp + ic;
-    // compensated (Kahan) fp32 summation in split order: fp64 is slow on this part; the loads of eight
-    // splits are issued before their sums
-    float s = 0.f, comp = 0.f;
-    const float* q = partial + static_cast<long>(oc) * Mk + m;
-    const long stride = static_cast<long>(OC) * Mk;
-    int k = 0;
-    for (; k + 8 <= splits; k += 8) {
-      float v[8];
+    const float* q = partial + static_cast<long>(oc) * Mk + static_cast<long>(tap) * ICp + ic;
+    if (V == 4) {
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f), c = s;
+      auto add = [](float& sum, float& comp, float x) {
+        const float y = x - comp;
+        const float t = sum + y;
+        comp = (t - sum) - y;
+        sum = t;
+      };
+      int k = 0;
+      for (; k + 8 <= splits; k += 8) {
+        float4 v[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = q[(k + j) * stride];
+        for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const float4*>(q + (k + j) * stride);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float yk = v[j] - comp;
+        for (int j = 0; j < 8; ++j) {
+          add(s.x, c.x, v[j].x);
+          add(s.y, c.y, v[j].y);
+          add(s.z, c.z, v[j].z);
+          add(s.w, c.w, v[j].w);
+        }
+      }
+      for (; k < splits; ++k) {
+        const float4 v = *reinterpret_cast<const float4*>(q + k * stride);
+        add(s.x, c.x, v.x);
+        add(s.y, c.y, v.y);
+        add(s.z, c.z, v.z);
+        add(s.w, c.w, v.w);
+      }
+      float4* d = reinterpret_cast<float4*>(dw + e);
+      float4 o = *d;
+      o.x += s.x;
+      o.y += s.y;
+      o.z += s.z;
+      o.w += s.w;
+      *d = o;
+    } else {
+      float s = 0.f, comp = 0.f;
+      int k = 0;
+      for (; k + 8 <= splits; k += 8) {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = q[(k + j) * stride];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float yk = v[j] - comp;
+          const float t = s + yk;
+          comp = (t - s) - yk;
+          s = t;
+        }
+      }
+      for (; k < splits; ++k) {
+        const float yk = q[k * stride] - comp;
         const float t = s + yk;
         comp = (t - s) - yk;
         s = t;
       }
+      dw[e] += s;
     }
-    for (; k < splits; ++k) {
-      const float yk = q[k * stride] - comp;
-      const float t = s + yk;
-      comp = (t - s) - yk;
-      s = t;
-    }
-    dw[i] += s;
   }
 }
 
@@ -1556,7 +1595,8 @@ cudaError_t launch_col2im(int dtype, const void* dcol, void* dx, int N, int H, i
 
 cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int taps, int ICp, int IC, float* dw,
                                 cudaStream_t st) {
-  const int g = grid_for(static_cast<long>(OC) * taps * IC, 256);
+  const int V = (IC == ICp && IC % 4 == 0) ? 4 : 1;  // channels per thread (see the kernel)
+  const int g = grid_for(static_cast<long>(OC) * taps * IC / V, 256);
   launch_k(wgrad_reduce_kernel, g, 256, 0, st, 1, partial, splits, OC, taps, ICp, IC, dw);
   return cudaGetLastError();
 }
