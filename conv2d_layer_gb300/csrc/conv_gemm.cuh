@@ -226,31 +226,32 @@ __device__ __forceinline__ float2 f2(uint32_t a, uint32_t b) { return make_float
 // the epilogue shift minus the statistics shift; both 8-byte aligned, indexed from the
 // chunk's first column). Two 16-lane loads give thread t rows t/4 + {0, 8, 16, 24} of the
 // column pairs 8j + 2(t%4) + {0, 1}: the four rows are added in the thread with packed
-// f32x2 arithmetic (one load at a time), then a transposed butterfly over lane bits 4, 3, 2 leaves each lane one
+// f32x2 arithmetic, then a transposed butterfly over lane bits 4, 3, 2 leaves each lane one
 // column pair of one statistic. rowmask bit i clears row t/4 + 8i (rows past the tile's
 // end); zero: the accumulator was never written (read as 0). Writes sum(d) to s1[0..31]
 // and sum(d*d) to s2[0..31]. Warp-collective. Kept out of line: inlined into both
 // statistics passes it pushed the epilogue past the register budget of the 320-thread CTA.
 static __device__ __noinline__ void colstats32(uint32_t taddr, bool zero, const float* a, const float* k, unsigned rowmask,
-                                           int lane, float* s1, float* s2) {
+                                               int lane, float* s1, float* s2) {
   const int cp = 2 * (lane & 3);
+  uint32_t r[2][16];
+  if (zero) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) r[0][e] = r[1][e] = 0u;
+  } else {  // both 16-lane halves in flight, one wait
+    tmem_ld16x256(taddr, r[0]);
+    tmem_ld16x256(taddr + (16u << 16), r[1]);
+    tmem_ld_wait16x2(r[0], r[1]);
+  }
   float x[16];  // x[2j + kk]: sum over the four rows of column 8j + cp + kk; x[8 + 2j + kk]: sum of squares
 #pragma unroll
   for (int e = 0; e < 16; ++e) x[e] = 0.f;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {  // lanes 0-15, then 16-31 of the quarter
-    uint32_t r[16];
-    if (zero) {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) r[e] = 0u;
-    } else {
-      tmem_ld16x256(taddr + (static_cast<uint32_t>(16 * h) << 16), r);
-      tmem_ld_wait(r);
-    }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float2 kv = *reinterpret_cast<const float2*>(k + 8 * j + cp);
-      float2 d0 = f2(r[4 * j], r[4 * j + 1]), d1 = f2(r[4 * j + 2], r[4 * j + 3]);
+      float2 d0 = f2(r[h][4 * j], r[h][4 * j + 1]), d1 = f2(r[h][4 * j + 2], r[h][4 * j + 3]);
       if (a) {
         const float2 av = *reinterpret_cast<const float2*>(a + 8 * j + cp);
         d0 = __ffma2_rn(d0, av, kv);
