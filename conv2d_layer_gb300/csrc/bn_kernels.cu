@@ -7,12 +7,13 @@
 // Phase 3; `backward_full` training branch) and the per-channel kernels of
 // "operations_cuda.h" (`bn_stats_training`, `bn_forward_affine`,
 // `bn_training_backward`, `bias_backward_partial/finalize`). The layout work
-// is different from those kernels: NHWC rows are read with 16-byte vector
-// loads, a thread keeps a fixed group of channels for its whole walk, and
-// each block writes one partial per channel that a small finalize kernel
-// merges in double in a fixed order (deterministic). The batch variance is
-// merged from per-tile two-pass (mean, M2) with Chan's formula, never
-// E[x^2] - mean^2.
+// is different from those kernels: NHWC rows stream through shared memory
+// (bulk copies) or are read with 16-byte vector loads, a thread keeps a fixed
+// group of channels for its whole walk, and each block writes one partial per
+// channel that a small finalize kernel merges in a fixed order
+// (deterministic; fp32 with compensated sums or Chan merges, fp64 only where
+// the work is a handful of operations). The batch variance is merged from
+// per-tile (mean, M2) with Chan's formula, never E[x^2] - mean^2.
 #include <algorithm>
 #include <cmath>
 #include <type_traits>
