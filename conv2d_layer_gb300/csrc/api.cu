@@ -483,6 +483,7 @@ struct Plan {
   size_t off[R_NREG];
   size_t total;
   RowWalk walk;
+  RowWalk walk3;  // batch-norm backward reduce: three blocks per SM (its own partials and finalize)
   WgradPlan wg;
 };
 
@@ -493,6 +494,7 @@ void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
   const bool gn = g.norm == CONV2D_NORM_GROUP;
   // layer and group norm walk each image as a segment of its own, statistics per group of channels
   pl->walk = make_walk(g.n_pix, g.OC, g.dt, sms, (ln || gn) ? g.N : 1, (ln || gn) ? g.OC / g.groups : 0);
+  pl->walk3 = make_walk(g.n_pix, g.OC, g.dt, sms, 1, 0, 3);
   const size_t G = pl->walk.G;
   if (op == CONV2D_OP_FWD_TRAIN || op == CONV2D_OP_FWD_INFER) {
     if (g.pack_x) sz[R_XP] = static_cast<size_t>(g.N) * g.H * g.W * g.ICp * es;
@@ -511,7 +513,7 @@ void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
     }
   } else {
     sz[R_DC] = static_cast<size_t>(g.n_pix) * g.OCp * es;
-    sz[R_PART] = G * g.OC * 2 * 4;
+    sz[R_PART] = std::max<size_t>(G, pl->walk3.G) * g.OC * 2 * 4;
     // channel sums, then per-(image, group) sums
     sz[R_C12] = 2 * (static_cast<size_t>(g.OC) + ((ln || gn) ? static_cast<size_t>(g.N) * g.groups : 0)) * 4;
     // dgrad weights: every phase's taps together hold each kernel tap once
@@ -1057,6 +1059,7 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
   Plan pl;
   plan_ws(g, CONV2D_OP_BWD, dev->sms, &pl);
   pl.walk.err = dev->err;
+  pl.walk3.err = dev->err;
   if (!ws || ws_bytes < pl.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CONV2D_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* dconv = region(ws, pl, R_DC);
@@ -1073,9 +1076,11 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
            launch_bn_bwd_apply(g.dt, pre_act, dy, pl.walk, g.OCp, save_mean, save_inv_std, gamma, beta, g.act, c12,
                                dconv, part, st));
   } else if (bn) {
+    // the reduce walks with three blocks per SM (its own block count; the partials are summed before the
+    // d_conv pass reuses the buffer)
     LAUNCH("bn_bwd_reduce", st,
-           launch_bn_bwd_reduce(g.dt, pre_act, dy, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, part, st));
-    LAUNCH("bn_bwd_finalize", st, launch_sum_finalize(part, pl.walk, 2, 0, c12, dbeta, dgamma, st));
+           launch_bn_bwd_reduce(g.dt, pre_act, dy, pl.walk3, save_mean, save_inv_std, gamma, beta, g.act, part, st));
+    LAUNCH("bn_bwd_finalize", st, launch_sum_finalize(part, pl.walk3, 2, 0, c12, dbeta, dgamma, st));
     // evaluation mode (frozen statistics): d_conv = d_norm * gamma * inv_std, no projection terms
     LAUNCH("bn_bwd_dconv", st,
            launch_bn_bwd_apply(g.dt, pre_act, dy, pl.walk, g.OCp, save_mean, save_inv_std, gamma, beta, g.act,

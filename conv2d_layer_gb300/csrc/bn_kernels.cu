@@ -1307,7 +1307,7 @@ static int pick_bps(int segs, long seg_rows, long resident, long ovh) {
   return best;
 }
 
-RowWalk make_walk(long rows, int C, int dtype, int sms, int segs, int cpg) {
+RowWalk make_walk(long rows, int C, int dtype, int sms, int segs, int cpg, int per_sm) {
   RowWalk w;
   w.rows = rows;
   w.C = C;
@@ -1322,13 +1322,14 @@ RowWalk make_walk(long rows, int C, int dtype, int sms, int segs, int cpg) {
   const int tpr = cg < kBlock ? cg : kBlock;
   const int rpp = kBlock / tpr;
   // Streamed walks use half-size chunks so that two blocks of the two-input kernels fit on an SM
-  // (their registers and shared memory allow two): more warps to hide the latency of each chunk's
-  // arithmetic than one block per SM with bigger chunks.
+  // (their registers and shared memory allow two; per_sm blocks for a kernel that fits more, such as the
+  // backward reduce): more warps to hide the latency of each chunk's arithmetic than one block per SM
+  // with bigger chunks.
   long resident;
   if (w.stream) {
     w.R = static_cast<int>(std::max<long>(1, (kChunkBytes / 2) / row_bytes));
     if (w.R > rpp) w.R = w.R / rpp * rpp;  // whole passes of the block's rows per chunk
-    resident = 2L * sms;
+    resident = static_cast<long>(per_sm < 2 ? 2 : per_sm) * sms;
   } else {
     w.R = 0;
     resident = 8L * sms;

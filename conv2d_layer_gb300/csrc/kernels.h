@@ -67,7 +67,7 @@ struct RowWalk {
   int R;       // rows per streamed chunk
   int* err;    // device error word for bounded waits
 };
-RowWalk make_walk(long rows, int C, int dtype, int sms, int segs, int cpg);
+RowWalk make_walk(long rows, int C, int dtype, int sms, int segs, int cpg, int per_sm = 2);
 
 // elementwise / reduction kernels (bn_kernels.cu); dtype 0 = fp32, 1 = bf16
 cudaError_t launch_pack_channels(int dtype, const void* src, void* dst, long rows, int C, int Cp, cudaStream_t st);
