@@ -419,6 +419,21 @@ def cpu_baseline(n_img=1):
                       % (n_img, flops / 1e9, dt)}
 
 
+def max_over_ranks(vals, device):
+    """Each value's maximum over the ranks of the default process group: the slowest rank sets the step
+    time of the job."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_tflops(world, flops_per_gpu, ms):
+    """Whole-job TFLOP/s: the work of every replica over the (slowest rank's) step time."""
+    return world * flops_per_gpu / (ms * 1e-3) / 1e12
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -459,15 +474,12 @@ def main():
     if rank == 0 and world == 1 and not args.no_per_config and not args.images:
         per_cfg = per_config_timing(_peaks())
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+        ms, e2e_ms = max_over_ranks([ms, e2e_ms], "cuda")
     if rank != 0:
         return
     spec = r["spec"]
     peaks = _peaks()
-    value = world * r["flops"] / (ms * 1e-3) / 1e12
+    value = job_tflops(world, r["flops"], ms)
     kern = gemm_roofline(spec, r["kern"], args.steps, peaks)
     gemms = {k: v for k, v in kern.items() if k.endswith("_gemm")}
     dom = max(gemms, key=lambda k: gemms[k]["avg_ms"] * gemms[k]["launches"])
@@ -493,7 +505,7 @@ def main():
         "kernels_timing": {"ms_per_step_instrumented": round(r["ms_instr"], 4),
                            "what": "per-launch CUDA events over a second timed region of the same steps"},
         "gpu_launches": r["per_step"] * args.steps,
-        "e2e": {"value": round(world * r["flops"] / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(job_tflops(world, r["flops"], e2e_ms), 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(e2e_ms, 4),
                 "what": "every step: pinned host X, dY copied in, dW, dbias, dgamma, dbeta copied out, same ABI "
                         "calls; the copies of step k+1 overlap step k (second stream, two input buffers)"},
