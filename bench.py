@@ -269,8 +269,9 @@ PER_CONFIG = (
 
 def per_config_timing(peaks, steps=10, warmup=3):
     """fwd_train + bwd of every workload (the mixed stack as its two chained layers) and of the BN-layer and
-    large shapes with layer norm: step time, TFLOP/s, and per-kernel times from one extra profiled step,
-    with the HBM fraction of the bandwidth-bound kernels."""
+    large shapes with layer and group norm: step time through the ABI calls, the same step replayed from a
+    CUDA graph (no host launch work), TFLOP/s, and per-kernel times from one extra profiled step, with the
+    HBM fraction of the bandwidth-bound kernels."""
     import torch
 
     from dataclasses import replace
@@ -306,6 +307,20 @@ def per_config_timing(peaks, steps=10, warmup=3):
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
+        # the same step captured once in a CUDA graph and replayed: no host launch work per step
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(steps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_graph = e0.elapsed_time(e1) / steps
+        del graph
         abi.conv2d_prof_enable(True)
         abi.conv2d_prof_read()
         # the GPU idles in a ~2 ms sleep kernel while the host queues the whole step, so that the per-launch
@@ -324,6 +339,7 @@ def per_config_timing(peaks, steps=10, warmup=3):
         hbm = {k: round(HBM_TENSORS[k] * tensor_bytes / (t * 1e-3) / 1e9 / peaks["hbm"], 3)
                for k, t in kern.items() if k in HBM_TENSORS}
         out[label] = {"ms_per_step": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
+                      "ms_per_step_graph": round(ms_graph, 4),
                       "dtype": "bf16" if specs[0].dtype == 1 else "fp32 (3xTF32)", "layers": len(specs),
                       "kernels_ms": {k: round(t, 4) for k, t in kern.items()}, "hbm_frac_of_measured": hbm}
         del layers, x, dy, inp
