@@ -952,6 +952,51 @@ __device__ __forceinline__ float dact_mul(float t, float dy) {
   else return dact_t<A, FAST>(t) * dy;
 }
 
+// The ReLU test on stored bf16 pre-activations, two channels per instruction and without forming t.
+// t = gs * (v - mean) + beta > 0 (gs = gamma * inv_std) holds exactly when s * v > s * th, with
+// th = mean - beta / gs and s the sign of gs. Because v is a bf16 value, s * v > s * th is the same as
+// s * v > floor_bf16(s * th): a packed bf16 compare of v (sign bit flipped by an XOR where s < 0)
+// with a key per channel, exact up to the fp32 rounding of th. gs == 0 leaves t = beta: a key of -inf
+// (every v passes) or +inf (none does); a NaN gs gives a NaN key (none passes, as t would be NaN).
+__device__ __forceinline__ void relu_key(float mean, float gs, float beta, uint32_t& key, uint32_t& sgn) {
+  sgn = 0;
+  if (gs > 0.f) {
+    key = __bfloat16_as_ushort(__float2bfloat16_rd(mean - beta / gs));
+  } else if (gs < 0.f) {
+    key = __bfloat16_as_ushort(__float2bfloat16_rd(beta / gs - mean));
+    sgn = 0x8000u;
+  } else if (gs == 0.f) {
+    key = beta > 0.f ? 0xff80u : 0x7f80u;
+  } else {
+    key = 0x7fc0u;
+  }
+}
+// Keys of channels 2q and 2q+1 in the low and high halves of key[q] / sgn[q] (nmu = -mean).
+template <int EC>
+__device__ __forceinline__ void relu_keys(const float* nmu, const float* gs, const float* be, uint32_t* key,
+                                          uint32_t* sgn) {
+#pragma unroll
+  for (int q = 0; q < EC / 2; ++q) {
+    uint32_t k0, s0, k1, s1;
+    relu_key(-nmu[2 * q], gs[2 * q], be[2 * q], k0, s0);
+    relu_key(-nmu[2 * q + 1], gs[2 * q + 1], be[2 * q + 1], k1, s1);
+    key[q] = k0 | (k1 << 16);
+    sgn[q] = s0 | (s1 << 16);
+  }
+}
+// 0xffff in each half of a packed bf16 pair v whose ReLU test passes, 0 elsewhere
+__device__ __forceinline__ uint32_t relu_mask2(uint32_t v, uint32_t key, uint32_t sgn) {
+  const uint32_t f = v ^ sgn;
+  return __hgt2_mask(*reinterpret_cast<const __nv_bfloat162*>(&f), *reinterpret_cast<const __nv_bfloat162*>(&key));
+}
+// a packed bf16 pair as floats (low half first, as stored)
+__device__ __forceinline__ float2 bf2f(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+// Streamed backward kernels take the packed path for bf16 layers with no activation or ReLU.
+template <typename T, int A>
+constexpr bool kPackedBwd = std::is_same<T, __nv_bfloat16>::value && (A == 0 || A == 1);
+
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -960,9 +1005,10 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 // Walk rows [r0, r1) of NIN tensors [rows][C] (EC channels per thread, the
-// group g fixed per thread); proc(row, v) gets the NIN vectors of one row.
+// group g fixed per thread); proc(row, v) gets the NIN vectors of one row as floats, or with RAW
+// proc(row, p) the NIN shared-memory addresses of the thread's EC elements, still in T.
 // Returns false if a wait gave up (recorded in *err).
-template <typename T, int EC, int NIN, typename Proc>
+template <typename T, int EC, int NIN, bool RAW = false, typename Proc>
 __device__ __forceinline__ bool stream_walk(const T* const (&in)[NIN], long r0, long r1, int C, int R, int g,
                                             int rl, int rpp, uint8_t* sm, uint64_t* full, int* err, int rev,
                                             Proc&& proc) {
@@ -995,11 +1041,18 @@ __device__ __forceinline__ bool stream_walk(const T* const (&in)[NIN], long r0, 
     const int nrows = static_cast<int>(chunk_end(k) - rb);
     if (rl < rpp) {
       for (int rr = rl; rr < nrows; rr += rpp) {
-        float v[NIN][EC];
+        const T* src[NIN];
 #pragma unroll
         for (int i = 0; i < NIN; ++i)
-          lds_v<EC>(reinterpret_cast<const T*>(sm + (s * NIN + i) * chunk) + static_cast<size_t>(rr) * C + g * EC, v[i]);
-        proc(rb + rr, v);
+          src[i] = reinterpret_cast<const T*>(sm + (s * NIN + i) * chunk) + static_cast<size_t>(rr) * C + g * EC;
+        if constexpr (RAW) {
+          proc(rb + rr, src);
+        } else {
+          float v[NIN][EC];
+#pragma unroll
+          for (int i = 0; i < NIN; ++i) lds_v<EC>(src[i], v[i]);
+          proc(rb + rr, v);
+        }
       }
     }
     __syncthreads();  // stage s consumed by every thread
@@ -1164,7 +1217,38 @@ __global__ void __launch_bounds__(kBlock, 3) bn_bwd_reduce_stream(const T* __res
     a[e] = b[e] = 0.f;
   }
   const T* const in[2] = {pre, dy};
-  {
+  if constexpr (kPackedBwd<T, A>) {
+    // b accumulates d_norm * (x - mean); the factor inv_std is applied once after the walk
+    uint32_t key[EC / 2], sgn[EC / 2];
+    if constexpr (A == 1) {
+      float gs[EC];
+#pragma unroll
+      for (int e = 0; e < EC; ++e) gs[e] = ga[e] * is[e];
+      relu_keys<EC>(nmu, gs, be, key, sgn);
+    }
+    stream_walk<T, EC, 2, true>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err, rev,
+                                [&](long, const T* const (&p)[2]) {
+                                  const uint4 pv = *reinterpret_cast<const uint4*>(p[0]);
+                                  const uint4 pd = *reinterpret_cast<const uint4*>(p[1]);
+                                  const uint32_t wv[4] = {pv.x, pv.y, pv.z, pv.w};
+                                  const uint32_t wd[4] = {pd.x, pd.y, pd.z, pd.w};
+#pragma unroll
+                                  for (int q = 0; q < EC / 2; ++q) {
+                                    const int e = 2 * q;
+                                    const uint32_t m = A == 1 ? relu_mask2(wv[q], key[q], sgn[q]) : 0xffffffffu;
+                                    const float2 dn = bf2f(wd[q] & m);
+                                    const float2 d = __fadd2_rn(bf2f(wv[q]), pr(nmu, e));
+                                    const float2 sa = __fadd2_rn(pr(a, e), dn);
+                                    const float2 sb = __ffma2_rn(dn, d, pr(b, e));
+                                    a[e] = sa.x;
+                                    a[e + 1] = sa.y;
+                                    b[e] = sb.x;
+                                    b[e + 1] = sb.y;
+                                  }
+                                });
+#pragma unroll
+    for (int e = 0; e < EC; ++e) b[e] *= is[e];
+  } else {
     stream_walk<T, EC, 2>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err, rev,
                           [&](long, const float (&v)[2][EC]) {
 #pragma unroll
@@ -1209,7 +1293,8 @@ __global__ void __launch_bounds__(kBlock, 3) bn_bwd_reduce_stream(const T* __res
 
 // d_conv (MODE 0: batch / layer norm, 1: no norm) and part[b][c] = sum d_conv.
 // Without an activation three blocks fit an SM (registers capped for it); an activation needs more
-// registers (ReLU: gamma and beta stay live for its test; capped for three blocks it spills): two.
+// registers (ReLU on bf16: 87, and capped for three blocks it spills, which measured slower than two
+// blocks without spills): two.
 template <typename T, int EC, int MODE, int A>
 __global__ void __launch_bounds__(kBlock, A == 0 ? 3 : 2) dconv_stream(const T* __restrict__ pre, const T* __restrict__ dy,
                                                           long seg_rows, int bps, int C, long rpb, int R, int cpg,
@@ -1241,7 +1326,51 @@ __global__ void __launch_bounds__(kBlock, A == 0 ? 3 : 2) dconv_stream(const T* 
     }
   }
   const T* const in[2] = {pre, dy};
-  {
+  if constexpr (kPackedBwd<T, A>) {
+    // MODE 0: d_conv = P * d_norm + (Q * (x - mean) + S), P = inv_std * gamma, Q = -inv_std^2 * k2,
+    // S = -inv_std * k1 (the same terms as inv_std * (gamma * d_norm - k1 - z * k2), z = (x - mean) * inv_std);
+    // MODE 1: d_conv = d_norm. The ReLU test has mean 0, gain 1 and beta 0 without a norm.
+    uint32_t key[EC / 2], sgn[EC / 2];
+    float P[EC], Q[EC], S[EC];
+#pragma unroll
+    for (int e = 0; e < EC; ++e) {
+      if (MODE == 0) {
+        P[e] = is[e] * ga[e];
+        Q[e] = -is[e] * is[e] * k2[e];
+        S[e] = is[e] * nk1[e];
+      } else {
+        nmu[e] = 0.f;
+        P[e] = 1.f;
+        be[e] = 0.f;
+      }
+    }
+    if constexpr (A == 1) relu_keys<EC>(nmu, P, be, key, sgn);
+    stream_walk<T, EC, 2, true>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err, rev,
+                                [&](long row, const T* const (&p)[2]) {
+                                  const uint4 pv = *reinterpret_cast<const uint4*>(p[0]);
+                                  const uint4 pd = *reinterpret_cast<const uint4*>(p[1]);
+                                  const uint32_t wv[4] = {pv.x, pv.y, pv.z, pv.w};
+                                  const uint32_t wd[4] = {pd.x, pd.y, pd.z, pd.w};
+                                  float o[EC];
+#pragma unroll
+                                  for (int q = 0; q < EC / 2; ++q) {
+                                    const int e = 2 * q;
+                                    const uint32_t m = A == 1 ? relu_mask2(wv[q], key[q], sgn[q]) : 0xffffffffu;
+                                    const float2 dn = bf2f(wd[q] & m);
+                                    float2 r = dn;
+                                    if (MODE == 0) {
+                                      const float2 d = __fadd2_rn(bf2f(wv[q]), pr(nmu, e));
+                                      r = __ffma2_rn(pr(P, e), dn, __ffma2_rn(pr(Q, e), d, pr(S, e)));
+                                    }
+                                    o[e] = r.x;
+                                    o[e + 1] = r.y;
+                                    const float2 sa = __fadd2_rn(pr(a, e), r);
+                                    a[e] = sa.x;
+                                    a[e + 1] = sa.y;
+                                  }
+                                  store_v<EC>(dconv + row * C + st.g * EC, o);
+                                });
+  } else {
     stream_walk<T, EC, 2>(in, st.r0, st.r1, C, R, st.g, st.rl, st.rpp, sm, full, err, rev,
                           [&](long row, const float (&v)[2][EC]) {
                             float o[EC];

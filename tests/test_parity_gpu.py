@@ -13,7 +13,8 @@ import torch
 from conv2d_layer_gb300 import abi
 from conv2d_layer_gb300.layer import Conv2dLayer
 from conv2d_layer_gb300.workloads import (ACT_IDENTITY, ACT_RELU, ACT_SIGMOID, ACT_TANH, BF16, FP32, NORM_BATCH,
-                                          NORM_NONE, WORKLOADS, LayerSpec, make_inputs, random_layer_inputs)
+                                          NORM_GROUP, NORM_LAYER, NORM_NONE, WORKLOADS, LayerSpec, make_inputs,
+                                          random_layer_inputs)
 from parity_util import check_pair, f64, oracle_layer, rel_err, run_pair, TOL
 
 import oracle
@@ -102,6 +103,29 @@ def test_edge_parity(name):
     inp = random_layer_inputs(spec, 7)
     gpu, ref = run_pair(spec, inp)
     check_pair(spec, gpu, ref)
+
+
+@pytest.mark.parametrize("dtype,norm", [(BF16, NORM_BATCH), (BF16, NORM_LAYER), (BF16, NORM_GROUP),
+                                        (FP32, NORM_BATCH)])
+def test_signed_gamma_relu(dtype, norm):
+    """ReLU after a norm whose gain is positive, negative or zero by channel. The backward's ReLU test
+    (on bf16, a packed compare of the stored pre-activation with a key per channel) must follow the
+    sign of gamma, and a zero gain leaves the decision to beta alone (both signs of beta present)."""
+    spec = LayerSpec(N=2, H=12, W=12, IC=64, OC=64, KH=3, KW=3, stride=1, pad=1, norm=norm,
+                     groups=8 if norm == NORM_GROUP else 1, act=ACT_RELU, dtype=dtype)
+    inp = random_layer_inputs(spec, 11)
+    li = inp["layers"][0]
+    c = torch.arange(spec.OC)
+    gamma, beta = li.gamma.clone(), li.beta.clone()
+    gamma[c % 4 == 1] *= -1.0
+    gamma[c % 4 == 3] = 0.0
+    beta[c % 8 == 3] = 0.3
+    beta[c % 8 == 7] = -0.3
+    inp["layers"][0] = replace(li, gamma=gamma, beta=beta)
+    gpu, ref = run_pair(spec, inp)
+    check_pair(spec, gpu, ref)
+    # the zero-gain channels put out beta (beta > 0) or nothing (beta < 0) at every pixel
+    assert np.all(ref["y"][..., 3::8] == float(np.float32(0.3))) and np.all(ref["y"][..., 7::8] == 0.0)
 
 
 @pytest.mark.parametrize("dtype", [FP32, BF16])
