@@ -274,28 +274,11 @@ def per_config_timing(peaks, steps=10, warmup=3):
     HBM fraction of the bandwidth-bound kernels."""
     import torch
 
-    from dataclasses import replace
-
     from conv2d_layer_gb300 import abi
-    from conv2d_layer_gb300.layer import Conv2dLayer
-    from conv2d_layer_gb300.workloads import WORKLOADS, make_inputs
 
     out = {}
     for label, name, over in PER_CONFIG:
-        wl = WORKLOADS[name]
-        specs = [replace(s, **over) for s in wl.layers]
-        inp = make_inputs(name, layers=specs)
-        layers = [Conv2dLayer(s, li.w, li.b, li.gamma, li.beta, li.running_mean, li.running_var)
-                  for s, li in zip(specs, inp["layers"])]
-        x, dy = inp["x"].cuda(), inp["dy"].cuda()
-
-        def step():
-            acts = [x]
-            for L in layers:
-                acts.append(L.fwd_train(acts[-1]))
-            g = dy
-            for L, a in zip(reversed(layers), reversed(acts[:-1])):
-                g = L.bwd(a, g)
+        specs, step, release = config_step(name, over)
 
         for _ in range(warmup):
             step()
@@ -342,10 +325,60 @@ def per_config_timing(peaks, steps=10, warmup=3):
                       "ms_per_step_graph": round(ms_graph, 4),
                       "dtype": "bf16" if specs[0].dtype == 1 else "fp32 (3xTF32)", "layers": len(specs),
                       "kernels_ms": {k: round(t, 4) for k, t in kern.items()}, "hbm_frac_of_measured": hbm}
-        del layers, x, dy, inp
+        release()
         torch.cuda.empty_cache()
     abi.check(abi.conv2d_device_status()[0], "device status")
     return out
+
+
+def config_step(name, over):
+    """Layers, inputs and the fwd_train + bwd step of one workload (every layer spec updated by `over`; a
+    stack chains its layers forward and backward). Returns (specs, step, release)."""
+    from dataclasses import replace
+
+    from conv2d_layer_gb300.layer import Conv2dLayer
+    from conv2d_layer_gb300.workloads import WORKLOADS, make_inputs
+
+    specs = [replace(s, **over) for s in WORKLOADS[name].layers]
+    inp = make_inputs(name, layers=specs)
+    state = {"layers": [Conv2dLayer(s, li.w, li.b, li.gamma, li.beta, li.running_mean, li.running_var)
+                        for s, li in zip(specs, inp["layers"])],
+             "x": inp["x"].cuda(), "dy": inp["dy"].cuda()}
+
+    def step():
+        layers = state["layers"]
+        acts = [state["x"]]
+        for L in layers:
+            acts.append(L.fwd_train(acts[-1]))
+        g = state["dy"]
+        for L, a in zip(reversed(layers), reversed(acts[:-1])):
+            g = L.bwd(a, g)
+
+    return specs, step, state.clear
+
+
+def profile_workload(label, steps, warmup):
+    """Training steps of one per-config entry and nothing else: a short program for profiler captures
+    of the smaller workloads. Prints the step time (CUDA events), not the benchmark line."""
+    import torch
+
+    from conv2d_layer_gb300 import abi
+
+    entry = {lab: (name, over) for lab, name, over in PER_CONFIG}[label]
+    _, step, release = config_step(*entry)
+    for _ in range(max(warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    abi.check(abi.conv2d_device_status()[0], "device status")
+    print(json.dumps({"profile_workload": label, "steps": steps, "ms_per_step": round(e0.elapsed_time(e1) / steps, 4)}),
+          flush=True)
+    release()
 
 
 def gemm_roofline(spec, kern, steps, peaks):
@@ -462,7 +495,13 @@ def main():
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--images", type=int, default=0,
                     help="run the large layer with this many images instead of 256 (small profiling cases)")
+    ap.add_argument("--profile-workload", default="", choices=[""] + [c[0] for c in PER_CONFIG],
+                    help="only run --steps training steps of this per-config entry (profiler captures)")
     args = ap.parse_args()
+
+    if args.profile_workload:
+        profile_workload(args.profile_workload, args.steps, args.warmup)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

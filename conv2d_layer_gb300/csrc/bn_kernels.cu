@@ -622,9 +622,10 @@ __global__ void prep_dgrad_weights_kernel(const T* __restrict__ w, T* __restrict
   }
 }
 
-// dW[oc][tap][ic] += sum over splits of partial[s][oc][tap*ICp + ic] (fixed order: deterministic).
-__global__ void wgrad_reduce_kernel(const float* __restrict__ partial, int splits, int OC, int taps, int ICp, int IC,
-                                    float* __restrict__ dw) {
+// dW[oc][tap][ic] += sum over splits of partial[s][oc][tap*ICp + ic] (fixed order: deterministic), one
+// thread per item over all splits: the form for a few splits (see launch_wgrad_reduce).
+__global__ void wgrad_reduce_serial_kernel(const float* __restrict__ partial, int splits, int OC, int taps, int ICp,
+                                           int IC, float* __restrict__ dw) {
   pdl_entry();
   // V consecutive input channels per thread (4 when IC == ICp is a multiple of 4: 16-byte loads and
   // stores), each summed over the splits with compensated (Kahan) fp32 summation in split order
@@ -699,6 +700,77 @@ __global__ void wgrad_reduce_kernel(const float* __restrict__ partial, int split
       }
       dw[e] += s;
     }
+  }
+}
+
+// dW[oc][tap][ic] += sum over splits of partial[s][oc][tap*ICp + ic] (fixed order: deterministic).
+// A block holds 32 items (V consecutive input channels each: 4 when IC == ICp is a multiple of 4, for
+// 16-byte loads and stores) and kRedGroups warps: warp g sums splits g, g + kRedGroups, ... of its
+// lane's item with compensated (Kahan) fp32 sums in split order (fp64 is slow on this part), so that a
+// thread's chain of dependent loads is splits / kRedGroups long; warp 0 then adds the group sums in
+// group order. 32-bit index arithmetic: the layer limits keep OC * taps * ICp below 2^30.
+constexpr int kRedGroups = 8;
+constexpr int kRedSerialMax = 48;  // split counts below this take wgrad_reduce_serial_kernel
+template <int V>
+__global__ void __launch_bounds__(32 * kRedGroups) wgrad_reduce_kernel(const float* __restrict__ partial, int splits,
+                                                                      int OC, int taps, int ICp, int IC,
+                                                                      float* __restrict__ dw) {
+  pdl_entry();
+  using VT = typename std::conditional<V == 4, float4, float>::type;
+  __shared__ VT s_sum[kRedGroups][32];
+  const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
+  const int total = OC * taps * IC / V;
+  const int item = blockIdx.x * 32 + lane;
+  const long stride = static_cast<long>(OC) * taps * ICp;
+  float sum[V], comp[V];
+#pragma unroll
+  for (int j = 0; j < V; ++j) sum[j] = comp[j] = 0.f;
+  int e = 0;
+  if (item < total) {
+    e = item * V;  // first dw element of this item
+    const int ot = e / IC;
+    const int ic = e - ot * IC;
+    const int oc = ot / taps;
+    const int tap = ot - oc * taps;
+    const float* q = partial + oc * taps * ICp + tap * ICp + ic;
+    int k = grp;
+    // four loads in flight per thread before their sums
+    for (; k + 3 * kRedGroups < splits; k += 4 * kRedGroups) {
+      VT v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const VT*>(q + (k + u * kRedGroups) * stride);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int j = 0; j < V; ++j) kahan_add(sum[j], comp[j], reinterpret_cast<const float*>(&v[u])[j]);
+    }
+    for (; k < splits; k += kRedGroups) {
+      const VT v = *reinterpret_cast<const VT*>(q + k * stride);
+#pragma unroll
+      for (int j = 0; j < V; ++j) kahan_add(sum[j], comp[j], reinterpret_cast<const float*>(&v)[j]);
+    }
+  }
+  {
+    VT t;
+#pragma unroll
+    for (int j = 0; j < V; ++j) reinterpret_cast<float*>(&t)[j] = sum[j] - comp[j];
+    s_sum[grp][lane] = t;
+  }
+  __syncthreads();
+  if (grp == 0 && item < total) {
+    float acc[V], cacc[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) acc[j] = cacc[j] = 0.f;
+    for (int g = 0; g < kRedGroups; ++g) {
+      const VT t = s_sum[g][lane];
+#pragma unroll
+      for (int j = 0; j < V; ++j) kahan_add(acc[j], cacc[j], reinterpret_cast<const float*>(&t)[j]);
+    }
+    VT* d = reinterpret_cast<VT*>(dw + e);
+    VT o = *d;
+#pragma unroll
+    for (int j = 0; j < V; ++j) reinterpret_cast<float*>(&o)[j] += acc[j];
+    *d = o;
   }
 }
 
@@ -1726,9 +1798,23 @@ cudaError_t launch_col2im(int dtype, const void* dcol, void* dx, int N, int H, i
 
 cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int taps, int ICp, int IC, float* dw,
                                 cudaStream_t st) {
-  const int V = (IC == ICp && IC % 4 == 0) ? 4 : 1;  // channels per thread (see the kernel)
-  const int g = grid_for(static_cast<long>(OC) * taps * IC / V, 256);
-  launch_k(wgrad_reduce_kernel, g, 256, 0, st, 1, partial, splits, OC, taps, ICp, IC, dw);
+  // Few splits: one thread per item over every split (measured faster for the 25 splits of a 256-image
+  // 3 x 3 layer). Many splits (the fp32 layers, 1 x 1 layers with one row tile): the split groups, which
+  // shorten each thread's chain of dependent loads.
+  if (splits < kRedSerialMax) {
+    const int V = (IC == ICp && IC % 4 == 0) ? 4 : 1;  // channels per thread (see the kernel)
+    const int g = grid_for(static_cast<long>(OC) * taps * IC / V, 256);
+    launch_k(wgrad_reduce_serial_kernel, g, 256, 0, st, 1, partial, splits, OC, taps, ICp, IC, dw);
+    return cudaGetLastError();
+  }
+  // 32 items of V channels per block (see the kernel)
+  if (IC == ICp && IC % 4 == 0) {
+    const int g = static_cast<int>((static_cast<long>(OC) * taps * IC / 4 + 31) / 32);
+    launch_k(wgrad_reduce_kernel<4>, g, 32 * kRedGroups, 0, st, 1, partial, splits, OC, taps, ICp, IC, dw);
+  } else {
+    const int g = static_cast<int>((static_cast<long>(OC) * taps * IC + 31) / 32);
+    launch_k(wgrad_reduce_kernel<1>, g, 32 * kRedGroups, 0, st, 1, partial, splits, OC, taps, ICp, IC, dw);
+  }
   return cudaGetLastError();
 }
 
