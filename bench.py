@@ -267,6 +267,92 @@ PER_CONFIG = (
 )
 
 
+# Images of each per-config workload the oracle runs for its CPU baseline (a bounded sample, a few
+# seconds in all on the host cores).
+CPU_SAMPLE_IMAGES = {"tiny": 2, "rl": 8, "bn": 4, "mixed": 1, "large": 1}
+
+
+def cpu_baseline_config(name, over, n_img):
+    """The oracle, as it stands, on a bounded sample of one per-config workload: n_img images through
+    fwd_train + bwd of every layer (a stack feeds each layer's output to the next and its dX back as the
+    previous layer's dY). Returns the cpu_baseline object of that entry."""
+    from dataclasses import replace
+
+    import oracle
+    from conv2d_layer_gb300.workloads import BF16, WORKLOADS, make_inputs
+
+    specs = [replace(sp, N=n_img, **over) for sp in WORKLOADS[name].layers]
+    inp = make_inputs(name, layers=specs)
+    f64 = lambda t: t.double().numpy()  # noqa: E731
+    ols = [oracle.Layer(sp.N, sp.H, sp.W, sp.IC, sp.OC, sp.KH, sp.KW, sp.stride, sp.pad, norm=sp.norm, act=sp.act,
+                        eps=sp.eps, momentum=sp.momentum, store="bf16" if sp.dtype == BF16 else "f32",
+                        groups=sp.groups) for sp in specs]
+    params = [(f64(li.w), f64(li.b), f64(li.gamma), f64(li.beta)) for li in inp["layers"]]
+    x0, dy = f64(inp["x"]), f64(inp["dy"])
+    t0 = time.perf_counter()
+    acts, fw = [x0], []
+    for OL, (w, b, gm, bt) in zip(ols, params):
+        f = oracle.fwd_train(OL, acts[-1], w, b, gm, bt)
+        fw.append(f)
+        acts.append(f["y"])
+    g = dy
+    for OL, (w, b, gm, bt), f, a in zip(reversed(ols), reversed(params), reversed(fw), reversed(acts[:-1])):
+        g = oracle.bwd(OL, a, w, f["ypre"], g, gm, bt, f["mean"], f["inv_std"])["dx"]
+    dt = time.perf_counter() - t0
+    flops = sum(sp.flops_step() for sp in specs)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d image(s) of this workload, one fwd_train + bwd step (%.3f GFLOP fp64, %.2f s)"
+                      % (n_img, flops / 1e9, dt)}
+
+
+def per_config_cpu():
+    """CPU baselines of every per-config entry (run before any GPU work)."""
+    return {label: cpu_baseline_config(name, over, CPU_SAMPLE_IMAGES[name]) for label, name, over in PER_CONFIG}
+
+
+def tf32_peak():
+    """Dense TF32 tensor throughput of this GPU: a cuBLAS fp32 matmul of 8192^3 with TF32 allowed
+    (torch.matmul), best of 10 CUDA-event timings. The fp32 layers run 3xTF32, whose bound is a third of
+    it. Measured in the run, outside every timed region."""
+    import torch
+
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        n = 8192
+        a = torch.randn(n, n, device="cuda")
+        b = torch.randn(n, n, device="cuda")
+        c = torch.empty(n, n, device="cuda")
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        best = 1e30
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b, c
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+def layer_bytes(sp):
+    """Algorithmic HBM bytes of one training step of a layer (each tensor moved once per pass that needs
+    it): the three GEMMs read and write their operands (fprop X, W, pre_act; dgrad d_conv, W, dX; wgrad
+    d_conv, X, dW in fp32); with a norm, apply 2|Y|, backward reduce 2|Y|, d_conv 3|Y|; without, the
+    activation is in the fprop epilogue (one more |Y| write) and d_conv 3|Y|."""
+    es = 2 if sp.dtype == 1 else 4
+    x = sp.N * sp.H * sp.W * sp.IC * es
+    y = sp.n_pix * sp.OC * es
+    w = sp.OC * sp.KH * sp.KW * sp.IC * es
+    gemm = (x + w + y) + (y + w + x) + (y + x + sp.OC * sp.KH * sp.KW * sp.IC * 4)
+    return gemm + (7 * y if sp.norm != 0 else 4 * y)
+
+
 def per_config_timing(peaks, steps=10, warmup=3):
     """fwd_train + bwd of every workload (the mixed stack as its two chained layers) and of the BN-layer and
     large shapes with layer and group norm: step time through the ABI calls, the same step replayed from a
@@ -321,10 +407,23 @@ def per_config_timing(peaks, steps=10, warmup=3):
         tensor_bytes = sum(s.n_pix * s.OC * (2 if s.dtype == 1 else 4) for s in specs)
         hbm = {k: round(HBM_TENSORS[k] * tensor_bytes / (t * 1e-3) / 1e9 / peaks["hbm"], 3)
                for k, t in kern.items() if k in HBM_TENSORS}
+        bf = specs[0].dtype == 1
+        # the tensor-core bound of the contractions: bf16 burst, or a third of the measured TF32 rate for
+        # 3xTF32; GEMM kernels (the column-form dgrad's GEMM is a launch named fprop_gemm)
+        gemm_ms = sum(t for k, t in kern.items() if k.endswith("_gemm"))
+        peak = peaks["bf16"] if bf else (peaks["tf32"] / 3 if peaks.get("tf32") else None)
+        ach = fl / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
+        floor_ms = sum(layer_bytes(sp) for sp in specs) / (peaks["hbm"] * 1e9) * 1e3
+        roof = {"bound": "tensor", "kind": "bf16 burst" if bf else "3xTF32: measured TF32 burst / 3",
+                "gemm_ms": round(gemm_ms, 4), "achieved": round(ach, 1) if ach else None, "unit": "TFLOP/s",
+                "peak": round(peak, 1) if peak else None,
+                "frac": round(ach / peak, 4) if (ach and peak) else None,
+                "memory_floor_ms": round(floor_ms, 4), "step_frac_of_memory_floor": round(floor_ms / ms, 4)}
         out[label] = {"ms_per_step": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
                       "ms_per_step_graph": round(ms_graph, 4),
-                      "dtype": "bf16" if specs[0].dtype == 1 else "fp32 (3xTF32)", "layers": len(specs),
-                      "kernels_ms": {k: round(t, 4) for k, t in kern.items()}, "hbm_frac_of_measured": hbm}
+                      "dtype": "bf16" if bf else "fp32 (3xTF32)", "layers": len(specs),
+                      "kernels_ms": {k: round(t, 4) for k, t in kern.items()}, "hbm_frac_of_measured": hbm,
+                      "roofline": roof}
         release()
         torch.cuda.empty_cache()
     abi.check(abi.conv2d_device_status()[0], "device status")
@@ -394,7 +493,7 @@ def gemm_roofline(spec, kern, steps, peaks):
         e = {"launches": n, "avg_ms": round(avg, 4), "share": 0.0}
         if name in ("fprop_gemm", "dgrad_gemm", "wgrad_gemm"):
             a = gemm_flops / (avg * 1e-3) / 1e12
-            e.update(bound="tensor", achieved=round(a, 1), unit="TFLOP/s", frac=round(a / peaks["bf16_sust"], 4))
+            e.update(bound="tensor", achieved=round(a, 1), unit="TFLOP/s", frac=round(a / peaks["bf16"], 4))
         elif name in bytes_per:
             a = bytes_per[name] / (avg * 1e-3) / 1e9
             e.update(bound="hbm", achieved=round(a, 1), unit="GB/s", frac=round(a / peaks["hbm"], 4))
@@ -515,8 +614,11 @@ def main():
 
     # the CPU baseline runs before any GPU work (rank 0, single GPU only)
     cpu = None
+    cpu_cfg = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.ref_images)
+        if not args.no_per_config and not args.images:
+            cpu_cfg = per_config_cpu()
 
     import torch
     if world > 1:
@@ -526,8 +628,12 @@ def main():
     r = run_gpu(args, rank, world, local_rank)
     ms, e2e_ms = r["ms"], r["e2e_ms"]
     per_cfg = None
+    tf32 = None
     if rank == 0 and world == 1 and not args.no_per_config and not args.images:
-        per_cfg = per_config_timing(_peaks())
+        tf32 = tf32_peak()
+        per_cfg = per_config_timing(dict(_peaks(), tf32=tf32))
+        for label, c in (cpu_cfg or {}).items():
+            per_cfg[label]["cpu_baseline"] = c
     if world > 1:
         ms, e2e_ms = max_over_ranks([ms, e2e_ms], "cuda")
     if rank != 0:
@@ -552,10 +658,11 @@ def main():
                               "of_measured_sustained": round(value / world / peaks["bf16_sust"], 4),
                               "of_nominal_2250": round(value / world / NOMINAL_BF16_TFLOPS, 4),
                               "peaks": peaks["src"]},
-        "roofline": {"kernel": dom, "bound": "tensor", "achieved": d["achieved"], "peak": peaks["bf16_sust"],
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": d["achieved"], "peak": peaks["bf16"],
                      "unit": "TFLOP/s", "frac": d["frac"],
                      "traffic": NCU_TRAFFIC_BYTES.get(dom) if spec.N == 256 else None,
-                     "peak_kind": "bf16 sustained (%s)" % peaks["src"]},
+                     "peak_kind": "bf16 burst (%s): the kernel is timed with CUDA events inside a region of "
+                                  "about 50 ms, not a seconds-long loop" % peaks["src"]},
         "kernels": kern,
         "kernels_timing": {"ms_per_step_instrumented": round(r["ms_instr"], 4),
                            "what": "per-launch CUDA events over a second timed region of the same steps"},
@@ -566,6 +673,8 @@ def main():
                         "calls; the copies of step k+1 overlap step k (second stream, two input buffers)"},
         "clocks": r["clocks"],
         "per_config": per_cfg,
+        "tf32_peak": ({"burst_tflops": round(tf32, 1), "how": "cuBLAS fp32 matmul 8192^3 with TF32 allowed "
+                       "(torch.matmul), best of 10, measured in this run"} if tf32 else None),
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

@@ -252,9 +252,28 @@ int make_geo(const conv2d_desc* d, Geo* g) {
 
 // ------------------------------------------------------------ GEMM planning
 struct Tile {
-  int BN, n_tiles, stages;
+  int BN, n_tiles, stages, kps;
   size_t smem;
 };
+
+// k-blocks per shared-memory stage (ConvGemmParams::kps): with the A operand by TMA, two when at least
+// three such stages fit, so that the producer, split and MMA warps pass one barrier per two k-blocks.
+constexpr int kKpsMax = kMaxKps;
+
+// Stages of `sub` bytes per k-block beside `reserve` bytes of epilogue scratch; grouped: the A operand
+// comes by TMA (k-blocks may be grouped per stage).
+void fit_stages(Tile& t, size_t sub, size_t reserve, bool grouped) {
+  const size_t room = kMaxDynSmem - 2048 - reserve;
+  t.kps = (grouped && kKpsMax > 1 && room / (kKpsMax * sub) >= 3) ? kKpsMax : 1;
+  t.stages = static_cast<int>(std::min<size_t>(kMaxStages, room / (t.kps * sub)));
+  t.smem = t.stages * t.kps * sub + 1024 + 512 + reserve;  // alignment slack, barriers + TMEM slot, scratch
+}
+
+// Shared-memory bytes of one k-block of a stage of the fprop / dgrad GEMM (pair: half of B per CTA).
+size_t conv_sub_bytes(const Geo& g, int BN, bool ts, bool pair) {
+  if (g.dt == CONV2D_BF16) return kBM * 128 + static_cast<size_t>(pair ? BN / 2 : BN) * 128;
+  return (ts ? 1 : 2) * static_cast<size_t>(kBM) * 128 + 2 * static_cast<size_t>(BN) * 128;
+}
 
 // fp32 (3xTF32): the tensor core's fp32 accumulation loses a little on every MMA step (12 per k-block),
 // and the loss grows with the steps that feed one accumulator, so a deep K loop accumulates in chunks of
@@ -271,12 +290,36 @@ Tile conv_tile(const Geo& g, int ncols, long kdepth) {
   if (g.dt != CONV2D_BF16) bn_max = std::max(32, std::min(bn_max, 512 / fp32_chunks(kdepth) / 32 * 32));
   t.n_tiles = static_cast<int>(ceil_div(ncols, bn_max));
   t.BN = static_cast<int>(round_up(ceil_div(ncols, t.n_tiles), 32));  // the epilogue reads 32 columns at a time
-  const size_t ns = g.dt == CONV2D_BF16 ? 1 : 2;
-  const size_t stage = ns * (kBM * 128 + static_cast<size_t>(t.BN) * 128);
-  const size_t stats = 12 * static_cast<size_t>(t.BN) * 4;  // epilogue statistics scratch + column constants
-  t.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048 - stats) / stage));
-  t.smem = t.stages * stage + 1024 + 512 + stats;  // alignment slack, barriers + TMEM slot, epilogue scratch
+  // epilogue statistics scratch + column constants; one k-block per stage until the A path is known
+  fit_stages(t, conv_sub_bytes(g, t.BN, false, false), 12 * static_cast<size_t>(t.BN) * 4, false);
   return t;
+}
+
+// fp32 GEMMs with the A operand by TMA hold A in TMEM (ConvGemmParams::ts): kTaKb * 64 TMEM columns for
+// A and at least two accumulators of 2 * BN columns per chunk beside them, so BN * chunks <= 64. A stage
+// then holds the raw A tiles and B's hi and lo rows. Returns false when the K loop needs more chunks.
+bool ts_tile(const Geo& g, int ncols, long kdepth, Tile* out) {
+  if (g.dt == CONV2D_BF16) return false;
+  const int nch = fp32_chunks(kdepth);
+  if (nch > 2) return false;
+  Tile t;
+  t.n_tiles = static_cast<int>(ceil_div(ncols, 64 / nch));
+  t.BN = static_cast<int>(round_up(ceil_div(ncols, t.n_tiles), 32));
+  if (t.BN * nch > 64) return false;
+  fit_stages(t, conv_sub_bytes(g, t.BN, true, false), 12 * static_cast<size_t>(t.BN) * 4, true);
+  *out = t;
+  return true;
+}
+
+// fprop A operand by TMA im2col: whole 128-byte channel chunks, or the folded view (see fold_kw)
+bool fold_kw(const Geo& g);
+bool fprop_a_tma(const Geo& g) { return g.ICp % g.BKE == 0 || fold_kw(g); }
+
+// Column tiles of the fprop GEMM (the layer-norm row partials are laid out per column tile).
+int fprop_n_tiles(const Geo& g) {
+  Tile t;
+  if (fprop_a_tma(g) && ts_tile(g, g.OC, g.Kf, &t)) return t.n_tiles;
+  return conv_tile(g, g.OC, g.Kf).n_tiles;
 }
 
 // Accumulator chunks of an fp32 GEMM whose longest tile K loop has max_kb k-blocks (see kFp32ChunkKb).
@@ -299,10 +342,9 @@ bool try_pair(ConvGemmParams& p, Tile& t, const Geo& g, const DevInfo* dev, long
   // an even tile count: every tile of a pair holds rows of the layer
   if (!kUsePair || g.dt != CONV2D_BF16 || !p.a_tma || p.num_phases != 1 || t.BN % 32 != 0 || (m_tiles & 1))
     return false;
-  const size_t stage = kBM * 128 + static_cast<size_t>(t.BN / 2) * 128;
-  const size_t stats = 12 * static_cast<size_t>(t.BN) * 4;
-  const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048 - stats) / stage));
-  const size_t smem = stages * stage + 1024 + 512 + stats;
+  Tile pt = t;
+  fit_stages(pt, conv_sub_bytes(g, t.BN, false, true), 12 * static_cast<size_t>(t.BN) * 4, true);
+  const size_t smem = pt.smem;
   static std::mutex mu;
   static size_t cached_smem = 0;
   static int cached_clusters = 0;
@@ -321,9 +363,9 @@ bool try_pair(ConvGemmParams& p, Tile& t, const Geo& g, const DevInfo* dev, long
   p.tmap_b = half;
   p.pair = 1;
   p.num_units = static_cast<int>(m_tiles / 2) * t.n_tiles;
-  p.stages = stages;
-  t.stages = stages;
-  t.smem = smem;
+  p.stages = pt.stages;
+  p.kps = pt.kps;
+  t = pt;
   *grid = 2 * std::min(p.num_units, std::min(clusters, dev->sms / 2));
   return true;
 }
@@ -395,11 +437,14 @@ WgradPlan wgrad_plan(const Geo& g, int sms) {
   const size_t stage = ns * (kBM * 128 + static_cast<size_t>(w.BN) * 128);
   w.rstages = 0;
   if (wgrad_raw_tma(g)) {
-    // two hi / lo stages for the MMA, the rest of shared memory for raw tiles in flight
+    // A (X) in TMEM: a stage holds the d_conv hi and lo rows, and each stage has a TMEM stage of A
+    // (64 columns) beside the two accumulators of 2 * BN columns; the rest of shared memory holds raw
+    // tiles in flight
+    const size_t tstage = 2 * static_cast<size_t>(w.BN) * 128;
     const size_t raw = kBM * 128 + static_cast<size_t>(w.BN) * 128;
-    w.stages = 2;
-    w.rstages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048 - 2 * stage) / raw));
-    w.smem = 2 * stage + w.rstages * raw + 1024 + 512;
+    w.stages = std::min(kMaxStages, (512 - 4 * w.BN) / 64);
+    w.rstages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048 - w.stages * tstage) / raw));
+    w.smem = w.stages * tstage + w.rstages * raw + 1024 + 512;
     return w;
   }
   w.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048) / stage));
@@ -414,6 +459,7 @@ struct DgradPlan {
   int Kd;
   int units;
   Tile tile;
+  int ts;  // fp32 with d_conv by TMA: A in TMEM (see ts_tile)
 };
 
 // dgrad through TMA im2col: stride 1 or 2 (one map per stride phase), whole 128-byte channel chunks of
@@ -425,6 +471,7 @@ DgradPlan dgrad_plan(const Geo& g) {
   std::memset(&d, 0, sizeof(d));
   d.tile = conv_tile(g, g.IC, static_cast<long>(g.taps) * g.OCp);
   d.table.flip = dgrad_tma(g) ? 1 : 0;
+  d.ts = d.table.flip && ts_tile(g, g.IC, static_cast<long>(g.taps) * g.OCp, &d.tile) ? 1 : 0;
   const int S = g.S;
   int unit = 0, col = 0, n = 0;
   for (int ph_h = 0; ph_h < S; ++ph_h)
@@ -503,7 +550,8 @@ void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
     if (op == CONV2D_OP_FWD_TRAIN && g.norm == CONV2D_NORM_BATCH)
       sz[R_PART] = static_cast<size_t>(ceil_div(g.n_pix, kBM)) * g.OC * 3 * 4;  // per-tile statistics
     if (ln)  // per-pixel, per-column-tile, per-half (mean, M2) of the stored conv output
-      sz[R_PART] = static_cast<size_t>(g.n_pix) * conv_tile(g, g.OC, g.Kf).n_tiles * 2 * 2 * 4;
+      sz[R_PART] = static_cast<size_t>(g.n_pix) * std::max(conv_tile(g, g.OC, g.Kf).n_tiles, fprop_n_tiles(g)) *
+                   2 * 2 * 4;
     if (gn)  // per-block, per-channel (rows, mean, M2) of the stored conv output
       sz[R_PART] = G * g.OC * 3 * 4;
     if (op == CONV2D_OP_FWD_INFER) {
@@ -559,8 +607,6 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   std::memset(&p, 0, sizeof(p));
   Tile t = conv_tile(g, g.OC, g.Kf);
   const bool bf = g.dt == CONV2D_BF16;
-  if (!encode_2d(&p.tmap_b, bhi, bf, g.Kf, g.OC, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
-  if (!bf && !encode_2d(&p.tmap_b_lo, blo, false, g.Kf, g.OC, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
   p.src = xsrc;
   p.Hs = g.H;
   p.Ws = g.W;
@@ -583,10 +629,7 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   ph.div_Wa = make_fastdiv(g.OW);
   ph.div_HaWa = make_fastdiv(g.OH * g.OW);
   ph.div_Tw = make_fastdiv(g.KW);
-  p.n_tiles = t.n_tiles;
-  p.BN = t.BN;
   p.N = g.OC;
-  p.num_units = static_cast<int>(ceil_div(g.n_pix, kBM)) * t.n_tiles;
   p.out = out;
   p.out2 = out2;
   p.out_ld = g.OC;
@@ -621,10 +664,20 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
     ph.a_lo_w = -g.P;
     ph.a_map = 0;
   }
+  // fp32 with A by TMA: A in TMEM when the K loop allows it (see ts_tile); bf16 with A by TMA: k-blocks
+  // grouped per stage
+  if (!bf && p.a_tma && ts_tile(g, g.OC, g.Kf, &t)) p.ts = 1;
+  if (bf && p.a_tma) fit_stages(t, conv_sub_bytes(g, t.BN, false, false), 12 * static_cast<size_t>(t.BN) * 4, true);
+  if (!encode_2d(&p.tmap_b, bhi, bf, g.Kf, g.OC, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
+  if (!bf && !encode_2d(&p.tmap_b_lo, blo, false, g.Kf, g.OC, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
+  p.n_tiles = t.n_tiles;
+  p.BN = t.BN;
+  p.num_units = static_cast<int>(ceil_div(g.n_pix, kBM)) * t.n_tiles;
   p.stages = t.stages;
+  p.kps = t.kps;
   p.err = dev->err;
   set_chunks(p, g, t.BN, ph.num_kb);
-  if (bf && t.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
+  if (bf && !p.a_tma && t.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;  // the gather's copies in flight
   if (rs_layout) {
     const bool ep8 = bf && p.a_tma;  // the kernel's eight-warp epilogue splits the columns in two halves
     rs_layout->n_tiles = t.n_tiles;
@@ -722,15 +775,19 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
     }
     p.a_tma = 1;
     p.a_chunks = g.OCp / g.BKE;
+    p.ts = d.ts;
   }
+  if (bf && p.a_tma)
+    fit_stages(d.tile, conv_sub_bytes(g, d.tile.BN, false, false), 12 * static_cast<size_t>(d.tile.BN) * 4, true);
   p.stages = d.tile.stages;
+  p.kps = d.tile.kps;
   p.err = dev->err;
   {
     int max_kb = 0;
     for (int i = 0; i < d.num_phases; ++i) max_kb = std::max(max_kb, d.ph[i].num_kb);
     set_chunks(p, g, d.tile.BN, max_kb);
   }
-  if (bf && d.tile.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
+  if (bf && !p.a_tma && d.tile.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;  // the gather's copies
   int grid = std::min(p.num_units, dev->sms);
   if (bf) try_pair(p, d.tile, g, dev, ceil_div(p.ph[0].rows, kBM), whi, d.Kd, g.ICp, &grid);
   LAUNCH("dgrad_gemm", st,
@@ -785,6 +842,7 @@ int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dc
         !encode_2d(&p.tmap_dc, dconv, false, g.OCp, g.n_pix, 32, 32))
       return CONV2D_ERR_CUDA;
     p.a_tma = 1;
+    p.ts = 1;
     p.rstages = w.rstages;
     if (fold) {
       p.Cs = cs;

@@ -37,6 +37,8 @@ constexpr int kMaxTmaPhases = 4;  // stride phases whose A operand may come by T
 constexpr int kBM = 128;          // rows of a tile (TMEM lanes)
 constexpr int kMaxTmemBufs = 8;   // TMEM accumulators of the fprop / dgrad kernel (512 columns / BN, capped)
 constexpr int kLag = 3;           // cp.async groups kept in flight per producer thread (needs >= 4 stages)
+constexpr int kTaKb = 4;          // fp32 with A in TMEM: k-blocks of A held in TMEM (hi and lo, 32 columns each)
+constexpr int kMaxKps = 2;        // k-blocks per shared-memory stage (TMA paths)
 
 // wait sites recorded in the error word
 enum : int { kSiteFull = 1, kSiteEmpty = 2, kSiteTFull = 3, kSiteTEmpty = 4 };
@@ -106,9 +108,19 @@ struct ConvGemmParams {
   int a_tma;
   int a_chunks;           // Cs / channels per chunk
   int stages;
+  // k-blocks per stage (1 .. kMaxKps; more than one only with the A operand by TMA): the barriers of a
+  // stage are passed once for all of its k-blocks, which halves the hand-offs between the producer, split
+  // and MMA warps (each costs about a hundred nanoseconds whatever the work behind it)
+  int kps;
   // fp32 (3xTF32) only: the K loop of a tile accumulates in nch chunks of kpc k-blocks, each in its own
-  // BN TMEM columns, summed by the epilogue (nch * BN <= 512); bf16 uses one chunk
+  // BN TMEM columns (2 * BN with ts), summed by the epilogue; bf16 uses one chunk
   int kpc, nch;
+  // fp32 with A by TMA: A in tensor memory. The producer warps split each landed A tile into tf32 hi / lo
+  // and store both into a ring of TMEM stages (kTaKb k-blocks in all); per 8-wide k-step the MMAs run
+  // D[:, 0:2BN] += A_hi x [B_hi; B_lo] and D[:, 0:BN] += A_lo x B_hi (B from shared memory, its lo rows
+  // right after its hi rows), and the epilogue adds columns BN .. 2BN - 1 into 0 .. BN - 1. A shared-memory
+  // stage then holds the raw A tile and B only, and the tensor core reads no A operand from shared memory
+  int ts;
   int* err;
   ConvPhase ph[kMaxPhases];
 };
@@ -131,6 +143,9 @@ struct WgradParams {
   float* partial;         // [splits][N][Mk]
   int stages;
   int pair;               // CTA pairs (cta_group::2, bf16 with A by TMA): m_tiles counts pairs of m-tiles
+  // fp32 with raw TMA tiles: A (X, k rows x 32 pixels) in tensor memory, one TMEM stage per shared-memory
+  // stage, which then holds the d_conv hi and lo rows only; the MMAs as in ConvGemmParams::ts
+  int ts;
   int* err;
 };
 
@@ -282,22 +297,26 @@ static __device__ __noinline__ void colstats32(uint32_t taddr, bool zero, const 
   *reinterpret_cast<float2*>(dst + 8 * j + cp) = make_float2(x[0], x[1]);
 }
 
-// Sum the accumulator chunks 1 .. n-1 of a tile into chunk 0, in fp32 round-to-nearest: columns
-// [c0, c1) (multiples of 16) of this warp's lane quarter, chunk i starting i * stride columns after
-// taddr. The tensor core's fp32 accumulation loses a little on every MMA step; a deep K loop split
-// over chunks keeps that loss to the steps of one chunk. Warp-collective.
+// Sum the accumulator chunks 1 .. n-1 (n >= 2) of a tile into chunk 0, in fp32 round-to-nearest and
+// chunk order: columns [c0, c1) (multiples of 32) of this warp's lane quarter, chunk i starting
+// i * stride columns after taddr. The tensor core's fp32 accumulation loses a little on every MMA step;
+// a deep K loop split over chunks keeps that loss to the steps of one chunk. With A in TMEM each chunk
+// is itself two column blocks (see ConvGemmParams::ts). Warp-collective.
 static __device__ __noinline__ void fold_chunks(uint32_t taddr, int stride, int n, int c0, int c1) {
-  for (int c = c0; c < c1; c += 16) {
-    uint32_t a[16], b[16];
-    tmem_ld16(taddr + c, a);
-    tmem_ld_wait(a);
-    for (int i = 1; i < n; ++i) {
-      tmem_ld16(taddr + static_cast<uint32_t>(i * stride + c), b);
-      tmem_ld_wait(b);
+  for (int c = c0; c < c1; c += 32) {
+    uint32_t a[32], b[32];
+    tmem_ld32(taddr + c, a);
+    tmem_ld32(taddr + static_cast<uint32_t>(stride + c), b);
+    tmem_ld_wait2(a, b);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) a[e] = __float_as_uint(__uint_as_float(a[e]) + __uint_as_float(b[e]));
+    for (int e = 0; e < 32; ++e) a[e] = __float_as_uint(__uint_as_float(a[e]) + __uint_as_float(b[e]));
+    for (int i = 2; i < n; ++i) {
+      tmem_ld32(taddr + static_cast<uint32_t>(i * stride + c), b);
+      tmem_ld_wait2(a, b);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) a[e] = __float_as_uint(__uint_as_float(a[e]) + __uint_as_float(b[e]));
     }
-    tmem_st16(taddr + c, a);
+    tmem_st32(taddr + c, a);
   }
   tmem_st_wait();
 }
@@ -378,14 +397,20 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
   const uint32_t a_bytes = kBM * 128, b_bytes = BN * 128;
   // a pair member holds its 128 rows of A and half of B's columns
   const uint32_t b_own = pair ? b_bytes / 2 : b_bytes;
-  const uint32_t stage_bytes = D::NS * (a_bytes + b_own);
+  // fp32 with A in TMEM (see ConvGemmParams::ts): a stage holds the raw A tile, B hi and B lo
+  const bool ts = DT == 0 && p.ts;
+  const uint32_t a_tiles = (DT == 0 && !ts) ? 2u : 1u;  // A tiles per k-block (fp32 in shared memory: hi, lo)
+  const int KPS = p.kps > 1 ? p.kps : 1;                // k-blocks per stage
+  const uint32_t sub_bytes = a_tiles * a_bytes + D::NS * b_own;  // one k-block of a stage
+  const uint32_t stage_bytes = KPS * sub_bytes;
   const int S = p.stages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_bytes);
   uint64_t* empty = full + kMaxStages;
   uint64_t* tfull = empty + kMaxStages;
   uint64_t* tempty = tfull + kMaxTmemBufs;
   uint64_t* sfull = tempty + kMaxTmemBufs;  // fp32 with A by TMA: the stage is split into hi / lo
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfull + kMaxStages);
+  uint64_t* aempty = sfull + kMaxStages;    // fp32 with A in TMEM: the MMAs have read a TMEM stage of A
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aempty + kMaxStages);
   const uint32_t sbase = smem_u32(smem);
   // fp32 with A by TMA: warps 2-5 split the stages (and the epilogue keeps four warps)
   const bool split_a = DT == 0 && p.a_tma;
@@ -402,9 +427,15 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
   // fp32: nch accumulator chunks of BN columns per tile (see ConvGemmParams::kpc)
   const int nch = DT == 0 && p.nch > 1 ? p.nch : 1;
   const int kpc = DT == 0 && p.nch > 1 ? p.kpc : (1 << 30);
-  const int tcs = nch * BN;  // TMEM columns of one tile
-  const int nbuf = 512 / tcs < kMaxTmemBufs ? 512 / tcs : kMaxTmemBufs;
-  const uint32_t tcols = tmem_cols_for(nbuf * tcs);
+  const int ccols = ts ? 2 * BN : BN;  // TMEM columns of one accumulator chunk
+  const int tcs = nch * ccols;         // TMEM columns of one tile
+  // with A in TMEM the last kTaKb * 64 columns hold TA stages of KPS k-blocks of A (per k-block hi: 32
+  // columns, then lo: 32)
+  const int TA = kTaKb / KPS;
+  const int ta_cols = ts ? kTaKb * 64 : 0;
+  const int nbuf = (512 - ta_cols) / tcs < kMaxTmemBufs ? (512 - ta_cols) / tcs : kMaxTmemBufs;
+  const uint32_t tcols = tmem_cols_for(nbuf * tcs + ta_cols);
+  const uint32_t ta0 = static_cast<uint32_t>(nbuf * tcs);  // first TMEM column of the A stages
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -416,8 +447,10 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       // one arrival per epilogue warp (of both CTAs when paired: the even CTA's MMA writes both TMEMs)
       mbar_init(&tempty[b], (ep8 ? 8 : 4) * (pair ? 2 : 1));
     }
-    if (split_a)
-      for (int s = 0; s < S; ++s) mbar_init(&sfull[s], 4);  // one arrival per splitting warp
+    if (split_a)  // with A in TMEM indexed by TMEM stage
+      for (int s = 0; s < (ts ? TA : S); ++s) mbar_init(&sfull[s], 4);  // one arrival per splitting warp
+    if (ts)
+      for (int j = 0; j < TA; ++j) mbar_init(&aempty[j], 1);  // the MMA warp's commit
     fence_mbar_init();
     tma_prefetch_desc(&p.tmap_b);
     if (D::NS == 2) tma_prefetch_desc(&p.tmap_b_lo);
@@ -459,33 +492,46 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           ah = a * p.rs + ph.a_lo_h;
           aw = (rem - a * ph.Wa) * p.rs + ph.a_lo_w;
         }
-        for (int kb = 0; kb < ph.num_kb; ++kb) {
+        // im2col offsets of k-block kb = (tt * Tw + tw) * a_chunks + ck, advanced by counters (this thread
+        // issues every copy of the CTA, so its per-k-block path is kept free of divisions)
+        int ck = 0, tw = 0, tt = 0;
+        for (int g0 = 0; g0 < ph.num_kb; g0 += KPS) {  // one stage: k-blocks g0 .. g0 + nk - 1
+          const int nk = min(KPS, ph.num_kb - g0);
           if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
             alive = false;
             break;
           }
-          const uint32_t a0 = sbase + s * stage_bytes;
-          const uint32_t b0 = a0 + D::NS * a_bytes;
+          // both pair members' loads complete on the even CTA's full barrier, which expects them all
+          const uint32_t bar = pair ? mapa_shared(smem_u32(&full[s]), 0) : 0u;
           if (pair) {
-            // both members' loads complete on the even CTA's full barrier, which expects them all
-            const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
-            if (leader) mbar_arrive_expect_tx(&full[s], 2 * (a_bytes + b_own));
-            const int tap = kb / p.a_chunks;
-            const int tt = static_cast<int>(fdiv(static_cast<uint32_t>(tap), ph.div_Tw));
-            tma_load_im2col_4d_pair(a0, &p.tmap_a[0], bar, (kb - tap * p.a_chunks) * D::BKE, aw, ah, an,
-                                    static_cast<uint16_t>(tap - tt * ph.Tw), static_cast<uint16_t>(tt));
-            tma_load_2d_pair(b0, &p.tmap_b, bar, ph.b_col + kb * D::BKE,
-                             n_tile * BN + static_cast<int>(rank) * (BN / 2));
+            if (leader) mbar_arrive_expect_tx(&full[s], 2u * nk * (a_bytes + b_own));
           } else {
-            mbar_arrive_expect_tx(&full[s], D::NS * b_bytes + (p.a_tma ? a_bytes : 0u));
-            if (p.a_tma) {
-              const int tap = kb / p.a_chunks;
-              const int tt = static_cast<int>(fdiv(static_cast<uint32_t>(tap), ph.div_Tw));
-              tma_load_im2col_4d(a0, &p.tmap_a[ph.a_map], &full[s], (kb - tap * p.a_chunks) * D::BKE, aw, ah, an,
-                                 static_cast<uint16_t>(tap - tt * ph.Tw), static_cast<uint16_t>(tt));
+            mbar_arrive_expect_tx(&full[s], nk * (D::NS * b_bytes + (p.a_tma ? a_bytes : 0u)));
+          }
+#pragma unroll
+          for (int i = 0; i < kMaxKps; ++i) {
+            if (i >= nk) break;
+            const int kcol = ph.b_col + (g0 + i) * D::BKE;
+            const uint32_t a0 = sbase + s * stage_bytes + i * sub_bytes;
+            const uint32_t b0 = a0 + a_tiles * a_bytes;
+            if (pair) {
+              tma_load_im2col_4d_pair(a0, &p.tmap_a[0], bar, ck * D::BKE, aw, ah, an, static_cast<uint16_t>(tw),
+                                      static_cast<uint16_t>(tt));
+              tma_load_2d_pair(b0, &p.tmap_b, bar, kcol, n_tile * BN + static_cast<int>(rank) * (BN / 2));
+            } else {
+              if (p.a_tma)
+                tma_load_im2col_4d(a0, &p.tmap_a[ph.a_map], &full[s], ck * D::BKE, aw, ah, an,
+                                   static_cast<uint16_t>(tw), static_cast<uint16_t>(tt));
+              tma_load_2d(b0, &p.tmap_b, &full[s], kcol, n_tile * BN);
+              if (D::NS == 2) tma_load_2d(b0 + b_bytes, &p.tmap_b_lo, &full[s], kcol, n_tile * BN);
             }
-            tma_load_2d(b0, &p.tmap_b, &full[s], ph.b_col + kb * D::BKE, n_tile * BN);
-            if (D::NS == 2) tma_load_2d(b0 + b_bytes, &p.tmap_b_lo, &full[s], ph.b_col + kb * D::BKE, n_tile * BN);
+            if (++ck == p.a_chunks) {  // (without A by TMA a_chunks is 0 and the counters are unused)
+              ck = 0;
+              if (++tw == ph.Tw) {
+                tw = 0;
+                ++tt;
+              }
+            }
           }
           if (++s == S) {
             s = 0;
@@ -509,8 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     // ------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       const uint32_t idesc = idesc_f32acc(pair ? 2 * kBM : kBM, BN, D::FMT, false, false);
-      int s = 0;
-      uint32_t par = 0;
+      const uint32_t idesc2 = idesc_f32acc(kBM, 2 * BN, D::FMT, false, false);  // A_hi x [B_hi; B_lo]
+      int s = 0, j = 0;
+      uint32_t par = 0, apar = 0;
       int tc = 0;
       bool alive = true;
       for (int u = cid; u < p.num_units && alive; u += ncl, ++tc) {
@@ -519,37 +566,60 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         if (!wait(&tempty[buf], ((tc / nbuf) & 1) ^ 1, p.err, kSiteTEmpty)) break;
         tc_fence_after();
         const uint32_t dt = tmem_base + buf * tcs;
-        for (int kb = 0; kb < ph.num_kb; ++kb) {
-          const uint32_t d = DT == 0 ? dt + static_cast<uint32_t>((kb / kpc) * BN) : dt;
-          const int kc = DT == 0 ? kb % kpc : kb;  // k-block within the accumulator chunk
-          if (!wait(split_a ? &sfull[s] : &full[s], par, p.err, kSiteFull)) {
+        for (int g0 = 0; g0 < ph.num_kb; g0 += KPS) {  // one stage: k-blocks g0 .. g0 + nk - 1
+          const int nk = min(KPS, ph.num_kb - g0);
+          // with A in TMEM the split warps arrive on the TMEM stage's barrier after the shared-memory stage
+          // has landed, so that one wait covers both
+          if (!wait(ts ? &sfull[j] : (split_a ? &sfull[s] : &full[s]), ts ? apar : par, p.err, kSiteFull)) {
             alive = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = sbase + s * stage_bytes;
-          const uint32_t b0 = a0 + D::NS * a_bytes;
 #pragma unroll
-          for (int kk = 0; kk < 128 / 32; ++kk) {
-            const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
-            const uint32_t acc = (kc | kk) ? 1u : 0u;
-            if (DT == 1) {
-              if (pair) mma_bf16_pair(d, ad, bd, idesc, acc);
-              else mma_bf16(d, ad, bd, idesc, acc);
-            } else {
-              const uint64_t al = sdesc_sw128(a0 + a_bytes + kk * 32, 16, 1024);
-              const uint64_t bl = sdesc_sw128(b0 + b_bytes + kk * 32, 16, 1024);
-              mma_tf32(d, al, bd, idesc, acc);
-              mma_tf32(d, ad, bl, idesc, 1u);
-              mma_tf32(d, ad, bd, idesc, 1u);
+          for (int i = 0; i < kMaxKps; ++i) {
+            if (i >= nk) break;
+            const int kb = g0 + i;
+            const uint32_t d = DT == 0 ? dt + static_cast<uint32_t>((kb / kpc) * ccols) : dt;
+            const int kc = DT == 0 ? kb % kpc : kb;  // k-block within the accumulator chunk
+            const uint32_t a0 = sbase + s * stage_bytes + i * sub_bytes;
+            const uint32_t b0 = a0 + a_tiles * a_bytes;
+            if (ts) {
+              const uint32_t ah = tmem_base + ta0 + static_cast<uint32_t>((j * KPS + i) * 64), al = ah + 32;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);  // 2 BN rows: hi, then lo
+                mma_tf32_ta(d, ah + kk * 8, bd, idesc2, (kc | kk) ? 1u : 0u);
+                mma_tf32_ta(d, al + kk * 8, bd, idesc, 1u);
+              }
+              continue;
+            }
+#pragma unroll
+            for (int kk = 0; kk < 128 / 32; ++kk) {
+              const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
+              const uint32_t acc = (kc | kk) ? 1u : 0u;
+              if (DT == 1) {
+                if (pair) mma_bf16_pair(d, ad, bd, idesc, acc);
+                else mma_bf16(d, ad, bd, idesc, acc);
+              } else {
+                const uint64_t al = sdesc_sw128(a0 + a_bytes + kk * 32, 16, 1024);
+                const uint64_t bl = sdesc_sw128(b0 + b_bytes + kk * 32, 16, 1024);
+                mma_tf32(d, al, bd, idesc, acc);
+                mma_tf32(d, ad, bl, idesc, 1u);
+                mma_tf32(d, ad, bd, idesc, 1u);
+              }
             }
           }
           if (pair) mma_commit_pair(&empty[s]);
           else mma_commit(&empty[s]);
+          if (ts) mma_commit(&aempty[j]);
           if (++s == S) {
             s = 0;
             par ^= 1;
+          }
+          if (ts && ++j == TA) {
+            j = 0;
+            apar ^= 1;
           }
         }
         if (alive) {
@@ -665,6 +735,67 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&full[q % S]);
+      }
+    }
+  } else if (warp < 6 && ts) {
+    // ------------------------------------------------ fp32 A split into TMEM (A by TMA)
+    // Warp w owns TMEM lane quarter w & 3, i.e. rows 32 (w & 3) .. + 31 of the A tiles; for each k-block
+    // of the landed stage each thread reads its row (32 channels, eight 16-byte chunks of the 128-byte
+    // swizzle), splits it into tf32 hi / lo and stores both into its 64 columns of TMEM stage j (hi:
+    // columns 0-31, lo: 32-63; column = k).
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ta0;
+    int s = 0, j = 0;
+    uint32_t par = 0, apar = 0;
+    bool alive = true;
+    for (int u = cid; u < p.num_units && alive; u += ncl) {
+      const ConvPhase& ph = find_phase(p, u);
+      for (int g0 = 0; g0 < ph.num_kb; g0 += KPS) {  // one stage: k-blocks g0 .. g0 + nk - 1
+        const int nk = min(KPS, ph.num_kb - g0);
+        // the raw tiles have landed, and the MMAs that read TMEM stage j before have completed
+        const bool ok = wait(&full[s], par, p.err, kSiteFull) && wait(&aempty[j], apar ^ 1, p.err, kSiteEmpty);
+        if (!__all_sync(0xffffffffu, ok)) {  // warp-uniform
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int i = 0; i < kMaxKps; ++i) {
+          if (i >= nk) break;
+          const uint32_t src = sbase + s * stage_bytes + i * sub_bytes + r * 128;
+          const uint32_t dst = tq + static_cast<uint32_t>((j * KPS + i) * 64);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {  // channels 16h .. 16h + 15
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int cc = 4 * h + c;
+              uint32_t x0, x1, x2, x3;
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                           : "r"(src + ((cc ^ (r & 7)) << 4)));
+              split_tf32(__uint_as_float(x0), hi[4 * c], lo[4 * c]);
+              split_tf32(__uint_as_float(x1), hi[4 * c + 1], lo[4 * c + 1]);
+              split_tf32(__uint_as_float(x2), hi[4 * c + 2], lo[4 * c + 2]);
+              split_tf32(__uint_as_float(x3), hi[4 * c + 3], lo[4 * c + 3]);
+            }
+            tmem_st16(dst + 16 * h, hi);
+            tmem_st16(dst + 32 + 16 * h, lo);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[j]);
+        if (++s == S) {
+          s = 0;
+          par ^= 1;
+        }
+        if (++j == TA) {
+          j = 0;
+          apar ^= 1;
+        }
       }
     }
   } else if (warp < 6 && split_a) {
@@ -798,7 +929,9 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       float rmean = 0.f, rm2 = 0.f;
       const bool zero = ph.num_kb == 0;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * tcs;
-      if (DT == 0 && ph.num_kb > kpc)  // several accumulator chunks: summed into the first
+      if (ts && !zero)  // each chunk's two halves (hi x hi + lo x hi, then hi x lo), summed into the first
+        fold_chunks(taddr, BN, 2 * ((ph.num_kb + kpc - 1) / kpc), cb, ce);
+      else if (DT == 0 && ph.num_kb > kpc)  // several accumulator chunks: summed into the first
         fold_chunks(taddr, BN, (ph.num_kb + kpc - 1) / kpc, cb, ce);
       // columns are read from TMEM 64 at a time (two 32-column loads, one wait)
       auto fetch = [&](int c0, uint32_t (&ra)[32], uint32_t (&rb)[32]) {
@@ -945,7 +1078,9 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
   static_assert(!PAIR || DT == 1, "CTA pairs run bf16 only");
   const uint32_t a_bytes = kBM * 128, b_bytes = BN * 128;
   const uint32_t b_own = pair ? b_bytes / 2 : b_bytes;  // a pair member holds half of the oc columns
-  const uint32_t stage_bytes = D::NS * (a_bytes + b_own);
+  // fp32 with A in TMEM (WgradParams::ts): a stage holds the d_conv hi and lo rows only
+  const bool ts = DT == 0 && p.ts;
+  const uint32_t stage_bytes = ts ? 2 * b_bytes : D::NS * (a_bytes + b_own);
   const int S = p.stages;
   // fp32 with X by TMA: a ring of raw tiles (X chunks then d_conv chunks, 32 pixel rows x 128 B each)
   const bool raw_a = DT == 0 && p.a_tma;
@@ -962,7 +1097,11 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
   const uint32_t sbase = smem_u32(smem);
   const uint32_t rbase = smem_u32(rawp);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t tcols = tmem_cols_for(2 * BN);
+  // two accumulators (2 * BN columns each with A in TMEM), then one TMEM stage of A per stage (hi: 32
+  // columns, lo: 32)
+  const int acols = ts ? 2 * BN : BN;
+  const uint32_t tcols = tmem_cols_for(2 * acols + (ts ? S * 64 : 0));
+  const uint32_t ta0 = static_cast<uint32_t>(2 * acols);
   constexpr int KP = (DT == 1) ? 64 : 32;  // pixels per k-block
   const uint32_t rank = pair ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;
@@ -1148,6 +1287,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
     // ------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       const uint32_t idesc = idesc_f32acc(pair ? 2 * kBM : kBM, BN, D::FMT, DT == 1, DT == 1);
+      const uint32_t idesc2 = idesc_f32acc(kBM, 2 * BN, D::FMT, false, false);  // A_hi x [B_hi; B_lo]
       int s = 0;
       uint32_t par = 0;
       int tc = 0;
@@ -1158,7 +1298,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
         const int buf = tc & 1;
         if (!wait(&tempty[buf], ((tc >> 1) & 1) ^ 1, p.err, kSiteTEmpty)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + buf * BN;
+        const uint32_t d = tmem_base + buf * acols;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait(&full[s], par, p.err, kSiteFull)) {
             alive = false;
@@ -1166,11 +1306,16 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
           }
           tc_fence_after();
           const uint32_t a0 = sbase + s * stage_bytes;
-          const uint32_t b0 = a0 + D::NS * a_bytes;
+          const uint32_t b0 = ts ? a0 : a0 + D::NS * a_bytes;
+          const uint32_t ah = tmem_base + ta0 + static_cast<uint32_t>(s * 64);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t acc = (kb > kb0 || kk) ? 1u : 0u;
-            if (DT == 1) {
+            if (ts) {
+              const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);  // 2 BN rows: hi, then lo
+              mma_tf32_ta(d, ah + kk * 8, bd, idesc2, acc);
+              mma_tf32_ta(d, ah + 32 + kk * 8, bd, idesc, 1u);
+            } else if (DT == 1) {
               // MN-major: 16 pixel rows per MMA (2048 B), atoms of 64 k / 64 oc 8192 B apart
               const uint64_t ad = sdesc_sw128(a0 + kk * 2048, 8192, 1024);
               const uint64_t bd = sdesc_sw128(b0 + kk * 2048, 8192, 1024);
@@ -1279,11 +1424,14 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
       // K-major rows of 32 pixels per channel. A warp iteration takes half a chunk: lane (pq, cq) reads the
       // 4 x 4 block of pixels 4pq.. and channels 4cq.. (four 16-byte reads), splits it and writes four
       // channel rows of four pixels to the hi and lo tiles (both sides spread over all banks).
+      // With A in TMEM (ts) warp w instead moves X chunk w & 3 (its TMEM lane quarter): lane ch reads
+      // channel ch of the chunk's 32 pixels, splits them and stores hi / lo into columns 0-31 / 32-63 of
+      // the stage's TMEM rows (column = pixel = k); the half-chunk transposes cover the d_conv chunks only.
       const int wi = warp - 2;
       const int pq = lane & 7, cql = lane >> 3;
       int r = 0;
       uint32_t rpar = 0;
-      const int nchunk = 4 + BN / 32;
+      const int nchunk = ts ? BN / 32 : 4 + BN / 32;
       for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
         int m_tile, n_tile, kb0, kb1;
         decode(u, m_tile, n_tile, kb0, kb1);
@@ -1297,9 +1445,33 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
           }
           const uint32_t r0 = rbase + r * raw_bytes;
           const uint32_t a0 = sbase + s * stage_bytes;
-          const uint32_t b0 = a0 + 2 * a_bytes;
+          const uint32_t b0 = ts ? a0 : a0 + 2 * a_bytes;
+          if (ts) {
+            tc_fence_after();  // the MMAs that read this TMEM stage have completed (empty[s])
+            const int q = warp & 3;
+            if (q < nvalid) {  // rows past Mk keep stale values: their dW rows are discarded
+              const uint32_t src = r0 + q * 4096 + (lane & 3) * 4;
+              const uint32_t dst = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ta0 + s * 64;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                  const int px = 16 * h + e;
+                  uint32_t x;
+                  asm volatile("ld.shared.b32 %0, [%1];"
+                               : "=r"(x)
+                               : "r"(src + px * 128 + ((((lane >> 2) ^ (px & 7))) << 4)));
+                  split_tf32(__uint_as_float(x), hi[e], lo[e]);
+                }
+                tmem_st16(dst + 16 * h, hi);
+                tmem_st16(dst + 32 + 16 * h, lo);
+              }
+              tmem_st_wait();
+            }
+          }
           for (int it = wi; it < 2 * nchunk; it += 4) {
-            const int c = it >> 1;
+            const int c = ts ? 4 + (it >> 1) : it >> 1;
             if (c < 4 && c >= nvalid) continue;  // uniform across the warp
             const int cq = cql + 4 * (it & 1);
             const bool isa = c < 4;
@@ -1330,6 +1502,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
               st_shared_v4(addr + lo_off, l[0], l[1], l[2], l[3]);
             }
           }
+          if (ts) tc_fence_before();
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -1476,7 +1649,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
       tc_fence_after();
       const int m = m_tile * kBM + row;
       const bool zero = kb1 <= kb0;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * acols;
       auto put = [&](int cc, const uint32_t (&r)[32]) {
         if (m >= p.Mk) return;
         float* dst = p.partial + (static_cast<size_t>(split) * p.N + n_tile * BN + cc) * p.Mk + m;
@@ -1484,14 +1657,26 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
         for (int e = 0; e < 32; ++e)
           if (n_tile * BN + cc + e < p.N) dst[static_cast<size_t>(e) * p.Mk] = zero ? 0.f : __uint_as_float(r[e]);
       };
-      for (int c0 = 0; c0 < BN; c0 += 64) {
-        uint32_t ra[32], rb[32];
-        const int c1 = c0 + 32 < BN ? c0 + 32 : c0;
-        tmem_ld32(taddr + c0, ra);
-        tmem_ld32(taddr + c1, rb);
-        tmem_ld_wait2(ra, rb);
-        put(c0, ra);
-        if (c0 + 32 < BN) put(c0 + 32, rb);
+      if (ts) {  // column c holds hi x hi + lo x hi, column BN + c hi x lo
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t ra[32], rb[32];
+          tmem_ld32(taddr + c0, ra);
+          tmem_ld32(taddr + BN + c0, rb);
+          tmem_ld_wait2(ra, rb);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ra[e] = __float_as_uint(__uint_as_float(ra[e]) + __uint_as_float(rb[e]));
+          put(c0, ra);
+        }
+      } else {
+        for (int c0 = 0; c0 < BN; c0 += 64) {
+          uint32_t ra[32], rb[32];
+          const int c1 = c0 + 32 < BN ? c0 + 32 : c0;
+          tmem_ld32(taddr + c0, ra);
+          tmem_ld32(taddr + c1, rb);
+          tmem_ld_wait2(ra, rb);
+          put(c0, ra);
+          if (c0 + 32 < BN) put(c0 + 32, rb);
+        }
       }
       tc_fence_before();
       __syncwarp();

@@ -36,6 +36,12 @@
  *     pages' `zero_gradient` does); dx is OVERWRITTEN.
  *   - The library is stateless apart from per-device constant data; it is
  *     safe to call from several host threads.
+ *   - Per-device data is looked up once, on the first call made on a device,
+ *     and cached for the life of the process: the SM count, the device
+ *     address of the library's error word and of the static scratch array of
+ *     conv2d_fwd_train_noalloc. cudaDeviceReset() on a device invalidates
+ *     those addresses, so resetting a device while this library is loaded in
+ *     the process is not supported.
  */
 #ifndef CONV2D_GB300_H
 #define CONV2D_GB300_H

@@ -87,6 +87,15 @@ EDGE_CASES = {
                                        norm=NORM_BATCH, act=ACT_IDENTITY, dtype=FP32),
     "fp32_deep_fprop_ic256": LayerSpec(N=2, H=9, W=9, IC=256, OC=40, KH=3, KW=3, stride=1, pad=1,
                                        norm=NORM_NONE, act=ACT_RELU, dtype=FP32),
+    # fp32 with A in tensor memory: three 64-column tiles of the fprop and of the weight gradient with
+    # batch statistics per row tile; a stride-2 dgrad with four stride phases; a K loop of 1152 over two
+    # accumulator chunks (32-column tiles)
+    "fp32_ts_ic32_oc160_bn": LayerSpec(N=2, H=12, W=10, IC=32, OC=160, KH=3, KW=3, stride=1, pad=1,
+                                       norm=NORM_BATCH, act=ACT_SIGMOID, dtype=FP32),
+    "fp32_ts_s2_phases": LayerSpec(N=2, H=13, W=11, IC=32, OC=64, KH=3, KW=3, stride=2, pad=1, norm=NORM_BATCH,
+                                   act=ACT_RELU, dtype=FP32),
+    "fp32_ts_two_chunks": LayerSpec(N=2, H=9, W=9, IC=128, OC=40, KH=3, KW=3, stride=1, pad=1, norm=NORM_NONE,
+                                    act=ACT_RELU, dtype=FP32),
     # 48 weight-gradient splits (fp32 caps a split at 32 k-blocks; 49152 pixels) with a channel count off
     # the vector width: the split-group reduce with one channel per thread
     "fp32_ic3_many_wgrad_splits": LayerSpec(N=12, H=64, W=64, IC=3, OC=8, KH=3, KW=3, stride=1, pad=1,
