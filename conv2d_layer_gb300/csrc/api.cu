@@ -856,11 +856,13 @@ int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dc
   if (bf && w.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
   int grid = std::min(p.num_units, dev->sms);
   size_t smem = w.smem;
-  // CTA pairs: two m-tiles per pair, each CTA with half of the d_conv columns
+  // CTA pairs: two m-tiles per pair, each CTA with half of the d_conv columns (one k-block per stage: two
+  // per stage, as in the fprop / dgrad kernel, measured slower here)
   if (kUsePair && bf && p.a_tma && (w.m_tiles % 2) == 0 && w.BN % 128 == 0) {
-    const size_t stage = kBM * 128 + static_cast<size_t>(w.BN / 2) * 128;
-    const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - 2048) / stage));
-    const size_t psmem = stages * stage + 1024 + 512;
+    Tile pt;
+    fit_stages(pt, kBM * 128 + static_cast<size_t>(w.BN / 2) * 128, 0, false);
+    const int stages = pt.stages;
+    const size_t psmem = pt.smem;
     static std::mutex mu;
     static size_t cached_smem = 0;
     static int cached_clusters = 0;
