@@ -515,6 +515,18 @@ DgradPlan dgrad_plan(const Geo& g) {
   return d;
 }
 
+// dgrad with every stride phase among the columns (ConvGemmParams::seg): when KH and KW are multiples of
+// the stride and so is the padding, every phase of the input grid sees the same Th x Tw taps (Th = KH / S,
+// Tw = KW / S) of the same d_conv neighbourhood, so one GEMM over the coarse grid of ceil(H / S) x
+// ceil(W / S) rows per image, with the S * S * IC phase-and-channel values of each S x S block of dX as its
+// columns, writes dX in place: no column tile of IC columns per phase, no column buffer. Each run of
+// S * IC columns is contiguous in dX (IC needs no padding), and the runs must tile the epilogue's
+// 32-column chunks; d_conv comes by TMA.
+bool dgrad_merged(const Geo& g) {
+  if (g.S < 2 || g.KH % g.S != 0 || g.KW % g.S != 0 || g.P % g.S != 0 || g.ICp != g.IC) return false;
+  return 32 % (g.S * g.IC) == 0 && g.OCp % g.BKE == 0;
+}
+
 // dgrad in column form (a 1x1 GEMM d_conv x W^T into dcol[pix][(tap, icp)], then a per-element gather)
 // for strided layers with few input channels: there the stride-phase GEMMs have a column tile of IC
 // padded to 32 and only KH*KW/S^2 taps each, so most of their tensor-core and operand traffic is waste.
@@ -569,7 +581,7 @@ void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
     sz[R_WD] = static_cast<size_t>(g.ICp) * kd * es;
     if (g.dt == CONV2D_FP32) sz[R_WDLO] = static_cast<size_t>(g.ICp) * kd * 4;
     if (g.pack_x) sz[R_XP] = static_cast<size_t>(g.N) * g.H * g.W * g.ICp * es;
-    if (dgrad_col2im(g)) sz[R_COL] = static_cast<size_t>(g.n_pix) * g.taps * g.ICp * es;
+    if (dgrad_col2im(g) && !dgrad_merged(g)) sz[R_COL] = static_cast<size_t>(g.n_pix) * g.taps * g.ICp * es;
     pl->wg = wgrad_plan(g, sms);
     sz[R_WPART] = static_cast<size_t>(pl->wg.splits) * g.OC * pl->wg.Mk * 4;
   }
@@ -719,8 +731,90 @@ int run_dgrad_col2im(const Geo& g, const DevInfo* dev, const void* w, const void
   return CONV2D_OK;
 }
 
+// Phase-merged dgrad (see dgrad_merged): one GEMM over the coarse grid, d_conv by TMA im2col with the
+// Th x Tw window, B = the merged weights, the epilogue storing each row as S runs of S * IC values.
+int run_dgrad_merged(const Geo& g, const DevInfo* dev, const void* w, const void* dconv, void* dx, void* ws,
+                     const Plan& pl, cudaStream_t st) {
+  static ConvGemmParams p;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  const bool bf = g.dt == CONV2D_BF16;
+  const int S = g.S, Th = g.KH / S, Tw = g.KW / S, p0 = g.P / S;
+  const int ncols = S * S * g.ICp;
+  const int Kd = Th * Tw * g.OCp;
+  void* whi = region(ws, pl, R_WD);
+  float* wlo = reinterpret_cast<float*>(region(ws, pl, R_WDLO));
+  LAUNCH("dgrad_weights", st,
+         launch_prep_dgrad_merged_weights(g.dt, w, whi, bf ? nullptr : wlo, g.OC, g.KH, g.KW, g.IC, g.ICp, g.OCp,
+                                          S, st));
+  std::memset(&p, 0, sizeof(p));
+  Tile t;
+  p.ts = (!bf && ts_tile(g, ncols, Kd, &t)) ? 1 : 0;
+  if (!p.ts) {
+    t = conv_tile(g, ncols, Kd);
+    if (bf) fit_stages(t, conv_sub_bytes(g, t.BN, false, false), 12 * static_cast<size_t>(t.BN) * 4, true);
+  }
+  if (!encode_2d(&p.tmap_b, whi, bf, Kd, ncols, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
+  if (!bf && !encode_2d(&p.tmap_b_lo, wlo, false, Kd, ncols, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
+  const int Ha = static_cast<int>(ceil_div(g.H, S)), Wa = static_cast<int>(ceil_div(g.W, S));
+  p.src = dconv;
+  p.Hs = g.OH;
+  p.Ws = g.OW;
+  p.Cs = g.OCp;
+  p.rs = 1;
+  p.tap_sign = -1;
+  p.div_Cs = make_fastdiv(g.OCp);
+  p.num_phases = 1;
+  ConvPhase& ph = p.ph[0];
+  ph.rows = g.N * Ha * Wa;
+  ph.Ha = Ha;
+  ph.Wa = Wa;
+  ph.qh = p0;
+  ph.qw = p0;
+  ph.Tw = Tw;
+  ph.K = Kd;
+  ph.num_kb = static_cast<int>(ceil_div(Kd, g.BKE));
+  ph.div_Wa = make_fastdiv(Wa);
+  ph.div_HaWa = make_fastdiv(Ha * Wa);
+  ph.div_Tw = make_fastdiv(Tw);
+  // row (a, b) reads d_conv at (a + p0 - t', b + p0 - u') for the kernel taps (ph + S t', ph + S u'): with
+  // the window corner (a + p0 - (Th - 1), b + p0 - (Tw - 1)) the im2col offsets are the reversed taps
+  ph.a_lo_h = p0 - (Th - 1);
+  ph.a_lo_w = p0 - (Tw - 1);
+  if (!encode_im2col(&p.tmap_a[0], dconv, g.N, g.OH, g.OW, g.OCp, ph.a_lo_h, ph.a_lo_w,
+                     (Ha - 1) + ph.a_lo_h - (g.OH - 1), (Wa - 1) + ph.a_lo_w - (g.OW - 1), 1, kBM, g.dt))
+    return CONV2D_ERR_CUDA;
+  p.a_tma = 1;
+  p.a_chunks = g.OCp / g.BKE;
+  p.n_tiles = t.n_tiles;
+  p.BN = t.BN;
+  p.N = ncols;
+  p.num_units = static_cast<int>(ceil_div(ph.rows, kBM)) * t.n_tiles;
+  p.out = dx;
+  p.out_ld = g.IC;
+  p.Ho = g.H;
+  p.Wo = g.W;
+  p.os = S;
+  p.seg = S * g.IC;
+  p.seg_ld = g.W * g.IC;
+  while ((1 << p.seg_sh) < p.seg) ++p.seg_sh;  // powers of two (dgrad_merged)
+  while ((1 << p.ic_sh) < g.IC) ++p.ic_sh;
+  p.out_h = g.H;
+  p.out_w = g.W;
+  p.stages = t.stages;
+  p.kps = t.kps;
+  p.err = dev->err;
+  set_chunks(p, g, t.BN, ph.num_kb);
+  int grid = std::min(p.num_units, dev->sms);
+  if (bf) try_pair(p, t, g, dev, ceil_div(ph.rows, kBM), whi, Kd, ncols, &grid);
+  LAUNCH("dgrad_gemm", st,
+         bf ? launch_conv_gemm_bf16(p, grid, t.smem, st) : launch_conv_gemm_tf32(p, grid, t.smem, st));
+  return CONV2D_OK;
+}
+
 int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv, void* dx, void* ws,
               const Plan& pl, cudaStream_t st) {
+  if (dgrad_merged(g)) return run_dgrad_merged(g, dev, w, dconv, dx, ws, pl, st);
   if (dgrad_col2im(g)) return run_dgrad_col2im(g, dev, w, dconv, dx, ws, pl, st);
   static ConvGemmParams p;
   static DgradPlan d;

@@ -622,6 +622,39 @@ __global__ void prep_dgrad_weights_kernel(const T* __restrict__ w, T* __restrict
   }
 }
 
+// Phase-merged dgrad weights (every stride phase has Th x Tw taps, KH = S Th, KW = S Tw, pad a multiple of
+// S): row (ph_h * S + ph_w) * ICp + ic, column (t * Tw + u) * OCp + oc holds W[oc][ph_h + S (Th-1-t)]
+// [ph_w + S (Tw-1-u)][ic] (taps reversed: the im2col window of d_conv starts Th-1, Tw-1 pixels up-left).
+template <typename T>
+__global__ void prep_dgrad_merged_weights_kernel(const T* __restrict__ w, T* __restrict__ bhi,
+                                                 float* __restrict__ blo, int OC, int KH, int KW, int IC, int ICp,
+                                                 int OCp, int S) {
+  pdl_entry();
+  const int Th = KH / S, Tw = KW / S;
+  const long Kd = static_cast<long>(Th) * Tw * OCp;
+  const long total = static_cast<long>(S) * S * ICp * Kd;
+  for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const long row = i / Kd;
+    const int col = static_cast<int>(i - row * Kd);
+    const int ic = static_cast<int>(row % ICp);
+    const int ph = static_cast<int>(row / ICp);
+    const int ph_h = ph / S, ph_w = ph % S;
+    const int oc = col % OCp, tap = col / OCp;
+    const int kh = ph_h + S * (Th - 1 - tap / Tw), kw = ph_w + S * (Tw - 1 - tap % Tw);
+    T v = T(0.f);
+    if (ic < IC && oc < OC) v = w[((static_cast<long>(oc) * KH + kh) * KW + kw) * IC + ic];
+    if constexpr (sizeof(T) == 4) {
+      uint32_t hi, lo;
+      split_tf32(static_cast<float>(v), hi, lo);
+      reinterpret_cast<uint32_t*>(bhi)[i] = hi;
+      reinterpret_cast<uint32_t*>(blo)[i] = lo;
+    } else {
+      bhi[i] = v;
+    }
+  }
+}
+
 // dW[oc][tap][ic] += sum over splits of partial[s][oc][tap*ICp + ic] (fixed order: deterministic), one
 // thread per item over all splits: the form for a few splits (see launch_wgrad_reduce).
 __global__ void wgrad_reduce_serial_kernel(const float* __restrict__ partial, int splits, int OC, int taps, int ICp,
@@ -1601,6 +1634,18 @@ cudaError_t launch_prep_dgrad_weights(int dtype, const void* w, void* bhi, float
   else
     launch_k(prep_dgrad_weights_kernel<float>, g, 256, 0, st, 1, static_cast<const float*>(w), static_cast<float*>(bhi), blo,
                                                         OC, KH, KW, IC, ICp, OCp, S, Kd, t);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep_dgrad_merged_weights(int dtype, const void* w, void* bhi, float* blo, int OC, int KH, int KW,
+                                             int IC, int ICp, int OCp, int S, cudaStream_t st) {
+  const int g = grid_for(static_cast<long>(ICp) * KH * KW * OCp, 256);
+  if (dtype == 1)
+    launch_k(prep_dgrad_merged_weights_kernel<__nv_bfloat16>, g, 256, 0, st, 1, static_cast<const __nv_bfloat16*>(w),
+             static_cast<__nv_bfloat16*>(bhi), nullptr, OC, KH, KW, IC, ICp, OCp, S);
+  else
+    launch_k(prep_dgrad_merged_weights_kernel<float>, g, 256, 0, st, 1, static_cast<const float*>(w),
+             static_cast<float*>(bhi), blo, OC, KH, KW, IC, ICp, OCp, S);
   return cudaGetLastError();
 }
 

@@ -121,6 +121,13 @@ struct ConvGemmParams {
   // right after its hi rows), and the epilogue adds columns BN .. 2BN - 1 into 0 .. BN - 1. A shared-memory
   // stage then holds the raw A tile and B only, and the tensor core reads no A operand from shared memory
   int ts;
+  // dgrad with every stride phase among the columns (phase-merged: the layer's phases all see the same
+  // taps of the same d_conv neighbourhood): column c of row (n, a, b) is dX element (ph_h, r) =
+  // (c / seg, c % seg) of the seg = S * IC contiguous values that start at pixel (S a + ph_h, S b), i.e.
+  // phase column ph_w = r / IC, channel r % IC; seg_ld elements from one such run to the next row's; seg
+  // and IC are powers of two, seg_sh and ic_sh their logarithms.
+  // Runs of rows at or past out_h, and values of columns at or past out_w, are not written. 0: off.
+  int seg, seg_sh, ic_sh, seg_ld, out_h, out_w;
   int* err;
   ConvPhase ph[kMaxPhases];
 };
@@ -351,6 +358,44 @@ __device__ __forceinline__ void store_row16<float>(float* dst, const float* v, i
 #pragma unroll
     for (int e = 0; e < 16; ++e)
       if (e < ncols) dst[e] = v[e];
+  }
+}
+
+// 32 columns col0 .. col0 + 31 of a phase-merged dgrad row (ConvGemmParams::seg) whose first output pixel
+// (h0, w0) = (S a, S b) is at out + obase. seg = S * IC divides 32, so it and IC are powers of two (seg_sh,
+// ic_sh their logarithms) and every 16-byte group of columns lies inside one run of seg contiguous dX
+// values; the groups are unrolled so that v stays in registers.
+template <typename T>
+__device__ __forceinline__ void store_phase_runs(T* out, size_t obase, int h0, int w0, int col0, const float (&v)[32],
+                                                 int ncols, const ConvGemmParams& p) {
+  constexpr int EC = 16 / sizeof(T);
+  const bool whole = w0 + (p.seg >> p.ic_sh) <= p.out_w;  // every phase column of a run inside the image
+#pragma unroll
+  for (int e = 0; e < 32; e += EC) {
+    if (e < ncols) {
+      const int c = col0 + e;
+      const int ph_h = c >> p.seg_sh, r = c - (ph_h << p.seg_sh);
+      if (h0 + ph_h < p.out_h) {
+        T* dst = out + obase + static_cast<size_t>(ph_h) * p.seg_ld + r;
+        if (whole) {
+          if constexpr (sizeof(T) == 4) {
+            *reinterpret_cast<float4*>(dst) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+          } else {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              __nv_bfloat162 h = __floats2bfloat162_rn(v[e + 2 * q], v[e + 2 * q + 1]);
+              w[q] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < EC; ++q)
+            if (w0 + ((r + q) >> p.ic_sh) < p.out_w) dst[q] = static_cast<T>(v[e + q]);
+        }
+      }
+    }
   }
 }
 
@@ -916,13 +961,15 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       const int m = m_tile * kBM + row;
       const bool valid = m < ph.rows;
       size_t obase = 0;
+      int oh_px = 0, ow_px = 0;  // output pixel of the row
       if (valid) {
         const int n = static_cast<int>(fdiv(static_cast<uint32_t>(m), ph.div_HaWa));
         const int rem = m - n * ph.Ha * ph.Wa;
         const int a = static_cast<int>(fdiv(static_cast<uint32_t>(rem), ph.div_Wa));
         const int b = rem - a * ph.Wa;
-        const int oh = ph.oh0 + a * p.os, ow = ph.ow0 + b * p.os;
-        obase = (static_cast<size_t>(n * p.Ho + oh) * p.Wo + ow) * p.out_ld;
+        oh_px = ph.oh0 + a * p.os;
+        ow_px = ph.ow0 + b * p.os;
+        obase = (static_cast<size_t>(n * p.Ho + oh_px) * p.Wo + ow_px) * p.out_ld;
       }
       // layer-norm partials of this row over the half's columns: exact two-pass per 32 columns, merged
       // across the chunks with Chan's formula (the chunks before column cc hold cc - cb values)
@@ -948,7 +995,9 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         // already use most of the shared-memory bandwidth)
         float v[32];
         ep_columns(r, zero, p.ep_scale != nullptr, sc_s + cc, sh_s + cc, v);
-        if (valid && !p.out_act && !p.rstats && !out2) {
+        if (valid && p.seg) {
+          store_phase_runs<T>(out, obase, oh_px, ow_px, col0, v, ncols, p);
+        } else if (valid && !p.out_act && !p.rstats && !out2) {
           store_row32<T>(out + obase + col0, v, ncols, vec);  // one rounding to T
         } else if (valid) {
           float o[32];

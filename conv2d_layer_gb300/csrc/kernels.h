@@ -76,6 +76,9 @@ cudaError_t launch_prep_fprop_weights(int dtype, const void* w, void* bhi, float
 cudaError_t launch_prep_dgrad_weights(int dtype, const void* w, void* bhi, float* blo, int OC, int KH, int KW,
                                       int IC, int ICp, int OCp, int S, int Kd, const DgradWeightTable& t,
                                       cudaStream_t st);
+// Phase-merged dgrad weights B[(ph_h, ph_w, icp)][(tap, oc)] (see prep_dgrad_merged_weights_kernel).
+cudaError_t launch_prep_dgrad_merged_weights(int dtype, const void* w, void* bhi, float* blo, int OC, int KH, int KW,
+                                             int IC, int ICp, int OCp, int S, cudaStream_t st);
 cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float eps, float momentum, float* mean,
                                      float* inv_std, float* rm, float* rv, cudaStream_t st);
 // rev != 0 walks the rows last to first (streamed path): the kernel starts on the rows the previous

@@ -96,6 +96,13 @@ EDGE_CASES = {
                                    act=ACT_RELU, dtype=FP32),
     "fp32_ts_two_chunks": LayerSpec(N=2, H=9, W=9, IC=128, OC=40, KH=3, KW=3, stride=1, pad=1, norm=NORM_NONE,
                                     act=ACT_RELU, dtype=FP32),
+    # phase-merged dgrad (kernel and padding multiples of the stride: every stride phase in the columns of
+    # one GEMM over the coarse grid, stored as runs of S * IC values): bf16 with padding 2 at stride 2, and
+    # fp32 at stride 4 with padding 4 and an input whose last coarse row and column are partly outside
+    "bf16_merged_k4s2p2": LayerSpec(N=2, H=11, W=13, IC=8, OC=64, KH=4, KW=4, stride=2, pad=2, norm=NORM_BATCH,
+                                    act=ACT_TANH, dtype=BF16),
+    "fp32_merged_k8s4p4_ragged": LayerSpec(N=2, H=18, W=17, IC=4, OC=32, KH=8, KW=8, stride=4, pad=4,
+                                           norm=NORM_NONE, act=ACT_RELU, dtype=FP32),
     # 48 weight-gradient splits (fp32 caps a split at 32 k-blocks; 49152 pixels) with a channel count off
     # the vector width: the split-group reduce with one channel per thread
     "fp32_ic3_many_wgrad_splits": LayerSpec(N=12, H=64, W=64, IC=3, OC=8, KH=3, KW=3, stride=1, pad=1,
