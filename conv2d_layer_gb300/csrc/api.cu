@@ -146,6 +146,30 @@ bool encode_2d(CUtensorMap* m, const void* base, bool bf16, uint64_t cols, uint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 GEMM B operand: the tf32 hi and lo matrices [rows][cols] (hi at `hi`, lo `lo`, 16-byte aligned,
+// lo after hi) seen as a 3-D tensor {cols, rows, 2 planes} whose plane stride is their distance, with
+// 128-byte swizzled boxes of 32 x box_rows x 2: one copy brings a k-block's hi rows and then its lo rows.
+bool encode_b_fp32(CUtensorMap* m, const void* hi, const void* lo, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const auto d = reinterpret_cast<uintptr_t>(lo) - reinterpret_cast<uintptr_t>(hi);
+  if (reinterpret_cast<uintptr_t>(lo) <= reinterpret_cast<uintptr_t>(hi) || d % 16 != 0 || d < rows * cols * 4)
+    return false;
+  cuuint64_t dims[3] = {cols, rows, 2};
+  cuuint64_t strides[2] = {cols * 4, static_cast<cuuint64_t>(d)};
+  cuuint32_t box[3] = {32, box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(hi), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// B operand of the fprop / dgrad GEMM (see ConvGemmParams::tmap_b).
+bool encode_b(CUtensorMap* m, bool bf, const void* hi, const void* lo, uint64_t cols, uint64_t rows,
+              uint32_t box_rows) {
+  return bf ? encode_2d(m, hi, true, cols, rows, 64, box_rows) : encode_b_fp32(m, hi, lo, cols, rows, box_rows);
+}
+
 typedef CUresult (*EncodeIm2colFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const int*, const int*, cuuint32_t, cuuint32_t,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -680,8 +704,7 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
   // grouped per stage
   if (!bf && p.a_tma && ts_tile(g, g.OC, g.Kf, &t)) p.ts = 1;
   if (bf && p.a_tma) fit_stages(t, conv_sub_bytes(g, t.BN, false, false), 12 * static_cast<size_t>(t.BN) * 4, true);
-  if (!encode_2d(&p.tmap_b, bhi, bf, g.Kf, g.OC, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
-  if (!bf && !encode_2d(&p.tmap_b_lo, blo, false, g.Kf, g.OC, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
+  if (!encode_b(&p.tmap_b, bf, bhi, blo, g.Kf, g.OC, t.BN)) return CONV2D_ERR_CUDA;
   p.n_tiles = t.n_tiles;
   p.BN = t.BN;
   p.num_units = static_cast<int>(ceil_div(g.n_pix, kBM)) * t.n_tiles;
@@ -754,8 +777,7 @@ int run_dgrad_merged(const Geo& g, const DevInfo* dev, const void* w, const void
     t = conv_tile(g, ncols, Kd);
     if (bf) fit_stages(t, conv_sub_bytes(g, t.BN, false, false), 12 * static_cast<size_t>(t.BN) * 4, true);
   }
-  if (!encode_2d(&p.tmap_b, whi, bf, Kd, ncols, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
-  if (!bf && !encode_2d(&p.tmap_b_lo, wlo, false, Kd, ncols, g.BKE, t.BN)) return CONV2D_ERR_CUDA;
+  if (!encode_b(&p.tmap_b, bf, whi, wlo, Kd, ncols, t.BN)) return CONV2D_ERR_CUDA;
   const int Ha = static_cast<int>(ceil_div(g.H, S)), Wa = static_cast<int>(ceil_div(g.W, S));
   p.src = dconv;
   p.Hs = g.OH;
@@ -828,8 +850,7 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
          launch_prep_dgrad_weights(g.dt, w, whi, bf ? nullptr : wlo, g.OC, g.KH, g.KW, g.IC, g.ICp, g.OCp, g.S, d.Kd,
                                    d.table, st));
   std::memset(&p, 0, sizeof(p));
-  if (!encode_2d(&p.tmap_b, whi, bf, d.Kd, g.ICp, g.BKE, d.tile.BN)) return CONV2D_ERR_CUDA;
-  if (!bf && !encode_2d(&p.tmap_b_lo, wlo, false, d.Kd, g.ICp, g.BKE, d.tile.BN)) return CONV2D_ERR_CUDA;
+  if (!encode_b(&p.tmap_b, bf, whi, wlo, d.Kd, g.ICp, d.tile.BN)) return CONV2D_ERR_CUDA;
   p.src = dconv;
   p.Hs = g.OH;
   p.Ws = g.OW;

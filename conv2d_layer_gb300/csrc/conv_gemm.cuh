@@ -77,8 +77,9 @@ struct ConvPhase {
 };
 
 struct ConvGemmParams {
-  CUtensorMap tmap_b;     // B [Nrows][Kcols] K-major (bf16, or tf32 hi)
-  CUtensorMap tmap_b_lo;  // tf32 lo (fp32 mode only)
+  // B [Nrows][Kcols] K-major: bf16, 2-D boxes of BN rows x 64; fp32 (3xTF32), a 3-D view of the tf32 hi and
+  // lo matrices as two planes, boxes of BN rows x 32 x both planes (hi rows then lo rows: one copy per k-block)
+  CUtensorMap tmap_b;
   const void* src;        // A source, NHWC [Nimg][Hs][Ws][Cs]
   int Hs, Ws, Cs;
   int rs, tap_sign;       // fprop: rs = stride, taps add; dgrad: rs = 1, taps subtract
@@ -498,7 +499,6 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       for (int j = 0; j < TA; ++j) mbar_init(&aempty[j], 1);  // the MMA warp's commit
     fence_mbar_init();
     tma_prefetch_desc(&p.tmap_b);
-    if (D::NS == 2) tma_prefetch_desc(&p.tmap_b_lo);
     if (p.a_tma)
       for (int i = 0; i < p.num_phases && i < kMaxTmaPhases; ++i) tma_prefetch_desc(&p.tmap_a[i]);
   }
@@ -567,8 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
               if (p.a_tma)
                 tma_load_im2col_4d(a0, &p.tmap_a[ph.a_map], &full[s], ck * D::BKE, aw, ah, an,
                                    static_cast<uint16_t>(tw), static_cast<uint16_t>(tt));
-              tma_load_2d(b0, &p.tmap_b, &full[s], kcol, n_tile * BN);
-              if (D::NS == 2) tma_load_2d(b0 + b_bytes, &p.tmap_b_lo, &full[s], kcol, n_tile * BN);
+              if (D::NS == 2) tma_load_3d(b0, &p.tmap_b, &full[s], kcol, n_tile * BN, 0);  // hi and lo rows
+              else tma_load_2d(b0, &p.tmap_b, &full[s], kcol, n_tile * BN);
             }
             if (++ck == p.a_chunks) {  // (without A by TMA a_chunks is 0 and the counters are unused)
               ck = 0;
