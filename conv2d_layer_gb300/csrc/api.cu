@@ -464,6 +464,7 @@ WgradPlan wgrad_plan(const Geo& g, int sms) {
     // A (X) in TMEM: a stage holds the d_conv hi and lo rows, and each stage has a TMEM stage of A
     // (64 columns) beside the two accumulators of 2 * BN columns; the rest of shared memory holds raw
     // tiles in flight
+    // (raw stages of two k-blocks, whose copies are twice as tall, measured slower: fewer stages in flight)
     const size_t tstage = 2 * static_cast<size_t>(w.BN) * 128;
     const size_t raw = kBM * 128 + static_cast<size_t>(w.BN) * 128;
     w.stages = std::min(kMaxStages, (512 - 4 * w.BN) / 64);
@@ -967,15 +968,22 @@ int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dc
     }
   }
   p.stages = w.stages;
+  p.kps = 1;
   p.err = dev->err;
-  if (bf && w.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;
+  if (bf && !p.a_tma && w.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;  // the gather's copies in flight
   int grid = std::min(p.num_units, dev->sms);
   size_t smem = w.smem;
-  // CTA pairs: two m-tiles per pair, each CTA with half of the d_conv columns (one k-block per stage: two
-  // per stage, as in the fprop / dgrad kernel, measured slower here)
+  if (bf && p.a_tma) {  // k-blocks grouped per stage, each copy covering them all (WgradParams::kps)
+    Tile t;
+    fit_stages(t, kBM * 128 + static_cast<size_t>(w.BN) * 128, 0, true);
+    p.stages = t.stages;
+    p.kps = t.kps;
+    smem = t.smem;
+  }
+  // CTA pairs: two m-tiles per pair, each CTA with half of the d_conv columns
   if (kUsePair && bf && p.a_tma && (w.m_tiles % 2) == 0 && w.BN % 128 == 0) {
     Tile pt;
-    fit_stages(pt, kBM * 128 + static_cast<size_t>(w.BN / 2) * 128, 0, false);
+    fit_stages(pt, kBM * 128 + static_cast<size_t>(w.BN / 2) * 128, 0, true);
     const int stages = pt.stages;
     const size_t psmem = pt.smem;
     static std::mutex mu;
@@ -995,9 +1003,16 @@ int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dc
       p.m_tiles = w.m_tiles / 2;
       p.num_units = w.units / 2;
       p.stages = stages;
+      p.kps = pt.kps;
       smem = psmem;
       grid = 2 * std::min(p.num_units, std::min(clusters, dev->sms / 2));
     }
+  }
+  if (bf && p.kps > 1) {  // copies of kps k-blocks: X panels and d_conv boxes kps * 64 pixels tall
+    if (!encode_im2col(&p.tmap_x, xsrc, g.N, g.H, g.W, g.ICp, -g.P, -g.P, (g.OH - 1) * g.S - g.P - (g.H - 1),
+                       (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, w.KP * p.kps) ||
+        !encode_2d(&p.tmap_dc, dconv, true, g.OCp, g.n_pix, 64, 64 * p.kps))
+      return CONV2D_ERR_CUDA;
   }
   LAUNCH("wgrad_gemm", st,
          bf ? launch_wgrad_gemm_bf16(p, grid, smem, st) : launch_wgrad_gemm_tf32(p, grid, smem, st));

@@ -151,6 +151,10 @@ struct WgradParams {
   float* partial;         // [splits][N][Mk]
   int stages;
   int pair;               // CTA pairs (cta_group::2, bf16 with A by TMA): m_tiles counts pairs of m-tiles
+  // bf16 with A by TMA: k-blocks per stage (1 or 2). With two, each copy covers both: the im2col panels and
+  // the d_conv boxes are 64 * kps pixels tall, so a panel holds k-block i at 8 KB * i and the panels (and
+  // the d_conv boxes) are kps * 8 KB apart; the barriers are passed once per two k-blocks
+  int kps;
   // fp32 with raw TMA tiles: A (X, k rows x 32 pixels) in tensor memory, one TMEM stage per shared-memory
   // stage, which then holds the d_conv hi and lo rows only; the MMAs as in ConvGemmParams::ts
   int ts;
@@ -1129,8 +1133,10 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
   const uint32_t b_own = pair ? b_bytes / 2 : b_bytes;  // a pair member holds half of the oc columns
   // fp32 with A in TMEM (WgradParams::ts): a stage holds the d_conv hi and lo rows only
   const bool ts = DT == 0 && p.ts;
-  const uint32_t stage_bytes = ts ? 2 * b_bytes : D::NS * (a_bytes + b_own);
+  const uint32_t stage_bytes = ts ? 2 * b_bytes : D::NS * (a_bytes + b_own) * (DT == 1 && p.kps > 1 ? p.kps : 1);
   const int S = p.stages;
+  const int KPS = DT == 1 && p.kps > 1 ? p.kps : 1;  // k-blocks per stage (bf16 with A by TMA)
+  const uint32_t panel = 8192u * KPS;                  // distance between MN-major panels / d_conv boxes
   // fp32 with X by TMA: a ring of raw tiles (X chunks then d_conv chunks, 32 pixel rows x 128 B each)
   const bool raw_a = DT == 0 && p.a_tma;
   const int NR = raw_a ? p.rstages : 0;
@@ -1228,17 +1234,17 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
           for (int j = 0; j < 2; ++j)
             if (peer * kBM + 64 * j < p.Mk) a_tx += 8192;
         }
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int g0 = kb0; g0 < kb1; g0 += KPS) {  // one stage: k-blocks g0 .. g0 + KPS - 1 (copies cover all)
           if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
             alive = false;
             break;
           }
           const uint32_t a0 = sbase + s * stage_bytes;
-          const uint32_t b0 = a0 + a_bytes;
+          const uint32_t b0 = a0 + KPS * a_bytes;
+          const int pix = g0 * KP;  // first pixel of the stage; the maps walk the next KPS * KP
           if (pair) {
             const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
-            if (leader) mbar_arrive_expect_tx(&full[s], b_bytes + a_tx);
-            const int pix = kb * KP;
+            if (leader) mbar_arrive_expect_tx(&full[s], KPS * (b_bytes + a_tx));
             const int n = static_cast<int>(fdiv(static_cast<uint32_t>(pix), p.div_OHOW));
             const int rem = pix - n * p.OH * p.OW;
             const int oh = static_cast<int>(fdiv(static_cast<uint32_t>(rem), p.div_OW));
@@ -1246,16 +1252,15 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
 #pragma unroll
             for (int j = 0; j < 2; ++j)
               if (pc[j] >= 0)
-                tma_load_im2col_4d_pair(a0 + j * 8192, &p.tmap_x, bar, pc[j], ow * p.S - p.P, oh * p.S - p.P, n,
+                tma_load_im2col_4d_pair(a0 + j * panel, &p.tmap_x, bar, pc[j], ow * p.S - p.P, oh * p.S - p.P, n,
                                         static_cast<uint16_t>(pkw[j]), static_cast<uint16_t>(pkh[j]));
             const int nb = BN / 128;  // this member's 64-column boxes
             for (int jn = 0; jn < nb; ++jn)
-              tma_load_2d_pair(b0 + jn * 8192, &p.tmap_dc, bar,
-                               n_tile * BN + 64 * (static_cast<int>(rank) * nb + jn), kb * KP);
+              tma_load_2d_pair(b0 + jn * panel, &p.tmap_dc, bar,
+                               n_tile * BN + 64 * (static_cast<int>(rank) * nb + jn), pix);
           } else {
-            mbar_arrive_expect_tx(&full[s], b_bytes + a_tx);
+            mbar_arrive_expect_tx(&full[s], KPS * (b_bytes + a_tx));
             if (p.a_tma) {
-              const int pix = kb * KP;  // first pixel of the k-block; the map walks the next 64
               const int n = static_cast<int>(fdiv(static_cast<uint32_t>(pix), p.div_OHOW));
               const int rem = pix - n * p.OH * p.OW;
               const int oh = static_cast<int>(fdiv(static_cast<uint32_t>(rem), p.div_OW));
@@ -1263,11 +1268,11 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
 #pragma unroll
               for (int j = 0; j < 2; ++j)
                 if (pc[j] >= 0)
-                  tma_load_im2col_4d(a0 + j * 8192, &p.tmap_x, &full[s], pc[j], ow * p.S - p.P, oh * p.S - p.P, n,
+                  tma_load_im2col_4d(a0 + j * panel, &p.tmap_x, &full[s], pc[j], ow * p.S - p.P, oh * p.S - p.P, n,
                                      static_cast<uint16_t>(pkw[j]), static_cast<uint16_t>(pkh[j]));
             }
             for (int jn = 0; jn < BN / 64; ++jn)
-              tma_load_2d(b0 + jn * 8192, &p.tmap_dc, &full[s], n_tile * BN + 64 * jn, kb * KP);
+              tma_load_2d(b0 + jn * panel, &p.tmap_dc, &full[s], n_tile * BN + 64 * jn, pix);
           }
           if (++s == S) {
             s = 0;
@@ -1348,36 +1353,43 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
         if (!wait(&tempty[buf], ((tc >> 1) & 1) ^ 1, p.err, kSiteTEmpty)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + buf * acols;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int g0 = kb0; g0 < kb1; g0 += KPS) {  // one stage: k-blocks g0 .. g0 + nk - 1
+          const int nk = min(KPS, kb1 - g0);
           if (!wait(&full[s], par, p.err, kSiteFull)) {
             alive = false;
             break;
           }
           tc_fence_after();
           const uint32_t a0 = sbase + s * stage_bytes;
-          const uint32_t b0 = ts ? a0 : a0 + D::NS * a_bytes;
+          const uint32_t b0 = ts ? a0 : a0 + D::NS * a_bytes * KPS;
           const uint32_t ah = tmem_base + ta0 + static_cast<uint32_t>(s * 64);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acc = (kb > kb0 || kk) ? 1u : 0u;
-            if (ts) {
-              const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);  // 2 BN rows: hi, then lo
-              mma_tf32_ta(d, ah + kk * 8, bd, idesc2, acc);
-              mma_tf32_ta(d, ah + 32 + kk * 8, bd, idesc, 1u);
-            } else if (DT == 1) {
-              // MN-major: 16 pixel rows per MMA (2048 B), atoms of 64 k / 64 oc 8192 B apart
-              const uint64_t ad = sdesc_sw128(a0 + kk * 2048, 8192, 1024);
-              const uint64_t bd = sdesc_sw128(b0 + kk * 2048, 8192, 1024);
-              if (pair) mma_bf16_pair(d, ad, bd, idesc, acc);
-              else mma_bf16(d, ad, bd, idesc, acc);
-            } else {
-              const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
-              const uint64_t al = sdesc_sw128(a0 + a_bytes + kk * 32, 16, 1024);
-              const uint64_t bl = sdesc_sw128(b0 + b_bytes + kk * 32, 16, 1024);
-              mma_tf32(d, al, bd, idesc, acc);
-              mma_tf32(d, ad, bl, idesc, 1u);
-              mma_tf32(d, ad, bd, idesc, 1u);
+          for (int i = 0; i < kMaxKps; ++i) {
+            if (i >= nk) break;
+            const int kb = g0 + i;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t acc = (kb > kb0 || kk) ? 1u : 0u;
+              if (ts) {
+                const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);  // 2 BN rows: hi, then lo
+                mma_tf32_ta(d, ah + kk * 8, bd, idesc2, acc);
+                mma_tf32_ta(d, ah + 32 + kk * 8, bd, idesc, 1u);
+              } else if (DT == 1) {
+                // MN-major: 16 pixel rows per MMA (2048 B) of k-block i (8 KB * i into each panel), panels of
+                // 64 k / 64 oc `panel` bytes apart
+                const uint64_t ad = sdesc_sw128(a0 + i * 8192 + kk * 2048, panel, 1024);
+                const uint64_t bd = sdesc_sw128(b0 + i * 8192 + kk * 2048, panel, 1024);
+                if (pair) mma_bf16_pair(d, ad, bd, idesc, acc);
+                else mma_bf16(d, ad, bd, idesc, acc);
+              } else {
+                const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
+                const uint64_t al = sdesc_sw128(a0 + a_bytes + kk * 32, 16, 1024);
+                const uint64_t bl = sdesc_sw128(b0 + b_bytes + kk * 32, 16, 1024);
+                mma_tf32(d, al, bd, idesc, acc);
+                mma_tf32(d, ad, bl, idesc, 1u);
+                mma_tf32(d, ad, bd, idesc, 1u);
+              }
             }
           }
           if (pair) mma_commit_pair(&empty[s]);
@@ -1524,7 +1536,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
             if (c < 4 && c >= nvalid) continue;  // uniform across the warp
             const int cq = cql + 4 * (it & 1);
             const bool isa = c < 4;
-            const uint32_t src = isa ? r0 + c * 4096 : r0 + a_bytes + (c - 4) * 4096;
+            const uint32_t src = r0 + c * 4096;  // X chunks 0-3, then d_conv chunks
             const uint32_t hi = isa ? a0 + c * 4096 : b0 + (c - 4) * 4096;
             const uint32_t lo_off = isa ? a_bytes : b_bytes;
             float v[4][4];
