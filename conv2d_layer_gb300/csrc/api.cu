@@ -357,15 +357,18 @@ void set_chunks(ConvGemmParams& p, const Geo& g, int BN, int max_kb) {
 }
 
 // CTA pairs (cta_group::2, clusters of two) for the bf16 fprop / dgrad GEMMs whose A operand comes by
-// TMA in a single phase: each CTA holds half of B's columns, so a stage is smaller (more stages), and
-// the shared-memory and TMA traffic per tile drops by a third.
+// TMA: each CTA holds half of B's columns, so a stage is smaller (more stages), and the shared-memory and
+// TMA traffic per tile drops by a third. A pair's two m-tiles belong to one stride phase, so every phase
+// needs an even m-tile count (every tile of a pair then holds rows of the layer). Single-phase GEMMs
+// only: on the stride-2 dgrad of a 256-channel 3 x 3 layer (four phases of 4, 2, 2 and 1 taps) pairs
+// measured slower (0.078 -> 0.082 ms).
 constexpr bool kUsePair = true;
 
-bool try_pair(ConvGemmParams& p, Tile& t, const Geo& g, const DevInfo* dev, long m_tiles, const void* bmat,
-              uint64_t bcols, uint64_t brows, int* grid) {
-  // an even tile count: every tile of a pair holds rows of the layer
-  if (!kUsePair || g.dt != CONV2D_BF16 || !p.a_tma || p.num_phases != 1 || t.BN % 32 != 0 || (m_tiles & 1))
-    return false;
+bool try_pair(ConvGemmParams& p, Tile& t, const Geo& g, const DevInfo* dev, const void* bmat, uint64_t bcols,
+              uint64_t brows, int* grid) {
+  if (!kUsePair || g.dt != CONV2D_BF16 || !p.a_tma || t.BN % 32 != 0 || p.num_phases != 1) return false;
+  for (int i = 0; i < p.num_phases; ++i)
+    if (ceil_div(p.ph[i].rows, kBM) & 1) return false;
   Tile pt = t;
   fit_stages(pt, conv_sub_bytes(g, t.BN, false, true), 12 * static_cast<size_t>(t.BN) * 4, true);
   const size_t smem = pt.smem;
@@ -386,7 +389,12 @@ bool try_pair(ConvGemmParams& p, Tile& t, const Geo& g, const DevInfo* dev, long
   if (!encode_2d(&half, bmat, true, bcols, brows, g.BKE, t.BN / 2)) return false;
   p.tmap_b = half;
   p.pair = 1;
-  p.num_units = static_cast<int>(m_tiles / 2) * t.n_tiles;
+  int unit = 0;  // units: pairs of m-tiles, phase by phase
+  for (int i = 0; i < p.num_phases; ++i) {
+    p.ph[i].unit_begin = unit;
+    unit += static_cast<int>(ceil_div(p.ph[i].rows, kBM) / 2) * t.n_tiles;
+  }
+  p.num_units = unit;
   p.stages = pt.stages;
   p.kps = pt.kps;
   t = pt;
@@ -722,7 +730,7 @@ int run_fprop(const Geo& g, const DevInfo* dev, const void* xsrc, const void* bh
     rs_layout->hcols = ep8 ? 32 * ((t.BN / 32 + 1) / 2) : t.BN;
   }
   int grid = std::min(p.num_units, dev->sms);
-  if (bf) try_pair(p, t, g, dev, ceil_div(g.n_pix, kBM), bhi, g.Kf, g.OC, &grid);
+  if (bf) try_pair(p, t, g, dev, bhi, g.Kf, g.OC, &grid);
   p.stats_per_cta = t.n_tiles == 1 ? 1 : 0;
   if (stats_groups) *stats_groups = p.stats_per_cta ? grid : static_cast<int>(ceil_div(g.n_pix, kBM));
   LAUNCH("fprop_gemm", st, bf ? launch_conv_gemm_bf16(p, grid, t.smem, st) : launch_conv_gemm_tf32(p, grid, t.smem, st));
@@ -829,7 +837,7 @@ int run_dgrad_merged(const Geo& g, const DevInfo* dev, const void* w, const void
   p.err = dev->err;
   set_chunks(p, g, t.BN, ph.num_kb);
   int grid = std::min(p.num_units, dev->sms);
-  if (bf) try_pair(p, t, g, dev, ceil_div(ph.rows, kBM), whi, Kd, ncols, &grid);
+  if (bf) try_pair(p, t, g, dev, whi, Kd, ncols, &grid);
   LAUNCH("dgrad_gemm", st,
          bf ? launch_conv_gemm_bf16(p, grid, t.smem, st) : launch_conv_gemm_tf32(p, grid, t.smem, st));
   return CONV2D_OK;
@@ -905,7 +913,7 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
   }
   if (bf && !p.a_tma && d.tile.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;  // the gather's copies
   int grid = std::min(p.num_units, dev->sms);
-  if (bf) try_pair(p, d.tile, g, dev, ceil_div(p.ph[0].rows, kBM), whi, d.Kd, g.ICp, &grid);
+  if (bf) try_pair(p, d.tile, g, dev, whi, d.Kd, g.ICp, &grid);
   LAUNCH("dgrad_gemm", st,
          bf ? launch_conv_gemm_bf16(p, grid, d.tile.smem, st) : launch_conv_gemm_tf32(p, grid, d.tile.smem, st));
   return CONV2D_OK;

@@ -95,8 +95,8 @@ struct ConvGemmParams {
   int act, out_act;       // out = out_act ? act(v) : T(v); out2 = act(T(v))
   float* stats;           // optional batch statistics (count, mean, M2) of v: [m_tile][N][3], or
   int stats_per_cta;      // [blockIdx][N][3] merged over the CTA's tiles (single column tile only)
-  int pair;               // CTA pairs (clusters of two, cta_group::2): units are pairs of m-tiles (an even
-                          // count); bf16 with A by TMA and one phase only; B tiles are BN/2 rows per CTA
+  int pair;               // CTA pairs (clusters of two, cta_group::2): units are pairs of m-tiles of one phase
+                          // (every phase an even count); bf16 with A by TMA; B tiles are BN/2 rows per CTA
   float* rstats;          // optional layer-norm partials of the stored value, one per output pixel,
                           // column tile and epilogue column half (two halves when a_tma, else one):
                           // [pixel][n_tiles][halves][2] = (mean, M2) over the half's columns
@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
             const uint32_t a0 = sbase + s * stage_bytes + i * sub_bytes;
             const uint32_t b0 = a0 + a_tiles * a_bytes;
             if (pair) {
-              tma_load_im2col_4d_pair(a0, &p.tmap_a[0], bar, ck * D::BKE, aw, ah, an, static_cast<uint16_t>(tw),
+              tma_load_im2col_4d_pair(a0, &p.tmap_a[ph.a_map], bar, ck * D::BKE, aw, ah, an, static_cast<uint16_t>(tw),
                                       static_cast<uint16_t>(tt));
               tma_load_2d_pair(b0, &p.tmap_b, bar, kcol, n_tile * BN + static_cast<int>(rank) * (BN / 2));
             } else {
