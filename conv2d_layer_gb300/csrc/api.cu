@@ -146,6 +146,21 @@ bool encode_2d(CUtensorMap* m, const void* base, bool bf16, uint64_t cols, uint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A bf16 matrix [rows][C] (C a multiple of 64) seen as 64-channel panels: a 3-D view {64 channels, rows,
+// C / 64 groups} with 128-byte swizzled boxes of 64 x box_rows x groups, so that one copy lands `groups`
+// panels of box_rows rows, panel after panel (groups past C / 64 read as zeros).
+bool encode_panels(CUtensorMap* m, const void* base, uint64_t C, uint64_t rows, uint32_t box_rows, uint32_t groups) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || C % 64 != 0) return false;
+  cuuint64_t dims[3] = {64, rows, C / 64};
+  cuuint64_t strides[2] = {C * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, groups};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // fp32 GEMM B operand: the tf32 hi and lo matrices [rows][cols] (hi at `hi`, lo `lo`, 16-byte aligned,
 // lo after hi) seen as a 3-D tensor {cols, rows, 2 planes} whose plane stride is their distance, with
 // 128-byte swizzled boxes of 32 x box_rows x 2: one copy brings a k-block's hi rows and then its lo rows.
@@ -421,13 +436,15 @@ bool fold_kw(const Geo& g) {
 
 bool wgrad_raw_tma(const Geo& g) { return g.dt != CONV2D_BF16 && (g.ICp % 32 == 0 || fold_kw(g)); }
 
-WgradPlan wgrad_plan(const Geo& g, int sms) {
+// fused: d_conv formed in the B producer (see bwd_fused); its stages hold the pre-activation and dY boxes of
+// the column tile, so the tile is at most 128 columns wide (four stages of 48 KB)
+WgradPlan wgrad_plan(const Geo& g, int sms, bool fused) {
   WgradPlan w;
   const bool bf = g.dt == CONV2D_BF16;
   w.Mk = static_cast<int>(g.Kf);
   w.m_tiles = static_cast<int>(ceil_div(w.Mk, kBM));
   if (bf) {
-    w.n_tiles = static_cast<int>(ceil_div(g.OC, 256));
+    w.n_tiles = static_cast<int>(ceil_div(g.OC, fused ? 128 : 256));
     w.BN = static_cast<int>(round_up(ceil_div(g.OC, w.n_tiles), 64));
   } else {
     // at most 64 columns: the fp32 producers keep two k-blocks of X and one of d_conv in registers
@@ -466,7 +483,8 @@ WgradPlan wgrad_plan(const Geo& g, int sms) {
   w.splits = static_cast<int>(ceil_div(w.kb_total, w.kb_per_split));
   w.units = base * w.splits;
   const size_t ns = bf ? 1 : 2;
-  const size_t stage = ns * (kBM * 128 + static_cast<size_t>(w.BN) * 128);
+  const size_t stage = fused ? kBM * 128 + 2 * static_cast<size_t>(w.BN) * 128
+                             : ns * (kBM * 128 + static_cast<size_t>(w.BN) * 128);
   w.rstages = 0;
   if (wgrad_raw_tma(g)) {
     // A (X) in TMEM: a stage holds the d_conv hi and lo rows, and each stage has a TMEM stage of A
@@ -568,6 +586,18 @@ bool dgrad_col2im(const Geo& g) {
   return g.S > 1 && g.IC <= 16 && g.OCp >= g.BKE && dcol <= (size_t(1) << 31);
 }
 
+// Batch-norm backward with d_conv formed inside the dgrad and wgrad producers, never stored: for a 1x1,
+// stride-1 layer without padding d_conv is the dgrad's A operand and the wgrad's B operand as it is (each
+// element read once per GEMM and column tile), so both GEMMs can read the pre-activation and dY tiles in its
+// place and form it in shared memory (dconv_xform). bf16 with whole 64-channel boxes (OC and IC multiples of
+// 64: X by TMA in the wgrad), tanh or sigmoid (the activations whose stand-alone d_conv pass uses the same
+// arithmetic), and a streamed backward reduce (its third partial, sum (x - mean), gives dbias).
+bool bwd_fused(const Geo& g, const RowWalk& w3) {
+  return g.dt == CONV2D_BF16 && g.norm == CONV2D_NORM_BATCH && !g.bn_eval && g.KH == 1 && g.KW == 1 && g.S == 1 &&
+         g.P == 0 && g.OC % 64 == 0 && g.IC % 64 == 0 &&
+         (g.act == CONV2D_ACT_TANH || g.act == CONV2D_ACT_SIGMOID) && w3.stream && w3.cpg == 0;
+}
+
 // ------------------------------------------------------------ workspace plan
 enum Reg { R_XP, R_WB, R_WBLO, R_PART, R_FOLD, R_DC, R_C12, R_WD, R_WDLO, R_WPART, R_COL, R_NREG };
 
@@ -577,11 +607,13 @@ struct Plan {
   RowWalk walk;
   RowWalk walk3;  // batch-norm backward reduce: three blocks per SM (its own partials and finalize)
   WgradPlan wg;
+  bool fused;     // backward with d_conv formed in the GEMM producers (bwd_fused)
 };
 
 void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
   size_t sz[R_NREG] = {0};
   const size_t es = g.ES;
+  pl->fused = false;
   const bool ln = g.norm == CONV2D_NORM_LAYER;
   const bool gn = g.norm == CONV2D_NORM_GROUP;
   // layer and group norm walk each image as a segment of its own, statistics per group of channels
@@ -605,17 +637,21 @@ void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
       if (ln || gn) sz[R_DC] = static_cast<size_t>(g.n_pix) * g.OC * es;  // stored conv output, normalised into y
     }
   } else {
-    sz[R_DC] = static_cast<size_t>(g.n_pix) * g.OCp * es;
-    sz[R_PART] = std::max<size_t>(G, pl->walk3.G) * g.OC * 2 * 4;
-    // channel sums, then per-(image, group) sums
-    sz[R_C12] = 2 * (static_cast<size_t>(g.OC) + ((ln || gn) ? static_cast<size_t>(g.N) * g.groups : 0)) * 4;
+    pl->fused = bwd_fused(g, pl->walk3);
+    // the reduce with the third partial runs two blocks per SM (its registers allow no more without spills)
+    if (pl->fused) pl->walk3 = make_walk(g.n_pix, g.OC, g.dt, sms, 1, 0, 2);
+    if (!pl->fused) sz[R_DC] = static_cast<size_t>(g.n_pix) * g.OCp * es;
+    sz[R_PART] = std::max<size_t>(G, pl->walk3.G) * g.OC * (pl->fused ? 3 : 2) * 4;
+    // channel sums, then per-(image, group) sums; fused: then the per-channel terms of d_conv [6][OC]
+    sz[R_C12] = 2 * (static_cast<size_t>(g.OC) + ((ln || gn) ? static_cast<size_t>(g.N) * g.groups : 0)) * 4 +
+                (pl->fused ? 6 * static_cast<size_t>(g.OC) * 4 : 0);
     // dgrad weights: every phase's taps together hold each kernel tap once
     const size_t kd = std::max<size_t>(static_cast<size_t>(g.taps) * g.OCp, g.BKE);
     sz[R_WD] = static_cast<size_t>(g.ICp) * kd * es;
     if (g.dt == CONV2D_FP32) sz[R_WDLO] = static_cast<size_t>(g.ICp) * kd * 4;
     if (g.pack_x) sz[R_XP] = static_cast<size_t>(g.N) * g.H * g.W * g.ICp * es;
     if (dgrad_col2im(g) && !dgrad_merged(g)) sz[R_COL] = static_cast<size_t>(g.n_pix) * g.taps * g.ICp * es;
-    pl->wg = wgrad_plan(g, sms);
+    pl->wg = wgrad_plan(g, sms, pl->fused);
     sz[R_WPART] = static_cast<size_t>(pl->wg.splits) * g.OC * pl->wg.Mk * 4;
   }
   size_t o = 0;
@@ -843,8 +879,17 @@ int run_dgrad_merged(const Geo& g, const DevInfo* dev, const void* w, const void
   return CONV2D_OK;
 }
 
+// Operands of a backward with d_conv formed in the GEMM producers (see bwd_fused): the layer's stored
+// pre-activation, dY and the per-channel terms of d_conv [6][OC].
+struct XfSrc {
+  const void* pre;
+  const void* dy;
+  const float* tbl;
+};
+
 int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv, void* dx, void* ws,
-              const Plan& pl, cudaStream_t st) {
+              const Plan& pl, cudaStream_t st, const XfSrc* xf = nullptr) {
+  if (xf && (g.S != 1 || g.KH != 1 || g.KW != 1 || g.P != 0)) return CONV2D_ERR_INVALID_ARG;
   if (dgrad_merged(g)) return run_dgrad_merged(g, dev, w, dconv, dx, ws, pl, st);
   if (dgrad_col2im(g)) return run_dgrad_col2im(g, dev, w, dconv, dx, ws, pl, st);
   static ConvGemmParams p;
@@ -881,7 +926,18 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
   p.os = g.S;
   p.act = 0;
   p.out_act = 0;
-  if (d.table.flip) {
+  if (xf) {
+    // A = d_conv [n_pix][OC] formed from the pre-activation and dY tiles (ConvGemmParams::xf)
+    if (!encode_2d(&p.tmap_a[0], xf->pre, true, g.OC, g.n_pix, 64, kBM) ||
+        !encode_2d(&p.tmap_a[1], xf->dy, true, g.OC, g.n_pix, 64, kBM))
+      return CONV2D_ERR_CUDA;
+    p.a_tma = 1;
+    p.a_chunks = 1;
+    p.xf = 1;
+    p.xf_C = g.OC;
+    p.xf_tbl = xf->tbl;
+    p.act = g.act;
+  } else if (d.table.flip) {
     // One im2col map per stride phase. Phase row (a, b) reads d_conv at (a + qh - tt, b + qw - uu) for
     // its taps (tt, uu) < (Th, Tw): with the window corner (a + qh - (Th - 1), b + qw - (Tw - 1)) the
     // tap offsets are the flipped indices (Th - 1 - tt, Tw - 1 - uu), matching the flipped weight
@@ -901,7 +957,10 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
     p.a_chunks = g.OCp / g.BKE;
     p.ts = d.ts;
   }
-  if (bf && p.a_tma)
+  if (p.xf)  // a stage: the pre-activation and dY tiles and B, one k-block
+    fit_stages(d.tile, 2 * kBM * 128 + static_cast<size_t>(d.tile.BN) * 128,
+               (12 * static_cast<size_t>(d.tile.BN) + 6 * static_cast<size_t>(g.OC)) * 4, false);
+  else if (bf && p.a_tma)
     fit_stages(d.tile, conv_sub_bytes(g, d.tile.BN, false, false), 12 * static_cast<size_t>(d.tile.BN) * 4, true);
   p.stages = d.tile.stages;
   p.kps = d.tile.kps;
@@ -913,19 +972,29 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
   }
   if (bf && !p.a_tma && d.tile.stages < kLag + 1) return CONV2D_ERR_UNSUPPORTED;  // the gather's copies
   int grid = std::min(p.num_units, dev->sms);
-  if (bf) try_pair(p, d.tile, g, dev, whi, d.Kd, g.ICp, &grid);
+  if (bf && !p.xf) try_pair(p, d.tile, g, dev, whi, d.Kd, g.ICp, &grid);
   LAUNCH("dgrad_gemm", st,
          bf ? launch_conv_gemm_bf16(p, grid, d.tile.smem, st) : launch_conv_gemm_tf32(p, grid, d.tile.smem, st));
   return CONV2D_OK;
 }
 
 int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dconv, float* dw, void* ws,
-              const Plan& pl, cudaStream_t st) {
+              const Plan& pl, cudaStream_t st, const XfSrc* xf = nullptr) {
   WgradParams p;
   std::memset(&p, 0, sizeof(p));
   const WgradPlan& w = pl.wg;
   const bool bf = g.dt == CONV2D_BF16;
-  if (bf && !encode_2d(&p.tmap_dc, dconv, true, g.OCp, g.n_pix, 64, 64)) return CONV2D_ERR_CUDA;
+  if (xf && (!bf || g.ICp % 64 != 0 || g.OCp != g.OC)) return CONV2D_ERR_INVALID_ARG;
+  if (bf && !xf && !encode_2d(&p.tmap_dc, dconv, true, g.OCp, g.n_pix, 64, 64)) return CONV2D_ERR_CUDA;
+  if (xf) {  // B = d_conv formed from the pre-activation (tmap_dc) and dY panels (WgradParams::xf)
+    if (!encode_panels(&p.tmap_dc, xf->pre, g.OC, g.n_pix, 64, w.BN / 64) ||
+        !encode_panels(&p.tmap_dy, xf->dy, g.OC, g.n_pix, 64, w.BN / 64))
+      return CONV2D_ERR_CUDA;
+    p.xf = 1;
+    p.xf_C = g.OC;
+    p.xf_tbl = xf->tbl;
+    p.act = g.act;
+  }
   p.x = xsrc;
   p.dc32 = bf ? nullptr : static_cast<const float*>(dconv);
   p.H = g.H;
@@ -952,10 +1021,14 @@ int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dc
   p.splits = w.splits;
   p.num_units = w.units;
   p.partial = reinterpret_cast<float*>(region(ws, pl, R_WPART));
-  if (bf && g.ICp % 64 == 0 &&
-      encode_im2col(&p.tmap_x, xsrc, g.N, g.H, g.W, g.ICp, -g.P, -g.P, (g.OH - 1) * g.S - g.P - (g.H - 1),
-                    (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, w.KP))
+  if (xf) {  // 1x1, stride 1: X [n_pix][ICp] as two 64-channel panels per m-tile, one copy
+    if (!encode_panels(&p.tmap_x, xsrc, g.ICp, g.n_pix, 64, 2)) return CONV2D_ERR_CUDA;
     p.a_tma = 1;
+  } else if (bf && g.ICp % 64 == 0 &&
+             encode_im2col(&p.tmap_x, xsrc, g.N, g.H, g.W, g.ICp, -g.P, -g.P, (g.OH - 1) * g.S - g.P - (g.H - 1),
+                           (g.OW - 1) * g.S - g.P - (g.W - 1), g.S, w.KP)) {
+    p.a_tma = 1;
+  }
   if (wgrad_raw_tma(g)) {
     // folded view: the rows of the weight gradient are (kh, kw, ic) with one 32-float run per kh, i.e.
     // 32-channel chunks of KW = 1 taps
@@ -983,13 +1056,17 @@ int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dc
   size_t smem = w.smem;
   if (bf && p.a_tma) {  // k-blocks grouped per stage, each copy covering them all (WgradParams::kps)
     Tile t;
-    fit_stages(t, kBM * 128 + static_cast<size_t>(w.BN) * 128, 0, true);
+    if (p.xf)  // the X panels, the pre-activation and the dY boxes; one k-block per stage; the terms of d_conv
+      fit_stages(t, kBM * 128 + 2 * static_cast<size_t>(w.BN) * 128, 6 * static_cast<size_t>(g.OC) * 4, false);
+    else
+      fit_stages(t, kBM * 128 + static_cast<size_t>(w.BN) * 128, 0, true);
     p.stages = t.stages;
     p.kps = t.kps;
     smem = t.smem;
   }
+  if (p.xf && !p.a_tma) return CONV2D_ERR_UNSUPPORTED;
   // CTA pairs: two m-tiles per pair, each CTA with half of the d_conv columns
-  if (kUsePair && bf && p.a_tma && (w.m_tiles % 2) == 0 && w.BN % 128 == 0) {
+  if (kUsePair && bf && p.a_tma && !p.xf && (w.m_tiles % 2) == 0 && w.BN % 128 == 0) {
     Tile pt;
     fit_stages(pt, kBM * 128 + static_cast<size_t>(w.BN / 2) * 128, 0, true);
     const int stages = pt.stages;
@@ -1267,17 +1344,28 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
     // per-channel sums of d_norm and d_norm * z (dbeta, dgamma) and, from the same image-aligned block
     // partials, the per-image sums of gamma * d_norm and gamma * d_norm * z
     LAUNCH("ln_bwd_reduce", st,
-           launch_bn_bwd_reduce(g.dt, pre_act, dy, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, part, st));
+           launch_bn_bwd_reduce(g.dt, pre_act, dy, pl.walk, save_mean, save_inv_std, gamma, beta, g.act, part, 2,
+                                st));
     LAUNCH("ln_bwd_finalize", st, launch_sum_finalize(part, pl.walk, 2, 0, c12, dbeta, dgamma, st));
     LAUNCH("ln_seg_finalize", st, launch_norm_seg_finalize(part, pl.walk, gamma, c12 + 2 * g.OC, st));
     LAUNCH("ln_bwd_dconv", st,
            launch_bn_bwd_apply(g.dt, pre_act, dy, pl.walk, g.OCp, save_mean, save_inv_std, gamma, beta, g.act, c12,
                                dconv, part, st));
+  } else if (bn && pl.fused) {
+    // d_conv is formed inside the dgrad and wgrad producers (bwd_fused): the reduce's third partial gives
+    // dbias, and the finalize writes the per-channel terms of d_conv
+    LAUNCH("bn_bwd_reduce", st,
+           launch_bn_bwd_reduce(g.dt, pre_act, dy, pl.walk3, save_mean, save_inv_std, gamma, beta, g.act, part, 3,
+                                st));
+    LAUNCH("bn_bwd_finalize", st,
+           launch_bn_bwd_fused_finalize(part, pl.walk3, save_mean, save_inv_std, gamma, beta, c12, dbeta, dgamma,
+                                        dbias, c12 + 2 * g.OC, st));
   } else if (bn) {
     // the reduce walks with three blocks per SM (its own block count; the partials are summed before the
     // d_conv pass reuses the buffer)
     LAUNCH("bn_bwd_reduce", st,
-           launch_bn_bwd_reduce(g.dt, pre_act, dy, pl.walk3, save_mean, save_inv_std, gamma, beta, g.act, part, st));
+           launch_bn_bwd_reduce(g.dt, pre_act, dy, pl.walk3, save_mean, save_inv_std, gamma, beta, g.act, part, 2,
+                                st));
     LAUNCH("bn_bwd_finalize", st, launch_sum_finalize(part, pl.walk3, 2, 0, c12, dbeta, dgamma, st));
     // evaluation mode (frozen statistics): d_conv = d_norm * gamma * inv_std, no projection terms
     LAUNCH("bn_bwd_dconv", st,
@@ -1286,8 +1374,12 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
   } else {
     LAUNCH("act_bwd_dconv", st, launch_act_bwd(g.dt, pre_act, dy, pl.walk, g.OCp, g.act, dconv, part, st));
   }
-  if (dbias) LAUNCH("dbias_finalize", st, launch_sum_finalize(part, pl.walk, 1, 1, nullptr, dbias, nullptr, st));
-  if (dx && (rc = run_dgrad(g, dev, w, dconv, dx, ws, pl, st))) return rc;
+  if (dbias && !pl.fused)
+    LAUNCH("dbias_finalize", st, launch_sum_finalize(part, pl.walk, 1, 1, nullptr, dbias, nullptr, st));
+  XfSrc xfs{pre_act, dy, c12 + 2 * g.OC};
+  const XfSrc* xf = pl.fused ? &xfs : nullptr;
+  if (pl.fused) dconv = nullptr;  // not formed
+  if (dx && (rc = run_dgrad(g, dev, w, dconv, dx, ws, pl, st, xf))) return rc;
   if (dw) {
     const void* xsrc = x;
     if (g.pack_x) {
@@ -1295,7 +1387,7 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
       LAUNCH("pack_x", st, launch_pack_channels(g.dt, x, xp, static_cast<long>(g.N) * g.H * g.W, g.IC, g.ICp, st));
       xsrc = xp;
     }
-    if ((rc = run_wgrad(g, dev, xsrc, dconv, dw, ws, pl, st))) return rc;
+    if ((rc = run_wgrad(g, dev, xsrc, dconv, dw, ws, pl, st, xf))) return rc;
   }
   return CONV2D_OK;
 }

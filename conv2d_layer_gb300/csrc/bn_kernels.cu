@@ -444,45 +444,87 @@ __device__ __forceinline__ void kahan_add(float& s, float& comp, float x) {
   s = t;
 }
 
-// Per-channel sums of per-block partials [G][C][nv]: one 128-thread block per channel; compensated
-// fp32 sums per thread over every 128th partial, fp64 shuffle trees within the warps and the four warp
-// totals added in a fixed order (the same result on every run). mode 0: c12 = (sum d_norm,
-// sum d_norm z), dbeta += first, dgamma += second; mode 1: dbias += the sum.
-__global__ void __launch_bounds__(128) sum_finalize_kernel(const float* __restrict__ part, int G, int C, int nv,
-                                                           int mode, float* c12, float* acc0, float* acc1) {
-  pdl_entry();
-  __shared__ double s_w[2][4];
-  const int c = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float a = 0.f, ca = 0.f, b = 0.f, cb = 0.f;
+// Per-channel sums of per-block partials [G][C][nv] (nv <= 3): one 128-thread block per channel;
+// compensated fp32 sums per thread over every 128th partial, fp64 shuffle trees within the warps and the
+// four warp totals added in a fixed order (the same result on every run). Block-collective; the totals
+// are valid in thread 0.
+__device__ __forceinline__ void channel_sums(const float* __restrict__ part, int G, int C, int nv, int c,
+                                             double (&tot)[3]) {
+  __shared__ double s_w[3][4];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float a[3] = {0.f, 0.f, 0.f}, ca[3] = {0.f, 0.f, 0.f};
 #pragma unroll 4
   for (int k = threadIdx.x; k < G; k += 128) {
     const float* p = part + (static_cast<size_t>(k) * C + c) * nv;
-    kahan_add(a, ca, p[0]);
-    if (nv > 1) kahan_add(b, cb, p[1]);
+    kahan_add(a[0], ca[0], p[0]);
+    if (nv > 1) kahan_add(a[1], ca[1], p[1]);
+    if (nv > 2) kahan_add(a[2], ca[2], p[2]);
   }
-  double da = static_cast<double>(a) - static_cast<double>(ca);
-  double db = static_cast<double>(b) - static_cast<double>(cb);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    da += __shfl_xor_sync(0xffffffffu, da, off);
-    db += __shfl_xor_sync(0xffffffffu, db, off);
-  }
-  if (lane == 0) {
-    s_w[0][w] = da;
-    s_w[1][w] = db;
+  for (int v = 0; v < 3; ++v) {
+    double d = static_cast<double>(a[v]) - static_cast<double>(ca[v]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+    if (lane == 0) s_w[v][w] = d;
   }
   __syncthreads();
+#pragma unroll
+  for (int v = 0; v < 3; ++v) tot[v] = (s_w[v][0] + s_w[v][1]) + (s_w[v][2] + s_w[v][3]);
+}
+
+// mode 0: c12 = (sum d_norm, sum d_norm z), dbeta += first, dgamma += second; mode 1: dbias += the sum.
+__global__ void __launch_bounds__(128) sum_finalize_kernel(const float* __restrict__ part, int G, int C, int nv,
+                                                           int mode, float* c12, float* acc0, float* acc1) {
+  pdl_entry();
+  const int c = blockIdx.x;
+  double t[3];
+  channel_sums(part, G, C, nv, c, t);
   if (threadIdx.x == 0) {
-    const double ta = (s_w[0][0] + s_w[0][1]) + (s_w[0][2] + s_w[0][3]);
-    const double tb = (s_w[1][0] + s_w[1][1]) + (s_w[1][2] + s_w[1][3]);
     if (mode == 0) {
-      c12[2 * c] = static_cast<float>(ta);
-      c12[2 * c + 1] = static_cast<float>(tb);
-      if (acc0) acc0[c] += static_cast<float>(ta);  // dbeta
-      if (acc1) acc1[c] += static_cast<float>(tb);  // dgamma
+      c12[2 * c] = static_cast<float>(t[0]);
+      c12[2 * c + 1] = static_cast<float>(t[1]);
+      if (acc0) acc0[c] += static_cast<float>(t[0]);  // dbeta
+      if (acc1) acc1[c] += static_cast<float>(t[1]);  // dgamma
     } else {
-      if (acc0) acc0[c] += static_cast<float>(ta);  // dbias
+      if (acc0) acc0[c] += static_cast<float>(t[0]);  // dbias
     }
+  }
+}
+
+// Batch norm (training statistics) with d_conv formed inside the GEMM producers: from the backward
+// reduce's partials (sum d_norm, sum d_norm z, sum (x - mean)) per channel, c12 and dbeta / dgamma as in
+// sum_finalize_kernel mode 0, the per-channel terms of d_conv tbl[6][C] = (-mean, inv_std, gamma, beta,
+// -k1, k2) with k1, k2 as norm_bwd_coef forms them, and dbias = sum over pixels of d_conv without the
+// d_conv tensor: sum of inv_std (gamma d_norm - k1 - z k2) = inv_std (gamma sum d_norm - n k1) - inv_std k2
+// sum z, whose first term vanishes by the definition of k1, so dbias += -inv_std^2 k2 sum (x - mean).
+__global__ void __launch_bounds__(128) bn_bwd_fused_finalize_kernel(const float* __restrict__ part, int G, int C,
+                                                                    long n, const float* __restrict__ mean,
+                                                                    const float* __restrict__ inv_std,
+                                                                    const float* __restrict__ gamma,
+                                                                    const float* __restrict__ beta, float* c12,
+                                                                    float* dbeta, float* dgamma, float* dbias,
+                                                                    float* tbl) {
+  pdl_entry();
+  const int c = blockIdx.x;
+  double t[3];
+  channel_sums(part, G, C, 3, c, t);
+  if (threadIdx.x == 0) {
+    const float s1 = static_cast<float>(t[0]), s2 = static_cast<float>(t[1]);
+    c12[2 * c] = s1;
+    c12[2 * c + 1] = s2;
+    if (dbeta) dbeta[c] += s1;
+    if (dgamma) dgamma[c] += s2;
+    const float ga = gamma[c], is = inv_std[c];
+    float k1, k2;
+    norm_bwd_coef(c12, 0, 0, c, C, ga, n, k1, k2);
+    tbl[c] = -mean[c];
+    tbl[C + c] = is;
+    tbl[2 * C + c] = ga;
+    tbl[3 * C + c] = beta[c];
+    tbl[4 * C + c] = -k1;
+    tbl[5 * C + c] = k2;
+    if (dbias)
+      dbias[c] += static_cast<float>(-static_cast<double>(is) * static_cast<double>(is) * static_cast<double>(k2) * t[2]);
   }
 }
 
@@ -1296,9 +1338,10 @@ __global__ void __launch_bounds__(kBlock, 1) norm_stats_stream(const T* __restri
   }
 }
 
-// part[b][c] = {sum d_norm, sum d_norm * z}
-template <typename T, int EC, int A>
-__global__ void __launch_bounds__(kBlock, 3) bn_bwd_reduce_stream(const T* __restrict__ pre, const T* __restrict__ dy,
+// part[b][c] = {sum d_norm, sum d_norm * z} (NV = 2), and with NV = 3 also sum (x - mean): with it the
+// finalize forms dbias = sum d_conv without the d_conv pass (see sum_finalize_kernel, mode 2).
+template <typename T, int EC, int A, int NV = 2>
+__global__ void __launch_bounds__(kBlock, NV == 3 ? 2 : 3) bn_bwd_reduce_stream(const T* __restrict__ pre, const T* __restrict__ dy,
                                                                   long seg_rows, int bps, int C, long rpb, int R,
                                                                   int cpg, int rev, const float* __restrict__ mean,
                                                                   const float* __restrict__ inv_std,
@@ -1310,7 +1353,7 @@ __global__ void __launch_bounds__(kBlock, 3) bn_bwd_reduce_stream(const T* __res
   __shared__ uint64_t full[kStreamStages];
   stream_init(full);
   const StreamSetup<T, EC, 2> st(seg_rows, bps, C, rpb, rev);
-  float nmu[EC], is[EC], ga[EC], be[EC], a[EC], b[EC];
+  float nmu[EC], is[EC], ga[EC], be[EC], a[EC], b[EC], x3[EC];
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
     const int c = st.g * EC + e;
@@ -1319,7 +1362,7 @@ __global__ void __launch_bounds__(kBlock, 3) bn_bwd_reduce_stream(const T* __res
     is[e] = inv_std[si];
     ga[e] = gamma[c];
     be[e] = beta[c];
-    a[e] = b[e] = 0.f;
+    a[e] = b[e] = x3[e] = 0.f;
   }
   const T* const in[2] = {pre, dy};
   if constexpr (kPackedBwd<T, A>) {
@@ -1349,6 +1392,11 @@ __global__ void __launch_bounds__(kBlock, 3) bn_bwd_reduce_stream(const T* __res
                                     a[e + 1] = sa.y;
                                     b[e] = sb.x;
                                     b[e + 1] = sb.y;
+                                    if constexpr (NV == 3) {
+                                      const float2 s3 = __fadd2_rn(pr(x3, e), d);
+                                      x3[e] = s3.x;
+                                      x3[e + 1] = s3.y;
+                                    }
                                   }
                                 });
 #pragma unroll
@@ -1358,7 +1406,8 @@ __global__ void __launch_bounds__(kBlock, 3) bn_bwd_reduce_stream(const T* __res
                           [&](long, const float (&v)[2][EC]) {
 #pragma unroll
                             for (int e = 0; e < EC; e += 2) {
-                              const float2 z = __fmul2_rn(__fadd2_rn(pr(v[0], e), pr(nmu, e)), pr(is, e));
+                              const float2 xm = __fadd2_rn(pr(v[0], e), pr(nmu, e));
+                              const float2 z = __fmul2_rn(xm, pr(is, e));
                               const float2 t = __ffma2_rn(pr(ga, e), z, pr(be, e));
                               const float2 dn = make_float2(dact_mul<A, kFastAct<T>>(t.x, v[1][e]),
                                                             dact_mul<A, kFastAct<T>>(t.y, v[1][e + 1]));
@@ -1368,30 +1417,40 @@ __global__ void __launch_bounds__(kBlock, 3) bn_bwd_reduce_stream(const T* __res
                               a[e + 1] = sa.y;
                               b[e] = sb.x;
                               b[e + 1] = sb.y;
+                              if constexpr (NV == 3) {
+                                const float2 s3 = __fadd2_rn(pr(x3, e), xm);
+                                x3[e] = s3.x;
+                                x3[e + 1] = s3.y;
+                              }
                             }
                           });
   }
   // the ring is free once the walk has returned (every chunk consumed, or the copies of a walk that
-  // gave up landed): it holds the block's per-thread sums (2 * kBlock * EC floats <= the ring)
+  // gave up landed): it holds the block's per-thread sums (NV * kBlock * EC floats, at most 24 KB; make_walk's
+  // chunks give a ring of two inputs at least 32 KB)
   __syncthreads();
   float* s_a = reinterpret_cast<float*>(sm);
   float* s_b = s_a + kBlock * EC;
+  float* s_c = s_b + kBlock * EC;
 #pragma unroll
   for (int e = 0; e < EC; ++e) {
     s_a[threadIdx.x * EC + e] = a[e];
     s_b[threadIdx.x * EC + e] = b[e];
+    if constexpr (NV == 3) s_c[threadIdx.x * EC + e] = x3[e];
   }
   __syncthreads();
   if (st.rl == 0) {
     for (int e = 0; e < EC; ++e) {
-      float sa = 0.f, sb = 0.f;
+      float sa = 0.f, sb = 0.f, sc = 0.f;
       for (int k = 0; k < st.rpp; ++k) {
         sa += s_a[(k * st.tpr + st.g) * EC + e];
         sb += s_b[(k * st.tpr + st.g) * EC + e];
+        if constexpr (NV == 3) sc += s_c[(k * st.tpr + st.g) * EC + e];
       }
-      float* o = part + (static_cast<size_t>(st.lb) * C + st.g * EC + e) * 2;
+      float* o = part + (static_cast<size_t>(st.lb) * C + st.g * EC + e) * NV;
       o[0] = sa;
       o[1] = sb;
+      if constexpr (NV == 3) o[2] = sc;
     }
   }
 }
@@ -1708,7 +1767,23 @@ cudaError_t launch_bn_apply(int dtype, const void* pre, void* y, const RowWalk& 
 
 cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, const RowWalk& wk, const float* mean,
                                  const float* inv_std, const float* gamma, const float* beta, int act, float* part,
-                                 cudaStream_t st) {
+                                 int nv, cudaStream_t st) {
+  if (nv == 3) {
+    // the third partial serves the backward that forms d_conv inside the GEMMs: streamed batch-norm walks
+    // of bf16 layers with tanh or sigmoid only; two blocks per SM
+    if (!(wk.stream && wk.cpg == 0 && dtype == 1 && (act == 2 || act == 3))) return cudaErrorInvalidValue;
+    constexpr int EC = 8;
+    using T = __nv_bfloat16;
+    const size_t smem = static_cast<size_t>(kStreamStages) * 2 * wk.R * wk.C * sizeof(T);
+    auto go = [&](auto kernel) {
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      launch_k(kernel, wk.G, kBlock, smem, st, 1, static_cast<const T*>(pre), static_cast<const T*>(dy), WALK_ARGS,
+               wk.R, LN_FLAG, 0, mean, inv_std, gamma, beta, part, wk.err);
+    };
+    if (act == 2) go(bn_bwd_reduce_stream<T, EC, 2, 3>);
+    else go(bn_bwd_reduce_stream<T, EC, 3, 3>);
+    return cudaGetLastError();
+  }
   if (wk.stream) {
     // three blocks per SM (registers capped for it); the column-sum scratch reuses the ring, so three
     // rings of full chunks fit in shared memory
@@ -1730,6 +1805,14 @@ cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, con
 cudaError_t launch_sum_finalize(const float* part, const RowWalk& wk, int nv, int mode, float* c12, float* acc0,
                                 float* acc1, cudaStream_t st) {
   launch_k(sum_finalize_kernel, wk.C, 128, 0, st, 1, part, wk.G, wk.C, nv, mode, c12, acc0, acc1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bn_bwd_fused_finalize(const float* part, const RowWalk& wk, const float* mean,
+                                         const float* inv_std, const float* gamma, const float* beta, float* c12,
+                                         float* dbeta, float* dgamma, float* dbias, float* tbl, cudaStream_t st) {
+  launch_k(bn_bwd_fused_finalize_kernel, wk.C, 128, 0, st, 1, part, wk.G, wk.C, wk.rows, mean, inv_std, gamma, beta,
+           c12, dbeta, dgamma, dbias, tbl);
   return cudaGetLastError();
 }
 

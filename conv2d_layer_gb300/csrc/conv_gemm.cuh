@@ -129,6 +129,12 @@ struct ConvGemmParams {
   // and IC are powers of two, seg_sh and ic_sh their logarithms.
   // Runs of rows at or past out_h, and values of columns at or past out_w, are not written. 0: off.
   int seg, seg_sh, ic_sh, seg_ld, out_h, out_w;
+  // bf16 dgrad of a 1x1, stride-1 batch-norm layer with d_conv formed in the A producer (no d_conv tensor):
+  // a k-block's A tile arrives as the stored pre-activation tile (tmap_a[0]) and the dY tile (tmap_a[1]),
+  // 2-D boxes of 64 channels x 128 rows, and warps 2-5 turn the first into d_conv (dconv_xform) before the
+  // MMA reads it. xf_tbl: the per-channel terms [6][xf_C]. One k-block per stage, single CTAs. 0: off.
+  int xf, xf_C;
+  const float* xf_tbl;
   int* err;
   ConvPhase ph[kMaxPhases];
 };
@@ -158,6 +164,14 @@ struct WgradParams {
   // fp32 with raw TMA tiles: A (X, k rows x 32 pixels) in tensor memory, one TMEM stage per shared-memory
   // stage, which then holds the d_conv hi and lo rows only; the MMAs as in ConvGemmParams::ts
   int ts;
+  // bf16 1x1, stride-1 layers: d_conv formed in the B producer (as ConvGemmParams::xf). A stage holds the X
+  // panels (tmap_x), the pre-activation panels (tmap_dc) and the dY panels (tmap_dy), each brought by one
+  // copy through a 3-D view of its [n_pix][channels] matrix (64 channels x pixels x 64-channel groups, boxes
+  // of 64 x 64 x panels); warps 2-5 turn the pre-activation panels into d_conv. One k-block per stage,
+  // single CTAs. 0: off.
+  CUtensorMap tmap_dy;
+  int xf, xf_C, act;      // act: the layer's activation (2 tanh or 3 sigmoid)
+  const float* xf_tbl;
   int* err;
 };
 
@@ -333,6 +347,83 @@ static __device__ __noinline__ void fold_chunks(uint32_t taddr, int stride, int 
   tmem_st_wait();
 }
 
+// d_conv of a batch-norm layer with training statistics, formed in a shared-memory stage from the layer's
+// stored pre-activation x and dY (bf16):
+//   z = (x - mean) inv_std, t = gamma z + beta, d_norm = act'(t) dY,
+//   d_conv = inv_std (gamma d_norm - k1 - z k2),  k1 = gamma sum(d_norm) / n,  k2 = gamma sum(d_norm z) / n,
+// in the operation order of the stand-alone d_conv pass (bf16 layers take the fast activations there too),
+// so that both round to the same bf16 values. The tiles are nbox boxes of NR * RS rows of 64 channels
+// (128-byte swizzle; box b at b * NR * RS * 128 bytes): x at xa, dY at the same offsets from ya; d_conv
+// replaces x. Thread t (of 8 RS) takes 16-byte chunk t & 7 of rows t / 8 + RS i of every box; under the
+// swizzle that chunk holds channels 8 ((t & 7) ^ (t / 8 & 7)) .. + 7 of the box in each of those rows.
+// All NR rows of a box are read before any is computed (one thread per row chunk leaves the arithmetic's
+// latency to the other rows to hide). tbl: per-channel terms [6][C] (-mean, inv_std, gamma, beta, -k1,
+// k2) in shared memory; c0: channel of box 0's first column; channels at or past C take zero terms; rows
+// at or past nvalid (pixels past the layer) are written as zeros.
+template <int A, int NR, int RS>
+__device__ __forceinline__ void dconv_xform(uint32_t xa, uint32_t ya, int nbox, const float* tbl, int C, int c0,
+                                            int nvalid, int t) {
+  const int pj = t & 7, r0 = t >> 3;
+  const int ch = 8 * (pj ^ (r0 & 7));
+  for (int b = 0; b < nbox; ++b) {
+    const int c = c0 + 64 * b + ch;
+    float k[6][8];
+#pragma unroll
+    for (int q = 0; q < 6; ++q) {
+      float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+      if (c < C) {  // C is a multiple of 8: the thread's eight channels are all inside or all outside
+        lo = *reinterpret_cast<const float4*>(tbl + q * C + c);
+        hi = *reinterpret_cast<const float4*>(tbl + q * C + c + 4);
+      }
+      k[q][0] = lo.x; k[q][1] = lo.y; k[q][2] = lo.z; k[q][3] = lo.w;
+      k[q][4] = hi.x; k[q][5] = hi.y; k[q][6] = hi.z; k[q][7] = hi.w;
+    }
+    const uint32_t bo = static_cast<uint32_t>(b * NR * RS * 128 + r0 * 128 + (pj << 4));
+    uint32_t wx[NR][4], wd[NR][4];
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+      const uint32_t off = bo + static_cast<uint32_t>(i * RS * 128);
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(wx[i][0]), "=r"(wx[i][1]), "=r"(wx[i][2]), "=r"(wx[i][3]) : "r"(xa + off));
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(wd[i][0]), "=r"(wd[i][1]), "=r"(wd[i][2]), "=r"(wd[i][3]) : "r"(ya + off));
+    }
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int e = 2 * q;
+        const float2 x = make_float2(__uint_as_float(wx[i][q] << 16), __uint_as_float(wx[i][q] & 0xffff0000u));
+        const float2 dy = make_float2(__uint_as_float(wd[i][q] << 16), __uint_as_float(wd[i][q] & 0xffff0000u));
+        const float2 ga = make_float2(k[2][e], k[2][e + 1]);
+        const float2 z = __fmul2_rn(__fadd2_rn(x, make_float2(k[0][e], k[0][e + 1])), make_float2(k[1][e], k[1][e + 1]));
+        const float2 tt = __ffma2_rn(ga, z, make_float2(k[3][e], k[3][e + 1]));
+        float2 dn;
+        if constexpr (A == 1) {
+          dn = make_float2(tt.x > 0.f ? dy.x : 0.f, tt.y > 0.f ? dy.y : 0.f);
+        } else {
+          dn = make_float2(dact_t<A, true>(tt.x) * dy.x, dact_t<A, true>(tt.y) * dy.y);
+        }
+        const float2 u = __ffma2_rn(ga, dn, make_float2(k[4][e], k[4][e + 1]));
+        const float2 v = __fmul2_rn(make_float2(k[1][e], k[1][e + 1]),
+                                    __ffma2_rn(make_float2(-z.x, -z.y), make_float2(k[5][e], k[5][e + 1]), u));
+        __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+        o[q] = r0 + RS * i < nvalid ? *reinterpret_cast<uint32_t*>(&h) : 0u;
+      }
+      st_shared_v4(xa + bo + static_cast<uint32_t>(i * RS * 128), o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+// The per-channel terms of d_conv [6][C] (C a multiple of 8) copied into shared memory by the 256 threads
+// of warps 2-9, which then pass named barrier 2 together.
+__device__ __forceinline__ void load_xform_terms(float* dst, const float* __restrict__ src, int C, int t) {
+  for (int i = 4 * t; i < 6 * C; i += 4 * 256)
+    *reinterpret_cast<float4*>(dst + i) = __ldg(reinterpret_cast<const float4*>(src + i));
+  named_bar_sync(2, 256);
+}
+
 template <typename T>
 __device__ __forceinline__ void store_row16(T* dst, const float* v, int ncols, bool vec);
 
@@ -449,7 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
   const uint32_t b_own = pair ? b_bytes / 2 : b_bytes;
   // fp32 with A in TMEM (see ConvGemmParams::ts): a stage holds the raw A tile, B hi and B lo
   const bool ts = DT == 0 && p.ts;
-  const uint32_t a_tiles = (DT == 0 && !ts) ? 2u : 1u;  // A tiles per k-block (fp32 in shared memory: hi, lo)
+  // d_conv formed from the pre-activation and dY tiles (see ConvGemmParams::xf)
+  const bool xf = DT == 1 && !PAIR && p.xf;
+  // A tiles per k-block (fp32 in shared memory: hi, lo; xf: pre-activation, dY)
+  const uint32_t a_tiles = ((DT == 0 && !ts) || xf) ? 2u : 1u;
   const int KPS = p.kps > 1 ? p.kps : 1;                // k-blocks per stage
   const uint32_t sub_bytes = a_tiles * a_bytes + D::NS * b_own;  // one k-block of a stage
   const uint32_t stage_bytes = KPS * sub_bytes;
@@ -465,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
   // fp32 with A by TMA: warps 2-5 split the stages (and the epilogue keeps four warps)
   const bool split_a = DT == 0 && p.a_tma;
   // epilogue of eight warps (warps 2-9) when the gather warps are free: bf16 with A by TMA
-  const bool ep8 = DT == 1 && p.a_tma;
+  const bool ep8 = DT == 1 && p.a_tma && !xf;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = pair ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;  // issues the MMAs of the pair
@@ -495,16 +589,17 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     for (int b = 0; b < nbuf; ++b) {
       mbar_init(&tfull[b], 1);
       // one arrival per epilogue warp (of both CTAs when paired: the even CTA's MMA writes both TMEMs)
-      mbar_init(&tempty[b], (ep8 ? 8 : 4) * (pair ? 2 : 1));
+      mbar_init(&tempty[b], ((ep8 || xf) ? 8 : 4) * (pair ? 2 : 1));
     }
-    if (split_a)  // with A in TMEM indexed by TMEM stage
-      for (int s = 0; s < (ts ? TA : S); ++s) mbar_init(&sfull[s], 4);  // one arrival per splitting warp
+    if (split_a || xf)  // with A in TMEM indexed by TMEM stage; one arrival per splitting / transforming warp
+      for (int s = 0; s < (ts ? TA : S); ++s) mbar_init(&sfull[s], xf ? 8 : 4);
     if (ts)
       for (int j = 0; j < TA; ++j) mbar_init(&aempty[j], 1);  // the MMA warp's commit
     fence_mbar_init();
     tma_prefetch_desc(&p.tmap_b);
     if (p.a_tma)
       for (int i = 0; i < p.num_phases && i < kMaxTmaPhases; ++i) tma_prefetch_desc(&p.tmap_a[i]);
+    if (xf) tma_prefetch_desc(&p.tmap_a[1]);
   }
   if (warp == 1) {
     if (pair) {
@@ -532,7 +627,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         const int local = u - ph.unit_begin;
         const int n_tile = local % p.n_tiles;
         int an = 0, ah = 0, aw = 0;  // window corner of the tile's first row (TMA im2col)
-        if (p.a_tma) {
+        const int xrow = xf ? (local / p.n_tiles) * kBM : 0;  // xf: first row of the tile
+        if (p.a_tma && !xf) {
           const int m_tile = pair ? 2 * (local / p.n_tiles) + static_cast<int>(rank) : local / p.n_tiles;
           const int m0 = m_tile * kBM;
           an = static_cast<int>(fdiv(static_cast<uint32_t>(m0), ph.div_HaWa));
@@ -555,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           if (pair) {
             if (leader) mbar_arrive_expect_tx(&full[s], 2u * nk * (a_bytes + b_own));
           } else {
-            mbar_arrive_expect_tx(&full[s], nk * (D::NS * b_bytes + (p.a_tma ? a_bytes : 0u)));
+            mbar_arrive_expect_tx(&full[s], nk * (D::NS * b_bytes + (p.a_tma ? (xf ? 2u : 1u) * a_bytes : 0u)));
           }
 #pragma unroll
           for (int i = 0; i < kMaxKps; ++i) {
@@ -568,9 +664,13 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
                                       static_cast<uint16_t>(tt));
               tma_load_2d_pair(b0, &p.tmap_b, bar, kcol, n_tile * BN + static_cast<int>(rank) * (BN / 2));
             } else {
-              if (p.a_tma)
+              if (xf) {  // the pre-activation and dY tiles of k-block g0 + i (64 channels each)
+                tma_load_2d(a0, &p.tmap_a[0], &full[s], (g0 + i) * D::BKE, xrow);
+                tma_load_2d(a0 + a_bytes, &p.tmap_a[1], &full[s], (g0 + i) * D::BKE, xrow);
+              } else if (p.a_tma) {
                 tma_load_im2col_4d(a0, &p.tmap_a[ph.a_map], &full[s], ck * D::BKE, aw, ah, an,
                                    static_cast<uint16_t>(tw), static_cast<uint16_t>(tt));
+              }
               if (D::NS == 2) tma_load_3d(b0, &p.tmap_b, &full[s], kcol, n_tile * BN, 0);  // hi and lo rows
               else tma_load_2d(b0, &p.tmap_b, &full[s], kcol, n_tile * BN);
             }
@@ -619,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           const int nk = min(KPS, ph.num_kb - g0);
           // with A in TMEM the split warps arrive on the TMEM stage's barrier after the shared-memory stage
           // has landed, so that one wait covers both
-          if (!wait(ts ? &sfull[j] : (split_a ? &sfull[s] : &full[s]), ts ? apar : par, p.err, kSiteFull)) {
+          if (!wait(ts ? &sfull[j] : ((split_a || xf) ? &sfull[s] : &full[s]), ts ? apar : par, p.err, kSiteFull)) {
             alive = false;
             break;
           }
@@ -888,6 +988,80 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         }
       }
     }
+  } else if (xf) {
+    // ------------------------------------------------ d_conv from the pre-activation and dY tiles, and the epilogue
+    // Warps 2-9 turn each landed stage's pre-activation tile into d_conv (four rows per thread; the MMA waits
+    // for sfull); after a tile's k-blocks they store the tile before it (its accumulator completed meanwhile):
+    // two warps per TMEM lane quarter, one per column half. The terms of d_conv follow the epilogue scratch.
+    const int t = threadIdx.x - 64;
+    float* tbl = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16) + 12 * BN;
+    load_xform_terms(tbl, p.xf_tbl, p.xf_C, t);
+    const int q = warp & 3, half = (warp - 2) >> 2;
+    const int hcols = 32 * ((BN / 32 + 1) / 2);
+    const int cb = half * hcols, ce = half ? BN : hcols;
+    const bool vec = (p.out_ld % D::EC) == 0;
+    // store tile u (the tc-th of this CTA): a 1x1, stride-1 dgrad writes row m of D to dX pixel m
+    auto epilogue = [&](int u, int tc) -> bool {
+      const ConvPhase& ph = find_phase(p, u);
+      const int local = u - ph.unit_begin;
+      const int m_tile = local / p.n_tiles, n_tile = local % p.n_tiles;
+      const int buf = tc % nbuf;
+      int ok = 1;
+      if (lane == 0) ok = wait(&tfull[buf], (tc / nbuf) & 1, p.err, kSiteTFull) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      tc_fence_after();
+      const int m = m_tile * kBM + q * 32 + lane;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * tcs;
+      T* out = static_cast<T*>(p.out) + static_cast<size_t>(m) * p.out_ld;
+      for (int c0 = cb; c0 < ce; c0 += 64) {  // 64 columns per wait (two 32-column loads)
+        if (n_tile * BN + c0 >= p.N) break;  // uniform across the warp
+        const int c1 = c0 + 32 < ce ? c0 + 32 : c0;
+        uint32_t ra[32], rb[32];
+        tmem_ld32(taddr + c0, ra);
+        tmem_ld32(taddr + c1, rb);
+        tmem_ld_wait2(ra, rb);
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(ra[e]);
+        if (m < ph.rows) store_row32<T>(out + n_tile * BN + c0, v, p.N - (n_tile * BN + c0), vec);
+        if (c1 != c0 && n_tile * BN + c1 < p.N) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(rb[e]);
+          if (m < ph.rows) store_row32<T>(out + n_tile * BN + c1, v, p.N - (n_tile * BN + c1), vec);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      return true;
+    };
+    int s = 0;
+    uint32_t par = 0;
+    bool alive = true;
+    int prev = -1, tc = 0;
+    for (int u = cid; u < p.num_units && alive; u += ncl, ++tc) {
+      const ConvPhase& ph = find_phase(p, u);
+      const int m0 = ((u - ph.unit_begin) / p.n_tiles) * kBM;
+      for (int kb = 0; kb < ph.num_kb; ++kb) {
+        if (!__all_sync(0xffffffffu, wait(&full[s], par, p.err, kSiteFull))) {  // warp-uniform
+          alive = false;
+          break;
+        }
+        const uint32_t a0 = sbase + s * stage_bytes;
+        if (p.act == 3) dconv_xform<3, kBM / 32, 32>(a0, a0 + a_bytes, 1, tbl, p.xf_C, kb * D::BKE, ph.rows - m0, t);
+        else dconv_xform<2, kBM / 32, 32>(a0, a0 + a_bytes, 1, tbl, p.xf_C, kb * D::BKE, ph.rows - m0, t);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[s]);
+        if (++s == S) {
+          s = 0;
+          par ^= 1;
+        }
+      }
+      if (alive && prev >= 0 && !epilogue(prev, tc - 1)) alive = false;
+      prev = u;
+    }
+    if (alive && prev >= 0) epilogue(prev, tc - 1);
   } else {
     // ------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -1133,7 +1307,11 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
   const uint32_t b_own = pair ? b_bytes / 2 : b_bytes;  // a pair member holds half of the oc columns
   // fp32 with A in TMEM (WgradParams::ts): a stage holds the d_conv hi and lo rows only
   const bool ts = DT == 0 && p.ts;
-  const uint32_t stage_bytes = ts ? 2 * b_bytes : D::NS * (a_bytes + b_own) * (DT == 1 && p.kps > 1 ? p.kps : 1);
+  // d_conv formed from the pre-activation and dY boxes (WgradParams::xf): a stage holds X, then both
+  const bool xf = DT == 1 && !PAIR && p.xf;
+  const uint32_t stage_bytes = ts ? 2 * b_bytes
+                                  : (xf ? a_bytes + 2 * b_bytes
+                                        : D::NS * (a_bytes + b_own) * (DT == 1 && p.kps > 1 ? p.kps : 1));
   const int S = p.stages;
   const int KPS = DT == 1 && p.kps > 1 ? p.kps : 1;  // k-blocks per stage (bf16 with A by TMA)
   const uint32_t panel = 8192u * KPS;                  // distance between MN-major panels / d_conv boxes
@@ -1148,7 +1326,8 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
   uint64_t* tempty = tfull + 2;
   uint64_t* rfull = tempty + 2;
   uint64_t* rempty = rfull + kMaxStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rempty + kMaxStages);
+  uint64_t* sfull = rempty + kMaxStages;  // xf: d_conv formed in the stage
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfull + kMaxStages);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t rbase = smem_u32(rawp);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1170,15 +1349,18 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], pair ? 8 : 4);  // epilogue warps (of both CTAs when paired)
+      mbar_init(&tempty[b], (pair || xf) ? 8 : 4);  // epilogue warps (of both CTAs when paired; xf: warps 2-9)
     }
     for (int r = 0; r < NR; ++r) {
       mbar_init(&rfull[r], 1);   // the TMA thread
       mbar_init(&rempty[r], 4);  // one arrival per transposing warp
     }
+    if (xf)
+      for (int s = 0; s < S; ++s) mbar_init(&sfull[s], 8);  // one arrival per transforming warp
     fence_mbar_init();
     if (DT == 1 || raw_a) tma_prefetch_desc(&p.tmap_dc);
     if (p.a_tma) tma_prefetch_desc(&p.tmap_x);
+    if (xf) tma_prefetch_desc(&p.tmap_dy);
   }
   if (warp == 1) {
     if (pair) {
@@ -1258,6 +1440,13 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
             for (int jn = 0; jn < nb; ++jn)
               tma_load_2d_pair(b0 + jn * panel, &p.tmap_dc, bar,
                                n_tile * BN + 64 * (static_cast<int>(rank) * nb + jn), pix);
+          } else if (xf) {
+            // 1x1, stride 1: X, the pre-activation and dY are [n_pix][channels] matrices; each comes as one
+            // copy of its 64-pixel panels (a 3-D view: 64 channels x pixels x 64-channel groups)
+            mbar_arrive_expect_tx(&full[s], a_bytes + 2 * b_bytes);
+            tma_load_3d(a0, &p.tmap_x, &full[s], 0, pix, 2 * m_tile);
+            tma_load_3d(b0, &p.tmap_dc, &full[s], 0, pix, n_tile * (BN / 64));
+            tma_load_3d(b0 + b_bytes, &p.tmap_dy, &full[s], 0, pix, n_tile * (BN / 64));
           } else {
             mbar_arrive_expect_tx(&full[s], KPS * (b_bytes + a_tx));
             if (p.a_tma) {
@@ -1355,7 +1544,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
         const uint32_t d = tmem_base + buf * acols;
         for (int g0 = kb0; g0 < kb1; g0 += KPS) {  // one stage: k-blocks g0 .. g0 + nk - 1
           const int nk = min(KPS, kb1 - g0);
-          if (!wait(&full[s], par, p.err, kSiteFull)) {
+          if (!wait(xf ? &sfull[s] : &full[s], par, p.err, kSiteFull)) {
             alive = false;
             break;
           }
@@ -1405,6 +1594,76 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
         }
       }
     }
+  } else if (xf) {
+    // ------------------------------------------------ d_conv from the pre-activation and dY panels, and the epilogue
+    // Warps 2-9 turn each landed stage's pre-activation panels into d_conv (two rows of every panel per thread;
+    // the MMA waits for sfull); after a unit's k-blocks they write the unit before it (its accumulator
+    // completed meanwhile): two warps per TMEM lane quarter, one per column half. The terms of d_conv follow
+    // the TMEM slot.
+    const int t = threadIdx.x - 64;
+    float* tbl = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16);
+    load_xform_terms(tbl, p.xf_tbl, p.xf_C, t);
+    const int q = warp & 3, half = (warp - 2) >> 2;
+    const int hcols = 32 * ((BN / 32 + 1) / 2);
+    const int cb = half * hcols, ce = half ? BN : hcols;
+    auto epilogue = [&](int u, int tc) -> bool {
+      int m_tile, n_tile, kb0, kb1;
+      decode(u, m_tile, n_tile, kb0, kb1);
+      const int split = u / (p.m_tiles * p.n_tiles);
+      const int buf = tc & 1;
+      int ok = 1;
+      if (lane == 0) ok = wait(&tfull[buf], (tc >> 1) & 1, p.err, kSiteTFull) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      tc_fence_after();
+      const int m = m_tile * kBM + q * 32 + lane;
+      const bool zero = kb1 <= kb0;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * acols;
+      for (int c0 = cb; c0 < ce; c0 += 32) {
+        if (n_tile * BN + c0 >= p.N) break;  // uniform across the warp
+        uint32_t r[32];
+        tmem_ld32(taddr + c0, r);
+        tmem_ld_wait32(r);
+        if (m < p.Mk) {
+          float* dst = p.partial + (static_cast<size_t>(split) * p.N + n_tile * BN + c0) * p.Mk + m;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (n_tile * BN + c0 + e < p.N) dst[static_cast<size_t>(e) * p.Mk] = zero ? 0.f : __uint_as_float(r[e]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      return true;
+    };
+    int s = 0;
+    uint32_t par = 0;
+    bool alive = true;
+    int prev = -1, tc = 0;
+    for (int u = cid; u < p.num_units && alive; u += ncl, ++tc) {
+      int m_tile, n_tile, kb0, kb1;
+      decode(u, m_tile, n_tile, kb0, kb1);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!__all_sync(0xffffffffu, wait(&full[s], par, p.err, kSiteFull))) {  // warp-uniform
+          alive = false;
+          break;
+        }
+        const uint32_t b0 = sbase + s * stage_bytes + a_bytes;
+        if (p.act == 3)
+          dconv_xform<3, KP / 32, 32>(b0, b0 + b_bytes, BN / 64, tbl, p.xf_C, n_tile * BN, p.n_pix - kb * KP, t);
+        else
+          dconv_xform<2, KP / 32, 32>(b0, b0 + b_bytes, BN / 64, tbl, p.xf_C, n_tile * BN, p.n_pix - kb * KP, t);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[s]);
+        if (++s == S) {
+          s = 0;
+          par ^= 1;
+        }
+      }
+      if (alive && prev >= 0 && !epilogue(prev, tc - 1)) alive = false;
+      prev = u;
+    }
+    if (alive && prev >= 0) epilogue(prev, tc - 1);
   } else if (warp < 6) {
     const int t = threadIdx.x - 64;
     const char* xs = static_cast<const char*>(p.x);

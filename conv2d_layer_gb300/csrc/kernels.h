@@ -86,13 +86,20 @@ cudaError_t launch_bn_stats_finalize(const float* part, const RowWalk& wk, float
 cudaError_t launch_bn_apply(int dtype, const void* pre, void* y, const RowWalk& wk, const float* mean,
                             const float* inv_std, const float* gamma, const float* beta, int act, int rev,
                             cudaStream_t st);
+// part[G][C][nv]: (sum d_norm, sum d_norm z) and, with nv = 3 (streamed batch-norm walks only), sum (x - mean)
 cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, const RowWalk& wk, const float* mean,
                                  const float* inv_std, const float* gamma, const float* beta, int act, float* part,
-                                 cudaStream_t st);
+                                 int nv, cudaStream_t st);
 // sums[c][v] over the G block partials (v < nv); mode 0: c12 <- sums, dbeta += s0, dgamma += s1;
 // mode 1: dbias += s0.
 cudaError_t launch_sum_finalize(const float* part, const RowWalk& wk, int nv, int mode, float* c12, float* acc0,
                                 float* acc1, cudaStream_t st);
+// Batch norm with d_conv formed inside the GEMM producers: from the nv = 3 reduce partials, c12, dbeta,
+// dgamma, dbias (each accumulated where non-null) and the per-channel terms tbl[6][C] of d_conv
+// (-mean, inv_std, gamma, beta, -k1, k2).
+cudaError_t launch_bn_bwd_fused_finalize(const float* part, const RowWalk& wk, const float* mean,
+                                         const float* inv_std, const float* gamma, const float* beta, float* c12,
+                                         float* dbeta, float* dgamma, float* dbias, float* tbl, cudaStream_t st);
 // d_conv under batch norm (c12 = per-channel sums from launch_sum_finalize; null: evaluation mode) or,
 // on a segmented walk, layer norm (c12 + 2C = the per-image sums of launch_ln_seg_finalize).
 cudaError_t launch_bn_bwd_apply(int dtype, const void* pre, const void* dy, const RowWalk& wk, int Cp,

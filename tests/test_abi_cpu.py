@@ -90,6 +90,20 @@ def test_workspace_sizes_positive_and_op_checked():
     assert abi.conv2d_workspace_size(d, abi.OP_BWD) >= 2 * 56 * 56 * 256 * 2
 
 
+def test_fused_backward_keeps_no_dconv_tensor():
+    # 1x1, stride-1 bf16 batch-norm layers with tanh or sigmoid form d_conv inside the dgrad and wgrad
+    # producers: their backward workspace holds no n_pix x OC d_conv tensor; ReLU (and fp32, and a 3x3
+    # kernel) keep it
+    shape = dict(N=64, H=56, W=56, IC=128, OC=256, KH=1, KW=1, stride=1, pad=0, dtype=abi.BF16)
+    dconv = 64 * 56 * 56 * 256 * 2
+    fused = [abi.conv2d_workspace_size(good(act=a, **shape), abi.OP_BWD) for a in (abi.ACT_TANH, abi.ACT_SIGMOID)]
+    kept = [abi.conv2d_workspace_size(good(**{**shape, **kw}), abi.OP_BWD)
+            for kw in (dict(act=abi.ACT_RELU), dict(act=abi.ACT_TANH, dtype=abi.FP32),
+                       dict(act=abi.ACT_TANH, KH=3, KW=3, pad=1), dict(act=abi.ACT_TANH, norm=abi.NORM_LAYER))]
+    assert all(0 < f < dconv for f in fused)
+    assert all(k >= dconv for k in kept)
+
+
 def test_null_and_misaligned_pointers_rejected_before_launch():
     d = good(norm=abi.NORM_NONE)
     ws = ctypes.create_string_buffer(1 << 16)

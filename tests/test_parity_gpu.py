@@ -79,6 +79,11 @@ EDGE_CASES = {
     # the same with four stride phases of 1156 rows each (ten m-tiles, the last with 4 rows)
     "bf16_s2_pair_phases": LayerSpec(N=4, H=34, W=34, IC=64, OC=64, KH=3, KW=3, stride=2, pad=1,
                                      norm=NORM_BATCH, act=ACT_RELU, dtype=BF16),
+    # batch-norm backward with d_conv formed inside the dgrad and wgrad producers (1x1, stride 1, bf16,
+    # sigmoid): a ragged pixel count (three 128-row tiles and 45 rows; six 64-pixel k-blocks and 45) and a
+    # weight-gradient column tile half outside the 192 channels
+    "bf16_fused_bwd_sigmoid_ragged": LayerSpec(N=3, H=13, W=11, IC=64, OC=192, KH=1, KW=1, stride=1, pad=0,
+                                               norm=NORM_BATCH, act=ACT_SIGMOID, dtype=BF16),
     # fp32 with KW * IC = 32 and no padding: X through the folded im2col view (each kernel row one
     # 32-float run) in the fprop and the weight gradient, at strides 2 and 1
     "fp32_fold_k8_s2": LayerSpec(N=2, H=20, W=21, IC=4, OC=16, KH=8, KW=8, stride=2, pad=0,
@@ -151,12 +156,13 @@ def test_signed_gamma_relu(dtype, norm):
     assert np.all(ref["y"][..., 3::8] == float(np.float32(0.3))) and np.all(ref["y"][..., 7::8] == 0.0)
 
 
-@pytest.mark.parametrize("dtype", [FP32, BF16])
-def test_accumulate_and_partial_backward(dtype):
+@pytest.mark.parametrize("dtype,k", [(FP32, 3), (BF16, 3), (BF16, 1)])
+def test_accumulate_and_partial_backward(dtype, k):
     """dW/dbias/dgamma/dbeta accumulate into existing values; dx is overwritten;
-    backward_input (params NULL) and backward (dx NULL) variants."""
-    spec = LayerSpec(N=2, H=12, W=12, IC=16, OC=32, KH=3, KW=3, stride=1, pad=1, norm=NORM_BATCH, act=ACT_TANH,
-                     dtype=dtype)
+    backward_input (params NULL) and backward (dx NULL) variants. The bf16 1x1 layer (64 -> 128 channels)
+    takes the backward that forms d_conv inside the GEMM producers."""
+    spec = LayerSpec(N=2, H=12, W=12, IC=16 if k == 3 else 64, OC=32 if k == 3 else 128, KH=k, KW=k, stride=1,
+                     pad=k // 2, norm=NORM_BATCH, act=ACT_TANH, dtype=dtype)
     inp = random_layer_inputs(spec, 11)
     gpu, ref = run_pair(spec, inp, prev_grads=True)
     check_pair(spec, gpu, ref)
