@@ -589,12 +589,15 @@ bool dgrad_col2im(const Geo& g) {
 // Batch-norm backward with d_conv formed inside the dgrad and wgrad producers, never stored: for a 1x1,
 // stride-1 layer without padding d_conv is the dgrad's A operand and the wgrad's B operand as it is (each
 // element read once per GEMM and column tile), so both GEMMs can read the pre-activation and dY tiles in its
-// place and form it in shared memory (dconv_xform). bf16 with whole 64-channel boxes (OC and IC multiples of
-// 64: X by TMA in the wgrad), tanh or sigmoid (the activations whose stand-alone d_conv pass uses the same
-// arithmetic), and a streamed backward reduce (its third partial, sum (x - mean), gives dbias).
+// place and form it on chip (dconv_row into tensor memory for the dgrad, dconv_xform in shared memory for
+// the wgrad). bf16 with whole 64-channel boxes (OC and IC multiples of 64: X by TMA in the wgrad), tanh or
+// sigmoid, a streamed backward reduce (its third partial, sum (x - mean), gives dbias), and a dgrad whose
+// weights stay resident in shared memory beside four 32 KB stages (at most 96 KB) as one column tile that
+// leaves two TMEM accumulators beside the A stages (IC <= 192).
 bool bwd_fused(const Geo& g, const RowWalk& w3) {
   return g.dt == CONV2D_BF16 && g.norm == CONV2D_NORM_BATCH && !g.bn_eval && g.KH == 1 && g.KW == 1 && g.S == 1 &&
-         g.P == 0 && g.OC % 64 == 0 && g.IC % 64 == 0 &&
+         g.P == 0 && g.OC % 64 == 0 && g.IC % 64 == 0 && g.IC <= 192 &&
+         static_cast<long>(g.OC) * g.IC * 2 <= 96 * 1024 &&
          (g.act == CONV2D_ACT_TANH || g.act == CONV2D_ACT_SIGMOID) && w3.stream && w3.cpg == 0;
 }
 
@@ -642,9 +645,9 @@ void plan_ws(const Geo& g, int op, int sms, Plan* pl) {
     if (pl->fused) pl->walk3 = make_walk(g.n_pix, g.OC, g.dt, sms, 1, 0, 2);
     if (!pl->fused) sz[R_DC] = static_cast<size_t>(g.n_pix) * g.OCp * es;
     sz[R_PART] = std::max<size_t>(G, pl->walk3.G) * g.OC * (pl->fused ? 3 : 2) * 4;
-    // channel sums, then per-(image, group) sums; fused: then the per-channel terms of d_conv [6][OC]
+    // channel sums, then per-(image, group) sums; fused: then the per-channel terms of d_conv [4][OC]
     sz[R_C12] = 2 * (static_cast<size_t>(g.OC) + ((ln || gn) ? static_cast<size_t>(g.N) * g.groups : 0)) * 4 +
-                (pl->fused ? 6 * static_cast<size_t>(g.OC) * 4 : 0);
+                (pl->fused ? 4 * static_cast<size_t>(g.OC) * 4 : 0);
     // dgrad weights: every phase's taps together hold each kernel tap once
     const size_t kd = std::max<size_t>(static_cast<size_t>(g.taps) * g.OCp, g.BKE);
     sz[R_WD] = static_cast<size_t>(g.ICp) * kd * es;
@@ -880,7 +883,7 @@ int run_dgrad_merged(const Geo& g, const DevInfo* dev, const void* w, const void
 }
 
 // Operands of a backward with d_conv formed in the GEMM producers (see bwd_fused): the layer's stored
-// pre-activation, dY and the per-channel terms of d_conv [6][OC].
+// pre-activation, dY and the per-channel terms of d_conv [4][OC].
 struct XfSrc {
   const void* pre;
   const void* dy;
@@ -957,11 +960,17 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
     p.a_chunks = g.OCp / g.BKE;
     p.ts = d.ts;
   }
-  if (p.xf)  // a stage: the pre-activation and dY tiles and B, one k-block
-    fit_stages(d.tile, 2 * kBM * 128 + static_cast<size_t>(d.tile.BN) * 128,
-               (12 * static_cast<size_t>(d.tile.BN) + 6 * static_cast<size_t>(g.OC)) * 4, false);
-  else if (bf && p.a_tma)
+  if (p.xf) {
+    // a stage: the pre-activation and dY tiles of one k-block; B resident (one column tile), then the
+    // epilogue scratch and the terms of d_conv
+    if (d.tile.n_tiles != 1 || d.num_phases != 1) return CONV2D_ERR_INVALID_ARG;
+    p.xf_bres = static_cast<uint32_t>(d.ph[0].num_kb * d.tile.BN * 128);
+    fit_stages(d.tile, 2 * kBM * 128,
+               (12 * static_cast<size_t>(d.tile.BN) + 4 * static_cast<size_t>(g.OC)) * 4 + p.xf_bres, false);
+    if (d.tile.stages < 2) return CONV2D_ERR_UNSUPPORTED;
+  } else if (bf && p.a_tma) {
     fit_stages(d.tile, conv_sub_bytes(g, d.tile.BN, false, false), 12 * static_cast<size_t>(d.tile.BN) * 4, true);
+  }
   p.stages = d.tile.stages;
   p.kps = d.tile.kps;
   p.err = dev->err;
@@ -1057,7 +1066,7 @@ int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dc
   if (bf && p.a_tma) {  // k-blocks grouped per stage, each copy covering them all (WgradParams::kps)
     Tile t;
     if (p.xf)  // the X panels, the pre-activation and the dY boxes; one k-block per stage; the terms of d_conv
-      fit_stages(t, kBM * 128 + 2 * static_cast<size_t>(w.BN) * 128, 6 * static_cast<size_t>(g.OC) * 4, false);
+      fit_stages(t, kBM * 128 + 2 * static_cast<size_t>(w.BN) * 128, 4 * static_cast<size_t>(g.OC) * 4, false);
     else
       fit_stages(t, kBM * 128 + static_cast<size_t>(w.BN) * 128, 0, true);
     p.stages = t.stages;
@@ -1359,7 +1368,7 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
                                 st));
     LAUNCH("bn_bwd_finalize", st,
            launch_bn_bwd_fused_finalize(part, pl.walk3, save_mean, save_inv_std, gamma, beta, c12, dbeta, dgamma,
-                                        dbias, c12 + 2 * g.OC, st));
+                                        dbias, c12 + 2 * g.OC, st));  // the terms of d_conv [4][OC] after c12
   } else if (bn) {
     // the reduce walks with three blocks per SM (its own block count; the partials are summed before the
     // d_conv pass reuses the buffer)

@@ -493,10 +493,12 @@ __global__ void __launch_bounds__(128) sum_finalize_kernel(const float* __restri
 
 // Batch norm (training statistics) with d_conv formed inside the GEMM producers: from the backward
 // reduce's partials (sum d_norm, sum d_norm z, sum (x - mean)) per channel, c12 and dbeta / dgamma as in
-// sum_finalize_kernel mode 0, the per-channel terms of d_conv tbl[6][C] = (-mean, inv_std, gamma, beta,
-// -k1, k2) with k1, k2 as norm_bwd_coef forms them, and dbias = sum over pixels of d_conv without the
-// d_conv tensor: sum of inv_std (gamma d_norm - k1 - z k2) = inv_std (gamma sum d_norm - n k1) - inv_std k2
-// sum z, whose first term vanishes by the definition of k1, so dbias += -inv_std^2 k2 sum (x - mean).
+// sum_finalize_kernel mode 0, and:
+//   the terms of d_conv tbl[4][C] = (G, B', Q, S'): with G = gamma inv_std and k1, k2 as norm_bwd_coef
+//   forms them, t = gamma z + beta = G x + B' (B' = beta - G mean) and d_conv = inv_std (gamma d_norm - k1
+//   - z k2) = G d_norm + Q x + S' (Q = -inv_std^2 k2, S' = -inv_std k1 - Q mean); B' and S' in fp64;
+//   dbias = sum over pixels of d_conv without the d_conv tensor: inv_std (gamma sum d_norm - n k1) - inv_std
+//   k2 sum z, whose first term vanishes by the definition of k1, so dbias += -inv_std^2 k2 sum (x - mean).
 __global__ void __launch_bounds__(128) bn_bwd_fused_finalize_kernel(const float* __restrict__ part, int G, int C,
                                                                     long n, const float* __restrict__ mean,
                                                                     const float* __restrict__ inv_std,
@@ -517,14 +519,12 @@ __global__ void __launch_bounds__(128) bn_bwd_fused_finalize_kernel(const float*
     const float ga = gamma[c], is = inv_std[c];
     float k1, k2;
     norm_bwd_coef(c12, 0, 0, c, C, ga, n, k1, k2);
-    tbl[c] = -mean[c];
-    tbl[C + c] = is;
-    tbl[2 * C + c] = ga;
-    tbl[3 * C + c] = beta[c];
-    tbl[4 * C + c] = -k1;
-    tbl[5 * C + c] = k2;
-    if (dbias)
-      dbias[c] += static_cast<float>(-static_cast<double>(is) * static_cast<double>(is) * static_cast<double>(k2) * t[2]);
+    const double g = static_cast<double>(ga) * is, q = -static_cast<double>(is) * is * k2;
+    tbl[c] = static_cast<float>(g);
+    tbl[C + c] = static_cast<float>(beta[c] - g * mean[c]);
+    tbl[2 * C + c] = static_cast<float>(q);
+    tbl[3 * C + c] = static_cast<float>(-static_cast<double>(is) * k1 - q * mean[c]);
+    if (dbias) dbias[c] += static_cast<float>(q * t[2]);
   }
 }
 

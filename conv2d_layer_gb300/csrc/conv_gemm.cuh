@@ -130,10 +130,14 @@ struct ConvGemmParams {
   // Runs of rows at or past out_h, and values of columns at or past out_w, are not written. 0: off.
   int seg, seg_sh, ic_sh, seg_ld, out_h, out_w;
   // bf16 dgrad of a 1x1, stride-1 batch-norm layer with d_conv formed in the A producer (no d_conv tensor):
-  // a k-block's A tile arrives as the stored pre-activation tile (tmap_a[0]) and the dY tile (tmap_a[1]),
-  // 2-D boxes of 64 channels x 128 rows, and warps 2-5 turn the first into d_conv (dconv_xform) before the
-  // MMA reads it. xf_tbl: the per-channel terms [6][xf_C]. One k-block per stage, single CTAs. 0: off.
+  // a stage holds a k-block's pre-activation tile (tmap_a[0]) and dY tile (tmap_a[1]), 2-D boxes of 64
+  // channels x 128 rows; warps 2-9 read them (half a row per thread), release the stage and write d_conv
+  // into a ring of kTaKb TMEM stages (dconv_row_half), from which the MMAs take A; the same warps run the
+  // epilogue one tile behind. B is one column tile, resident in
+  // shared memory behind the ring (xf_bres bytes: one BN x 64 tile per k-block). xf_tbl: the per-channel
+  // terms [4][xf_C]. One k-block per stage, single CTAs. 0: off.
   int xf, xf_C;
+  uint32_t xf_bres;
   const float* xf_tbl;
   int* err;
   ConvPhase ph[kMaxPhases];
@@ -347,19 +351,36 @@ static __device__ __noinline__ void fold_chunks(uint32_t taddr, int stride, int 
   tmem_st_wait();
 }
 
-// d_conv of a batch-norm layer with training statistics, formed in a shared-memory stage from the layer's
-// stored pre-activation x and dY (bf16):
+// d_conv of a batch-norm layer with training statistics from its stored pre-activation x and dY (bf16):
 //   z = (x - mean) inv_std, t = gamma z + beta, d_norm = act'(t) dY,
 //   d_conv = inv_std (gamma d_norm - k1 - z k2),  k1 = gamma sum(d_norm) / n,  k2 = gamma sum(d_norm z) / n,
-// in the operation order of the stand-alone d_conv pass (bf16 layers take the fast activations there too),
-// so that both round to the same bf16 values. The tiles are nbox boxes of NR * RS rows of 64 channels
-// (128-byte swizzle; box b at b * NR * RS * 128 bytes): x at xa, dY at the same offsets from ya; d_conv
-// replaces x. Thread t (of 8 RS) takes 16-byte chunk t & 7 of rows t / 8 + RS i of every box; under the
-// swizzle that chunk holds channels 8 ((t & 7) ^ (t / 8 & 7)) .. + 7 of the box in each of those rows.
-// All NR rows of a box are read before any is computed (one thread per row chunk leaves the arithmetic's
-// latency to the other rows to hide). tbl: per-channel terms [6][C] (-mean, inv_std, gamma, beta, -k1,
-// k2) in shared memory; c0: channel of box 0's first column; channels at or past C take zero terms; rows
-// at or past nvalid (pixels past the layer) are written as zeros.
+// taken per channel as t = G x + B' and d_conv = G d_norm + Q x + S' (G = gamma inv_std, B' = beta - G mean,
+// Q = -inv_std^2 k2, S' = -inv_std k1 - Q mean: bn_bwd_fused_finalize_kernel); bf16 layers take the fast
+// activations, as the stand-alone d_conv pass does. Two channels: the packed bf16 pairs of x and dY in, the
+// packed bf16 pair of d_conv out.
+template <int A>
+__device__ __forceinline__ uint32_t dconv_pair(uint32_t wx, uint32_t wd, float2 G, float2 Bp, float2 Q, float2 Sp) {
+  const float2 x = make_float2(__uint_as_float(wx << 16), __uint_as_float(wx & 0xffff0000u));
+  const float2 dy = make_float2(__uint_as_float(wd << 16), __uint_as_float(wd & 0xffff0000u));
+  const float2 t = __ffma2_rn(G, x, Bp);
+  float2 dn;
+  if constexpr (A == 1) {
+    dn = make_float2(t.x > 0.f ? dy.x : 0.f, t.y > 0.f ? dy.y : 0.f);
+  } else {
+    dn = make_float2(dact_t<A, true>(t.x) * dy.x, dact_t<A, true>(t.y) * dy.y);
+  }
+  const float2 v = __ffma2_rn(G, dn, __ffma2_rn(Q, x, Sp));
+  __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// d_conv formed in a shared-memory stage (see dconv_pair). The tiles are nbox boxes of NR * RS rows of 64
+// channels (128-byte swizzle; box b at b * NR * RS * 128 bytes): x at xa, dY at the same offsets from ya;
+// d_conv replaces x. Thread t (of 8 RS) takes 16-byte chunk t & 7 of rows t / 8 + RS i of every box; under
+// the swizzle that chunk holds channels 8 ((t & 7) ^ (t / 8 & 7)) .. + 7 of the box in each of those rows.
+// All NR rows of a box are read before any is computed. tbl: the terms [4][C] (G, B', Q, S') in shared
+// memory; c0: channel of box 0's first column; channels at or past C take zero terms; rows at or past
+// nvalid (pixels past the layer) are written as zeros.
 template <int A, int NR, int RS>
 __device__ __forceinline__ void dconv_xform(uint32_t xa, uint32_t ya, int nbox, const float* tbl, int C, int c0,
                                             int nvalid, int t) {
@@ -367,9 +388,9 @@ __device__ __forceinline__ void dconv_xform(uint32_t xa, uint32_t ya, int nbox, 
   const int ch = 8 * (pj ^ (r0 & 7));
   for (int b = 0; b < nbox; ++b) {
     const int c = c0 + 64 * b + ch;
-    float k[6][8];
+    float k[4][8];
 #pragma unroll
-    for (int q = 0; q < 6; ++q) {
+    for (int q = 0; q < 4; ++q) {
       float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
       if (c < C) {  // C is a multiple of 8: the thread's eight channels are all inside or all outside
         lo = *reinterpret_cast<const float4*>(tbl + q * C + c);
@@ -394,34 +415,62 @@ __device__ __forceinline__ void dconv_xform(uint32_t xa, uint32_t ya, int nbox, 
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int e = 2 * q;
-        const float2 x = make_float2(__uint_as_float(wx[i][q] << 16), __uint_as_float(wx[i][q] & 0xffff0000u));
-        const float2 dy = make_float2(__uint_as_float(wd[i][q] << 16), __uint_as_float(wd[i][q] & 0xffff0000u));
-        const float2 ga = make_float2(k[2][e], k[2][e + 1]);
-        const float2 z = __fmul2_rn(__fadd2_rn(x, make_float2(k[0][e], k[0][e + 1])), make_float2(k[1][e], k[1][e + 1]));
-        const float2 tt = __ffma2_rn(ga, z, make_float2(k[3][e], k[3][e + 1]));
-        float2 dn;
-        if constexpr (A == 1) {
-          dn = make_float2(tt.x > 0.f ? dy.x : 0.f, tt.y > 0.f ? dy.y : 0.f);
-        } else {
-          dn = make_float2(dact_t<A, true>(tt.x) * dy.x, dact_t<A, true>(tt.y) * dy.y);
-        }
-        const float2 u = __ffma2_rn(ga, dn, make_float2(k[4][e], k[4][e + 1]));
-        const float2 v = __fmul2_rn(make_float2(k[1][e], k[1][e + 1]),
-                                    __ffma2_rn(make_float2(-z.x, -z.y), make_float2(k[5][e], k[5][e + 1]), u));
-        __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
-        o[q] = r0 + RS * i < nvalid ? *reinterpret_cast<uint32_t*>(&h) : 0u;
+        const uint32_t v = dconv_pair<A>(wx[i][q], wd[i][q], make_float2(k[0][e], k[0][e + 1]),
+                                         make_float2(k[1][e], k[1][e + 1]), make_float2(k[2][e], k[2][e + 1]),
+                                         make_float2(k[3][e], k[3][e + 1]));
+        o[q] = r0 + RS * i < nvalid ? v : 0u;
       }
       st_shared_v4(xa + bo + static_cast<uint32_t>(i * RS * 128), o[0], o[1], o[2], o[3]);
     }
   }
 }
 
-// The per-channel terms of d_conv [6][C] (C a multiple of 8) copied into shared memory by the 256 threads
-// of warps 2-9, which then pass named barrier 2 together.
-__device__ __forceinline__ void load_xform_terms(float* dst, const float* __restrict__ src, int C, int t) {
-  for (int i = 4 * t; i < 6 * C; i += 4 * 256)
+// d_conv of one half row of a 128-row x 64-channel stage (the calling thread's row r, its TMEM lane, and
+// channels 32 H .. 32 H + 31) from the pre-activation tile at xa and the dY tile at ya (128-byte swizzle):
+// dconv_row_load reads the half row's four 16-byte chunks of both (logical chunk cc at physical chunk
+// cc ^ (r & 7)); dconv_row_half forms them as the 16 packed bf16 pairs of an A operand in tensor memory
+// (column c = channels 2c, 2c + 1). tbl: the terms [4][C]; c0: channel of the tile's first column;
+// zero = the row is past the layer (written as zeros).
+__device__ __forceinline__ void dconv_row_load(uint32_t xa, uint32_t ya, int r, int H, uint32_t (&wx)[4][4],
+                                               uint32_t (&wd)[4][4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int cc = 4 * H + i;
+    const uint32_t off = static_cast<uint32_t>(r * 128 + ((cc ^ (r & 7)) << 4));
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(wx[i][0]), "=r"(wx[i][1]), "=r"(wx[i][2]), "=r"(wx[i][3]) : "r"(xa + off));
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(wd[i][0]), "=r"(wd[i][1]), "=r"(wd[i][2]), "=r"(wd[i][3]) : "r"(ya + off));
+  }
+}
+template <int A>
+__device__ __forceinline__ void dconv_row_half(const uint32_t (&wx)[4][4], const uint32_t (&wd)[4][4], int H,
+                                               const float* tbl, int C, int c0, bool zero, uint32_t (&o)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float* k = tbl + c0 + 8 * (4 * H + i);  // the same channels in every lane: broadcast reads
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float4 g = *reinterpret_cast<const float4*>(k + 4 * h);
+      const float4 bp = *reinterpret_cast<const float4*>(k + C + 4 * h);
+      const float4 qq = *reinterpret_cast<const float4*>(k + 2 * C + 4 * h);
+      const float4 sp = *reinterpret_cast<const float4*>(k + 3 * C + 4 * h);
+      const uint32_t v0 = dconv_pair<A>(wx[i][2 * h], wd[i][2 * h], make_float2(g.x, g.y), make_float2(bp.x, bp.y),
+                                        make_float2(qq.x, qq.y), make_float2(sp.x, sp.y));
+      const uint32_t v1 = dconv_pair<A>(wx[i][2 * h + 1], wd[i][2 * h + 1], make_float2(g.z, g.w),
+                                        make_float2(bp.z, bp.w), make_float2(qq.z, qq.w), make_float2(sp.z, sp.w));
+      o[4 * i + 2 * h] = zero ? 0u : v0;
+      o[4 * i + 2 * h + 1] = zero ? 0u : v1;
+    }
+  }
+}
+
+// The per-channel terms of d_conv [4][C] (C a multiple of 8) copied into shared memory by the nthr threads
+// of the transforming warps, which then pass named barrier 2 together.
+__device__ __forceinline__ void load_xform_terms(float* dst, const float* __restrict__ src, int C, int t, int nthr) {
+  for (int i = 4 * t; i < 4 * C; i += 4 * nthr)
     *reinterpret_cast<float4*>(dst + i) = __ldg(reinterpret_cast<const float4*>(src + i));
-  named_bar_sync(2, 256);
+  named_bar_sync(2, nthr);
 }
 
 template <typename T>
@@ -540,20 +589,21 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
   const uint32_t b_own = pair ? b_bytes / 2 : b_bytes;
   // fp32 with A in TMEM (see ConvGemmParams::ts): a stage holds the raw A tile, B hi and B lo
   const bool ts = DT == 0 && p.ts;
-  // d_conv formed from the pre-activation and dY tiles (see ConvGemmParams::xf)
+  // d_conv formed from the pre-activation and dY tiles into tensor memory (see ConvGemmParams::xf): a
+  // stage holds those two tiles only, and B is resident behind the ring
   const bool xf = DT == 1 && !PAIR && p.xf;
-  // A tiles per k-block (fp32 in shared memory: hi, lo; xf: pre-activation, dY)
-  const uint32_t a_tiles = ((DT == 0 && !ts) || xf) ? 2u : 1u;
+  const uint32_t a_tiles = (DT == 0 && !ts) ? 2u : 1u;  // A tiles per k-block (fp32 in shared memory: hi, lo)
   const int KPS = p.kps > 1 ? p.kps : 1;                // k-blocks per stage
-  const uint32_t sub_bytes = a_tiles * a_bytes + D::NS * b_own;  // one k-block of a stage
+  const uint32_t sub_bytes = xf ? 2 * a_bytes : a_tiles * a_bytes + D::NS * b_own;  // one k-block of a stage
   const uint32_t stage_bytes = KPS * sub_bytes;
   const int S = p.stages;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_bytes + (xf ? p.xf_bres : 0u));
   uint64_t* empty = full + kMaxStages;
   uint64_t* tfull = empty + kMaxStages;
   uint64_t* tempty = tfull + kMaxTmemBufs;
   uint64_t* sfull = tempty + kMaxTmemBufs;  // fp32 with A by TMA: the stage is split into hi / lo
-  uint64_t* aempty = sfull + kMaxStages;    // fp32 with A in TMEM: the MMAs have read a TMEM stage of A
+  uint64_t* aempty = sfull + kMaxStages;    // A in TMEM: the MMAs have read a TMEM stage of A
+  uint64_t* bfull = &sfull[kMaxStages - 1];  // xf: the resident B tiles have landed (TA < kMaxStages - 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aempty + kMaxStages);
   const uint32_t sbase = smem_u32(smem);
   // fp32 with A by TMA: warps 2-5 split the stages (and the epilogue keeps four warps)
@@ -573,10 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
   const int kpc = DT == 0 && p.nch > 1 ? p.kpc : (1 << 30);
   const int ccols = ts ? 2 * BN : BN;  // TMEM columns of one accumulator chunk
   const int tcs = nch * ccols;         // TMEM columns of one tile
-  // with A in TMEM the last kTaKb * 64 columns hold TA stages of KPS k-blocks of A (per k-block hi: 32
-  // columns, then lo: 32)
+  // with A in TMEM the last columns hold TA stages of KPS k-blocks of A (fp32: per k-block hi, 32 columns,
+  // then lo, 32; xf: 32 columns of packed bf16 pairs per k-block)
   const int TA = kTaKb / KPS;
-  const int ta_cols = ts ? kTaKb * 64 : 0;
+  const int ta_cols = ts ? kTaKb * 64 : (xf ? kTaKb * 32 : 0);
   const int nbuf = (512 - ta_cols) / tcs < kMaxTmemBufs ? (512 - ta_cols) / tcs : kMaxTmemBufs;
   const uint32_t tcols = tmem_cols_for(nbuf * tcs + ta_cols);
   const uint32_t ta0 = static_cast<uint32_t>(nbuf * tcs);  // first TMEM column of the A stages
@@ -584,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], p.a_tma ? 1 : 4 + 1);  // the TMA thread (+ one arrival per producer warp)
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], xf ? 8 : 1);          // the MMA's commit (xf: one arrival per transforming warp)
     }
     for (int b = 0; b < nbuf; ++b) {
       mbar_init(&tfull[b], 1);
@@ -592,9 +642,10 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       mbar_init(&tempty[b], ((ep8 || xf) ? 8 : 4) * (pair ? 2 : 1));
     }
     if (split_a || xf)  // with A in TMEM indexed by TMEM stage; one arrival per splitting / transforming warp
-      for (int s = 0; s < (ts ? TA : S); ++s) mbar_init(&sfull[s], xf ? 8 : 4);
-    if (ts)
+      for (int s = 0; s < ((ts || xf) ? TA : S); ++s) mbar_init(&sfull[s], xf ? 8 : 4);
+    if (ts || xf)
       for (int j = 0; j < TA; ++j) mbar_init(&aempty[j], 1);  // the MMA warp's commit
+    if (xf) mbar_init(bfull, 1);
     fence_mbar_init();
     tma_prefetch_desc(&p.tmap_b);
     if (p.a_tma)
@@ -618,7 +669,34 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
 
   if (warp == 0) {
     // ------------------------------------------------ B producer (TMA)
-    if (lane == 0) {
+    if (lane == 0 && xf) {
+      // the resident B tiles once (one column tile), then the pre-activation and dY tiles of every k-block
+      const uint32_t bres = sbase + S * stage_bytes;  // the resident B tiles, one per k-block
+      const ConvPhase& ph0 = p.ph[0];
+      mbar_arrive_expect_tx(bfull, p.xf_bres);
+      for (int kb = 0; kb < ph0.num_kb; ++kb) tma_load_2d(bres + kb * b_bytes, &p.tmap_b, bfull, ph0.b_col + kb * D::BKE, 0);
+      int s = 0;
+      uint32_t par = 0;
+      bool alive = true;
+      for (int u = cid; u < p.num_units && alive; u += ncl) {
+        const ConvPhase& ph = find_phase(p, u);
+        const int row0 = ((u - ph.unit_begin) / p.n_tiles) * kBM;
+        for (int kb = 0; kb < ph.num_kb; ++kb) {
+          if (!wait(&empty[s], par ^ 1, p.err, kSiteEmpty)) {
+            alive = false;
+            break;
+          }
+          const uint32_t a0 = sbase + s * stage_bytes;
+          mbar_arrive_expect_tx(&full[s], 2 * a_bytes);
+          tma_load_2d(a0, &p.tmap_a[0], &full[s], kb * D::BKE, row0);
+          tma_load_2d(a0 + a_bytes, &p.tmap_a[1], &full[s], kb * D::BKE, row0);
+          if (++s == S) {
+            s = 0;
+            par ^= 1;
+          }
+        }
+      }
+    } else if (lane == 0) {
       int s = 0;
       uint32_t par = 0;
       bool alive = true;
@@ -627,8 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         const int local = u - ph.unit_begin;
         const int n_tile = local % p.n_tiles;
         int an = 0, ah = 0, aw = 0;  // window corner of the tile's first row (TMA im2col)
-        const int xrow = xf ? (local / p.n_tiles) * kBM : 0;  // xf: first row of the tile
-        if (p.a_tma && !xf) {
+        if (p.a_tma) {
           const int m_tile = pair ? 2 * (local / p.n_tiles) + static_cast<int>(rank) : local / p.n_tiles;
           const int m0 = m_tile * kBM;
           an = static_cast<int>(fdiv(static_cast<uint32_t>(m0), ph.div_HaWa));
@@ -651,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           if (pair) {
             if (leader) mbar_arrive_expect_tx(&full[s], 2u * nk * (a_bytes + b_own));
           } else {
-            mbar_arrive_expect_tx(&full[s], nk * (D::NS * b_bytes + (p.a_tma ? (xf ? 2u : 1u) * a_bytes : 0u)));
+            mbar_arrive_expect_tx(&full[s], nk * (D::NS * b_bytes + (p.a_tma ? a_bytes : 0u)));
           }
 #pragma unroll
           for (int i = 0; i < kMaxKps; ++i) {
@@ -664,13 +741,9 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
                                       static_cast<uint16_t>(tt));
               tma_load_2d_pair(b0, &p.tmap_b, bar, kcol, n_tile * BN + static_cast<int>(rank) * (BN / 2));
             } else {
-              if (xf) {  // the pre-activation and dY tiles of k-block g0 + i (64 channels each)
-                tma_load_2d(a0, &p.tmap_a[0], &full[s], (g0 + i) * D::BKE, xrow);
-                tma_load_2d(a0 + a_bytes, &p.tmap_a[1], &full[s], (g0 + i) * D::BKE, xrow);
-              } else if (p.a_tma) {
+              if (p.a_tma)
                 tma_load_im2col_4d(a0, &p.tmap_a[ph.a_map], &full[s], ck * D::BKE, aw, ah, an,
                                    static_cast<uint16_t>(tw), static_cast<uint16_t>(tt));
-              }
               if (D::NS == 2) tma_load_3d(b0, &p.tmap_b, &full[s], kcol, n_tile * BN, 0);  // hi and lo rows
               else tma_load_2d(b0, &p.tmap_b, &full[s], kcol, n_tile * BN);
             }
@@ -702,7 +775,38 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
-    if (lane == 0 && leader) {
+    if (lane == 0 && xf) {
+      // A (d_conv) from the TMEM stages the transforming warps fill, B from the resident tiles
+      const uint32_t bres = sbase + S * stage_bytes;
+      const uint32_t idesc = idesc_f32acc(kBM, BN, D::FMT, false, false);
+      int j = 0, tc = 0;
+      uint32_t apar = 0;
+      bool alive = wait(bfull, 0, p.err, kSiteFull);
+      for (int u = cid; u < p.num_units && alive; u += ncl, ++tc) {
+        const ConvPhase& ph = find_phase(p, u);
+        const int buf = tc % nbuf;
+        if (!wait(&tempty[buf], ((tc / nbuf) & 1) ^ 1, p.err, kSiteTEmpty)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * tcs;
+        for (int kb = 0; kb < ph.num_kb; ++kb) {
+          if (!wait(&sfull[j], apar, p.err, kSiteFull)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = tmem_base + ta0 + static_cast<uint32_t>(j * 32);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ta(d, a + kk * 8, sdesc_sw128(bres + kb * b_bytes + kk * 32, 16, 1024), idesc, (kb | kk) ? 1u : 0u);
+          mma_commit(&aempty[j]);
+          if (++j == TA) {
+            j = 0;
+            apar ^= 1;
+          }
+        }
+        if (alive) mma_commit(&tfull[buf]);
+      }
+    } else if (lane == 0 && leader) {
       const uint32_t idesc = idesc_f32acc(pair ? 2 * kBM : kBM, BN, D::FMT, false, false);
       const uint32_t idesc2 = idesc_f32acc(kBM, 2 * BN, D::FMT, false, false);  // A_hi x [B_hi; B_lo]
       int s = 0, j = 0;
@@ -719,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           const int nk = min(KPS, ph.num_kb - g0);
           // with A in TMEM the split warps arrive on the TMEM stage's barrier after the shared-memory stage
           // has landed, so that one wait covers both
-          if (!wait(ts ? &sfull[j] : ((split_a || xf) ? &sfull[s] : &full[s]), ts ? apar : par, p.err, kSiteFull)) {
+          if (!wait(ts ? &sfull[j] : (split_a ? &sfull[s] : &full[s]), ts ? apar : par, p.err, kSiteFull)) {
             alive = false;
             break;
           }
@@ -989,16 +1093,20 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       }
     }
   } else if (xf) {
-    // ------------------------------------------------ d_conv from the pre-activation and dY tiles, and the epilogue
-    // Warps 2-9 turn each landed stage's pre-activation tile into d_conv (four rows per thread; the MMA waits
-    // for sfull); after a tile's k-blocks they store the tile before it (its accumulator completed meanwhile):
-    // two warps per TMEM lane quarter, one per column half. The terms of d_conv follow the epilogue scratch.
-    const int t = threadIdx.x - 64;
+    // ------------------------------------------------ d_conv into TMEM, and the epilogue
+    // Warps w and w + 4 (w = 2..5) own TMEM lane quarter w & 3, i.e. rows 32 (w & 3) .. + 31 of a tile, and
+    // channel half h = (w - 2) / 4 of each k-block: each thread reads its half row of both tiles, releases
+    // the stage to the producer, and writes 16 columns of packed bf16 pairs of d_conv into TMEM stage j once
+    // the MMAs of its previous use have completed. After a tile's k-blocks the eight warps store the tile
+    // before it (its accumulator completed meanwhile), each its lane quarter and column half. The terms of
+    // d_conv follow the epilogue scratch.
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int r = q * 32 + lane;
     float* tbl = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16) + 12 * BN;
-    load_xform_terms(tbl, p.xf_tbl, p.xf_C, t);
-    const int q = warp & 3, half = (warp - 2) >> 2;
+    load_xform_terms(tbl, p.xf_tbl, p.xf_C, threadIdx.x - 64, 256);
+    const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ta0 + 16 * h;
     const int hcols = 32 * ((BN / 32 + 1) / 2);
-    const int cb = half * hcols, ce = half ? BN : hcols;
+    const int cb = h * hcols, ce = h ? BN : hcols;
     const bool vec = (p.out_ld % D::EC) == 0;
     // store tile u (the tc-th of this CTA): a 1x1, stride-1 dgrad writes row m of D to dX pixel m
     auto epilogue = [&](int u, int tc) -> bool {
@@ -1010,7 +1118,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       if (lane == 0) ok = wait(&tfull[buf], (tc / nbuf) & 1, p.err, kSiteTFull) ? 1 : 0;
       if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
       tc_fence_after();
-      const int m = m_tile * kBM + q * 32 + lane;
+      const int m = m_tile * kBM + r;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * tcs;
       T* out = static_cast<T*>(p.out) + static_cast<size_t>(m) * p.out_ld;
       for (int c0 = cb; c0 < ce; c0 += 64) {  // 64 columns per wait (two 32-column loads)
@@ -1035,27 +1143,41 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       if (lane == 0) mbar_arrive(&tempty[buf]);
       return true;
     };
-    int s = 0;
-    uint32_t par = 0;
+    int s = 0, j = 0;
+    uint32_t par = 0, apar = 0;
     bool alive = true;
     int prev = -1, tc = 0;
     for (int u = cid; u < p.num_units && alive; u += ncl, ++tc) {
       const ConvPhase& ph = find_phase(p, u);
-      const int m0 = ((u - ph.unit_begin) / p.n_tiles) * kBM;
+      const bool past = ((u - ph.unit_begin) / p.n_tiles) * kBM + r >= ph.rows;
       for (int kb = 0; kb < ph.num_kb; ++kb) {
-        if (!__all_sync(0xffffffffu, wait(&full[s], par, p.err, kSiteFull))) {  // warp-uniform
+        // the stage has landed, and the MMAs that read TMEM stage j before have completed (they run ahead
+        // of the copies, so that wait rarely waits)
+        const bool ok = wait(&full[s], par, p.err, kSiteFull) && wait(&aempty[j], apar ^ 1, p.err, kSiteEmpty);
+        if (!__all_sync(0xffffffffu, ok)) {  // warp-uniform
           alive = false;
           break;
         }
+        tc_fence_after();
         const uint32_t a0 = sbase + s * stage_bytes;
-        if (p.act == 3) dconv_xform<3, kBM / 32, 32>(a0, a0 + a_bytes, 1, tbl, p.xf_C, kb * D::BKE, ph.rows - m0, t);
-        else dconv_xform<2, kBM / 32, 32>(a0, a0 + a_bytes, 1, tbl, p.xf_C, kb * D::BKE, ph.rows - m0, t);
-        fence_proxy_async_smem();
+        uint32_t wx[4][4], wd[4][4], o[16];
+        dconv_row_load(a0, a0 + a_bytes, r, h, wx, wd);
+        if (p.act == 3) dconv_row_half<3>(wx, wd, h, tbl, p.xf_C, kb * D::BKE, past, o);
+        else dconv_row_half<2>(wx, wd, h, tbl, p.xf_C, kb * D::BKE, past, o);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sfull[s]);
+        if (lane == 0) mbar_arrive(&empty[s]);  // ordered after this warp's reads of the stage (release)
+        tmem_st16(tq + static_cast<uint32_t>(j * 32), o);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[j]);
         if (++s == S) {
           s = 0;
           par ^= 1;
+        }
+        if (++j == TA) {
+          j = 0;
+          apar ^= 1;
         }
       }
       if (alive && prev >= 0 && !epilogue(prev, tc - 1)) alive = false;
@@ -1602,7 +1724,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
     // the TMEM slot.
     const int t = threadIdx.x - 64;
     float* tbl = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16);
-    load_xform_terms(tbl, p.xf_tbl, p.xf_C, t);
+    load_xform_terms(tbl, p.xf_tbl, p.xf_C, t, 256);
     const int q = warp & 3, half = (warp - 2) >> 2;
     const int hcols = 32 * ((BN / 32 + 1) / 2);
     const int cb = half * hcols, ce = half ? BN : hcols;

@@ -95,8 +95,8 @@ cudaError_t launch_bn_bwd_reduce(int dtype, const void* pre, const void* dy, con
 cudaError_t launch_sum_finalize(const float* part, const RowWalk& wk, int nv, int mode, float* c12, float* acc0,
                                 float* acc1, cudaStream_t st);
 // Batch norm with d_conv formed inside the GEMM producers: from the nv = 3 reduce partials, c12, dbeta,
-// dgamma, dbias (each accumulated where non-null) and the per-channel terms tbl[6][C] of d_conv
-// (-mean, inv_std, gamma, beta, -k1, k2).
+// dgamma, dbias (each accumulated where non-null) and the per-channel terms tbl[4][C] of d_conv
+// (G, B', Q, S': t = G x + B', d_conv = G d_norm + Q x + S').
 cudaError_t launch_bn_bwd_fused_finalize(const float* part, const RowWalk& wk, const float* mean,
                                          const float* inv_std, const float* gamma, const float* beta, float* c12,
                                          float* dbeta, float* dgamma, float* dbias, float* tbl, cudaStream_t st);

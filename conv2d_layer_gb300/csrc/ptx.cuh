@@ -250,6 +250,16 @@ __device__ __forceinline__ void mma_tf32_ta(uint32_t d, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+// bf16 (kind::f16) with the A operand in tensor memory: lane = row of A, one 32-bit column per two k
+// elements (k = 2c in the low half, 2c + 1 in the high half), the k-step's eight columns starting at
+// a_tmem; B from shared memory.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
 // M = 256 over a CTA pair (issued by the even CTA): A rows 0-127 / 128-255 and the two halves of B's
 // columns come from the two CTAs' shared memory at the same offsets; D lands in both CTAs' TMEM.
 __device__ __forceinline__ void mma_bf16_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
