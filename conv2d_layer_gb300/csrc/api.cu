@@ -459,10 +459,15 @@ WgradPlan wgrad_plan(const Geo& g, int sms, bool fused) {
   const double flops_kb = 2.0 * kBM * w.BN * w.KP * (bf ? 1.0 : 6.0);
   const double t_kb = flops_kb / (2.25e15 / 152.0);
   const double t_split = static_cast<double>(base) * kBM * w.BN * 8.0 / 6.8e12;
-  int best = 1;
+  // 3xTF32: the tensor core's fp32 accumulation is not round-to-nearest, and its error grows with the
+  // number of accumulations into one TMEM accumulator; a split holds at most 32 k-blocks (1024 pixels),
+  // and the splits are summed in fp64. The search starts there, so that the wave balance is chosen among
+  // the allowed counts.
+  const int smin = bf ? 1 : static_cast<int>(ceil_div(w.kb_total, 32));
+  int best = smin;
   double best_t = 1e30;
-  const int smax = std::max(1, std::min(w.kb_total, 16 * sms));
-  for (int s = 1; s <= smax; ++s) {
+  const int smax = std::max(smin, std::min(w.kb_total, 16 * sms));
+  for (int s = smin; s <= smax; ++s) {
     const int kbp = static_cast<int>(ceil_div(w.kb_total, s));
     const int s_eff = static_cast<int>(ceil_div(w.kb_total, kbp));
     if (s_eff != s) continue;
@@ -475,10 +480,6 @@ WgradPlan wgrad_plan(const Geo& g, int sms, bool fused) {
     }
   }
   w.splits = best;
-  // 3xTF32: the tensor core's fp32 accumulation is not round-to-nearest, and its error grows with the
-  // number of accumulations into one TMEM accumulator; cap a split at 32 k-blocks (1024 pixels), the
-  // splits are then summed in fp64
-  if (!bf) w.splits = std::max(w.splits, static_cast<int>(ceil_div(w.kb_total, 32)));
   w.kb_per_split = static_cast<int>(ceil_div(w.kb_total, w.splits));
   w.splits = static_cast<int>(ceil_div(w.kb_total, w.kb_per_split));
   w.units = base * w.splits;
@@ -964,9 +965,9 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
     // a stage: the pre-activation and dY tiles of one k-block; B resident (one column tile), then the
     // epilogue scratch and the terms of d_conv
     if (d.tile.n_tiles != 1 || d.num_phases != 1) return CONV2D_ERR_INVALID_ARG;
-    p.xf_bres = static_cast<uint32_t>(d.ph[0].num_kb * d.tile.BN * 128);
+    p.bres = static_cast<uint32_t>(d.ph[0].num_kb * d.tile.BN * 128);
     fit_stages(d.tile, 2 * kBM * 128,
-               (12 * static_cast<size_t>(d.tile.BN) + 4 * static_cast<size_t>(g.OC)) * 4 + p.xf_bres, false);
+               (12 * static_cast<size_t>(d.tile.BN) + 4 * static_cast<size_t>(g.OC)) * 4 + p.bres, false);
     if (d.tile.stages < 2) return CONV2D_ERR_UNSUPPORTED;
   } else if (bf && p.a_tma) {
     fit_stages(d.tile, conv_sub_bytes(g, d.tile.BN, false, false), 12 * static_cast<size_t>(d.tile.BN) * 4, true);

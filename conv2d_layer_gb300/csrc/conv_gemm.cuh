@@ -133,12 +133,12 @@ struct ConvGemmParams {
   // a stage holds a k-block's pre-activation tile (tmap_a[0]) and dY tile (tmap_a[1]), 2-D boxes of 64
   // channels x 128 rows; warps 2-9 read them (half a row per thread), release the stage and write d_conv
   // into a ring of kTaKb TMEM stages (dconv_row_half), from which the MMAs take A; the same warps run the
-  // epilogue one tile behind. B is one column tile, resident in
-  // shared memory behind the ring (xf_bres bytes: one BN x 64 tile per k-block). xf_tbl: the per-channel
-  // terms [4][xf_C]. One k-block per stage, single CTAs. 0: off.
+  // epilogue one tile behind. B is resident (bres). xf_tbl: the per-channel terms [4][xf_C]. One k-block per
+  // stage, single CTAs. 0: off.
   int xf, xf_C;
-  uint32_t xf_bres;
   const float* xf_tbl;
+  // xf: the weights resident in shared memory behind the ring, bres bytes (one BN x 64 tile per k-block)
+  uint32_t bres;
   int* err;
   ConvPhase ph[kMaxPhases];
 };
@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
   const uint32_t sub_bytes = xf ? 2 * a_bytes : a_tiles * a_bytes + D::NS * b_own;  // one k-block of a stage
   const uint32_t stage_bytes = KPS * sub_bytes;
   const int S = p.stages;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_bytes + (xf ? p.xf_bres : 0u));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_bytes + (xf ? p.bres : 0u));
   uint64_t* empty = full + kMaxStages;
   uint64_t* tfull = empty + kMaxStages;
   uint64_t* tempty = tfull + kMaxTmemBufs;
@@ -673,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       // the resident B tiles once (one column tile), then the pre-activation and dY tiles of every k-block
       const uint32_t bres = sbase + S * stage_bytes;  // the resident B tiles, one per k-block
       const ConvPhase& ph0 = p.ph[0];
-      mbar_arrive_expect_tx(bfull, p.xf_bres);
+      mbar_arrive_expect_tx(bfull, p.bres);
       for (int kb = 0; kb < ph0.num_kb; ++kb) tma_load_2d(bres + kb * b_bytes, &p.tmap_b, bfull, ph0.b_col + kb * D::BKE, 0);
       int s = 0;
       uint32_t par = 0;
@@ -1276,7 +1276,11 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
       float rmean = 0.f, rm2 = 0.f;
       const bool zero = ph.num_kb == 0;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * tcs;
-      if (ts && !zero)  // each chunk's two halves (hi x hi + lo x hi, then hi x lo), summed into the first
+      // A in TMEM: each chunk's two halves (hi x hi + lo x hi, then hi x lo). One chunk and no statistics
+      // pass (which reads the accumulator again): the halves are added in registers below; else they are
+      // summed into the first block in TMEM
+      const bool ts_sum = ts && !zero && !p.stats && ph.num_kb <= kpc;
+      if (ts && !zero && !ts_sum)
         fold_chunks(taddr, BN, 2 * ((ph.num_kb + kpc - 1) / kpc), cb, ce);
       else if (DT == 0 && ph.num_kb > kpc)  // several accumulator chunks: summed into the first
         fold_chunks(taddr, BN, (ph.num_kb + kpc - 1) / kpc, cb, ce);
@@ -1327,11 +1331,20 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           }
         }
       };
-      for (int c0 = cb; c0 < ce; c0 += 64) {
+      // 64 columns per step (32 with ts_sum: columns c0 .. c0 + 31 of both halves, added)
+      for (int c0 = cb; c0 < ce; c0 += ts_sum ? 32 : 64) {
         uint32_t ra[32], rb[32];
-        fetch(c0, ra, rb);
+        if (ts_sum) {
+          tmem_ld32(taddr + c0, ra);
+          tmem_ld32(taddr + static_cast<uint32_t>(BN + c0), rb);
+          tmem_ld_wait2(ra, rb);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ra[e] = __float_as_uint(__uint_as_float(ra[e]) + __uint_as_float(rb[e]));
+        } else {
+          fetch(c0, ra, rb);
+        }
         pass1(c0, ra);
-        if (c0 + 32 < ce) pass1(c0 + 32, rb);
+        if (!ts_sum && c0 + 32 < ce) pass1(c0 + 32, rb);
       }
       if (p.rstats && valid) {
         const int nh = ep8 ? 2 : 1;
