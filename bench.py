@@ -32,7 +32,7 @@ NOMINAL_BF16_TFLOPS = 2250.0
 # DRAM bytes (read + write) per launch of the GEMM kernels on the 256-image layer, from the ncu capture
 # summarised in profiles/large_step_kernels.md (96-image case, scaled by 256/96). Reset to None whenever
 # a GEMM kernel changes and re-capture.
-NCU_TRAFFIC_BYTES = {"fprop_gemm": 694e6, "dgrad_gemm": 687e6, "wgrad_gemm": 823e6}
+NCU_TRAFFIC_BYTES = {"fprop_gemm": 692e6, "dgrad_gemm": 685e6, "wgrad_gemm": 822e6}
 
 
 def _peaks():
@@ -391,6 +391,14 @@ def per_config_timing(peaks, steps=10, warmup=3):
         ms_graph = e0.elapsed_time(e1) / steps
         del graph
         abi.conv2d_prof_enable(True)
+        # the launches of each ABI call of the step (a stack's layers launch different kernels: the layer of
+        # every launch below comes from these counts)
+        owner = []
+        for li, call in step.calls():
+            abi.conv2d_prof_read()
+            call()
+            torch.cuda.synchronize()
+            owner += [li] * len(abi.conv2d_prof_read(4096))
         abi.conv2d_prof_read()
         # the GPU idles in a ~2 ms sleep kernel while the host queues the whole step, so that the per-launch
         # events bracket back-to-back kernels (not the host's launch work between short kernels)
@@ -398,15 +406,21 @@ def per_config_timing(peaks, steps=10, warmup=3):
         step()
         torch.cuda.synchronize()
         abi.conv2d_prof_enable(False)
+        recs = abi.conv2d_prof_read(4096)
         kern = {}
-        for kname, t in abi.conv2d_prof_read(4096):
+        for kname, t in recs:
             kern[kname] = kern.get(kname, 0.0) + t
         fl = sum(s.flops_step() for s in specs)
-        # a layer's output tensor; over a stack (every layer with the same norm and activation) the
-        # algorithmic bytes and the kernel times are both summed over the layers
-        tensor_bytes = sum(s.n_pix * s.OC * (2 if s.dtype == 1 else 4) for s in specs)
-        hbm = {k: round(HBM_TENSORS[k] * tensor_bytes / (t * 1e-3) / 1e9 / peaks["hbm"], 3)
-               for k, t in kern.items() if k in HBM_TENSORS}
+        # algorithmic bytes of each bandwidth-bound launch from its own layer's output tensor, summed with
+        # the times over the launches of the same kernel
+        hb, ht = {}, {}
+        if len(owner) == len(recs):
+            for (kname, t), li in zip(recs, owner):
+                if kname in HBM_TENSORS:
+                    sp = specs[li]
+                    hb[kname] = hb.get(kname, 0.0) + HBM_TENSORS[kname] * sp.n_pix * sp.OC * (2 if sp.dtype == 1 else 4)
+                    ht[kname] = ht.get(kname, 0.0) + t
+        hbm = {k: round(hb[k] / (ht[k] * 1e-3) / 1e9 / peaks["hbm"], 3) for k in hb}
         bf = specs[0].dtype == 1
         # the tensor-core bound of the contractions: bf16 burst, or a third of the measured TF32 rate for
         # 3xTF32; GEMM kernels (the column-form dgrad's GEMM is a launch named fprop_gemm)
@@ -444,15 +458,26 @@ def config_step(name, over):
                         for s, li in zip(specs, inp["layers"])],
              "x": inp["x"].cuda(), "dy": inp["dy"].cuda()}
 
-    def step():
+    def calls():
+        """The step's ABI calls in order, as (layer index, call): every layer's fwd_train, then every
+        layer's bwd from the last layer back."""
         layers = state["layers"]
         acts = [state["x"]]
-        for L in layers:
-            acts.append(L.fwd_train(acts[-1]))
-        g = state["dy"]
-        for L, a in zip(reversed(layers), reversed(acts[:-1])):
-            g = L.bwd(a, g)
+        g = [state["dy"]]
+        seq = []
+        for i, L in enumerate(layers):
+            seq.append((i, lambda i=i, L=L: acts.append(L.fwd_train(acts[i]))))
+        for i in reversed(range(len(layers))):
+            def b(i=i):
+                g[0] = layers[i].bwd(acts[i], g[0])
+            seq.append((i, b))
+        return seq
 
+    def step():
+        for _, call in calls():
+            call()
+
+    step.calls = calls
     return specs, step, state.clear
 
 
@@ -660,7 +685,7 @@ def main():
                               "peaks": peaks["src"]},
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": d["achieved"], "peak": peaks["bf16"],
                      "unit": "TFLOP/s", "frac": d["frac"],
-                     "traffic": NCU_TRAFFIC_BYTES.get(dom) if spec.N == 256 else None,
+                     "traffic": (NCU_TRAFFIC_BYTES or {}).get(dom) if spec.N == 256 else None,
                      "peak_kind": "bf16 burst (%s): the kernel is timed with CUDA events inside a region of "
                                   "about 50 ms, not a seconds-long loop" % peaks["src"]},
         "kernels": kern,
