@@ -544,8 +544,17 @@ __device__ __forceinline__ void store_phase_runs(T* out, size_t obase, int h0, i
   }
 }
 
+// 32 bytes to global memory in one store (the address 32-byte aligned): a whole sector per lane
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// 32 values of a row to T at dst: 16-byte stores (vec: dst 16-byte aligned), for bf16 32-byte ones (vec32:
+// dst 32-byte aligned), else one value at a time; columns at or past ncols are not written.
 template <typename T>
-__device__ __forceinline__ void store_row32(T* dst, const float (&v)[32], int ncols, bool vec) {
+__device__ __forceinline__ void store_row32(T* dst, const float (&v)[32], int ncols, bool vec, bool vec32 = false) {
   if (vec && ncols >= 32) {
     if constexpr (sizeof(T) == 2) {
       uint32_t w[16];
@@ -554,9 +563,14 @@ __device__ __forceinline__ void store_row32(T* dst, const float (&v)[32], int nc
         __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
         w[e] = *reinterpret_cast<uint32_t*>(&h);
       }
+      if (vec32) {
+        st_global_v8(dst, w);
+        st_global_v8(dst + 16, w + 8);
+      } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        reinterpret_cast<uint4*>(dst)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        for (int e = 0; e < 4; ++e)
+          reinterpret_cast<uint4*>(dst)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+      }
     } else {
 #pragma unroll
       for (int e = 0; e < 8; ++e)
@@ -1108,6 +1122,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     const int hcols = 32 * ((BN / 32 + 1) / 2);
     const int cb = h * hcols, ce = h ? BN : hcols;
     const bool vec = (p.out_ld % D::EC) == 0;
+    const bool vec32 = vec && (((static_cast<size_t>(p.out_ld) * sizeof(T)) | reinterpret_cast<uintptr_t>(p.out)) & 31u) == 0;
     // store tile u (the tc-th of this CTA): a 1x1, stride-1 dgrad writes row m of D to dX pixel m
     auto epilogue = [&](int u, int tc) -> bool {
       const ConvPhase& ph = find_phase(p, u);
@@ -1131,11 +1146,11 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         float v[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(ra[e]);
-        if (m < ph.rows) store_row32<T>(out + n_tile * BN + c0, v, p.N - (n_tile * BN + c0), vec);
+        if (m < ph.rows) store_row32<T>(out + n_tile * BN + c0, v, p.N - (n_tile * BN + c0), vec, vec32);
         if (c1 != c0 && n_tile * BN + c1 < p.N) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(rb[e]);
-          if (m < ph.rows) store_row32<T>(out + n_tile * BN + c1, v, p.N - (n_tile * BN + c1), vec);
+          if (m < ph.rows) store_row32<T>(out + n_tile * BN + c1, v, p.N - (n_tile * BN + c1), vec, vec32);
         }
       }
       tc_fence_before();
@@ -1199,6 +1214,10 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
     T* out = static_cast<T*>(p.out);
     T* out2 = static_cast<T*>(p.out2);
     const bool vec = (p.out_ld % D::EC) == 0;
+    // bf16: whole 32-byte stores (a whole sector per lane) when the rows and both outputs start on 32-byte
+    // boundaries; fp32 keeps 16-byte stores
+    const bool vec32 = DT == 1 && vec && (((static_cast<size_t>(p.out_ld) * sizeof(T)) | reinterpret_cast<uintptr_t>(p.out) |
+                                           reinterpret_cast<uintptr_t>(p.out2)) & 31u) == 0;
     // batch-statistics scratch: per-warp column sums and squares, tile means
     float* red = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tmem_slot) + 16);
     float* red2 = red + 4 * BN;
@@ -1302,7 +1321,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         if (valid && p.seg) {
           store_phase_runs<T>(out, obase, oh_px, ow_px, col0, v, ncols, p);
         } else if (valid && !p.out_act && !p.rstats && !out2) {
-          store_row32<T>(out + obase + col0, v, ncols, vec);  // one rounding to T
+          store_row32<T>(out + obase + col0, v, ncols, vec, vec32);  // one rounding to T
         } else if (valid) {
           float o[32];
 #pragma unroll
@@ -1323,11 +1342,11 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
             rmean = fmaf(dl, f, rmean);
             rm2 += m2 + dl * dl * rn * f;
           }
-          store_row32<T>(out + obase + col0, o, ncols, vec);
+          store_row32<T>(out + obase + col0, o, ncols, vec, vec32);
           if (out2) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = act_f(p.act, to_stored<T>(v[e]), DT == 1);
-            store_row32<T>(out2 + obase + col0, o, ncols, vec);
+            store_row32<T>(out2 + obase + col0, o, ncols, vec, vec32);
           }
         }
       };
