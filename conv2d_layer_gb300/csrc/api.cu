@@ -146,6 +146,21 @@ bool encode_2d(CUtensorMap* m, const void* base, bool bf16, uint64_t cols, uint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 weights W [OC][taps][IC] (IC a multiple of 64) as the dgrad's MN-major B operand (ConvGemmParams::
+// b_mn): a 4-D view {64 input channels, OC, IC / 64 channel groups, taps}, boxes of 64 x 64 x groups x 1,
+// so that one copy lands `groups` panels of 64 output-channel rows x 64 input channels of one tap.
+bool encode_w_mn(CUtensorMap* m, const void* w, uint64_t OC, uint64_t taps, uint64_t IC, uint32_t groups) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || IC % 64 != 0) return false;
+  cuuint64_t dims[4] = {64, OC, IC / 64, taps};
+  cuuint64_t strides[3] = {taps * IC * 2, 128, IC * 2};
+  cuuint32_t box[4] = {64, 64, groups, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(w), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A bf16 matrix [rows][C] (C a multiple of 64) seen as 64-channel panels: a 3-D view {64 channels, rows,
 // C / 64 groups} with 128-byte swizzled boxes of 64 x box_rows x groups, so that one copy lands `groups`
 // panels of box_rows rows, panel after panel (groups past C / 64 read as zeros).
@@ -401,7 +416,12 @@ bool try_pair(ConvGemmParams& p, Tile& t, const Geo& g, const DevInfo* dev, cons
   }
   if (clusters < 1) return false;
   CUtensorMap half;
-  if (!encode_2d(&half, bmat, true, bcols, brows, g.BKE, t.BN / 2)) return false;
+  if (p.b_mn) {
+    if ((t.BN / 2) % 64 != 0 || !encode_w_mn(&half, bmat, g.OC, g.taps, g.IC, static_cast<uint32_t>(t.BN / 128)))
+      return false;
+  } else if (!encode_2d(&half, bmat, true, bcols, brows, g.BKE, t.BN / 2)) {
+    return false;
+  }
   p.tmap_b = half;
   p.pair = 1;
   int unit = 0;  // units: pairs of m-tiles, phase by phase
@@ -547,6 +567,9 @@ DgradPlan dgrad_plan(const Geo& g) {
       p.b_col = col;
       p.oh0 = ph_h;
       p.ow0 = ph_w;
+      p.Th = Th;
+      p.rh = rh;
+      p.rw = rw;
       p.div_Wa = make_fastdiv(Wa);
       p.div_HaWa = make_fastdiv(Ha * Wa);
       p.div_Tw = make_fastdiv(p.Tw);
@@ -904,11 +927,24 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
   d = dgrad_plan(g);
   void* whi = region(ws, pl, R_WD);
   float* wlo = reinterpret_cast<float*>(region(ws, pl, R_WDLO));
-  LAUNCH("dgrad_weights", st,
-         launch_prep_dgrad_weights(g.dt, w, whi, bf ? nullptr : wlo, g.OC, g.KH, g.KW, g.IC, g.ICp, g.OCp, g.S, d.Kd,
-                                   d.table, st));
   std::memset(&p, 0, sizeof(p));
-  if (!encode_b(&p.tmap_b, bf, whi, wlo, d.Kd, g.ICp, d.tile.BN)) return CONV2D_ERR_CUDA;
+  // bf16 with d_conv by TMA over several stride phases, whole 64-channel groups: the weights as an MN-major B
+  // operand, no transposed copy (`mixed` layer 2: 0.5225 -> 0.5165 ms a step). A one-phase dgrad keeps the
+  // copy: there, with CTA pairs, the strided reads of W cost what the copy saves (`large` 2.006 -> 2.009 ms).
+  const bool b_mn = bf && !xf && d.table.flip && d.num_phases > 1 && g.IC % 64 == 0 && g.OC == g.OCp &&
+                    d.tile.BN % 64 == 0;
+  if (b_mn) {
+    if (!encode_w_mn(&p.tmap_b, w, g.OC, g.taps, g.IC, static_cast<uint32_t>(d.tile.BN / 64))) return CONV2D_ERR_CUDA;
+    p.b_mn = 1;
+    p.S = g.S;
+    p.KW = g.KW;
+    whi = const_cast<void*>(w);
+  } else {
+    LAUNCH("dgrad_weights", st,
+           launch_prep_dgrad_weights(g.dt, w, whi, bf ? nullptr : wlo, g.OC, g.KH, g.KW, g.IC, g.ICp, g.OCp, g.S, d.Kd,
+                                     d.table, st));
+    if (!encode_b(&p.tmap_b, bf, whi, wlo, d.Kd, g.ICp, d.tile.BN)) return CONV2D_ERR_CUDA;
+  }
   p.src = dconv;
   p.Hs = g.OH;
   p.Ws = g.OW;

@@ -73,6 +73,7 @@ struct ConvPhase {
   int oh0, ow0;        // output pixel = (oh0 + a*os, ow0 + b*os)
   int a_lo_h, a_lo_w;  // A by TMA im2col: window corner of row (a, b) = (a*rs + a_lo_h, b*rs + a_lo_w)
   int a_map;           // ... and the index of this phase's im2col map
+  int Th, rh, rw;      // dgrad taps: Th rows of taps; the phase's kernel taps are (rh + S t, rw + S u)
   FastDiv div_Wa, div_HaWa, div_Tw;
 };
 
@@ -139,6 +140,12 @@ struct ConvGemmParams {
   const float* xf_tbl;
   // xf: the weights resident in shared memory behind the ring, bres bytes (one BN x 64 tile per k-block)
   uint32_t bres;
+  // bf16 dgrad with d_conv by TMA: B read straight from the layer's weights W [OC][KH][KW][IC] as an MN-major
+  // operand (no transposed copy): tmap_b is a 4-D view {64 input channels, OC, IC / 64 channel groups, KH * KW
+  // taps}, and the k-block (tap counters tt, tw; output-channel chunk ck) of a phase takes the kernel tap
+  // (rh + S (Th - 1 - tt), rw + S (Tw - 1 - tw)) (the flipped taps of the im2col order), oc ck * 64 ..: one copy
+  // lands BN / 64 panels of 64 oc rows x 64 channels (128-byte swizzle). IC and BN multiples of 64. 0: off.
+  int b_mn, S, KW;
   int* err;
   ConvPhase ph[kMaxPhases];
 };
@@ -587,8 +594,10 @@ __device__ __forceinline__ void store_row32(T* dst, const float (&v)[32], int nc
 // fprop / dgrad
 // --------------------------------------------------------------------------
 // PAIR: CTA pairs (cta_group::2); bf16 with A by TMA and one phase only. A kernel may not mix
-// single-CTA and pair tcgen05 forms, hence the separate instantiation.
-template <int DT, bool PAIR>
+// single-CTA and pair tcgen05 forms, hence the separate instantiation. BMN: B read straight from the
+// weights as an MN-major operand (ConvGemmParams::b_mn), an instantiation of its own so that the other
+// GEMMs' MMA loop carries no test of it.
+template <int DT, bool PAIR, bool BMN = false>
 __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_constant__ ConvGemmParams p) {
   pdl_entry();
   using D = Dt<DT>;
@@ -598,6 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
   const int BN = p.BN;
   constexpr bool pair = PAIR;
   static_assert(!PAIR || DT == 1, "CTA pairs run bf16 only");
+  static_assert(!BMN || DT == 1, "weights read as an MN-major operand in bf16 only");
   const uint32_t a_bytes = kBM * 128, b_bytes = BN * 128;
   // a pair member holds its 128 rows of A and half of B's columns
   const uint32_t b_own = pair ? b_bytes / 2 : b_bytes;
@@ -750,10 +760,20 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
             const int kcol = ph.b_col + (g0 + i) * D::BKE;
             const uint32_t a0 = sbase + s * stage_bytes + i * sub_bytes;
             const uint32_t b0 = a0 + a_tiles * a_bytes;
+            // BMN: the kernel tap of this k-block (the flipped im2col order)
+            const int wtap = BMN ? (ph.rh + p.S * (ph.Th - 1 - tt)) * p.KW + ph.rw + p.S * (ph.Tw - 1 - tw) : 0;
             if (pair) {
               tma_load_im2col_4d_pair(a0, &p.tmap_a[ph.a_map], bar, ck * D::BKE, aw, ah, an, static_cast<uint16_t>(tw),
                                       static_cast<uint16_t>(tt));
-              tma_load_2d_pair(b0, &p.tmap_b, bar, kcol, n_tile * BN + static_cast<int>(rank) * (BN / 2));
+              if (BMN)
+                tma_load_4d_pair(b0, &p.tmap_b, bar, 0, ck * D::BKE, (n_tile * BN + static_cast<int>(rank) * (BN / 2)) / 64,
+                                 wtap);
+              else
+                tma_load_2d_pair(b0, &p.tmap_b, bar, kcol, n_tile * BN + static_cast<int>(rank) * (BN / 2));
+            } else if (BMN) {
+              tma_load_im2col_4d(a0, &p.tmap_a[ph.a_map], &full[s], ck * D::BKE, aw, ah, an, static_cast<uint16_t>(tw),
+                                 static_cast<uint16_t>(tt));
+              tma_load_4d(b0, &p.tmap_b, &full[s], 0, ck * D::BKE, n_tile * BN / 64, wtap);
             } else {
               if (p.a_tma)
                 tma_load_im2col_4d(a0, &p.tmap_a[ph.a_map], &full[s], ck * D::BKE, aw, ah, an,
@@ -821,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         if (alive) mma_commit(&tfull[buf]);
       }
     } else if (lane == 0 && leader) {
-      const uint32_t idesc = idesc_f32acc(pair ? 2 * kBM : kBM, BN, D::FMT, false, false);
+      const uint32_t idesc = idesc_f32acc(pair ? 2 * kBM : kBM, BN, D::FMT, false, BMN);
       const uint32_t idesc2 = idesc_f32acc(kBM, 2 * BN, D::FMT, false, false);  // A_hi x [B_hi; B_lo]
       int s = 0, j = 0;
       uint32_t par = 0, apar = 0;
@@ -863,7 +883,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
 #pragma unroll
             for (int kk = 0; kk < 128 / 32; ++kk) {
               const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
+              // BMN: 16 oc rows (2 KB) of every 8 KB panel per k-step
+              const uint64_t bd = BMN ? sdesc_sw128(b0 + kk * 2048, 8192, 1024) : sdesc_sw128(b0 + kk * 32, 16, 1024);
               const uint32_t acc = (kc | kk) ? 1u : 0u;
               if (DT == 1) {
                 if (pair) mma_bf16_pair(d, ad, bd, idesc, acc);

@@ -4,19 +4,20 @@
 
 namespace c2d {
 
-cudaError_t launch_conv_gemm_bf16(const ConvGemmParams& p, int grid, size_t smem, cudaStream_t st) {
-  if (!p.pair) {
-    cudaError_t e = cudaFuncSetAttribute(conv_gemm_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    launch_k(conv_gemm_kernel<1, false>, grid, kThreads, smem, st, 1, p);
-    return cudaGetLastError();
-  }
-  // CTA pairs: clusters of two (grid even)
-  cudaError_t e = cudaFuncSetAttribute(conv_gemm_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+// One instantiation of the bf16 fprop / dgrad kernel (see conv_gemm_kernel's PAIR and BMN).
+template <bool PAIR, bool BMN>
+static cudaError_t launch_conv(const ConvGemmParams& p, int grid, size_t smem, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(conv_gemm_kernel<1, PAIR, BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_k(conv_gemm_kernel<1, true>, grid, kThreads, smem, st, 2, p);
+  if (PAIR) return launch_k(conv_gemm_kernel<1, PAIR, BMN>, grid, kThreads, smem, st, 2, p);  // clusters of two
+  launch_k(conv_gemm_kernel<1, PAIR, BMN>, grid, kThreads, smem, st, 1, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conv_gemm_bf16(const ConvGemmParams& p, int grid, size_t smem, cudaStream_t st) {
+  if (p.b_mn) return p.pair ? launch_conv<true, true>(p, grid, smem, st) : launch_conv<false, true>(p, grid, smem, st);
+  return p.pair ? launch_conv<true, false>(p, grid, smem, st) : launch_conv<false, false>(p, grid, smem, st);
 }
 
 int conv_gemm_pair_clusters(size_t smem) {

@@ -76,6 +76,9 @@ EDGE_CASES = {
                                     norm=NORM_BATCH, act=ACT_RELU, dtype=BF16),
     "bf16_k4s2_tma_phases": LayerSpec(N=2, H=10, W=10, IC=64, OC=64, KH=4, KW=4, stride=2, pad=1,
                                       norm=NORM_NONE, act=ACT_TANH, dtype=BF16),
+    # stride-2 dgrad reading the weights directly as an MN-major operand: three 64-channel groups per tile
+    "bf16_s2_weights_mn_ic192": LayerSpec(N=2, H=12, W=10, IC=192, OC=128, KH=3, KW=3, stride=2, pad=1,
+                                          norm=NORM_BATCH, act=ACT_RELU, dtype=BF16),
     # the same with four stride phases of 1156 rows each (ten m-tiles, the last with 4 rows)
     "bf16_s2_pair_phases": LayerSpec(N=4, H=34, W=34, IC=64, OC=64, KH=3, KW=3, stride=2, pad=1,
                                      norm=NORM_BATCH, act=ACT_RELU, dtype=BF16),
