@@ -32,7 +32,7 @@ NOMINAL_BF16_TFLOPS = 2250.0
 # DRAM bytes (read + write) per launch of the GEMM kernels on the 256-image layer, from the ncu capture
 # summarised in profiles/large_step_kernels.md (96-image case, scaled by 256/96). Reset to None whenever
 # a GEMM kernel changes and re-capture.
-NCU_TRAFFIC_BYTES = {"fprop_gemm": 692e6, "dgrad_gemm": 685e6, "wgrad_gemm": 822e6}
+NCU_TRAFFIC_BYTES = {"fprop_gemm": 715e6, "dgrad_gemm": 706e6, "wgrad_gemm": 822e6}
 
 
 def _peaks():
