@@ -1024,8 +1024,10 @@ int run_dgrad(const Geo& g, const DevInfo* dev, const void* w, const void* dconv
   return CONV2D_OK;
 }
 
+// bpart, bG, dbias: the dbias partials [bG][OC] summed into dbias by the split reduce's launch (null: none).
 int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dconv, float* dw, void* ws,
-              const Plan& pl, cudaStream_t st, const XfSrc* xf = nullptr) {
+              const Plan& pl, cudaStream_t st, const XfSrc* xf = nullptr, const float* bpart = nullptr, int bG = 0,
+              float* dbias = nullptr) {
   WgradParams p;
   std::memset(&p, 0, sizeof(p));
   const WgradPlan& w = pl.wg;
@@ -1147,7 +1149,8 @@ int run_wgrad(const Geo& g, const DevInfo* dev, const void* xsrc, const void* dc
   }
   LAUNCH("wgrad_gemm", st,
          bf ? launch_wgrad_gemm_bf16(p, grid, smem, st) : launch_wgrad_gemm_tf32(p, grid, smem, st));
-  LAUNCH("wgrad_reduce", st, launch_wgrad_reduce(p.partial, w.splits, g.OC, g.taps, g.ICp, g.IC, dw, st));
+  LAUNCH("wgrad_reduce", st,
+         launch_wgrad_reduce(p.partial, w.splits, g.OC, g.taps, g.ICp, g.IC, dw, bpart, bG, dbias, st));
   return CONV2D_OK;
 }
 
@@ -1420,7 +1423,10 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
   } else {
     LAUNCH("act_bwd_dconv", st, launch_act_bwd(g.dt, pre_act, dy, pl.walk, g.OCp, g.act, dconv, part, st));
   }
-  if (dbias && !pl.fused)
+  // dbias = the sum of the d_conv pass's partials: in the split reduce's launch when dW is computed (the
+  // partials stay untouched until then), else on its own (the fused backward has formed it already)
+  const bool dbias_in_reduce = dbias && dw && !pl.fused;
+  if (dbias && !dw && !pl.fused)
     LAUNCH("dbias_finalize", st, launch_sum_finalize(part, pl.walk, 1, 1, nullptr, dbias, nullptr, st));
   XfSrc xfs{pre_act, dy, c12 + 2 * g.OC};
   const XfSrc* xf = pl.fused ? &xfs : nullptr;
@@ -1433,7 +1439,9 @@ int conv2d_bwd(const conv2d_desc* desc, const void* x, const void* w, const floa
       LAUNCH("pack_x", st, launch_pack_channels(g.dt, x, xp, static_cast<long>(g.N) * g.H * g.W, g.IC, g.ICp, st));
       xsrc = xp;
     }
-    if ((rc = run_wgrad(g, dev, xsrc, dconv, dw, ws, pl, st, xf))) return rc;
+    if ((rc = run_wgrad(g, dev, xsrc, dconv, dw, ws, pl, st, xf, dbias_in_reduce ? part : nullptr, pl.walk.G,
+                        dbias_in_reduce ? dbias : nullptr)))
+      return rc;
   }
   return CONV2D_OK;
 }

@@ -444,17 +444,17 @@ __device__ __forceinline__ void kahan_add(float& s, float& comp, float x) {
   s = t;
 }
 
-// Per-channel sums of per-block partials [G][C][nv] (nv <= 3): one 128-thread block per channel;
-// compensated fp32 sums per thread over every 128th partial, fp64 shuffle trees within the warps and the
-// four warp totals added in a fixed order (the same result on every run). Block-collective; the totals
-// are valid in thread 0.
+// Per-channel sums of per-block partials [G][C][nv] (nv <= 3) by one block of 128 or 256 threads:
+// compensated fp32 sums per thread over every blockDim-th partial, fp64 shuffle trees within the warps and
+// the warp totals added in a fixed order (the same result on every run). Block-collective; the totals are
+// valid in thread 0.
 __device__ __forceinline__ void channel_sums(const float* __restrict__ part, int G, int C, int nv, int c,
                                              double (&tot)[3]) {
-  __shared__ double s_w[3][4];
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ double s_w[3][8];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   float a[3] = {0.f, 0.f, 0.f}, ca[3] = {0.f, 0.f, 0.f};
 #pragma unroll 4
-  for (int k = threadIdx.x; k < G; k += 128) {
+  for (int k = threadIdx.x; k < G; k += blockDim.x) {
     const float* p = part + (static_cast<size_t>(k) * C + c) * nv;
     kahan_add(a[0], ca[0], p[0]);
     if (nv > 1) kahan_add(a[1], ca[1], p[1]);
@@ -469,7 +469,22 @@ __device__ __forceinline__ void channel_sums(const float* __restrict__ part, int
   }
   __syncthreads();
 #pragma unroll
-  for (int v = 0; v < 3; ++v) tot[v] = (s_w[v][0] + s_w[v][1]) + (s_w[v][2] + s_w[v][3]);
+  for (int v = 0; v < 3; ++v) {
+    tot[v] = (s_w[v][0] + s_w[v][1]) + (s_w[v][2] + s_w[v][3]);
+    if (nw == 8) tot[v] += (s_w[v][4] + s_w[v][5]) + (s_w[v][6] + s_w[v][7]);
+  }
+}
+
+// Blocks past the split reduce's own (blockIdx.x >= nb) sum the dbias partials bpart[bG][C] of channel
+// blockIdx.x - nb into dbias (the dbias finalize, folded into the last launch of the backward). Returns
+// true for those blocks.
+__device__ __forceinline__ bool dbias_block(int nb, const float* __restrict__ bpart, int bG, int C, float* dbias) {
+  if (static_cast<int>(blockIdx.x) < nb) return false;
+  const int c = blockIdx.x - nb;
+  double t[3];
+  channel_sums(bpart, bG, C, 1, c, t);
+  if (threadIdx.x == 0) dbias[c] += static_cast<float>(t[0]);
+  return true;
 }
 
 // mode 0: c12 = (sum d_norm, sum d_norm z), dbeta += first, dgamma += second; mode 1: dbias += the sum.
@@ -700,8 +715,10 @@ __global__ void prep_dgrad_merged_weights_kernel(const T* __restrict__ w, T* __r
 // dW[oc][tap][ic] += sum over splits of partial[s][oc][tap*ICp + ic] (fixed order: deterministic), one
 // thread per item over all splits: the form for a few splits (see launch_wgrad_reduce).
 __global__ void wgrad_reduce_serial_kernel(const float* __restrict__ partial, int splits, int OC, int taps, int ICp,
-                                           int IC, float* __restrict__ dw) {
+                                           int IC, float* __restrict__ dw, int nb, const float* __restrict__ bpart,
+                                           int bG, float* dbias) {
   pdl_entry();
+  if (dbias_block(nb, bpart, bG, OC, dbias)) return;
   // V consecutive input channels per thread (4 when IC == ICp is a multiple of 4: 16-byte loads and
   // stores), each summed over the splits with compensated (Kahan) fp32 summation in split order
   // (fp64 is slow on this part); the loads of eight splits are issued before their sums
@@ -710,7 +727,7 @@ __global__ void wgrad_reduce_serial_kernel(const float* __restrict__ partial, in
   const long Mk = static_cast<long>(taps) * ICp;
   const long stride = static_cast<long>(OC) * Mk;
   for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long>(gridDim.x) * blockDim.x) {
+       i += static_cast<long>(nb) * blockDim.x) {
     const long e = i * V;  // first dw element of this thread
     const int ic = static_cast<int>(e % IC);
     const long ot = e / IC;
@@ -789,8 +806,11 @@ constexpr int kRedSerialMax = 48;  // split counts below this take wgrad_reduce_
 template <int V>
 __global__ void __launch_bounds__(32 * kRedGroups) wgrad_reduce_kernel(const float* __restrict__ partial, int splits,
                                                                       int OC, int taps, int ICp, int IC,
-                                                                      float* __restrict__ dw) {
+                                                                      float* __restrict__ dw, int nb,
+                                                                      const float* __restrict__ bpart, int bG,
+                                                                      float* dbias) {
   pdl_entry();
+  if (dbias_block(nb, bpart, bG, OC, dbias)) return;
   using VT = typename std::conditional<V == 4, float4, float>::type;
   __shared__ VT s_sum[kRedGroups][32];
   const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
@@ -1925,23 +1945,27 @@ cudaError_t launch_col2im(int dtype, const void* dcol, void* dx, int N, int H, i
 }
 
 cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int taps, int ICp, int IC, float* dw,
-                                cudaStream_t st) {
+                                const float* bpart, int bG, float* dbias, cudaStream_t st) {
+  const int nbias = dbias ? OC : 0;  // one more block per channel for the dbias sums
   // Few splits: one thread per item over every split (measured faster for the 25 splits of a 256-image
   // 3 x 3 layer). Many splits (the fp32 layers, 1 x 1 layers with one row tile): the split groups, which
   // shorten each thread's chain of dependent loads.
   if (splits < kRedSerialMax) {
     const int V = (IC == ICp && IC % 4 == 0) ? 4 : 1;  // channels per thread (see the kernel)
     const int g = grid_for(static_cast<long>(OC) * taps * IC / V, 256);
-    launch_k(wgrad_reduce_serial_kernel, g, 256, 0, st, 1, partial, splits, OC, taps, ICp, IC, dw);
+    launch_k(wgrad_reduce_serial_kernel, g + nbias, 256, 0, st, 1, partial, splits, OC, taps, ICp, IC, dw, g, bpart,
+             bG, dbias);
     return cudaGetLastError();
   }
   // 32 items of V channels per block (see the kernel)
   if (IC == ICp && IC % 4 == 0) {
     const int g = static_cast<int>((static_cast<long>(OC) * taps * IC / 4 + 31) / 32);
-    launch_k(wgrad_reduce_kernel<4>, g, 32 * kRedGroups, 0, st, 1, partial, splits, OC, taps, ICp, IC, dw);
+    launch_k(wgrad_reduce_kernel<4>, g + nbias, 32 * kRedGroups, 0, st, 1, partial, splits, OC, taps, ICp, IC, dw, g,
+             bpart, bG, dbias);
   } else {
     const int g = static_cast<int>((static_cast<long>(OC) * taps * IC + 31) / 32);
-    launch_k(wgrad_reduce_kernel<1>, g, 32 * kRedGroups, 0, st, 1, partial, splits, OC, taps, ICp, IC, dw);
+    launch_k(wgrad_reduce_kernel<1>, g + nbias, 32 * kRedGroups, 0, st, 1, partial, splits, OC, taps, ICp, IC, dw, g,
+             bpart, bG, dbias);
   }
   return cudaGetLastError();
 }

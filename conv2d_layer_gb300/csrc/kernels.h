@@ -127,8 +127,10 @@ cudaError_t launch_prep_col2im_weights(int dtype, const void* w, void* bhi, floa
                                        int ICp, int OCp, cudaStream_t st);
 cudaError_t launch_col2im(int dtype, const void* dcol, void* dx, int N, int H, int W, int IC, int ICp, int OH, int OW,
                           int KH, int KW, int S, int P, cudaStream_t st);
+// dW += the sum of the split partials; with dbias, also dbias[c] += the sum of bpart[0..bG)[c] (the dbias
+// finalize, in OC more blocks of the same launch).
 cudaError_t launch_wgrad_reduce(const float* partial, int splits, int OC, int taps, int ICp, int IC, float* dw,
-                                cudaStream_t st);
+                                const float* bpart, int bG, float* dbias, cudaStream_t st);
 cudaError_t launch_bn_eval_stats(const float* rm, const float* rv, float eps, int C, float* mean, float* inv_std,
                                  cudaStream_t st);
 cudaError_t launch_infer_fold(const float* bias, const float* gamma, const float* beta, const float* rm,
