@@ -1650,10 +1650,13 @@ RowWalk make_walk(long rows, int C, int dtype, int sms, int segs, int cpg, int p
   const long unit = std::max<long>(w.R, rpp);  // rows of one chunk (streamed) or one pass
   if (w.segs == 1) {
     // Several waves of blocks of about 28 units each, so that blocks finishing early on fast SMs
-    // take more work (one wave of equal blocks waits for the slowest SM); at least one full wave.
+    // take more work (one wave of equal blocks waits for the slowest SM); at least one full wave, and a
+    // whole number of waves (a last wave of a few blocks would run on a nearly idle GPU: the 256-image
+    // 56 x 56 x 256 layer's backward reduce had 4.04 waves).
     long g = (rows + 28 * unit - 1) / (28 * unit);
-    g = std::max(g, std::min<long>((rows + unit - 1) / unit, resident));
+    g = std::max<long>(1, (g + resident / 2) / resident) * resident;
     g = std::min(g, 8 * resident);
+    g = std::min(g, (rows + unit - 1) / unit);  // no block without rows
     if (g < 1) g = 1;
     w.G = static_cast<int>(g);
     w.bps = w.G;
