@@ -211,10 +211,14 @@ __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t a) {
 __device__ __forceinline__ uint32_t to_tf32(float x) {
   return (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
 }
-// x = hi + lo with hi, lo tf32 values (the split used by 3xTF32).
+// x = hi + lo, the split used by 3xTF32: hi = x rounded to tf32, lo = x - hi, exact in fp32 (the part
+// rounded off fits in the 13 dropped bits). lo is left unrounded: whether the tensor core drops or rounds
+// the 13 low bits of a tf32 operand, it takes lo to within one tf32 ulp of lo, 2^-10 |lo| <= 2^-21 |x|,
+// an unbiased error (lo has either sign) below that of the fp32 accumulation; rounding it here as well
+// cost two instructions per element on the split, the operand path's busiest loop.
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
   hi = to_tf32(x);
-  lo = to_tf32(x - __uint_as_float(hi));
+  lo = __float_as_uint(x - __uint_as_float(hi));
 }
 
 // ---------------------------------------------------------------- tcgen05
