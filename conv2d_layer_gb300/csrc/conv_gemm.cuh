@@ -942,10 +942,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
         uint32_t x0, x1, x2, x3;
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3) : "r"(dst));
         uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
-        split_tf32(__uint_as_float(x0), h0, l0);
-        split_tf32(__uint_as_float(x1), h1, l1);
-        split_tf32(__uint_as_float(x2), h2, l2);
-        split_tf32(__uint_as_float(x3), h3, l3);
+        split_tf32x2(__uint_as_float(x0), __uint_as_float(x1), h0, l0, h1, l1);
+        split_tf32x2(__uint_as_float(x2), __uint_as_float(x3), h2, l2, h3, l3);
         st_shared_v4(dst, h0, h1, h2, h3);
         st_shared_v4(dst + a_bytes, l0, l1, l2, l3);
       }
@@ -1063,10 +1061,10 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
               asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                            : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
                            : "r"(src + ((cc ^ (r & 7)) << 4)));
-              split_tf32(__uint_as_float(x0), hi[4 * c], lo[4 * c]);
-              split_tf32(__uint_as_float(x1), hi[4 * c + 1], lo[4 * c + 1]);
-              split_tf32(__uint_as_float(x2), hi[4 * c + 2], lo[4 * c + 2]);
-              split_tf32(__uint_as_float(x3), hi[4 * c + 3], lo[4 * c + 3]);
+              split_tf32x2(__uint_as_float(x0), __uint_as_float(x1), hi[4 * c], lo[4 * c], hi[4 * c + 1],
+                           lo[4 * c + 1]);
+              split_tf32x2(__uint_as_float(x2), __uint_as_float(x3), hi[4 * c + 2], lo[4 * c + 2], hi[4 * c + 3],
+                           lo[4 * c + 3]);
             }
             tmem_st16(dst + 16 * h, hi);
             tmem_st16(dst + 32 + 16 * h, lo);
@@ -1111,10 +1109,8 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           uint32_t x0, x1, x2, x3;
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3) : "r"(dst));
           uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
-          split_tf32(__uint_as_float(x0), h0, l0);
-          split_tf32(__uint_as_float(x1), h1, l1);
-          split_tf32(__uint_as_float(x2), h2, l2);
-          split_tf32(__uint_as_float(x3), h3, l3);
+          split_tf32x2(__uint_as_float(x0), __uint_as_float(x1), h0, l0, h1, l1);
+          split_tf32x2(__uint_as_float(x2), __uint_as_float(x3), h2, l2, h3, l3);
           st_shared_v4(dst, h0, h1, h2, h3);
           st_shared_v4(dst + a_bytes, l0, l1, l2, l3);
         }
@@ -1379,7 +1375,11 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           tmem_ld32(taddr + static_cast<uint32_t>(BN + c0), rb);
           tmem_ld_wait2(ra, rb);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ra[e] = __float_as_uint(__uint_as_float(ra[e]) + __uint_as_float(rb[e]));
+          for (int e = 0; e < 32; e += 2) {
+            const float2 v2 = __fadd2_rn(f2(ra[e], ra[e + 1]), f2(rb[e], rb[e + 1]));
+            ra[e] = __float_as_uint(v2.x);
+            ra[e + 1] = __float_as_uint(v2.y);
+          }
         } else {
           fetch(c0, ra, rb);
         }
@@ -1951,13 +1951,16 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
               for (int h = 0; h < 2; ++h) {
                 uint32_t hi[16], lo[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
+                for (int e = 0; e < 16; e += 2) {
                   const int px = 16 * h + e;
-                  uint32_t x;
+                  uint32_t x, y;
                   asm volatile("ld.shared.b32 %0, [%1];"
                                : "=r"(x)
                                : "r"(src + px * 128 + ((((lane >> 2) ^ (px & 7))) << 4)));
-                  split_tf32(__uint_as_float(x), hi[e], lo[e]);
+                  asm volatile("ld.shared.b32 %0, [%1];"
+                               : "=r"(y)
+                               : "r"(src + (px + 1) * 128 + ((((lane >> 2) ^ ((px + 1) & 7))) << 4)));
+                  split_tf32x2(__uint_as_float(x), __uint_as_float(y), hi[e], lo[e], hi[e + 1], lo[e + 1]);
                 }
                 tmem_st16(dst + 16 * h, hi);
                 tmem_st16(dst + 32 + 16 * h, lo);
@@ -1992,7 +1995,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
               const uint32_t addr = hi + row * 128 + ((pq ^ (row & 7)) << 4);
               uint32_t h[4], l[4];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) split_tf32(v[i][e], h[i], l[i]);
+              for (int i = 0; i < 4; i += 2) split_tf32x2(v[i][e], v[i + 1][e], h[i], l[i], h[i + 1], l[i + 1]);
               st_shared_v4(addr, h[0], h[1], h[2], h[3]);
               st_shared_v4(addr + lo_off, l[0], l[1], l[2], l[3]);
             }

@@ -220,6 +220,16 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) 
   hi = to_tf32(x);
   lo = __float_as_uint(x - __uint_as_float(hi));
 }
+// Two splits at once, the two subtractions as one packed f32x2 FMA (x + hi * -1, exact like x - hi).
+__device__ __forceinline__ void split_tf32x2(float x0, float x1, uint32_t& h0, uint32_t& l0, uint32_t& h1,
+                                             uint32_t& l1) {
+  h0 = to_tf32(x0);
+  h1 = to_tf32(x1);
+  const float2 l = __ffma2_rn(make_float2(__uint_as_float(h0), __uint_as_float(h1)), make_float2(-1.f, -1.f),
+                              make_float2(x0, x1));
+  l0 = __float_as_uint(l.x);
+  l1 = __float_as_uint(l.y);
+}
 
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
