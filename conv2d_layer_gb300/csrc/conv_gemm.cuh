@@ -1519,16 +1519,18 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], DT == 1 ? (p.a_tma ? 1 : 4 + 1) : 4);  // the TMA thread and/or one per producer warp
+      // the TMA thread and/or one per producer warp (fp32 raw tiles: one per transposing warp, 2-9)
+      mbar_init(&full[s], DT == 1 ? (p.a_tma ? 1 : 4 + 1) : (raw_a ? 8 : 4));
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], (pair || xf) ? 8 : 4);  // epilogue warps (of both CTAs when paired; xf: warps 2-9)
+      // epilogue warps (of both CTAs when paired; xf and fp32 raw tiles: warps 2-9)
+      mbar_init(&tempty[b], (pair || xf || raw_a) ? 8 : 4);
     }
     for (int r = 0; r < NR; ++r) {
       mbar_init(&rfull[r], 1);   // the TMA thread
-      mbar_init(&rempty[r], 4);  // one arrival per transposing warp
+      mbar_init(&rempty[r], 8);  // one arrival per transposing warp (2-9)
     }
     if (xf)
       for (int s = 0; s < S; ++s) mbar_init(&sfull[s], 8);  // one arrival per transforming warp
@@ -1839,6 +1841,157 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
       prev = u;
     }
     if (alive && prev >= 0) epilogue(prev, tc - 1);
+  } else if (raw_a) {
+    // ------------------------------------------------ fp32: transpose the raw tiles into tf32 hi / lo, and the epilogue
+    // Warps 2-9. A raw chunk is 32 pixel rows x 32 channels (128-byte swizzle as the TMA wrote it); the stage
+    // wants K-major rows of 32 pixels per channel. A half-chunk transpose: lane (pq, cq) reads the 4 x 4 block
+    // of pixels 4pq.. and channels 4cq.. (four 16-byte reads), splits it and writes four channel rows of four
+    // pixels to the hi and lo tiles (both sides spread over all banks); warps 2-5 take them in turn.
+    // With A in TMEM (ts) the X chunks go to TMEM instead: warp w moves pixels 16h .. 16h + 15 (h = 0 for
+    // warps 2-5, 1 for warps 6-9) of X chunk w & 3 (its TMEM lane quarter), lane ch reading channel ch, and
+    // stores hi / lo into columns 16h.. / 32 + 16h.. of the stage's TMEM rows (column = pixel = k); the
+    // half-chunk transposes cover the d_conv chunks only. After a unit's k-blocks the eight warps write the
+    // unit before it (its accumulator completed meanwhile), one column half each.
+    const int wi = warp - 2;
+    const int q = warp & 3, half = wi >> 2;
+    const int pq = lane & 7, cql = lane >> 3;
+    const int hcols = 32 * ((BN / 32 + 1) / 2);
+    const int cb = half * hcols, ce = half ? BN : hcols;
+    auto epilogue = [&](int u, int tcu) -> bool {
+      int m_tile, n_tile, kb0, kb1;
+      decode(u, m_tile, n_tile, kb0, kb1);
+      const int split = u / (p.m_tiles * p.n_tiles);
+      const int buf = tcu & 1;
+      int ok = 1;
+      if (lane == 0) ok = wait(&tfull[buf], (tcu >> 1) & 1, p.err, kSiteTFull) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      tc_fence_after();
+      const int m = m_tile * kBM + q * 32 + lane;
+      const bool zero = kb1 <= kb0;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * acols;
+      for (int c0 = cb; c0 < ce; c0 += 32) {
+        if (n_tile * BN + c0 >= p.N) break;  // uniform across the warp
+        uint32_t ra[32], rb[32];
+        tmem_ld32(taddr + c0, ra);
+        if (ts) {  // column c holds hi x hi + lo x hi, column BN + c hi x lo
+          tmem_ld32(taddr + BN + c0, rb);
+          tmem_ld_wait2(ra, rb);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 v2 = __fadd2_rn(f2(ra[e], ra[e + 1]), f2(rb[e], rb[e + 1]));
+            ra[e] = __float_as_uint(v2.x);
+            ra[e + 1] = __float_as_uint(v2.y);
+          }
+        } else {
+          tmem_ld_wait32(ra);
+        }
+        if (m < p.Mk) {
+          float* dst = p.partial + (static_cast<size_t>(split) * p.N + n_tile * BN + c0) * p.Mk + m;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (n_tile * BN + c0 + e < p.N) dst[static_cast<size_t>(e) * p.Mk] = zero ? 0.f : __uint_as_float(ra[e]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      return true;
+    };
+    int r = 0, s = 0;
+    uint32_t rpar = 0, par = 0;
+    bool alive = true;
+    int prev = -1, tc = 0;
+    const int nchunk = ts ? BN / 32 : 4 + BN / 32;
+    for (int u = cid; u < p.num_units && alive; u += ncl, ++tc) {
+      int m_tile, n_tile, kb0, kb1;
+      decode(u, m_tile, n_tile, kb0, kb1);
+      (void)n_tile;
+      const int nvalid = min(4, (p.Mk - m_tile * kBM + 31) / 32);  // X chunks inside Mk
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!__all_sync(0xffffffffu, wait(&rfull[r], rpar, p.err, kSiteFull) &&
+                                         wait(&empty[s], par ^ 1, p.err, kSiteEmpty))) {  // warp-uniform
+          alive = false;
+          break;
+        }
+        const uint32_t r0 = rbase + r * raw_bytes;
+        const uint32_t a0 = sbase + s * stage_bytes;
+        const uint32_t b0 = ts ? a0 : a0 + 2 * a_bytes;
+        if (ts) {
+          tc_fence_after();  // the MMAs that read this TMEM stage have completed (empty[s])
+          if (q < nvalid) {  // rows past Mk keep stale values: their dW rows are discarded
+            const uint32_t src = r0 + q * 4096 + (lane & 3) * 4;
+            const uint32_t dst = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ta0 + s * 64;
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const int px = 16 * half + e;
+              uint32_t x, y;
+              asm volatile("ld.shared.b32 %0, [%1];"
+                           : "=r"(x)
+                           : "r"(src + px * 128 + ((((lane >> 2) ^ (px & 7))) << 4)));
+              asm volatile("ld.shared.b32 %0, [%1];"
+                           : "=r"(y)
+                           : "r"(src + (px + 1) * 128 + ((((lane >> 2) ^ ((px + 1) & 7))) << 4)));
+              split_tf32x2(__uint_as_float(x), __uint_as_float(y), hi[e], lo[e], hi[e + 1], lo[e + 1]);
+            }
+            tmem_st16(dst + 16 * half, hi);
+            tmem_st16(dst + 32 + 16 * half, lo);
+            tmem_st_wait();
+          }
+        }
+        for (int it = wi; it < 2 * nchunk; it += 4) {
+          if (half) break;  // the half-chunk transposes: warps 2-5
+          const int c = ts ? 4 + (it >> 1) : it >> 1;
+          if (c < 4 && c >= nvalid) continue;  // uniform across the warp
+          const int cq = cql + 4 * (it & 1);
+          const bool isa = c < 4;
+          const uint32_t src = r0 + c * 4096;  // X chunks 0-3, then d_conv chunks
+          const uint32_t hi = isa ? a0 + c * 4096 : b0 + (c - 4) * 4096;
+          const uint32_t lo_off = isa ? a_bytes : b_bytes;
+          float v[4][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int px = 4 * pq + i;
+            uint32_t x0, x1, x2, x3;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                         : "r"(src + px * 128 + ((cq ^ (px & 7)) << 4)));
+            v[i][0] = __uint_as_float(x0);
+            v[i][1] = __uint_as_float(x1);
+            v[i][2] = __uint_as_float(x2);
+            v[i][3] = __uint_as_float(x3);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int row = 4 * cq + e;  // channel row within the chunk (the chunk starts on an 8-row atom)
+            const uint32_t addr = hi + row * 128 + ((pq ^ (row & 7)) << 4);
+            uint32_t h[4], l[4];
+#pragma unroll
+            for (int i = 0; i < 4; i += 2) split_tf32x2(v[i][e], v[i + 1][e], h[i], l[i], h[i + 1], l[i + 1]);
+            st_shared_v4(addr, h[0], h[1], h[2], h[3]);
+            st_shared_v4(addr + lo_off, l[0], l[1], l[2], l[3]);
+          }
+        }
+        if (ts) tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&full[s]);
+          mbar_arrive(&rempty[r]);
+        }
+        if (++r == NR) {
+          r = 0;
+          rpar ^= 1;
+        }
+        if (++s == S) {
+          s = 0;
+          par ^= 1;
+        }
+      }
+      if (alive && prev >= 0 && !epilogue(prev, tc - 1)) alive = false;
+      prev = u;
+    }
+    if (alive && prev >= 0) epilogue(prev, tc - 1);
   } else if (warp < 6) {
     const int t = threadIdx.x - 64;
     const char* xs = static_cast<const char*>(p.x);
@@ -1913,110 +2066,6 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_gemm_kernel(const __grid_co
       __syncwarp();
       if (alive && lane == 0)
         for (int q2 = (it > kLag ? it - kLag : 0); q2 < it; ++q2) mbar_arrive(&full[q2 % S]);
-    } else if (raw_a) {
-      // ------------------------------------------------ fp32: transpose the raw tiles into tf32 hi / lo
-      // A raw chunk is 32 pixel rows x 32 channels (128-byte swizzle as the TMA wrote it); the stage wants
-      // K-major rows of 32 pixels per channel. A warp iteration takes half a chunk: lane (pq, cq) reads the
-      // 4 x 4 block of pixels 4pq.. and channels 4cq.. (four 16-byte reads), splits it and writes four
-      // channel rows of four pixels to the hi and lo tiles (both sides spread over all banks).
-      // With A in TMEM (ts) warp w instead moves X chunk w & 3 (its TMEM lane quarter): lane ch reads
-      // channel ch of the chunk's 32 pixels, splits them and stores hi / lo into columns 0-31 / 32-63 of
-      // the stage's TMEM rows (column = pixel = k); the half-chunk transposes cover the d_conv chunks only.
-      const int wi = warp - 2;
-      const int pq = lane & 7, cql = lane >> 3;
-      int r = 0;
-      uint32_t rpar = 0;
-      const int nchunk = ts ? BN / 32 : 4 + BN / 32;
-      for (int u = blockIdx.x; u < p.num_units && alive; u += gridDim.x) {
-        int m_tile, n_tile, kb0, kb1;
-        decode(u, m_tile, n_tile, kb0, kb1);
-        (void)n_tile;
-        const int nvalid = min(4, (p.Mk - m_tile * kBM + 31) / 32);  // X chunks inside Mk
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!__all_sync(0xffffffffu, wait(&rfull[r], rpar, p.err, kSiteFull) &&
-                                           wait(&empty[s], par ^ 1, p.err, kSiteEmpty))) {  // warp-uniform
-            alive = false;
-            break;
-          }
-          const uint32_t r0 = rbase + r * raw_bytes;
-          const uint32_t a0 = sbase + s * stage_bytes;
-          const uint32_t b0 = ts ? a0 : a0 + 2 * a_bytes;
-          if (ts) {
-            tc_fence_after();  // the MMAs that read this TMEM stage have completed (empty[s])
-            const int q = warp & 3;
-            if (q < nvalid) {  // rows past Mk keep stale values: their dW rows are discarded
-              const uint32_t src = r0 + q * 4096 + (lane & 3) * 4;
-              const uint32_t dst = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ta0 + s * 64;
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                uint32_t hi[16], lo[16];
-#pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                  const int px = 16 * h + e;
-                  uint32_t x, y;
-                  asm volatile("ld.shared.b32 %0, [%1];"
-                               : "=r"(x)
-                               : "r"(src + px * 128 + ((((lane >> 2) ^ (px & 7))) << 4)));
-                  asm volatile("ld.shared.b32 %0, [%1];"
-                               : "=r"(y)
-                               : "r"(src + (px + 1) * 128 + ((((lane >> 2) ^ ((px + 1) & 7))) << 4)));
-                  split_tf32x2(__uint_as_float(x), __uint_as_float(y), hi[e], lo[e], hi[e + 1], lo[e + 1]);
-                }
-                tmem_st16(dst + 16 * h, hi);
-                tmem_st16(dst + 32 + 16 * h, lo);
-              }
-              tmem_st_wait();
-            }
-          }
-          for (int it = wi; it < 2 * nchunk; it += 4) {
-            const int c = ts ? 4 + (it >> 1) : it >> 1;
-            if (c < 4 && c >= nvalid) continue;  // uniform across the warp
-            const int cq = cql + 4 * (it & 1);
-            const bool isa = c < 4;
-            const uint32_t src = r0 + c * 4096;  // X chunks 0-3, then d_conv chunks
-            const uint32_t hi = isa ? a0 + c * 4096 : b0 + (c - 4) * 4096;
-            const uint32_t lo_off = isa ? a_bytes : b_bytes;
-            float v[4][4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int px = 4 * pq + i;
-              uint32_t x0, x1, x2, x3;
-              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                           : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
-                           : "r"(src + px * 128 + ((cq ^ (px & 7)) << 4)));
-              v[i][0] = __uint_as_float(x0);
-              v[i][1] = __uint_as_float(x1);
-              v[i][2] = __uint_as_float(x2);
-              v[i][3] = __uint_as_float(x3);
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int row = 4 * cq + e;  // channel row within the chunk (the chunk starts on an 8-row atom)
-              const uint32_t addr = hi + row * 128 + ((pq ^ (row & 7)) << 4);
-              uint32_t h[4], l[4];
-#pragma unroll
-              for (int i = 0; i < 4; i += 2) split_tf32x2(v[i][e], v[i + 1][e], h[i], l[i], h[i + 1], l[i + 1]);
-              st_shared_v4(addr, h[0], h[1], h[2], h[3]);
-              st_shared_v4(addr + lo_off, l[0], l[1], l[2], l[3]);
-            }
-          }
-          if (ts) tc_fence_before();
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&full[s]);
-            mbar_arrive(&rempty[r]);
-          }
-          if (++r == NR) {
-            r = 0;
-            rpar ^= 1;
-          }
-          if (++s == S) {
-            s = 0;
-            par ^= 1;
-          }
-        }
-      }
     } else {
       // ------------------------------------------------ A and B producers, fp32 -> tf32 hi/lo, K-major
       // A smem rows: k (128), 32 pixel columns; B smem rows: oc (BN), 32 pixel columns.
