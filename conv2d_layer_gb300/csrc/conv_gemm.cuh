@@ -1341,8 +1341,19 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           store_row32<T>(out + obase + col0, v, ncols, vec, vec32);  // one rounding to T
         } else if (valid) {
           float o[32];
+          if constexpr (DT == 0) {  // fp32: the activation dispatched once per segment (see act_row32)
+            if (p.out_act) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = p.out_act ? act_f(p.act, v[e], DT == 1) : to_stored<T>(v[e]);
+              for (int e = 0; e < 32; ++e) o[e] = v[e];
+              act_row32<false>(p.act, o);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = to_stored<T>(v[e]);
+            }
+          } else {  // bf16: the fast activations are single instructions
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = p.out_act ? act_f(p.act, v[e], true) : to_stored<T>(v[e]);
+          }
           if (p.rstats) {  // o holds the stored value (the host never combines rstats with out_act)
             const int nc = ncols < 32 ? ncols : 32;
             float sum = 0.f;
@@ -1361,8 +1372,14 @@ __global__ void __launch_bounds__(kThreads, 1) conv_gemm_kernel(const __grid_con
           }
           store_row32<T>(out + obase + col0, o, ncols, vec, vec32);
           if (out2) {
+            if constexpr (DT == 0) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = act_f(p.act, to_stored<T>(v[e]), DT == 1);
+              for (int e = 0; e < 32; ++e) o[e] = to_stored<T>(v[e]);
+              act_row32<false>(p.act, o);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = act_f(p.act, to_stored<T>(v[e]), true);
+            }
             store_row32<T>(out2 + obase + col0, o, ncols, vec, vec32);
           }
         }
